@@ -1,0 +1,374 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE expert layer with tile-level overlapped return copy on GB300.
+
+One step = one whole layer (route, plan, permute, SwiGLU grouped GEMM, down-projection GEMM with
+per-tile flags + consumer copy, combine) over one batch of synthetic tokens already resident in
+HBM. Default workload: the Mixtral-shaped layer (T=4096, d=4096, ffn=14336, E=8, top-2, R=4,
+tile_M=128). Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Multi-GPU: the layer does not shard in this build (R owners are logical partitions on one GPU),
+so N GPUs run N independent replicas (weak scaling), timed between barriers, max over ranks.
+`--impl reference` times the CPU oracle (float64, NumPy) on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from tile_level_copy_gb300 import inputs  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; grouped-GEMM % of BF16 peak; return-copy overlap %"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--consumers", type=int, default=8, help="c_CTA: SMs of the consumer partition")
+    ap.add_argument("--mgb", type=int, default=1)
+    ap.add_argument("--no-tail-assist", action="store_true", help="keep finished producer CTAs out of the copy")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="ncu DRAM bytes per launch of the SwiGLU GEMM (from profiles/), for the roofline")
+    return ap.parse_args()
+
+
+def workload_desc(w) -> str:
+    return (f"{w.name}: T={w.T} d={w.d} ffn={w.ffn} E={w.E} top-{w.topk} R={w.R} tile_M={w.tile_M}"
+            + (" zipf-bias" if w.skew else ""))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------------- dist
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        rank = dist.get_rank()
+        if torch.cuda.is_available():
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+        return rank, world
+    return 0, 1
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(local_seconds: float, local_units: float, world: int):
+    """Whole-job throughput: units over all ranks / the slowest rank's time."""
+    t = reduce_max(local_seconds, world)
+    return local_units * world / t, t
+
+
+# ------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------- our arm
+def run_ours(args, rank: int, world: int):
+    import tile_level_copy_gb300 as tlc
+    from tile_level_copy_gb300 import build as tlc_build
+
+    tlc_build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = inputs.WORKLOADS[args.workload]
+    seed = args.seed + rank
+    flags = 0 if args.no_tail_assist else tlc.MOE_TAIL_ASSIST
+    cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags)
+    peaks, peaks_src = load_peaks()
+
+    logits_np = inputs.make_logits(w, seed)
+    x_cpu = inputs.make_x(w, seed)
+    logits, x = torch.from_numpy(logits_np).to(dev), x_cpu.to(dev)
+    W = {}
+    for n in ("W1", "W3", "W2"):
+        shape = (w.E, w.ffn, w.d) if n != "W2" else (w.E, w.d, w.ffn)
+        W[n] = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        inputs.make_weight_into(w, seed, n, W[n])
+    ws = tlc.Workspace(cfg, dev)
+    out = torch.empty(w.T, w.d, dtype=torch.float32, device=dev)
+    K, Wm = args.steps, args.warmup
+
+    def step(seq, events=None):
+        tlc.forward(cfg, logits, x, W["W1"], W["W3"], W["W2"], out, ws, sequential=seq, events=events)
+
+    def timed(seq):
+        evs = [tlc.stage_events() for _ in range(K)]
+        for _ in range(Wm):
+            step(seq)
+        rc, detail = tlc.status(cfg, ws)
+        if rc != tlc.MOE_OK:
+            raise RuntimeError(f"device status {rc} ({detail}): {tlc.lib().moe_last_error().decode()}")
+        barrier(world)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(dev.index) as clk:
+            t0.record()
+            for i in range(K):
+                step(seq, evs[i])
+            t1.record()
+            torch.cuda.synchronize()
+        barrier(world)
+        rc, detail = tlc.status(cfg, ws)
+        if rc != tlc.MOE_OK:
+            raise RuntimeError(f"device status {rc} ({detail}) in the timed region")
+        stages = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(tlc.EV_COUNT - 1)] for e in evs])
+        return t0.elapsed_time(t1) / 1e3, stages, clk.summary()
+
+    sec_ovl, st_ovl, clocks = timed(False)
+    value, sec_max = aggregate(sec_ovl, w.T * K, world)
+    sec_seq, st_seq, clocks_seq = timed(True)
+    seq_value, _ = aggregate(sec_seq, w.T * K, world)
+
+    # overlap from %globaltimer stamps of a few extra overlapped steps
+    hidden, tails = [], []
+    copy_alone_ms = float(np.median(st_seq[:, tlc.EV_DOWN]))
+    for _ in range(5):
+        step(False)
+        torch.cuda.synchronize()
+        tr = ws.view("trace").cpu().numpy().astype(np.int64)
+        tail_ms = max(0, int(tr[tlc.TRACE_COPY_END]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e6
+        tails.append(tail_ms)
+        hidden.append(1.0 - tail_ms / copy_alone_ms)
+    ms_ovl, ms_seq = sec_ovl * 1e3 / K, sec_seq * 1e3 / K
+
+    # GEMM numbers: real rows = T*k; executed rows = P (padded)
+    P = int(ws.view("meta")[0].item())
+    TK = w.T * w.topk
+    up_ms = float(np.median(st_ovl[:, tlc.EV_PLANNED]))
+    down_ms = float(np.median(st_seq[:, tlc.EV_UP]))
+    fl_up_alg, fl_down_alg = 4.0 * TK * w.d * w.ffn, 2.0 * TK * w.d * w.ffn
+    fl_up_exe, fl_down_exe = 4.0 * P * w.d * w.ffn, 2.0 * P * w.d * w.ffn
+    gemm_exec_tflops = (fl_up_exe + fl_down_exe) / ((up_ms + down_ms) * 1e-3) / 1e12
+    gemm_alg_tflops = (fl_up_alg + fl_down_alg) / ((up_ms + down_ms) * 1e-3) / 1e12
+    peak_tc = peaks["bf16_tflops_sustained"]
+
+    roof_achieved = fl_up_alg / (up_ms * 1e-3) / 1e12
+    roofline = {"kernel": "gemm_kernel<1> (SwiGLU up-projection)", "bound": "tensor",
+                "achieved": round(roof_achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
+                "frac": round(roof_achieved / peak_tc, 4), "traffic": args.traffic,
+                "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
+                "executed_tflops": round(fl_up_exe / (up_ms * 1e-3) / 1e12, 1),
+                "algorithmic_flops_per_launch": fl_up_alg, "launch_ms": round(up_ms, 4)}
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": round(sec_max * 1e3 / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "ffn": w.ffn, "E": w.E, "topk": w.topk,
+                   "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "mgb": args.mgb,
+                   "tail_assist": not args.no_tail_assist, "seed": args.seed,
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "no flush: each step streams 2.8 GB of weights and a 0.35 GB hidden buffer (> 129 MB L2)"},
+        "gpu_launches": 6 * K,
+        "clocks": clocks,
+        "roofline": roofline,
+        "gemm": {"executed_tflops": round(gemm_exec_tflops, 1), "algorithmic_tflops": round(gemm_alg_tflops, 1),
+                 "executed_frac_of_peak": round(gemm_exec_tflops / peak_tc, 4),
+                 "algorithmic_frac_of_peak": round(gemm_alg_tflops / peak_tc, 4),
+                 "executed_frac_of_burst_peak": round(gemm_exec_tflops / peaks["bf16_tflops"], 4),
+                 "peak_tflops": peak_tc, "peak_source": peaks_src, "up_ms": round(up_ms, 4),
+                 "down_ms": round(down_ms, 4), "padded_rows": P, "real_rows": TK},
+        "overlap": {"hidden_pct": round(100 * statistics.median(hidden), 2),
+                    "tail_ms": round(statistics.median(tails), 4), "copy_alone_ms": round(copy_alone_ms, 4),
+                    "wall_pct": round(100 * (ms_seq - ms_ovl) / copy_alone_ms, 2),
+                    "sequential_ms_per_step": round(ms_seq, 4), "sequential_tokens_per_s": round(seq_value, 1),
+                    "speedup_vs_sequential": round(ms_seq / ms_ovl, 4)},
+        "stages_ms": {"overlapped": {n: round(float(np.median(st_ovl[:, i])), 4) for i, n in enumerate(
+            ["route_plan_permute", "swiglu_gemm", "down_gemm_and_copy", "copy", "combine"])},
+            "sequential": {n: round(float(np.median(st_seq[:, i])), 4) for i, n in enumerate(
+                ["route_plan_permute", "swiglu_gemm", "down_gemm", "copy", "combine"])}},
+        "clocks_sequential": clocks_seq,
+    }
+
+    if not args.no_e2e:
+        logits_h = torch.from_numpy(logits_np).pin_memory()
+        x_h = x_cpu.pin_memory()
+        out_h = torch.empty(w.T, w.d, dtype=torch.float32).pin_memory()
+        for _ in range(Wm):
+            tlc.forward_host(cfg, logits_h, x_h, W["W1"], W["W3"], W["W2"], out_h, ws)
+        torch.cuda.synchronize()
+        barrier(world)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(K):
+            tlc.forward_host(cfg, logits_h, x_h, W["W1"], W["W3"], W["W2"], out_h, ws)
+        t1.record()
+        torch.cuda.synchronize()
+        e2e_value, _ = aggregate(t0.elapsed_time(t1) / 1e3, w.T * K, world)
+        res["e2e"] = {"value": round(e2e_value, 1), "unit": "tokens/s",
+                      "h2d_bytes_per_step": logits_h.numel() * 4 + x_h.numel() * 2,
+                      "d2h_bytes_per_step": out_h.numel() * 4, "call": "moe_forward_host"}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args.seed, tokens=256, W=W)
+    return res
+
+
+# ------------------------------------------------------------------------ CPU oracle timing
+def sample_workload(w, tokens: int):
+    per = max(1, tokens // w.R)
+    return w.replace(T=per * w.R)
+
+
+def oracle_weights(w, seed, W=None):
+    if W is not None:
+        return {n: W[n].double().cpu().numpy() for n in ("W1", "W3", "W2")}
+    return {n: inputs.make_weight(w, seed, n).double().numpy() for n in ("W1", "W3", "W2")}
+
+
+def cpu_baseline(w, seed: int, tokens: int, W=None, Wf=None):
+    """The oracle (fp64 NumPy) on the first `tokens` tokens of the same workload."""
+    from oracle import moe_ref
+
+    ws_ = sample_workload(w, tokens)
+    logits = inputs.make_logits(w, seed)[:ws_.T]
+    x = inputs.bf16_to_f64(inputs.make_x(w, seed)[:ws_.T])
+    Wf = Wf or oracle_weights(w, seed, W)
+    t = time.perf_counter()
+    moe_ref.moe_layer(logits, x, Wf["W1"], Wf["W3"], Wf["W2"], R=w.R, tbM=w.tile_M, k=w.topk)
+    dt = time.perf_counter() - t
+    return {"value": round(ws_.T / dt, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {ws_.T} tokens of the {w.name} workload (same d, ffn, E, top-k, R, tile_M, weights), "
+                      f"one oracle pass of {dt:.1f} s, float64 NumPy with its default BLAS threads"}
+
+
+def run_reference(args, rank: int, world: int):
+    w = inputs.WORKLOADS[args.workload]
+    if rank != 0:
+        return None
+    tokens = 256
+    Wf = oracle_weights(w, args.seed)
+    for _ in range(args.warmup):
+        cpu_baseline(w, args.seed, tokens, Wf=Wf)
+    times = []
+    for _ in range(args.steps):
+        r = cpu_baseline(w, args.seed, tokens, Wf=Wf)
+        times.append(sample_workload(w, tokens).T / r["value"])
+    T_s = sample_workload(w, tokens).T
+    value = T_s * len(times) / sum(times)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "ffn": w.ffn, "E": w.E, "topk": w.topk,
+                   "R": w.R, "tile_M": w.tile_M, "sample_tokens": T_s},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"each step: the first {T_s} tokens of the {w.name} workload through the "
+                                   f"fp64 oracle"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world = dist_setup(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py --impl ours needs a CUDA device")
+        res = run_ours(args, rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

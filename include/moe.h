@@ -1,0 +1,229 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) MoE expert layer with tile-level return-copy overlap.
+ *
+ * The method is the one of the review page "Fine-grained Computation-Communication Overlap via
+ * Tile-level Signaling and Scheduling for Mixture-of-Experts" (Cui, Wingkvist, Ericsson;
+ * pith.science/paper/W2ZARMHG), cited here as [TLS] with the section of that page:
+ *
+ *   [TLS "The pith" / "Core claim"]      the return of expert outputs to the rank that sent each
+ *        token need not wait for all expert compute: a persistent GEMM (producer) covering all
+ *        experts publishes a readiness flag per output tile; a persistent copy kernel (consumer)
+ *        on a small SM partition polls the flags and moves ready row bands to their owner.
+ *   [TLS "What carries the argument"]    remote-owner-aligned row layout (rows grouped by expert,
+ *        then by owner, each group padded to the tile height, so each tile has one owner),
+ *        remote-first tile schedule (largest transfers first), row-band segments.
+ *   [TLS "Load-bearing premise"] and [TLS "Referee Report", major comment 2, §3.3.1]  the tile
+ *        must be visible before the flag is seen: here the producer's stores are released at GPU
+ *        scope and the consumer acquires the flag before it reads.
+ *   [TLS Figure 9 caption]               the sequential baseline: per-expert GEMM, then the bulk
+ *        return copy, on identical inputs.
+ *
+ * On one GPU the R "ranks" are R logical owner partitions of the tokens: owner(t) = t / (T/R).
+ * Each owner has a return buffer (a slice of Ret) in the same HBM; the "put" is a device copy.
+ *
+ * Conventions for every entry point
+ *   - All arrays are row-major and contiguous. "device" pointers point to memory of the current
+ *     CUDA device; "host" pointers to host memory (pinned for asynchronous copies).
+ *   - bf16 arrays are passed as uint16_t bit patterns (IEEE bfloat16).
+ *   - The caller owns every buffer and the stream. The library never allocates device memory,
+ *     never frees anything and never synchronises the stream except in moe_status().
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default stream.
+ *   - Return value: MOE_OK or a negative MOE_ERR_* code; no exception crosses the ABI, and the
+ *     device never traps. moe_last_error() gives a message for the calling thread.
+ *   - Work is enqueued on `stream`; results are valid once the stream has reached that point.
+ *   - One workspace must not be used by two calls that can run at the same time.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_API __attribute__((visibility("default")))
+
+/* ---- return codes ---------------------------------------------------------------------- */
+#define MOE_OK 0
+#define MOE_ERR_ARG (-1)       /* invalid config, NULL pointer, misaligned pointer          */
+#define MOE_ERR_WORKSPACE (-2) /* workspace smaller than moe_workspace_size()               */
+#define MOE_ERR_CUDA (-3)      /* a CUDA runtime / driver call failed (launch, copy, ...)   */
+#define MOE_ERR_TIMEOUT (-4)   /* a bounded device wait ran out (reported by moe_status)    */
+#define MOE_ERR_DEVICE (-5)    /* current device is not sm_103 / lacks the needed resources */
+#define MOE_ERR_PLAN (-6)      /* a device-side bounds check on plan indices failed         */
+
+/* ---- config flags ---------------------------------------------------------------------- */
+#define MOE_PLAN_SKIP_PERMUTE 0x1u    /* moe_plan: stop after the plan, do not fill Xp        */
+#define MOE_TAIL_ASSIST 0x2u          /* producer CTAs that finish their GEMM tiles join the  */
+                                      /* copy (the consumer partition is unchanged)           */
+#define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
+                                      /* producer writes, so their bounded wait runs out      */
+
+/*
+ * Problem and knobs.
+ *   T tokens, model width d, expert hidden width ffn, E experts, top-k = topk, R owners,
+ *   tile_M = GEMM tile height tbM (each (expert, owner) group is padded to a multiple of it).
+ *   consumer_ctas = c_CTA, the SMs given to the consumer ([TLS "Axiom & Free-Parameter Ledger"],
+ *   swept 2-24 on the page); mgb = bands per interior segment (same section, 1 or 2 there).
+ *   timeout_us bounds every device-side wait (0 = 2,000,000 us).
+ * Limits: d % 128 == 0, ffn % 128 == 0, 1 <= topk <= min(E, 8), 1 <= E <= 256, T % R == 0,
+ *   E*R <= 1024, tile_M in {64, 128}, 1 <= mgb <= 4, 1 <= consumer_ctas <= SMs/2 (checked at
+ *   launch), P_max < 2^30 (see moe_layout).
+ */
+typedef struct moe_config {
+    int32_t T, d, ffn, E, topk, R, tile_M;
+    int32_t consumer_ctas;
+    int32_t mgb;
+    uint32_t flags;
+    uint32_t timeout_us;
+    int32_t reserved[5]; /* must be zero */
+} moe_config;
+
+/*
+ * Byte offsets (from the workspace base) and sizes of the regions of a workspace. Every region
+ * starts on a 1024-byte boundary. Shapes use P_max = the largest padded row count the routing can
+ * produce, T*topk + min(E*R, T*topk)*(tile_M-1) rounded up to tile_M ([TLS "Referee Report",
+ * major comment 1]: padding is per (expert, owner) group), and MT_max = P_max / tile_M.
+ */
+typedef struct moe_layout {
+    size_t bytes;                     /* total workspace size                              */
+    int32_t P_max, MT_max, n_chunks, chunk_tokens, n_tiles_n2, block_n2, rows_per_unit, units_per_band;
+    size_t idx;        /* int32 [T, topk]   expert of pair (t, j), descending logit            */
+    size_t gate;       /* f32   [T, topk]   gate of pair (t, j)                                */
+    size_t rank;       /* int32 [T, topk]   rank of t among the chunk's tokens routed to e     */
+    size_t chunk_cnt;  /* int32 [n_chunks, E]                                                  */
+    size_t chunk_base; /* int32 [n_chunks, E] rows of e in earlier chunks of the same owner    */
+    size_t counts;     /* int32 [E, R]      n_{e,r} = |G_{e,r}|                                */
+    size_t offsets;    /* int32 [E*R + 1]   first padded row of group e*R+r; last entry = P    */
+    size_t ret_off;    /* int32 [R, E + 1]  exclusive prefix over e of n_{e,r}                 */
+    size_t tiles;      /* int32 [MT_max, 4] (e, r, row0, valid) per M-tile, layout order       */
+    size_t tile_ret;   /* int32 [MT_max]    row of Ret receiving the tile's first row          */
+    size_t sched;      /* int32 [MT_max]    M-tile at each schedule position                   */
+    size_t seg;        /* int32 [MT_max, 2] (first position, bands) of each position's segment */
+    size_t experts;    /* int32 [E, 2]      (first M-tile, M-tiles) of each expert             */
+    size_t slot;       /* int32 [T, topk]   row of pair (t, j) in Xp / Yp                      */
+    size_t ret_slot;   /* int32 [T, topk]   row of pair (t, j) in Ret                          */
+    size_t meta;       /* int32 [64]        P, M-tiles, work counters, status (see csrc)       */
+    size_t flags;      /* uint32 [MT_max, n_tiles_n2] per-tile readiness flags                 */
+    size_t trace;      /* uint64 [16]       %globaltimer stamps of the last call (ns)          */
+    size_t Xp;         /* bf16 [P_max, d]   permuted tokens                                    */
+    size_t Hp;         /* bf16 [P_max, ffn] SwiGLU hidden                                      */
+    size_t Yp;         /* bf16 [P_max, d]   expert outputs                                     */
+    size_t Ret;        /* bf16 [T*topk, d]  owner return buffers, R slices of (T/R)*topk rows  */
+    size_t in_logits;  /* f32  [T, E]       staging for moe_forward_host                       */
+    size_t in_x;       /* bf16 [T, d]       staging for moe_forward_host                       */
+    size_t out;        /* f32  [T, d]       staging for moe_forward_host                       */
+} moe_layout;
+
+/* Trace slots (uint64 ns, %globaltimer) written by the last moe_forward / _sequential call. */
+#define MOE_TRACE_GEMM2_START 0  /* earliest start of a down-projection tile                 */
+#define MOE_TRACE_GEMM2_END 1    /* latest readiness flag (overlapped) / tile end (sequential) */
+#define MOE_TRACE_COPY_START 2   /* earliest start of a row-band copy                        */
+#define MOE_TRACE_COPY_END 3     /* latest completion of a row-band copy                     */
+
+/* Size in bytes of the workspace for `cfg` (host-only arithmetic, no CUDA call).
+ * Returns MOE_ERR_ARG for an invalid config. */
+MOE_API int moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Offsets of the workspace regions for `cfg` (host-only arithmetic). For tests and tools that
+ * read the plan or the intermediates; the contents are valid after a call on the stream. */
+MOE_API int moe_workspace_layout(const moe_config* cfg, moe_layout* out);
+
+/*
+ * moe_plan: router + layout, the first half of the forward pass.
+ *   logits   device f32  [T, E]   router logits (finite)
+ *   x        device bf16 [T, d]   tokens (may be NULL with MOE_PLAN_SKIP_PERMUTE)
+ *   topk_idx device int32 [T, topk] or NULL: copy of the routing (experts, descending logit,
+ *            ties to the lower expert id)
+ *   topk_w   device f32 [T, topk] or NULL: gates, softmax over the k chosen logits
+ *   ws       device workspace of ws_bytes >= moe_workspace_size(cfg), 256-byte aligned
+ * Fills the workspace's idx, gate, counts, offsets, tiles, sched, seg, slot, ret_slot, ... and
+ * (unless MOE_PLAN_SKIP_PERMUTE) Xp with zero padding rows. The histogram / scan / tile-owner map
+ * follow [TLS "What carries the argument"]; the plan is built on the device, so no host round
+ * trip is needed before the GEMMs ([TLS "Referee Report", minor comment 4, §2.2]).
+ */
+MOE_API int moe_plan(const moe_config* cfg, const float* logits, const uint16_t* x, int32_t* topk_idx,
+                     float* topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward: the whole MoE layer with the tile-level overlapped return copy.
+ *   logits device f32 [T, E]; x device bf16 [T, d];
+ *   W1, W3 device bf16 [E, ffn, d] (gate and up projections, K-major);
+ *   W2     device bf16 [E, d, ffn] (down projection, K-major);
+ *   out    device f32 [T, d]: out[t] = sum_j gate[t, j] * FFN_{idx[t, j]}(x[t]),
+ *          FFN_e(v) = W2_e (silu(W1_e v) * (W3_e v));
+ *   ws     workspace as in moe_plan. Weights and x are only read; 16-byte aligned pointers.
+ * Steps on `stream`: route, plan, permute, SwiGLU grouped GEMM over all experts (one persistent
+ * launch), then one cooperative launch in which SMs - consumer_ctas CTAs run the down-projection
+ * GEMM in remote-first order and release a flag per finished tile while consumer_ctas CTAs acquire
+ * the flags and copy each ready segment of row bands into its owner's slice of Ret, then the
+ * weighted top-k combine. A bounded wait that runs out is reported by moe_status(), not here.
+ */
+MOE_API int moe_forward(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
+                        const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * moe_forward_sequential: same arguments and result as moe_forward; the down-projection GEMM runs
+ * on all SMs without flags, then the return copy runs on all SMs, then the combine. This is the
+ * GEMM-then-copy baseline of [TLS Figure 9 caption]; the two GEMM launches use the same tile code,
+ * so its out, Yp and Ret are bitwise equal to moe_forward's.
+ */
+MOE_API int moe_forward_sequential(const moe_config* cfg, const float* logits, const uint16_t* x,
+                                   const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, float* out,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward_ex: moe_forward (sequential == 0) or moe_forward_sequential (sequential != 0) that
+ * also records caller-created CUDA events (cudaEvent_t passed as void*) on `stream` between the
+ * launches, for per-stage timing; stage_events may be NULL, and so may any entry:
+ *   [MOE_EV_BEGIN]     before routing            [MOE_EV_PLANNED] after the permute
+ *   [MOE_EV_UP]        after the SwiGLU GEMM     [MOE_EV_DOWN]    after the down-projection launch
+ *                                                                 (overlapped: GEMM + return copy)
+ *   [MOE_EV_COPIED]    after the return copy (overlapped: same point as MOE_EV_DOWN)
+ *   [MOE_EV_END]       after the combine
+ */
+#define MOE_EV_BEGIN 0
+#define MOE_EV_PLANNED 1
+#define MOE_EV_UP 2
+#define MOE_EV_DOWN 3
+#define MOE_EV_COPIED 4
+#define MOE_EV_END 5
+#define MOE_EV_COUNT 6
+MOE_API int moe_forward_ex(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
+                           const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes,
+                           int sequential, void* const* stage_events, void* stream);
+
+/*
+ * moe_forward_host: moe_forward with host inputs and output, the call a serving process makes per
+ * batch with weights resident on the device. logits_h (f32 [T, E]) and x_h (bf16 [T, d]) are copied
+ * into the workspace's staging regions, the layer runs, and out_h (f32 [T, d]) receives the result;
+ * all on `stream` (use pinned host memory for asynchronous copies). out_h is valid once the stream
+ * has reached the end of this call. `sequential` != 0 selects the GEMM-then-copy baseline.
+ */
+MOE_API int moe_forward_host(const moe_config* cfg, const float* logits_h, const uint16_t* x_h,
+                             const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, float* out_h,
+                             void* ws, size_t ws_bytes, int sequential, void* stream);
+
+/*
+ * moe_status: synchronises `stream`, then reads the device status word of the last call that used
+ * `ws`. Returns MOE_OK, MOE_ERR_TIMEOUT (a flag or pipeline wait ran out; *detail = where) or
+ * MOE_ERR_PLAN (a bounds check on plan indices failed). The word is cleared by the next call.
+ * detail may be NULL.
+ */
+MOE_API int moe_status(const moe_config* cfg, const void* ws, void* stream, int32_t* detail);
+
+/* Number of SMs of the current device and whether it is supported (sm_103); host query only. */
+MOE_API int moe_device_info(int32_t* sm_count, int32_t* supported);
+
+/* Message of the last error on the calling thread ("" if none). The pointer stays valid until
+ * the thread's next call into the library. */
+MOE_API const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

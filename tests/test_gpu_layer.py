@@ -1,0 +1,139 @@
+"""The whole MoE layer on the GPU against the fp64 oracle, and overlapped against sequential.
+
+Bar: layer output within max-abs 2e-2 and relative L2 5e-3 of the fp64 oracle; routing indices
+bit-exact; the overlapped path bitwise equal to the GEMM-then-copy path (both run the same tile
+code); every copied row of Ret byte-equal to its row of Yp.
+"""
+import numpy as np
+import pytest
+import torch
+
+import tile_level_copy_gb300 as tlc
+from oracle import moe_ref
+from tile_level_copy_gb300 import inputs
+from tests.gpu_util import MAX_ABS, REL_L2, Layer, parity, per_token_rel_distance, small
+
+pytestmark = pytest.mark.gpu
+
+
+def check_ret_is_copy_of_yp(L: Layer, plan):
+    Yp = L.ws.view("Yp").view(torch.int16)
+    Ret = L.ws.view("Ret").view(torch.int16)
+    slot = torch.from_numpy(plan.slot.reshape(-1)).long().cuda()
+    rslot = torch.from_numpy(plan.ret_slot.reshape(-1)).long().cuda()
+    assert torch.equal(Ret[rslot], Yp[slot])
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "skew", "fine"])
+def test_layer_matches_oracle_small_shapes(name):
+    w = small(name)
+    L = Layer(w, seed=0, cfg_kw=dict(consumer_ctas=8))
+    ref = L.oracle_layer()
+    out_ovl = L.run(sequential=False).double().cpu().numpy()
+    np.testing.assert_array_equal(L.ws.view("idx").cpu().numpy(), ref.idx)
+    err, rel = parity(out_ovl, ref.out)
+    assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
+    # intermediates: SwiGLU hidden and expert outputs on the real rows
+    rows = ref.plan.slot.reshape(-1)
+    Hp = L.ws.view("Hp")[:ref.plan.P].double().cpu().numpy()
+    _, hrel = parity(Hp[rows], ref.Hp[rows])
+    assert hrel <= 5e-3, hrel
+    Yp = L.ws.view("Yp")[:ref.plan.P].double().cpu().numpy()
+    _, yrel = parity(Yp[rows], ref.Yp[rows])
+    assert yrel <= 5e-3, yrel
+    check_ret_is_copy_of_yp(L, ref.plan)
+    # the page's per-token relative distance, reported beside the gate
+    assert per_token_rel_distance(out_ovl, ref.out).max() < 5e-2
+    # sequential baseline: bitwise equal
+    ret_ovl = L.ws.view("Ret").clone()
+    out_seq = L.run(sequential=True).double().cpu().numpy()
+    np.testing.assert_array_equal(out_seq, out_ovl)
+    assert torch.equal(L.ws.view("Ret"), ret_ovl)
+
+
+@pytest.mark.parametrize("consumers,mgb,flags", [
+    (1, 1, 0), (2, 2, 0), (4, 1, tlc.MOE_TAIL_ASSIST), (16, 2, tlc.MOE_TAIL_ASSIST), (32, 4, 0),
+])
+def test_partition_and_segment_knobs_do_not_change_results(consumers, mgb, flags):
+    w = small("skew")
+    L = Layer(w, seed=1)
+    base = L.run(sequential=True)
+    cfg = tlc.Config.from_workload(w, consumer_ctas=consumers, mgb=mgb, flags=flags)
+    got = L.run(sequential=False, cfg=cfg)
+    assert torch.equal(got, base)
+
+
+@pytest.mark.parametrize("seed", range(100))
+def test_tile_checksum_falsifier(seed):
+    """Every tile the consumer copied must equal, byte for byte, the tile the producer stored.
+
+    This is the page's proposed falsifier of the flag protocol ("What would settle it": checksummed
+    tiles under stress) run over 100 seeds of the skewed workload with a tiny consumer partition.
+    """
+    w = inputs.WORKLOADS["skew"].replace(T=1024, d=256, ffn=256)
+    L = Layer(w, seed=seed, cfg_kw=dict(consumer_ctas=2 + seed % 7, mgb=1 + seed % 2,
+                                        flags=tlc.MOE_TAIL_ASSIST if seed % 3 == 0 else 0))
+    L.run(sequential=False)
+    idx, _ = moe_ref.route_topk(L.logits_np, w.topk)
+    plan = moe_ref.build_plan(idx, w.E, w.R, w.tile_M, L.cfg.mgb)
+    check_ret_is_copy_of_yp(L, plan)
+
+
+def test_stalled_consumer_times_out_and_context_survives():
+    w = small("tiny")
+    L = Layer(w, seed=0)
+    want = L.run(sequential=True)
+    cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=tlc.MOE_TEST_STALL_CONSUMER, timeout_us=20000)
+    tlc.forward(cfg, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws)
+    rc, detail = tlc.status(cfg, L.ws)
+    assert rc == tlc.MOE_ERR_TIMEOUT
+    assert "timed out" in tlc.lib().moe_last_error().decode()
+    # the context is still usable and the next call is correct
+    assert torch.equal(L.run(sequential=False), want)
+
+
+def test_forward_host_equals_device_forward():
+    w = small("mixtral")
+    L = Layer(w, seed=2, cfg_kw=dict(consumer_ctas=8))
+    want = L.run(sequential=False).cpu()
+    logits_h = torch.from_numpy(L.logits_np).pin_memory()
+    x_h = L.x_cpu.pin_memory()
+    out_h = torch.empty(w.T, w.d, dtype=torch.float32).pin_memory()
+    tlc.forward_host(L.cfg, logits_h, x_h, L.W["W1"], L.W["W3"], L.W["W2"], out_h, L.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, want)
+
+
+def test_argument_errors_on_gpu():
+    w = small("tiny")
+    L = Layer(w, seed=0)
+    small_ws = tlc.Workspace(L.cfg)
+    small_ws.nbytes = small_ws.nbytes - 1024
+    with pytest.raises(tlc.MoEError) as ei:
+        tlc.forward(L.cfg, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, small_ws)
+    assert ei.value.code == tlc.MOE_ERR_WORKSPACE
+    sms, ok = tlc.device_info()
+    assert ok and sms >= 100
+    bad = tlc.Config.from_workload(w, consumer_ctas=sms)
+    with pytest.raises(tlc.MoEError) as ei:
+        tlc.forward(bad, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws)
+    assert ei.value.code == tlc.MOE_ERR_ARG
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mixtral", "skew", "fine"])
+def test_full_size_sampled_tokens(name):
+    """Full workload sizes in the bench's launch configuration; 48 sampled tokens against the
+    oracle's per-token definition, plus bitwise overlapped == sequential over all tokens."""
+    w = inputs.WORKLOADS[name]
+    L = Layer(w, seed=0, cfg_kw=dict(consumer_ctas=8, flags=tlc.MOE_TAIL_ASSIST))
+    got = L.run(sequential=False)
+    seq = L.run(sequential=True)
+    assert torch.equal(got, seq)
+    rng = np.random.default_rng(7)
+    tokens = np.sort(rng.choice(w.T, size=48, replace=False))
+    tokens[0], tokens[-1] = 0, w.T - 1  # include both ends
+    x_rows = inputs.bf16_to_f64(L.x_cpu[tokens])
+    _, _, want = moe_ref.moe_tokens(tokens, L.logits_np, x_rows, L.weights_f64, w.topk)
+    err, rel = parity(got.double().cpu().numpy()[tokens], want)
+    assert err <= MAX_ABS and rel <= REL_L2, (err, rel)

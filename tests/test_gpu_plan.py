@@ -1,0 +1,106 @@
+"""Routing, plan and permute on the GPU, bit-exact against the oracle.
+
+Indices, counts, offsets, tile-owner map, schedule, segments, slots, return slots and the permuted
+rows (with zero padding) have exactly one correct value each, so they are compared for equality.
+"""
+import numpy as np
+import pytest
+import torch
+
+import tile_level_copy_gb300 as tlc
+from oracle import moe_ref
+from tile_level_copy_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def run_plan(w: inputs.Workload, logits_np: np.ndarray, x_cpu, mgb=1, skip_permute=False):
+    cfg = tlc.Config.from_workload(w, mgb=mgb, flags=tlc.MOE_PLAN_SKIP_PERMUTE if skip_permute else 0)
+    ws = tlc.Workspace(cfg)
+    logits = torch.from_numpy(logits_np).cuda()
+    x = None if x_cpu is None else x_cpu.cuda()
+    idx = torch.empty(w.T, w.topk, dtype=torch.int32, device="cuda")
+    gate = torch.empty(w.T, w.topk, dtype=torch.float32, device="cuda")
+    tlc.plan(cfg, logits, x, ws, idx, gate)
+    rc, detail = tlc.status(cfg, ws)
+    assert rc == tlc.MOE_OK, (rc, detail)
+    return cfg, ws, idx.cpu().numpy(), gate.cpu().numpy()
+
+
+def check_plan(w, logits_np, x_cpu, mgb=1):
+    cfg, ws, idx, gate = run_plan(w, logits_np, x_cpu, mgb)
+    ridx, rgate = moe_ref.route_topk(logits_np, w.topk)
+    np.testing.assert_array_equal(idx, ridx)
+    np.testing.assert_allclose(gate, rgate, rtol=2e-6, atol=1e-7)
+    plan = moe_ref.build_plan(ridx, w.E, w.R, w.tile_M, mgb)
+    v = lambda n: ws.view(n).cpu().numpy()
+    meta = v("meta")
+    assert meta[0] == plan.P and meta[1] == plan.num_tiles
+    MT = plan.num_tiles
+    np.testing.assert_array_equal(v("counts"), plan.n)
+    np.testing.assert_array_equal(v("offsets"), plan.off)
+    np.testing.assert_array_equal(v("ret_off"), plan.ret_off)
+    np.testing.assert_array_equal(v("tiles")[:MT], plan.tiles)
+    np.testing.assert_array_equal(v("tile_ret")[:MT], plan.ret_row0)
+    np.testing.assert_array_equal(v("sched")[:MT], plan.sched)
+    np.testing.assert_array_equal(v("seg")[:MT], plan.seg)
+    np.testing.assert_array_equal(v("slot"), plan.slot)
+    np.testing.assert_array_equal(v("ret_slot"), plan.ret_slot)
+    if x_cpu is not None:
+        xb = x_cpu.view(torch.int16).numpy()
+        want = moe_ref.permute(xb, plan)
+        got = ws.view("Xp")[:plan.P].view(torch.int16).cpu().numpy()
+        np.testing.assert_array_equal(got, want)
+    return plan
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "skew", "fine"])
+@pytest.mark.parametrize("mgb", [1, 2])
+def test_plan_bitexact_full_size(name, mgb):
+    w = inputs.WORKLOADS[name]
+    check_plan(w, inputs.make_logits(w, 0), inputs.make_x(w, 0) if mgb == 1 else None, mgb)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_plan_bitexact_seeds_skew(seed):
+    w = inputs.WORKLOADS["skew"]
+    plan = check_plan(w, inputs.make_logits(w, seed), inputs.make_x(w, seed))
+    assert (plan.n == 0).any()  # the Zipf bias leaves some groups empty
+
+
+def test_forced_ties_go_to_lowest_expert():
+    w = inputs.WORKLOADS["fine"].replace(T=1024)
+    rng = np.random.default_rng(5)
+    logits = rng.integers(-1, 2, size=(w.T, w.E)).astype(np.float32)  # massive ties
+    logits[::7] = 0.0                                                  # whole rows tied
+    logits[3, :] = -0.0
+    check_plan(w, logits, inputs.make_x(w, 0))
+
+
+@pytest.mark.parametrize("shape", [
+    dict(T=8, d=128, ffn=128, E=1, topk=1, R=1, tile_M=64),     # one group, ragged tile
+    dict(T=6, d=128, ffn=128, E=3, topk=2, R=3, tile_M=128),    # T/R = 2: chunks of 2 tokens
+    dict(T=300, d=256, ffn=128, E=5, topk=3, R=5, tile_M=64),   # T/R = 60: chunks of 4 tokens
+    dict(T=1000, d=128, ffn=256, E=256, topk=8, R=4, tile_M=128),  # max E, max k, mostly 1-row groups
+    dict(T=64, d=128, ffn=128, E=16, topk=1, R=64, tile_M=128),  # one token per owner
+])
+def test_plan_edge_shapes(shape):
+    w = inputs.Workload("edge", **shape)
+    check_plan(w, inputs.make_logits(w, 3), inputs.make_x(w, 3))
+
+
+def test_all_tokens_to_one_expert():
+    w = inputs.WORKLOADS["skew"].replace(T=2048)
+    logits = np.full((w.T, w.E), -5.0, np.float32)
+    logits[:, 7] = 1.0
+    logits[:, 2] = 0.5
+    plan = check_plan(w, logits, inputs.make_x(w, 1))
+    assert set(plan.tiles[:, 0].tolist()) == {2, 7}
+
+
+def test_plan_skip_permute_leaves_xp_untouched():
+    w = inputs.WORKLOADS["tiny"]
+    cfg, ws, _, _ = run_plan(w, inputs.make_logits(w, 0), None, skip_permute=True)
+    ref_idx, _ = moe_ref.route_topk(inputs.make_logits(w, 0), w.topk)
+    plan = moe_ref.build_plan(ref_idx, w.E, w.R, w.tile_M)
+    np.testing.assert_array_equal(ws.view("slot").cpu().numpy(), plan.slot)

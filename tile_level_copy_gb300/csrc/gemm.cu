@@ -1,0 +1,384 @@
+// Persistent grouped expert GEMMs on tcgen05 (UMMA 128 x N x 16, fp32 accumulators in TMEM),
+// fed by TMA through a 4-stage shared-memory ring, with warp-specialised roles:
+//   warp 0      one thread issues the TMA loads of A (token rows) and B (expert weights)
+//   warp 1      allocates 512 TMEM columns; one thread issues the UMMAs (two accumulators, so the
+//               epilogue of tile i overlaps the main loop of tile i+1)
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, conversion, stores to global memory
+//
+// Method: "Fine-grained Computation-Communication Overlap via Tile-level Signaling and Scheduling
+// for Mixture-of-Experts" (pith.science/paper/W2ZARMHG):
+//   "Core claim" - one rank-wide persistent GEMM covers all experts in one launch and publishes a
+//       readiness flag after each tile's epilogue store;
+//   "Load-bearing premise" and "Referee Report" major comment 2 (§3.3.1) - the tile must be
+//       visible before the flag: every epilogue thread fences its stores at GPU scope, each of the
+//       four epilogue warps then adds 1 to the tile flag with red.release.gpu; the consumer reads
+//       the flag with ld.acquire.gpu (ready at 4) and fences the async proxy before its bulk copy.
+//   "What carries the argument" - the consumer runs on a small dedicated SM partition; here the
+//       partition is the last consumer_ctas CTAs of the same cooperative launch, so producers and
+//       consumers are guaranteed to be co-resident.
+#include "copy_ring.cuh"
+
+namespace moe {
+
+struct Smem {
+    uint8_t* stages;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* acc_full;
+    uint64_t* acc_empty;
+    uint64_t* drain;
+    uint64_t* cbar;
+    uint32_t* tmem_base;
+    volatile int* abort;
+    volatile int* unit;
+    int* tab;  // [cum (E+1) | first (E) | count (E)]
+};
+
+__device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
+    Smem sm;
+    const uint32_t a = smem_u32(raw);
+    uint8_t* base = raw + (((a + 1023u) & ~1023u) - a);
+    sm.stages = base;
+    uint8_t* misc = base + STAGES * STAGE_BYTES;
+    sm.full = reinterpret_cast<uint64_t*>(misc);
+    sm.empty = sm.full + STAGES;
+    sm.acc_full = sm.empty + STAGES;
+    sm.acc_empty = sm.acc_full + 2;
+    sm.drain = sm.acc_empty + 2;
+    sm.cbar = sm.drain + 1;
+    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.cbar + COPY_NBUF);
+    sm.abort = reinterpret_cast<volatile int*>(sm.tmem_base + 1);
+    sm.unit = sm.abort + 1;
+    sm.tab = const_cast<int*>(sm.unit + 2);
+    return sm;
+}
+
+struct TileRef {
+    int m, n, e, row0;
+};
+
+// SwiGLU GEMM order: expert-major; inside an expert, N tiles outer and M tiles inner, so the CTAs
+// working at the same time share each weight tile through L2.
+__device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, int nN, const int32_t* tiles) {
+    const int* cum = tab;
+    const int* first = tab + (E + 1);
+    const int* count = first + E;
+    int lo = 0, hi = E - 1;  // largest e with cum[e] <= t
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo, local = t - cum[e], cnt = count[e];
+    TileRef r;
+    r.n = local / cnt;
+    r.m = first[e] + local % cnt;
+    r.e = e;
+    r.row0 = tiles[4 * r.m + 2];
+    (void)nN;
+    return r;
+}
+
+// Down-projection order: schedule positions (remote-first), all N tiles of a band together.
+__device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* sched, const int32_t* tiles) {
+    TileRef r;
+    const int pos = t / nN;
+    r.n = t - pos * nN;
+    r.m = sched[pos];
+    r.e = tiles[4 * r.m + 0];
+    r.row0 = tiles[4 * r.m + 2];
+    return r;
+}
+
+template <int MODE>  // 1: SwiGLU up-projection -> Hp; 2: down-projection -> Yp (+ flags / consumer)
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, int num_producers, int overlapped) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem sm = carve_smem(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const bool producer = (int)blockIdx.x < num_producers;
+
+    int MT = p.meta[META_MTILES];
+    if (MT < 0 || MT > s.MT_max) MT = 0;
+    const int nN = (MODE == 1) ? s.ffn / BN1 : s.n_tiles_n2;
+    const int BN = (MODE == 1) ? 2 * BN1 : s.bn2;  // UMMA N
+    const int KB = ((MODE == 1) ? s.d : s.ffn) / BK;
+    const int total = MT * nN;
+    const uint32_t tx_bytes = A_STAGE_BYTES + BN * BK * 2;
+    const unsigned long long tmo = s.timeout_ns;
+
+    if (tid == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.acc_full[i], 1);
+            mbar_init(&sm.acc_empty[i], 128);
+        }
+        mbar_init(sm.drain, 1);
+        for (int i = 0; i < COPY_NBUF; ++i) mbar_init(&sm.cbar[i], 1);
+        *sm.abort = 0;
+        mbar_fence_init();
+    }
+    if (MODE == 1) {
+        for (int e = tid; e < s.E; e += GEMM_THREADS) {
+            sm.tab[(s.E + 1) + e] = p.experts[2 * e + 0];
+            sm.tab[(s.E + 1) + s.E + e] = p.experts[2 * e + 1];
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0;
+            for (int e = 0; e < s.E; ++e) {
+                sm.tab[e] = acc;
+                acc += sm.tab[(s.E + 1) + s.E + e] * nN;
+            }
+            sm.tab[s.E] = acc;
+        }
+    }
+    if (producer && warp == 1) {
+        tmem_alloc(sm.tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (producer && tid == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB0);
+        if (MODE == 1) tma_prefetch_desc(&tmB1);
+        if (MODE == 2) atomicMin(&p.trace[MOE_TRACE_GEMM2_START], globaltimer());
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = producer ? *sm.tmem_base : 0u;
+    unsigned long long last_end = 0;
+
+    if (producer) {
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer ----------------
+            int st = 0;
+            uint32_t ph = 0, issued = 0, last_ph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += num_producers) {
+                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, nN, p.tiles)
+                                               : decode_down(t, nN, p.sched, p.tiles);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.full[st], tx_bytes);
+                    uint8_t* a = sm.stages + st * STAGE_BYTES;
+                    uint8_t* b = a + A_STAGE_BYTES;
+                    tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.row0);
+                    if (MODE == 1) {
+                        tma_load_3d(b, &tmB0, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
+                        tma_load_3d(b + BN1 * BK * 2, &tmB1, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
+                    } else {
+                        tma_load_3d(b, &tmB0, &sm.full[st], kb * BK, tr.n * BN, tr.e);
+                    }
+                    issued |= 1u << st;
+                    last_ph = (last_ph & ~(1u << st)) | (ph << st);
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 0);
+                *sm.abort = 1;
+                int never = 0;
+                for (int i = 0; i < STAGES; ++i)  // let loads in flight land before the CTA leaves
+                    if (issued & (1u << i)) mbar_wait(&sm.full[i], (last_ph >> i) & 1u, tmo, &never);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ---------------- UMMA issuer ----------------
+            const uint32_t idesc = umma_idesc_bf16(BM, BN);
+            int st = 0, b = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true, any = false;
+            for (int t = blockIdx.x; t < total && ok; t += num_producers) {
+                if (!mbar_wait(&sm.acc_empty[b], aph ^ 1u, tmo, sm.abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dt = tmem + (uint32_t)(b * 256);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&sm.full[st], ph, tmo, sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sm.stages + st * STAGE_BYTES);
+                    const uint64_t ad = sdesc_sw128(a_addr);
+                    const uint64_t bd = sdesc_sw128(a_addr + A_STAGE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)  // +32 bytes along K per UMMA_K = 16
+                        umma_bf16(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    umma_commit(&sm.empty[st]);
+                    any = true;
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&sm.acc_full[b]);
+                b ^= 1;
+                if (b == 0) aph ^= 1u;
+            }
+            if (!ok) {
+                if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 1);
+                *sm.abort = 1;
+                if (any) {  // wait for the UMMAs in flight before TMEM is released
+                    int never = 0;
+                    umma_commit(sm.drain);
+                    mbar_wait(sm.drain, 0, tmo, &never);
+                }
+            }
+        } else if (warp >= 2) {
+            // ---------------- epilogue ----------------
+            const int q = warp & 3;  // TMEM lane quarter this warp may access
+            const int row = q * 32 + lane;
+            const bool store = row < s.tbM;
+            const bool flags = (MODE == 2) && overlapped;
+            int b = 0;
+            uint32_t aph = 0;
+            for (int t = blockIdx.x; t < total; t += num_producers) {
+                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, nN, p.tiles)
+                                               : decode_down(t, nN, p.sched, p.tiles);
+                if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
+                    if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 2);
+                    *sm.abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
+                if (MODE == 1) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.Hp + (size_t)(tr.row0 + row) * s.ffn + tr.n * BN1);
+#pragma unroll 1
+                    for (int c = 0; c < BN1 / 32; ++c) {
+                        uint32_t g[32], u[32];
+                        tmem_ld32(tb + c * 32, g);
+                        tmem_ld32(tb + BN1 + c * 32, u);
+                        if (store) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                                const float h0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * i]);
+                                const float h1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
+                                pk[i] = pack_bf16x2(h0, h1);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        }
+                    }
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(p.Yp + (size_t)(tr.row0 + row) * s.d + tr.n * BN);
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(tb + c * 32, v);
+                        if (store) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&sm.acc_empty[b]);
+                if (MODE == 2) {
+                    if (flags) {
+                        // Each epilogue warp publishes its quarter of the tile: every lane fences its
+                        // stores at GPU scope, the warp converges, then lane 0 adds 1 to the tile's
+                        // flag with release semantics. The tile is ready when the flag reaches 4.
+                        __threadfence();
+                        __syncwarp();
+                        if (lane == 0) red_release_gpu_add(p.flags + (size_t)tr.m * s.n_tiles_n2 + tr.n, 1u);
+                    }
+                    if (lane == 0) last_end = globaltimer();
+                }
+                b ^= 1;
+                if (b == 0) aph ^= 1u;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (producer && warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+    if (MODE == 2 && producer && warp >= 2 && lane == 0 && last_end)
+        atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
+
+    if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST))) {
+        CopyRing cr{sm.stages, sm.cbar, 0u, 0u};
+        const uint32_t want = (s.flags & MOE_TEST_STALL_CONSUMER) ? FLAG_READY + 1u : FLAG_READY;
+        copy_units(s, p, cr, sm.unit, sm.abort, META_QUEUE, true, want);
+    }
+}
+
+static cudaError_t set_smem_attr(const void* fn) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+}
+
+cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW1,
+                               const CUtensorMap& tmW3, int sms, cudaStream_t st) {
+    cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<1>));
+    if (e != cudaSuccess) return e;
+    gemm_kernel<1><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(s, p, tmA, tmW1, tmW3, sms, 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2,
+                             int sms, int consumers, bool overlapped, cudaStream_t st) {
+    cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<2>));
+    if (e != cudaSuccess) return e;
+    const int producers = overlapped ? sms - consumers : sms;
+    int ov = overlapped ? 1 : 0;
+    Shape sa = s;
+    PlanPtrs pa = p;
+    CUtensorMap a = tmA, b0 = tmW2, b1 = tmW2;
+    if (!overlapped) {
+        gemm_kernel<2><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(sa, pa, a, b0, b1, producers, ov);
+        return cudaGetLastError();
+    }
+    // Cooperative launch: every CTA (producers and consumers) is resident at once, or the launch
+    // fails; the consumers' waits on producer flags can therefore always be satisfied.
+    void* args[] = {&sa, &pa, &a, &b0, &b1, (void*)&producers, &ov};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&gemm_kernel<2>), dim3(sms), dim3(GEMM_THREADS),
+                                       args, GEMM_SMEM, st);
+}
+
+// Sequential return copy: every SM takes copy units, no flags ([TLS Figure 9 caption] baseline).
+__global__ void __launch_bounds__(GEMM_THREADS, 1) copy_seq_kernel(Shape s, PlanPtrs p) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem sm = carve_smem(smem_raw);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < COPY_NBUF; ++i) mbar_init(&sm.cbar[i], 1);
+        *sm.abort = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    CopyRing cr{sm.stages, sm.cbar, 0u, 0u};
+    copy_units(s, p, cr, sm.unit, sm.abort, META_QUEUE_SEQ, false, 0u);
+}
+
+cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st) {
+    cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&copy_seq_kernel));
+    if (e != cudaSuccess) return e;
+    copy_seq_kernel<<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(s, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

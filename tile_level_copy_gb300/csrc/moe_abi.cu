@@ -1,0 +1,439 @@
+// Host side of libmoe: argument checks, workspace layout, TMA descriptors and the launch
+// sequences behind the C ABI declared in include/moe.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+    moe_layout L;
+    Shape S;
+};
+
+// Checks the config and derives the workspace layout and the kernel shape.
+int make_layout(const moe_config* c, Layout* out) {
+    if (!c) return fail(MOE_ERR_ARG, "config is NULL");
+    const int64_t T = c->T, d = c->d, F = c->ffn, E = c->E, k = c->topk, R = c->R, tbM = c->tile_M;
+    if (T <= 0 || d <= 0 || F <= 0 || E <= 0 || k <= 0 || R <= 0)
+        return fail(MOE_ERR_ARG, "T, d, ffn, E, topk, R must be positive");
+    if (d % 128) return fail(MOE_ERR_ARG, "d=%lld must be a multiple of 128", (long long)d);
+    if (F % 128) return fail(MOE_ERR_ARG, "ffn=%lld must be a multiple of 128", (long long)F);
+    if (E > MAX_E) return fail(MOE_ERR_ARG, "E=%lld exceeds %d", (long long)E, MAX_E);
+    if (k > E || k > 8) return fail(MOE_ERR_ARG, "topk=%lld must be <= min(E, 8)", (long long)k);
+    if (T % R) return fail(MOE_ERR_ARG, "R=%lld must divide T=%lld", (long long)R, (long long)T);
+    if (E * R > 1024) return fail(MOE_ERR_ARG, "E*R=%lld exceeds 1024", (long long)(E * R));
+    if (tbM != 64 && tbM != 128) return fail(MOE_ERR_ARG, "tile_M=%lld must be 64 or 128", (long long)tbM);
+    if (c->mgb < 1 || c->mgb > 4) return fail(MOE_ERR_ARG, "mgb=%d must be in [1, 4]", c->mgb);
+    for (int i = 0; i < 5; ++i)
+        if (c->reserved[i]) return fail(MOE_ERR_ARG, "reserved fields must be zero");
+
+    const int64_t TK = T * k, G = E * R;
+    const int64_t P_max = (int64_t)align_up((size_t)(TK + (G < TK ? G : TK) * (tbM - 1)), (size_t)tbM);
+    if (P_max >= (int64_t(1) << 30)) return fail(MOE_ERR_ARG, "padded rows %lld too large", (long long)P_max);
+    const int64_t MT_max = P_max / tbM;
+    int64_t C = 256;
+    while ((T / R) % C) C >>= 1;
+    const int bn2 = (d % 256 == 0) ? 256 : 128;
+    const int nN2 = (int)(d / bn2);
+    if ((int64_t)c->mgb * nN2 > GEMM_THREADS)
+        return fail(MOE_ERR_ARG, "mgb * d/%d = %lld exceeds %d", bn2, (long long)c->mgb * nN2, GEMM_THREADS);
+    int64_t rpu = UNIT_BYTES / (2 * d);
+    if (rpu < 1) rpu = 1;
+    if (rpu > tbM) rpu = tbM;
+
+    Layout o;
+    memset(&o, 0, sizeof(o));
+    moe_layout& L = o.L;
+    L.P_max = (int32_t)P_max;
+    L.MT_max = (int32_t)MT_max;
+    L.n_chunks = (int32_t)(T / C);
+    L.chunk_tokens = (int32_t)C;
+    L.n_tiles_n2 = nN2;
+    L.block_n2 = bn2;
+    L.rows_per_unit = (int32_t)rpu;
+    L.units_per_band = (int32_t)((tbM + rpu - 1) / rpu);
+
+    size_t cur = 0;
+    auto put = [&](size_t bytes) {
+        const size_t at = cur;
+        cur = align_up(cur + bytes, 1024);
+        return at;
+    };
+    L.idx = put(TK * 4);
+    L.gate = put(TK * 4);
+    L.rank = put(TK * 4);
+    L.chunk_cnt = put((size_t)L.n_chunks * E * 4);
+    L.chunk_base = put((size_t)L.n_chunks * E * 4);
+    L.counts = put(G * 4);
+    L.offsets = put((G + 1) * 4);
+    L.ret_off = put(R * (E + 1) * 4);
+    L.tiles = put(MT_max * 16);
+    L.tile_ret = put(MT_max * 4);
+    L.sched = put(MT_max * 4);
+    L.seg = put(MT_max * 8);
+    L.experts = put(E * 8);
+    L.slot = put(TK * 4);
+    L.ret_slot = put(TK * 4);
+    L.meta = put(META_COUNT * 4);
+    L.flags = put(MT_max * nN2 * 4);
+    L.trace = put(TR_COUNT * 8);
+    L.Xp = put((size_t)P_max * d * 2);
+    L.Hp = put((size_t)P_max * F * 2);
+    L.Yp = put((size_t)P_max * d * 2);
+    L.Ret = put((size_t)TK * d * 2);
+    L.in_logits = put((size_t)T * E * 4);
+    L.in_x = put((size_t)T * d * 2);
+    L.out = put((size_t)T * d * 4);
+    L.bytes = cur;
+
+    Shape& S = o.S;
+    S.T = (int)T;
+    S.d = (int)d;
+    S.ffn = (int)F;
+    S.E = (int)E;
+    S.k = (int)k;
+    S.R = (int)R;
+    S.tbM = (int)tbM;
+    S.mgb = c->mgb;
+    S.chunk_tokens = (int)C;
+    S.n_chunks = L.n_chunks;
+    S.P_max = L.P_max;
+    S.MT_max = L.MT_max;
+    S.bn2 = bn2;
+    S.n_tiles_n2 = nN2;
+    S.rows_per_unit = L.rows_per_unit;
+    S.units_per_band = L.units_per_band;
+    S.timeout_ns = (unsigned long long)(c->timeout_us ? c->timeout_us : 2000000u) * 1000ull;
+    S.flags = c->flags;
+    *out = o;
+    return MOE_OK;
+}
+
+PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    PlanPtrs p;
+    p.idx = reinterpret_cast<int32_t*>(b + L.idx);
+    p.gate = reinterpret_cast<float*>(b + L.gate);
+    p.rank = reinterpret_cast<int32_t*>(b + L.rank);
+    p.chunk_cnt = reinterpret_cast<int32_t*>(b + L.chunk_cnt);
+    p.chunk_base = reinterpret_cast<int32_t*>(b + L.chunk_base);
+    p.counts = reinterpret_cast<int32_t*>(b + L.counts);
+    p.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+    p.ret_off = reinterpret_cast<int32_t*>(b + L.ret_off);
+    p.tiles = reinterpret_cast<int32_t*>(b + L.tiles);
+    p.tile_ret = reinterpret_cast<int32_t*>(b + L.tile_ret);
+    p.sched = reinterpret_cast<int32_t*>(b + L.sched);
+    p.seg = reinterpret_cast<int32_t*>(b + L.seg);
+    p.experts = reinterpret_cast<int32_t*>(b + L.experts);
+    p.slot = reinterpret_cast<int32_t*>(b + L.slot);
+    p.ret_slot = reinterpret_cast<int32_t*>(b + L.ret_slot);
+    p.meta = reinterpret_cast<int32_t*>(b + L.meta);
+    p.flags = reinterpret_cast<uint32_t*>(b + L.flags);
+    p.trace = reinterpret_cast<unsigned long long*>(b + L.trace);
+    p.Xp = reinterpret_cast<__nv_bfloat16*>(b + L.Xp);
+    p.Hp = reinterpret_cast<__nv_bfloat16*>(b + L.Hp);
+    p.Yp = reinterpret_cast<__nv_bfloat16*>(b + L.Yp);
+    p.Ret = reinterpret_cast<__nv_bfloat16*>(b + L.Ret);
+    return p;
+}
+
+// ---- device query ------------------------------------------------------------------------------
+struct DeviceInfo {
+    int sms = 0;
+    bool supported = false;
+};
+
+int device_info(DeviceInfo* di) {
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    di->sms = sms;
+    di->supported = (major == 10 && minor == 3);
+    return MOE_OK;
+}
+
+// ---- TMA descriptors ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor [outer][mid][inner] (rank 3) or [mid][inner] (rank 2, outer = 1); box 64 x box_mid (x 1),
+// 128-byte swizzle, out-of-bounds elements read as zero.
+int make_map(CUtensorMap* m, const void* ptr, int rank, uint64_t inner, uint64_t mid, uint64_t outer,
+             uint32_t box_mid, const char* what) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[3] = {inner, mid, outer};
+    cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, box_mid, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box,
+                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+    return MOE_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Call {
+    Layout lay;
+    PlanPtrs p;
+    DeviceInfo di;
+    cudaStream_t st;
+    int consumers;
+};
+
+int begin_call(const moe_config* cfg, void* ws, size_t ws_bytes, void* stream, Call* c) {
+    g_err.clear();
+    int rc = make_layout(cfg, &c->lay);
+    if (rc) return rc;
+    if (!ws) return fail(MOE_ERR_ARG, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(MOE_ERR_ARG, "workspace must be 256-byte aligned");
+    if (ws_bytes < c->lay.L.bytes)
+        return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, c->lay.L.bytes);
+    rc = device_info(&c->di);
+    if (rc) return rc;
+    if (!c->di.supported) return fail(MOE_ERR_DEVICE, "current device is not sm_103 (GB300)");
+    c->p = plan_ptrs(c->lay.L, ws);
+    c->st = static_cast<cudaStream_t>(stream);
+    c->consumers = cfg->consumer_ctas;
+    return MOE_OK;
+}
+
+int run_plan(Call& c, const float* logits, const uint16_t* x, bool permute) {
+    cudaError_t e = launch_route(c.lay.S, logits, c.p, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "route kernel launch");
+    e = launch_plan(c.lay.S, c.p, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "plan kernel launch");
+    e = launch_permute(c.lay.S, permute ? reinterpret_cast<const __nv_bfloat16*>(x) : nullptr, c.p, c.di.sms, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "permute kernel launch");
+    return MOE_OK;
+}
+
+int record(void* const* ev, int i, cudaStream_t st) {
+    if (!ev || !ev[i]) return MOE_OK;
+    const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaEventRecord of a stage event");
+}
+
+int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
+                const uint16_t* W2, float* out, bool overlapped, void* const* ev = nullptr) {
+    const Shape& S = c.lay.S;
+    const moe_layout& L = c.lay.L;
+    if (!logits || !x || !W1 || !W3 || !W2 || !out) return fail(MOE_ERR_ARG, "NULL input or output pointer");
+    if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W3, 16) || !aligned(W2, 16) || !aligned(out, 16) ||
+        !aligned(logits, 4))
+        return fail(MOE_ERR_ARG, "x, W1, W3, W2, out must be 16-byte aligned, logits 4-byte aligned");
+    if (overlapped && (c.consumers < 1 || c.consumers > c.di.sms / 2))
+        return fail(MOE_ERR_ARG, "consumer_ctas=%d must be in [1, %d]", c.consumers, c.di.sms / 2);
+
+    CUtensorMap tXp, tHp, tW1, tW3, tW2;
+    int rc = make_map(&tXp, c.p.Xp, 2, S.d, S.P_max, 1, BM, "Xp");
+    if (!rc) rc = make_map(&tHp, c.p.Hp, 2, S.ffn, S.P_max, 1, BM, "Hp");
+    if (!rc) rc = make_map(&tW1, W1, 3, S.d, S.ffn, S.E, BN1, "W1");
+    if (!rc) rc = make_map(&tW3, W3, 3, S.d, S.ffn, S.E, BN1, "W3");
+    if (!rc) rc = make_map(&tW2, W2, 3, S.ffn, S.d, S.E, S.bn2, "W2");
+    if (rc) return rc;
+    (void)L;
+
+    if ((rc = record(ev, MOE_EV_BEGIN, c.st))) return rc;
+    rc = run_plan(c, logits, x, true);
+    if (rc) return rc;
+    if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
+    cudaError_t e = launch_gemm_swiglu(S, c.p, tXp, tW1, tW3, c.di.sms, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
+    if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
+    if (overlapped) {
+        e = launch_gemm_down(S, c.p, tHp, tW2, c.di.sms, c.consumers, true, c.st);
+        if (e != cudaSuccess) return cuda_fail(e, "overlapped down-projection launch");
+        if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
+    } else {
+        e = launch_gemm_down(S, c.p, tHp, tW2, c.di.sms, 0, false, c.st);
+        if (e != cudaSuccess) return cuda_fail(e, "down-projection launch");
+        if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
+        e = launch_copy_seq(S, c.p, c.di.sms, c.st);
+        if (e != cudaSuccess) return cuda_fail(e, "return copy launch");
+    }
+    if ((rc = record(ev, MOE_EV_COPIED, c.st))) return rc;
+    e = launch_combine(S, c.p, out, c.di.sms, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return record(ev, MOE_EV_END, c.st);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+MOE_API int moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+    g_err.clear();
+    if (!bytes) return fail(MOE_ERR_ARG, "bytes is NULL");
+    Layout lay;
+    const int rc = make_layout(cfg, &lay);
+    if (rc) return rc;
+    *bytes = lay.L.bytes;
+    return MOE_OK;
+}
+
+MOE_API int moe_workspace_layout(const moe_config* cfg, moe_layout* out) {
+    g_err.clear();
+    if (!out) return fail(MOE_ERR_ARG, "out is NULL");
+    Layout lay;
+    const int rc = make_layout(cfg, &lay);
+    if (rc) return rc;
+    *out = lay.L;
+    return MOE_OK;
+}
+
+MOE_API int moe_plan(const moe_config* cfg, const float* logits, const uint16_t* x, int32_t* topk_idx, float* topk_w,
+                     void* ws, size_t ws_bytes, void* stream) {
+    Call c;
+    int rc = begin_call(cfg, ws, ws_bytes, stream, &c);
+    if (rc) return rc;
+    const bool permute = !(cfg->flags & MOE_PLAN_SKIP_PERMUTE);
+    if (!logits) return fail(MOE_ERR_ARG, "logits is NULL");
+    if (permute && (!x || !aligned(x, 16))) return fail(MOE_ERR_ARG, "x must be non-NULL and 16-byte aligned");
+    rc = run_plan(c, logits, x, permute);
+    if (rc) return rc;
+    const size_t tk = (size_t)cfg->T * cfg->topk;
+    if (topk_idx) {
+        cudaError_t e = cudaMemcpyAsync(topk_idx, c.p.idx, tk * 4, cudaMemcpyDeviceToDevice, c.st);
+        if (e != cudaSuccess) return cuda_fail(e, "copy of topk_idx");
+    }
+    if (topk_w) {
+        cudaError_t e = cudaMemcpyAsync(topk_w, c.p.gate, tk * 4, cudaMemcpyDeviceToDevice, c.st);
+        if (e != cudaSuccess) return cuda_fail(e, "copy of topk_w");
+    }
+    return MOE_OK;
+}
+
+MOE_API int moe_forward(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
+                        const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes, void* stream) {
+    Call c;
+    const int rc = begin_call(cfg, ws, ws_bytes, stream, &c);
+    if (rc) return rc;
+    return run_forward(c, logits, x, W1, W3, W2, out, true);
+}
+
+MOE_API int moe_forward_sequential(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
+                                   const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes,
+                                   void* stream) {
+    Call c;
+    const int rc = begin_call(cfg, ws, ws_bytes, stream, &c);
+    if (rc) return rc;
+    return run_forward(c, logits, x, W1, W3, W2, out, false);
+}
+
+MOE_API int moe_forward_ex(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
+                           const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes, int sequential,
+                           void* const* stage_events, void* stream) {
+    Call c;
+    const int rc = begin_call(cfg, ws, ws_bytes, stream, &c);
+    if (rc) return rc;
+    return run_forward(c, logits, x, W1, W3, W2, out, sequential == 0, stage_events);
+}
+
+MOE_API int moe_forward_host(const moe_config* cfg, const float* logits_h, const uint16_t* x_h, const uint16_t* W1,
+                             const uint16_t* W3, const uint16_t* W2, float* out_h, void* ws, size_t ws_bytes,
+                             int sequential, void* stream) {
+    Call c;
+    int rc = begin_call(cfg, ws, ws_bytes, stream, &c);
+    if (rc) return rc;
+    if (!logits_h || !x_h || !out_h) return fail(MOE_ERR_ARG, "NULL host pointer");
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    float* d_logits = reinterpret_cast<float*>(b + c.lay.L.in_logits);
+    uint16_t* d_x = reinterpret_cast<uint16_t*>(b + c.lay.L.in_x);
+    float* d_out = reinterpret_cast<float*>(b + c.lay.L.out);
+    const size_t T = cfg->T;
+    cudaError_t e = cudaMemcpyAsync(d_logits, logits_h, T * cfg->E * 4, cudaMemcpyHostToDevice, c.st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_x, x_h, T * cfg->d * 2, cudaMemcpyHostToDevice, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of the inputs");
+    rc = run_forward(c, d_logits, d_x, W1, W3, W2, d_out, sequential == 0);
+    if (rc) return rc;
+    e = cudaMemcpyAsync(out_h, d_out, T * cfg->d * 4, cudaMemcpyDeviceToHost, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of the output");
+    return MOE_OK;
+}
+
+MOE_API int moe_status(const moe_config* cfg, const void* ws, void* stream, int32_t* detail) {
+    g_err.clear();
+    Layout lay;
+    int rc = make_layout(cfg, &lay);
+    if (rc) return rc;
+    if (!ws) return fail(MOE_ERR_ARG, "workspace is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    int32_t w[2] = {0, 0};
+    e = cudaMemcpy(w, static_cast<const uint8_t*>(ws) + lay.L.meta + META_STATUS * 4, sizeof(w),
+                   cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (detail) *detail = w[1];
+    switch (w[0]) {
+        case ST_OK: return MOE_OK;
+        case ST_FLAG_TIMEOUT: return fail(MOE_ERR_TIMEOUT, "consumer flag wait timed out (M-tile %d)", w[1]);
+        case ST_PIPE_TIMEOUT: return fail(MOE_ERR_TIMEOUT, "GEMM pipeline wait timed out (role %d)", w[1]);
+        case ST_COPY_TIMEOUT: return fail(MOE_ERR_TIMEOUT, "row-band copy timed out (M-tile %d)", w[1]);
+        case ST_BAD_PLAN: return fail(MOE_ERR_PLAN, "plan index out of bounds (%d)", w[1]);
+        default: return fail(MOE_ERR_PLAN, "unknown device status %d", w[0]);
+    }
+}
+
+MOE_API int moe_device_info(int32_t* sm_count, int32_t* supported) {
+    g_err.clear();
+    DeviceInfo di;
+    const int rc = device_info(&di);
+    if (rc) return rc;
+    if (sm_count) *sm_count = di.sms;
+    if (supported) *supported = di.supported ? 1 : 0;
+    return MOE_OK;
+}
+
+MOE_API const char* moe_last_error(void) { return g_err.c_str(); }
+
+}  // extern "C"

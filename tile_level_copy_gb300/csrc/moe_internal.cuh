@@ -1,0 +1,301 @@
+// Internal definitions shared by the kernels and the host side of libmoe.
+// Hand-written inline PTX for sm_103a: mbarrier, TMA (cp.async.bulk.tensor), bulk copies,
+// tcgen05 (TMEM allocation, UMMA, TMEM loads) and GPU-scope release/acquire.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---- meta word indices (int32 [64] in the workspace) -------------------------------------
+enum Meta : int {
+    META_P = 0,            // padded rows P of this call
+    META_MTILES = 1,       // M-tiles = P / tile_M
+    META_UNITS = 2,        // copy units = M-tiles * units_per_band
+    META_QUEUE = 3,        // next copy unit to hand out (overlapped consumer)
+    META_QUEUE_SEQ = 4,    // next copy unit to hand out (sequential copy)
+    META_STATUS = 5,       // 0 or a Status code (first error wins)
+    META_STATUS_DETAIL = 6,
+    META_COUNT = 64,
+};
+
+enum Status : int {
+    ST_OK = 0,
+    ST_FLAG_TIMEOUT = 1,   // consumer gave up waiting on a tile flag
+    ST_PIPE_TIMEOUT = 2,   // an mbarrier wait of the GEMM pipeline gave up
+    ST_COPY_TIMEOUT = 3,   // a bulk copy did not complete in time
+    ST_BAD_PLAN = 4,       // a plan index failed its bounds check
+};
+
+// Trace slots (uint64) beyond the public ones.
+enum Trace : int { TR_COUNT = 16 };
+
+// ---- GEMM geometry --------------------------------------------------------------------------
+constexpr int BM = 128;            // UMMA M (rows of one MMA tile)
+constexpr int BK = 64;             // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;             // 16 KB
+constexpr int B_STAGE_BYTES = 256 * BK * 2;            // 32 KB (up to N = 256)
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int GEMM_THREADS = 192;                      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int MISC_BYTES = 4096;
+constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + MISC_BYTES + 1024;  // + alignment slack
+constexpr int TMEM_COLS = 512;                         // two 256-column fp32 accumulators
+constexpr int BN1 = 128;                               // output columns of a SwiGLU tile
+constexpr uint32_t FLAG_READY = 4;                     // one release-add per epilogue warp
+constexpr int MAX_E = 256;
+
+// bulk copy ring of the consumer (reuses the stage area)
+constexpr int COPY_PIECE = 32768;
+constexpr int COPY_NBUF = (STAGES * STAGE_BYTES) / COPY_PIECE;   // 6
+constexpr int UNIT_BYTES = 131072;                     // target bytes of one copy unit
+
+// ---- parameters passed by value to kernels --------------------------------------------------
+struct PlanPtrs {
+    int32_t* idx;
+    float* gate;
+    int32_t* rank;
+    int32_t* chunk_cnt;
+    int32_t* chunk_base;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* ret_off;
+    int32_t* tiles;      // [MT_max][4]
+    int32_t* tile_ret;
+    int32_t* sched;
+    int32_t* seg;        // [MT_max][2]
+    int32_t* experts;    // [E][2]
+    int32_t* slot;
+    int32_t* ret_slot;
+    int32_t* meta;
+    uint32_t* flags;
+    unsigned long long* trace;
+    __nv_bfloat16* Xp;
+    __nv_bfloat16* Hp;
+    __nv_bfloat16* Yp;
+    __nv_bfloat16* Ret;
+};
+
+struct Shape {
+    int T, d, ffn, E, k, R, tbM;
+    int mgb;
+    int chunk_tokens, n_chunks;
+    int P_max, MT_max;
+    int bn2, n_tiles_n2;            // down-projection N tile and N tiles per band
+    int rows_per_unit, units_per_band;
+    unsigned long long timeout_ns;
+    uint32_t flags;
+};
+
+// ---- host-side launchers (defined in the .cu files) ------------------------------------------
+cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p, cudaStream_t st);
+cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st);
+cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtrs& p, int sms, cudaStream_t st);
+cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW1,
+                               const CUtensorMap& tmW3, int sms, cudaStream_t st);
+cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2,
+                             int sms, int consumers, bool overlapped, cudaStream_t st);
+cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
+cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
+
+// ============================================================================================
+// Device primitives
+// ============================================================================================
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Record the first error of a call in the status word.
+__device__ __forceinline__ void set_status(int32_t* meta, int code, int detail) {
+    if (atomicCAS(&meta[META_STATUS], 0, code) == 0) atomicExch(&meta[META_STATUS_DETAIL], detail);
+}
+
+// ---- mbarrier ------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity to complete. Gives up (returns
+// false) after timeout_ns of %globaltimer or when another role has raised *abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns,
+                                          volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > timeout_ns) return false;
+        }
+    }
+}
+
+// ---- TMA -----------------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---- untiled bulk copies (global <-> shared) --------------------------------------------------
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(src_gmem)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst_gmem, const void* src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst_gmem)),
+                 "r"(smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Make generic-proxy global writes observed by this thread visible to its later async-proxy reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---- GPU-scope release / acquire -----------------------------------------------------------------
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// ---- tcgen05 ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, one thread issues.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Instruction descriptor of kind::f16: D f32, A and B bf16, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+    return (1u << 4)                              // D format: f32
+           | (1u << 7)                            // A format: bf16
+           | (1u << 10)                           // B format: bf16
+           | (uint32_t(N >> 3) << 17)             // N / 8
+           | (uint32_t(M >> 4) << 24);            // M / 16
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes, groups of
+// 8 rows 1024 bytes apart (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B and a 64-element
+// bf16 inner box). Tile bases are 1024-byte aligned, so the base-offset field is 0.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= uint64_t((smem_addr & 0x3FFFF) >> 4);    // start address / 16
+    d |= uint64_t(1) << 16;                       // leading byte offset (unused by swizzled K-major)
+    d |= uint64_t(1024 >> 4) << 32;               // stride byte offset: 8 rows * 128 B
+    d |= uint64_t(1) << 46;                       // descriptor version of tcgen05
+    d |= uint64_t(2) << 61;                       // layout: SWIZZLE_128B
+    return d;
+}
+
+// 32 lanes x 32 columns of 32-bit TMEM data into 32 registers per thread, then wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace moe

@@ -1,0 +1,382 @@
+// Router top-k, per-chunk ranking, the layout plan (histogram, padded offsets, tile-owner map,
+// remote-first schedule, segments, return plan) and the permute into the owner-aligned layout.
+//
+// Method: "Fine-grained Computation-Communication Overlap via Tile-level Signaling and Scheduling
+// for Mixture-of-Experts" (pith.science/paper/W2ZARMHG), section "What carries the argument": rows
+// of each expert are grouped by owner and every group is padded to a multiple of the tile height so
+// that each output tile has one owner; tiles bound for owners are scheduled largest first.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+constexpr int ROUTE_THREADS = 256;   // 8 warps; one CTA ranks one chunk of <= 256 tokens
+constexpr int KMAX = 8;
+
+// ---------------------------------------------------------------------------------------------
+// route_kernel: one CTA per chunk of `chunk_tokens` consecutive tokens (a chunk never straddles
+// two owners). Phase 1, one warp per token: top-k of the token's E logits, descending, ties to the
+// lower expert id; gates = softmax over the k chosen logits in fp32. Phase 2: for every expert, the
+// rank of each token among the chunk's tokens routed to it (ascending token order) by warp ballots,
+// and the chunk's count per expert.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const float* __restrict__ logits, PlanPtrs p) {
+    __shared__ int32_t s_idx[256][KMAX];
+    __shared__ uint32_t s_mask[ROUTE_THREADS / 32][MAX_E];
+    __shared__ int32_t s_wpre[ROUTE_THREADS / 32][MAX_E];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = s.chunk_tokens, E = s.E, k = s.k;
+    const int t0 = blockIdx.x * C;
+
+    for (int tl = warp; tl < C; tl += ROUTE_THREADS / 32) {
+        const int t = t0 + tl;
+        const float* row = logits + (size_t)t * E;
+        float v[MAX_E / 32];
+        bool taken[MAX_E / 32];
+#pragma unroll
+        for (int i = 0; i < MAX_E / 32; ++i) {
+            const int e = lane + 32 * i;
+            v[i] = (e < E) ? row[e] : -INFINITY;
+            taken[i] = (e >= E);
+        }
+        float sel_v[KMAX];
+        int sel_e[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (j >= k) break;
+            float bv = -INFINITY;
+            int be = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < MAX_E / 32; ++i) {
+                const int e = lane + 32 * i;
+                if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) {
+                    bv = v[i];
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            sel_v[j] = bv;
+            sel_e[j] = be;
+#pragma unroll
+            for (int i = 0; i < MAX_E / 32; ++i)
+                if (lane + 32 * i == be) taken[i] = true;
+        }
+        // gates: softmax over the chosen logits (sel_v[0] is the maximum)
+        float z[KMAX], sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (j >= k) break;
+            z[j] = expf(sel_v[j] - sel_v[0]);
+            sum += z[j];
+        }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (j >= k) break;
+            if (lane == j) {
+                p.idx[(size_t)t * k + j] = sel_e[j];
+                p.gate[(size_t)t * k + j] = z[j] / sum;
+                s_idx[tl][j] = sel_e[j];
+            }
+        }
+    }
+    __syncthreads();
+
+    // phase 2: ballots per expert over the chunk's tokens (thread tl <-> token t0 + tl)
+    const int tl = threadIdx.x;
+    const bool live = tl < C;
+    for (int e = 0; e < E; ++e) {
+        bool has = false;
+        if (live) {
+            for (int j = 0; j < k; ++j) has |= (s_idx[tl][j] == e);
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, has);
+        if (lane == 0) s_mask[warp][e] = m;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += ROUTE_THREADS) {
+        int acc = 0;
+        for (int w = 0; w < ROUTE_THREADS / 32; ++w) {
+            s_wpre[w][e] = acc;
+            acc += __popc(s_mask[w][e]);
+        }
+        p.chunk_cnt[(size_t)blockIdx.x * E + e] = acc;
+    }
+    __syncthreads();
+    if (live) {
+        const uint32_t lt = (1u << lane) - 1u;
+        const int t = t0 + tl;
+        for (int j = 0; j < k; ++j) {
+            const int e = s_idx[tl][j];
+            p.rank[(size_t)t * k + j] = s_wpre[warp][e] + __popc(s_mask[warp][e] & lt);
+        }
+    }
+}
+
+cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p, cudaStream_t st) {
+    route_kernel<<<s.n_chunks, ROUTE_THREADS, 0, st>>>(s, logits, p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// plan_kernel: one CTA of 1024 threads builds the whole plan from the per-chunk counts.
+// ---------------------------------------------------------------------------------------------
+constexpr int PLAN_THREADS = 1024;
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* s_total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < PLAN_THREADS / 32) ? s_warp[lane] : 0;
+        int wx = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wx, o);
+            if (lane >= o) wx += y;
+        }
+        s_warp[lane] = wx - w;
+        if (lane == 31) *s_total = wx;
+    }
+    __syncthreads();
+    const int r = s_warp[warp] + x - v;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p) {
+    __shared__ int s_n[1024];        // n_{e,r}, group g = e*R + r
+    __shared__ int s_off[1025];
+    __shared__ int s_load[MAX_E];    // rows per expert
+    __shared__ int s_erank[MAX_E];   // position of the expert in (load desc, id asc) order
+    __shared__ int s_fb[MAX_E];      // full bands per expert
+    __shared__ int s_fbase[MAX_E];   // first schedule position of the expert's full bands
+    __shared__ int s_warp[32];
+    __shared__ int s_total, s_full_total;
+
+    const int E = s.E, R = s.R, G = E * R, tbM = s.tbM, tid = threadIdx.x;
+    const int cpo = (s.T / R) / s.chunk_tokens;  // chunks per owner
+    const int slice = (s.T / R) * s.k;           // rows per owner slice of Ret
+
+    // 1. per group: chunk bases (exclusive prefix over the owner's chunks) and n_{e,r}
+    for (int g = tid; g < G; g += PLAN_THREADS) {
+        const int e = g / R, r = g % R;
+        int acc = 0;
+        for (int c = r * cpo; c < (r + 1) * cpo; ++c) {
+            p.chunk_base[(size_t)c * E + e] = acc;
+            acc += p.chunk_cnt[(size_t)c * E + e];
+        }
+        s_n[g] = acc;
+        p.counts[g] = acc;
+    }
+    __syncthreads();
+
+    // 2. padded offsets: exclusive scan of ceil(n / tbM) * tbM over g (e-major, r-minor)
+    {
+        const int g = tid;
+        const int padded = (g < G) ? ((s_n[g] + tbM - 1) / tbM) * tbM : 0;
+        const int o = block_exclusive_scan(padded, s_warp, &s_total);
+        if (g < G) s_off[g] = o;
+        if (g == 0) s_off[G] = s_total;
+    }
+    __syncthreads();
+    const int P = s_off[G];
+    const int MT = P / tbM;
+    for (int g = tid; g <= G; g += PLAN_THREADS) p.offsets[g] = s_off[g];
+
+    // 3. owner return offsets: ret_off[r][e] = sum_{e' < e} n_{e',r}
+    for (int r = tid; r < R; r += PLAN_THREADS) {
+        int acc = 0;
+        for (int e = 0; e < E; ++e) {
+            p.ret_off[r * (E + 1) + e] = acc;
+            acc += s_n[e * R + r];
+        }
+        p.ret_off[r * (E + 1) + E] = acc;
+    }
+
+    // 4. expert loads, full bands, expert table
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        int load = 0, fb = 0;
+        for (int r = 0; r < R; ++r) {
+            load += s_n[e * R + r];
+            fb += s_n[e * R + r] / tbM;
+        }
+        s_load[e] = load;
+        s_fb[e] = fb;
+        p.experts[2 * e + 0] = s_off[e * R] / tbM;
+        p.experts[2 * e + 1] = (s_off[(e + 1) * R] - s_off[e * R]) / tbM;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        int rk = 0;
+        for (int f = 0; f < E; ++f)
+            rk += (s_load[f] > s_load[e]) || (s_load[f] == s_load[e] && f < e);
+        s_erank[e] = rk;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        int base = 0;
+        for (int f = 0; f < E; ++f)
+            if (s_erank[f] < s_erank[e]) base += s_fb[f];
+        s_fbase[e] = base;
+    }
+    if (tid == 0) {
+        int tot = 0;
+        for (int e = 0; e < E; ++e) tot += s_fb[e];
+        s_full_total = tot;
+    }
+    __syncthreads();
+
+    // 5. tiles, destination rows, and schedule positions.
+    // Schedule key (-valid, expert rank, owner, row): full bands first, expert by expert in rank
+    // order, each expert's full bands in layout order; then the partial bands by valid rows desc.
+    for (int g = tid; g < G; g += PLAN_THREADS) {
+        const int e = g / R, r = g % R, n = s_n[g];
+        const int m0 = s_off[g] / tbM;
+        const int nt = (n + tbM - 1) / tbM, nfull = n / tbM;
+        int fpre = 0;
+        for (int q = 0; q < r; ++q) fpre += s_n[e * R + q] / tbM;
+        const int rbase = r * slice + p.ret_off[r * (E + 1) + e];
+        for (int i = 0; i < nt; ++i) {
+            const int m = m0 + i;
+            const int valid = min(tbM, n - i * tbM);
+            p.tiles[4 * m + 0] = e;
+            p.tiles[4 * m + 1] = r;
+            p.tiles[4 * m + 2] = s_off[g] + i * tbM;
+            p.tiles[4 * m + 3] = valid;
+            p.tile_ret[m] = rbase + i * tbM;
+            if (i < nfull) p.sched[s_fbase[e] + fpre + i] = m;
+        }
+        if (nt > nfull) {  // one partial band
+            const int valid = n - nfull * tbM;
+            int pos = 0;
+            for (int h = 0; h < G; ++h) {
+                const int nh = s_n[h];
+                const int vh = nh % tbM;
+                if (vh == 0 || h == g) continue;
+                const int eh = h / R, rh = h % R;
+                const bool before = (vh > valid) || (vh == valid && (s_erank[eh] < s_erank[e] ||
+                                                                      (s_erank[eh] == s_erank[e] && rh < r)));
+                pos += before;
+            }
+            p.sched[s_full_total + pos] = m0 + nfull;
+        }
+    }
+    __syncthreads();
+    __threadfence_block();
+
+    // 6. segments: runs of adjacent bands of one group, cut into pieces of mgb bands
+    for (int q = tid; q < MT; q += PLAN_THREADS) {
+        auto adjacent = [&](int a, int b) {
+            const int ma = p.sched[a], mb = p.sched[b];
+            return p.tiles[4 * ma] == p.tiles[4 * mb] && p.tiles[4 * ma + 1] == p.tiles[4 * mb + 1] &&
+                   p.tiles[4 * mb + 2] == p.tiles[4 * ma + 2] + tbM;
+        };
+        int start = q;
+        while (start > 0 && adjacent(start - 1, start)) --start;
+        int end = q + 1;
+        while (end < MT && adjacent(end - 1, end)) ++end;
+        const int first = start + ((q - start) / s.mgb) * s.mgb;
+        p.seg[2 * q + 0] = first;
+        p.seg[2 * q + 1] = min(s.mgb, end - first);
+    }
+
+    // 7. per-call meta, flags and trace reset
+    if (tid == 0) {
+        p.meta[META_P] = P;
+        p.meta[META_MTILES] = MT;
+        p.meta[META_UNITS] = MT * s.units_per_band;
+        p.meta[META_QUEUE] = 0;
+        p.meta[META_QUEUE_SEQ] = 0;
+        p.meta[META_STATUS] = (P > s.P_max) ? ST_BAD_PLAN : 0;
+        p.meta[META_STATUS_DETAIL] = (P > s.P_max) ? P : 0;
+    }
+    if (tid < TR_COUNT) p.trace[tid] = (tid == MOE_TRACE_GEMM2_START || tid == MOE_TRACE_COPY_START) ? ~0ull : 0ull;
+    const int nflags = min(MT, s.MT_max) * s.n_tiles_n2;
+    for (int i = tid; i < nflags; i += PLAN_THREADS) p.flags[i] = 0u;
+}
+
+cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
+    plan_kernel<<<1, PLAN_THREADS, 0, st>>>(s, p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// permute_kernel: one warp per work item. Items [0, T): token t computes its k slots and return
+// slots and copies x[t] into the k rows of Xp with 16-byte vectors. Items [T, T + M-tiles): the
+// padding rows of that M-tile are zeroed. With x == nullptr only the slots are written.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat16* __restrict__ x, PlanPtrs p) {
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int MT = p.meta[META_MTILES];
+    const int per = s.T / s.R, slice = per * s.k, E = s.E, R = s.R, k = s.k;
+    const int vec = s.d / 8;  // 16-byte vectors per row
+    const uint4* xs = reinterpret_cast<const uint4*>(x);
+    uint4* xp = reinterpret_cast<uint4*>(p.Xp);
+    const bool ok_mt = MT <= s.MT_max;
+
+    const int pad_items = (ok_mt && xs != nullptr) ? MT : 0;
+    for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < s.T + pad_items; item += nwarps) {
+        if (item < s.T) {
+            const int t = item, r = t / per, c = t / s.chunk_tokens;
+            int my_slot = 0;
+            if (lane < k) {
+                const int e = p.idx[(size_t)t * k + lane];
+                const int rk = p.chunk_base[(size_t)c * E + e] + p.rank[(size_t)t * k + lane];
+                my_slot = p.offsets[e * R + r] + rk;
+                p.slot[(size_t)t * k + lane] = my_slot;
+                p.ret_slot[(size_t)t * k + lane] = r * slice + p.ret_off[r * (E + 1) + e] + rk;
+            }
+            int sl[KMAX];
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j) sl[j] = __shfl_sync(0xffffffffu, my_slot, j);
+            bool good = true;
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (j < k) good &= (sl[j] >= 0 && sl[j] < s.P_max);
+            if (!good) {
+                if (lane == 0) set_status(p.meta, ST_BAD_PLAN, t);
+                continue;
+            }
+            if (xs == nullptr) continue;  // plan only: slots without the row copy
+            for (int v = lane; v < vec; v += 32) {
+                const uint4 val = __ldg(xs + (size_t)t * vec + v);
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j)
+                    if (j < k) xp[(size_t)sl[j] * vec + v] = val;
+            }
+        } else {
+            const int m = item - s.T;
+            const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int rr = valid; rr < s.tbM; ++rr) {
+                const size_t row = (size_t)row0 + rr;
+                if (row >= (size_t)s.P_max) break;
+                for (int v = lane; v < vec; v += 32) xp[row * vec + v] = z;
+            }
+        }
+    }
+}
+
+cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtrs& p, int sms, cudaStream_t st) {
+    const int items = s.T + s.MT_max;
+    const int blocks = min((items + 7) / 8, sms * 8);
+    permute_kernel<<<blocks, 256, 0, st>>>(s, x, p);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
