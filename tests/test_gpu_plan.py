@@ -28,7 +28,7 @@ def run_plan(w: inputs.Workload, logits_np: np.ndarray, x_cpu, mgb=1, skip_permu
 
 
 def check_plan(w, logits_np, x_cpu, mgb=1):
-    cfg, ws, idx, gate = run_plan(w, logits_np, x_cpu, mgb)
+    cfg, ws, idx, gate = run_plan(w, logits_np, x_cpu, mgb, skip_permute=x_cpu is None)
     ridx, rgate = moe_ref.route_topk(logits_np, w.topk)
     np.testing.assert_array_equal(idx, ridx)
     np.testing.assert_allclose(gate, rgate, rtol=2e-6, atol=1e-7)
