@@ -218,6 +218,29 @@ MOE_API int moe_status(const moe_config* cfg, const void* ws, void* stream, int3
 /* Number of SMs of the current device and whether it is supported (sm_103); host query only. */
 MOE_API int moe_device_info(int32_t* sm_count, int32_t* supported);
 
+/*
+ * moe_route_static: routing and the row layout for callers that cannot allocate device memory and so
+ * cannot provide moe_plan's workspace: code running inside a custom allocator's callback, a plugin
+ * whose host application owns all device memory and hands none out, or a serving runtime whose
+ * memory pool is fixed at start-up and may not grow while requests are in flight.
+ * The paper has no counterpart of this entry point; it is a deployment convenience.
+ *   logits   device f32 [T, E]  (input, as in moe_plan)
+ *   topk_idx device int32 [T, topk], topk_w device f32 [T, topk]: the routing (as moe_plan's)
+ *   slot, ret_slot device int32 [T, topk]: row of pair (t, j) in the padded layout / the return
+ *            buffer; offsets device int32 [E*R + 1]: first padded row of each (expert, owner) group
+ *            and the padded total P (all as in the workspace written by moe_plan)
+ * It allocates nothing: its internal scratch (ranks, per-chunk counts, tile map, schedule, status)
+ * is a file-scope device array of MOE_STATIC_SCRATCH_BYTES that every GPU which loads the library
+ * holds until the process exits. A config whose scratch would exceed that size returns MOE_ERR_ARG
+ * with the needed size in moe_last_error(). The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream capture. All calls share
+ * the one array and each call overwrites what it reads: calls that can overlap on the GPU (two
+ * streams, or two host threads) race and must be serialised by the caller.
+ */
+#define MOE_STATIC_SCRATCH_BYTES (4 << 20)
+MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t* topk_idx, float* topk_w,
+                             int32_t* slot, int32_t* ret_slot, int32_t* offsets, void* stream);
+
 /* Message of the last error on the calling thread ("" if none). The pointer stays valid until
  * the thread's next call into the library. */
 MOE_API const char* moe_last_error(void);

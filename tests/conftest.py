@@ -28,3 +28,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    """Build libmoe once per session (a no-op when the sources did not change)."""
+    from tile_level_copy_gb300 import build
+    build.build()
+    import tile_level_copy_gb300 as tlc
+    return tlc.lib()

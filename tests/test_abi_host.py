@@ -7,16 +7,9 @@ import re
 import pytest
 
 import tile_level_copy_gb300 as tlc
-from tile_level_copy_gb300 import build as tlc_build
 from tile_level_copy_gb300 import inputs
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-
-
-@pytest.fixture(scope="session", autouse=True)
-def built_library():
-    tlc_build.build()
-    return tlc.lib()
 
 
 def declared_symbols():

@@ -32,7 +32,8 @@ TRACE_GEMM2_START, TRACE_GEMM2_END, TRACE_COPY_START, TRACE_COPY_END = 0, 1, 2, 
 
 # names of the C entry points (each declared in include/moe.h)
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_plan", "moe_forward", "moe_forward_sequential",
-           "moe_forward_ex", "moe_forward_host", "moe_status", "moe_device_info", "moe_last_error")
+           "moe_forward_ex", "moe_forward_host", "moe_status", "moe_device_info", "moe_route_static",
+           "moe_last_error")
 
 # stage events of moe_forward_ex
 EV_BEGIN, EV_PLANNED, EV_UP, EV_DOWN, EV_COPIED, EV_END, EV_COUNT = range(7)
@@ -109,6 +110,7 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_host.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, ctypes.c_int, vp]
         L.moe_status.argtypes = [cfgp, vp, vp, i32p]
         L.moe_device_info.argtypes = [i32p, i32p]
+        L.moe_route_static.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp]
         L.moe_last_error.restype = ctypes.c_char_p
         for n in EXPORTS[:-1]:
             getattr(L, n).restype = ctypes.c_int
@@ -247,6 +249,17 @@ def status(cfg: Config, ws: Workspace, stream=None):
     detail = ctypes.c_int32()
     rc = lib().moe_status(ctypes.byref(c), ws.ptr, _stream(stream), ctypes.byref(detail))
     return rc, detail.value
+
+
+def route_static(cfg: Config, logits: torch.Tensor, topk_idx: torch.Tensor, topk_w: torch.Tensor,
+                 slot: torch.Tensor, ret_slot: torch.Tensor, offsets: torch.Tensor, stream=None) -> None:
+    """moe_route_static: routing and row layout with the library's own static scratch (no workspace)."""
+    c = cfg.to_c()
+    i32 = torch.int32
+    _check(lib().moe_route_static(ctypes.byref(c), _ptr(logits, torch.float32, "cuda", "logits"),
+                                  _ptr(topk_idx, i32, "cuda", "topk_idx"), _ptr(topk_w, torch.float32, "cuda", "topk_w"),
+                                  _ptr(slot, i32, "cuda", "slot"), _ptr(ret_slot, i32, "cuda", "ret_slot"),
+                                  _ptr(offsets, i32, "cuda", "offsets"), _stream(stream)))
 
 
 def device_info():

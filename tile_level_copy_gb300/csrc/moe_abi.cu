@@ -306,6 +306,39 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
 }  // namespace
 }  // namespace moe
 
+// ---- static-scratch routing plan ------------------------------------------------------------------
+// Scratch of moe_route_static: one file-scope array per GPU that loads the library, kept until the
+// process exits. Host code must not pass `g_static_scratch` itself to a kernel (on the host the name
+// is only a stand-in); each device's address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES];
+
+namespace moe {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device (set up on the first call per device).
+int static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_DEVICE, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
+        g_static_addr[dev] = p;
+    }
+    *out = g_static_addr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -431,6 +464,65 @@ MOE_API int moe_device_info(int32_t* sm_count, int32_t* supported) {
     if (rc) return rc;
     if (sm_count) *sm_count = di.sms;
     if (supported) *supported = di.supported ? 1 : 0;
+    return MOE_OK;
+}
+
+MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t* topk_idx, float* topk_w,
+                             int32_t* slot, int32_t* ret_slot, int32_t* offsets, void* stream) {
+    g_err.clear();
+    Layout lay;
+    int rc = make_layout(cfg, &lay);
+    if (rc) return rc;
+    if (!logits || !topk_idx || !topk_w || !slot || !ret_slot || !offsets)
+        return fail(MOE_ERR_ARG, "NULL input or output pointer");
+    const moe_layout& L = lay.L;
+    const Shape& S = lay.S;
+    // scratch regions, packed in the static array
+    size_t cur = 0;
+    auto put = [&](size_t bytes) {
+        const size_t at = cur;
+        cur = align_up(cur + bytes, 256);
+        return at;
+    };
+    const size_t TK = (size_t)S.T * S.k, E = S.E, R = S.R, MT = L.MT_max;
+    const size_t o_rank = put(TK * 4), o_cnt = put((size_t)L.n_chunks * E * 4),
+                 o_base = put((size_t)L.n_chunks * E * 4), o_counts = put(E * R * 4), o_ret = put(R * (E + 1) * 4),
+                 o_tiles = put(MT * 16), o_tret = put(MT * 4), o_sched = put(MT * 4), o_seg = put(MT * 8),
+                 o_exp = put(E * 8), o_meta = put(META_COUNT * 4), o_flags = put(MT * (size_t)L.n_tiles_n2 * 4),
+                 o_trace = put(TR_COUNT * 8);
+    if (cur > (size_t)MOE_STATIC_SCRATCH_BYTES)
+        return fail(MOE_ERR_ARG, "this config needs %zu bytes of static scratch; the limit is %d", cur,
+                    MOE_STATIC_SCRATCH_BYTES);
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    if (!di.supported) return fail(MOE_ERR_DEVICE, "current device is not sm_103 (GB300)");
+    void* base = nullptr;
+    if ((rc = static_scratch(&base))) return rc;
+    uint8_t* b = static_cast<uint8_t*>(base);
+    PlanPtrs p{};
+    p.idx = topk_idx;
+    p.gate = topk_w;
+    p.rank = reinterpret_cast<int32_t*>(b + o_rank);
+    p.chunk_cnt = reinterpret_cast<int32_t*>(b + o_cnt);
+    p.chunk_base = reinterpret_cast<int32_t*>(b + o_base);
+    p.counts = reinterpret_cast<int32_t*>(b + o_counts);
+    p.offsets = offsets;
+    p.ret_off = reinterpret_cast<int32_t*>(b + o_ret);
+    p.tiles = reinterpret_cast<int32_t*>(b + o_tiles);
+    p.tile_ret = reinterpret_cast<int32_t*>(b + o_tret);
+    p.sched = reinterpret_cast<int32_t*>(b + o_sched);
+    p.seg = reinterpret_cast<int32_t*>(b + o_seg);
+    p.experts = reinterpret_cast<int32_t*>(b + o_exp);
+    p.slot = slot;
+    p.ret_slot = ret_slot;
+    p.meta = reinterpret_cast<int32_t*>(b + o_meta);
+    p.flags = reinterpret_cast<uint32_t*>(b + o_flags);
+    p.trace = reinterpret_cast<unsigned long long*>(b + o_trace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_route(S, logits, p, st);
+    if (e == cudaSuccess) e = launch_plan(S, p, st);
+    if (e == cudaSuccess) e = launch_permute(S, nullptr, p, di.sms, st);
+    if (e != cudaSuccess) return cuda_fail(e, "static-scratch plan launch");
     return MOE_OK;
 }
 
