@@ -35,7 +35,7 @@ Readings where the page is silent (each listed in the design notes):
     silu(a) = a / (1 + exp(-a));
   * rows inside a group: ascending token id; padding rows of Xp are zero;
   * owner return buffer: packed rows, experts ascending, then group order;
-  * schedule: bands sorted by (-valid rows, -expert load, expert, owner, row);
+  * schedule: bands sorted by (-expert load, expert, -valid rows, owner, row);
   * segment: up to mgb consecutive schedule positions holding adjacent bands of one
     group, counted from the start of each such run.
 
@@ -189,17 +189,18 @@ def build_plan(idx: np.ndarray, E: int, R: int, tbM: int, mgb: int = 1) -> Plan:
 def remote_first_schedule(tiles: np.ndarray, n: np.ndarray) -> np.ndarray:
     """Order of M-tiles for the producer: largest owner-bound transfers first.
 
-    [TLS "What carries the argument"] and [TLS "Core claim"]: remote-bound tiles are
-    scheduled first and the largest transfers are emitted earliest. Reading: every
-    group is owner-bound on one GPU, so bands are sorted by their transfer size
-    (valid rows) descending; ties go to the more loaded expert (then lower id), then
-    the lower owner, then the lower row.
+    [TLS "What carries the argument"] and [TLS "Core claim"]: one producer covers all
+    experts, schedules remote-bound tiles first and emits the largest transfers
+    earliest. Reading: every group is owner-bound on one GPU; the producer takes the
+    experts one after another, the most loaded first (ties to the lower id), and inside
+    an expert the bands with the most valid rows first (ties to the lower owner, then
+    the lower row). Key: (-expert load, expert, -valid, owner, row).
     """
     if tiles.shape[0] == 0:
         return np.zeros(0, dtype=np.int64)
     e, r, row0, valid = tiles[:, 0], tiles[:, 1], tiles[:, 2], tiles[:, 3]
     load = n.sum(axis=1)[e]
-    return np.lexsort((row0, r, e, -load, -valid)).astype(np.int64)
+    return np.lexsort((row0, r, -valid, e, -load)).astype(np.int64)
 
 
 def segments(tiles: np.ndarray, sched: np.ndarray, tbM: int, mgb: int) -> np.ndarray:

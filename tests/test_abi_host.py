@@ -44,7 +44,7 @@ def test_layout_regions_are_aligned_and_disjoint(name):
     TK, G = w.T * w.topk, w.E * w.R
     assert L["P_max"] == -(-(TK + min(G, TK) * (w.tile_M - 1)) // w.tile_M) * w.tile_M
     assert L["MT_max"] * w.tile_M == L["P_max"]
-    assert (w.T // w.R) % L["chunk_tokens"] == 0 and L["chunk_tokens"] <= 256
+    assert (w.T // w.R) % L["chunk_tokens"] == 0 and L["chunk_tokens"] <= 128
     offs = sorted(L[r] for r in tlc.LAYOUT_REGIONS)
     assert all(o % 1024 == 0 for o in offs)
     assert len(set(offs)) == len(offs) and offs[-1] < L["bytes"]

@@ -11,7 +11,8 @@ Routing (descending logit, ties to the lower id):
 Groups (pairs (t, j), ascending t): e0r0 (0,0)(2,0); e0r1 (4,0)(6,0)(7,1); e1r0 (1,0)(2,1)(3,1);
   e1r1 (4,1)(5,0)(6,1); e2r0 (0,1)(1,1)(3,0); e2r1 (5,1)(7,0).
 Padded sizes 2,4,4,4,4,2 -> offsets 0,2,6,10,14,18,20.
-Expert loads 5, 6, 5 -> expert order e1, e0, e2; full bands first, then partial bands.
+Expert loads 5, 6, 5 -> expert order e1, e0, e2; inside each expert full bands first (in layout
+order), then partial bands by valid rows (ties to the lower owner).
 """
 import math
 
@@ -42,8 +43,10 @@ def test_hand_example_layout():
     assert p.ret_off.tolist() == [[0, 2, 5, 8], [0, 3, 6, 8]]
     assert p.ret_slot.tolist() == [[0, 5], [2, 6], [1, 3], [7, 4], [8, 11], [12, 14], [9, 13], [15, 10]]
     assert p.ret_row0.tolist() == [0, 8, 10, 2, 4, 11, 13, 5, 7, 14]
-    assert p.sched.tolist() == [3, 5, 0, 1, 7, 9, 4, 6, 2, 8]
-    assert p.seg.tolist() == [[q, 1] for q in range(10)]  # no two adjacent bands of one group
+    # e1: full m3, m5, partial m4, m6; e0: full m0, m1, partial m2; e2: full m7, m9, partial m8
+    assert p.sched.tolist() == [3, 5, 4, 6, 0, 1, 2, 7, 9, 8]
+    # m1 (rows 2-3) and m2 (row 4) are adjacent bands of group e0r1 -> one segment of 2 bands
+    assert p.seg.tolist() == [[0, 1], [1, 1], [2, 1], [3, 1], [4, 1], [5, 2], [5, 2], [7, 1], [8, 1], [9, 1]]
 
 
 def test_hand_example_segments():

@@ -132,7 +132,7 @@ def test_skew_has_empty_groups_and_invariants_hold():
 
 def brute_schedule(plan):
     load = plan.n.sum(1)
-    keys = [(-t[3], -load[t[0]], t[0], t[1], t[2]) for t in plan.tiles.tolist()]
+    keys = [(-load[t[0]], t[0], -t[3], t[1], t[2]) for t in plan.tiles.tolist()]
     return sorted(range(len(keys)), key=lambda m: keys[m])
 
 
@@ -167,9 +167,14 @@ def test_schedule_and_segments_bruteforce(mgb, seed):
     plan = ref.build_plan(idx.astype(np.int32), E, R, tbM, mgb)
     assert plan.sched.tolist() == brute_schedule(plan)
     assert [tuple(v) for v in plan.seg.tolist()] == brute_segments(plan, mgb)
-    # full bands come before partial bands; segments never span groups
-    valid = plan.tiles[plan.sched, 3]
-    assert np.all(np.diff(valid) <= 0)
+    # experts one after another, most loaded first; inside an expert full bands before
+    # partial ones; segments never span groups
+    e = plan.tiles[plan.sched, 0]
+    assert all(len(set(e[i:].tolist()) & set(e[:i].tolist())) == 0 for i in range(1, len(e)) if e[i] != e[i - 1])
+    load = plan.n.sum(1)[e]
+    assert np.all(np.diff(load) <= 0)
+    for x in np.unique(e):
+        assert np.all(np.diff(plan.tiles[plan.sched[e == x], 3]) <= 0)
     for p, (first, ln) in enumerate(plan.seg.tolist()):
         assert first <= p < first + ln <= len(plan.sched) and 1 <= ln <= mgb
         grp = {tuple(plan.tiles[plan.sched[q], :2]) for q in range(first, first + ln)}

@@ -3,16 +3,18 @@
 //   warp 0      one thread issues the TMA loads of A (token rows) and B (expert weights)
 //   warp 1      allocates 512 TMEM columns; one thread issues the UMMAs (two accumulators, so the
 //               epilogue of tile i overlaps the main loop of tile i+1)
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, conversion, stores to global memory
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, conversion, staging in shared memory and
+//               TMA tensor stores of 32 x 32 chunks to global memory
 //
 // Method: "Fine-grained Computation-Communication Overlap via Tile-level Signaling and Scheduling
 // for Mixture-of-Experts" (pith.science/paper/W2ZARMHG):
 //   "Core claim" - one rank-wide persistent GEMM covers all experts in one launch and publishes a
 //       readiness flag after each tile's epilogue store;
 //   "Load-bearing premise" and "Referee Report" major comment 2 (§3.3.1) - the tile must be
-//       visible before the flag: every epilogue thread fences its stores at GPU scope, each of the
-//       four epilogue warps then adds 1 to the tile flag with red.release.gpu; the consumer reads
-//       the flag with ld.acquire.gpu (ready at 4) and fences the async proxy before its bulk copy.
+//       visible before the flag: each of the four epilogue warps waits until its TMA stores of the
+//       tile have completed, fences the async proxy, then adds 1 to the tile flag with
+//       red.release.gpu; the consumer reads the flag with ld.acquire.gpu (ready at 4) and fences
+//       the async proxy before its bulk copy.
 //   "What carries the argument" - the consumer runs on a small dedicated SM partition; here the
 //       partition is the last consumer_ctas CTAs of the same cooperative launch, so producers and
 //       consumers are guaranteed to be co-resident.
@@ -22,6 +24,7 @@ namespace moe {
 
 struct Smem {
     uint8_t* stages;
+    uint8_t* epi;
     uint64_t* full;
     uint64_t* empty;
     uint64_t* acc_full;
@@ -39,7 +42,8 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
     const uint32_t a = smem_u32(raw);
     uint8_t* base = raw + (((a + 1023u) & ~1023u) - a);
     sm.stages = base;
-    uint8_t* misc = base + STAGES * STAGE_BYTES;
+    sm.epi = base + STAGES * STAGE_BYTES;
+    uint8_t* misc = sm.epi + EPI_BYTES;
     sm.full = reinterpret_cast<uint64_t*>(misc);
     sm.empty = sm.full + STAGES;
     sm.acc_full = sm.empty + STAGES;
@@ -92,7 +96,8 @@ __device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* sch
 template <int MODE>  // 1: SwiGLU up-projection -> Hp; 2: down-projection -> Yp (+ flags / consumer)
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                const __grid_constant__ CUtensorMap tmB1, int num_producers, int overlapped) {
+                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut, int num_producers,
+                int overlapped) {
     extern __shared__ uint8_t smem_raw[];
     Smem sm = carve_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -143,6 +148,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (producer && tid == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB0);
+        tma_prefetch_desc(&tmOut);
         if (MODE == 1) tma_prefetch_desc(&tmB1);
         if (MODE == 2) atomicMin(&p.trace[MOE_TRACE_GEMM2_START], globaltimer());
     }
@@ -239,12 +245,37 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
         } else if (warp >= 2) {
             // ---------------- epilogue ----------------
+            // Each warp owns TMEM lanes 32q..32q+31 (tile rows). Per 32-column chunk: tcgen05.ld,
+            // convert, write the 32 x 32 bf16 chunk to a shared staging buffer (each lane its row,
+            // 16-byte pieces in a lane-rotated order, free of bank conflicts), then lane 0 issues one
+            // TMA tensor store of the chunk. Two staging buffers per warp alternate.
             const int q = warp & 3;  // TMEM lane quarter this warp may access
-            const int row = q * 32 + lane;
-            const bool store = row < s.tbM;
+            const bool active = q * 32 < s.tbM;  // rows of this warp lie inside the tile
             const bool flags = (MODE == 2) && overlapped;
+            uint8_t* ebuf = sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES;
+            int eb = 0;
             int b = 0;
             uint32_t aph = 0;
+            auto stage_chunk = [&](const uint32_t (&pk)[16], int x, int y) {
+                if (lane == 0) bulk_wait_read_1();  // the store that last used this buffer has read it
+                __syncwarp();
+                uint4* dst = reinterpret_cast<uint4*>(ebuf + eb * EPI_CHUNK_BYTES + lane * (EPI_CHUNK * 2));
+                const uint4 u0 = make_uint4(pk[0], pk[1], pk[2], pk[3]), u1 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                const uint4 u2 = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+                const uint4 u3 = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int pi = (i + lane) & 3;
+                    dst[pi] = pi == 0 ? u0 : pi == 1 ? u1 : pi == 2 ? u2 : u3;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmOut, ebuf + eb * EPI_CHUNK_BYTES, x, y);
+                    bulk_commit();
+                }
+                eb ^= 1;
+            };
             for (int t = blockIdx.x; t < total; t += num_producers) {
                 const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, nN, p.tiles)
                                                : decode_down(t, nN, p.sched, p.tiles);
@@ -255,41 +286,36 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
+                const int y = tr.row0 + q * 32;
                 if (MODE == 1) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.Hp + (size_t)(tr.row0 + row) * s.ffn + tr.n * BN1);
 #pragma unroll 1
                     for (int c = 0; c < BN1 / 32; ++c) {
                         uint32_t g[32], u[32];
                         tmem_ld32(tb + c * 32, g);
                         tmem_ld32(tb + BN1 + c * 32, u);
-                        if (store) {
+                        if (active) {
                             uint32_t pk[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-                                const float h0 = g0 / (1.0f + __expf(-g0)) * __uint_as_float(u[2 * i]);
-                                const float h1 = g1 / (1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
+                                const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * __uint_as_float(u[2 * i]);
+                                const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
                                 pk[i] = pack_bf16x2(h0, h1);
                             }
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                dst[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                            stage_chunk(pk, tr.n * BN1 + c * 32, y);
                         }
                     }
                 } else {
-                    uint4* dst = reinterpret_cast<uint4*>(p.Yp + (size_t)(tr.row0 + row) * s.d + tr.n * BN);
 #pragma unroll 1
                     for (int c = 0; c < BN / 32; ++c) {
                         uint32_t v[32];
                         tmem_ld32(tb + c * 32, v);
-                        if (store) {
+                        if (active) {
                             uint32_t pk[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
                                 pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                dst[c * 4 + i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                            stage_chunk(pk, tr.n * BN + c * 32, y);
                         }
                     }
                 }
@@ -297,18 +323,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 mbar_arrive(&sm.acc_empty[b]);
                 if (MODE == 2) {
                     if (flags) {
-                        // Each epilogue warp publishes its quarter of the tile: every lane fences its
-                        // stores at GPU scope, the warp converges, then lane 0 adds 1 to the tile's
-                        // flag with release semantics. The tile is ready when the flag reaches 4.
-                        __threadfence();
+                        // Publish this warp's quarter of the tile: its TMA stores must be complete
+                        // (not only read out of shared memory), the async proxy fenced against the
+                        // generic one, then lane 0 adds 1 to the tile's flag with release semantics.
+                        // The tile is ready when the flag reaches 4.
+                        if (lane == 0) {
+                            bulk_wait_all();
+                            fence_proxy_async_global();
+                            __threadfence();
+                            red_release_gpu_add(p.flags + (size_t)tr.m * s.n_tiles_n2 + tr.n, 1u);
+                        }
                         __syncwarp();
-                        if (lane == 0) red_release_gpu_add(p.flags + (size_t)tr.m * s.n_tiles_n2 + tr.n, 1u);
                     }
                     if (lane == 0) last_end = globaltimer();
                 }
                 b ^= 1;
                 if (b == 0) aph ^= 1u;
             }
+            if (lane == 0) bulk_wait_all();  // staging buffers stay valid until every store is done
+            __syncwarp();
         }
     }
     tc_fence_before();
@@ -322,9 +355,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
 
     if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST))) {
-        CopyRing cr{sm.stages, sm.cbar, 0u, 0u};
         const uint32_t want = (s.flags & MOE_TEST_STALL_CONSUMER) ? FLAG_READY + 1u : FLAG_READY;
-        copy_units(s, p, cr, sm.unit, sm.abort, META_QUEUE, true, want);
+        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want);
     }
 }
 
@@ -333,29 +365,29 @@ static cudaError_t set_smem_attr(const void* fn) {
 }
 
 cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW1,
-                               const CUtensorMap& tmW3, int sms, cudaStream_t st) {
+                               const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms, cudaStream_t st) {
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<1>));
     if (e != cudaSuccess) return e;
-    gemm_kernel<1><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(s, p, tmA, tmW1, tmW3, sms, 0);
+    gemm_kernel<1><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(s, p, tmA, tmW1, tmW3, tmOut, sms, 0);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2,
-                             int sms, int consumers, bool overlapped, cudaStream_t st) {
+                             const CUtensorMap& tmOut, int sms, int consumers, bool overlapped, cudaStream_t st) {
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<2>));
     if (e != cudaSuccess) return e;
     const int producers = overlapped ? sms - consumers : sms;
     int ov = overlapped ? 1 : 0;
     Shape sa = s;
     PlanPtrs pa = p;
-    CUtensorMap a = tmA, b0 = tmW2, b1 = tmW2;
+    CUtensorMap a = tmA, b0 = tmW2, b1 = tmW2, o = tmOut;
     if (!overlapped) {
-        gemm_kernel<2><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(sa, pa, a, b0, b1, producers, ov);
+        gemm_kernel<2><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(sa, pa, a, b0, b1, o, producers, ov);
         return cudaGetLastError();
     }
     // Cooperative launch: every CTA (producers and consumers) is resident at once, or the launch
     // fails; the consumers' waits on producer flags can therefore always be satisfied.
-    void* args[] = {&sa, &pa, &a, &b0, &b1, (void*)&producers, &ov};
+    void* args[] = {&sa, &pa, &a, &b0, &b1, &o, (void*)&producers, &ov};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&gemm_kernel<2>), dim3(sms), dim3(GEMM_THREADS),
                                        args, GEMM_SMEM, st);
 }
@@ -370,8 +402,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) copy_seq_kernel(Shape s, Plan
         mbar_fence_init();
     }
     __syncthreads();
-    CopyRing cr{sm.stages, sm.cbar, 0u, 0u};
-    copy_units(s, p, cr, sm.unit, sm.abort, META_QUEUE_SEQ, false, 0u);
+    copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE_SEQ, false, 0u);
 }
 
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st) {

@@ -56,7 +56,9 @@ int make_layout(const moe_config* c, Layout* out) {
     const int64_t P_max = (int64_t)align_up((size_t)(TK + (G < TK ? G : TK) * (tbM - 1)), (size_t)tbM);
     if (P_max >= (int64_t(1) << 30)) return fail(MOE_ERR_ARG, "padded rows %lld too large", (long long)P_max);
     const int64_t MT_max = P_max / tbM;
-    int64_t C = 256;
+    // route chunk: <= 128 tokens and <= 32 KB of staged logits, a power of two dividing T/R
+    int64_t C = 128;
+    while (C > 1 && C * (E + 1) * 4 > 32768) C >>= 1;
     while ((T / R) % C) C >>= 1;
     const int bn2 = (d % 256 == 0) ? 256 : 128;
     const int nN2 = (int)(d / bn2);
@@ -199,18 +201,21 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// bf16 tensor [outer][mid][inner] (rank 3) or [mid][inner] (rank 2, outer = 1); box 64 x box_mid (x 1),
-// 128-byte swizzle, out-of-bounds elements read as zero.
+// bf16 tensor [outer][mid][inner] (rank 3) or [mid][inner] (rank 2, outer = 1); box box_inner x
+// box_mid (x 1). Operand maps: 64-element inner box with the 128-byte swizzle the UMMA descriptors
+// expect; output maps: 32 x 32 boxes, unswizzled (row pitch 64 bytes in shared memory).
+// Out-of-bounds elements read as zero.
 int make_map(CUtensorMap* m, const void* ptr, int rank, uint64_t inner, uint64_t mid, uint64_t outer,
-             uint32_t box_mid, const char* what) {
+             uint32_t box_mid, const char* what, uint32_t box_inner = BK, bool swizzle = true) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[3] = {inner, mid, outer};
     cuuint64_t strides[2] = {inner * 2, inner * mid * 2};
-    cuuint32_t box[3] = {(cuuint32_t)BK, box_mid, 1};
+    cuuint32_t box[3] = {box_inner, box_mid, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box,
-                    es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
     return MOE_OK;
@@ -270,9 +275,11 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     if (overlapped && (c.consumers < 1 || c.consumers > c.di.sms / 2))
         return fail(MOE_ERR_ARG, "consumer_ctas=%d must be in [1, %d]", c.consumers, c.di.sms / 2);
 
-    CUtensorMap tXp, tHp, tW1, tW3, tW2;
+    CUtensorMap tXp, tHp, tW1, tW3, tW2, tHpOut, tYpOut;
     int rc = make_map(&tXp, c.p.Xp, 2, S.d, S.P_max, 1, BM, "Xp");
     if (!rc) rc = make_map(&tHp, c.p.Hp, 2, S.ffn, S.P_max, 1, BM, "Hp");
+    if (!rc) rc = make_map(&tHpOut, c.p.Hp, 2, S.ffn, S.P_max, 1, 32, "Hp (store)", EPI_CHUNK, false);
+    if (!rc) rc = make_map(&tYpOut, c.p.Yp, 2, S.d, S.P_max, 1, 32, "Yp (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tW1, W1, 3, S.d, S.ffn, S.E, BN1, "W1");
     if (!rc) rc = make_map(&tW3, W3, 3, S.d, S.ffn, S.E, BN1, "W3");
     if (!rc) rc = make_map(&tW2, W2, 3, S.ffn, S.d, S.E, S.bn2, "W2");
@@ -283,15 +290,15 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     rc = run_plan(c, logits, x, true);
     if (rc) return rc;
     if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
-    cudaError_t e = launch_gemm_swiglu(S, c.p, tXp, tW1, tW3, c.di.sms, c.st);
+    cudaError_t e = launch_gemm_swiglu(S, c.p, tXp, tW1, tW3, tHpOut, c.di.sms, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
     if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
     if (overlapped) {
-        e = launch_gemm_down(S, c.p, tHp, tW2, c.di.sms, c.consumers, true, c.st);
+        e = launch_gemm_down(S, c.p, tHp, tW2, tYpOut, c.di.sms, c.consumers, true, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "overlapped down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
     } else {
-        e = launch_gemm_down(S, c.p, tHp, tW2, c.di.sms, 0, false, c.st);
+        e = launch_gemm_down(S, c.p, tHp, tW2, tYpOut, c.di.sms, 0, false, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
         e = launch_copy_seq(S, c.p, c.di.sms, c.st);

@@ -44,16 +44,23 @@ constexpr int B_STAGE_BYTES = 256 * BK * 2;            // 32 KB (up to N = 256)
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int GEMM_THREADS = 192;                      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int MISC_BYTES = 4096;
-constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + MISC_BYTES + 1024;  // + alignment slack
+// epilogue staging: per epilogue warp two 32-row x 32-column bf16 chunks (2 KB each), written to
+// global memory by TMA tensor stores
+constexpr int EPI_CHUNK = 32;
+constexpr int EPI_CHUNK_BYTES = 32 * EPI_CHUNK * 2;
+constexpr int EPI_BYTES = 4 * 2 * EPI_CHUNK_BYTES;
+constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + EPI_BYTES + MISC_BYTES + 1024;  // + alignment slack
 constexpr int TMEM_COLS = 512;                         // two 256-column fp32 accumulators
 constexpr int BN1 = 128;                               // output columns of a SwiGLU tile
 constexpr uint32_t FLAG_READY = 4;                     // one release-add per epilogue warp
 constexpr int MAX_E = 256;
 
-// bulk copy ring of the consumer (reuses the stage area)
-constexpr int COPY_PIECE = 32768;
-constexpr int COPY_NBUF = (STAGES * STAGE_BYTES) / COPY_PIECE;   // 6
-constexpr int UNIT_BYTES = 131072;                     // target bytes of one copy unit
+// copy engines of the consumer (one per warp, two staging buffers each, in the stage area)
+constexpr int COPY_PIECE = 16384;
+constexpr int COPY_WARPS = GEMM_THREADS / 32;                    // 6
+constexpr int COPY_NBUF = 2 * COPY_WARPS;                        // 12 buffers / mbarriers
+static_assert(COPY_NBUF * COPY_PIECE <= STAGES * STAGE_BYTES, "copy staging must fit the stage area");
+constexpr int UNIT_BYTES = 65536;                      // target bytes of one copy unit
 
 // ---- parameters passed by value to kernels --------------------------------------------------
 struct PlanPtrs {
@@ -97,9 +104,9 @@ cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p,
 cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st);
 cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW1,
-                               const CUtensorMap& tmW3, int sms, cudaStream_t st);
+                               const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms, cudaStream_t st);
 cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2,
-                             int sms, int consumers, bool overlapped, cudaStream_t st);
+                             const CUtensorMap& tmOut, int sms, int consumers, bool overlapped, cudaStream_t st);
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
 
@@ -183,6 +190,19 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
         "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
+
+// shared -> global tensor store of one box, tracked as a bulk async-group of the issuing thread
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
 // ---- untiled bulk copies (global <-> shared) --------------------------------------------------
 __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {

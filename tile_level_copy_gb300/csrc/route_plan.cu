@@ -9,67 +9,57 @@
 
 namespace moe {
 
-constexpr int ROUTE_THREADS = 256;   // 8 warps; one CTA ranks one chunk of <= 256 tokens
+constexpr int ROUTE_THREADS = 128;   // one thread per token of a chunk of <= 128 tokens
 constexpr int KMAX = 8;
 
 // ---------------------------------------------------------------------------------------------
 // route_kernel: one CTA per chunk of `chunk_tokens` consecutive tokens (a chunk never straddles
-// two owners). Phase 1, one warp per token: top-k of the token's E logits, descending, ties to the
-// lower expert id; gates = softmax over the k chosen logits in fp32. Phase 2: for every expert, the
-// rank of each token among the chunk's tokens routed to it (ascending token order) by warp ballots,
-// and the chunk's count per expert.
+// two owners). The chunk's logits are staged in shared memory with coalesced loads (rows padded
+// to E+1 words against bank conflicts); then thread t, for token t of the chunk: top-k of the E
+// logits, descending, ties to the lower expert id, and gates = softmax over the k chosen logits in
+// fp32. Last, per expert, warp ballots give each token's rank among the chunk's tokens routed to
+// that expert (ascending token order) and the chunk's count per expert.
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const float* __restrict__ logits, PlanPtrs p) {
-    __shared__ int32_t s_idx[256][KMAX];
+    extern __shared__ float s_logit[];  // [C][E + 1]
     __shared__ uint32_t s_mask[ROUTE_THREADS / 32][MAX_E];
     __shared__ int32_t s_wpre[ROUTE_THREADS / 32][MAX_E];
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int C = s.chunk_tokens, E = s.E, k = s.k;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tl = threadIdx.x;
+    const int C = s.chunk_tokens, E = s.E, k = s.k, ld = E + 1;
     const int t0 = blockIdx.x * C;
+    const float* src = logits + (size_t)t0 * E;
+    for (int i = threadIdx.x; i < C * E; i += ROUTE_THREADS) s_logit[(i / E) * ld + (i % E)] = __ldg(src + i);
+    __syncthreads();
 
-    for (int tl = warp; tl < C; tl += ROUTE_THREADS / 32) {
-        const int t = t0 + tl;
-        const float* row = logits + (size_t)t * E;
-        float v[MAX_E / 32];
-        bool taken[MAX_E / 32];
+    const bool live = tl < C;
+    int sel_e[KMAX];
 #pragma unroll
-        for (int i = 0; i < MAX_E / 32; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = (e < E) ? row[e] : -INFINITY;
-            taken[i] = (e >= E);
-        }
+    for (int j = 0; j < KMAX; ++j) sel_e[j] = -1;
+    if (live) {
+        const float* row = s_logit + tl * ld;
         float sel_v[KMAX];
-        int sel_e[KMAX];
+        float prev_v = INFINITY;
+        int prev_e = -1;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             if (j >= k) break;
+            // next in (value desc, id asc) order after (prev_v, prev_e)
             float bv = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < MAX_E / 32; ++i) {
-                const int e = lane + 32 * i;
-                if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) {
-                    bv = v[i];
+            int be = -1;
+            for (int e = 0; e < E; ++e) {
+                const float v = row[e];
+                const bool after = (v < prev_v) || (v == prev_v && e > prev_e);
+                if (after && (be < 0 || v > bv)) {
+                    bv = v;
                     be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
                 }
             }
             sel_v[j] = bv;
             sel_e[j] = be;
-#pragma unroll
-            for (int i = 0; i < MAX_E / 32; ++i)
-                if (lane + 32 * i == be) taken[i] = true;
+            prev_v = bv;
+            prev_e = be;
         }
-        // gates: softmax over the chosen logits (sel_v[0] is the maximum)
         float z[KMAX], sum = 0.f;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
@@ -77,26 +67,20 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
             z[j] = expf(sel_v[j] - sel_v[0]);
             sum += z[j];
         }
+        const int t = t0 + tl;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             if (j >= k) break;
-            if (lane == j) {
-                p.idx[(size_t)t * k + j] = sel_e[j];
-                p.gate[(size_t)t * k + j] = z[j] / sum;
-                s_idx[tl][j] = sel_e[j];
-            }
+            p.idx[(size_t)t * k + j] = sel_e[j];
+            p.gate[(size_t)t * k + j] = z[j] / sum;
         }
     }
-    __syncthreads();
 
-    // phase 2: ballots per expert over the chunk's tokens (thread tl <-> token t0 + tl)
-    const int tl = threadIdx.x;
-    const bool live = tl < C;
+    // ranks: ballots per expert over the chunk's tokens
     for (int e = 0; e < E; ++e) {
         bool has = false;
-        if (live) {
-            for (int j = 0; j < k; ++j) has |= (s_idx[tl][j] == e);
-        }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) has |= (sel_e[j] == e);
         const uint32_t m = __ballot_sync(0xffffffffu, has);
         if (lane == 0) s_mask[warp][e] = m;
     }
@@ -113,15 +97,18 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
     if (live) {
         const uint32_t lt = (1u << lane) - 1u;
         const int t = t0 + tl;
-        for (int j = 0; j < k; ++j) {
-            const int e = s_idx[tl][j];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (j >= k) break;
+            const int e = sel_e[j];
             p.rank[(size_t)t * k + j] = s_wpre[warp][e] + __popc(s_mask[warp][e] & lt);
         }
     }
 }
 
 cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p, cudaStream_t st) {
-    route_kernel<<<s.n_chunks, ROUTE_THREADS, 0, st>>>(s, logits, p);
+    const size_t smem = (size_t)s.chunk_tokens * (s.E + 1) * sizeof(float);
+    route_kernel<<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p);
     return cudaGetLastError();
 }
 
@@ -163,9 +150,10 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     __shared__ int s_load[MAX_E];    // rows per expert
     __shared__ int s_erank[MAX_E];   // position of the expert in (load desc, id asc) order
     __shared__ int s_fb[MAX_E];      // full bands per expert
-    __shared__ int s_fbase[MAX_E];   // first schedule position of the expert's full bands
+    __shared__ int s_mt[MAX_E];      // M-tiles per expert
+    __shared__ int s_ebase[MAX_E];   // first schedule position of the expert's bands
     __shared__ int s_warp[32];
-    __shared__ int s_total, s_full_total;
+    __shared__ int s_total;
 
     const int E = s.E, R = s.R, G = E * R, tbM = s.tbM, tid = threadIdx.x;
     const int cpo = (s.T / R) / s.chunk_tokens;  // chunks per owner
@@ -216,8 +204,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         }
         s_load[e] = load;
         s_fb[e] = fb;
+        s_mt[e] = (s_off[(e + 1) * R] - s_off[e * R]) / tbM;
         p.experts[2 * e + 0] = s_off[e * R] / tbM;
-        p.experts[2 * e + 1] = (s_off[(e + 1) * R] - s_off[e * R]) / tbM;
+        p.experts[2 * e + 1] = s_mt[e];
     }
     __syncthreads();
     for (int e = tid; e < E; e += PLAN_THREADS) {
@@ -230,19 +219,15 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     for (int e = tid; e < E; e += PLAN_THREADS) {
         int base = 0;
         for (int f = 0; f < E; ++f)
-            if (s_erank[f] < s_erank[e]) base += s_fb[f];
-        s_fbase[e] = base;
-    }
-    if (tid == 0) {
-        int tot = 0;
-        for (int e = 0; e < E; ++e) tot += s_fb[e];
-        s_full_total = tot;
+            if (s_erank[f] < s_erank[e]) base += s_mt[f];
+        s_ebase[e] = base;
     }
     __syncthreads();
 
     // 5. tiles, destination rows, and schedule positions.
-    // Schedule key (-valid, expert rank, owner, row): full bands first, expert by expert in rank
-    // order, each expert's full bands in layout order; then the partial bands by valid rows desc.
+    // Schedule key (expert rank, -valid, owner, row): experts one after another in rank order
+    // (most loaded first); inside an expert its full bands in layout order, then its partial
+    // bands by valid rows descending (ties to the lower owner).
     for (int g = tid; g < G; g += PLAN_THREADS) {
         const int e = g / R, r = g % R, n = s_n[g];
         const int m0 = s_off[g] / tbM;
@@ -258,21 +243,17 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             p.tiles[4 * m + 2] = s_off[g] + i * tbM;
             p.tiles[4 * m + 3] = valid;
             p.tile_ret[m] = rbase + i * tbM;
-            if (i < nfull) p.sched[s_fbase[e] + fpre + i] = m;
+            if (i < nfull) p.sched[s_ebase[e] + fpre + i] = m;
         }
         if (nt > nfull) {  // one partial band
             const int valid = n - nfull * tbM;
             int pos = 0;
-            for (int h = 0; h < G; ++h) {
-                const int nh = s_n[h];
-                const int vh = nh % tbM;
-                if (vh == 0 || h == g) continue;
-                const int eh = h / R, rh = h % R;
-                const bool before = (vh > valid) || (vh == valid && (s_erank[eh] < s_erank[e] ||
-                                                                      (s_erank[eh] == s_erank[e] && rh < r)));
-                pos += before;
+            for (int rh = 0; rh < R; ++rh) {
+                const int vh = s_n[e * R + rh] % tbM;
+                if (vh == 0 || rh == r) continue;
+                pos += (vh > valid) || (vh == valid && rh < r);
             }
-            p.sched[s_full_total + pos] = m0 + nfull;
+            p.sched[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
         }
     }
     __syncthreads();
@@ -316,9 +297,13 @@ cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
 
 // ---------------------------------------------------------------------------------------------
 // permute_kernel: one warp per work item. Items [0, T): token t computes its k slots and return
-// slots and copies x[t] into the k rows of Xp with 16-byte vectors. Items [T, T + M-tiles): the
-// padding rows of that M-tile are zeroed. With x == nullptr only the slots are written.
+// slots and copies x[t] into the k rows of Xp: each lane first loads up to 16 vectors of 16 bytes
+// (all loads in flight together), then stores them to the k rows. Items [T, T + M-tiles * tbM/8):
+// one group of 8 rows of an M-tile, zeroing those rows that are padding (row >= valid). With
+// x == nullptr only the slots are written.
 // ---------------------------------------------------------------------------------------------
+constexpr int PERM_VEC = 16;  // 16-byte vectors per lane per pass
+
 __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat16* __restrict__ x, PlanPtrs p) {
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -328,8 +313,9 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
     const uint4* xs = reinterpret_cast<const uint4*>(x);
     uint4* xp = reinterpret_cast<uint4*>(p.Xp);
     const bool ok_mt = MT <= s.MT_max;
+    const int groups = s.tbM / 8;
+    const int pad_items = (ok_mt && xs != nullptr) ? MT * groups : 0;
 
-    const int pad_items = (ok_mt && xs != nullptr) ? MT : 0;
     for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < s.T + pad_items; item += nwarps) {
         if (item < s.T) {
             const int t = item, r = t / per, c = t / s.chunk_tokens;
@@ -353,17 +339,28 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
                 continue;
             }
             if (xs == nullptr) continue;  // plan only: slots without the row copy
-            for (int v = lane; v < vec; v += 32) {
-                const uint4 val = __ldg(xs + (size_t)t * vec + v);
+            for (int base = 0; base < vec; base += 32 * PERM_VEC) {
+                uint4 v[PERM_VEC];
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j)
-                    if (j < k) xp[(size_t)sl[j] * vec + v] = val;
+                for (int i = 0; i < PERM_VEC; ++i) {
+                    const int vi = base + i * 32 + lane;
+                    if (vi < vec) v[i] = __ldg(xs + (size_t)t * vec + vi);
+                }
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j >= k) break;
+#pragma unroll
+                    for (int i = 0; i < PERM_VEC; ++i) {
+                        const int vi = base + i * 32 + lane;
+                        if (vi < vec) xp[(size_t)sl[j] * vec + vi] = v[i];
+                    }
+                }
             }
         } else {
-            const int m = item - s.T;
+            const int q = item - s.T, m = q / groups, g = q % groups;
             const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
             const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int rr = valid; rr < s.tbM; ++rr) {
+            for (int rr = max(valid, g * 8); rr < (g + 1) * 8; ++rr) {
                 const size_t row = (size_t)row0 + rr;
                 if (row >= (size_t)s.P_max) break;
                 for (int v = lane; v < vec; v += 32) xp[row * vec + v] = z;
@@ -373,8 +370,8 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
 }
 
 cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtrs& p, int sms, cudaStream_t st) {
-    const int items = s.T + s.MT_max;
-    const int blocks = min((items + 7) / 8, sms * 8);
+    const int items = s.T + s.MT_max * (s.tbM / 8);
+    const int blocks = min((items + 7) / 8, sms * 16);
     permute_kernel<<<blocks, 256, 0, st>>>(s, x, p);
     return cudaGetLastError();
 }
