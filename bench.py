@@ -35,6 +35,9 @@ from tile_level_copy_gb300 import inputs  # noqa: E402
 METRIC = "MoE-layer tokens/s; grouped-GEMM % of BF16 peak; return-copy overlap %"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Consumer partition per workload: enough copy engines to keep up with the down-projection's
+# output rate (the fine-grained layer returns 6 rows per token over a short GEMM).
+DEFAULT_CONSUMERS = {"tiny": 4, "mixtral": 8, "skew": 8, "fine": 16}
 
 
 def parse_args():
@@ -44,7 +47,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral", choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--consumers", type=int, default=8, help="c_CTA: SMs of the consumer partition")
+    ap.add_argument("--consumers", type=int, default=None,
+                    help="c_CTA: SMs of the consumer partition (default per workload, see DEFAULT_CONSUMERS)")
     ap.add_argument("--mgb", type=int, default=1)
     ap.add_argument("--no-tail-assist", action="store_true", help="keep finished producer CTAs out of the copy")
     ap.add_argument("--seed", type=int, default=0)
@@ -166,6 +170,8 @@ def run_ours(args, rank: int, world: int):
     tlc_build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
     w = inputs.WORKLOADS[args.workload]
+    if args.consumers is None:
+        args.consumers = DEFAULT_CONSUMERS.get(args.workload, 8)
     seed = args.seed + rank
     flags = 0 if args.no_tail_assist else tlc.MOE_TAIL_ASSIST
     cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags)
@@ -215,7 +221,7 @@ def run_ours(args, rank: int, world: int):
     seq_value, _ = aggregate(sec_seq, w.T * K, world)
 
     # overlap from %globaltimer stamps of a few extra overlapped steps
-    hidden, tails = [], []
+    hidden, tails, marks = [], [], []
     copy_alone_ms = float(np.median(st_seq[:, tlc.EV_DOWN]))
     for _ in range(5):
         step(False)
@@ -224,6 +230,9 @@ def run_ours(args, rank: int, world: int):
         tail_ms = max(0, int(tr[tlc.TRACE_COPY_END]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e6
         tails.append(tail_ms)
         hidden.append(1.0 - tail_ms / copy_alone_ms)
+        marks.append([(int(tr[i]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e3 for i in
+                      (tlc.TRACE_BAND_DONE, tlc.TRACE_LAST_ACQUIRE, tlc.TRACE_LAST_LOAD, tlc.TRACE_LAST_DRAIN,
+                       tlc.TRACE_COPY_END)])
     ms_ovl, ms_seq = sec_ovl * 1e3 / K, sec_seq * 1e3 / K
 
     # GEMM numbers: real rows = T*k; executed rows = P (padded)
@@ -265,6 +274,8 @@ def run_ours(args, rank: int, world: int):
                  "down_ms": round(down_ms, 4), "padded_rows": P, "real_rows": TK},
         "overlap": {"hidden_pct": round(100 * statistics.median(hidden), 2),
                     "tail_ms": round(statistics.median(tails), 4), "copy_alone_ms": round(copy_alone_ms, 4),
+                    "tail_marks_us": dict(zip(["band_done", "last_acquire", "last_load", "last_drain", "copy_end"],
+                                              [round(float(v), 2) for v in np.median(np.array(marks), 0)])),
                     "wall_pct": round(100 * (ms_seq - ms_ovl) / copy_alone_ms, 2),
                     "sequential_ms_per_step": round(ms_seq, 4), "sequential_tokens_per_s": round(seq_value, 1),
                     "speedup_vs_sequential": round(ms_seq / ms_ovl, 4)},

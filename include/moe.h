@@ -107,6 +107,7 @@ typedef struct moe_layout {
     size_t ret_slot;   /* int32 [T, topk]   row of pair (t, j) in Ret                          */
     size_t meta;       /* int32 [64]        P, M-tiles, work counters, status (see csrc)       */
     size_t flags;      /* uint32 [MT_max, n_tiles_n2] per-tile readiness flags                 */
+    size_t bands;      /* uint32 [MT_max]   per-band count of finished tile quarters           */
     size_t trace;      /* uint64 [16]       %globaltimer stamps of the last call (ns)          */
     size_t Xp;         /* bf16 [P_max, d]   permuted tokens                                    */
     size_t Hp;         /* bf16 [P_max, ffn] SwiGLU hidden                                      */
@@ -122,6 +123,10 @@ typedef struct moe_layout {
 #define MOE_TRACE_GEMM2_END 1    /* latest readiness flag (overlapped) / tile end (sequential) */
 #define MOE_TRACE_COPY_START 2   /* earliest start of a row-band copy                        */
 #define MOE_TRACE_COPY_END 3     /* latest completion of a row-band copy                     */
+#define MOE_TRACE_BAND_DONE 4    /* overlapped: latest time a band's last tile was published   */
+#define MOE_TRACE_LAST_ACQUIRE 5 /* overlapped: latest time a copy engine acquired a band      */
+#define MOE_TRACE_LAST_LOAD 6    /* latest issue of a bulk load by a copy engine               */
+#define MOE_TRACE_LAST_DRAIN 7   /* latest start of a copy engine's final drain                */
 
 /* Size in bytes of the workspace for `cfg` (host-only arithmetic, no CUDA call).
  * Returns MOE_ERR_ARG for an invalid config. */

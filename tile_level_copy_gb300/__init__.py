@@ -29,6 +29,7 @@ MOE_TAIL_ASSIST = 0x2
 MOE_TEST_STALL_CONSUMER = 0x100
 
 TRACE_GEMM2_START, TRACE_GEMM2_END, TRACE_COPY_START, TRACE_COPY_END = 0, 1, 2, 3
+TRACE_BAND_DONE, TRACE_LAST_ACQUIRE, TRACE_LAST_LOAD, TRACE_LAST_DRAIN = 4, 5, 6, 7
 
 # names of the C entry points (each declared in include/moe.h)
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_plan", "moe_forward", "moe_forward_sequential",
@@ -53,7 +54,7 @@ class _Config(ctypes.Structure):
 _LAYOUT_INTS = ("P_max", "MT_max", "n_chunks", "chunk_tokens", "n_tiles_n2", "block_n2", "rows_per_unit",
                 "units_per_band")
 LAYOUT_REGIONS = ("idx", "gate", "rank", "chunk_cnt", "chunk_base", "counts", "offsets", "ret_off", "tiles",
-                  "tile_ret", "sched", "seg", "experts", "slot", "ret_slot", "meta", "flags", "trace", "Xp", "Hp",
+                  "tile_ret", "sched", "seg", "experts", "slot", "ret_slot", "meta", "flags", "bands", "trace", "Xp", "Hp",
                   "Yp", "Ret", "in_logits", "in_x", "out")
 
 
@@ -165,6 +166,7 @@ class Workspace:
            "offsets": (torch.int32, "G1"), "ret_off": (torch.int32, "RE1"), "tiles": (torch.int32, "MT4"),
            "tile_ret": (torch.int32, "MT"), "sched": (torch.int32, "MT"), "seg": (torch.int32, "MT2"),
            "experts": (torch.int32, "E2"), "meta": (torch.int32, "META"), "flags": (torch.int32, "FL"),
+           "bands": (torch.int32, "MT"),
            "trace": (torch.int64, "TR"), "Xp": (torch.bfloat16, "Pd"), "Hp": (torch.bfloat16, "PF"),
            "Yp": (torch.bfloat16, "Pd"), "Ret": (torch.bfloat16, "TKd")}
 

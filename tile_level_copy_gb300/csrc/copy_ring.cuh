@@ -6,7 +6,7 @@
 // HBM-to-HBM copy. Every warp of a copying CTA is an independent copy engine: it takes a work unit,
 // waits for the unit's flags, and moves the rows through two shared-memory buffers with TMA bulk
 // copies (global -> shared completes on an mbarrier, shared -> global is a bulk group), so each
-// warp keeps two loads in flight and a 6-warp CTA about 192 KB.
+// warp keeps two 16 KB loads in flight, also across unit boundaries.
 //
 // Work units: band (schedule position) x row chunk of rows_per_unit rows, handed out in schedule
 // order by an atomic counter, so idle engines always take the oldest outstanding band.
@@ -16,107 +16,129 @@
 
 namespace moe {
 
-// Per-warp copy engine: two COPY_PIECE staging buffers and their mbarriers. Lane 0 issues.
+// Per-warp copy engine: two COPY_PIECE staging buffers used in FIFO order, their mbarriers, and
+// the destination of the piece each holds. Lane 0 issues all bulk operations; pieces flow through
+// the two buffers continuously, across unit boundaries.
 struct CopyEngine {
     uint8_t* buf;         // 2 * COPY_PIECE bytes, 1024-byte aligned
     uint64_t* bar;        // 2 mbarriers, count 1
+    uint8_t* dst[2];      // destination of the piece loaded into each buffer
+    uint32_t len[2];
     uint32_t phase_bits;  // parity to wait for next, per buffer
-    uint32_t pending;     // buffers with a load in flight that has not been waited for
+    int head, count;      // oldest occupied buffer, occupied buffers
 };
 
-// Lane 0 only. Copies `bytes` (a multiple of 16) from src to dst, keeping two bulk loads in
-// flight. Returns false on timeout.
-__device__ __forceinline__ bool engine_copy(CopyEngine& ce, const uint8_t* src, uint8_t* dst, size_t bytes,
-                                            unsigned long long timeout_ns, volatile int* abort) {
-    const int np = (int)((bytes + COPY_PIECE - 1) / COPY_PIECE);
-    bulk_wait_read_all();  // every earlier store of this lane has finished reading its buffer
-    auto piece = [&](int i) { return (uint32_t)min((size_t)COPY_PIECE, bytes - (size_t)i * COPY_PIECE); };
-    auto issue = [&](int i) {
-        const int b = i & 1;
-        mbar_arrive_expect_tx(&ce.bar[b], piece(i));
-        bulk_load(ce.buf + (size_t)b * COPY_PIECE, src + (size_t)i * COPY_PIECE, piece(i), &ce.bar[b]);
-        ce.pending |= 1u << b;
-    };
-    for (int i = 0; i < min(np, 2); ++i) issue(i);
-    for (int i = 0; i < np; ++i) {
-        const int b = i & 1;
-        if (!mbar_wait(&ce.bar[b], (ce.phase_bits >> b) & 1u, timeout_ns, abort)) return false;
-        ce.phase_bits ^= 1u << b;
-        ce.pending &= ~(1u << b);
-        bulk_store(dst + (size_t)i * COPY_PIECE, ce.buf + (size_t)b * COPY_PIECE, piece(i));
-        bulk_commit();
-        if (i + 2 < np) {
-            bulk_wait_read_all();  // store i has read buffer b
-            issue(i + 2);
-        }
-    }
+// Lane 0: wait for the oldest load, store it out. Returns false on timeout.
+__device__ __forceinline__ bool engine_retire(CopyEngine& ce, unsigned long long timeout_ns, volatile int* abort) {
+    const int b = ce.head;
+    if (!mbar_wait(&ce.bar[b], (ce.phase_bits >> b) & 1u, timeout_ns, abort)) return false;
+    ce.phase_bits ^= 1u << b;
+    bulk_store(ce.dst[b], ce.buf + (size_t)b * COPY_PIECE, ce.len[b]);
+    bulk_commit();
+    ce.head ^= 1;
+    --ce.count;
     return true;
 }
 
-// Lane 0, before the CTA leaves: wait (bounded) for loads still in flight, then for all stores.
+// Lane 0: queue one piece (len <= COPY_PIECE, a multiple of 16). Returns false on timeout.
+__device__ __forceinline__ bool engine_push(CopyEngine& ce, const uint8_t* src, uint8_t* dst, uint32_t len,
+                                            unsigned long long timeout_ns, volatile int* abort) {
+    if (ce.count == 2 && !engine_retire(ce, timeout_ns, abort)) return false;
+    const int b = ce.head ^ ce.count;  // next free buffer in FIFO order
+    bulk_wait_read_all();              // the store that last used buffer b has read it
+    ce.dst[b] = dst;
+    ce.len[b] = len;
+    mbar_arrive_expect_tx(&ce.bar[b], len);
+    bulk_load(ce.buf + (size_t)b * COPY_PIECE, src, len, &ce.bar[b]);
+    ++ce.count;
+    return true;
+}
+
+// Lane 0: store every piece that is loaded (before the engine waits on a band that is not ready,
+// so finished data does not sit in shared memory meanwhile). Returns false on timeout.
+__device__ __forceinline__ bool engine_flush(CopyEngine& ce, unsigned long long timeout_ns, volatile int* abort) {
+    while (ce.count > 0)
+        if (!engine_retire(ce, timeout_ns, abort)) return false;
+    return true;
+}
+
+// Lane 0, before the CTA leaves: store what is still loaded, then wait for every store. The
+// waits are bounded; after a timeout the remaining loads are still waited for (bounded) so that
+// no copy into shared memory is in flight when the CTA exits.
 __device__ __forceinline__ void engine_drain(CopyEngine& ce, unsigned long long timeout_ns) {
     int never = 0;
-    for (int b = 0; b < 2; ++b)
-        if (ce.pending & (1u << b)) {
-            mbar_wait(&ce.bar[b], (ce.phase_bits >> b) & 1u, timeout_ns, &never);
-            ce.phase_bits ^= 1u << b;
+    while (ce.count > 0)
+        if (!engine_retire(ce, timeout_ns, &never)) {
+            ce.head ^= 1;
+            --ce.count;
         }
-    ce.pending = 0;
     bulk_wait_all();
 }
 
 // Called by every thread of the CTA. Each warp is an independent copy engine with its own slice of
 // the staging area (`ring`, COPY_WARPS * 2 * COPY_PIECE bytes) and two of the mbarriers in `bars`;
-// it takes units from meta[queue] until none is left. wait_flags: acquire every tile flag of the
-// unit's segment (== want) before copying.
+// it takes units from meta[queue] until none is left. wait_flags: acquire the band counter of every
+// band of the unit's segment (== want: all tiles of the band published) before copying. The next
+// unit's counters are polled while the previous unit's pieces are still in flight.
 __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uint64_t* bars, volatile int* s_abort,
                            int queue, bool wait_flags, uint32_t want) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int MT = p.meta[META_MTILES];
     if (MT < 0 || MT > s.MT_max) MT = 0;
-    const int units = MT * s.units_per_band;
+    const int units = copy_unit_count(s, MT);
     const size_t rowb = (size_t)s.d * 2;
-    CopyEngine ce{ring + (size_t)warp * 2 * COPY_PIECE, bars + 2 * warp, 0u, 0u};
-    unsigned long long t_first = ~0ull;
+    CopyEngine ce{};
+    ce.buf = ring + (size_t)warp * 2 * COPY_PIECE;
+    ce.bar = bars + 2 * warp;
+    unsigned long long t_first = ~0ull, t_acq = 0, t_load = 0;
     bool did = false;
 
+    int u_next = 0;
+    if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
     for (;;) {
-        int u = 0;
-        if (lane == 0) u = atomicAdd(&p.meta[queue], 1);
-        u = __shfl_sync(0xffffffffu, u, 0);
+        const int u = __shfl_sync(0xffffffffu, u_next, 0);
         if (__any_sync(0xffffffffu, *s_abort != 0) || u >= units) break;
-        const int pos = u / s.units_per_band, c = u - pos * s.units_per_band;
+        if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);  // in flight while this unit is handled
+        int pos, rb, rpu;
+        copy_unit_decode(s, MT, u, &pos, &rb, &rpu);
         const int m = p.sched[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
-        const int rb = c * s.rows_per_unit;
         if (rb >= valid) continue;
-        const int re = min(valid, rb + s.rows_per_unit);
+        const int re = min(valid, rb + rpu);
 
         if (wait_flags) {
-            const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
-            const int nf = nb * s.n_tiles_n2;
+            // lane 0 acquires the counter of every band of the unit's segment (all its tiles done)
             bool failed = false;
-            for (int f = lane; f < nf && !failed; f += 32) {
-                const int mb = p.sched[first + f / s.n_tiles_n2];
-                const uint32_t* fl = p.flags + (size_t)mb * s.n_tiles_n2 + (f % s.n_tiles_n2);
-                if (ld_acquire_gpu(fl) == want) continue;
-                const unsigned long long t0 = globaltimer();
-                for (;;) {
-                    __nanosleep(32);
-                    if (ld_acquire_gpu(fl) == want) break;
-                    if (*s_abort) {
+            if (lane == 0) {
+                const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
+                for (int i = 0; i < nb && !failed; ++i) {
+                    const uint32_t* bc = p.bands + p.sched[first + i];
+                    if (ld_acquire_gpu(bc) == want) continue;
+                    if (!engine_flush(ce, s.timeout_ns, s_abort)) {
+                        *s_abort = 1;
+                        set_status(p.meta, ST_COPY_TIMEOUT, m);
                         failed = true;
                         break;
                     }
-                    if (globaltimer() - t0 > s.timeout_ns) {
-                        *s_abort = 1;
-                        set_status(p.meta, ST_FLAG_TIMEOUT, mb);
-                        failed = true;
-                        break;
+                    const unsigned long long t0 = globaltimer();
+                    for (;;) {
+                        __nanosleep(100);
+                        if (ld_acquire_gpu(bc) == want) break;
+                        if (*s_abort) {
+                            failed = true;
+                            break;
+                        }
+                        if (globaltimer() - t0 > s.timeout_ns) {
+                            *s_abort = 1;
+                            set_status(p.meta, ST_FLAG_TIMEOUT, p.sched[first + i]);
+                            failed = true;
+                            break;
+                        }
                     }
                 }
             }
             if (__any_sync(0xffffffffu, failed)) break;
+            if (lane == 0) t_acq = globaltimer();
         }
         if (lane == 0) {
             if (!did) t_first = globaltimer();
@@ -124,18 +146,28 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
             fence_proxy_async_global();
             const uint8_t* src = reinterpret_cast<const uint8_t*>(p.Yp) + (size_t)(row0 + rb) * rowb;
             uint8_t* dst = reinterpret_cast<uint8_t*>(p.Ret) + (size_t)(p.tile_ret[m] + rb) * rowb;
-            if (!engine_copy(ce, src, dst, (size_t)(re - rb) * rowb, s.timeout_ns, s_abort)) {
-                *s_abort = 1;
-                set_status(p.meta, ST_COPY_TIMEOUT, m);
+            const size_t bytes = (size_t)(re - rb) * rowb;
+            for (size_t o = 0; o < bytes; o += COPY_PIECE) {
+                const uint32_t len = (uint32_t)min((size_t)COPY_PIECE, bytes - o);
+                if (!engine_push(ce, src + o, dst + o, len, s.timeout_ns, s_abort)) {
+                    *s_abort = 1;
+                    set_status(p.meta, ST_COPY_TIMEOUT, m);
+                    break;
+                }
             }
+            t_load = globaltimer();
         }
         __syncwarp();
     }
     if (lane == 0) {
+        const unsigned long long t_drain = globaltimer();
         engine_drain(ce, s.timeout_ns);
         if (did) {
             atomicMin(&p.trace[MOE_TRACE_COPY_START], t_first);
             atomicMax(&p.trace[MOE_TRACE_COPY_END], globaltimer());
+            atomicMax(&p.trace[MOE_TRACE_LAST_LOAD], t_load);
+            atomicMax(&p.trace[MOE_TRACE_LAST_DRAIN], t_drain);
+            if (t_acq) atomicMax(&p.trace[MOE_TRACE_LAST_ACQUIRE], t_acq);
         }
     }
     __syncwarp();

@@ -325,13 +325,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     if (flags) {
                         // Publish this warp's quarter of the tile: its TMA stores must be complete
                         // (not only read out of shared memory), the async proxy fenced against the
-                        // generic one, then lane 0 adds 1 to the tile's flag with release semantics.
-                        // The tile is ready when the flag reaches 4.
+                        // generic one, then lane 0 adds 1 to the tile's flag with release semantics
+                        // (the tile is ready when it reaches 4) and 1 to its band's counter (the
+                        // band is ready at 4 x tiles per band), which is what consumers poll.
                         if (lane == 0) {
                             bulk_wait_all();
                             fence_proxy_async_global();
                             __threadfence();
                             red_release_gpu_add(p.flags + (size_t)tr.m * s.n_tiles_n2 + tr.n, 1u);
+                            const uint32_t before = atom_release_gpu_add(p.bands + tr.m, 1u);
+                            if (before + 1u == FLAG_READY * (uint32_t)s.n_tiles_n2)
+                                atomicMax(&p.trace[MOE_TRACE_BAND_DONE], globaltimer());
                         }
                         __syncwarp();
                     }
@@ -355,7 +359,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
 
     if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST))) {
-        const uint32_t want = (s.flags & MOE_TEST_STALL_CONSUMER) ? FLAG_READY + 1u : FLAG_READY;
+        const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
         copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want);
     }
 }

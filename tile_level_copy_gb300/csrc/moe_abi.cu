@@ -64,9 +64,11 @@ int make_layout(const moe_config* c, Layout* out) {
     const int nN2 = (int)(d / bn2);
     if ((int64_t)c->mgb * nN2 > GEMM_THREADS)
         return fail(MOE_ERR_ARG, "mgb * d/%d = %lld exceeds %d", bn2, (long long)c->mgb * nN2, GEMM_THREADS);
-    int64_t rpu = UNIT_BYTES / (2 * d);
-    if (rpu < 1) rpu = 1;
-    if (rpu > tbM) rpu = tbM;
+    auto rows_for = [&](int64_t bytes) {
+        int64_t r = bytes / (2 * d);
+        return r < 1 ? int64_t(1) : (r > tbM ? tbM : r);
+    };
+    const int64_t rpu = rows_for(UNIT_BYTES), rpu_tail = rows_for(TAIL_UNIT_BYTES);
 
     Layout o;
     memset(&o, 0, sizeof(o));
@@ -103,6 +105,7 @@ int make_layout(const moe_config* c, Layout* out) {
     L.ret_slot = put(TK * 4);
     L.meta = put(META_COUNT * 4);
     L.flags = put(MT_max * nN2 * 4);
+    L.bands = put(MT_max * 4);
     L.trace = put(TR_COUNT * 8);
     L.Xp = put((size_t)P_max * d * 2);
     L.Hp = put((size_t)P_max * F * 2);
@@ -130,6 +133,9 @@ int make_layout(const moe_config* c, Layout* out) {
     S.n_tiles_n2 = nN2;
     S.rows_per_unit = L.rows_per_unit;
     S.units_per_band = L.units_per_band;
+    S.rows_per_unit_tail = (int)rpu_tail;
+    S.units_per_band_tail = (int)((tbM + rpu_tail - 1) / rpu_tail);
+    S.tail_bands = (TAIL_TILES + nN2 - 1) / nN2;
     S.timeout_ns = (unsigned long long)(c->timeout_us ? c->timeout_us : 2000000u) * 1000ull;
     S.flags = c->flags;
     *out = o;
@@ -156,6 +162,7 @@ PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     p.ret_slot = reinterpret_cast<int32_t*>(b + L.ret_slot);
     p.meta = reinterpret_cast<int32_t*>(b + L.meta);
     p.flags = reinterpret_cast<uint32_t*>(b + L.flags);
+    p.bands = reinterpret_cast<uint32_t*>(b + L.bands);
     p.trace = reinterpret_cast<unsigned long long*>(b + L.trace);
     p.Xp = reinterpret_cast<__nv_bfloat16*>(b + L.Xp);
     p.Hp = reinterpret_cast<__nv_bfloat16*>(b + L.Hp);
@@ -496,7 +503,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
                  o_base = put((size_t)L.n_chunks * E * 4), o_counts = put(E * R * 4), o_ret = put(R * (E + 1) * 4),
                  o_tiles = put(MT * 16), o_tret = put(MT * 4), o_sched = put(MT * 4), o_seg = put(MT * 8),
                  o_exp = put(E * 8), o_meta = put(META_COUNT * 4), o_flags = put(MT * (size_t)L.n_tiles_n2 * 4),
-                 o_trace = put(TR_COUNT * 8);
+                 o_bands = put(MT * 4), o_trace = put(TR_COUNT * 8);
     if (cur > (size_t)MOE_STATIC_SCRATCH_BYTES)
         return fail(MOE_ERR_ARG, "this config needs %zu bytes of static scratch; the limit is %d", cur,
                     MOE_STATIC_SCRATCH_BYTES);
@@ -524,6 +531,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.ret_slot = ret_slot;
     p.meta = reinterpret_cast<int32_t*>(b + o_meta);
     p.flags = reinterpret_cast<uint32_t*>(b + o_flags);
+    p.bands = reinterpret_cast<uint32_t*>(b + o_bands);
     p.trace = reinterpret_cast<unsigned long long*>(b + o_trace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_route(S, logits, p, st);

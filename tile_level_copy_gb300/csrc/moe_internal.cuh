@@ -61,6 +61,8 @@ constexpr int COPY_WARPS = GEMM_THREADS / 32;                    // 6
 constexpr int COPY_NBUF = 2 * COPY_WARPS;                        // 12 buffers / mbarriers
 static_assert(COPY_NBUF * COPY_PIECE <= STAGES * STAGE_BYTES, "copy staging must fit the stage area");
 constexpr int UNIT_BYTES = 65536;                      // target bytes of one copy unit
+constexpr int TAIL_UNIT_BYTES = COPY_PIECE;            // units of the last bands: one piece each
+constexpr int TAIL_TILES = 320;                        // tiles of the last bands (about two waves)
 
 // ---- parameters passed by value to kernels --------------------------------------------------
 struct PlanPtrs {
@@ -81,6 +83,7 @@ struct PlanPtrs {
     int32_t* ret_slot;
     int32_t* meta;
     uint32_t* flags;
+    uint32_t* bands;
     unsigned long long* trace;
     __nv_bfloat16* Xp;
     __nv_bfloat16* Hp;
@@ -94,7 +97,9 @@ struct Shape {
     int chunk_tokens, n_chunks;
     int P_max, MT_max;
     int bn2, n_tiles_n2;            // down-projection N tile and N tiles per band
-    int rows_per_unit, units_per_band;
+    int rows_per_unit, units_per_band;           // copy units of the leading bands
+    int rows_per_unit_tail, units_per_band_tail;  // ... and of the last tail_bands bands
+    int tail_bands;
     unsigned long long timeout_ns;
     uint32_t flags;
 };
@@ -109,6 +114,28 @@ cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMa
                              const CUtensorMap& tmOut, int sms, int consumers, bool overlapped, cudaStream_t st);
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
+
+// Copy units of a call with MT bands: the last min(tail_bands, MT) bands in schedule order are cut
+// into smaller units than the others, so the copy after the last tile spreads over more engines.
+__host__ __device__ inline int copy_unit_count(const Shape& s, int MT) {
+    const int tb = MT < s.tail_bands ? MT : s.tail_bands;
+    return (MT - tb) * s.units_per_band + tb * s.units_per_band_tail;
+}
+// Unit u -> (schedule position, first row within the band, rows per unit of that band).
+__host__ __device__ inline void copy_unit_decode(const Shape& s, int MT, int u, int* pos, int* rb, int* rpu) {
+    const int tb = MT < s.tail_bands ? MT : s.tail_bands;
+    const int lead = (MT - tb) * s.units_per_band;
+    if (u < lead) {
+        *pos = u / s.units_per_band;
+        *rb = (u - *pos * s.units_per_band) * s.rows_per_unit;
+        *rpu = s.rows_per_unit;
+    } else {
+        const int v = u - lead, q = v / s.units_per_band_tail;
+        *pos = (MT - tb) + q;
+        *rb = (v - q * s.units_per_band_tail) * s.rows_per_unit_tail;
+        *rpu = s.rows_per_unit_tail;
+    }
+}
 
 // ============================================================================================
 // Device primitives
@@ -232,6 +259,11 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
 }
 __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_release_gpu_add(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;

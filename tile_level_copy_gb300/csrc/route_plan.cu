@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     if (tid == 0) {
         p.meta[META_P] = P;
         p.meta[META_MTILES] = MT;
-        p.meta[META_UNITS] = MT * s.units_per_band;
+        p.meta[META_UNITS] = copy_unit_count(s, MT);
         p.meta[META_QUEUE] = 0;
         p.meta[META_QUEUE_SEQ] = 0;
         p.meta[META_STATUS] = (P > s.P_max) ? ST_BAD_PLAN : 0;
@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     if (tid < TR_COUNT) p.trace[tid] = (tid == MOE_TRACE_GEMM2_START || tid == MOE_TRACE_COPY_START) ? ~0ull : 0ull;
     const int nflags = min(MT, s.MT_max) * s.n_tiles_n2;
     for (int i = tid; i < nflags; i += PLAN_THREADS) p.flags[i] = 0u;
+    for (int i = tid; i < min(MT, s.MT_max); i += PLAN_THREADS) p.bands[i] = 0u;
 }
 
 cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
