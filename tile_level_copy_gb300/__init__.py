@@ -165,7 +165,7 @@ class Workspace:
            "slot": (torch.int32, "TK"), "ret_slot": (torch.int32, "TK"), "counts": (torch.int32, "ER"),
            "offsets": (torch.int32, "G1"), "ret_off": (torch.int32, "RE1"), "tiles": (torch.int32, "MT4"),
            "tile_ret": (torch.int32, "MT"), "sched": (torch.int32, "MT"), "seg": (torch.int32, "MT2"),
-           "experts": (torch.int32, "E2"), "meta": (torch.int32, "META"), "flags": (torch.int32, "FL"),
+           "experts": (torch.int32, "E4"), "meta": (torch.int32, "META"), "flags": (torch.int32, "FL"),
            "bands": (torch.int32, "MT"),
            "trace": (torch.int64, "TR"), "Xp": (torch.bfloat16, "Pd"), "Hp": (torch.bfloat16, "PF"),
            "Yp": (torch.bfloat16, "Pd"), "Ret": (torch.bfloat16, "TKd")}
@@ -181,7 +181,7 @@ class Workspace:
         dt, kind = self._DT[name]
         TK = c.T * c.topk
         shape = {"TK": (c.T, c.topk), "ER": (c.E, c.R), "G1": (c.E * c.R + 1,), "RE1": (c.R, c.E + 1),
-                 "MT4": (L["MT_max"], 4), "MT": (L["MT_max"],), "MT2": (L["MT_max"], 2), "E2": (c.E, 2),
+                 "MT4": (L["MT_max"], 4), "MT": (L["MT_max"],), "MT2": (L["MT_max"], 2), "E4": (c.E, 4),
                  "META": (64,), "FL": (L["MT_max"], L["n_tiles_n2"]), "TR": (16,), "Pd": (L["P_max"], c.d),
                  "PF": (L["P_max"], c.ffn), "TKd": (TK, c.d)}[kind]
         n = 1

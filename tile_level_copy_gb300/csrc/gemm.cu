@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     if (MODE == 1) {
         for (int e = tid; e < s.E; e += GEMM_THREADS) {
-            sm.tab[(s.E + 1) + e] = p.experts[2 * e + 0];
-            sm.tab[(s.E + 1) + s.E + e] = p.experts[2 * e + 1];
+            sm.tab[(s.E + 1) + e] = p.experts[4 * e + 0];
+            sm.tab[(s.E + 1) + s.E + e] = p.experts[4 * e + 1];
         }
         __syncthreads();
         if (tid == 0) {

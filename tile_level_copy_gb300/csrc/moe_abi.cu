@@ -100,7 +100,7 @@ int make_layout(const moe_config* c, Layout* out) {
     L.tile_ret = put(MT_max * 4);
     L.sched = put(MT_max * 4);
     L.seg = put(MT_max * 8);
-    L.experts = put(E * 8);
+    L.experts = put(E * 16);
     L.slot = put(TK * 4);
     L.ret_slot = put(TK * 4);
     L.meta = put(META_COUNT * 4);
@@ -502,7 +502,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     const size_t o_rank = put(TK * 4), o_cnt = put((size_t)L.n_chunks * E * 4),
                  o_base = put((size_t)L.n_chunks * E * 4), o_counts = put(E * R * 4), o_ret = put(R * (E + 1) * 4),
                  o_tiles = put(MT * 16), o_tret = put(MT * 4), o_sched = put(MT * 4), o_seg = put(MT * 8),
-                 o_exp = put(E * 8), o_meta = put(META_COUNT * 4), o_flags = put(MT * (size_t)L.n_tiles_n2 * 4),
+                 o_exp = put(E * 16), o_meta = put(META_COUNT * 4), o_flags = put(MT * (size_t)L.n_tiles_n2 * 4),
                  o_bands = put(MT * 4), o_trace = put(TR_COUNT * 8);
     if (cur > (size_t)MOE_STATIC_SCRATCH_BYTES)
         return fail(MOE_ERR_ARG, "this config needs %zu bytes of static scratch; the limit is %d", cur,

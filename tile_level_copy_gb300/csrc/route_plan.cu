@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         s_load[e] = load;
         s_fb[e] = fb;
         s_mt[e] = (s_off[(e + 1) * R] - s_off[e * R]) / tbM;
-        p.experts[2 * e + 0] = s_off[e * R] / tbM;
-        p.experts[2 * e + 1] = s_mt[e];
+        p.experts[4 * e + 0] = s_off[e * R] / tbM;
+        p.experts[4 * e + 1] = s_mt[e];
     }
     __syncthreads();
     for (int e = tid; e < E; e += PLAN_THREADS) {
@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         for (int f = 0; f < E; ++f)
             if (s_erank[f] < s_erank[e]) base += s_mt[f];
         s_ebase[e] = base;
+        p.experts[4 * e + 2] = base;        // first schedule position of the expert's bands
+        p.experts[4 * e + 3] = s_erank[e];  // the expert's rank in schedule order
     }
     __syncthreads();
 
