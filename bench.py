@@ -235,13 +235,16 @@ def run_ours(args, rank: int, world: int):
                        tlc.TRACE_COPY_END)])
     ms_ovl, ms_seq = sec_ovl * 1e3 / K, sec_seq * 1e3 / K
 
-    # GEMM numbers: real rows = T*k; executed rows = P (padded)
-    P = int(ws.view("meta")[0].item())
+    # GEMM numbers: real rows = T*k; executed rows = 128 per work item (a band, or two bands that
+    # need at most 64 rows each); P = padded rows of the layout
+    meta = ws.view("meta").cpu()
+    P, items = int(meta[0].item()), int(meta[7].item())
     TK = w.T * w.topk
+    exec_rows = 128 * items
     up_ms = float(np.median(st_ovl[:, tlc.EV_PLANNED]))
     down_ms = float(np.median(st_seq[:, tlc.EV_UP]))
     fl_up_alg, fl_down_alg = 4.0 * TK * w.d * w.ffn, 2.0 * TK * w.d * w.ffn
-    fl_up_exe, fl_down_exe = 4.0 * P * w.d * w.ffn, 2.0 * P * w.d * w.ffn
+    fl_up_exe, fl_down_exe = 4.0 * exec_rows * w.d * w.ffn, 2.0 * exec_rows * w.d * w.ffn
     gemm_exec_tflops = (fl_up_exe + fl_down_exe) / ((up_ms + down_ms) * 1e-3) / 1e12
     gemm_alg_tflops = (fl_up_alg + fl_down_alg) / ((up_ms + down_ms) * 1e-3) / 1e12
     peak_tc = peaks["bf16_tflops_sustained"]
@@ -262,7 +265,8 @@ def run_ours(args, rank: int, world: int):
                    "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "mgb": args.mgb,
                    "tail_assist": not args.no_tail_assist, "seed": args.seed,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "l2": "no flush: each step streams 2.8 GB of weights and a 0.35 GB hidden buffer (> 129 MB L2)"},
+                   "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "
+                      f"(> 129 MB L2)"},
         "gpu_launches": 6 * K,
         "clocks": clocks,
         "roofline": roofline,
@@ -271,7 +275,8 @@ def run_ours(args, rank: int, world: int):
                  "algorithmic_frac_of_peak": round(gemm_alg_tflops / peak_tc, 4),
                  "executed_frac_of_burst_peak": round(gemm_exec_tflops / peaks["bf16_tflops"], 4),
                  "peak_tflops": peak_tc, "peak_source": peaks_src, "up_ms": round(up_ms, 4),
-                 "down_ms": round(down_ms, 4), "padded_rows": P, "real_rows": TK},
+                 "down_ms": round(down_ms, 4), "padded_rows": P, "executed_rows": exec_rows, "work_items": items,
+                 "real_rows": TK},
         "overlap": {"hidden_pct": round(100 * statistics.median(hidden), 2),
                     "tail_ms": round(statistics.median(tails), 4), "copy_alone_ms": round(copy_alone_ms, 4),
                     "tail_marks_us": dict(zip(["band_done", "last_acquire", "last_load", "last_drain", "copy_end"],

@@ -102,8 +102,10 @@ typedef struct moe_layout {
     size_t tile_ret;   /* int32 [MT_max]    row of Ret receiving the tile's first row          */
     size_t sched;      /* int32 [MT_max]    M-tile at each schedule position                   */
     size_t seg;        /* int32 [MT_max, 2] (first position, bands) of each position's segment */
-    size_t experts;    /* int32 [E, 4]      first M-tile, M-tiles, first schedule position and */
-                       /*                   schedule rank of each expert                       */
+    size_t experts;    /* int32 [E, 8]      first M-tile, M-tiles, first schedule position,    */
+                       /*                   schedule rank, work items, first item of each list */
+    size_t items_up;   /* int32 [MT_max, 2] GEMM work items (one band, or two bands of <= 64   */
+    size_t items_down; /* int32 [MT_max, 2] rows) of the SwiGLU GEMM / the down-projection     */
     size_t slot;       /* int32 [T, topk]   row of pair (t, j) in Xp / Yp                      */
     size_t ret_slot;   /* int32 [T, topk]   row of pair (t, j) in Ret                          */
     size_t meta;       /* int32 [64]        P, M-tiles, work counters, status (see csrc)       */

@@ -104,3 +104,33 @@ def test_plan_skip_permute_leaves_xp_untouched():
     ref_idx, _ = moe_ref.route_topk(inputs.make_logits(w, 0), w.topk)
     plan = moe_ref.build_plan(ref_idx, w.E, w.R, w.tile_M)
     np.testing.assert_array_equal(ws.view("slot").cpu().numpy(), plan.slot)
+
+
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "skew", "fine"])
+def test_work_items_cover_every_band_once(name):
+    """GEMM work items: every band in exactly one item of each list; a shared item holds two bands
+    of the same expert that each need at most 64 rows; the down-projection list follows the
+    schedule."""
+    w = inputs.WORKLOADS[name]
+    cfg, ws, _, _ = run_plan(w, inputs.make_logits(w, 0), None, skip_permute=True)
+    meta = ws.view("meta").cpu().numpy()
+    MT, NI = int(meta[1]), int(meta[7])
+    tiles = ws.view("tiles").cpu().numpy()[:MT]
+    sched = ws.view("sched").cpu().numpy()[:MT]
+    for name_ in ("items_up", "items_down"):
+        items = ws.view(name_).cpu().numpy()[:NI]
+        seen = []
+        for a, b in items.tolist():
+            seen.append(a)
+            if b == a:
+                assert w.tile_M == 128
+            elif b == -1:
+                assert w.tile_M == 64 and tiles[a, 3] <= 64
+            else:
+                seen.append(b)
+                assert tiles[a, 0] == tiles[b, 0] and tiles[a, 3] <= 64 and tiles[b, 3] <= 64
+        assert sorted(seen) == list(range(MT))
+        if name_ == "items_down":
+            assert seen == sched.tolist()
+    # two half bands cut the GEMM work wherever partial bands are small
+    assert NI <= MT and (w.tile_M == 128 or NI == (MT + 1) // 2 or NI < MT)

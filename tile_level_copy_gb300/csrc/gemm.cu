@@ -57,13 +57,29 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
     return sm;
 }
 
+// One GEMM tile: work item (mA, mB) x N tile n of expert e. Rows 0-63 of the UMMA tile come from
+// row rowA on, rows 64-127 from row rowB on (rowB = rowA + 64 when the item is a single band).
+// mB == mA: one band of 128 rows; mB == -1: one band of 64 rows alone; otherwise two half bands.
 struct TileRef {
-    int m, n, e, row0;
+    int mA, mB, n, e, rowA, rowB;
 };
 
-// SwiGLU GEMM order: expert-major; inside an expert, N tiles outer and M tiles inner, so the CTAs
-// working at the same time share each weight tile through L2.
-__device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, int nN, const int32_t* tiles) {
+__device__ __forceinline__ TileRef make_ref(int mA, int mB, int n, const int32_t* tiles) {
+    TileRef r;
+    r.mA = mA;
+    r.mB = mB;
+    r.n = n;
+    r.e = tiles[4 * mA + 0];
+    r.rowA = tiles[4 * mA + 2];
+    r.rowB = (mB >= 0 && mB != mA) ? tiles[4 * mB + 2] : r.rowA + 64;
+    return r;
+}
+
+// SwiGLU GEMM order: expert-major; inside an expert, N tiles outer and work items inner, so the
+// CTAs working at the same time share each weight tile through L2.
+// tab = [cum (E+1) | first item (E) | items (E)]
+__device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, const int32_t* items,
+                                             const int32_t* tiles) {
     const int* cum = tab;
     const int* first = tab + (E + 1);
     const int* count = first + E;
@@ -73,24 +89,14 @@ __device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, int n
         if (cum[mid] <= t) lo = mid; else hi = mid - 1;
     }
     const int e = lo, local = t - cum[e], cnt = count[e];
-    TileRef r;
-    r.n = local / cnt;
-    r.m = first[e] + local % cnt;
-    r.e = e;
-    r.row0 = tiles[4 * r.m + 2];
-    (void)nN;
-    return r;
+    const int n = local / cnt, it = first[e] + local % cnt;
+    return make_ref(items[2 * it], items[2 * it + 1], n, tiles);
 }
 
-// Down-projection order: schedule positions (remote-first), all N tiles of a band together.
-__device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* sched, const int32_t* tiles) {
-    TileRef r;
-    const int pos = t / nN;
-    r.n = t - pos * nN;
-    r.m = sched[pos];
-    r.e = tiles[4 * r.m + 0];
-    r.row0 = tiles[4 * r.m + 2];
-    return r;
+// Down-projection order: work items in schedule (remote-first) order, all N tiles of an item together.
+__device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* items, const int32_t* tiles) {
+    const int it = t / nN;
+    return make_ref(items[2 * it], items[2 * it + 1], t - it * nN, tiles);
 }
 
 template <int MODE>  // 1: SwiGLU up-projection -> Hp; 2: down-projection -> Yp (+ flags / consumer)
@@ -103,12 +109,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const bool producer = (int)blockIdx.x < num_producers;
 
-    int MT = p.meta[META_MTILES];
-    if (MT < 0 || MT > s.MT_max) MT = 0;
+    int MT = p.meta[META_MTILES], NI = p.meta[META_ITEMS];
+    if (MT < 0 || MT > s.MT_max || NI < 0 || NI > MT) MT = NI = 0;
     const int nN = (MODE == 1) ? s.ffn / BN1 : s.n_tiles_n2;
     const int BN = (MODE == 1) ? 2 * BN1 : s.bn2;  // UMMA N
     const int KB = ((MODE == 1) ? s.d : s.ffn) / BK;
-    const int total = MT * nN;
+    const int total = NI * nN;
     const uint32_t tx_bytes = A_STAGE_BYTES + BN * BK * 2;
     const unsigned long long tmo = s.timeout_ns;
 
@@ -128,8 +134,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     if (MODE == 1) {
         for (int e = tid; e < s.E; e += GEMM_THREADS) {
-            sm.tab[(s.E + 1) + e] = p.experts[4 * e + 0];
-            sm.tab[(s.E + 1) + s.E + e] = p.experts[4 * e + 1];
+            sm.tab[(s.E + 1) + e] = p.experts[8 * e + 5];         // first work item
+            sm.tab[(s.E + 1) + s.E + e] = p.experts[8 * e + 4];   // work items
         }
         __syncthreads();
         if (tid == 0) {
@@ -165,8 +171,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint32_t ph = 0, issued = 0, last_ph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += num_producers) {
-                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, nN, p.tiles)
-                                               : decode_down(t, nN, p.sched, p.tiles);
+                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up, p.tiles)
+                                               : decode_down(t, nN, p.items_down, p.tiles);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
                         ok = false;
@@ -175,7 +181,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     mbar_arrive_expect_tx(&sm.full[st], tx_bytes);
                     uint8_t* a = sm.stages + st * STAGE_BYTES;
                     uint8_t* b = a + A_STAGE_BYTES;
-                    tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.row0);
+                    tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.rowA);
+                    tma_load_2d(a + A_STAGE_BYTES / 2, &tmA, &sm.full[st], kb * BK, tr.rowB);
                     if (MODE == 1) {
                         tma_load_3d(b, &tmB0, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
                         tma_load_3d(b + BN1 * BK * 2, &tmB1, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
@@ -250,7 +257,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // 16-byte pieces in a lane-rotated order, free of bank conflicts), then lane 0 issues one
             // TMA tensor store of the chunk. Two staging buffers per warp alternate.
             const int q = warp & 3;  // TMEM lane quarter this warp may access
-            const bool active = q * 32 < s.tbM;  // rows of this warp lie inside the tile
             const bool flags = (MODE == 2) && overlapped;
             uint8_t* ebuf = sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES;
             int eb = 0;
@@ -277,8 +283,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 eb ^= 1;
             };
             for (int t = blockIdx.x; t < total; t += num_producers) {
-                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, nN, p.tiles)
-                                               : decode_down(t, nN, p.sched, p.tiles);
+                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up, p.tiles)
+                                               : decode_down(t, nN, p.items_down, p.tiles);
                 if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
                     if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 2);
                     *sm.abort = 1;
@@ -286,7 +292,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
-                const int y = tr.row0 + q * 32;
+                // rows 0-63 belong to band mA, rows 64-127 to band mB (or to mA for a 128-row band)
+                const int mq = (q < 2) ? tr.mA : tr.mB;
+                const bool active = mq >= 0;
+                const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
+                const uint32_t inc = (tr.mB == tr.mA) ? 1u : 2u;  // quarters per band: 4 in all
                 if (MODE == 1) {
 #pragma unroll 1
                     for (int c = 0; c < BN1 / 32; ++c) {
@@ -321,20 +331,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
                 tc_fence_before();
                 mbar_arrive(&sm.acc_empty[b]);
-                if (MODE == 2) {
+                if (MODE == 2 && active) {
                     if (flags) {
-                        // Publish this warp's quarter of the tile: its TMA stores must be complete
-                        // (not only read out of shared memory), the async proxy fenced against the
-                        // generic one, then lane 0 adds 1 to the tile's flag with release semantics
-                        // (the tile is ready when it reaches 4) and 1 to its band's counter (the
-                        // band is ready at 4 x tiles per band), which is what consumers poll.
+                        // Publish this warp's rows of the tile: its TMA stores must be complete (not
+                        // only read out of shared memory), the async proxy fenced against the generic
+                        // one, then lane 0 adds its share (1 for a quarter of a 128-row band, 2 for
+                        // half of a 64-row one) to the tile's flag with release semantics (the tile
+                        // is ready at 4) and to its band's counter (the band is ready at 4 x tiles
+                        // per band), which is what consumers poll.
                         if (lane == 0) {
                             bulk_wait_all();
                             fence_proxy_async_global();
                             __threadfence();
-                            red_release_gpu_add(p.flags + (size_t)tr.m * s.n_tiles_n2 + tr.n, 1u);
-                            const uint32_t before = atom_release_gpu_add(p.bands + tr.m, 1u);
-                            if (before + 1u == FLAG_READY * (uint32_t)s.n_tiles_n2)
+                            red_release_gpu_add(p.flags + (size_t)mq * s.n_tiles_n2 + tr.n, inc);
+                            const uint32_t before = atom_release_gpu_add(p.bands + mq, inc);
+                            if (before + inc == FLAG_READY * (uint32_t)s.n_tiles_n2)
                                 atomicMax(&p.trace[MOE_TRACE_BAND_DONE], globaltimer());
                         }
                         __syncwarp();

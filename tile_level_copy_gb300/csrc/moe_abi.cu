@@ -100,7 +100,9 @@ int make_layout(const moe_config* c, Layout* out) {
     L.tile_ret = put(MT_max * 4);
     L.sched = put(MT_max * 4);
     L.seg = put(MT_max * 8);
-    L.experts = put(E * 16);
+    L.experts = put(E * 32);
+    L.items_up = put(MT_max * 8);
+    L.items_down = put(MT_max * 8);
     L.slot = put(TK * 4);
     L.ret_slot = put(TK * 4);
     L.meta = put(META_COUNT * 4);
@@ -158,6 +160,8 @@ PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     p.sched = reinterpret_cast<int32_t*>(b + L.sched);
     p.seg = reinterpret_cast<int32_t*>(b + L.seg);
     p.experts = reinterpret_cast<int32_t*>(b + L.experts);
+    p.items_up = reinterpret_cast<int32_t*>(b + L.items_up);
+    p.items_down = reinterpret_cast<int32_t*>(b + L.items_down);
     p.slot = reinterpret_cast<int32_t*>(b + L.slot);
     p.ret_slot = reinterpret_cast<int32_t*>(b + L.ret_slot);
     p.meta = reinterpret_cast<int32_t*>(b + L.meta);
@@ -283,8 +287,8 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
         return fail(MOE_ERR_ARG, "consumer_ctas=%d must be in [1, %d]", c.consumers, c.di.sms / 2);
 
     CUtensorMap tXp, tHp, tW1, tW3, tW2, tHpOut, tYpOut;
-    int rc = make_map(&tXp, c.p.Xp, 2, S.d, S.P_max, 1, BM, "Xp");
-    if (!rc) rc = make_map(&tHp, c.p.Hp, 2, S.ffn, S.P_max, 1, BM, "Hp");
+    int rc = make_map(&tXp, c.p.Xp, 2, S.d, S.P_max, 1, BM / 2, "Xp");  // A: two 64-row boxes per stage
+    if (!rc) rc = make_map(&tHp, c.p.Hp, 2, S.ffn, S.P_max, 1, BM / 2, "Hp");
     if (!rc) rc = make_map(&tHpOut, c.p.Hp, 2, S.ffn, S.P_max, 1, 32, "Hp (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tYpOut, c.p.Yp, 2, S.d, S.P_max, 1, 32, "Yp (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tW1, W1, 3, S.d, S.ffn, S.E, BN1, "W1");
@@ -502,7 +506,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     const size_t o_rank = put(TK * 4), o_cnt = put((size_t)L.n_chunks * E * 4),
                  o_base = put((size_t)L.n_chunks * E * 4), o_counts = put(E * R * 4), o_ret = put(R * (E + 1) * 4),
                  o_tiles = put(MT * 16), o_tret = put(MT * 4), o_sched = put(MT * 4), o_seg = put(MT * 8),
-                 o_exp = put(E * 16), o_meta = put(META_COUNT * 4), o_flags = put(MT * (size_t)L.n_tiles_n2 * 4),
+                 o_exp = put(E * 32), o_iu = put(MT * 8), o_id = put(MT * 8), o_meta = put(META_COUNT * 4), o_flags = put(MT * (size_t)L.n_tiles_n2 * 4),
                  o_bands = put(MT * 4), o_trace = put(TR_COUNT * 8);
     if (cur > (size_t)MOE_STATIC_SCRATCH_BYTES)
         return fail(MOE_ERR_ARG, "this config needs %zu bytes of static scratch; the limit is %d", cur,
@@ -527,6 +531,8 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.sched = reinterpret_cast<int32_t*>(b + o_sched);
     p.seg = reinterpret_cast<int32_t*>(b + o_seg);
     p.experts = reinterpret_cast<int32_t*>(b + o_exp);
+    p.items_up = reinterpret_cast<int32_t*>(b + o_iu);
+    p.items_down = reinterpret_cast<int32_t*>(b + o_id);
     p.slot = slot;
     p.ret_slot = ret_slot;
     p.meta = reinterpret_cast<int32_t*>(b + o_meta);

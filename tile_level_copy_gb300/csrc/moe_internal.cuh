@@ -21,6 +21,7 @@ enum Meta : int {
     META_QUEUE_SEQ = 4,    // next copy unit to hand out (sequential copy)
     META_STATUS = 5,       // 0 or a Status code (first error wins)
     META_STATUS_DETAIL = 6,
+    META_ITEMS = 7,        // GEMM work items (one band, or two bands of <= 64 rows)
     META_COUNT = 64,
 };
 
@@ -78,7 +79,10 @@ struct PlanPtrs {
     int32_t* tile_ret;
     int32_t* sched;
     int32_t* seg;        // [MT_max][2]
-    int32_t* experts;    // [E][2]
+    int32_t* experts;    // [E][8]: first M-tile, M-tiles, first schedule position, schedule rank,
+                         //         work items, first item (id-order list), first item (schedule list)
+    int32_t* items_up;   // [MT_max][2] work items of the SwiGLU GEMM, experts in id order
+    int32_t* items_down; // [MT_max][2] work items of the down-projection, in schedule order
     int32_t* slot;
     int32_t* ret_slot;
     int32_t* meta;

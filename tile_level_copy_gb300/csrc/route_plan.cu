@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         s_load[e] = load;
         s_fb[e] = fb;
         s_mt[e] = (s_off[(e + 1) * R] - s_off[e * R]) / tbM;
-        p.experts[4 * e + 0] = s_off[e * R] / tbM;
-        p.experts[4 * e + 1] = s_mt[e];
+        p.experts[8 * e + 0] = s_off[e * R] / tbM;
+        p.experts[8 * e + 1] = s_mt[e];
     }
     __syncthreads();
     for (int e = tid; e < E; e += PLAN_THREADS) {
@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         for (int f = 0; f < E; ++f)
             if (s_erank[f] < s_erank[e]) base += s_mt[f];
         s_ebase[e] = base;
-        p.experts[4 * e + 2] = base;        // first schedule position of the expert's bands
-        p.experts[4 * e + 3] = s_erank[e];  // the expert's rank in schedule order
+        p.experts[8 * e + 2] = base;        // first schedule position of the expert's bands
+        p.experts[8 * e + 3] = s_erank[e];  // the expert's rank in schedule order
     }
     __syncthreads();
 
@@ -277,11 +277,67 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         p.seg[2 * q + 1] = min(s.mgb, end - first);
     }
 
-    // 7. per-call meta, flags and trace reset
+    // 7. GEMM work items. A UMMA tile has 128 rows; a band that needs only 64 of them (every band
+    // when tbM = 64, a band with <= 64 valid rows when tbM = 128) shares a work item with another
+    // such band of the same expert: each is loaded as a 64-row box into one half of the A tile.
+    // Item (mA, mB): mB == mA one 128-row band; mB == -1 one 64-row band alone; else two half bands.
+    __shared__ int s_items[MAX_E], s_ibase_up[MAX_E], s_ibase_down[MAX_E];
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        const int m0 = s_off[e * R] / tbM, cnt = s_mt[e];
+        int half = 0;
+        for (int i = 0; i < cnt; ++i) half += (p.tiles[4 * (m0 + i) + 3] <= 64);
+        s_items[e] = (cnt - half) + (half + 1) / 2;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        int up = 0, down = 0;
+        for (int f = 0; f < E; ++f) {
+            up += (f < e) ? s_items[f] : 0;
+            down += (s_erank[f] < s_erank[e]) ? s_items[f] : 0;
+        }
+        s_ibase_up[e] = up;
+        s_ibase_down[e] = down;
+        p.experts[8 * e + 4] = s_items[e];
+        p.experts[8 * e + 5] = up;
+        p.experts[8 * e + 6] = down;
+        p.experts[8 * e + 7] = 0;
+    }
+    __syncthreads();
+    for (int e = tid; e < 2 * E; e += PLAN_THREADS) {  // thread pairs: (expert, list)
+        const int x = e >> 1;
+        const bool down = e & 1;
+        const int cnt = s_mt[x];
+        int* out = (down ? p.items_down : p.items_up) + 2 * (down ? s_ibase_down[x] : s_ibase_up[x]);
+        int n = 0, pending = -1;
+        for (int i = 0; i < cnt; ++i) {
+            const int m = down ? p.sched[s_ebase[x] + i] : s_off[x * R] / tbM + i;
+            if (p.tiles[4 * m + 3] > 64) {
+                out[2 * n] = m;
+                out[2 * n + 1] = m;
+                ++n;
+            } else if (pending < 0) {
+                pending = m;
+            } else {
+                out[2 * n] = pending;
+                out[2 * n + 1] = m;
+                ++n;
+                pending = -1;
+            }
+        }
+        if (pending >= 0) {
+            out[2 * n] = pending;
+            out[2 * n + 1] = tbM == 64 ? -1 : pending;
+        }
+    }
+
+    // 8. per-call meta, flags and trace reset
     if (tid == 0) {
         p.meta[META_P] = P;
         p.meta[META_MTILES] = MT;
         p.meta[META_UNITS] = copy_unit_count(s, MT);
+        int items = 0;
+        for (int e = 0; e < E; ++e) items += s_items[e];
+        p.meta[META_ITEMS] = items;
         p.meta[META_QUEUE] = 0;
         p.meta[META_QUEUE_SEQ] = 0;
         p.meta[META_STATUS] = (P > s.P_max) ? ST_BAD_PLAN : 0;
