@@ -101,9 +101,9 @@ __device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* ite
 
 template <int MODE>  // 1: SwiGLU up-projection -> Hp; 2: down-projection -> Yp (+ flags / consumer)
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut, int num_producers,
-                int overlapped) {
+    gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAh,
+                const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                const __grid_constant__ CUtensorMap tmOut, int num_producers, int overlapped) {
     extern __shared__ uint8_t smem_raw[];
     Smem sm = carve_smem(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     if (producer && tid == 0) {
         tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmAh);
         tma_prefetch_desc(&tmB0);
         tma_prefetch_desc(&tmOut);
         if (MODE == 1) tma_prefetch_desc(&tmB1);
@@ -181,8 +182,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     mbar_arrive_expect_tx(&sm.full[st], tx_bytes);
                     uint8_t* a = sm.stages + st * STAGE_BYTES;
                     uint8_t* b = a + A_STAGE_BYTES;
-                    tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.rowA);
-                    tma_load_2d(a + A_STAGE_BYTES / 2, &tmA, &sm.full[st], kb * BK, tr.rowB);
+                    if (tr.mB >= 0 && tr.mB != tr.mA) {  // two half bands: two 64-row boxes
+                        tma_load_2d(a, &tmAh, &sm.full[st], kb * BK, tr.rowA);
+                        tma_load_2d(a + A_STAGE_BYTES / 2, &tmAh, &sm.full[st], kb * BK, tr.rowB);
+                    } else {
+                        tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.rowA);
+                    }
                     if (MODE == 1) {
                         tma_load_3d(b, &tmB0, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
                         tma_load_3d(b + BN1 * BK * 2, &tmB1, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
@@ -379,30 +384,32 @@ static cudaError_t set_smem_attr(const void* fn) {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
 }
 
-cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW1,
-                               const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms, cudaStream_t st) {
+cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
+                               const CUtensorMap& tmW1, const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms,
+                               cudaStream_t st) {
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<1>));
     if (e != cudaSuccess) return e;
-    gemm_kernel<1><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(s, p, tmA, tmW1, tmW3, tmOut, sms, 0);
+    gemm_kernel<1><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(s, p, tmA, tmAh, tmW1, tmW3, tmOut, sms, 0);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2,
-                             const CUtensorMap& tmOut, int sms, int consumers, bool overlapped, cudaStream_t st) {
+cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
+                             const CUtensorMap& tmW2, const CUtensorMap& tmOut, int sms, int consumers, bool overlapped,
+                             cudaStream_t st) {
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<2>));
     if (e != cudaSuccess) return e;
     const int producers = overlapped ? sms - consumers : sms;
     int ov = overlapped ? 1 : 0;
     Shape sa = s;
     PlanPtrs pa = p;
-    CUtensorMap a = tmA, b0 = tmW2, b1 = tmW2, o = tmOut;
+    CUtensorMap a = tmA, ah = tmAh, b0 = tmW2, b1 = tmW2, o = tmOut;
     if (!overlapped) {
-        gemm_kernel<2><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(sa, pa, a, b0, b1, o, producers, ov);
+        gemm_kernel<2><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(sa, pa, a, ah, b0, b1, o, producers, ov);
         return cudaGetLastError();
     }
     // Cooperative launch: every CTA (producers and consumers) is resident at once, or the launch
     // fails; the consumers' waits on producer flags can therefore always be satisfied.
-    void* args[] = {&sa, &pa, &a, &b0, &b1, &o, (void*)&producers, &ov};
+    void* args[] = {&sa, &pa, &a, &ah, &b0, &b1, &o, (void*)&producers, &ov};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&gemm_kernel<2>), dim3(sms), dim3(GEMM_THREADS),
                                        args, GEMM_SMEM, st);
 }

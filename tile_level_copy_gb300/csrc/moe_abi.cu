@@ -286,9 +286,11 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     if (overlapped && (c.consumers < 1 || c.consumers > c.di.sms / 2))
         return fail(MOE_ERR_ARG, "consumer_ctas=%d must be in [1, %d]", c.consumers, c.di.sms / 2);
 
-    CUtensorMap tXp, tHp, tW1, tW3, tW2, tHpOut, tYpOut;
-    int rc = make_map(&tXp, c.p.Xp, 2, S.d, S.P_max, 1, BM / 2, "Xp");  // A: two 64-row boxes per stage
-    if (!rc) rc = make_map(&tHp, c.p.Hp, 2, S.ffn, S.P_max, 1, BM / 2, "Hp");
+    CUtensorMap tXp, tXph, tHp, tHph, tW1, tW3, tW2, tHpOut, tYpOut;
+    int rc = make_map(&tXp, c.p.Xp, 2, S.d, S.P_max, 1, BM, "Xp");
+    if (!rc) rc = make_map(&tXph, c.p.Xp, 2, S.d, S.P_max, 1, BM / 2, "Xp (half)");
+    if (!rc) rc = make_map(&tHp, c.p.Hp, 2, S.ffn, S.P_max, 1, BM, "Hp");
+    if (!rc) rc = make_map(&tHph, c.p.Hp, 2, S.ffn, S.P_max, 1, BM / 2, "Hp (half)");
     if (!rc) rc = make_map(&tHpOut, c.p.Hp, 2, S.ffn, S.P_max, 1, 32, "Hp (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tYpOut, c.p.Yp, 2, S.d, S.P_max, 1, 32, "Yp (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tW1, W1, 3, S.d, S.ffn, S.E, BN1, "W1");
@@ -301,15 +303,15 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     rc = run_plan(c, logits, x, true);
     if (rc) return rc;
     if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
-    cudaError_t e = launch_gemm_swiglu(S, c.p, tXp, tW1, tW3, tHpOut, c.di.sms, c.st);
+    cudaError_t e = launch_gemm_swiglu(S, c.p, tXp, tXph, tW1, tW3, tHpOut, c.di.sms, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
     if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
     if (overlapped) {
-        e = launch_gemm_down(S, c.p, tHp, tW2, tYpOut, c.di.sms, c.consumers, true, c.st);
+        e = launch_gemm_down(S, c.p, tHp, tHph, tW2, tYpOut, c.di.sms, c.consumers, true, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "overlapped down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
     } else {
-        e = launch_gemm_down(S, c.p, tHp, tW2, tYpOut, c.di.sms, 0, false, c.st);
+        e = launch_gemm_down(S, c.p, tHp, tHph, tW2, tYpOut, c.di.sms, 0, false, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
         e = launch_copy_seq(S, c.p, c.di.sms, c.st);

@@ -112,10 +112,13 @@ struct Shape {
 cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p, cudaStream_t st);
 cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st);
 cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtrs& p, int sms, cudaStream_t st);
-cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW1,
-                               const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms, cudaStream_t st);
-cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2,
-                             const CUtensorMap& tmOut, int sms, int consumers, bool overlapped, cudaStream_t st);
+// tmA: 128-row boxes of the token rows; tmAh: 64-row boxes of the same tensor (shared work items)
+cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
+                               const CUtensorMap& tmW1, const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms,
+                               cudaStream_t st);
+cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
+                             const CUtensorMap& tmW2, const CUtensorMap& tmOut, int sms, int consumers, bool overlapped,
+                             cudaStream_t st);
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
 
