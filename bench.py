@@ -35,9 +35,11 @@ from tile_level_copy_gb300 import inputs  # noqa: E402
 METRIC = "MoE-layer tokens/s; grouped-GEMM % of BF16 peak; return-copy overlap %"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# Consumer partition per workload: enough copy engines to keep up with the down-projection's
-# output rate (the fine-grained layer returns 6 rows per token over a short GEMM).
-DEFAULT_CONSUMERS = {"tiny": 4, "mixtral": 8, "skew": 8, "fine": 16}
+# Copy configuration per workload (consumer CTAs, copy warps in the producer CTAs), the fastest
+# measured on one GB300: with the producers' copy warps the fine-grained layer needs no dedicated
+# partition and the Mixtral-shaped one only 4 CTAs; the skewed layer is fastest with 8 dedicated
+# CTAs alone.
+DEFAULT_COPY = {"tiny": (4, False), "mixtral": (4, True), "skew": (8, False), "fine": (0, True)}
 
 
 def parse_args():
@@ -48,9 +50,12 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--consumers", type=int, default=None,
-                    help="c_CTA: SMs of the consumer partition (default per workload, see DEFAULT_CONSUMERS)")
+                    help="c_CTA: SMs of the consumer partition (default per workload, see DEFAULT_COPY)")
     ap.add_argument("--mgb", type=int, default=1)
     ap.add_argument("--no-tail-assist", action="store_true", help="keep finished producer CTAs out of the copy")
+    ap.add_argument("--copy-warps", action=argparse.BooleanOptionalAction, default=None,
+                    help="also run copy engines as extra warps in every producer CTA (consumers may then be 0; "
+                         "default per workload, see DEFAULT_COPY)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -170,10 +175,13 @@ def run_ours(args, rank: int, world: int):
     tlc_build.build()
     dev = torch.device("cuda", torch.cuda.current_device())
     w = inputs.WORKLOADS[args.workload]
+    dc, dw = DEFAULT_COPY.get(args.workload, (8, False))
     if args.consumers is None:
-        args.consumers = DEFAULT_CONSUMERS.get(args.workload, 8)
+        args.consumers = dc
+    if args.copy_warps is None:
+        args.copy_warps = dw
     seed = args.seed + rank
-    flags = 0 if args.no_tail_assist else tlc.MOE_TAIL_ASSIST
+    flags = (0 if args.no_tail_assist else tlc.MOE_TAIL_ASSIST) | (tlc.MOE_COPY_WARPS if args.copy_warps else 0)
     cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags)
     peaks, peaks_src = load_peaks()
 
@@ -257,12 +265,29 @@ def run_ours(args, rank: int, world: int):
                 "executed_tflops": round(fl_up_exe / (up_ms * 1e-3) / 1e12, 1),
                 "algorithmic_flops_per_launch": fl_up_alg, "launch_ms": round(up_ms, 4)}
 
+    # HBM-bound stages against the measured copy bandwidth (algorithmic bytes / stage time)
+    hbm = peaks["hbm_gbs"]
+    E_, k_, d_ = w.E, w.topk, w.d
+    pad_rows = P - TK
+    stage_bytes = {
+        # route: logits in, idx/gate/rank out; permute: x in, k rows + padding rows of Xp out
+        "route_plan_permute": w.T * E_ * 4 + TK * 12 + w.T * d_ * 2 + (TK + pad_rows) * d_ * 2,
+        "copy": 2 * TK * d_ * 2,                                  # Yp rows in, Ret rows out
+        "combine": TK * d_ * 2 + w.T * d_ * 4 + TK * 8,          # Ret rows + gates in, out written
+    }
+    stage_ms = {"route_plan_permute": float(np.median(st_seq[:, tlc.EV_BEGIN])),
+                "copy": copy_alone_ms, "combine": float(np.median(st_seq[:, tlc.EV_COPIED]))}
+    hbm_stages = {n: {"bytes": int(b), "ms": round(stage_ms[n], 4),
+                      "achieved_gbs": round(b / (stage_ms[n] * 1e-3) / 1e9, 1),
+                      "frac_of_measured_hbm": round(b / (stage_ms[n] * 1e-3) / 1e9 / hbm, 3)}
+                  for n, b in stage_bytes.items()}
+
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": round(sec_max * 1e3 / K, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "ffn": w.ffn, "E": w.E, "topk": w.topk,
-                   "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "mgb": args.mgb,
+                   "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps), "mgb": args.mgb,
                    "tail_assist": not args.no_tail_assist, "seed": args.seed,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "
@@ -289,6 +314,7 @@ def run_ours(args, rank: int, world: int):
             "sequential": {n: round(float(np.median(st_seq[:, i])), 4) for i, n in enumerate(
                 ["route_plan_permute", "swiglu_gemm", "down_gemm", "copy", "combine"])}},
         "clocks_sequential": clocks_seq,
+        "hbm_stages": hbm_stages,
     }
 
     if not args.no_e2e:

@@ -58,6 +58,9 @@ extern "C" {
 #define MOE_PLAN_SKIP_PERMUTE 0x1u    /* moe_plan: stop after the plan, do not fill Xp        */
 #define MOE_TAIL_ASSIST 0x2u          /* producer CTAs that finish their GEMM tiles join the  */
                                       /* copy (the consumer partition is unchanged)           */
+#define MOE_COPY_WARPS 0x4u           /* copy engines also run as two extra warps in every    */
+                                      /* producer CTA (16-byte loads/stores, no shared memory),*/
+                                      /* so consumer_ctas may be 0: no SM leaves the GEMM       */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
 

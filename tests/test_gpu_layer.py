@@ -56,8 +56,12 @@ def test_layer_matches_oracle_small_shapes(name):
     assert torch.equal(L.ws.view("Ret"), ret_ovl)
 
 
+CW = tlc.MOE_COPY_WARPS
+
+
 @pytest.mark.parametrize("consumers,mgb,flags", [
     (1, 1, 0), (2, 2, 0), (4, 1, tlc.MOE_TAIL_ASSIST), (16, 2, tlc.MOE_TAIL_ASSIST), (32, 4, 0),
+    (0, 1, CW), (0, 2, CW | tlc.MOE_TAIL_ASSIST), (4, 1, CW | tlc.MOE_TAIL_ASSIST), (8, 4, CW),
 ])
 def test_partition_and_segment_knobs_do_not_change_results(consumers, mgb, flags):
     w = small("skew")
@@ -76,19 +80,23 @@ def test_tile_checksum_falsifier(seed):
     tiles under stress) run over 100 seeds of the skewed workload with a tiny consumer partition.
     """
     w = inputs.WORKLOADS["skew"].replace(T=1024, d=256, ffn=256)
-    L = Layer(w, seed=seed, cfg_kw=dict(consumer_ctas=2 + seed % 7, mgb=1 + seed % 2,
-                                        flags=tlc.MOE_TAIL_ASSIST if seed % 3 == 0 else 0))
+    copy_warps = seed % 4 == 1  # a quarter of the seeds copy with the producers' extra warps only
+    L = Layer(w, seed=seed, cfg_kw=dict(consumer_ctas=0 if copy_warps else 2 + seed % 7, mgb=1 + seed % 2,
+                                        flags=(tlc.MOE_TAIL_ASSIST if seed % 3 == 0 else 0) |
+                                        (CW if copy_warps else 0)))
     L.run(sequential=False)
     idx, _ = moe_ref.route_topk(L.logits_np, w.topk)
     plan = moe_ref.build_plan(idx, w.E, w.R, w.tile_M, L.cfg.mgb)
     check_ret_is_copy_of_yp(L, plan)
 
 
-def test_stalled_consumer_times_out_and_context_survives():
+@pytest.mark.parametrize("consumers,flags", [(4, 0), (0, CW)])
+def test_stalled_consumer_times_out_and_context_survives(consumers, flags):
     w = small("tiny")
     L = Layer(w, seed=0)
     want = L.run(sequential=True)
-    cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=tlc.MOE_TEST_STALL_CONSUMER, timeout_us=20000)
+    cfg = tlc.Config.from_workload(w, consumer_ctas=consumers, flags=flags | tlc.MOE_TEST_STALL_CONSUMER,
+                                   timeout_us=20000)
     tlc.forward(cfg, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws)
     rc, detail = tlc.status(cfg, L.ws)
     assert rc == tlc.MOE_ERR_TIMEOUT
@@ -119,22 +127,25 @@ def test_argument_errors_on_gpu():
     assert ei.value.code == tlc.MOE_ERR_WORKSPACE
     sms, ok = tlc.device_info()
     assert ok and sms >= 100
-    bad = tlc.Config.from_workload(w, consumer_ctas=sms)
-    with pytest.raises(tlc.MoEError) as ei:
-        tlc.forward(bad, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws)
-    assert ei.value.code == tlc.MOE_ERR_ARG
+    for bad in (tlc.Config.from_workload(w, consumer_ctas=sms), tlc.Config.from_workload(w, consumer_ctas=0)):
+        with pytest.raises(tlc.MoEError) as ei:
+            tlc.forward(bad, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws)
+        assert ei.value.code == tlc.MOE_ERR_ARG
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mixtral", "skew", "fine"])
 def test_full_size_sampled_tokens(name):
     """Full workload sizes in the bench's launch configuration; 48 sampled tokens against the
-    oracle's per-token definition, plus bitwise overlapped == sequential over all tokens."""
+    oracle's per-token definition, plus bitwise overlapped == sequential over all tokens (also with
+    the producers' extra copy warps and no consumer partition)."""
     w = inputs.WORKLOADS[name]
     L = Layer(w, seed=0, cfg_kw=dict(consumer_ctas=8, flags=tlc.MOE_TAIL_ASSIST))
     got = L.run(sequential=False)
     seq = L.run(sequential=True)
     assert torch.equal(got, seq)
+    cw = tlc.Config.from_workload(w, consumer_ctas=0, flags=CW | tlc.MOE_TAIL_ASSIST)
+    assert torch.equal(L.run(sequential=False, cfg=cw), seq)
     rng = np.random.default_rng(7)
     tokens = np.sort(rng.choice(w.T, size=48, replace=False))
     tokens[0], tokens[-1] = 0, w.T - 1  # include both ends

@@ -55,13 +55,17 @@ def test_sweep_overlapped_equals_sequential(weights, T):
         assert tlc.status(base_cfg, ws)[0] == tlc.MOE_OK
         want = out.clone()
         for c in CONSUMERS:
-            for flags in (0, tlc.MOE_TAIL_ASSIST):
+            for flags in (0, tlc.MOE_TAIL_ASSIST, tlc.MOE_TAIL_ASSIST | tlc.MOE_COPY_WARPS):
                 cfg = tlc.Config.from_workload(w, consumer_ctas=c, flags=flags)
                 out.zero_()
                 tlc.forward(cfg, logits, x, weights["W1"], weights["W3"], weights["W2"], out, ws)
                 rc, detail = tlc.status(cfg, ws)
                 assert rc == tlc.MOE_OK, (T, R, c, flags, rc, detail)
                 assert torch.equal(out, want), (T, R, c, flags)
+        cfg = tlc.Config.from_workload(w, consumer_ctas=0, flags=tlc.MOE_TAIL_ASSIST | tlc.MOE_COPY_WARPS)
+        out.zero_()
+        tlc.forward(cfg, logits, x, weights["W1"], weights["W3"], weights["W2"], out, ws)
+        assert tlc.status(cfg, ws)[0] == tlc.MOE_OK and torch.equal(out, want), (T, R, 0)
         if not checked:  # sampled tokens against the oracle once per T
             rng = np.random.default_rng(T)
             tokens = np.sort(rng.choice(T, size=16, replace=False))

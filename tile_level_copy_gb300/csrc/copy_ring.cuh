@@ -173,4 +173,98 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
     __syncwarp();
 }
 
+// SIMT copy engine: one warp, 16-byte loads and stores through registers (16 per lane in flight),
+// no shared memory, so it can run beside a producer's GEMM warps in the same CTA. Same queue, same
+// band-counter acquire as copy_units; the generic-proxy loads need no proxy fence because producers
+// fence their TMA stores into the generic proxy before they release the counter.
+__device__ __forceinline__ uint4 ld_cg_v4(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_cg_v4(uint4* p, const uint4& v) {
+    asm volatile("st.global.cg.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int* s_abort, int queue, uint32_t want) {
+    const int lane = threadIdx.x & 31;
+    int MT = p.meta[META_MTILES];
+    if (MT < 0 || MT > s.MT_max) MT = 0;
+    const int units = copy_unit_count(s, MT);
+    const size_t rowb = (size_t)s.d * 2;
+    unsigned long long t_first = ~0ull, t_acq = 0;
+    bool did = false;
+    constexpr int UNROLL = 16;
+
+    int u_next = 0;
+    if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
+    for (;;) {
+        const int u = __shfl_sync(0xffffffffu, u_next, 0);
+        if (__any_sync(0xffffffffu, *s_abort != 0) || u >= units) break;
+        if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
+        int pos, rb, rpu;
+        copy_unit_decode(s, MT, u, &pos, &rb, &rpu);
+        const int m = p.sched[pos];
+        const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
+        if (rb >= valid) continue;
+        const int re = min(valid, rb + rpu);
+        bool failed = false;
+        if (lane == 0) {
+            const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
+            for (int i = 0; i < nb && !failed; ++i) {
+                const uint32_t* bc = p.bands + p.sched[first + i];
+                if (ld_acquire_gpu(bc) == want) continue;
+                const unsigned long long t0 = globaltimer();
+                for (unsigned ns = 64;; ns = ns < 512 ? 2 * ns : ns) {
+                    __nanosleep(ns);
+                    if (ld_acquire_gpu(bc) == want) break;
+                    if (*s_abort) {
+                        failed = true;
+                        break;
+                    }
+                    if (globaltimer() - t0 > s.timeout_ns) {
+                        *s_abort = 1;
+                        set_status(p.meta, ST_FLAG_TIMEOUT, p.sched[first + i]);
+                        failed = true;
+                        break;
+                    }
+                }
+            }
+            t_acq = globaltimer();
+            if (!did) t_first = t_acq;
+        }
+        if (__any_sync(0xffffffffu, failed)) break;
+        __syncwarp();  // orders lane 0's acquire before every lane's loads
+        did = true;
+        const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.Yp) +
+                                                          (size_t)(row0 + rb) * rowb);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.Ret) + (size_t)(p.tile_ret[m] + rb) * rowb);
+        const int n = (int)((size_t)(re - rb) * rowb / 16);
+        for (int base = 0; base < n; base += 32 * UNROLL) {
+            uint4 v[UNROLL];
+#pragma unroll
+            for (int i = 0; i < UNROLL; ++i) {
+                const int idx = base + i * 32 + lane;
+                if (idx < n) v[i] = ld_cg_v4(src + idx);
+            }
+#pragma unroll
+            for (int i = 0; i < UNROLL; ++i) {
+                const int idx = base + i * 32 + lane;
+                if (idx < n) st_cg_v4(dst + idx, v[i]);
+            }
+        }
+    }
+    __threadfence();  // this lane's stores performed before the completion stamp
+    __syncwarp();
+    if (lane == 0 && did) {
+        const unsigned long long t_end = globaltimer();
+        atomicMin(&p.trace[MOE_TRACE_COPY_START], t_first);
+        atomicMax(&p.trace[MOE_TRACE_COPY_END], t_end);
+        atomicMax(&p.trace[MOE_TRACE_LAST_LOAD], t_end);
+        atomicMax(&p.trace[MOE_TRACE_LAST_DRAIN], t_end);
+        atomicMax(&p.trace[MOE_TRACE_LAST_ACQUIRE], t_acq);
+    }
+}
+
 }  // namespace moe

@@ -100,7 +100,7 @@ __device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* ite
 }
 
 template <int MODE>  // 1: SwiGLU up-projection -> Hp; 2: down-projection -> Yp (+ flags / consumer)
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAh,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const __grid_constant__ CUtensorMap tmOut, int num_producers, int overlapped) {
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         mbar_fence_init();
     }
     if (MODE == 1) {
-        for (int e = tid; e < s.E; e += GEMM_THREADS) {
+        for (int e = tid; e < s.E; e += blockDim.x) {
             sm.tab[(s.E + 1) + e] = p.experts[8 * e + 5];         // first work item
             sm.tab[(s.E + 1) + s.E + e] = p.experts[8 * e + 4];   // work items
         }
@@ -164,6 +164,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = producer ? *sm.tmem_base : 0u;
     unsigned long long last_end = 0;
+    const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
+
+    // Extra warps (launched with MOE_COPY_WARPS): SIMT copy engines beside the GEMM warps.
+    if (warp >= GEMM_WARPS) {
+        if (MODE == 2 && overlapped) copy_units_simt(s, p, sm.abort, META_QUEUE, want);
+        return;
+    }
 
     if (producer) {
         if (warp == 0 && lane == 0) {
@@ -365,7 +372,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     }
     tc_fence_before();
-    __syncthreads();
+    named_bar_sync(1, GEMM_THREADS);  // the GEMM warps only: extra copy warps run on independently
     if (producer && warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -374,10 +381,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (MODE == 2 && producer && warp >= 2 && lane == 0 && last_end)
         atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
 
-    if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST))) {
-        const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
+    if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
         copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want);
-    }
 }
 
 static cudaError_t set_smem_attr(const void* fn) {
@@ -400,6 +405,7 @@ cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMa
     if (e != cudaSuccess) return e;
     const int producers = overlapped ? sms - consumers : sms;
     int ov = overlapped ? 1 : 0;
+    const int threads = (overlapped && (s.flags & MOE_COPY_WARPS)) ? GEMM_THREADS_MAX : GEMM_THREADS;
     Shape sa = s;
     PlanPtrs pa = p;
     CUtensorMap a = tmA, ah = tmAh, b0 = tmW2, b1 = tmW2, o = tmOut;
@@ -410,7 +416,7 @@ cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMa
     // Cooperative launch: every CTA (producers and consumers) is resident at once, or the launch
     // fails; the consumers' waits on producer flags can therefore always be satisfied.
     void* args[] = {&sa, &pa, &a, &ah, &b0, &b1, &o, (void*)&producers, &ov};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&gemm_kernel<2>), dim3(sms), dim3(GEMM_THREADS),
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&gemm_kernel<2>), dim3(sms), dim3(threads),
                                        args, GEMM_SMEM, st);
 }
 

@@ -283,8 +283,9 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W3, 16) || !aligned(W2, 16) || !aligned(out, 16) ||
         !aligned(logits, 4))
         return fail(MOE_ERR_ARG, "x, W1, W3, W2, out must be 16-byte aligned, logits 4-byte aligned");
-    if (overlapped && (c.consumers < 1 || c.consumers > c.di.sms / 2))
-        return fail(MOE_ERR_ARG, "consumer_ctas=%d must be in [1, %d]", c.consumers, c.di.sms / 2);
+    const int min_consumers = (S.flags & MOE_COPY_WARPS) ? 0 : 1;
+    if (overlapped && (c.consumers < min_consumers || c.consumers > c.di.sms / 2))
+        return fail(MOE_ERR_ARG, "consumer_ctas=%d must be in [%d, %d]", c.consumers, min_consumers, c.di.sms / 2);
 
     CUtensorMap tXp, tXph, tHp, tHph, tW1, tW3, tW2, tHpOut, tYpOut;
     int rc = make_map(&tXp, c.p.Xp, 2, S.d, S.P_max, 1, BM, "Xp");

@@ -44,6 +44,9 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_STAGE_BYTES = 256 * BK * 2;            // 32 KB (up to N = 256)
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int GEMM_THREADS = 192;                      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int GEMM_WARPS = GEMM_THREADS / 32;
+constexpr int COPY_WARPS_EXTRA = 2;                    // copy-engine warps added with MOE_COPY_WARPS
+constexpr int GEMM_THREADS_MAX = GEMM_THREADS + 32 * COPY_WARPS_EXTRA;
 constexpr int MISC_BYTES = 6144;  // barriers, flags and the expert table (4E+1 ints)
 // epilogue staging: per epilogue warp two 32-row x 32-column bf16 chunks (2 KB each), written to
 // global memory by TMA tensor stores
