@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--copy-warps", action=argparse.BooleanOptionalAction, default=None,
                     help="also run copy engines as extra warps in every producer CTA (consumers may then be 0; "
                          "default per workload, see DEFAULT_COPY)")
+    ap.add_argument("--pair-umma", action=argparse.BooleanOptionalAction, default=False,
+                    help="SwiGLU GEMM on CTA pairs (UMMA 256 x 256 over two SMs)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -181,7 +183,8 @@ def run_ours(args, rank: int, world: int):
     if args.copy_warps is None:
         args.copy_warps = dw
     seed = args.seed + rank
-    flags = (0 if args.no_tail_assist else tlc.MOE_TAIL_ASSIST) | (tlc.MOE_COPY_WARPS if args.copy_warps else 0)
+    flags = (0 if args.no_tail_assist else tlc.MOE_TAIL_ASSIST) | (tlc.MOE_COPY_WARPS if args.copy_warps else 0) | \
+        (tlc.MOE_PAIR_UMMA if args.pair_umma else 0)
     cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags)
     peaks, peaks_src = load_peaks()
 
@@ -287,7 +290,8 @@ def run_ours(args, rank: int, world: int):
         "ms_per_step": round(sec_max * 1e3 / K, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "ffn": w.ffn, "E": w.E, "topk": w.topk,
-                   "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps), "mgb": args.mgb,
+                   "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps),
+                   "pair_umma": bool(args.pair_umma), "mgb": args.mgb,
                    "tail_assist": not args.no_tail_assist, "seed": args.seed,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "

@@ -61,6 +61,8 @@ extern "C" {
 #define MOE_COPY_WARPS 0x4u           /* copy engines also run as two extra warps in every    */
                                       /* producer CTA (16-byte loads/stores, no shared memory),*/
                                       /* so consumer_ctas may be 0: no SM leaves the GEMM       */
+#define MOE_PAIR_UMMA 0x8u            /* SwiGLU GEMM on CTA pairs: UMMA 256 x 256 over two SMs */
+                                      /* (tcgen05 cta_group::2), half the B tile per SM        */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
 

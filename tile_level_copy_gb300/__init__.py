@@ -27,6 +27,7 @@ MOE_ERR_PLAN = -6
 MOE_PLAN_SKIP_PERMUTE = 0x1
 MOE_TAIL_ASSIST = 0x2
 MOE_COPY_WARPS = 0x4
+MOE_PAIR_UMMA = 0x8
 MOE_TEST_STALL_CONSUMER = 0x100
 
 TRACE_GEMM2_START, TRACE_GEMM2_END, TRACE_COPY_START, TRACE_COPY_END = 0, 1, 2, 3

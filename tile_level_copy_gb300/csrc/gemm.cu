@@ -99,6 +99,75 @@ __device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* ite
     return make_ref(items[2 * it], items[2 * it + 1], t - it * nN, tiles);
 }
 
+// One epilogue warp's staging in shared memory: two 32-row x 32-column bf16 chunk buffers, used
+// alternately. put(): each lane writes its row (16-byte pieces in a lane-rotated order, free of
+// bank conflicts), then lane 0 stores the chunk with one TMA tensor store.
+struct EpiStage {
+    uint8_t* buf;
+    int eb;
+    __device__ __forceinline__ void put(const CUtensorMap* tm, const uint32_t (&pk)[16], int x, int y, int lane) {
+        if (lane == 0) bulk_wait_read_1();  // the store that last used this buffer has read it
+        __syncwarp();
+        uint4* dst = reinterpret_cast<uint4*>(buf + eb * EPI_CHUNK_BYTES + lane * (EPI_CHUNK * 2));
+        const uint4 u0 = make_uint4(pk[0], pk[1], pk[2], pk[3]), u1 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        const uint4 u2 = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+        const uint4 u3 = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int pi = (i + lane) & 3;
+            dst[pi] = pi == 0 ? u0 : pi == 1 ? u1 : pi == 2 ? u2 : u3;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tm, buf + eb * EPI_CHUNK_BYTES, x, y);
+            bulk_commit();
+        }
+        eb ^= 1;
+    }
+};
+
+// Epilogue of one warp's 32 accumulator lanes (tile rows y..y+31) of a finished tile at TMEM
+// address tb. MODE 1: columns 0-127 hold the gate and 128-255 the up projection of output columns
+// n*128..; h = silu(gate) * up, rounded to bf16. MODE 2: the BN columns of output columns n*BN..,
+// rounded to bf16. Inactive warps (padding half of a 64-row band) read TMEM but store nothing.
+template <int MODE>
+__device__ __forceinline__ void epilogue_rows(EpiStage& es, const CUtensorMap* tmOut, uint32_t tb, int n, int BN,
+                                              int y, bool active, int lane) {
+    if (MODE == 1) {
+#pragma unroll 1
+        for (int c = 0; c < BN1 / 32; ++c) {
+            uint32_t g[32], u[32];
+            tmem_ld32(tb + c * 32, g);
+            tmem_ld32(tb + BN1 + c * 32, u);
+            if (active) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                    const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * __uint_as_float(u[2 * i]);
+                    const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
+                    pk[i] = pack_bf16x2(h0, h1);
+                }
+                es.put(tmOut, pk, n * BN1 + c * 32, y, lane);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tb + c * 32, v);
+            if (active) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                es.put(tmOut, pk, n * BN + c * 32, y, lane);
+            }
+        }
+    }
+}
+
 template <int MODE>  // 1: SwiGLU up-projection -> Hp; 2: down-projection -> Yp (+ flags / consumer)
 __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAh,
@@ -270,30 +339,9 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
             // TMA tensor store of the chunk. Two staging buffers per warp alternate.
             const int q = warp & 3;  // TMEM lane quarter this warp may access
             const bool flags = (MODE == 2) && overlapped;
-            uint8_t* ebuf = sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES;
-            int eb = 0;
+            EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
             int b = 0;
             uint32_t aph = 0;
-            auto stage_chunk = [&](const uint32_t (&pk)[16], int x, int y) {
-                if (lane == 0) bulk_wait_read_1();  // the store that last used this buffer has read it
-                __syncwarp();
-                uint4* dst = reinterpret_cast<uint4*>(ebuf + eb * EPI_CHUNK_BYTES + lane * (EPI_CHUNK * 2));
-                const uint4 u0 = make_uint4(pk[0], pk[1], pk[2], pk[3]), u1 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                const uint4 u2 = make_uint4(pk[8], pk[9], pk[10], pk[11]);
-                const uint4 u3 = make_uint4(pk[12], pk[13], pk[14], pk[15]);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int pi = (i + lane) & 3;
-                    dst[pi] = pi == 0 ? u0 : pi == 1 ? u1 : pi == 2 ? u2 : u3;
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmOut, ebuf + eb * EPI_CHUNK_BYTES, x, y);
-                    bulk_commit();
-                }
-                eb ^= 1;
-            };
             for (int t = blockIdx.x; t < total; t += num_producers) {
                 const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up, p.tiles)
                                                : decode_down(t, nN, p.items_down, p.tiles);
@@ -309,38 +357,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                 const bool active = mq >= 0;
                 const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
                 const uint32_t inc = (tr.mB == tr.mA) ? 1u : 2u;  // quarters per band: 4 in all
-                if (MODE == 1) {
-#pragma unroll 1
-                    for (int c = 0; c < BN1 / 32; ++c) {
-                        uint32_t g[32], u[32];
-                        tmem_ld32(tb + c * 32, g);
-                        tmem_ld32(tb + BN1 + c * 32, u);
-                        if (active) {
-                            uint32_t pk[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-                                const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * __uint_as_float(u[2 * i]);
-                                const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
-                                pk[i] = pack_bf16x2(h0, h1);
-                            }
-                            stage_chunk(pk, tr.n * BN1 + c * 32, y);
-                        }
-                    }
-                } else {
-#pragma unroll 1
-                    for (int c = 0; c < BN / 32; ++c) {
-                        uint32_t v[32];
-                        tmem_ld32(tb + c * 32, v);
-                        if (active) {
-                            uint32_t pk[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                            stage_chunk(pk, tr.n * BN + c * 32, y);
-                        }
-                    }
-                }
+                epilogue_rows<MODE>(es, &tmOut, tb, tr.n, BN, y, active, lane);
                 tc_fence_before();
                 mbar_arrive(&sm.acc_empty[b]);
                 if (MODE == 2 && active) {
@@ -385,6 +402,307 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
         copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want);
 }
 
+// =============================================================================================
+// SwiGLU GEMM on CTA pairs. A cluster of two CTAs computes one 256-row x 256-column UMMA tile:
+// the even CTA (rank 0) stages the 128 token rows of one work item and the gate half (W1 rows) of
+// the B tile, the odd CTA the rows of the expert's next work item and the up half (W3 rows); one
+// thread of rank 0 issues tcgen05.mma.cta_group::2, and each CTA's TMEM receives its own 128 rows
+// x (128 gate | 128 up) columns, so the epilogue is the single-CTA one. An expert with an odd
+// number of work items leaves the odd CTA without rows in its last pair tile (it still loads its
+// B half; its accumulator rows are not stored).
+//
+// Barriers: full[s] (this CTA's TMA bytes landed), empty[s] (UMMAs of the stage done; committed
+// to both CTAs), pready[s] on rank 0 (rank 1's stage s is full: rank 1's warp 1 relays its own
+// full[s] with a cluster-scope release arrive), acc_full[b] (committed to both CTAs), acc_empty[b]
+// on rank 0 (count 8: the four epilogue warps of each CTA). Every wait is bounded; a timeout
+// raises the abort word of both CTAs.
+// =============================================================================================
+struct PairSmem {
+    uint8_t* stages;
+    uint8_t* epi;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* pready;
+    uint64_t* acc_full;
+    uint64_t* acc_empty;
+    uint64_t* drain;
+    uint32_t* tmem_base;
+    uint32_t* peer_base;
+    volatile int* abort;
+    int* tab;  // [cum (E+1) | first item (E) | items (E)]
+};
+
+__device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
+    PairSmem sm;
+    const uint32_t a = smem_u32(raw);
+    uint8_t* base = raw + (((a + 1023u) & ~1023u) - a);
+    sm.stages = base;
+    sm.epi = base + PAIR_STAGES * PAIR_STAGE_BYTES;
+    uint8_t* misc = sm.epi + EPI_BYTES;
+    sm.full = reinterpret_cast<uint64_t*>(misc);
+    sm.empty = sm.full + PAIR_STAGES;
+    sm.pready = sm.empty + PAIR_STAGES;
+    sm.acc_full = sm.pready + PAIR_STAGES;
+    sm.acc_empty = sm.acc_full + 2;
+    sm.drain = sm.acc_empty + 2;
+    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.drain + 1);
+    sm.peer_base = sm.tmem_base + 1;
+    sm.abort = reinterpret_cast<volatile int*>(sm.peer_base + 1);
+    sm.tab = const_cast<int*>(sm.abort + 1);
+    return sm;
+}
+
+// Raise the abort word of both CTAs of the pair.
+__device__ __forceinline__ void pair_abort(const PairSmem& sm, uint32_t rank) {
+    *sm.abort = 1;
+    st_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(sm.abort)), rank ^ 1u), 1u);
+}
+
+// Pair tile t -> this CTA's rows. Order as in decode_up with two work items per pair: experts in
+// id order, N tiles outer, pairs inner; rank r takes item 2 * pair + r of the expert (mA = -1: none).
+__device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, const int32_t* items,
+                                                  const int32_t* tiles, uint32_t rank) {
+    const int* cum = tab;
+    const int* first = tab + (E + 1);
+    const int* count = first + E;
+    int lo = 0, hi = E - 1;  // largest e with cum[e] <= t
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo, local = t - cum[e], cnt = count[e], np = (cnt + 1) >> 1;
+    const int n = local / np, it = 2 * (local - n * np) + (int)rank;
+    if (it >= cnt) {
+        TileRef r;
+        r.mA = r.mB = -1;
+        r.n = n;
+        r.e = e;
+        r.rowA = r.rowB = 0;
+        return r;
+    }
+    const int item = first[e] + it;
+    TileRef r = make_ref(items[2 * item], items[2 * item + 1], n, tiles);
+    r.e = e;
+    return r;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+    gemm_pair_swiglu_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmW1,
+                            const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmOut) {
+    extern __shared__ uint8_t smem_raw[];
+    const PairSmem sm = carve_pair(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    int MT = p.meta[META_MTILES], NI = p.meta[META_ITEMS];
+    if (MT < 0 || MT > s.MT_max || NI < 0 || NI > MT) MT = NI = 0;
+    const int nN = s.ffn / BN1;
+    const int KB = s.d / BK;
+    const unsigned long long tmo = s.timeout_ns;
+
+    if (tid == 0) {
+        for (int i = 0; i < PAIR_STAGES; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], 1);
+            mbar_init(&sm.pready[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.acc_full[i], 1);
+            mbar_init(&sm.acc_empty[i], 8);
+        }
+        mbar_init(sm.drain, 1);
+        *sm.abort = 0;
+        mbar_fence_init();
+    }
+    for (int e = tid; e < s.E; e += blockDim.x) {
+        sm.tab[(s.E + 1) + e] = p.experts[8 * e + 5];         // first work item
+        sm.tab[(s.E + 1) + s.E + e] = p.experts[8 * e + 4];   // work items
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int e = 0; e < s.E; ++e) {
+            sm.tab[e] = acc;
+            acc += ((sm.tab[(s.E + 1) + s.E + e] + 1) >> 1) * nN;
+        }
+        sm.tab[s.E] = acc;
+    }
+    if (warp == 1) {
+        __syncwarp();
+        tmem_alloc_pair(sm.tmem_base, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    if (tid == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmAh);
+        tma_prefetch_desc(&tmW1);
+        tma_prefetch_desc(&tmW3);
+        tma_prefetch_desc(&tmOut);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs started, their barriers initialised and TMEM allocated
+    tc_fence_after();
+    if (rank == 1 && tid == 0) st_cluster_u32(mapa_shared(smem_u32(sm.peer_base), 0u), *sm.tmem_base);
+    cluster_sync();  // rank 1's column base delivered to rank 0
+    const uint32_t tmem = *sm.tmem_base;
+    const int total = NI > 0 ? sm.tab[s.E] : 0;
+    const bool bad = rank == 0 && *sm.peer_base != tmem;  // the allocation was not one pair allocation
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer (both CTAs): own A rows + own half of B ----------------
+        int st = 0;
+        uint32_t ph = 0, issued = 0, last_ph = 0;
+        bool ok = true;
+        for (int t = pair; t < total && ok && !bad; t += npairs) {
+            const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, p.tiles, rank);
+            const uint32_t bytes = (tr.mA >= 0 ? PAIR_A_BYTES : 0) + PAIR_B_BYTES;
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.full[st], bytes);
+                uint8_t* a = sm.stages + st * PAIR_STAGE_BYTES;
+                uint8_t* b = a + PAIR_A_BYTES;
+                if (tr.mA >= 0) {
+                    if (tr.mB >= 0 && tr.mB != tr.mA) {  // two half bands: two 64-row boxes
+                        tma_load_2d(a, &tmAh, &sm.full[st], kb * BK, tr.rowA);
+                        tma_load_2d(a + PAIR_A_BYTES / 2, &tmAh, &sm.full[st], kb * BK, tr.rowB);
+                    } else {
+                        tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.rowA);
+                    }
+                }
+                tma_load_3d(b, rank == 0 ? &tmW1 : &tmW3, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
+                issued |= 1u << st;
+                last_ph = (last_ph & ~(1u << st)) | (ph << st);
+                if (++st == PAIR_STAGES) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 10 + (int)rank);
+            pair_abort(sm, rank);
+            int never = 0;
+            for (int i = 0; i < PAIR_STAGES; ++i)  // let loads in flight land before the CTA leaves
+                if (issued & (1u << i)) mbar_wait(&sm.full[i], (last_ph >> i) & 1u, tmo, &never);
+        }
+    } else if (warp == 1 && lane == 0) {
+        int st = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        if (rank == 0) {
+            // ---------------- UMMA issuer (rank 0) ----------------
+            if (bad) {
+                set_status(p.meta, ST_PAIR_TMEM, (int)*sm.peer_base);
+                pair_abort(sm, rank);
+            }
+            const uint32_t idesc = umma_idesc_bf16(2 * BM, 2 * BN1);
+            int b = 0;
+            uint32_t aph = 0;
+            for (int t = pair; t < total && ok && !bad; t += npairs) {
+                if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1u, tmo, sm.abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dt = tmem + (uint32_t)(b * 256);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&sm.full[st], ph, tmo, sm.abort) ||
+                        !mbar_wait_cluster(&sm.pready[st], ph, tmo, sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(sm.stages + st * PAIR_STAGE_BYTES);
+                    const uint64_t ad = sdesc_sw128(a_addr);
+                    const uint64_t bd = sdesc_sw128(a_addr + PAIR_A_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16_pair(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    umma_commit_pair(&sm.empty[st], 0x3);
+                    if (++st == PAIR_STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(&sm.acc_full[b], 0x3);
+                b ^= 1;
+                if (b == 0) aph ^= 1u;
+            }
+            // Final commit to both CTAs' drain barrier: every UMMA issued has completed when it fires.
+            umma_commit_pair(sm.drain, 0x3);
+        } else {
+            // ---------------- relay (rank 1): own stage full -> rank 0's pready ----------------
+            // The payload (the stage's bytes) is written by this CTA's TMA unit, which completes
+            // the full barrier only once the bytes are in shared memory; the relay forwards that
+            // event with a relaxed arrive (a release arrive would fence this SM's in-flight loads
+            // and, measured, more than halves the pair's throughput).
+            const uint32_t pready0 = mapa_shared(smem_u32(sm.pready), 0u);
+            for (int t = pair; t < total && ok; t += npairs) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(&sm.full[st], ph, tmo, sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster_relaxed(pready0 + st * 8u);
+                    if (++st == PAIR_STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+        if (!ok) {
+            if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 12 + (int)rank);
+            pair_abort(sm, rank);
+        }
+        int never = 0;
+        if (!mbar_wait(sm.drain, 0, tmo, &never) && !*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 14 + (int)rank);
+    } else if (warp >= 2) {
+        // ---------------- epilogue (both CTAs): this CTA's 128 rows ----------------
+        const int q = warp & 3;
+        EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
+        const uint32_t acc_empty0 = mapa_shared(smem_u32(sm.acc_empty), 0u);
+        int b = 0;
+        uint32_t aph = 0;
+        for (int t = pair; t < total && !bad; t += npairs) {
+            const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, p.tiles, rank);
+            if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
+                if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 16 + (int)rank);
+                if (lane == 0) pair_abort(sm, rank);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
+            const int mq = (q < 2) ? tr.mA : tr.mB;
+            const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
+            epilogue_rows<1>(es, &tmOut, tb, tr.n, 2 * BN1, y, mq >= 0, lane);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty0 + b * 8u);
+            b ^= 1;
+            if (b == 0) aph ^= 1u;
+        }
+        if (lane == 0) bulk_wait_all();  // staging buffers stay valid until every store is done
+        __syncwarp();
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync();  // both CTAs: all roles done, all UMMAs complete (drain), no remote access left
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+    __syncwarp();
+    cluster_sync();  // neither CTA leaves while the pair's TMEM release is in progress
+}
+
 static cudaError_t set_smem_attr(const void* fn) {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
 }
@@ -395,6 +713,33 @@ cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensor
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<1>));
     if (e != cudaSuccess) return e;
     gemm_kernel<1><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(s, p, tmA, tmAh, tmW1, tmW3, tmOut, sms, 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA,
+                                    const CUtensorMap& tmAh, const CUtensorMap& tmW1, const CUtensorMap& tmW3,
+                                    const CUtensorMap& tmOut, cudaStream_t st) {
+    const void* fn = reinterpret_cast<const void*>(&gemm_pair_swiglu_kernel);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static int pairs_cache[64] = {0};  // co-resident pairs per device (cluster occupancy query)
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (pairs_cache[dev] == 0) {
+        cudaLaunchConfig_t q = {};  // the cluster size (2) is the kernel's compile-time one
+        q.gridDim = dim3(2, 1, 1);
+        q.blockDim = dim3(GEMM_THREADS, 1, 1);
+        q.dynamicSmemBytes = PAIR_SMEM;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, fn, &q);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        pairs_cache[dev] = n;
+    }
+    gemm_pair_swiglu_kernel<<<2 * pairs_cache[dev], GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmAh, tmW1, tmW3,
+                                                                                  tmOut);
     return cudaGetLastError();
 }
 

@@ -304,7 +304,8 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     rc = run_plan(c, logits, x, true);
     if (rc) return rc;
     if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
-    cudaError_t e = launch_gemm_swiglu(S, c.p, tXp, tXph, tW1, tW3, tHpOut, c.di.sms, c.st);
+    cudaError_t e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXp, tXph, tW1, tW3, tHpOut, c.st)
+                                              : launch_gemm_swiglu(S, c.p, tXp, tXph, tW1, tW3, tHpOut, c.di.sms, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
     if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
     if (overlapped) {
@@ -474,6 +475,7 @@ MOE_API int moe_status(const moe_config* cfg, const void* ws, void* stream, int3
         case ST_PIPE_TIMEOUT: return fail(MOE_ERR_TIMEOUT, "GEMM pipeline wait timed out (role %d)", w[1]);
         case ST_COPY_TIMEOUT: return fail(MOE_ERR_TIMEOUT, "row-band copy timed out (M-tile %d)", w[1]);
         case ST_BAD_PLAN: return fail(MOE_ERR_PLAN, "plan index out of bounds (%d)", w[1]);
+        case ST_PAIR_TMEM: return fail(MOE_ERR_DEVICE, "CTA pair got different TMEM bases (peer %d)", w[1]);
         default: return fail(MOE_ERR_PLAN, "unknown device status %d", w[0]);
     }
 }

@@ -31,6 +31,7 @@ enum Status : int {
     ST_PIPE_TIMEOUT = 2,   // an mbarrier wait of the GEMM pipeline gave up
     ST_COPY_TIMEOUT = 3,   // a bulk copy did not complete in time
     ST_BAD_PLAN = 4,       // a plan index failed its bounds check
+    ST_PAIR_TMEM = 5,      // the two CTAs of a pair got different TMEM column bases
 };
 
 // Trace slots (uint64) beyond the public ones.
@@ -55,6 +56,15 @@ constexpr int EPI_CHUNK_BYTES = 32 * EPI_CHUNK * 2;
 constexpr int EPI_BYTES = 4 * 2 * EPI_CHUNK_BYTES;
 constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + EPI_BYTES + MISC_BYTES + 1024;  // + alignment slack
 constexpr int TMEM_COLS = 512;                         // two 256-column fp32 accumulators
+// CTA-pair GEMM (tcgen05 cta_group::2, UMMA 256 x 256 x 16 over two SMs): each CTA stages its own
+// 128 token rows of A and one half (128 rows) of the 256-row B tile, so per k-block an SM writes
+// and reads 32 KB of shared memory instead of 48 KB.
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_A_BYTES = BM * BK * 2;              // 16 KB
+constexpr int PAIR_B_BYTES = 128 * BK * 2;             // 16 KB
+constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_SMEM = PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES + MISC_BYTES + 1024;
+static_assert(PAIR_SMEM <= 227 * 1024, "pair GEMM shared memory");
 constexpr int BN1 = 128;                               // output columns of a SwiGLU tile
 constexpr uint32_t FLAG_READY = 4;                     // one release-add per epilogue warp
 constexpr int MAX_E = 256;
@@ -119,6 +129,10 @@ cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtr
 cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
                                const CUtensorMap& tmW1, const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms,
                                cudaStream_t st);
+// The same SwiGLU GEMM on CTA pairs (cluster of 2, UMMA M = 256); grid = 2 x co-resident pairs.
+cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA,
+                                    const CUtensorMap& tmAh, const CUtensorMap& tmW1, const CUtensorMap& tmW3,
+                                    const CUtensorMap& tmOut, cudaStream_t st);
 cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
                              const CUtensorMap& tmW2, const CUtensorMap& tmOut, int sms, int consumers, bool overlapped,
                              cudaStream_t st);
@@ -346,6 +360,93 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
+        : "memory");
+}
+
+// ---- CTA pairs (clusters of two) -------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address in CTA `rank`'s shared memory of the variable at shared::cta address `addr` of this CTA.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Every thread of both CTAs: release this thread's prior memory operations, wait for all. Also
+// the first step before any access to the peer's shared memory (the peer has started).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// Arrive on a barrier of the pair (own or peer) with release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// The same without release semantics: orders none of this thread's memory operations, so it costs
+// no cluster-scope fence (measured: the release form adds ~0.6 us per arrive while TMA loads of
+// the CTA are in flight). For signals whose payload is not written by this thread.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// mbar_wait for a barrier that the peer CTA arrives on (cluster-scope acquire).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, unsigned long long timeout_ns,
+                                                  volatile int* abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 63) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > timeout_ns) return false;
+        }
+    }
+}
+// tcgen05 with cta_group::2: one warp of each CTA of the pair allocates / frees together (both
+// get the same column base); one thread of the even CTA issues the UMMAs, which read A rows and
+// B halves from the same shared-memory offsets in both CTAs and write each CTA's own TMEM lanes.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the barrier at `bar`'s offset in every CTA of `mask` when the UMMAs issued so far
+// by this thread have completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
         : "memory");
 }
 
