@@ -246,16 +246,23 @@ def run_ours(args, rank: int, world: int):
                        tlc.TRACE_COPY_END)])
     ms_ovl, ms_seq = sec_ovl * 1e3 / K, sec_seq * 1e3 / K
 
-    # GEMM numbers: real rows = T*k; executed rows = 128 per work item (a band, or two bands that
-    # need at most 64 rows each); P = padded rows of the layout
+    # GEMM numbers: real rows = T*k; executed rows = 128 per work item: SwiGLU items are 128 rows of
+    # one expert in the compact layout (with CTA pairs, an expert's odd item also occupies the idle
+    # half of its pair), down-projection items a band or two bands that need at most 64 rows each;
+    # P = padded rows of the owner-aligned layout, PC = rows of the compact layout
     meta = ws.view("meta").cpu()
-    P, items = int(meta[0].item()), int(meta[7].item())
+    P, items, items_up, PC = (int(meta[i].item()) for i in (0, 7, 8, 9))
     TK = w.T * w.topk
+    if cfg.flags & tlc.MOE_PAIR_UMMA:
+        iu = ws.view("experts").cpu().numpy()[:, 4]
+        exec_rows_up = 128 * int(np.sum(2 * ((iu + 1) // 2)))
+    else:
+        exec_rows_up = 128 * items_up
     exec_rows = 128 * items
     up_ms = float(np.median(st_ovl[:, tlc.EV_PLANNED]))
     down_ms = float(np.median(st_seq[:, tlc.EV_UP]))
     fl_up_alg, fl_down_alg = 4.0 * TK * w.d * w.ffn, 2.0 * TK * w.d * w.ffn
-    fl_up_exe, fl_down_exe = 4.0 * exec_rows * w.d * w.ffn, 2.0 * exec_rows * w.d * w.ffn
+    fl_up_exe, fl_down_exe = 4.0 * exec_rows_up * w.d * w.ffn, 2.0 * exec_rows * w.d * w.ffn
     gemm_exec_tflops = (fl_up_exe + fl_down_exe) / ((up_ms + down_ms) * 1e-3) / 1e12
     gemm_alg_tflops = (fl_up_alg + fl_down_alg) / ((up_ms + down_ms) * 1e-3) / 1e12
     peak_tc = peaks["bf16_tflops_sustained"]
@@ -271,9 +278,9 @@ def run_ours(args, rank: int, world: int):
     # HBM-bound stages against the measured copy bandwidth (algorithmic bytes / stage time)
     hbm = peaks["hbm_gbs"]
     E_, k_, d_ = w.E, w.topk, w.d
-    pad_rows = P - TK
+    pad_rows = PC - TK
     stage_bytes = {
-        # route: logits in, idx/gate/rank out; permute: x in, k rows + padding rows of Xp out
+        # route: logits in, idx/gate/rank out; permute: x in, k rows + padding rows of Xc out
         "route_plan_permute": w.T * E_ * 4 + TK * 12 + w.T * d_ * 2 + (TK + pad_rows) * d_ * 2,
         "copy": 2 * TK * d_ * 2,                                  # Yp rows in, Ret rows out
         "combine": TK * d_ * 2 + w.T * d_ * 4 + TK * 8,          # Ret rows + gates in, out written
@@ -304,8 +311,9 @@ def run_ours(args, rank: int, world: int):
                  "algorithmic_frac_of_peak": round(gemm_alg_tflops / peak_tc, 4),
                  "executed_frac_of_burst_peak": round(gemm_exec_tflops / peaks["bf16_tflops"], 4),
                  "peak_tflops": peak_tc, "peak_source": peaks_src, "up_ms": round(up_ms, 4),
-                 "down_ms": round(down_ms, 4), "padded_rows": P, "executed_rows": exec_rows, "work_items": items,
-                 "real_rows": TK},
+                 "down_ms": round(down_ms, 4), "padded_rows": P, "compact_rows": PC,
+                 "executed_rows_up": exec_rows_up, "executed_rows_down": exec_rows, "work_items_up": items_up,
+                 "work_items_down": items, "real_rows": TK},
         "overlap": {"hidden_pct": round(100 * statistics.median(hidden), 2),
                     "tail_ms": round(statistics.median(tails), 4), "copy_alone_ms": round(copy_alone_ms, 4),
                     "tail_marks_us": dict(zip(["band_done", "last_acquire", "last_load", "last_drain", "copy_end"],

@@ -55,7 +55,7 @@ extern "C" {
 #define MOE_ERR_PLAN (-6)      /* a device-side bounds check on plan indices failed         */
 
 /* ---- config flags ---------------------------------------------------------------------- */
-#define MOE_PLAN_SKIP_PERMUTE 0x1u    /* moe_plan: stop after the plan, do not fill Xp        */
+#define MOE_PLAN_SKIP_PERMUTE 0x1u    /* moe_plan: stop after the plan, do not fill Xc        */
 #define MOE_TAIL_ASSIST 0x2u          /* producer CTAs that finish their GEMM tiles join the  */
                                       /* copy (the consumer partition is unchanged)           */
 #define MOE_COPY_WARPS 0x4u           /* copy engines also run as two extra warps in every    */
@@ -91,10 +91,19 @@ typedef struct moe_config {
  * starts on a 1024-byte boundary. Shapes use P_max = the largest padded row count the routing can
  * produce, T*topk + min(E*R, T*topk)*(tile_M-1) rounded up to tile_M ([TLS "Referee Report",
  * major comment 1]: padding is per (expert, owner) group), and MT_max = P_max / tile_M.
+ *
+ * Two row layouts. The owner-aligned padded layout of the plan (rows `slot`, P rows, every
+ * (expert, owner) group padded to tile_M) is the layout of the expert outputs Yp, so that each
+ * output tile has one owner. The GEMM inputs Xc and Hc use the expert-compact layout (rows
+ * `cslot`): the rows of each expert contiguous, its groups in owner order and each group's rows
+ * in plan order, each expert's run padded with zero rows to a multiple of 128 (the UMMA tile
+ * height); PC_max = T*topk + min(E, T*topk)*127 rounded up to 128. The SwiGLU GEMM then runs
+ * whole 128-row tiles of one expert instead of padded owner groups.
  */
 typedef struct moe_layout {
     size_t bytes;                     /* total workspace size                              */
     int32_t P_max, MT_max, n_chunks, chunk_tokens, n_tiles_n2, block_n2, rows_per_unit, units_per_band;
+    int32_t PC_max, IU_max;           /* rows of Xc / Hc; SwiGLU work items (PC_max / 128)     */
     size_t idx;        /* int32 [T, topk]   expert of pair (t, j), descending logit            */
     size_t gate;       /* f32   [T, topk]   gate of pair (t, j)                                */
     size_t rank;       /* int32 [T, topk]   rank of t among the chunk's tokens routed to e     */
@@ -108,17 +117,22 @@ typedef struct moe_layout {
     size_t sched;      /* int32 [MT_max]    M-tile at each schedule position                   */
     size_t seg;        /* int32 [MT_max, 2] (first position, bands) of each position's segment */
     size_t experts;    /* int32 [E, 8]      first M-tile, M-tiles, first schedule position,    */
-                       /*                   schedule rank, work items, first item of each list */
-    size_t items_up;   /* int32 [MT_max, 2] GEMM work items (one band, or two bands of <= 64   */
-    size_t items_down; /* int32 [MT_max, 2] rows) of the SwiGLU GEMM / the down-projection     */
-    size_t slot;       /* int32 [T, topk]   row of pair (t, j) in Xp / Yp                      */
+                       /*                   schedule rank, SwiGLU work items, first SwiGLU    */
+                       /*                   item, first down-projection item, first Xc row    */
+    size_t items_up;   /* int32 [IU_max, 2] SwiGLU work items: (first Xc row, expert), 128 rows */
+    size_t items_down; /* int32 [MT_max, 2] down-projection work items: one band, or two bands */
+                       /*                   of one expert with <= 64 valid rows each          */
+    size_t slot;       /* int32 [T, topk]   row of pair (t, j) in Yp (padded layout)            */
+    size_t cslot;      /* int32 [T, topk]   row of pair (t, j) in Xc / Hc (compact layout)      */
     size_t ret_slot;   /* int32 [T, topk]   row of pair (t, j) in Ret                          */
+    size_t ccoff;      /* int32 [E*R]       first Xc row of group e*R+r                         */
+    size_t tile_crow;  /* int32 [MT_max]    Xc / Hc row of the first row of each M-tile (band) */
     size_t meta;       /* int32 [64]        P, M-tiles, work counters, status (see csrc)       */
     size_t flags;      /* uint32 [MT_max, n_tiles_n2] per-tile readiness flags                 */
     size_t bands;      /* uint32 [MT_max]   per-band count of finished tile quarters           */
     size_t trace;      /* uint64 [16]       %globaltimer stamps of the last call (ns)          */
-    size_t Xp;         /* bf16 [P_max, d]   permuted tokens                                    */
-    size_t Hp;         /* bf16 [P_max, ffn] SwiGLU hidden                                      */
+    size_t Xc;         /* bf16 [PC_max, d]  permuted tokens, expert-compact, zero padding rows */
+    size_t Hc;         /* bf16 [PC_max, ffn] SwiGLU hidden, same rows                          */
     size_t Yp;         /* bf16 [P_max, d]   expert outputs                                     */
     size_t Ret;        /* bf16 [T*topk, d]  owner return buffers, R slices of (T/R)*topk rows  */
     size_t in_logits;  /* f32  [T, E]       staging for moe_forward_host                       */
@@ -152,8 +166,8 @@ MOE_API int moe_workspace_layout(const moe_config* cfg, moe_layout* out);
  *            ties to the lower expert id)
  *   topk_w   device f32 [T, topk] or NULL: gates, softmax over the k chosen logits
  *   ws       device workspace of ws_bytes >= moe_workspace_size(cfg), 256-byte aligned
- * Fills the workspace's idx, gate, counts, offsets, tiles, sched, seg, slot, ret_slot, ... and
- * (unless MOE_PLAN_SKIP_PERMUTE) Xp with zero padding rows. The histogram / scan / tile-owner map
+ * Fills the workspace's idx, gate, counts, offsets, tiles, sched, seg, slot, cslot, ret_slot, ...
+ * and (unless MOE_PLAN_SKIP_PERMUTE) Xc with zero padding rows. The histogram / scan / tile-owner map
  * follow [TLS "What carries the argument"]; the plan is built on the device, so no host round
  * trip is needed before the GEMMs ([TLS "Referee Report", minor comment 4, §2.2]).
  */

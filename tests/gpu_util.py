@@ -64,6 +64,23 @@ class Layer:
                                  k=w.topk)
 
 
+def compact_layout(plan: moe_ref.Plan, idx: np.ndarray):
+    """Expected expert-compact layout of the GEMM inputs for an oracle plan.
+
+    Each expert's rows contiguous (its groups in owner order, each group's rows in plan order), each
+    expert's run padded to a multiple of the 128-row UMMA tile. Returns (cbase [E], ccoff [E*R],
+    cslot [T, k], PC)."""
+    E, R, T = plan.E, plan.R, plan.T
+    n = plan.n.astype(np.int64)
+    runs = -(-n.sum(1) // 128) * 128
+    cbase = np.concatenate([[0], np.cumsum(runs)])[:E]
+    before = np.concatenate([np.zeros((E, 1), np.int64), np.cumsum(n, 1)[:, :-1]], 1)
+    ccoff = (cbase[:, None] + before).reshape(-1)
+    g = np.asarray(idx, np.int64) * R + moe_ref.owners(T, R)[:, None]
+    cslot = ccoff[g] + (plan.slot - plan.off[g])
+    return cbase, ccoff, cslot, int(runs.sum())
+
+
 def parity(got: np.ndarray, want: np.ndarray):
     err = np.abs(got - want)
     rel = np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-30)

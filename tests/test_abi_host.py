@@ -44,11 +44,14 @@ def test_layout_regions_are_aligned_and_disjoint(name):
     TK, G = w.T * w.topk, w.E * w.R
     assert L["P_max"] == -(-(TK + min(G, TK) * (w.tile_M - 1)) // w.tile_M) * w.tile_M
     assert L["MT_max"] * w.tile_M == L["P_max"]
+    # compact GEMM input rows: every expert's run padded to the 128-row UMMA tile
+    assert L["PC_max"] == -(-(TK + min(w.E, TK) * 127) // 128) * 128 and L["IU_max"] * 128 == L["PC_max"]
     assert (w.T // w.R) % L["chunk_tokens"] == 0 and L["chunk_tokens"] <= 128
     offs = sorted(L[r] for r in tlc.LAYOUT_REGIONS)
     assert all(o % 1024 == 0 for o in offs)
     assert len(set(offs)) == len(offs) and offs[-1] < L["bytes"]
-    ws_view_sizes = {"Xp": L["P_max"] * w.d * 2, "Hp": L["P_max"] * w.ffn * 2, "Ret": TK * w.d * 2}
+    ws_view_sizes = {"Xc": L["PC_max"] * w.d * 2, "Hc": L["PC_max"] * w.ffn * 2, "Yp": L["P_max"] * w.d * 2,
+                     "Ret": TK * w.d * 2, "items_up": L["IU_max"] * 8, "tile_crow": L["MT_max"] * 4}
     for r, n in ws_view_sizes.items():
         nxt = min(o for o in offs if o > L[r]) if L[r] != offs[-1] else L["bytes"]
         assert nxt - L[r] >= n

@@ -35,8 +35,9 @@ def test_layer_matches_oracle_small_shapes(name):
     assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
     # intermediates: SwiGLU hidden and expert outputs on the real rows
     rows = ref.plan.slot.reshape(-1)
-    Hp = L.ws.view("Hp")[:ref.plan.P].double().cpu().numpy()
-    _, hrel = parity(Hp[rows], ref.Hp[rows])
+    crows = torch.from_numpy(L.ws.view("cslot").cpu().numpy().reshape(-1)).long().cuda()
+    Hc = L.ws.view("Hc")[crows].double().cpu().numpy()  # the compact rows of the same pairs
+    _, hrel = parity(Hc, ref.Hp[rows])
     assert hrel <= 5e-3, hrel
     Yp = L.ws.view("Yp")[:ref.plan.P].double().cpu().numpy()
     _, yrel = parity(Yp[rows], ref.Yp[rows])

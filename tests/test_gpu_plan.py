@@ -2,6 +2,8 @@
 
 Indices, counts, offsets, tile-owner map, schedule, segments, slots, return slots and the permuted
 rows (with zero padding) have exactly one correct value each, so they are compared for equality.
+The permuted rows are checked in the expert-compact layout of the GEMM inputs, whose rows follow
+from the oracle's plan (tests.gpu_util.compact_layout).
 """
 import numpy as np
 import pytest
@@ -10,6 +12,7 @@ import torch
 import tile_level_copy_gb300 as tlc
 from oracle import moe_ref
 from tile_level_copy_gb300 import inputs
+from tests.gpu_util import compact_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -46,11 +49,28 @@ def check_plan(w, logits_np, x_cpu, mgb=1):
     np.testing.assert_array_equal(v("seg")[:MT], plan.seg)
     np.testing.assert_array_equal(v("slot"), plan.slot)
     np.testing.assert_array_equal(v("ret_slot"), plan.ret_slot)
+    # expert-compact layout of the GEMM inputs
+    cbase, ccoff, cslot, PC = compact_layout(plan, ridx)
+    assert meta[9] == PC and meta[8] == PC // 128
+    np.testing.assert_array_equal(v("ccoff").reshape(-1), ccoff)
+    np.testing.assert_array_equal(v("cslot"), cslot)
+    g_t = plan.tiles[:, 0] * w.R + plan.tiles[:, 1]
+    np.testing.assert_array_equal(v("tile_crow")[:MT], ccoff[g_t] + plan.tiles[:, 2] - plan.off[g_t])
+    runs = -(-plan.n.sum(1) // 128)
+    experts = v("experts").reshape(-1, 8)
+    np.testing.assert_array_equal(experts[:, 4], runs)
+    np.testing.assert_array_equal(experts[:, 5], cbase // 128)
+    np.testing.assert_array_equal(experts[:, 7], cbase)
+    want_items = [(cbase[e] + 128 * i, e) for e in range(w.E) for i in range(runs[e])]
+    np.testing.assert_array_equal(v("items_up")[:PC // 128], np.array(want_items).reshape(-1, 2))
     if x_cpu is not None:
         xb = x_cpu.view(torch.int16).numpy()
-        want = moe_ref.permute(xb, plan)
-        got = ws.view("Xp")[:plan.P].view(torch.int16).cpu().numpy()
+        want = np.zeros((PC, w.d), np.int16)  # padding rows are zero
+        want[cslot.reshape(-1)] = np.repeat(xb, w.topk, axis=0)
+        got = ws.view("Xc")[:PC].view(torch.int16).cpu().numpy()
         np.testing.assert_array_equal(got, want)
+        # the same rows as the page's padded layout, row for row
+        np.testing.assert_array_equal(got[cslot.reshape(-1)], moe_ref.permute(xb, plan)[plan.slot.reshape(-1)])
     return plan
 
 
@@ -108,29 +128,34 @@ def test_plan_skip_permute_leaves_xp_untouched():
 
 @pytest.mark.parametrize("name", ["tiny", "mixtral", "skew", "fine"])
 def test_work_items_cover_every_band_once(name):
-    """GEMM work items: every band in exactly one item of each list; a shared item holds two bands
-    of the same expert that each need at most 64 rows; the down-projection list follows the
-    schedule."""
+    """Down-projection work items: every band in exactly one item; a shared item holds two bands of
+    the same expert that each need at most 64 rows; the list follows the schedule. SwiGLU work items
+    cover every real row of the compact layout once, 128 rows of one expert each, and are never more
+    than the down-projection's."""
     w = inputs.WORKLOADS[name]
     cfg, ws, _, _ = run_plan(w, inputs.make_logits(w, 0), None, skip_permute=True)
     meta = ws.view("meta").cpu().numpy()
-    MT, NI = int(meta[1]), int(meta[7])
+    MT, NI, NU, PC = int(meta[1]), int(meta[7]), int(meta[8]), int(meta[9])
     tiles = ws.view("tiles").cpu().numpy()[:MT]
     sched = ws.view("sched").cpu().numpy()[:MT]
-    for name_ in ("items_up", "items_down"):
-        items = ws.view(name_).cpu().numpy()[:NI]
-        seen = []
-        for a, b in items.tolist():
-            seen.append(a)
-            if b == a:
-                assert w.tile_M == 128
-            elif b == -1:
-                assert w.tile_M == 64 and tiles[a, 3] <= 64
-            else:
-                seen.append(b)
-                assert tiles[a, 0] == tiles[b, 0] and tiles[a, 3] <= 64 and tiles[b, 3] <= 64
-        assert sorted(seen) == list(range(MT))
-        if name_ == "items_down":
-            assert seen == sched.tolist()
+    items = ws.view("items_down").cpu().numpy()[:NI]
+    seen = []
+    for a, b in items.tolist():
+        seen.append(a)
+        if b == a:
+            assert w.tile_M == 128
+        elif b == -1:
+            assert w.tile_M == 64 and tiles[a, 3] <= 64
+        else:
+            seen.append(b)
+            assert tiles[a, 0] == tiles[b, 0] and tiles[a, 3] <= 64 and tiles[b, 3] <= 64
+    assert seen == sched.tolist() and sorted(seen) == list(range(MT))
     # two half bands cut the GEMM work wherever partial bands are small
     assert NI <= MT and (w.tile_M == 128 or NI == (MT + 1) // 2 or NI < MT)
+    up = ws.view("items_up").cpu().numpy()[:NU]
+    cslot = ws.view("cslot").cpu().numpy().reshape(-1)
+    idx = ws.view("idx").cpu().numpy().reshape(-1)
+    assert NU * 128 == PC and NU <= NI
+    rows_of = {(r0 + i): e for r0, e in up.tolist() for i in range(128)}
+    assert len(rows_of) == PC  # disjoint 128-row items
+    assert all(rows_of[c] == e for c, e in zip(cslot.tolist(), idx.tolist()))

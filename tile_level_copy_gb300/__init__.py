@@ -54,10 +54,10 @@ class _Config(ctypes.Structure):
 
 
 _LAYOUT_INTS = ("P_max", "MT_max", "n_chunks", "chunk_tokens", "n_tiles_n2", "block_n2", "rows_per_unit",
-                "units_per_band")
+                "units_per_band", "PC_max", "IU_max")
 LAYOUT_REGIONS = ("idx", "gate", "rank", "chunk_cnt", "chunk_base", "counts", "offsets", "ret_off", "tiles",
-                  "tile_ret", "sched", "seg", "experts", "items_up", "items_down", "slot", "ret_slot", "meta", "flags", "bands", "trace", "Xp", "Hp",
-                  "Yp", "Ret", "in_logits", "in_x", "out")
+                  "tile_ret", "sched", "seg", "experts", "items_up", "items_down", "slot", "cslot", "ret_slot", "ccoff",
+                  "tile_crow", "meta", "flags", "bands", "trace", "Xc", "Hc", "Yp", "Ret", "in_logits", "in_x", "out")
 
 
 class _Layout(ctypes.Structure):
@@ -164,13 +164,14 @@ class Workspace:
     """Device workspace of one config (a torch uint8 buffer) with typed views of its regions."""
 
     _DT = {"idx": (torch.int32, "TK"), "gate": (torch.float32, "TK"), "rank": (torch.int32, "TK"),
-           "slot": (torch.int32, "TK"), "ret_slot": (torch.int32, "TK"), "counts": (torch.int32, "ER"),
+           "slot": (torch.int32, "TK"), "cslot": (torch.int32, "TK"), "ret_slot": (torch.int32, "TK"),
+           "counts": (torch.int32, "ER"), "ccoff": (torch.int32, "ER"), "tile_crow": (torch.int32, "MT"),
            "offsets": (torch.int32, "G1"), "ret_off": (torch.int32, "RE1"), "tiles": (torch.int32, "MT4"),
            "tile_ret": (torch.int32, "MT"), "sched": (torch.int32, "MT"), "seg": (torch.int32, "MT2"),
-           "experts": (torch.int32, "E8"), "items_up": (torch.int32, "MT2"),
+           "experts": (torch.int32, "E8"), "items_up": (torch.int32, "IU2"),
            "items_down": (torch.int32, "MT2"), "meta": (torch.int32, "META"), "flags": (torch.int32, "FL"),
            "bands": (torch.int32, "MT"),
-           "trace": (torch.int64, "TR"), "Xp": (torch.bfloat16, "Pd"), "Hp": (torch.bfloat16, "PF"),
+           "trace": (torch.int64, "TR"), "Xc": (torch.bfloat16, "PCd"), "Hc": (torch.bfloat16, "PCF"),
            "Yp": (torch.bfloat16, "Pd"), "Ret": (torch.bfloat16, "TKd")}
 
     def __init__(self, cfg: Config, device="cuda"):
@@ -186,7 +187,8 @@ class Workspace:
         shape = {"TK": (c.T, c.topk), "ER": (c.E, c.R), "G1": (c.E * c.R + 1,), "RE1": (c.R, c.E + 1),
                  "MT4": (L["MT_max"], 4), "MT": (L["MT_max"],), "MT2": (L["MT_max"], 2), "E8": (c.E, 8),
                  "META": (64,), "FL": (L["MT_max"], L["n_tiles_n2"]), "TR": (16,), "Pd": (L["P_max"], c.d),
-                 "PF": (L["P_max"], c.ffn), "TKd": (TK, c.d)}[kind]
+                 "PCd": (L["PC_max"], c.d), "PCF": (L["PC_max"], c.ffn), "IU2": (L["IU_max"], 2),
+                 "TKd": (TK, c.d)}[kind]
         n = 1
         for s in shape:
             n *= s

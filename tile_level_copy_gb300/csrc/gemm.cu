@@ -57,29 +57,44 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
     return sm;
 }
 
-// One GEMM tile: work item (mA, mB) x N tile n of expert e. Rows 0-63 of the UMMA tile come from
-// row rowA on, rows 64-127 from row rowB on (rowB = rowA + 64 when the item is a single band).
-// mB == mA: one band of 128 rows; mB == -1: one band of 64 rows alone; otherwise two half bands.
+// One GEMM tile: work item (mA, mB) x N tile n of expert e. Rows 0-63 of the UMMA tile are loaded
+// from input row lrowA on and stored to output row rowA on, rows 64-127 from lrowB / to rowB
+// (lrowA + 64 / rowA + 64 when the item is a single 128-row run). Down-projection items are bands
+// (mB == mA: one band of 128 rows; mB == -1: one 64-row band alone; otherwise two half bands), read
+// from the compact layout and written to the padded one; SwiGLU items are 128 compact rows of one
+// expert (mA = mB = 0), read and written in the compact layout.
 struct TileRef {
-    int mA, mB, n, e, rowA, rowB;
+    int mA, mB, n, e, rowA, rowB, lrowA, lrowB;
 };
 
-__device__ __forceinline__ TileRef make_ref(int mA, int mB, int n, const int32_t* tiles) {
+__device__ __forceinline__ TileRef make_ref(int mA, int mB, int n, const int32_t* tiles, const int32_t* crow) {
     TileRef r;
     r.mA = mA;
     r.mB = mB;
     r.n = n;
     r.e = tiles[4 * mA + 0];
     r.rowA = tiles[4 * mA + 2];
-    r.rowB = (mB >= 0 && mB != mA) ? tiles[4 * mB + 2] : r.rowA + 64;
+    r.lrowA = crow[mA];
+    const bool two = mB >= 0 && mB != mA;
+    r.rowB = two ? tiles[4 * mB + 2] : r.rowA + 64;
+    r.lrowB = two ? crow[mB] : r.lrowA + 64;
+    return r;
+}
+
+__device__ __forceinline__ TileRef compact_ref(int row, int n, int e) {
+    TileRef r;
+    r.mA = r.mB = 0;
+    r.n = n;
+    r.e = e;
+    r.rowA = r.lrowA = row;
+    r.rowB = r.lrowB = row + 64;
     return r;
 }
 
 // SwiGLU GEMM order: expert-major; inside an expert, N tiles outer and work items inner, so the
 // CTAs working at the same time share each weight tile through L2.
-// tab = [cum (E+1) | first item (E) | items (E)]
-__device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, const int32_t* items,
-                                             const int32_t* tiles) {
+// tab = [cum (E+1) | first item (E) | items (E)]; items = (first compact row, expert)
+__device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, const int32_t* items) {
     const int* cum = tab;
     const int* first = tab + (E + 1);
     const int* count = first + E;
@@ -90,13 +105,14 @@ __device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, const
     }
     const int e = lo, local = t - cum[e], cnt = count[e];
     const int n = local / cnt, it = first[e] + local % cnt;
-    return make_ref(items[2 * it], items[2 * it + 1], n, tiles);
+    return compact_ref(items[2 * it], n, e);
 }
 
 // Down-projection order: work items in schedule (remote-first) order, all N tiles of an item together.
-__device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* items, const int32_t* tiles) {
+__device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* items, const int32_t* tiles,
+                                               const int32_t* crow) {
     const int it = t / nN;
-    return make_ref(items[2 * it], items[2 * it + 1], t - it * nN, tiles);
+    return make_ref(items[2 * it], items[2 * it + 1], t - it * nN, tiles, crow);
 }
 
 // One epilogue warp's staging in shared memory: two 32-row x 32-column bf16 chunk buffers, used
@@ -168,7 +184,7 @@ __device__ __forceinline__ void epilogue_rows(EpiStage& es, const CUtensorMap* t
     }
 }
 
-template <int MODE>  // 1: SwiGLU up-projection -> Hp; 2: down-projection -> Yp (+ flags / consumer)
+template <int MODE>  // 1: SwiGLU up-projection -> Hc; 2: down-projection -> Yp (+ flags / consumer)
 __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAh,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
@@ -178,8 +194,8 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const bool producer = (int)blockIdx.x < num_producers;
 
-    int MT = p.meta[META_MTILES], NI = p.meta[META_ITEMS];
-    if (MT < 0 || MT > s.MT_max || NI < 0 || NI > MT) MT = NI = 0;
+    int MT = p.meta[META_MTILES], NI = p.meta[(MODE == 1) ? META_ITEMS_UP : META_ITEMS];
+    if (MT < 0 || MT > s.MT_max || NI < 0 || NI > ((MODE == 1) ? s.IU_max : MT)) MT = NI = 0;
     const int nN = (MODE == 1) ? s.ffn / BN1 : s.n_tiles_n2;
     const int BN = (MODE == 1) ? 2 * BN1 : s.bn2;  // UMMA N
     const int KB = ((MODE == 1) ? s.d : s.ffn) / BK;
@@ -248,8 +264,8 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
             uint32_t ph = 0, issued = 0, last_ph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += num_producers) {
-                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up, p.tiles)
-                                               : decode_down(t, nN, p.items_down, p.tiles);
+                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up)
+                                               : decode_down(t, nN, p.items_down, p.tiles, p.tile_crow);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
                         ok = false;
@@ -259,10 +275,10 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                     uint8_t* a = sm.stages + st * STAGE_BYTES;
                     uint8_t* b = a + A_STAGE_BYTES;
                     if (tr.mB >= 0 && tr.mB != tr.mA) {  // two half bands: two 64-row boxes
-                        tma_load_2d(a, &tmAh, &sm.full[st], kb * BK, tr.rowA);
-                        tma_load_2d(a + A_STAGE_BYTES / 2, &tmAh, &sm.full[st], kb * BK, tr.rowB);
+                        tma_load_2d(a, &tmAh, &sm.full[st], kb * BK, tr.lrowA);
+                        tma_load_2d(a + A_STAGE_BYTES / 2, &tmAh, &sm.full[st], kb * BK, tr.lrowB);
                     } else {
-                        tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.rowA);
+                        tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.lrowA);
                     }
                     if (MODE == 1) {
                         tma_load_3d(b, &tmB0, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
@@ -343,8 +359,8 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
             int b = 0;
             uint32_t aph = 0;
             for (int t = blockIdx.x; t < total; t += num_producers) {
-                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up, p.tiles)
-                                               : decode_down(t, nN, p.items_down, p.tiles);
+                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up)
+                                               : decode_down(t, nN, p.items_down, p.tiles, p.tile_crow);
                 if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
                     if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 2);
                     *sm.abort = 1;
@@ -461,7 +477,7 @@ __device__ __forceinline__ void pair_abort(const PairSmem& sm, uint32_t rank) {
 // Pair tile t -> this CTA's rows. Order as in decode_up with two work items per pair: experts in
 // id order, N tiles outer, pairs inner; rank r takes item 2 * pair + r of the expert (mA = -1: none).
 __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, const int32_t* items,
-                                                  const int32_t* tiles, uint32_t rank) {
+                                                  uint32_t rank) {
     const int* cum = tab;
     const int* first = tab + (E + 1);
     const int* count = first + E;
@@ -477,13 +493,11 @@ __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, 
         r.mA = r.mB = -1;
         r.n = n;
         r.e = e;
-        r.rowA = r.rowB = 0;
+        r.rowA = r.rowB = r.lrowA = r.lrowB = 0;
         return r;
     }
     const int item = first[e] + it;
-    TileRef r = make_ref(items[2 * item], items[2 * item + 1], n, tiles);
-    r.e = e;
-    return r;
+    return compact_ref(items[2 * item], n, e);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
@@ -495,8 +509,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    int MT = p.meta[META_MTILES], NI = p.meta[META_ITEMS];
-    if (MT < 0 || MT > s.MT_max || NI < 0 || NI > MT) MT = NI = 0;
+    int NI = p.meta[META_ITEMS_UP];
+    if (NI < 0 || NI > s.IU_max) NI = 0;
     const int nN = s.ffn / BN1;
     const int KB = s.d / BK;
     const unsigned long long tmo = s.timeout_ns;
@@ -556,7 +570,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         uint32_t ph = 0, issued = 0, last_ph = 0;
         bool ok = true;
         for (int t = pair; t < total && ok && !bad; t += npairs) {
-            const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, p.tiles, rank);
+            const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, rank);
             const uint32_t bytes = (tr.mA >= 0 ? PAIR_A_BYTES : 0) + PAIR_B_BYTES;
             for (int kb = 0; kb < KB; ++kb) {
                 if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
@@ -566,14 +580,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 mbar_arrive_expect_tx(&sm.full[st], bytes);
                 uint8_t* a = sm.stages + st * PAIR_STAGE_BYTES;
                 uint8_t* b = a + PAIR_A_BYTES;
-                if (tr.mA >= 0) {
-                    if (tr.mB >= 0 && tr.mB != tr.mA) {  // two half bands: two 64-row boxes
-                        tma_load_2d(a, &tmAh, &sm.full[st], kb * BK, tr.rowA);
-                        tma_load_2d(a + PAIR_A_BYTES / 2, &tmAh, &sm.full[st], kb * BK, tr.rowB);
-                    } else {
-                        tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.rowA);
-                    }
-                }
+                if (tr.mA >= 0) tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
                 tma_load_3d(b, rank == 0 ? &tmW1 : &tmW3, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
                 issued |= 1u << st;
                 last_ph = (last_ph & ~(1u << st)) | (ph << st);
@@ -671,7 +678,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         int b = 0;
         uint32_t aph = 0;
         for (int t = pair; t < total && !bad; t += npairs) {
-            const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, p.tiles, rank);
+            const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, rank);
             if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
                 if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 16 + (int)rank);
                 if (lane == 0) pair_abort(sm, rank);

@@ -56,6 +56,8 @@ int make_layout(const moe_config* c, Layout* out) {
     const int64_t P_max = (int64_t)align_up((size_t)(TK + (G < TK ? G : TK) * (tbM - 1)), (size_t)tbM);
     if (P_max >= (int64_t(1) << 30)) return fail(MOE_ERR_ARG, "padded rows %lld too large", (long long)P_max);
     const int64_t MT_max = P_max / tbM;
+    const int64_t PC_max = (int64_t)align_up((size_t)(TK + (E < TK ? E : TK) * (BM - 1)), (size_t)BM);
+    const int64_t IU_max = PC_max / BM;
     // route chunk: <= 128 tokens and <= 32 KB of staged logits, a power of two dividing T/R
     int64_t C = 128;
     while (C > 1 && C * (E + 1) * 4 > 32768) C >>= 1;
@@ -75,6 +77,8 @@ int make_layout(const moe_config* c, Layout* out) {
     moe_layout& L = o.L;
     L.P_max = (int32_t)P_max;
     L.MT_max = (int32_t)MT_max;
+    L.PC_max = (int32_t)PC_max;
+    L.IU_max = (int32_t)IU_max;
     L.n_chunks = (int32_t)(T / C);
     L.chunk_tokens = (int32_t)C;
     L.n_tiles_n2 = nN2;
@@ -101,16 +105,19 @@ int make_layout(const moe_config* c, Layout* out) {
     L.sched = put(MT_max * 4);
     L.seg = put(MT_max * 8);
     L.experts = put(E * 32);
-    L.items_up = put(MT_max * 8);
+    L.items_up = put(IU_max * 8);
     L.items_down = put(MT_max * 8);
     L.slot = put(TK * 4);
+    L.cslot = put(TK * 4);
     L.ret_slot = put(TK * 4);
+    L.ccoff = put(G * 4);
+    L.tile_crow = put(MT_max * 4);
     L.meta = put(META_COUNT * 4);
     L.flags = put(MT_max * nN2 * 4);
     L.bands = put(MT_max * 4);
     L.trace = put(TR_COUNT * 8);
-    L.Xp = put((size_t)P_max * d * 2);
-    L.Hp = put((size_t)P_max * F * 2);
+    L.Xc = put((size_t)PC_max * d * 2);
+    L.Hc = put((size_t)PC_max * F * 2);
     L.Yp = put((size_t)P_max * d * 2);
     L.Ret = put((size_t)TK * d * 2);
     L.in_logits = put((size_t)T * E * 4);
@@ -131,6 +138,8 @@ int make_layout(const moe_config* c, Layout* out) {
     S.n_chunks = L.n_chunks;
     S.P_max = L.P_max;
     S.MT_max = L.MT_max;
+    S.PC_max = L.PC_max;
+    S.IU_max = L.IU_max;
     S.bn2 = bn2;
     S.n_tiles_n2 = nN2;
     S.rows_per_unit = L.rows_per_unit;
@@ -163,13 +172,16 @@ PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     p.items_up = reinterpret_cast<int32_t*>(b + L.items_up);
     p.items_down = reinterpret_cast<int32_t*>(b + L.items_down);
     p.slot = reinterpret_cast<int32_t*>(b + L.slot);
+    p.cslot = reinterpret_cast<int32_t*>(b + L.cslot);
     p.ret_slot = reinterpret_cast<int32_t*>(b + L.ret_slot);
+    p.ccoff = reinterpret_cast<int32_t*>(b + L.ccoff);
+    p.tile_crow = reinterpret_cast<int32_t*>(b + L.tile_crow);
     p.meta = reinterpret_cast<int32_t*>(b + L.meta);
     p.flags = reinterpret_cast<uint32_t*>(b + L.flags);
     p.bands = reinterpret_cast<uint32_t*>(b + L.bands);
     p.trace = reinterpret_cast<unsigned long long*>(b + L.trace);
-    p.Xp = reinterpret_cast<__nv_bfloat16*>(b + L.Xp);
-    p.Hp = reinterpret_cast<__nv_bfloat16*>(b + L.Hp);
+    p.Xc = reinterpret_cast<__nv_bfloat16*>(b + L.Xc);
+    p.Hc = reinterpret_cast<__nv_bfloat16*>(b + L.Hc);
     p.Yp = reinterpret_cast<__nv_bfloat16*>(b + L.Yp);
     p.Ret = reinterpret_cast<__nv_bfloat16*>(b + L.Ret);
     return p;
@@ -287,12 +299,12 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     if (overlapped && (c.consumers < min_consumers || c.consumers > c.di.sms / 2))
         return fail(MOE_ERR_ARG, "consumer_ctas=%d must be in [%d, %d]", c.consumers, min_consumers, c.di.sms / 2);
 
-    CUtensorMap tXp, tXph, tHp, tHph, tW1, tW3, tW2, tHpOut, tYpOut;
-    int rc = make_map(&tXp, c.p.Xp, 2, S.d, S.P_max, 1, BM, "Xp");
-    if (!rc) rc = make_map(&tXph, c.p.Xp, 2, S.d, S.P_max, 1, BM / 2, "Xp (half)");
-    if (!rc) rc = make_map(&tHp, c.p.Hp, 2, S.ffn, S.P_max, 1, BM, "Hp");
-    if (!rc) rc = make_map(&tHph, c.p.Hp, 2, S.ffn, S.P_max, 1, BM / 2, "Hp (half)");
-    if (!rc) rc = make_map(&tHpOut, c.p.Hp, 2, S.ffn, S.P_max, 1, 32, "Hp (store)", EPI_CHUNK, false);
+    CUtensorMap tXc, tXch, tHc, tHch, tW1, tW3, tW2, tHcOut, tYpOut;
+    int rc = make_map(&tXc, c.p.Xc, 2, S.d, S.PC_max, 1, BM, "Xc");
+    if (!rc) rc = make_map(&tXch, c.p.Xc, 2, S.d, S.PC_max, 1, BM / 2, "Xc (half)");
+    if (!rc) rc = make_map(&tHc, c.p.Hc, 2, S.ffn, S.PC_max, 1, BM, "Hc");
+    if (!rc) rc = make_map(&tHch, c.p.Hc, 2, S.ffn, S.PC_max, 1, BM / 2, "Hc (half)");
+    if (!rc) rc = make_map(&tHcOut, c.p.Hc, 2, S.ffn, S.PC_max, 1, 32, "Hc (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tYpOut, c.p.Yp, 2, S.d, S.P_max, 1, 32, "Yp (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tW1, W1, 3, S.d, S.ffn, S.E, BN1, "W1");
     if (!rc) rc = make_map(&tW3, W3, 3, S.d, S.ffn, S.E, BN1, "W3");
@@ -304,16 +316,16 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     rc = run_plan(c, logits, x, true);
     if (rc) return rc;
     if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
-    cudaError_t e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXp, tXph, tW1, tW3, tHpOut, c.st)
-                                              : launch_gemm_swiglu(S, c.p, tXp, tXph, tW1, tW3, tHpOut, c.di.sms, c.st);
+    cudaError_t e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.st)
+                                              : launch_gemm_swiglu(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.di.sms, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
     if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
     if (overlapped) {
-        e = launch_gemm_down(S, c.p, tHp, tHph, tW2, tYpOut, c.di.sms, c.consumers, true, c.st);
+        e = launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, c.consumers, true, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "overlapped down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
     } else {
-        e = launch_gemm_down(S, c.p, tHp, tHph, tW2, tYpOut, c.di.sms, 0, false, c.st);
+        e = launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, 0, false, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
         e = launch_copy_seq(S, c.p, c.di.sms, c.st);
@@ -511,8 +523,9 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     const size_t o_rank = put(TK * 4), o_cnt = put((size_t)L.n_chunks * E * 4),
                  o_base = put((size_t)L.n_chunks * E * 4), o_counts = put(E * R * 4), o_ret = put(R * (E + 1) * 4),
                  o_tiles = put(MT * 16), o_tret = put(MT * 4), o_sched = put(MT * 4), o_seg = put(MT * 8),
-                 o_exp = put(E * 32), o_iu = put(MT * 8), o_id = put(MT * 8), o_meta = put(META_COUNT * 4), o_flags = put(MT * (size_t)L.n_tiles_n2 * 4),
-                 o_bands = put(MT * 4), o_trace = put(TR_COUNT * 8);
+                 o_exp = put(E * 32), o_iu = put((size_t)L.IU_max * 8), o_id = put(MT * 8), o_meta = put(META_COUNT * 4),
+                 o_flags = put(MT * (size_t)L.n_tiles_n2 * 4), o_bands = put(MT * 4), o_trace = put(TR_COUNT * 8),
+                 o_cslot = put(TK * 4), o_ccoff = put(E * R * 4), o_tcrow = put(MT * 4);
     if (cur > (size_t)MOE_STATIC_SCRATCH_BYTES)
         return fail(MOE_ERR_ARG, "this config needs %zu bytes of static scratch; the limit is %d", cur,
                     MOE_STATIC_SCRATCH_BYTES);
@@ -539,7 +552,10 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.items_up = reinterpret_cast<int32_t*>(b + o_iu);
     p.items_down = reinterpret_cast<int32_t*>(b + o_id);
     p.slot = slot;
+    p.cslot = reinterpret_cast<int32_t*>(b + o_cslot);
     p.ret_slot = ret_slot;
+    p.ccoff = reinterpret_cast<int32_t*>(b + o_ccoff);
+    p.tile_crow = reinterpret_cast<int32_t*>(b + o_tcrow);
     p.meta = reinterpret_cast<int32_t*>(b + o_meta);
     p.flags = reinterpret_cast<uint32_t*>(b + o_flags);
     p.bands = reinterpret_cast<uint32_t*>(b + o_bands);

@@ -21,7 +21,9 @@ enum Meta : int {
     META_QUEUE_SEQ = 4,    // next copy unit to hand out (sequential copy)
     META_STATUS = 5,       // 0 or a Status code (first error wins)
     META_STATUS_DETAIL = 6,
-    META_ITEMS = 7,        // GEMM work items (one band, or two bands of <= 64 rows)
+    META_ITEMS = 7,        // down-projection work items (one band, or two bands of <= 64 rows)
+    META_ITEMS_UP = 8,     // SwiGLU work items (128 rows of one expert in the compact layout)
+    META_PC = 9,           // rows of the compact layout used by this call
     META_COUNT = 64,
 };
 
@@ -93,17 +95,20 @@ struct PlanPtrs {
     int32_t* sched;
     int32_t* seg;        // [MT_max][2]
     int32_t* experts;    // [E][8]: first M-tile, M-tiles, first schedule position, schedule rank,
-                         //         work items, first item (id-order list), first item (schedule list)
-    int32_t* items_up;   // [MT_max][2] work items of the SwiGLU GEMM, experts in id order
+                         //         SwiGLU items, first SwiGLU item, first down item, first Xc row
+    int32_t* items_up;   // [IU_max][2] SwiGLU work items (first Xc row, expert), experts in id order
     int32_t* items_down; // [MT_max][2] work items of the down-projection, in schedule order
-    int32_t* slot;
+    int32_t* slot;       // padded-layout row (Yp) of each (token, choice)
+    int32_t* cslot;      // compact-layout row (Xc, Hc) of each (token, choice)
     int32_t* ret_slot;
+    int32_t* ccoff;      // [E*R] first compact row of each group
+    int32_t* tile_crow;  // [MT_max] compact row of each band's first row
     int32_t* meta;
     uint32_t* flags;
     uint32_t* bands;
     unsigned long long* trace;
-    __nv_bfloat16* Xp;
-    __nv_bfloat16* Hp;
+    __nv_bfloat16* Xc;
+    __nv_bfloat16* Hc;
     __nv_bfloat16* Yp;
     __nv_bfloat16* Ret;
 };
@@ -113,6 +118,7 @@ struct Shape {
     int mgb;
     int chunk_tokens, n_chunks;
     int P_max, MT_max;
+    int PC_max, IU_max;             // compact rows and SwiGLU work items (PC_max / 128)
     int bn2, n_tiles_n2;            // down-projection N tile and N tiles per band
     int rows_per_unit, units_per_band;           // copy units of the leading bands
     int rows_per_unit_tail, units_per_band_tail;  // ... and of the last tail_bands bands

@@ -1,5 +1,6 @@
 // Router top-k, per-chunk ranking, the layout plan (histogram, padded offsets, tile-owner map,
-// remote-first schedule, segments, return plan) and the permute into the owner-aligned layout.
+// remote-first schedule, segments, return plan, expert-compact rows of the GEMM inputs) and the
+// permute of the tokens into those rows.
 //
 // Method: "Fine-grained Computation-Communication Overlap via Tile-level Signaling and Scheduling
 // for Mixture-of-Experts" (pith.science/paper/W2ZARMHG), section "What carries the argument": rows
@@ -152,6 +153,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     __shared__ int s_fb[MAX_E];      // full bands per expert
     __shared__ int s_mt[MAX_E];      // M-tiles per expert
     __shared__ int s_ebase[MAX_E];   // first schedule position of the expert's bands
+    __shared__ int s_cbase[MAX_E];   // first row of the expert in the compact layout
+    __shared__ int s_cc[1024];       // first compact row of group g
     __shared__ int s_warp[32];
     __shared__ int s_total;
 
@@ -209,6 +212,24 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         p.experts[8 * e + 1] = s_mt[e];
     }
     __syncthreads();
+
+    // 4b. expert-compact layout of the GEMM inputs: each expert's rows contiguous (its groups in
+    // owner order, rows in plan order), the run padded to a multiple of the UMMA tile height BM.
+    {
+        const int e = tid;
+        const int rows = (e < E) ? ((s_load[e] + BM - 1) / BM) * BM : 0;
+        const int o = block_exclusive_scan(rows, s_warp, &s_total);
+        if (e < E) s_cbase[e] = o;
+    }
+    __syncthreads();
+    const int PC = s_total;
+    for (int g = tid; g < G; g += PLAN_THREADS) {
+        const int e = g / R, r = g % R;
+        int acc = s_cbase[e];
+        for (int q = 0; q < r; ++q) acc += s_n[e * R + q];
+        s_cc[g] = acc;
+        p.ccoff[g] = acc;
+    }
     for (int e = tid; e < E; e += PLAN_THREADS) {
         int rk = 0;
         for (int f = 0; f < E; ++f)
@@ -245,6 +266,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             p.tiles[4 * m + 2] = s_off[g] + i * tbM;
             p.tiles[4 * m + 3] = valid;
             p.tile_ret[m] = rbase + i * tbM;
+            p.tile_crow[m] = s_cc[g] + i * tbM;
             if (i < nfull) p.sched[s_ebase[e] + fpre + i] = m;
         }
         if (nt > nfull) {  // one partial band
@@ -277,11 +299,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         p.seg[2 * q + 1] = min(s.mgb, end - first);
     }
 
-    // 7. GEMM work items. A UMMA tile has 128 rows; a band that needs only 64 of them (every band
-    // when tbM = 64, a band with <= 64 valid rows when tbM = 128) shares a work item with another
-    // such band of the same expert: each is loaded as a 64-row box into one half of the A tile.
-    // Item (mA, mB): mB == mA one 128-row band; mB == -1 one 64-row band alone; else two half bands.
-    __shared__ int s_items[MAX_E], s_ibase_up[MAX_E], s_ibase_down[MAX_E];
+    // 7. GEMM work items. SwiGLU GEMM: the expert's compact run cut into BM-row tiles, item
+    // (first compact row, expert), experts in id order. Down-projection (output tiles must have one
+    // owner): a band that needs only 64 of the UMMA tile's 128 rows (every band when tbM = 64, a
+    // band with <= 64 valid rows when tbM = 128) shares a work item with another such band of the
+    // same expert, each loaded as a 64-row box into one half of the A tile. Item (mA, mB): mB == mA
+    // one 128-row band; mB == -1 one 64-row band alone; else two half bands; schedule order.
+    __shared__ int s_items[MAX_E], s_ibase_down[MAX_E];
     for (int e = tid; e < E; e += PLAN_THREADS) {
         const int m0 = s_off[e * R] / tbM, cnt = s_mt[e];
         int half = 0;
@@ -290,27 +314,27 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     }
     __syncthreads();
     for (int e = tid; e < E; e += PLAN_THREADS) {
-        int up = 0, down = 0;
-        for (int f = 0; f < E; ++f) {
-            up += (f < e) ? s_items[f] : 0;
-            down += (s_erank[f] < s_erank[e]) ? s_items[f] : 0;
-        }
-        s_ibase_up[e] = up;
+        int down = 0;
+        for (int f = 0; f < E; ++f) down += (s_erank[f] < s_erank[e]) ? s_items[f] : 0;
         s_ibase_down[e] = down;
-        p.experts[8 * e + 4] = s_items[e];
-        p.experts[8 * e + 5] = up;
+        const int iu = (s_load[e] + BM - 1) / BM;
+        p.experts[8 * e + 4] = iu;
+        p.experts[8 * e + 5] = s_cbase[e] / BM;
         p.experts[8 * e + 6] = down;
-        p.experts[8 * e + 7] = 0;
+        p.experts[8 * e + 7] = s_cbase[e];
+        if (s_cbase[e] / BM + iu <= s.IU_max)
+            for (int i = 0; i < iu; ++i) {
+                p.items_up[2 * (s_cbase[e] / BM + i)] = s_cbase[e] + i * BM;
+                p.items_up[2 * (s_cbase[e] / BM + i) + 1] = e;
+            }
     }
     __syncthreads();
-    for (int e = tid; e < 2 * E; e += PLAN_THREADS) {  // thread pairs: (expert, list)
-        const int x = e >> 1;
-        const bool down = e & 1;
+    for (int x = tid; x < E; x += PLAN_THREADS) {
         const int cnt = s_mt[x];
-        int* out = (down ? p.items_down : p.items_up) + 2 * (down ? s_ibase_down[x] : s_ibase_up[x]);
+        int* out = p.items_down + 2 * s_ibase_down[x];
         int n = 0, pending = -1;
         for (int i = 0; i < cnt; ++i) {
-            const int m = down ? p.sched[s_ebase[x] + i] : s_off[x * R] / tbM + i;
+            const int m = p.sched[s_ebase[x] + i];
             if (p.tiles[4 * m + 3] > 64) {
                 out[2 * n] = m;
                 out[2 * n + 1] = m;
@@ -338,10 +362,13 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         int items = 0;
         for (int e = 0; e < E; ++e) items += s_items[e];
         p.meta[META_ITEMS] = items;
+        p.meta[META_ITEMS_UP] = PC / BM;
+        p.meta[META_PC] = PC;
         p.meta[META_QUEUE] = 0;
         p.meta[META_QUEUE_SEQ] = 0;
-        p.meta[META_STATUS] = (P > s.P_max) ? ST_BAD_PLAN : 0;
-        p.meta[META_STATUS_DETAIL] = (P > s.P_max) ? P : 0;
+        const bool bad = P > s.P_max || PC > s.PC_max;
+        p.meta[META_STATUS] = bad ? ST_BAD_PLAN : 0;
+        p.meta[META_STATUS_DETAIL] = bad ? (P > s.P_max ? P : PC) : 0;
     }
     if (tid < TR_COUNT) p.trace[tid] = (tid == MOE_TRACE_GEMM2_START || tid == MOE_TRACE_COPY_START) ? ~0ull : 0ull;
     const int nflags = min(MT, s.MT_max) * s.n_tiles_n2;
@@ -355,44 +382,45 @@ cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// permute_kernel: one warp per work item. Items [0, T): token t computes its k slots and return
-// slots and copies x[t] into the k rows of Xp: each lane first loads up to 16 vectors of 16 bytes
-// (all loads in flight together), then stores them to the k rows. Items [T, T + M-tiles * tbM/8):
-// one group of 8 rows of an M-tile, zeroing those rows that are padding (row >= valid). With
-// x == nullptr only the slots are written.
+// permute_kernel: one warp per work item. Items [0, T): token t computes its k slots (padded
+// layout), compact slots and return slots, and copies x[t] into its k rows of Xc: each lane first
+// loads up to 16 vectors of 16 bytes (all loads in flight together), then stores them to the k
+// rows. Items [T, T + E * BM/8): one group of 8 rows of an expert's last BM-row tile in the compact
+// layout, zeroing those rows past the expert's rows. With x == nullptr only the slots are written.
 // ---------------------------------------------------------------------------------------------
 constexpr int PERM_VEC = 16;  // 16-byte vectors per lane per pass
 
 __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat16* __restrict__ x, PlanPtrs p) {
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    const int MT = p.meta[META_MTILES];
+    const int PC = p.meta[META_PC];
     const int per = s.T / s.R, slice = per * s.k, E = s.E, R = s.R, k = s.k;
     const int vec = s.d / 8;  // 16-byte vectors per row
     const uint4* xs = reinterpret_cast<const uint4*>(x);
-    uint4* xp = reinterpret_cast<uint4*>(p.Xp);
-    const bool ok_mt = MT <= s.MT_max;
-    const int groups = s.tbM / 8;
-    const int pad_items = (ok_mt && xs != nullptr) ? MT * groups : 0;
+    uint4* xc = reinterpret_cast<uint4*>(p.Xc);
+    const bool ok_pc = PC >= 0 && PC <= s.PC_max;
+    const int groups = BM / 8;
+    const int pad_items = (ok_pc && xs != nullptr) ? E * groups : 0;
 
     for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < s.T + pad_items; item += nwarps) {
         if (item < s.T) {
             const int t = item, r = t / per, c = t / s.chunk_tokens;
-            int my_slot = 0;
+            int my_cs = 0;
             if (lane < k) {
                 const int e = p.idx[(size_t)t * k + lane];
                 const int rk = p.chunk_base[(size_t)c * E + e] + p.rank[(size_t)t * k + lane];
-                my_slot = p.offsets[e * R + r] + rk;
-                p.slot[(size_t)t * k + lane] = my_slot;
+                my_cs = p.ccoff[e * R + r] + rk;
+                p.slot[(size_t)t * k + lane] = p.offsets[e * R + r] + rk;
+                p.cslot[(size_t)t * k + lane] = my_cs;
                 p.ret_slot[(size_t)t * k + lane] = r * slice + p.ret_off[r * (E + 1) + e] + rk;
             }
-            int sl[KMAX];
+            int cs[KMAX];
 #pragma unroll
-            for (int j = 0; j < KMAX; ++j) sl[j] = __shfl_sync(0xffffffffu, my_slot, j);
-            bool good = true;
+            for (int j = 0; j < KMAX; ++j) cs[j] = __shfl_sync(0xffffffffu, my_cs, j);
+            bool good = ok_pc;
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                if (j < k) good &= (sl[j] >= 0 && sl[j] < s.P_max);
+                if (j < k) good &= (cs[j] >= 0 && cs[j] < PC);
             if (!good) {
                 if (lane == 0) set_status(p.meta, ST_BAD_PLAN, t);
                 continue;
@@ -411,25 +439,28 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
 #pragma unroll
                     for (int i = 0; i < PERM_VEC; ++i) {
                         const int vi = base + i * 32 + lane;
-                        if (vi < vec) xp[(size_t)sl[j] * vec + vi] = v[i];
+                        if (vi < vec) xc[(size_t)cs[j] * vec + vi] = v[i];
                     }
                 }
             }
         } else {
-            const int q = item - s.T, m = q / groups, g = q % groups;
-            const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
+            // the expert's run is [cb, cb + iu * BM) and holds `rows` real rows
+            const int q = item - s.T, e = q / groups, g = q % groups;
+            const int iu = p.experts[8 * e + 4], cb = p.experts[8 * e + 7];
+            const int rows = p.ccoff[e * R + R - 1] + p.counts[e * R + R - 1] - cb;
+            if (iu <= 0) continue;
             const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int rr = max(valid, g * 8); rr < (g + 1) * 8; ++rr) {
-                const size_t row = (size_t)row0 + rr;
-                if (row >= (size_t)s.P_max) break;
-                for (int v = lane; v < vec; v += 32) xp[row * vec + v] = z;
+            for (int rr = max(rows, (iu - 1) * BM + g * 8); rr < (iu - 1) * BM + (g + 1) * 8; ++rr) {
+                const size_t row = (size_t)cb + rr;
+                if (row >= (size_t)PC) break;
+                for (int v = lane; v < vec; v += 32) xc[row * vec + v] = z;
             }
         }
     }
 }
 
 cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtrs& p, int sms, cudaStream_t st) {
-    const int items = s.T + s.MT_max * (s.tbM / 8);
+    const int items = s.T + s.E * (BM / 8);
     const int blocks = min((items + 7) / 8, sms * 16);
     permute_kernel<<<blocks, 256, 0, st>>>(s, x, p);
     return cudaGetLastError();
