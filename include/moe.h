@@ -135,9 +135,9 @@ typedef struct moe_layout {
     size_t Hc;         /* bf16 [PC_max, ffn] SwiGLU hidden, same rows                          */
     size_t Yp;         /* bf16 [P_max, d]   expert outputs                                     */
     size_t Ret;        /* bf16 [T*topk, d]  owner return buffers, R slices of (T/R)*topk rows  */
-    size_t in_logits;  /* f32  [T, E]       staging for moe_forward_host                       */
-    size_t in_x;       /* bf16 [T, d]       staging for moe_forward_host                       */
-    size_t out;        /* f32  [T, d]       staging for moe_forward_host                       */
+    size_t in_logits;  /* f32  [2, T, E]    staging for moe_forward_host(_pipelined), 2 slots   */
+    size_t in_x;       /* bf16 [2, T, d]    staging for moe_forward_host(_pipelined), 2 slots   */
+    size_t out;        /* f32  [2, T, d]    staging for moe_forward_host(_pipelined), 2 slots   */
 } moe_layout;
 
 /* Trace slots (uint64 ns, %globaltimer) written by the last moe_forward / _sequential call. */
@@ -233,6 +233,21 @@ MOE_API int moe_forward_ex(const moe_config* cfg, const float* logits, const uin
 MOE_API int moe_forward_host(const moe_config* cfg, const float* logits_h, const uint16_t* x_h,
                              const uint16_t* W1, const uint16_t* W3, const uint16_t* W2, float* out_h,
                              void* ws, size_t ws_bytes, int sequential, void* stream);
+
+/*
+ * moe_forward_host_pipelined: `steps` independent batches of the same shape through the layer,
+ * each with its own host inputs and output (arrays of `steps` host pointers; pinned memory), with
+ * the transfers of neighbouring batches overlapped with the layer: the inputs of batch i+1 are
+ * copied in and the output of batch i-1 is copied out on two internal streams while batch i runs
+ * on `stream`, through two staging slots in the workspace. Results equal `steps` calls of
+ * moe_forward_host. Every out_h[i] is valid once `stream` has reached the end of this call; the
+ * host inputs must stay unchanged until then. No counterpart in the method's pages: the serving
+ * loop around the layer.
+ */
+MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const float* const* logits_h,
+                                       const uint16_t* const* x_h, const uint16_t* W1, const uint16_t* W3,
+                                       const uint16_t* W2, float* const* out_h, void* ws, size_t ws_bytes,
+                                       int sequential, void* stream);
 
 /*
  * moe_status: synchronises `stream`, then reads the device status word of the last call that used

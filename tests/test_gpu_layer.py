@@ -118,6 +118,30 @@ def test_forward_host_equals_device_forward():
     assert torch.equal(out_h, want)
 
 
+@pytest.mark.parametrize("sequential", [False, True])
+def test_forward_host_pipelined_equals_device_forward(sequential):
+    """Four batches with different tokens and routing through the pipelined host call (both staging
+    slots used twice): each output equals the device forward of its batch."""
+    w = small("mixtral")
+    L = Layer(w, seed=2, cfg_kw=dict(consumer_ctas=8))
+    seeds = (2, 5, 7, 11)
+    logits_h, x_h, want = [], [], []
+    for sd in seeds:
+        lg, x = inputs.make_logits(w, sd), inputs.make_x(w, sd)
+        tlc.forward(L.cfg, torch.from_numpy(lg).cuda(), x.cuda(), L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws,
+                    sequential=sequential)
+        want.append(L.out.cpu().clone())
+        logits_h.append(torch.from_numpy(lg).pin_memory())
+        x_h.append(x.pin_memory())
+    out_h = [torch.full((w.T, w.d), float("nan")).pin_memory() for _ in seeds]
+    tlc.forward_host_pipelined(L.cfg, logits_h, x_h, L.W["W1"], L.W["W3"], L.W["W2"], out_h, L.ws,
+                               sequential=sequential)
+    torch.cuda.synchronize()
+    assert tlc.status(L.cfg, L.ws)[0] == tlc.MOE_OK
+    for got, ref in zip(out_h, want):
+        assert torch.equal(got, ref)
+
+
 def test_argument_errors_on_gpu():
     w = small("tiny")
     L = Layer(w, seed=0)

@@ -35,7 +35,7 @@ TRACE_BAND_DONE, TRACE_LAST_ACQUIRE, TRACE_LAST_LOAD, TRACE_LAST_DRAIN = 4, 5, 6
 
 # names of the C entry points (each declared in include/moe.h)
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_plan", "moe_forward", "moe_forward_sequential",
-           "moe_forward_ex", "moe_forward_host", "moe_status", "moe_device_info", "moe_route_static",
+           "moe_forward_ex", "moe_forward_host", "moe_forward_host_pipelined", "moe_status", "moe_device_info", "moe_route_static",
            "moe_last_error")
 
 # stage events of moe_forward_ex
@@ -111,6 +111,8 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_sequential.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.moe_forward_ex.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, ctypes.c_int, ctypes.POINTER(vp), vp]
         L.moe_forward_host.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, ctypes.c_int, vp]
+        L.moe_forward_host_pipelined.argtypes = [cfgp, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp,
+                                                 vp, ctypes.POINTER(vp), vp, sz, ctypes.c_int, vp]
         L.moe_status.argtypes = [cfgp, vp, vp, i32p]
         L.moe_device_info.argtypes = [i32p, i32p]
         L.moe_route_static.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp]
@@ -248,6 +250,24 @@ def forward_host(cfg: Config, logits_h: torch.Tensor, x_h: torch.Tensor, W1: tor
                                   _ptr(W3, bf, "cuda", "W3"), _ptr(W2, bf, "cuda", "W2"),
                                   _ptr(out_h, torch.float32, "cpu", "out_h"), ws.ptr, ws.nbytes,
                                   1 if sequential else 0, _stream(stream)))
+
+
+def forward_host_pipelined(cfg: Config, logits_h, x_h, W1: torch.Tensor, W3: torch.Tensor, W2: torch.Tensor,
+                           out_h, ws: Workspace, sequential: bool = False, stream=None) -> None:
+    """moe_forward_host_pipelined: len(out_h) batches, host inputs / outputs given as lists of pinned
+    tensors (one per batch), transfers of neighbouring batches overlapped with the layer."""
+    c = cfg.to_c()
+    bf = torch.bfloat16
+    n = len(out_h)
+    if len(logits_h) != n or len(x_h) != n:
+        raise ValueError("logits_h, x_h and out_h must have one entry per batch")
+    arr = ctypes.c_void_p * max(n, 1)
+    pl = arr(*[_ptr(t, torch.float32, "cpu", "logits_h") for t in logits_h])
+    px = arr(*[_ptr(t, bf, "cpu", "x_h") for t in x_h])
+    po = arr(*[_ptr(t, torch.float32, "cpu", "out_h") for t in out_h])
+    _check(lib().moe_forward_host_pipelined(ctypes.byref(c), n, pl, px, _ptr(W1, bf, "cuda", "W1"),
+                                            _ptr(W3, bf, "cuda", "W3"), _ptr(W2, bf, "cuda", "W2"), po, ws.ptr,
+                                            ws.nbytes, 1 if sequential else 0, _stream(stream)))
 
 
 def status(cfg: Config, ws: Workspace, stream=None):

@@ -120,9 +120,9 @@ int make_layout(const moe_config* c, Layout* out) {
     L.Hc = put((size_t)PC_max * F * 2);
     L.Yp = put((size_t)P_max * d * 2);
     L.Ret = put((size_t)TK * d * 2);
-    L.in_logits = put((size_t)T * E * 4);
-    L.in_x = put((size_t)T * d * 2);
-    L.out = put((size_t)T * d * 4);
+    L.in_logits = put(2 * (size_t)T * E * 4);
+    L.in_x = put(2 * (size_t)T * d * 2);
+    L.out = put(2 * (size_t)T * d * 4);
     L.bytes = cur;
 
     Shape& S = o.S;
@@ -464,6 +464,82 @@ MOE_API int moe_forward_host(const moe_config* cfg, const float* logits_h, const
     if (rc) return rc;
     e = cudaMemcpyAsync(out_h, d_out, T * cfg->d * 4, cudaMemcpyDeviceToHost, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of the output");
+    return MOE_OK;
+}
+
+// Internal copy streams and events of the pipelined host entry, created once per device.
+struct HostPipe {
+    cudaStream_t cin = nullptr, cout = nullptr;
+    cudaEvent_t in_done[2], out_ready[2], out_free[2], slot_free[2];
+    bool ok = false;
+};
+
+static int host_pipe(HostPipe** out) {
+    static HostPipe pipes[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(MOE_ERR_DEVICE, "device index %d out of range", dev);
+    HostPipe& h = pipes[dev];
+    if (!h.ok) {
+        e = cudaStreamCreateWithFlags(&h.cin, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.cout, cudaStreamNonBlocking);
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+            e = cudaEventCreateWithFlags(&h.in_done[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.out_ready[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.out_free[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.slot_free[i], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "creating the copy streams and events");
+        h.ok = true;
+    }
+    *out = &h;
+    return MOE_OK;
+}
+
+MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const float* const* logits_h,
+                                       const uint16_t* const* x_h, const uint16_t* W1, const uint16_t* W3,
+                                       const uint16_t* W2, float* const* out_h, void* ws, size_t ws_bytes,
+                                       int sequential, void* stream) {
+    Call c;
+    int rc = begin_call(cfg, ws, ws_bytes, stream, &c);
+    if (rc) return rc;
+    if (steps < 0) return fail(MOE_ERR_ARG, "steps=%d must be >= 0", steps);
+    if (steps > 0 && (!logits_h || !x_h || !out_h)) return fail(MOE_ERR_ARG, "NULL host pointer array");
+    for (int i = 0; i < steps; ++i)
+        if (!logits_h[i] || !x_h[i] || !out_h[i]) return fail(MOE_ERR_ARG, "NULL host pointer (step %d)", i);
+    HostPipe* h = nullptr;
+    if ((rc = host_pipe(&h))) return rc;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    const size_t T = cfg->T, nl = T * cfg->E * 4, nx = T * cfg->d * 2, no = T * cfg->d * 4;
+    cudaError_t e = cudaSuccess;
+    // slot s of step i: its inputs go in after the layer of step i-2 (which read slot s) is done; its
+    // layer waits for them and for the copy-out of step i-2 (which read slot s's output)
+    for (int i = 0; i < steps && e == cudaSuccess; ++i) {
+        const int sl = i & 1;
+        float* d_logits = reinterpret_cast<float*>(b + c.lay.L.in_logits + sl * nl);
+        uint16_t* d_x = reinterpret_cast<uint16_t*>(b + c.lay.L.in_x + sl * nx);
+        float* d_out = reinterpret_cast<float*>(b + c.lay.L.out + sl * no);
+        if (i == 0) e = cudaEventRecord(h->slot_free[0], c.st);  // the caller's earlier work on the workspace
+        if (i == 0 && e == cudaSuccess) e = cudaEventRecord(h->slot_free[1], c.st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->cin, h->slot_free[sl], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(d_logits, logits_h[i], nl, cudaMemcpyHostToDevice, h->cin);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(d_x, x_h[i], nx, cudaMemcpyHostToDevice, h->cin);
+        if (e == cudaSuccess) e = cudaEventRecord(h->in_done[sl], h->cin);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(c.st, h->in_done[sl], 0);
+        if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(c.st, h->out_free[sl], 0);
+        if (e != cudaSuccess) break;
+        rc = run_forward(c, d_logits, reinterpret_cast<const uint16_t*>(d_x), W1, W3, W2, d_out, sequential == 0);
+        if (rc) return rc;
+        e = cudaEventRecord(h->out_ready[sl], c.st);
+        if (e == cudaSuccess) e = cudaEventRecord(h->slot_free[sl], c.st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(h->cout, h->out_ready[sl], 0);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(out_h[i], d_out, no, cudaMemcpyDeviceToHost, h->cout);
+        if (e == cudaSuccess) e = cudaEventRecord(h->out_free[sl], h->cout);
+    }
+    // the caller's stream reaches the end of this call only after every copy-out
+    for (int sl = 0; sl < 2 && e == cudaSuccess && steps > sl; ++sl) e = cudaStreamWaitEvent(c.st, h->out_free[sl], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "pipelined host copies");
     return MOE_OK;
 }
 
