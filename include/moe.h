@@ -203,6 +203,16 @@ MOE_API int moe_forward_sequential(const moe_config* cfg, const float* logits, c
                                    void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_copy_only: the return copy alone (every valid row of every band of Yp into its owner's slice
+ * of Ret, 16 KB TMA bulk copies through shared memory) on `ctas` CTAs, one per SM, for measuring
+ * the copy's bandwidth against the size of the consumer partition ([TLS "What carries the
+ * argument"]: the consumer's SM budget c_CTA). Uses the plan and Yp of the last moe_forward /
+ * moe_forward_sequential on `ws`; writes only Ret and a work counter. 1 <= ctas <= SMs, else
+ * MOE_ERR_ARG.
+ */
+MOE_API int moe_copy_only(const moe_config* cfg, void* ws, size_t ws_bytes, int ctas, void* stream);
+
+/*
  * moe_forward_ex: moe_forward (sequential == 0) or moe_forward_sequential (sequential != 0) that
  * also records caller-created CUDA events (cudaEvent_t passed as void*) on `stream` between the
  * launches, for per-stage timing; stage_events may be NULL, and so may any entry:

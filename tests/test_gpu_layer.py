@@ -142,6 +142,22 @@ def test_forward_host_pipelined_equals_device_forward(sequential):
         assert torch.equal(got, ref)
 
 
+def test_copy_only_reproduces_the_return_copy():
+    """moe_copy_only on a few SMs rewrites Ret exactly as the forward's copy did."""
+    w = small("skew")
+    L = Layer(w, seed=3)
+    L.run(sequential=True)
+    want = L.ws.view("Ret").clone()
+    for ctas in (1, 3, 16):
+        L.ws.view("Ret").zero_()
+        tlc.copy_only(L.cfg, L.ws, ctas)
+        assert tlc.status(L.cfg, L.ws)[0] == tlc.MOE_OK
+        assert torch.equal(L.ws.view("Ret"), want)
+    with pytest.raises(tlc.MoEError) as ei:
+        tlc.copy_only(L.cfg, L.ws, 0)
+    assert ei.value.code == tlc.MOE_ERR_ARG
+
+
 def test_argument_errors_on_gpu():
     w = small("tiny")
     L = Layer(w, seed=0)

@@ -35,7 +35,7 @@ TRACE_BAND_DONE, TRACE_LAST_ACQUIRE, TRACE_LAST_LOAD, TRACE_LAST_DRAIN = 4, 5, 6
 
 # names of the C entry points (each declared in include/moe.h)
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_plan", "moe_forward", "moe_forward_sequential",
-           "moe_forward_ex", "moe_forward_host", "moe_forward_host_pipelined", "moe_status", "moe_device_info", "moe_route_static",
+           "moe_forward_ex", "moe_forward_host", "moe_forward_host_pipelined", "moe_copy_only", "moe_status", "moe_device_info", "moe_route_static",
            "moe_last_error")
 
 # stage events of moe_forward_ex
@@ -113,6 +113,7 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_host.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, ctypes.c_int, vp]
         L.moe_forward_host_pipelined.argtypes = [cfgp, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp,
                                                  vp, ctypes.POINTER(vp), vp, sz, ctypes.c_int, vp]
+        L.moe_copy_only.argtypes = [cfgp, vp, sz, ctypes.c_int, vp]
         L.moe_status.argtypes = [cfgp, vp, vp, i32p]
         L.moe_device_info.argtypes = [i32p, i32p]
         L.moe_route_static.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp]
@@ -268,6 +269,12 @@ def forward_host_pipelined(cfg: Config, logits_h, x_h, W1: torch.Tensor, W3: tor
     _check(lib().moe_forward_host_pipelined(ctypes.byref(c), n, pl, px, _ptr(W1, bf, "cuda", "W1"),
                                             _ptr(W3, bf, "cuda", "W3"), _ptr(W2, bf, "cuda", "W2"), po, ws.ptr,
                                             ws.nbytes, 1 if sequential else 0, _stream(stream)))
+
+
+def copy_only(cfg: Config, ws: Workspace, ctas: int, stream=None) -> None:
+    """moe_copy_only: the return copy of the last forward on ws, alone, on `ctas` SMs."""
+    c = cfg.to_c()
+    _check(lib().moe_copy_only(ctypes.byref(c), ws.ptr, ws.nbytes, int(ctas), _stream(stream)))
 
 
 def status(cfg: Config, ws: Workspace, stream=None):

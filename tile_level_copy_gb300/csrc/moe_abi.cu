@@ -436,6 +436,17 @@ MOE_API int moe_forward_sequential(const moe_config* cfg, const float* logits, c
     return run_forward(c, logits, x, W1, W3, W2, out, false);
 }
 
+MOE_API int moe_copy_only(const moe_config* cfg, void* ws, size_t ws_bytes, int ctas, void* stream) {
+    Call c;
+    const int rc = begin_call(cfg, ws, ws_bytes, stream, &c);
+    if (rc) return rc;
+    if (ctas < 1 || ctas > c.di.sms) return fail(MOE_ERR_ARG, "ctas=%d must be in [1, %d]", ctas, c.di.sms);
+    cudaError_t e = cudaMemsetAsync(c.p.meta + META_QUEUE_SEQ, 0, sizeof(int32_t), c.st);
+    if (e == cudaSuccess) e = launch_copy_seq(c.lay.S, c.p, ctas, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "copy-only launch");
+    return MOE_OK;
+}
+
 MOE_API int moe_forward_ex(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
                            const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes, int sequential,
                            void* const* stage_events, void* stream) {

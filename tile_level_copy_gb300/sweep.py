@@ -1,12 +1,18 @@
-"""Consumer-partition sweep of the Mixtral-shaped layer (tokens x consumer CTAs x owners).
+"""Consumer-partition study of the Mixtral-shaped layer on one GB300.
 
 The tile-level signaling page sweeps the consumer SM budget c_CTA from 2 to 24 and reports layer
-latency against a GEMM-then-transfer baseline (its Figure 9) and the overlap ratio as experts per
-rank vary (Figure 4b). This module measures the same on one GB300: for every (T, c, R) the
-overlapped layer, the sequential layer, the copy alone, the exposed copy tail and the hidden
-fraction. One JSON object per point on stdout.
+latency against a GEMM-then-transfer baseline (its Figure 9), the overlap ratio as experts per rank
+vary (Figure 4b), and the consumer's copy bandwidth and segment size (mgb). This module measures
+the same on one GB300, in three parts (one JSON object per point on stdout, "part" names it):
 
-  python -m tile_level_copy_gb300.sweep [--tokens 1024 4096 ...] [--consumers 4 8 ...] [--owners 2 4 8]
+  layer  for every (T, R, c): the overlapped layer, the GEMM-then-copy layer, the copy alone, the
+         exposed copy tail, the hidden fraction, and the GEMM slowdown of taking c SMs from the
+         down-projection (its producer span over the span of the same GEMM on all SMs)
+  mgb    at T=4096, R=4: hidden fraction and tail against the segment size mgb and c
+  copy   the return copy alone on c SMs (moe_copy_only): copy bandwidth against c
+
+  python -m tile_level_copy_gb300.sweep [--parts layer mgb copy] [--tokens 1024 4096 ...]
+      [--consumers 4 8 ...] [--owners 2 4 8] [--mgbs 1 2 4] [--copy-ctas 1 2 4 ...]
 """
 from __future__ import annotations
 
@@ -60,39 +66,49 @@ def time_steps(cfg, args_, ws, seq: bool, steps: int, warmup: int):
     return float(np.median(st.sum(1))), np.median(st, 0)
 
 
-def main():
-    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--tokens", type=int, nargs="+", default=[1024, 4096, 16384, 32768])
-    ap.add_argument("--consumers", type=int, nargs="+", default=[4, 8, 16, 24, 32])
-    ap.add_argument("--owners", type=int, nargs="+", default=[2, 4, 8])
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--no-tail-assist", action="store_true")
-    a = ap.parse_args()
+def trace_of(cfg, args_, ws, seq: bool, reps: int = 5):
+    """Median over reps of (copy tail after the last flag, down-projection span) in ms."""
+    tails, spans = [], []
+    for _ in range(reps):
+        tlc.forward(cfg, *args_, ws, sequential=seq)
+        torch.cuda.synchronize()
+        tr = ws.view("trace").cpu().numpy().astype(np.int64)
+        tails.append(max(0, int(tr[tlc.TRACE_COPY_END]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e6)
+        spans.append((int(tr[tlc.TRACE_GEMM2_END]) - int(tr[tlc.TRACE_GEMM2_START])) / 1e6)
+    return statistics.median(tails), statistics.median(spans)
 
-    build.build()
-    dev = torch.device("cuda")
-    base = inputs.WORKLOADS["mixtral"]
-    W = {}
-    for n in ("W1", "W3", "W2"):
-        shape = (base.E, base.ffn, base.d) if n != "W2" else (base.E, base.d, base.ffn)
-        W[n] = torch.empty(shape, dtype=torch.bfloat16, device=dev)
-        inputs.make_weight_into(base, 0, n, W[n])
-    flags = 0 if a.no_tail_assist else tlc.MOE_TAIL_ASSIST
+
+class Setup:
+    """Mixtral-shaped weights on the device, inputs per (T, R)."""
+
+    def __init__(self):
+        build.build()
+        self.dev = torch.device("cuda")
+        self.base = inputs.WORKLOADS["mixtral"]
+        self.W = {}
+        for n in ("W1", "W3", "W2"):
+            b = self.base
+            shape = (b.E, b.ffn, b.d) if n != "W2" else (b.E, b.d, b.ffn)
+            self.W[n] = torch.empty(shape, dtype=torch.bfloat16, device=self.dev)
+            inputs.make_weight_into(b, 0, n, self.W[n])
+
+    def layer(self, T, R):
+        w = self.base.replace(T=T, R=R)
+        logits = torch.from_numpy(inputs.make_logits(w, 0)).to(self.dev)
+        x = inputs.make_x(w, 0).to(self.dev)
+        out = torch.empty(T, w.d, dtype=torch.float32, device=self.dev)
+        return w, (logits, x, self.W["W1"], self.W["W3"], self.W["W2"], out)
+
+
+def part_layer(S: Setup, a, flags):
     for T in a.tokens:
-        out = torch.empty(T, base.d, dtype=torch.float32, device=dev)
         for R in a.owners:
-            w = base.replace(T=T, R=R)
-            logits = torch.from_numpy(inputs.make_logits(w, 0)).to(dev)
-            x = inputs.make_x(w, 0).to(dev)
-            cfg0 = tlc.Config.from_workload(w, consumer_ctas=8, flags=flags)
-            ws = tlc.Workspace(cfg0, dev)
-            args_ = (logits, x, W["W1"], W["W3"], W["W2"], out)
+            w, args_ = S.layer(T, R)
+            ws = tlc.Workspace(tlc.Config.from_workload(w, consumer_ctas=8, flags=flags), S.dev)
             for c in a.consumers:
                 cfg = tlc.Config.from_workload(w, consumer_ctas=c, flags=flags)
-                # sequential and overlapped measured in alternation, so both see the same clocks
                 seqs, ovls, copies = [], [], []
-                with ClockWatch() as clk:
+                with ClockWatch() as clk:  # sequential and overlapped in alternation: same clocks
                     for _ in range(2):
                         seq_ms, seq_st = time_steps(cfg, args_, ws, True, a.steps, a.warmup)
                         ovl_ms, _ = time_steps(cfg, args_, ws, False, a.steps, a.warmup)
@@ -100,20 +116,88 @@ def main():
                         ovls.append(ovl_ms)
                         copies.append(float(seq_st[tlc.EV_DOWN]))
                 seq_ms, ovl_ms, copy_ms = min(seqs), min(ovls), statistics.median(copies)
-                tails = []
-                for _ in range(5):
-                    tlc.forward(cfg, *args_, ws)
-                    torch.cuda.synchronize()
-                    tr = ws.view("trace").cpu().numpy().astype(np.int64)
-                    tails.append(max(0, int(tr[tlc.TRACE_COPY_END]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e6)
-                tail = statistics.median(tails)
-                print(json.dumps({"T": T, "R": R, "consumer_ctas": c, "tail_assist": not a.no_tail_assist,
+                tail, span_ovl = trace_of(cfg, args_, ws, False)
+                _, span_seq = trace_of(cfg, args_, ws, True)
+                print(json.dumps({"part": "layer", "T": T, "R": R, "consumer_ctas": c,
+                                  "copy_warps": bool(flags & tlc.MOE_COPY_WARPS),
                                   "overlapped_ms": round(ovl_ms, 4), "sequential_ms": round(seq_ms, 4),
                                   "copy_alone_ms": round(copy_ms, 4), "tail_ms": round(tail, 4),
                                   "hidden_pct": round(100 * (1 - tail / copy_ms), 2),
                                   "speedup": round(seq_ms / ovl_ms, 4),
+                                  "gemm_span_overlapped_ms": round(span_ovl, 4),
+                                  "gemm_span_all_sms_ms": round(span_seq, 4),
+                                  "gemm_slowdown": round(span_ovl / span_seq, 4),
                                   "tokens_per_s": round(T / ovl_ms * 1e3, 1), "sm_mhz": clk.median()}), flush=True)
             del ws
+
+
+def part_mgb(S: Setup, a, flags):
+    w, args_ = S.layer(4096, 4)
+    ws = tlc.Workspace(tlc.Config.from_workload(w, consumer_ctas=8, flags=flags, mgb=max(a.mgbs)), S.dev)
+    for mgb in a.mgbs:
+        for c in a.consumers:
+            cfg = tlc.Config.from_workload(w, consumer_ctas=c, flags=flags, mgb=mgb)
+            ovl_ms, _ = time_steps(cfg, args_, ws, False, a.steps, a.warmup)
+            _, seq_st = time_steps(cfg, args_, ws, True, a.steps, a.warmup)
+            tail, _ = trace_of(cfg, args_, ws, False)
+            copy_ms = float(seq_st[tlc.EV_DOWN])
+            print(json.dumps({"part": "mgb", "T": 4096, "R": 4, "mgb": mgb, "consumer_ctas": c,
+                              "overlapped_ms": round(ovl_ms, 4), "copy_alone_ms": round(copy_ms, 4),
+                              "tail_ms": round(tail, 4), "hidden_pct": round(100 * (1 - tail / copy_ms), 2)}),
+                  flush=True)
+
+
+def part_copy(S: Setup, a):
+    w, args_ = S.layer(4096, 4)
+    cfg = tlc.Config.from_workload(w, consumer_ctas=8)
+    ws = tlc.Workspace(cfg, S.dev)
+    tlc.forward(cfg, *args_, ws, sequential=True)  # plan and Yp in the workspace
+    nbytes = 2 * w.T * w.topk * w.d * 2              # every real row read from Yp and written to Ret
+    sms, _ = tlc.device_info()
+    for c in a.copy_ctas:
+        if c > sms:
+            continue
+        for _ in range(a.warmup):
+            tlc.copy_only(cfg, ws, c)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(a.steps):
+            t0.record()
+            tlc.copy_only(cfg, ws, c)
+            t1.record()
+            torch.cuda.synchronize()
+            times.append(t0.elapsed_time(t1))
+        rc, detail = tlc.status(cfg, ws)
+        if rc != tlc.MOE_OK:
+            raise RuntimeError(f"device status {rc} ({detail})")
+        ms = statistics.median(times)
+        print(json.dumps({"part": "copy", "T": 4096, "R": 4, "ctas": c, "copy_ms": round(ms, 4),
+                          "bytes": nbytes, "gb_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                          "gb_per_s_per_sm": round(nbytes / (ms * 1e-3) / 1e9 / c, 2)}), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--parts", nargs="+", default=["layer", "mgb", "copy"], choices=["layer", "mgb", "copy"])
+    ap.add_argument("--tokens", type=int, nargs="+", default=[1024, 4096, 16384, 32768])
+    ap.add_argument("--consumers", type=int, nargs="+", default=[4, 8, 16, 24, 32])
+    ap.add_argument("--owners", type=int, nargs="+", default=[2, 4, 8])
+    ap.add_argument("--mgbs", type=int, nargs="+", default=[1, 2, 4])
+    ap.add_argument("--copy-ctas", type=int, nargs="+", default=[1, 2, 4, 8, 16, 24, 32, 64, 152])
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--no-tail-assist", action="store_true")
+    ap.add_argument("--copy-warps", action="store_true", help="also run copy warps in the producer CTAs")
+    a = ap.parse_args()
+
+    flags = (0 if a.no_tail_assist else tlc.MOE_TAIL_ASSIST) | (tlc.MOE_COPY_WARPS if a.copy_warps else 0)
+    S = Setup()
+    if "copy" in a.parts:
+        part_copy(S, a)
+    if "mgb" in a.parts:
+        part_mgb(S, a, flags)
+    if "layer" in a.parts:
+        part_layer(S, a, flags)
 
 
 if __name__ == "__main__":
