@@ -60,6 +60,49 @@ def test_layer_matches_oracle_small_shapes(name):
 CW = tlc.MOE_COPY_WARPS
 
 
+EDGE_SHAPES = [
+    dict(T=8, d=128, ffn=128, E=1, topk=1, R=1, tile_M=64),      # one group, one ragged tile, N tiles of 128
+    dict(T=6, d=128, ffn=128, E=3, topk=2, R=3, tile_M=128),     # T/R = 2: chunks of 2 tokens
+    dict(T=300, d=256, ffn=128, E=5, topk=3, R=5, tile_M=64),    # 64-row bands, uneven groups
+    dict(T=1000, d=128, ffn=256, E=256, topk=8, R=4, tile_M=128),  # max E, max k, mostly 1-row groups
+    dict(T=64, d=128, ffn=128, E=16, topk=1, R=64, tile_M=128),  # one token per owner
+    dict(T=512, d=384, ffn=384, E=6, topk=2, R=2, tile_M=128),   # d, ffn not multiples of 256
+]
+
+
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda sh: "-".join(f"{k}{v}" for k, v in sh.items()))
+def test_layer_edge_shapes(shape):
+    """Degenerate and extreme shapes through the whole layer: oracle parity, and the overlapped path
+    (dedicated consumers; copy warps only; CTA-pair SwiGLU GEMM) bitwise equal to the sequential one."""
+    w = inputs.Workload("edge", **shape)
+    L = Layer(w, seed=4, cfg_kw=dict(consumer_ctas=4, timeout_us=500000))
+    ref = L.oracle_layer()
+    seq = L.run(sequential=True)
+    np.testing.assert_array_equal(L.ws.view("idx").cpu().numpy(), ref.idx)
+    err, rel = parity(seq.double().cpu().numpy(), ref.out)
+    assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
+    for c, flags in ((4, tlc.MOE_TAIL_ASSIST), (0, tlc.MOE_COPY_WARPS), (2, tlc.MOE_PAIR_UMMA)):
+        cfg = tlc.Config.from_workload(w, consumer_ctas=c, flags=flags, timeout_us=500000)
+        assert torch.equal(L.run(sequential=False, cfg=cfg), seq), (c, flags)
+    check_ret_is_copy_of_yp(L, ref.plan)
+
+
+def test_all_tokens_to_one_expert_layer():
+    """Every token routed to the same two experts: all other experts have no rows (no work items)."""
+    w = inputs.WORKLOADS["skew"].replace(T=2048, d=256, ffn=256)
+    L = Layer(w, seed=1, cfg_kw=dict(consumer_ctas=4))
+    lg = np.full((w.T, w.E), -5.0, np.float32)
+    lg[:, 7], lg[:, 2] = 1.0, 0.5
+    L.logits_np, L.logits = lg, torch.from_numpy(lg).cuda()
+    ref = L.oracle_layer()
+    seq = L.run(sequential=True)
+    err, rel = parity(seq.double().cpu().numpy(), ref.out)
+    assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
+    for flags in (tlc.MOE_TAIL_ASSIST, tlc.MOE_PAIR_UMMA):
+        cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=flags)
+        assert torch.equal(L.run(sequential=False, cfg=cfg), seq)
+
+
 @pytest.mark.parametrize("consumers,mgb,flags", [
     (1, 1, 0), (2, 2, 0), (4, 1, tlc.MOE_TAIL_ASSIST), (16, 2, tlc.MOE_TAIL_ASSIST), (32, 4, 0),
     (0, 1, CW), (0, 2, CW | tlc.MOE_TAIL_ASSIST), (4, 1, CW | tlc.MOE_TAIL_ASSIST), (8, 4, CW),
