@@ -6,31 +6,41 @@
 
 namespace moe {
 
-constexpr int KMAX_C = 8;
-
 // One warp per token; each lane handles 8 consecutive columns per step (16-byte bf16 loads,
-// two 16-byte fp32 stores).
-__global__ void __launch_bounds__(256) combine_kernel(Shape s, PlanPtrs p, float* __restrict__ out) {
+// two 16-byte fp32 stores). The k rows' loads of a step are all issued before any is used (and the
+// next token's slots and gates are fetched while the current token is combined), so each lane has
+// k loads in flight instead of one.
+template <int K>  // K = top-k, so that the per-lane arrays have exactly K entries
+__global__ void __launch_bounds__(256, 4) combine_kernel(Shape s, PlanPtrs p, float* __restrict__ out) {
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int vec = s.d / 8;
+    constexpr int k = K;
     const uint4* ret = reinterpret_cast<const uint4*>(p.Ret);
-    const int rows = s.T * s.k;
-    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < s.T; t += nwarps) {
-        int my_slot = 0;
-        float my_w = 0.f;
-        if (lane < s.k) {
-            my_slot = p.ret_slot[(size_t)t * s.k + lane];
-            my_w = p.gate[(size_t)t * s.k + lane];
+    const int rows = s.T * k;
+    int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    int nx_slot = 0;
+    float nx_w = 0.f;
+    if (t < s.T && lane < k) {
+        nx_slot = __ldg(p.ret_slot + (size_t)t * k + lane);
+        nx_w = __ldg(p.gate + (size_t)t * k + lane);
+    }
+    for (; t < s.T; t += nwarps) {
+        const int my_slot = nx_slot;
+        const float my_w = nx_w;
+        const int tn = t + nwarps;
+        if (tn < s.T && lane < k) {  // the next token's plan entries, in flight meanwhile
+            nx_slot = __ldg(p.ret_slot + (size_t)tn * k + lane);
+            nx_w = __ldg(p.gate + (size_t)tn * k + lane);
         }
-        int sl[KMAX_C];
-        float w[KMAX_C];
+        int sl[K];
+        float w[K];
         bool good = true;
 #pragma unroll
-        for (int j = 0; j < KMAX_C; ++j) {
+        for (int j = 0; j < K; ++j) {
             sl[j] = __shfl_sync(0xffffffffu, my_slot, j);
             w[j] = __shfl_sync(0xffffffffu, my_w, j);
-            if (j < s.k) good &= (sl[j] >= 0 && sl[j] < rows);
+            good &= (sl[j] >= 0 && sl[j] < rows);
         }
         if (!good) {
             if (lane == 0) set_status(p.meta, ST_BAD_PLAN, t);
@@ -38,12 +48,13 @@ __global__ void __launch_bounds__(256) combine_kernel(Shape s, PlanPtrs p, float
         }
         float4* o = reinterpret_cast<float4*>(out + (size_t)t * s.d);
         for (int v = lane; v < vec; v += 32) {
+            uint4 r[K];
+#pragma unroll
+            for (int j = 0; j < K; ++j) r[j] = ret[(size_t)sl[j] * vec + v];
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < KMAX_C; ++j) {
-                if (j >= s.k) break;
-                const uint4 r = ret[(size_t)sl[j] * vec + v];
-                const uint32_t q[4] = {r.x, r.y, r.z, r.w};
+            for (int j = 0; j < K; ++j) {
+                const uint32_t q[4] = {r[j].x, r[j].y, r[j].z, r[j].w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float lo = __uint_as_float(q[i] << 16);
@@ -60,7 +71,17 @@ __global__ void __launch_bounds__(256) combine_kernel(Shape s, PlanPtrs p, float
 
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st) {
     const int blocks = min((s.T + 7) / 8, sms * 8);
-    combine_kernel<<<blocks, 256, 0, st>>>(s, p, out);
+    switch (s.k) {
+        case 1: combine_kernel<1><<<blocks, 256, 0, st>>>(s, p, out); break;
+        case 2: combine_kernel<2><<<blocks, 256, 0, st>>>(s, p, out); break;
+        case 3: combine_kernel<3><<<blocks, 256, 0, st>>>(s, p, out); break;
+        case 4: combine_kernel<4><<<blocks, 256, 0, st>>>(s, p, out); break;
+        case 5: combine_kernel<5><<<blocks, 256, 0, st>>>(s, p, out); break;
+        case 6: combine_kernel<6><<<blocks, 256, 0, st>>>(s, p, out); break;
+        case 7: combine_kernel<7><<<blocks, 256, 0, st>>>(s, p, out); break;
+        case 8: combine_kernel<8><<<blocks, 256, 0, st>>>(s, p, out); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

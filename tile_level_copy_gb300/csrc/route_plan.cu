@@ -30,7 +30,20 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
     const int C = s.chunk_tokens, E = s.E, k = s.k, ld = E + 1;
     const int t0 = blockIdx.x * C;
     const float* src = logits + (size_t)t0 * E;
-    for (int i = threadIdx.x; i < C * E; i += ROUTE_THREADS) s_logit[(i / E) * ld + (i % E)] = __ldg(src + i);
+    const int n = C * E;
+    for (int i0 = threadIdx.x; i0 < n; i0 += ROUTE_THREADS * 8) {  // eight loads in flight per thread
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * ROUTE_THREADS;
+            v[u] = (i < n) ? __ldg(src + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * ROUTE_THREADS;
+            if (i < n) s_logit[(i / E) * ld + (i % E)] = v[u];
+        }
+    }
     __syncthreads();
 
     const bool live = tl < C;
@@ -117,6 +130,7 @@ cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p,
 // plan_kernel: one CTA of 1024 threads builds the whole plan from the per-chunk counts.
 // ---------------------------------------------------------------------------------------------
 constexpr int PLAN_THREADS = 1024;
+constexpr int PLAN_SMEM_TILES = 16384;  // tiles whose schedule and group fit in shared memory (128 KB)
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* s_total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -162,13 +176,36 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     const int cpo = (s.T / R) / s.chunk_tokens;  // chunks per owner
     const int slice = (s.T / R) * s.k;           // rows per owner slice of Ret
 
-    // 1. per group: chunk bases (exclusive prefix over the owner's chunks) and n_{e,r}
+    // Shared-memory copies of the schedule and of each tile's group, read by steps 6 and 7 (global
+    // memory when the tile count exceeds PLAN_SMEM_TILES).
+    extern __shared__ int s_dyn[];
+    const bool mirror = s.MT_max <= PLAN_SMEM_TILES;
+    int* s_sched = s_dyn;
+    int* s_tg = s_dyn + (mirror ? s.MT_max : 0);
+
+    // 1. per group: chunk bases (exclusive prefix over the owner's chunks) and n_{e,r}; the counts
+    // are read eight at a time so that their loads are in flight together
     for (int g = tid; g < G; g += PLAN_THREADS) {
         const int e = g / R, r = g % R;
+        const int32_t* __restrict__ cnt = p.chunk_cnt + e;
+        int32_t* __restrict__ base = p.chunk_base + e;
         int acc = 0;
-        for (int c = r * cpo; c < (r + 1) * cpo; ++c) {
-            p.chunk_base[(size_t)c * E + e] = acc;
-            acc += p.chunk_cnt[(size_t)c * E + e];
+        int c = r * cpo;
+        const int c_end = (r + 1) * cpo;
+        for (; c + 8 <= c_end; c += 8) {
+            int v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(cnt + (size_t)(c + i) * E);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                base[(size_t)(c + i) * E] = acc;
+                acc += v[i];
+            }
+        }
+        for (; c < c_end; ++c) {
+            const int v = __ldcg(cnt + (size_t)c * E);
+            base[(size_t)c * E] = acc;
+            acc += v;
         }
         s_n[g] = acc;
         p.counts[g] = acc;
@@ -267,7 +304,11 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             p.tiles[4 * m + 3] = valid;
             p.tile_ret[m] = rbase + i * tbM;
             p.tile_crow[m] = s_cc[g] + i * tbM;
-            if (i < nfull) p.sched[s_ebase[e] + fpre + i] = m;
+            if (mirror) s_tg[m] = g;
+            if (i < nfull) {
+                p.sched[s_ebase[e] + fpre + i] = m;
+                if (mirror) s_sched[s_ebase[e] + fpre + i] = m;
+            }
         }
         if (nt > nfull) {  // one partial band
             const int valid = n - nfull * tbM;
@@ -278,17 +319,23 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
                 pos += (vh > valid) || (vh == valid && rh < r);
             }
             p.sched[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
+            if (mirror) s_sched[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
         }
     }
     __syncthreads();
     __threadfence_block();
+    auto sched_at = [&](int pos) { return mirror ? s_sched[pos] : p.sched[pos]; };
+    auto group_of = [&](int m) { return mirror ? s_tg[m] : p.tiles[4 * m] * R + p.tiles[4 * m + 1]; };
+    auto valid_of = [&](int m) {  // valid rows of tile m, from its group's row count
+        const int g = group_of(m), i = m - s_off[g] / tbM;
+        return min(tbM, s_n[g] - i * tbM);
+    };
 
     // 6. segments: runs of adjacent bands of one group, cut into pieces of mgb bands
     for (int q = tid; q < MT; q += PLAN_THREADS) {
-        auto adjacent = [&](int a, int b) {
-            const int ma = p.sched[a], mb = p.sched[b];
-            return p.tiles[4 * ma] == p.tiles[4 * mb] && p.tiles[4 * ma + 1] == p.tiles[4 * mb + 1] &&
-                   p.tiles[4 * mb + 2] == p.tiles[4 * ma + 2] + tbM;
+        auto adjacent = [&](int a, int b) {  // same group, consecutive bands (rows tbM apart)
+            const int ma = sched_at(a), mb = sched_at(b);
+            return mb == ma + 1 && group_of(ma) == group_of(mb);
         };
         int start = q;
         while (start > 0 && adjacent(start - 1, start)) --start;
@@ -307,9 +354,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     // one 128-row band; mB == -1 one 64-row band alone; else two half bands; schedule order.
     __shared__ int s_items[MAX_E], s_ibase_down[MAX_E];
     for (int e = tid; e < E; e += PLAN_THREADS) {
-        const int m0 = s_off[e * R] / tbM, cnt = s_mt[e];
-        int half = 0;
-        for (int i = 0; i < cnt; ++i) half += (p.tiles[4 * (m0 + i) + 3] <= 64);
+        const int cnt = s_mt[e];
+        int half = 0;  // bands with <= 64 valid rows: all of them when tbM = 64, else partial ones
+        for (int r = 0; r < R; ++r) {
+            const int n = s_n[e * R + r];
+            half += (tbM == 64) ? (n + 63) / 64 : (n % 128 != 0 && n % 128 <= 64);
+        }
         s_items[e] = (cnt - half) + (half + 1) / 2;
     }
     __syncthreads();
@@ -334,8 +384,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         int* out = p.items_down + 2 * s_ibase_down[x];
         int n = 0, pending = -1;
         for (int i = 0; i < cnt; ++i) {
-            const int m = p.sched[s_ebase[x] + i];
-            if (p.tiles[4 * m + 3] > 64) {
+            const int m = sched_at(s_ebase[x] + i);
+            if (valid_of(m) > 64) {
                 out[2 * n] = m;
                 out[2 * n + 1] = m;
                 ++n;
@@ -377,7 +427,14 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
 }
 
 cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
-    plan_kernel<<<1, PLAN_THREADS, 0, st>>>(s, p);
+    const size_t smem = (s.MT_max <= PLAN_SMEM_TILES) ? (size_t)s.MT_max * 2 * sizeof(int) : 0;
+    if (smem > 0) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(reinterpret_cast<const void*>(&plan_kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    plan_kernel<<<1, PLAN_THREADS, smem, st>>>(s, p);
     return cudaGetLastError();
 }
 
