@@ -14,20 +14,24 @@ constexpr int ROUTE_THREADS = 128;   // one thread per token of a chunk of <= 12
 constexpr int KMAX = 8;
 
 // ---------------------------------------------------------------------------------------------
-// route_kernel: one CTA per chunk of `chunk_tokens` consecutive tokens (a chunk never straddles
-// two owners). The chunk's logits are staged in shared memory with coalesced loads (rows padded
-// to E+1 words against bank conflicts); then thread t, for token t of the chunk: top-k of the E
-// logits, descending, ties to the lower expert id, and gates = softmax over the k chosen logits in
-// fp32. Last, per expert, warp ballots give each token's rank among the chunk's tokens routed to
-// that expert (ascending token order) and the chunk's count per expert.
+// route_kernel<K>: one CTA per chunk of `chunk_tokens` consecutive tokens (a chunk never straddles
+// two owners), K = top-k. The chunk's logits are staged in shared memory with coalesced loads (rows
+// padded to E+1 words against bank conflicts); then thread t, for token t of the chunk, scans its E
+// logits once, keeping a sorted list of the K best (value descending, ties to the lower expert id:
+// a logit enters only if strictly greater than the list's last, and is inserted after every entry
+// not smaller than it), and forms the gates = softmax over the K chosen logits in fp32. Last, each
+// warp ORs its lanes into a per-expert lane mask in shared memory, which gives each token's rank
+// among the chunk's tokens routed to that expert (ascending token order) and the chunk's count per
+// expert.
 // ---------------------------------------------------------------------------------------------
+template <int K>
 __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const float* __restrict__ logits, PlanPtrs p) {
     extern __shared__ float s_logit[];  // [C][E + 1]
     __shared__ uint32_t s_mask[ROUTE_THREADS / 32][MAX_E];
     __shared__ int32_t s_wpre[ROUTE_THREADS / 32][MAX_E];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tl = threadIdx.x;
-    const int C = s.chunk_tokens, E = s.E, k = s.k, ld = E + 1;
+    const int C = s.chunk_tokens, E = s.E, ld = E + 1;
     const int t0 = blockIdx.x * C;
     const float* src = logits + (size_t)t0 * E;
     const int n = C * E;
@@ -45,58 +49,52 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
         }
     }
     __syncthreads();
+    for (int e = lane; e < E; e += 32) s_mask[warp][e] = 0u;
+    __syncwarp();
 
     const bool live = tl < C;
-    int sel_e[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) sel_e[j] = -1;
+    int te[K];
     if (live) {
         const float* row = s_logit + tl * ld;
-        float sel_v[KMAX];
-        float prev_v = INFINITY;
-        int prev_e = -1;
+        float tv[K];
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            if (j >= k) break;
-            // next in (value desc, id asc) order after (prev_v, prev_e)
-            float bv = -INFINITY;
-            int be = -1;
-            for (int e = 0; e < E; ++e) {
-                const float v = row[e];
-                const bool after = (v < prev_v) || (v == prev_v && e > prev_e);
-                if (after && (be < 0 || v > bv)) {
-                    bv = v;
-                    be = e;
+        for (int j = 0; j < K; ++j) {
+            tv[j] = -INFINITY;
+            te[j] = -1;
+        }
+        for (int e = 0; e < E; ++e) {
+            const float v = row[e];
+            if (te[K - 1] < 0 || v > tv[K - 1]) {
+                float cv = v;
+                int ce = e;
+                bool shift = false;  // from the insertion point on, every entry moves down one place
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    if (shift || te[j] < 0 || cv > tv[j]) {
+                        const float fv = tv[j];
+                        const int fe = te[j];
+                        tv[j] = cv;
+                        te[j] = ce;
+                        cv = fv;
+                        ce = fe;
+                        shift = true;
+                    }
                 }
             }
-            sel_v[j] = bv;
-            sel_e[j] = be;
-            prev_v = bv;
-            prev_e = be;
         }
-        float z[KMAX], sum = 0.f;
+        float z[K], sum = 0.f;
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            if (j >= k) break;
-            z[j] = expf(sel_v[j] - sel_v[0]);
+        for (int j = 0; j < K; ++j) {
+            z[j] = expf(tv[j] - tv[0]);
             sum += z[j];
         }
         const int t = t0 + tl;
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            if (j >= k) break;
-            p.idx[(size_t)t * k + j] = sel_e[j];
-            p.gate[(size_t)t * k + j] = z[j] / sum;
+        for (int j = 0; j < K; ++j) {
+            p.idx[(size_t)t * K + j] = te[j];
+            p.gate[(size_t)t * K + j] = z[j] / sum;
+            atomicOr(&s_mask[warp][te[j]], 1u << lane);
         }
-    }
-
-    // ranks: ballots per expert over the chunk's tokens
-    for (int e = 0; e < E; ++e) {
-        bool has = false;
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) has |= (sel_e[j] == e);
-        const uint32_t m = __ballot_sync(0xffffffffu, has);
-        if (lane == 0) s_mask[warp][e] = m;
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += ROUTE_THREADS) {
@@ -112,17 +110,26 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
         const uint32_t lt = (1u << lane) - 1u;
         const int t = t0 + tl;
 #pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            if (j >= k) break;
-            const int e = sel_e[j];
-            p.rank[(size_t)t * k + j] = s_wpre[warp][e] + __popc(s_mask[warp][e] & lt);
+        for (int j = 0; j < K; ++j) {
+            const int e = te[j];
+            p.rank[(size_t)t * K + j] = s_wpre[warp][e] + __popc(s_mask[warp][e] & lt);
         }
     }
 }
 
 cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p, cudaStream_t st) {
     const size_t smem = (size_t)s.chunk_tokens * (s.E + 1) * sizeof(float);
-    route_kernel<<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p);
+    switch (s.k) {
+        case 1: route_kernel<1><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
+        case 2: route_kernel<2><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
+        case 3: route_kernel<3><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
+        case 4: route_kernel<4><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
+        case 5: route_kernel<5><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
+        case 6: route_kernel<6><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
+        case 7: route_kernel<7><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
+        case 8: route_kernel<8><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
