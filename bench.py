@@ -79,8 +79,9 @@ def parse_args():
     ap.add_argument("--copy-warps", action=argparse.BooleanOptionalAction, default=None,
                     help="also run copy engines as extra warps in every producer CTA (consumers may then be 0; "
                          "default per workload, see DEFAULT_COPY)")
-    ap.add_argument("--pair-umma", action=argparse.BooleanOptionalAction, default=False,
-                    help="SwiGLU GEMM on CTA pairs (UMMA 256 x 256 over two SMs)")
+    ap.add_argument("--pair-umma", action=argparse.BooleanOptionalAction, default=True,
+                    help="SwiGLU GEMM on CTA pairs (UMMA 256 x 256 over two SMs; the default, the fastest "
+                         "measured on every workload)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -427,9 +427,9 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 // number of work items leaves the odd CTA without rows in its last pair tile (it still loads its
 // B half; its accumulator rows are not stored).
 //
-// Barriers: full[s] (this CTA's TMA bytes landed), empty[s] (UMMAs of the stage done; committed
-// to both CTAs), pready[s] on rank 0 (rank 1's stage s is full: rank 1's warp 1 relays its own
-// full[s] with a cluster-scope release arrive), acc_full[b] (committed to both CTAs), acc_empty[b]
+// Barriers: full[s] on rank 0 (the stage's bytes of both CTAs landed: rank 0 arms it with both
+// CTAs' byte counts, and rank 1's TMA loads complete on it through cta_group::2), empty[s] (UMMAs
+// of the stage done; committed to both CTAs), acc_full[b] (committed to both CTAs), acc_empty[b]
 // on rank 0 (count 8: the four epilogue warps of each CTA). Every wait is bounded; a timeout
 // raises the abort word of both CTAs.
 // =============================================================================================
@@ -438,7 +438,6 @@ struct PairSmem {
     uint8_t* epi;
     uint64_t* full;
     uint64_t* empty;
-    uint64_t* pready;
     uint64_t* acc_full;
     uint64_t* acc_empty;
     uint64_t* drain;
@@ -457,8 +456,7 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
     uint8_t* misc = sm.epi + EPI_BYTES;
     sm.full = reinterpret_cast<uint64_t*>(misc);
     sm.empty = sm.full + PAIR_STAGES;
-    sm.pready = sm.empty + PAIR_STAGES;
-    sm.acc_full = sm.pready + PAIR_STAGES;
+    sm.acc_full = sm.empty + PAIR_STAGES;
     sm.acc_empty = sm.acc_full + 2;
     sm.drain = sm.acc_empty + 2;
     sm.tmem_base = reinterpret_cast<uint32_t*>(sm.drain + 1);
@@ -519,7 +517,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         for (int i = 0; i < PAIR_STAGES; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], 1);
-            mbar_init(&sm.pready[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.acc_full[i], 1);
@@ -566,22 +563,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer (both CTAs): own A rows + own half of B ----------------
+        // Rank 0 arms its full barrier with the stage's bytes of both CTAs; rank 1's loads complete
+        // on that barrier (cta_group::2), so the UMMA issuer waits on one barrier per stage.
         int st = 0;
         uint32_t ph = 0, issued = 0, last_ph = 0;
         bool ok = true;
         for (int t = pair; t < total && ok && !bad; t += npairs) {
             const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, rank);
-            const uint32_t bytes = (tr.mA >= 0 ? PAIR_A_BYTES : 0) + PAIR_B_BYTES;
+            const TileRef tq = decode_pair_up(t, sm.tab, s.E, p.items_up, 1u);  // rank 1's rows
+            const uint32_t bytes = (tr.mA >= 0 ? PAIR_A_BYTES : 0) + (tq.mA >= 0 ? PAIR_A_BYTES : 0) + 2 * PAIR_B_BYTES;
             for (int kb = 0; kb < KB; ++kb) {
                 if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&sm.full[st], bytes);
                 uint8_t* a = sm.stages + st * PAIR_STAGE_BYTES;
                 uint8_t* b = a + PAIR_A_BYTES;
-                if (tr.mA >= 0) tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
-                tma_load_3d(b, rank == 0 ? &tmW1 : &tmW3, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
+                if (rank == 0) {
+                    mbar_arrive_expect_tx(&sm.full[st], bytes);
+                    if (tr.mA >= 0) tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
+                    tma_load_3d(b, &tmW1, &sm.full[st], kb * BK, tr.n * BN1, tr.e);        // gate rows
+                } else {
+                    const uint32_t full0 = mapa_shared(smem_u32(&sm.full[st]), 0u);
+                    if (tr.mA >= 0) tma_load_2d_pair(a, &tmA, full0, kb * BK, tr.lrowA);
+                    tma_load_3d_pair(b, &tmW3, full0, kb * BK, tr.n * BN1, tr.e);           // up rows
+                }
                 issued |= 1u << st;
                 last_ph = (last_ph & ~(1u << st)) | (ph << st);
                 if (++st == PAIR_STAGES) {
@@ -593,9 +599,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         if (!ok) {
             if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 10 + (int)rank);
             pair_abort(sm, rank);
+            // let loads in flight land before the CTA leaves: rank 0 waits on its barriers; rank 1's
+            // complete on rank 0's, so it waits a fixed 50 us (a tile load takes a few us)
             int never = 0;
-            for (int i = 0; i < PAIR_STAGES; ++i)  // let loads in flight land before the CTA leaves
-                if (issued & (1u << i)) mbar_wait(&sm.full[i], (last_ph >> i) & 1u, tmo, &never);
+            if (rank == 0) {
+                for (int i = 0; i < PAIR_STAGES; ++i)
+                    if (issued & (1u << i)) mbar_wait(&sm.full[i], (last_ph >> i) & 1u, tmo, &never);
+            } else if (issued) {
+                const unsigned long long t0 = globaltimer();
+                while (globaltimer() - t0 < 50000ull) __nanosleep(1000);
+            }
         }
     } else if (warp == 1 && lane == 0) {
         int st = 0;
@@ -618,8 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 tc_fence_after();
                 const uint32_t dt = tmem + (uint32_t)(b * 256);
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&sm.full[st], ph, tmo, sm.abort) ||
-                        !mbar_wait_cluster(&sm.pready[st], ph, tmo, sm.abort)) {
+                    if (!mbar_wait_cluster(&sm.full[st], ph, tmo, sm.abort)) {
                         ok = false;
                         break;
                     }
@@ -643,26 +655,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             }
             // Final commit to both CTAs' drain barrier: every UMMA issued has completed when it fires.
             umma_commit_pair(sm.drain, 0x3);
-        } else {
-            // ---------------- relay (rank 1): own stage full -> rank 0's pready ----------------
-            // The payload (the stage's bytes) is written by this CTA's TMA unit, which completes
-            // the full barrier only once the bytes are in shared memory; the relay forwards that
-            // event with a relaxed arrive (a release arrive would fence this SM's in-flight loads
-            // and, measured, more than halves the pair's throughput).
-            const uint32_t pready0 = mapa_shared(smem_u32(sm.pready), 0u);
-            for (int t = pair; t < total && ok; t += npairs) {
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait(&sm.full[st], ph, tmo, sm.abort)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_cluster_relaxed(pready0 + st * 8u);
-                    if (++st == PAIR_STAGES) {
-                        st = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
         }
         if (!ok) {
             if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 12 + (int)rank);
