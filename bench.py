@@ -36,19 +36,19 @@ METRIC = "MoE-layer tokens/s; grouped-GEMM % of BF16 peak; return-copy overlap %
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes per launch of the SwiGLU GEMM (dram__bytes_read.sum + dram__bytes_write.sum) from the
-# ncu capture summarised in profiles/gemm_swiglu_mixtral_T4096.md, with the SHA-256 of the kernel
-# sources it was taken on: the bench reports it only while those sources are unchanged and the
-# launch configuration is the captured one (single-CTA GEMM).
-SWIGLU_TRAFFIC = {"mixtral": {"bytes": 1952175000 + 245434368,
-                              "sources_sha256": "261e0a2297033232897312751fffe617634db0b74cd88dfe5dc7ea4facaa7f1e"}}
+# ncu capture summarised in profiles/gemm_swiglu_mixtral_T4096.md, per (workload, CTA-pair kernel),
+# with the SHA-256 of the kernel sources it was taken on: the bench reports it only while those
+# sources are unchanged and the launch configuration is the captured one.
+SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 2953622000 + 250155264,
+                                      "sources_sha256": "4e9f27188384b547aac6242a108b503e2680b6d0218dd2a402ecc3afb187e0b3"}}
 KERNEL_SOURCES = ("tile_level_copy_gb300/csrc/gemm.cu", "tile_level_copy_gb300/csrc/moe_internal.cuh",
                   "tile_level_copy_gb300/csrc/copy_ring.cuh")
 
 
 def captured_traffic(workload: str, pair_umma: bool):
     import hashlib
-    entry = SWIGLU_TRAFFIC.get(workload)
-    if entry is None or pair_umma:
+    entry = SWIGLU_TRAFFIC.get((workload, bool(pair_umma)))
+    if entry is None:
         return None
     h = hashlib.sha256()
     root = os.path.dirname(os.path.abspath(__file__))
@@ -294,7 +294,8 @@ def run_ours(args, rank: int, world: int):
     roof_achieved = fl_up_alg / (up_ms * 1e-3) / 1e12
     # algorithmic DRAM bytes of the SwiGLU GEMM: W1 and W3 once, the compact rows in, the hidden out
     alg_bytes_up = 2 * w.E * w.ffn * w.d * 2 + PC * w.d * 2 + PC * w.ffn * 2
-    roofline = {"kernel": "gemm_kernel<1> (SwiGLU up-projection)", "bound": "tensor",
+    roofline = {"kernel": ("gemm_pair_swiglu_kernel (SwiGLU up-projection, CTA pairs)" if args.pair_umma
+                           else "gemm_kernel<1> (SwiGLU up-projection)"), "bound": "tensor",
                 "achieved": round(roof_achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
                 "frac": round(roof_achieved / peak_tc, 4),
                 "traffic": args.traffic if args.traffic is not None else captured_traffic(args.workload, args.pair_umma),
