@@ -82,6 +82,9 @@ def parse_args():
     ap.add_argument("--pair-umma", action=argparse.BooleanOptionalAction, default=True,
                     help="SwiGLU GEMM on CTA pairs (UMMA 256 x 256 over two SMs; the default, the fastest "
                          "measured on every workload)")
+    ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=True,
+                    help="time the steps as replays of a CUDA graph of one step (default); the eager "
+                         "launches are timed too and reported beside")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -250,10 +253,48 @@ def run_ours(args, rank: int, world: int):
         stages = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(tlc.EV_COUNT - 1)] for e in evs])
         return t0.elapsed_time(t1) / 1e3, stages, clk.summary()
 
-    sec_ovl, st_ovl, clocks = timed(False)
+    def timed_graph(seq):
+        # one step captured as a CUDA graph (the launches and their dependencies recorded once) and
+        # replayed K times: the serving form of a fixed-shape layer
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                step(seq)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(seq)
+        for _ in range(Wm):
+            graph.replay()
+        rc, detail = tlc.status(cfg, ws)
+        if rc != tlc.MOE_OK:
+            raise RuntimeError(f"device status {rc} ({detail}) in the graph warm-up")
+        barrier(world)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(dev.index) as clk:
+            t0.record()
+            for _ in range(K):
+                graph.replay()
+            t1.record()
+            torch.cuda.synchronize()
+        barrier(world)
+        rc, detail = tlc.status(cfg, ws)
+        if rc != tlc.MOE_OK:
+            raise RuntimeError(f"device status {rc} ({detail}) in the timed graph replays")
+        return t0.elapsed_time(t1) / 1e3, clk.summary()
+
+    sec_ovl_eager, st_ovl, clocks_eager = timed(False)
+    sec_seq_eager, st_seq, clocks_seq_eager = timed(True)
+    if args.graph:
+        sec_ovl, clocks = timed_graph(False)
+        sec_seq, clocks_seq = timed_graph(True)
+    else:
+        sec_ovl, clocks, sec_seq, clocks_seq = sec_ovl_eager, clocks_eager, sec_seq_eager, clocks_seq_eager
     value, sec_max = aggregate(sec_ovl, w.T * K, world)
-    sec_seq, st_seq, clocks_seq = timed(True)
     seq_value, _ = aggregate(sec_seq, w.T * K, world)
+    eager_value, eager_sec_max = aggregate(sec_ovl_eager, w.T * K, world)
 
     # overlap from %globaltimer stamps of a few extra overlapped steps
     hidden, tails, marks = [], [], []
@@ -335,6 +376,10 @@ def run_ours(args, rank: int, world: int):
                    "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "
                       f"(> 129 MB L2)"},
         "gpu_launches": 6 * K,
+        "timing": ("CUDA-graph replays of one captured step (route, plan, permute, SwiGLU GEMM, "
+                   "down-projection + copy, combine)" if args.graph else "eager launches"),
+        "eager": {"value": round(eager_value, 1), "ms_per_step": round(eager_sec_max * 1e3 / K, 4),
+                  "clocks": clocks_eager},
         "clocks": clocks,
         "roofline": roofline,
         "gemm": {"executed_tflops": round(gemm_exec_tflops, 1), "algorithmic_tflops": round(gemm_alg_tflops, 1),
