@@ -201,6 +201,20 @@ def test_copy_only_reproduces_the_return_copy():
     assert ei.value.code == tlc.MOE_ERR_ARG
 
 
+def test_corrupt_plan_entry_is_reported_not_used():
+    """A schedule entry pointing past the last band makes the copy report MOE_ERR_PLAN (its bounds
+    check runs before the entry is used); the next forward re-plans and is correct again."""
+    w = small("skew")
+    L = Layer(w, seed=3)
+    want = L.run(sequential=True)
+    MT = int(L.ws.view("meta")[1].item())
+    L.ws.view("sched")[0] = MT + 7
+    tlc.copy_only(L.cfg, L.ws, 4)
+    rc, detail = tlc.status(L.cfg, L.ws)
+    assert rc == tlc.MOE_ERR_PLAN and detail == 0
+    assert torch.equal(L.run(sequential=False), want)
+
+
 def test_argument_errors_on_gpu():
     w = small("tiny")
     L = Layer(w, seed=0)

@@ -80,6 +80,26 @@ __device__ __forceinline__ void engine_drain(CopyEngine& ce, unsigned long long 
 // it takes units from meta[queue] until none is left. wait_flags: acquire the band counter of every
 // band of the unit's segment (== want: all tiles of the band published) before copying. The next
 // unit's counters are polled while the previous unit's pieces are still in flight.
+// Bounds check of the plan entries one copy unit reads (schedule position pos -> band m, its rows
+// in Yp and Ret, and the bands of its segment). A failure is reported as ST_BAD_PLAN and the copy
+// stops, so a corrupt plan never turns into an out-of-range access.
+__device__ __forceinline__ bool copy_unit_ok(const Shape& s, const PlanPtrs& p, int MT, int pos, bool wait_flags) {
+    const int m = p.sched[pos];
+    if (m < 0 || m >= MT) return false;
+    const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3], ret0 = p.tile_ret[m];
+    if (valid < 1 || valid > s.tbM || row0 < 0 || row0 + valid > s.P_max || ret0 < 0 || ret0 + valid > s.T * s.k)
+        return false;
+    if (wait_flags) {
+        const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
+        if (first < 0 || nb < 1 || nb > s.mgb || first + nb > MT) return false;
+        for (int i = 0; i < nb; ++i) {
+            const int b = p.sched[first + i];
+            if (b < 0 || b >= MT) return false;
+        }
+    }
+    return true;
+}
+
 __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uint64_t* bars, volatile int* s_abort,
                            int queue, bool wait_flags, uint32_t want) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -101,6 +121,13 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
         if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);  // in flight while this unit is handled
         int pos, rb, rpu;
         copy_unit_decode(s, MT, u, &pos, &rb, &rpu);
+        if (!__all_sync(0xffffffffu, copy_unit_ok(s, p, MT, pos, wait_flags))) {
+            if (lane == 0) {
+                set_status(p.meta, ST_BAD_PLAN, pos);
+                *s_abort = 1;
+            }
+            break;
+        }
         const int m = p.sched[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
         if (rb >= valid) continue;
@@ -205,6 +232,13 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
         if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
         int pos, rb, rpu;
         copy_unit_decode(s, MT, u, &pos, &rb, &rpu);
+        if (!__all_sync(0xffffffffu, copy_unit_ok(s, p, MT, pos, true))) {
+            if (lane == 0) {
+                set_status(p.meta, ST_BAD_PLAN, pos);
+                *s_abort = 1;
+            }
+            break;
+        }
         const int m = p.sched[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
         if (rb >= valid) continue;

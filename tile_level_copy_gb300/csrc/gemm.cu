@@ -184,6 +184,41 @@ __device__ __forceinline__ void epilogue_rows(EpiStage& es, const CUtensorMap* t
     }
 }
 
+// Bounds check of the plan entries a GEMM launch reads, by all threads of a CTA before any tile:
+// SwiGLU items (first compact row, expert) and the expert table of the item lists; down-projection
+// items (bands mA, mB) and each band's expert, output rows and compact rows. Returns the index of a
+// bad entry + 1, or 0. Every CTA reaches the same answer, so a corrupt plan stops the whole launch.
+__device__ __forceinline__ int plan_items_bad(const Shape& s, const PlanPtrs& p, int mode, int NI, int MT) {
+    int bad = 0;
+    if (mode == 1) {
+        for (int it = threadIdx.x; it < NI && !bad; it += blockDim.x) {
+            const int crow = p.items_up[2 * it], e = p.items_up[2 * it + 1];
+            if (e < 0 || e >= s.E || crow < 0 || crow % BM != 0 || crow + BM > s.PC_max) bad = it + 1;
+        }
+        for (int e = threadIdx.x; e < s.E && !bad; e += blockDim.x) {
+            const int cnt = p.experts[8 * e + 4], first = p.experts[8 * e + 5];
+            if (cnt < 0 || first < 0 || first + cnt > NI) bad = e + 1;
+        }
+    } else {
+        for (int it = threadIdx.x; it < NI && !bad; it += blockDim.x) {
+            const int mA = p.items_down[2 * it], mB = p.items_down[2 * it + 1];
+            const int ms[2] = {mA, mB};
+            if (mA < 0 || mA >= MT || mB < -1 || mB >= MT) {
+                bad = it + 1;
+                break;
+            }
+            for (int j = 0; j < 2; ++j) {
+                const int m = ms[j];
+                if (m < 0) continue;
+                const int e = p.tiles[4 * m], row0 = p.tiles[4 * m + 2], crow = p.tile_crow[m];
+                if (e < 0 || e >= s.E || row0 < 0 || row0 + s.tbM > s.P_max || crow < 0 || crow >= s.PC_max)
+                    bad = it + 1;
+            }
+        }
+    }
+    return bad;
+}
+
 template <int MODE>  // 1: SwiGLU up-projection -> Hc; 2: down-projection -> Yp (+ flags / consumer)
 __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAh,
@@ -199,6 +234,8 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     const int nN = (MODE == 1) ? s.ffn / BN1 : s.n_tiles_n2;
     const int BN = (MODE == 1) ? 2 * BN1 : s.bn2;  // UMMA N
     const int KB = ((MODE == 1) ? s.d : s.ffn) / BK;
+    const int bad_item = __syncthreads_or(plan_items_bad(s, p, MODE, NI, MT));
+    if (bad_item) NI = 0;  // no tile runs; the copy engines stop at the abort word set below
     const int total = NI * nN;
     const uint32_t tx_bytes = A_STAGE_BYTES + BN * BK * 2;
     const unsigned long long tmo = s.timeout_ns;
@@ -214,7 +251,8 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
         }
         mbar_init(sm.drain, 1);
         for (int i = 0; i < COPY_NBUF; ++i) mbar_init(&sm.cbar[i], 1);
-        *sm.abort = 0;
+        *sm.abort = bad_item ? 1 : 0;
+        if (bad_item) set_status(p.meta, ST_BAD_PLAN, bad_item - 1);
         mbar_fence_init();
     }
     if (MODE == 1) {
@@ -512,6 +550,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const int nN = s.ffn / BN1;
     const int KB = s.d / BK;
     const unsigned long long tmo = s.timeout_ns;
+    const int bad_item = __syncthreads_or(plan_items_bad(s, p, 1, NI, 0));  // same answer in both CTAs
+    if (bad_item) {
+        if (threadIdx.x == 0 && cluster_ctarank() == 0) set_status(p.meta, ST_BAD_PLAN, bad_item - 1);
+        NI = 0;
+    }
 
     if (tid == 0) {
         for (int i = 0; i < PAIR_STAGES; ++i) {
