@@ -1,10 +1,13 @@
-// Persistent grouped expert GEMMs on tcgen05 (UMMA 128 x N x 16, fp32 accumulators in TMEM),
-// fed by TMA through a 4-stage shared-memory ring, with warp-specialised roles:
+// Persistent grouped expert GEMMs on tcgen05 (fp32 accumulators in TMEM), fed by TMA through a
+// shared-memory ring, with warp-specialised roles:
 //   warp 0      one thread issues the TMA loads of A (token rows) and B (expert weights)
 //   warp 1      allocates 512 TMEM columns; one thread issues the UMMAs (two accumulators, so the
 //               epilogue of tile i overlaps the main loop of tile i+1)
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, conversion, staging in shared memory and
 //               TMA tensor stores of 32 x 32 chunks to global memory
+//   warps 6-7   (down-projection with MOE_COPY_WARPS) SIMT copy engines of the return copy
+// gemm_kernel<1|2> is the single-CTA kernel (UMMA 128 x N x 16, 4-stage ring); gemm_pair_swiglu_kernel
+// runs the SwiGLU GEMM on CTA pairs (UMMA 256 x 256 x 16, cta_group::2, 6-stage ring per CTA).
 //
 // Method: "Fine-grained Computation-Communication Overlap via Tile-level Signaling and Scheduling
 // for Mixture-of-Experts" (pith.science/paper/W2ZARMHG):
@@ -12,9 +15,9 @@
 //       readiness flag after each tile's epilogue store;
 //   "Load-bearing premise" and "Referee Report" major comment 2 (§3.3.1) - the tile must be
 //       visible before the flag: each of the four epilogue warps waits until its TMA stores of the
-//       tile have completed, fences the async proxy, then adds 1 to the tile flag with
-//       red.release.gpu; the consumer reads the flag with ld.acquire.gpu (ready at 4) and fences
-//       the async proxy before its bulk copy.
+//       tile have completed, fences the async proxy, then adds its share to the tile flag and to
+//       the band's counter with release semantics; copy engines read the band counter with
+//       ld.acquire.gpu (ready at 4 x tiles per band); bulk engines fence the async proxy first.
 //   "What carries the argument" - the consumer runs on a small dedicated SM partition; here the
 //       partition is the last consumer_ctas CTAs of the same cooperative launch, so producers and
 //       consumers are guaranteed to be co-resident.
@@ -33,7 +36,6 @@ struct Smem {
     uint64_t* cbar;
     uint32_t* tmem_base;
     volatile int* abort;
-    volatile int* unit;
     int* tab;  // [cum (E+1) | first (E) | count (E)]
 };
 
@@ -52,8 +54,7 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
     sm.cbar = sm.drain + 1;
     sm.tmem_base = reinterpret_cast<uint32_t*>(sm.cbar + COPY_NBUF);
     sm.abort = reinterpret_cast<volatile int*>(sm.tmem_base + 1);
-    sm.unit = sm.abort + 1;
-    sm.tab = const_cast<int*>(sm.unit + 2);
+    sm.tab = const_cast<int*>(sm.abort + 1);
     return sm;
 }
 
@@ -186,8 +187,9 @@ __device__ __forceinline__ void epilogue_rows(EpiStage& es, const CUtensorMap* t
 
 // Bounds check of the plan entries a GEMM launch reads, by all threads of a CTA before any tile:
 // SwiGLU items (first compact row, expert) and the expert table of the item lists; down-projection
-// items (bands mA, mB) and each band's expert, output rows and compact rows. Returns the index of a
-// bad entry + 1, or 0. Every CTA reaches the same answer, so a corrupt plan stops the whole launch.
+// items (bands mA, mB) and each band's expert, output rows and compact rows. Returns nonzero if this
+// thread found a bad entry. Every CTA reaches the same answer, so a corrupt plan stops the whole
+// launch; the status detail is -1 (SwiGLU items) or -2 (down-projection items).
 __device__ __forceinline__ int plan_items_bad(const Shape& s, const PlanPtrs& p, int mode, int NI, int MT) {
     int bad = 0;
     if (mode == 1) {
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
         mbar_init(sm.drain, 1);
         for (int i = 0; i < COPY_NBUF; ++i) mbar_init(&sm.cbar[i], 1);
         *sm.abort = bad_item ? 1 : 0;
-        if (bad_item) set_status(p.meta, ST_BAD_PLAN, bad_item - 1);
+        if (bad_item) set_status(p.meta, ST_BAD_PLAN, -MODE);
         mbar_fence_init();
     }
     if (MODE == 1) {
@@ -552,7 +554,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const unsigned long long tmo = s.timeout_ns;
     const int bad_item = __syncthreads_or(plan_items_bad(s, p, 1, NI, 0));  // same answer in both CTAs
     if (bad_item) {
-        if (threadIdx.x == 0 && cluster_ctarank() == 0) set_status(p.meta, ST_BAD_PLAN, bad_item - 1);
+        if (threadIdx.x == 0 && cluster_ctarank() == 0) set_status(p.meta, ST_BAD_PLAN, -1);
         NI = 0;
     }
 
