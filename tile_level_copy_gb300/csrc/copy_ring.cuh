@@ -1,12 +1,16 @@
-// Row-band copy engine of the return path: Yp rows -> the owner's slice of Ret.
+// Row-band copy engines of the return path: Yp rows -> the owner's slice of Ret.
 //
 // "Fine-grained Computation-Communication Overlap via Tile-level Signaling and Scheduling for
 // Mixture-of-Experts" (pith.science/paper/W2ZARMHG), "Core claim": the consumer polls the tile
 // flags and issues one contiguous write per row-band segment. On one GPU the write is an
-// HBM-to-HBM copy. Every warp of a copying CTA is an independent copy engine: it takes a work unit,
-// waits for the unit's flags, and moves the rows through two shared-memory buffers with TMA bulk
-// copies (global -> shared completes on an mbarrier, shared -> global is a bulk group), so each
-// warp keeps two 16 KB loads in flight, also across unit boundaries.
+// HBM-to-HBM copy, and the poll reads one counter per band, which every finished tile quarter of
+// the band release-adds to beside its tile flag (ready at 4 x tiles per band).
+//
+// Bulk engine (copy_units): every warp of a copying CTA takes a work unit, waits for the unit's
+// bands, and moves the rows through two shared-memory buffers with TMA bulk copies (global ->
+// shared completes on an mbarrier, shared -> global is a bulk group), keeping two 16 KB loads in
+// flight, also across unit boundaries. SIMT engine (copy_units_simt): one warp moving rows through
+// registers with 16-byte loads and stores, no shared memory, for the extra warps of producer CTAs.
 //
 // Work units: band (schedule position) x row chunk of rows_per_unit rows, handed out in schedule
 // order by an atomic counter, so idle engines always take the oldest outstanding band.
