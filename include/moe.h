@@ -74,8 +74,8 @@ extern "C" {
  *   swept 2-24 on the page); mgb = bands per interior segment (same section, 1 or 2 there).
  *   timeout_us bounds every device-side wait (0 = 2,000,000 us).
  * Limits: d % 128 == 0, ffn % 128 == 0, 1 <= topk <= min(E, 8), 1 <= E <= 256, T % R == 0,
- *   E*R <= 1024, tile_M in {64, 128}, 1 <= mgb <= 4, 1 <= consumer_ctas <= SMs/2 (checked at
- *   launch), P_max < 2^30 (see moe_layout).
+ *   E*R <= 1024, tile_M in {64, 128}, 1 <= mgb <= 4, 1 <= consumer_ctas <= SMs/2 (0 allowed
+ *   with MOE_COPY_WARPS; checked at launch), P_max < 2^30 (see moe_layout).
  */
 typedef struct moe_config {
     int32_t T, d, ffn, E, topk, R, tile_M;
@@ -186,7 +186,11 @@ MOE_API int moe_plan(const moe_config* cfg, const float* logits, const uint16_t*
  * launch), then one cooperative launch in which SMs - consumer_ctas CTAs run the down-projection
  * GEMM in remote-first order and release a flag per finished tile while consumer_ctas CTAs acquire
  * the flags and copy each ready segment of row bands into its owner's slice of Ret, then the
- * weighted top-k combine. A bounded wait that runs out is reported by moe_status(), not here.
+ * weighted top-k combine. Flags: MOE_TAIL_ASSIST (producers that finished join the copy),
+ * MOE_COPY_WARPS (copy engines also inside every producer CTA; consumer_ctas may be 0),
+ * MOE_PAIR_UMMA (the SwiGLU GEMM on CTA pairs); none changes the result, bit for bit. A bounded
+ * wait that runs out, or a plan entry that fails its bounds check, is reported by moe_status(),
+ * not here.
  */
 MOE_API int moe_forward(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
                         const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes,
