@@ -616,7 +616,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         for (int t = pair; t < total && ok && !bad; t += npairs) {
             const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, rank);
             const TileRef tq = decode_pair_up(t, sm.tab, s.E, p.items_up, 1u);  // rank 1's rows
-            const uint32_t bytes = (tr.mA >= 0 ? PAIR_A_BYTES : 0) + (tq.mA >= 0 ? PAIR_A_BYTES : 0) + 2 * PAIR_B_BYTES;
+            (void)tq;
+            const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
             for (int kb = 0; kb < KB; ++kb) {
                 if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
                     ok = false;
@@ -630,7 +631,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     tma_load_3d(b, &tmW1, &sm.full[st], kb * BK, tr.n * BN1, tr.e);        // gate rows
                 } else {
                     const uint32_t full0 = mapa_shared(smem_u32(&sm.full[st]), 0u);
-                    if (tr.mA >= 0) tma_load_2d_pair(a, &tmA, full0, kb * BK, tr.lrowA);
+                    // an odd CTA without rows loads a box past the last row: zeros, so its idle
+                    // half of the UMMA multiplies zeros (less switching power than stale rows)
+                    tma_load_2d_pair(a, &tmA, full0, kb * BK, tr.mA >= 0 ? tr.lrowA : s.PC_max);
                     tma_load_3d_pair(b, &tmW3, full0, kb * BK, tr.n * BN1, tr.e);           // up rows
                 }
                 issued |= 1u << st;
