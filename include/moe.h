@@ -253,8 +253,10 @@ MOE_API int moe_forward_host(const moe_config* cfg, const float* logits_h, const
  * each with its own host inputs and output (arrays of `steps` host pointers; pinned memory), with
  * the transfers of neighbouring batches overlapped with the layer: the inputs of batch i+1 are
  * copied in and the output of batch i-1 is copied out on two internal streams while batch i runs
- * on `stream`, through two staging slots in the workspace. Results equal `steps` calls of
- * moe_forward_host. Every out_h[i] is valid once `stream` has reached the end of this call; the
+ * on `stream`, through two staging slots in the workspace. With steps > 1 the layer's launches for
+ * each slot are captured once as a CUDA graph (kept for the last 4 (config, workspace, weights)
+ * combinations per device) and replayed. Results equal `steps` calls of moe_forward_host. Not for
+ * concurrent use from several host threads (the copy streams, events and graphs are per device). Every out_h[i] is valid once `stream` has reached the end of this call; the
  * host inputs must stay unchanged until then. No counterpart in the method's pages: the serving
  * loop around the layer.
  */

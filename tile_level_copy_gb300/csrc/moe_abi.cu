@@ -479,9 +479,22 @@ MOE_API int moe_forward_host(const moe_config* cfg, const float* logits_h, const
 }
 
 // Internal copy streams and events of the pipelined host entry, created once per device.
+// The layer's launches for one staging slot, captured once as a CUDA graph and replayed per batch
+// (the tensor maps and pointers are fixed for a given config, workspace and weights).
+struct LayerGraph {
+    moe_config cfg;
+    const void *ws, *W1, *W3, *W2;
+    int sequential;
+    cudaGraphExec_t exec[2];
+    bool valid = false;
+};
+constexpr int LAYER_GRAPHS = 4;  // cached per device, oldest replaced first
+
 struct HostPipe {
-    cudaStream_t cin = nullptr, cout = nullptr;
+    cudaStream_t cin = nullptr, cout = nullptr, cap = nullptr;
     cudaEvent_t in_done[2], out_ready[2], out_free[2], slot_free[2];
+    LayerGraph graphs[LAYER_GRAPHS];
+    int next_graph = 0;
     bool ok = false;
 };
 
@@ -495,6 +508,7 @@ static int host_pipe(HostPipe** out) {
     if (!h.ok) {
         e = cudaStreamCreateWithFlags(&h.cin, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.cout, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.cap, cudaStreamNonBlocking);
         for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
             e = cudaEventCreateWithFlags(&h.in_done[i], cudaEventDisableTiming);
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.out_ready[i], cudaEventDisableTiming);
@@ -506,6 +520,54 @@ static int host_pipe(HostPipe** out) {
     }
     *out = &h;
     return MOE_OK;
+}
+
+// Graphs of the layer for the two staging slots of (cfg, ws, weights, sequential), captured on the
+// pipe's capture stream at first use. Returns nullptr (and the caller launches eagerly) if the
+// capture fails.
+static const LayerGraph* layer_graphs(HostPipe* h, const Call& c, const moe_config* cfg, void* ws, const uint16_t* W1,
+                                      const uint16_t* W3, const uint16_t* W2, int sequential) {
+    for (const LayerGraph& g : h->graphs)
+        if (g.valid && g.ws == ws && g.W1 == W1 && g.W3 == W3 && g.W2 == W2 && g.sequential == sequential &&
+            memcmp(&g.cfg, cfg, sizeof(moe_config)) == 0)
+            return &g;
+    LayerGraph& g = h->graphs[h->next_graph];
+    if (g.valid) {
+        for (int sl = 0; sl < 2; ++sl) cudaGraphExecDestroy(g.exec[sl]);
+        g.valid = false;
+    }
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    const size_t T = cfg->T, nl = T * cfg->E * 4, nx = T * cfg->d * 2, no = T * cfg->d * 4;
+    Call cc = c;
+    cc.st = h->cap;
+    for (int sl = 0; sl < 2; ++sl) {
+        cudaGraph_t graph = nullptr;
+        if (cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return nullptr;
+        const int rc = run_forward(cc, reinterpret_cast<const float*>(b + c.lay.L.in_logits + sl * nl),
+                                   reinterpret_cast<const uint16_t*>(b + c.lay.L.in_x + sl * nx), W1, W3, W2,
+                                   reinterpret_cast<float*>(b + c.lay.L.out + sl * no), sequential == 0);
+        const cudaError_t e = cudaStreamEndCapture(h->cap, &graph);
+        cudaGraphExec_t exec = nullptr;
+        const bool ok = rc == MOE_OK && e == cudaSuccess && graph &&
+                        cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+        if (graph) cudaGraphDestroy(graph);
+        if (!ok) {
+            if (sl == 1) cudaGraphExecDestroy(g.exec[0]);
+            cudaGetLastError();  // the eager path reports its own errors
+            g_err.clear();
+            return nullptr;
+        }
+        g.exec[sl] = exec;
+    }
+    g.cfg = *cfg;
+    g.ws = ws;
+    g.W1 = W1;
+    g.W3 = W3;
+    g.W2 = W2;
+    g.sequential = sequential;
+    g.valid = true;
+    h->next_graph = (h->next_graph + 1) % LAYER_GRAPHS;
+    return &g;
 }
 
 MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const float* const* logits_h,
@@ -521,6 +583,7 @@ MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const f
         if (!logits_h[i] || !x_h[i] || !out_h[i]) return fail(MOE_ERR_ARG, "NULL host pointer (step %d)", i);
     HostPipe* h = nullptr;
     if ((rc = host_pipe(&h))) return rc;
+    const LayerGraph* lg = steps > 1 ? layer_graphs(h, c, cfg, ws, W1, W3, W2, sequential) : nullptr;
     uint8_t* b = static_cast<uint8_t*>(ws);
     const size_t T = cfg->T, nl = T * cfg->E * 4, nx = T * cfg->d * 2, no = T * cfg->d * 4;
     cudaError_t e = cudaSuccess;
@@ -540,8 +603,14 @@ MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const f
         if (e == cudaSuccess) e = cudaStreamWaitEvent(c.st, h->in_done[sl], 0);
         if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(c.st, h->out_free[sl], 0);
         if (e != cudaSuccess) break;
-        rc = run_forward(c, d_logits, reinterpret_cast<const uint16_t*>(d_x), W1, W3, W2, d_out, sequential == 0);
-        if (rc) return rc;
+        if (lg) {
+            e = cudaGraphLaunch(lg->exec[sl], c.st);
+            if (e != cudaSuccess) break;
+        } else {
+            rc = run_forward(c, d_logits, reinterpret_cast<const uint16_t*>(d_x), W1, W3, W2, d_out,
+                             sequential == 0);
+            if (rc) return rc;
+        }
         e = cudaEventRecord(h->out_ready[sl], c.st);
         if (e == cudaSuccess) e = cudaEventRecord(h->slot_free[sl], c.st);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(h->cout, h->out_ready[sl], 0);
