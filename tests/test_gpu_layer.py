@@ -234,16 +234,20 @@ def test_argument_errors_on_gpu():
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mixtral", "skew", "fine"])
 def test_full_size_sampled_tokens(name):
-    """Full workload sizes in the bench's launch configuration; 48 sampled tokens against the
-    oracle's per-token definition, plus bitwise overlapped == sequential over all tokens (also with
-    the producers' extra copy warps and no consumer partition)."""
+    """Full workload sizes in the bench's launch configuration (its per-workload copy configuration,
+    CTA-pair SwiGLU GEMM, tail assist); 48 sampled tokens against the oracle's per-token definition,
+    plus bitwise overlapped == sequential over all tokens, also for the page's dedicated partition
+    (8 consumer CTAs, single-CTA GEMMs) and for copy warps alone."""
+    import bench
     w = inputs.WORKLOADS[name]
-    L = Layer(w, seed=0, cfg_kw=dict(consumer_ctas=8, flags=tlc.MOE_TAIL_ASSIST))
+    c, warps = bench.DEFAULT_COPY[name]
+    flags = tlc.MOE_TAIL_ASSIST | tlc.MOE_PAIR_UMMA | (CW if warps else 0)
+    L = Layer(w, seed=0, cfg_kw=dict(consumer_ctas=c, flags=flags))
     got = L.run(sequential=False)
     seq = L.run(sequential=True)
     assert torch.equal(got, seq)
-    cw = tlc.Config.from_workload(w, consumer_ctas=0, flags=CW | tlc.MOE_TAIL_ASSIST)
-    assert torch.equal(L.run(sequential=False, cfg=cw), seq)
+    for c2, f2 in ((8, tlc.MOE_TAIL_ASSIST), (0, CW | tlc.MOE_TAIL_ASSIST)):
+        assert torch.equal(L.run(sequential=False, cfg=tlc.Config.from_workload(w, consumer_ctas=c2, flags=f2)), seq)
     rng = np.random.default_rng(7)
     tokens = np.sort(rng.choice(w.T, size=48, replace=False))
     tokens[0], tokens[-1] = 0, w.T - 1  # include both ends
