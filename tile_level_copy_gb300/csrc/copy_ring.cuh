@@ -82,8 +82,9 @@ __device__ __forceinline__ void engine_drain(CopyEngine& ce, unsigned long long 
 // Called by every thread of the CTA. Each warp is an independent copy engine with its own slice of
 // the staging area (`ring`, COPY_WARPS * 2 * COPY_PIECE bytes) and two of the mbarriers in `bars`;
 // it takes units from meta[queue] until none is left. wait_flags: acquire the band counter of every
-// band of the unit's segment (== want: all tiles of the band published) before copying. The next
-// unit's counters are polled while the previous unit's pieces are still in flight.
+// band of the unit's segment (== want: all tiles of the band published) before copying. An engine
+// claims its next unit only once the current one is acquired (never while it waits on a band), and
+// the next unit's counters are polled while the previous unit's pieces are still in flight.
 // Bounds check of the plan entries one copy unit reads (schedule position pos -> band m, its rows
 // in Yp and Ret, and the bands of its segment). A failure is reported as ST_BAD_PLAN and the copy
 // stops, so a corrupt plan never turns into an out-of-range access.
@@ -122,7 +123,6 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
     for (;;) {
         const int u = __shfl_sync(0xffffffffu, u_next, 0);
         if (__any_sync(0xffffffffu, *s_abort != 0) || u >= units) break;
-        if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);  // in flight while this unit is handled
         int pos, rb, rpu;
         copy_unit_decode(s, MT, u, &pos, &rb, &rpu);
         if (!__all_sync(0xffffffffu, copy_unit_ok(s, p, MT, pos, wait_flags))) {
@@ -134,7 +134,10 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
         }
         const int m = p.sched[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
-        if (rb >= valid) continue;
+        if (rb >= valid) {
+            if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
+            continue;
+        }
         const int re = min(valid, rb + rpu);
 
         if (wait_flags) {
@@ -171,6 +174,10 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
             if (__any_sync(0xffffffffu, failed)) break;
             if (lane == 0) t_acq = globaltimer();
         }
+        // The next unit is claimed only now that this one is ready, so a unit queued behind a band
+        // that is still being computed is never held by an engine waiting on that band; the claim
+        // is in flight while this unit's rows move.
+        if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
         if (lane == 0) {
             if (!did) t_first = globaltimer();
             did = true;
@@ -233,7 +240,6 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
     for (;;) {
         const int u = __shfl_sync(0xffffffffu, u_next, 0);
         if (__any_sync(0xffffffffu, *s_abort != 0) || u >= units) break;
-        if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
         int pos, rb, rpu;
         copy_unit_decode(s, MT, u, &pos, &rb, &rpu);
         if (!__all_sync(0xffffffffu, copy_unit_ok(s, p, MT, pos, true))) {
@@ -245,7 +251,10 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
         }
         const int m = p.sched[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
-        if (rb >= valid) continue;
+        if (rb >= valid) {
+            if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
+            continue;
+        }
         const int re = min(valid, rb + rpu);
         bool failed = false;
         if (lane == 0) {
@@ -271,6 +280,7 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
             }
             t_acq = globaltimer();
             if (!did) t_first = t_acq;
+            if (!failed) u_next = atomicAdd(&p.meta[queue], 1);  // claimed once this unit is ready
         }
         if (__any_sync(0xffffffffu, failed)) break;
         __syncwarp();  // orders lane 0's acquire before every lane's loads
