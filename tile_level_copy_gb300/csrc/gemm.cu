@@ -34,8 +34,11 @@ struct Smem {
     uint64_t* acc_empty;
     uint64_t* drain;
     uint64_t* cbar;
+    uint64_t* tq_full;   // tile hand-out ring: slot written (count 1)
+    uint64_t* tq_empty;  // slot read by the UMMA issuer and the 4 epilogue warps (count 5)
     uint32_t* tmem_base;
     volatile int* abort;
+    volatile int* tq;    // TILE_Q slots: tile index, or -1 when the CTA has no more tiles
     int* tab;  // [cum (E+1) | first (E) | count (E)]
 };
 
@@ -52,10 +55,30 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
     sm.acc_empty = sm.acc_full + 2;
     sm.drain = sm.acc_empty + 2;
     sm.cbar = sm.drain + 1;
-    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.cbar + COPY_NBUF);
+    sm.tq_full = sm.cbar + COPY_NBUF;
+    sm.tq_empty = sm.tq_full + TILE_Q;
+    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.tq_empty + TILE_Q);
     sm.abort = reinterpret_cast<volatile int*>(sm.tmem_base + 1);
-    sm.tab = const_cast<int*>(sm.abort + 1);
+    sm.tq = sm.abort + 1;
+    sm.tab = const_cast<int*>(sm.tq + TILE_Q);
     return sm;
+}
+
+// Tile hand-out. Each producer CTA's TMA thread takes its first tile statically (blockIdx.x) and
+// every further one from a per-GEMM counter in the plan's meta words when it has issued the loads
+// of the previous one, so tiles go to whichever CTA is free first and a CTA slowed down (a tile whose
+// expert weights came from DRAM rather than L2) takes fewer of them. Which CTA computes a tile does
+// not change its result. The index reaches the UMMA issuer and the epilogue warps through a ring of
+// TILE_Q shared-memory slots (tq_full / tq_empty); -1 ends the CTA's tiles.
+constexpr int TILE_ABORT = -2;
+
+// One thread: the j-th tile index of this CTA from the hand-out ring (TILE_ABORT if the wait ran out).
+__device__ __forceinline__ int tile_take(const Smem& sm, int j, unsigned long long tmo) {
+    const int slot = j % TILE_Q;
+    if (!mbar_wait(&sm.tq_full[slot], (uint32_t)(j / TILE_Q) & 1u, tmo, sm.abort)) return TILE_ABORT;
+    const int t = sm.tq[slot];
+    mbar_arrive(&sm.tq_empty[slot]);
+    return t;
 }
 
 // One GEMM tile: work item (mA, mB) x N tile n of expert e. Rows 0-63 of the UMMA tile are loaded
@@ -253,6 +276,10 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
         }
         mbar_init(sm.drain, 1);
         for (int i = 0; i < COPY_NBUF; ++i) mbar_init(&sm.cbar[i], 1);
+        for (int i = 0; i < TILE_Q; ++i) {
+            mbar_init(&sm.tq_full[i], 1);
+            mbar_init(&sm.tq_empty[i], 1 + 4);
+        }
         *sm.abort = bad_item ? 1 : 0;
         if (bad_item) set_status(p.meta, ST_BAD_PLAN, -MODE);
         mbar_fence_init();
@@ -303,10 +330,26 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
             int st = 0;
             uint32_t ph = 0, issued = 0, last_ph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += num_producers) {
+            int t = blockIdx.x;  // first tile static, the others from the hand-out counter
+            int* tile_counter = &p.meta[(MODE == 1) ? META_TILES_UP : META_TILES_DOWN];
+            const int claim_kb = KB > 8 ? KB - 8 : 0;
+            for (int j = 0; ok; ++j) {
+                const int slot = j % TILE_Q;
+                if (!mbar_wait(&sm.tq_empty[slot], ((uint32_t)(j / TILE_Q) & 1u) ^ 1u, tmo, sm.abort)) {
+                    ok = false;
+                    break;
+                }
+                sm.tq[slot] = t < total ? t : -1;
+                mbar_arrive(&sm.tq_full[slot]);
+                if (t >= total) break;
                 const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up)
                                                : decode_down(t, nN, p.items_down, p.tiles, p.tile_crow);
+                int next = total;
                 for (int kb = 0; kb < KB; ++kb) {
+                    // the next tile is taken a few k-blocks before this one's loads are all issued,
+                    // so the atomic's latency is hidden: a CTA that ran slower (weights streamed
+                    // from DRAM) takes fewer tiles
+                    if (kb == claim_kb) next = num_producers + atomicAdd(tile_counter, 1);
                     if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
                         ok = false;
                         break;
@@ -333,6 +376,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                         ph ^= 1u;
                     }
                 }
+                t = next;
             }
             if (!ok) {
                 if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 0);
@@ -347,7 +391,13 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
             int st = 0, b = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true, any = false;
-            for (int t = blockIdx.x; t < total && ok; t += num_producers) {
+            for (int j = 0; ok; ++j) {
+                const int t = tile_take(sm, j, tmo);
+                if (t == TILE_ABORT) {
+                    ok = false;
+                    break;
+                }
+                if (t < 0) break;
                 if (!mbar_wait(&sm.acc_empty[b], aph ^ 1u, tmo, sm.abort)) {
                     ok = false;
                     break;
@@ -398,7 +448,18 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
             EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
             int b = 0;
             uint32_t aph = 0;
-            for (int t = blockIdx.x; t < total; t += num_producers) {
+            for (int j = 0;; ++j) {
+                int t = 0;
+                if (lane == 0) t = tile_take(sm, j, tmo);
+                t = __shfl_sync(0xffffffffu, t, 0);
+                if (t == TILE_ABORT) {
+                    if (lane == 0) {
+                        if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 3);
+                        *sm.abort = 1;
+                    }
+                    break;
+                }
+                if (t < 0) break;
                 const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up)
                                                : decode_down(t, nN, p.items_down, p.tiles, p.tile_crow);
                 if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {

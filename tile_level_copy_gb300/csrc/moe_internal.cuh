@@ -24,6 +24,9 @@ enum Meta : int {
     META_ITEMS = 7,        // down-projection work items (one band, or two bands of <= 64 rows)
     META_ITEMS_UP = 8,     // SwiGLU work items (128 rows of one expert in the compact layout)
     META_PC = 9,           // rows of the compact layout used by this call
+    META_TILES_UP = 32,    // next SwiGLU GEMM tile to hand out (single-CTA kernel), minus the grid
+    META_TILES_DOWN = 48,  // next down-projection tile to hand out, minus the producer count
+                           // (both on a 128-byte line away from the copy queues' line)
     META_COUNT = 64,
 };
 
@@ -50,6 +53,7 @@ constexpr int GEMM_THREADS = 192;                      // warp 0 TMA, warp 1 MMA
 constexpr int GEMM_WARPS = GEMM_THREADS / 32;
 constexpr int COPY_WARPS_EXTRA = 2;                    // copy-engine warps added with MOE_COPY_WARPS
 constexpr int GEMM_THREADS_MAX = GEMM_THREADS + 32 * COPY_WARPS_EXTRA;
+constexpr int TILE_Q = 4;          // slots of the tile hand-out ring (TMA thread -> UMMA issuer, epilogue)
 constexpr int MISC_BYTES = 6144;  // barriers, flags and the expert table (4E+1 ints)
 // epilogue staging: per epilogue warp two 32-row x 32-column bf16 chunks (2 KB each), written to
 // global memory by TMA tensor stores

@@ -423,6 +423,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         p.meta[META_PC] = PC;
         p.meta[META_QUEUE] = 0;
         p.meta[META_QUEUE_SEQ] = 0;
+        p.meta[META_TILES_UP] = 0;
+        p.meta[META_TILES_DOWN] = 0;
         const bool bad = P > s.P_max || PC > s.PC_max;
         p.meta[META_STATUS] = bad ? ST_BAD_PLAN : 0;
         p.meta[META_STATUS_DETAIL] = bad ? (P > s.P_max ? P : PC) : 0;
