@@ -533,6 +533,16 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 // of the stage done; committed to both CTAs), acc_full[b] (committed to both CTAs), acc_empty[b]
 // on rank 0 (count 8: the four epilogue warps of each CTA). Every wait is bounded; a timeout
 // raises the abort word of both CTAs.
+//
+// Tile hand-out: rank 0's TMA thread takes the pair's first tile by pair index and every further
+// one from the META_TILES_UP counter (as in gemm_kernel), and publishes each index in a ring of
+// PAIR_TILE_Q slots of both CTAs: its own slot with a store and an arrive on tq_full, the peer's
+// with st.async, which completes 4 transaction bytes on the peer's tq_full (armed by the peer's TMA
+// thread, once at start and again each time it has read the slot). Rank 0's tq_empty (count 9)
+// collects rank 0's UMMA issuer and the epilogue warps of both CTAs. Rank 1's TMA thread needs no
+// arrive there: rank 0's TMA thread cannot run more than PAIR_STAGES k-blocks ahead of it (every
+// stage's barrier waits for rank 1's loads), so when rank 0 reuses a slot PAIR_TILE_Q tiles later,
+// rank 1 has long since read it.
 // =============================================================================================
 struct PairSmem {
     uint8_t* stages;
@@ -542,9 +552,12 @@ struct PairSmem {
     uint64_t* acc_full;
     uint64_t* acc_empty;
     uint64_t* drain;
+    uint64_t* tq_full;   // PAIR_TILE_Q tile hand-out slots (see above)
+    uint64_t* tq_empty;
     uint32_t* tmem_base;
     uint32_t* peer_base;
     volatile int* abort;
+    volatile int* tq;
     int* tab;  // [cum (E+1) | first item (E) | items (E)]
 };
 
@@ -560,11 +573,25 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
     sm.acc_full = sm.empty + PAIR_STAGES;
     sm.acc_empty = sm.acc_full + 2;
     sm.drain = sm.acc_empty + 2;
-    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.drain + 1);
+    sm.tq_full = sm.drain + 1;
+    sm.tq_empty = sm.tq_full + PAIR_TILE_Q;
+    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.tq_empty + PAIR_TILE_Q);
     sm.peer_base = sm.tmem_base + 1;
     sm.abort = reinterpret_cast<volatile int*>(sm.peer_base + 1);
-    sm.tab = const_cast<int*>(sm.abort + 1);
+    sm.tq = sm.abort + 1;
+    sm.tab = const_cast<int*>(sm.tq + PAIR_TILE_Q);
     return sm;
+}
+
+// One thread: the j-th tile index of the pair from this CTA's hand-out ring (TILE_ABORT if the wait
+// ran out). Rank 1's slots are filled by st.async from rank 0, so the wait acquires at cluster
+// scope. The caller then releases the slot: rank 0's consumers with a local arrive on tq_empty, rank
+// 1's epilogue warps with a cluster arrive on rank 0's tq_empty, rank 1's TMA thread by arming its
+// tq_full for the slot's next use.
+__device__ __forceinline__ int pair_tile_wait(const PairSmem& sm, int j, unsigned long long tmo) {
+    const int slot = j % PAIR_TILE_Q;
+    if (!mbar_wait_cluster(&sm.tq_full[slot], (uint32_t)(j / PAIR_TILE_Q) & 1u, tmo, sm.abort)) return TILE_ABORT;
+    return sm.tq[slot];
 }
 
 // Raise the abort word of both CTAs of the pair.
@@ -629,8 +656,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             mbar_init(&sm.acc_empty[i], 8);
         }
         mbar_init(sm.drain, 1);
+        for (int i = 0; i < PAIR_TILE_Q; ++i) {
+            mbar_init(&sm.tq_full[i], 1);
+            mbar_init(&sm.tq_empty[i], 1 + 4 + 4);
+        }
         *sm.abort = 0;
         mbar_fence_init();
+        if (cluster_ctarank() == 1)  // arm every slot for rank 0's first st.async
+            for (int i = 0; i < PAIR_TILE_Q; ++i) mbar_arrive_expect_tx(&sm.tq_full[i], 4);
     }
     for (int e = tid; e < s.E; e += blockDim.x) {
         sm.tab[(s.E + 1) + e] = p.experts[8 * e + 5];         // first work item
@@ -674,12 +707,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         int st = 0;
         uint32_t ph = 0, issued = 0, last_ph = 0;
         bool ok = true;
-        for (int t = pair; t < total && ok && !bad; t += npairs) {
+        int t = pair;  // rank 0: first tile static, the others from the hand-out counter
+        const int claim_kb = KB > 8 ? KB - 8 : 0;
+        for (int j = 0; ok && !bad; ++j) {
+            const int slot = j % PAIR_TILE_Q;
+            if (rank == 0) {
+                if (!mbar_wait(&sm.tq_empty[slot], ((uint32_t)(j / PAIR_TILE_Q) & 1u) ^ 1u, tmo, sm.abort)) {
+                    ok = false;
+                    break;
+                }
+                const int v = t < total ? t : -1;
+                sm.tq[slot] = v;
+                mbar_arrive(&sm.tq_full[slot]);
+                st_async_u32(mapa_shared(smem_u32(const_cast<int*>(sm.tq + slot)), 1u), (uint32_t)v,
+                             mapa_shared(smem_u32(&sm.tq_full[slot]), 1u));
+            } else {
+                t = pair_tile_wait(sm, j, tmo);
+                if (t == TILE_ABORT) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.tq_full[slot], 4);  // armed for the slot's next use
+            }
+            if (t < 0 || t >= total) break;
             const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, rank);
-            const TileRef tq = decode_pair_up(t, sm.tab, s.E, p.items_up, 1u);  // rank 1's rows
-            (void)tq;
             const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
+            int next = total;
             for (int kb = 0; kb < KB; ++kb) {
+                if (rank == 0 && kb == claim_kb) next = npairs + atomicAdd(&p.meta[META_TILES_UP], 1);
                 if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
                     ok = false;
                     break;
@@ -704,6 +759,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     ph ^= 1u;
                 }
             }
+            if (rank == 0) t = next;
         }
         if (!ok) {
             if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 10 + (int)rank);
@@ -732,7 +788,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             const uint32_t idesc = umma_idesc_bf16(2 * BM, 2 * BN1);
             int b = 0;
             uint32_t aph = 0;
-            for (int t = pair; t < total && ok && !bad; t += npairs) {
+            for (int j = 0; ok && !bad; ++j) {
+                const int t = pair_tile_wait(sm, j, tmo);
+                if (t == TILE_ABORT) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
+                if (t < 0) break;
                 if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1u, tmo, sm.abort)) {
                     ok = false;
                     break;
@@ -778,7 +841,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t acc_empty0 = mapa_shared(smem_u32(sm.acc_empty), 0u);
         int b = 0;
         uint32_t aph = 0;
-        for (int t = pair; t < total && !bad; t += npairs) {
+        const uint32_t tq_empty0 = mapa_shared(smem_u32(sm.tq_empty), 0u);
+        for (int j = 0; !bad; ++j) {
+            int t = 0;
+            if (lane == 0) {
+                t = pair_tile_wait(sm, j, tmo);
+                if (t != TILE_ABORT) {
+                    if (rank == 0) mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
+                    else mbar_arrive_cluster(tq_empty0 + 8u * (uint32_t)(j % PAIR_TILE_Q));
+                }
+            }
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t == TILE_ABORT) {
+                if (lane == 0) {
+                    if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 18 + (int)rank);
+                    pair_abort(sm, rank);
+                }
+                break;
+            }
+            if (t < 0) break;
             const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, rank);
             if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
                 if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 16 + (int)rank);

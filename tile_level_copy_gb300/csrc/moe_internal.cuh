@@ -54,6 +54,7 @@ constexpr int GEMM_WARPS = GEMM_THREADS / 32;
 constexpr int COPY_WARPS_EXTRA = 2;                    // copy-engine warps added with MOE_COPY_WARPS
 constexpr int GEMM_THREADS_MAX = GEMM_THREADS + 32 * COPY_WARPS_EXTRA;
 constexpr int TILE_Q = 4;          // slots of the tile hand-out ring (TMA thread -> UMMA issuer, epilogue)
+constexpr int PAIR_TILE_Q = 8;     // the CTA-pair kernel's ring (>= PAIR_STAGES + 2, see gemm.cu)
 constexpr int MISC_BYTES = 6144;  // barriers, flags and the expert table (4E+1 ints)
 // epilogue staging: per epilogue warp two 32-row x 32-column bf16 chunks (2 KB each), written to
 // global memory by TMA tensor stores
@@ -392,6 +393,13 @@ __device__ __forceinline__ void cluster_sync() {
 }
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// Store a 32-bit value into a peer CTA's shared memory; the store completes as 4 transaction bytes
+// on the peer's mbarrier (both addresses in the peer CTA, from mapa).
+__device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t v, uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(cluster_addr),
+                 "r"(v), "r"(cluster_bar)
+                 : "memory");
 }
 // Arrive on a barrier of the pair (own or peer) with release semantics at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
