@@ -61,8 +61,10 @@ extern "C" {
 #define MOE_COPY_WARPS 0x4u           /* copy engines also run as two extra warps in every    */
                                       /* producer CTA (16-byte loads/stores, no shared memory),*/
                                       /* so consumer_ctas may be 0: no SM leaves the GEMM       */
-#define MOE_PAIR_UMMA 0x8u            /* SwiGLU GEMM on CTA pairs: UMMA 256 x 256 over two SMs */
-                                      /* (tcgen05 cta_group::2), half the B tile per SM        */
+#define MOE_PAIR_UMMA 0x8u            /* expert GEMMs on CTA pairs: UMMA 256 x 256 over two SMs*/
+                                      /* (tcgen05 cta_group::2), half the B tile per SM; the   */
+                                      /* down-projection too when d % 256 == 0, consumer_ctas  */
+                                      /* is even and MOE_COPY_WARPS is not set                 */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
 
@@ -188,7 +190,7 @@ MOE_API int moe_plan(const moe_config* cfg, const float* logits, const uint16_t*
  * the flags and copy each ready segment of row bands into its owner's slice of Ret, then the
  * weighted top-k combine. Flags: MOE_TAIL_ASSIST (producers that finished join the copy),
  * MOE_COPY_WARPS (copy engines also inside every producer CTA; consumer_ctas may be 0),
- * MOE_PAIR_UMMA (the SwiGLU GEMM on CTA pairs); none changes the result, bit for bit. A bounded
+ * MOE_PAIR_UMMA (the expert GEMMs on CTA pairs); none changes the result, bit for bit. A bounded
  * wait that runs out, or a plan entry that fails its bounds check, is reported by moe_status(),
  * not here.
  */

@@ -240,6 +240,10 @@ __device__ __forceinline__ int plan_items_bad(const Shape& s, const PlanPtrs& p,
                     bad = it + 1;
             }
         }
+        for (int e = threadIdx.x; e < s.E && !bad; e += blockDim.x) {  // first item of each expert
+            const int first = p.experts[8 * e + 6];
+            if (first < 0 || first > NI) bad = NI + e + 1;
+        }
     }
     return bad;
 }
@@ -520,13 +524,22 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 }
 
 // =============================================================================================
-// SwiGLU GEMM on CTA pairs. A cluster of two CTAs computes one 256-row x 256-column UMMA tile:
-// the even CTA (rank 0) stages the 128 token rows of one work item and the gate half (W1 rows) of
-// the B tile, the odd CTA the rows of the expert's next work item and the up half (W3 rows); one
-// thread of rank 0 issues tcgen05.mma.cta_group::2, and each CTA's TMEM receives its own 128 rows
-// x (128 gate | 128 up) columns, so the epilogue is the single-CTA one. An expert with an odd
-// number of work items leaves the odd CTA without rows in its last pair tile (it still loads its
-// B half; its accumulator rows are not stored).
+// Expert GEMMs on CTA pairs (MOE_PAIR_UMMA). A cluster of two CTAs computes one 256-row x 256-column
+// UMMA tile: each CTA stages the 128 rows of one work item of the expert and one half of the B
+// tile; one thread of rank 0 issues tcgen05.mma.cta_group::2, and each CTA's TMEM receives its own
+// 128 rows x 256 columns, so each CTA runs the single-CTA epilogue on its rows.
+//   MODE 1 (SwiGLU up-projection): rank 0 stages the gate half of B (W1 rows), rank 1 the up half
+//       (W3 rows); each CTA's accumulator holds 128 gate | 128 up columns. Work items of an expert
+//       in pairs, N tiles outer.
+//   MODE 2 (down-projection): rank 0 stages rows 0-127 of the 256-row W2 tile, rank 1 rows
+//       128-255; each CTA's item is one band (or two half bands) of the page's padded layout, and
+//       its epilogue publishes the band flags as in gemm_kernel. Work items of an expert in pairs,
+//       in schedule order, all N tiles of a pair item together. Consumer CTAs (the last
+//       consumer_ctas blocks, whole clusters) and, with tail assist, finished producer CTAs run the
+//       bulk copy engines.
+// An expert with an odd number of work items leaves rank 1 without rows in its last pair tile: it
+// still loads its B half (rank 0's columns need it), its A box lies past the last compact row
+// (zeros), and its accumulator rows are not stored.
 //
 // Barriers: full[s] on rank 0 (the stage's bytes of both CTAs landed: rank 0 arms it with both
 // CTAs' byte counts, and rank 1's TMA loads complete on it through cta_group::2), empty[s] (UMMAs
@@ -534,15 +547,16 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 // on rank 0 (count 8: the four epilogue warps of each CTA). Every wait is bounded; a timeout
 // raises the abort word of both CTAs.
 //
-// Tile hand-out: rank 0's TMA thread takes the pair's first tile by pair index and every further
-// one from the META_TILES_UP counter (as in gemm_kernel), and publishes each index in a ring of
-// PAIR_TILE_Q slots of both CTAs: its own slot with a store and an arrive on tq_full, the peer's
-// with st.async, which completes 4 transaction bytes on the peer's tq_full (armed by the peer's TMA
-// thread, once at start and again each time it has read the slot). Rank 0's tq_empty (count 9)
-// collects rank 0's UMMA issuer and the epilogue warps of both CTAs. Rank 1's TMA thread needs no
-// arrive there: rank 0's TMA thread cannot run more than PAIR_STAGES k-blocks ahead of it (every
-// stage's barrier waits for rank 1's loads), so when rank 0 reuses a slot PAIR_TILE_Q tiles later,
-// rank 1 has long since read it.
+// Tile hand-out: rank 0's TMA thread takes every tile of the pair from the GEMM's counter in the
+// plan's meta words (the next one a few k-blocks before the current one's loads are all issued), so
+// tiles go to whichever pair is free first and no tile waits for a particular pair to be resident.
+// It publishes each index in a ring of PAIR_TILE_Q slots of both CTAs: its own slot with a store and
+// an arrive on tq_full, the peer's with st.async, which completes 4 transaction bytes on the peer's
+// tq_full (armed by the peer's TMA thread, once at start and again each time it has read the slot).
+// Rank 0's tq_empty (count 9) collects rank 0's UMMA issuer and the epilogue warps of both CTAs.
+// Rank 1's TMA thread needs no arrive there: rank 0's TMA thread cannot run more than PAIR_STAGES
+// k-blocks ahead of it (every stage's barrier waits for rank 1's loads), so when rank 0 reuses a
+// slot PAIR_TILE_Q tiles later, rank 1 has long since read it.
 // =============================================================================================
 struct PairSmem {
     uint8_t* stages;
@@ -554,6 +568,7 @@ struct PairSmem {
     uint64_t* drain;
     uint64_t* tq_full;   // PAIR_TILE_Q tile hand-out slots (see above)
     uint64_t* tq_empty;
+    uint64_t* cbar;      // copy engines (down-projection consumers and tail assist)
     uint32_t* tmem_base;
     uint32_t* peer_base;
     volatile int* abort;
@@ -575,13 +590,15 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
     sm.drain = sm.acc_empty + 2;
     sm.tq_full = sm.drain + 1;
     sm.tq_empty = sm.tq_full + PAIR_TILE_Q;
-    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.tq_empty + PAIR_TILE_Q);
+    sm.cbar = sm.tq_empty + PAIR_TILE_Q;
+    sm.tmem_base = reinterpret_cast<uint32_t*>(sm.cbar + COPY_NBUF);
     sm.peer_base = sm.tmem_base + 1;
     sm.abort = reinterpret_cast<volatile int*>(sm.peer_base + 1);
     sm.tq = sm.abort + 1;
     sm.tab = const_cast<int*>(sm.tq + PAIR_TILE_Q);
     return sm;
 }
+static_assert(COPY_NBUF * COPY_PIECE <= PAIR_STAGES * PAIR_STAGE_BYTES, "copy staging must fit the pair stage area");
 
 // One thread: the j-th tile index of the pair from this CTA's hand-out ring (TILE_ABORT if the wait
 // ran out). Rank 1's slots are filled by st.async from rank 0, so the wait acquires at cluster
@@ -600,19 +617,25 @@ __device__ __forceinline__ void pair_abort(const PairSmem& sm, uint32_t rank) {
     st_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(sm.abort)), rank ^ 1u), 1u);
 }
 
-// Pair tile t -> this CTA's rows. Order as in decode_up with two work items per pair: experts in
-// id order, N tiles outer, pairs inner; rank r takes item 2 * pair + r of the expert (mA = -1: none).
+// Largest e with cum[e] <= t (cum non-decreasing, cum[0] = 0 <= t).
+__device__ __forceinline__ int tab_segment(const int* cum, int E, int t) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Pair tile t -> this CTA's rows (MODE 1). Order as in decode_up with two work items per pair:
+// experts in id order, N tiles outer, pairs inner; rank r takes item 2 * pair + r of the expert
+// (mA = -1: none).
 __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, const int32_t* items,
                                                   uint32_t rank) {
     const int* cum = tab;
     const int* first = tab + (E + 1);
     const int* count = first + E;
-    int lo = 0, hi = E - 1;  // largest e with cum[e] <= t
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (cum[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    const int e = lo, local = t - cum[e], cnt = count[e], np = (cnt + 1) >> 1;
+    const int e = tab_segment(cum, E, t), local = t - cum[e], cnt = count[e], np = (cnt + 1) >> 1;
     const int n = local / np, it = 2 * (local - n * np) + (int)rank;
     if (it >= cnt) {
         TileRef r;
@@ -626,25 +649,47 @@ __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, 
     return compact_ref(items[2 * item], n, e);
 }
 
+// Pair tile t -> this CTA's band(s) (MODE 2). tab lists the experts in schedule order (first
+// down-projection item, items); the expert's items in pairs, all nN tiles of a pair item together;
+// rank r takes item 2 * pair + r (mA = mB = -1: none, with the expert of rank 0's item).
+__device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E, int nN, const int32_t* items,
+                                                    const int32_t* tiles, const int32_t* crow, uint32_t rank) {
+    const int* cum = tab;
+    const int* first = tab + (E + 1);
+    const int* count = first + E;
+    const int r = tab_segment(cum, E, t), local = t - cum[r];
+    const int pi = local / nN, n = local - pi * nN, it = 2 * pi + (int)rank;
+    if (it >= count[r]) {
+        TileRef x;
+        x.mA = x.mB = -1;
+        x.n = n;
+        x.e = tiles[4 * items[2 * (first[r] + 2 * pi)]];
+        x.rowA = x.rowB = x.lrowA = x.lrowB = 0;
+        return x;
+    }
+    const int item = first[r] + it;
+    return make_ref(items[2 * item], items[2 * item + 1], n, tiles, crow);
+}
+
+template <int MODE>  // 1: SwiGLU up-projection -> Hc; 2: down-projection -> Yp (+ flags / consumers)
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
-    gemm_pair_swiglu_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmW1,
-                            const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmOut) {
+    gemm_pair_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmB0,
+                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut,
+                     int num_producers, int overlapped) {
     extern __shared__ uint8_t smem_raw[];
     const PairSmem sm = carve_pair(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
-    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    int NI = p.meta[META_ITEMS_UP];
-    if (NI < 0 || NI > s.IU_max) NI = 0;
-    const int nN = s.ffn / BN1;
-    const int KB = s.d / BK;
+    const bool producer = (int)blockIdx.x < num_producers;  // even: both CTAs of a cluster share the role
+    int MT = (MODE == 2) ? p.meta[META_MTILES] : 0;
+    int NI = p.meta[(MODE == 1) ? META_ITEMS_UP : META_ITEMS];
+    if (MT < 0 || MT > s.MT_max || NI < 0 || NI > ((MODE == 1) ? s.IU_max : MT)) MT = NI = 0;
+    const int nN = (MODE == 1) ? s.ffn / BN1 : s.n_tiles_n2;
+    const int KB = ((MODE == 1) ? s.d : s.ffn) / BK;
     const unsigned long long tmo = s.timeout_ns;
-    const int bad_item = __syncthreads_or(plan_items_bad(s, p, 1, NI, 0));  // same answer in both CTAs
-    if (bad_item) {
-        if (threadIdx.x == 0 && cluster_ctarank() == 0) set_status(p.meta, ST_BAD_PLAN, -1);
-        NI = 0;
-    }
+    const int bad_item = __syncthreads_or(plan_items_bad(s, p, MODE, NI, MT));  // same answer in every CTA
+    if (bad_item) NI = 0;
 
     if (tid == 0) {
         for (int i = 0; i < PAIR_STAGES; ++i) {
@@ -660,25 +705,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             mbar_init(&sm.tq_full[i], 1);
             mbar_init(&sm.tq_empty[i], 1 + 4 + 4);
         }
-        *sm.abort = 0;
+        for (int i = 0; i < COPY_NBUF; ++i) mbar_init(&sm.cbar[i], 1);
+        *sm.abort = bad_item ? 1 : 0;  // a corrupt plan also stops the copy engines
+        if (bad_item && rank == 0) set_status(p.meta, ST_BAD_PLAN, -MODE);
         mbar_fence_init();
-        if (cluster_ctarank() == 1)  // arm every slot for rank 0's first st.async
+        if (rank == 1)  // arm every slot for rank 0's first st.async
             for (int i = 0; i < PAIR_TILE_Q; ++i) mbar_arrive_expect_tx(&sm.tq_full[i], 4);
     }
-    for (int e = tid; e < s.E; e += blockDim.x) {
-        sm.tab[(s.E + 1) + e] = p.experts[8 * e + 5];         // first work item
-        sm.tab[(s.E + 1) + s.E + e] = p.experts[8 * e + 4];   // work items
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int acc = 0;
+    if (MODE == 1) {
+        for (int e = tid; e < s.E; e += blockDim.x) {
+            sm.tab[(s.E + 1) + e] = p.experts[8 * e + 5];         // first work item
+            sm.tab[(s.E + 1) + s.E + e] = p.experts[8 * e + 4];   // work items
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0;
+            for (int e = 0; e < s.E; ++e) {
+                sm.tab[e] = acc;
+                acc += ((sm.tab[(s.E + 1) + s.E + e] + 1) >> 1) * nN;
+            }
+            sm.tab[s.E] = acc;
+        }
+    } else if (tid == 0) {
+        // experts in schedule order: each expert's down-projection items are contiguous in the item
+        // list, experts in schedule order, so sorting the first items (0 <= first <= NI, checked by
+        // plan_items_bad) gives the order and the item counts
+        int* first = sm.tab + (s.E + 1);
+        int* count = first + s.E;
         for (int e = 0; e < s.E; ++e) {
-            sm.tab[e] = acc;
-            acc += ((sm.tab[(s.E + 1) + s.E + e] + 1) >> 1) * nN;
+            const int f = p.experts[8 * e + 6];
+            int i = e;
+            while (i > 0 && first[i - 1] > f) {
+                first[i] = first[i - 1];
+                --i;
+            }
+            first[i] = f;
+        }
+        int acc = 0;
+        for (int r = 0; r < s.E; ++r) {
+            count[r] = ((r + 1 < s.E) ? first[r + 1] : NI) - first[r];
+            sm.tab[r] = acc;
+            acc += ((count[r] + 1) >> 1) * nN;
         }
         sm.tab[s.E] = acc;
     }
-    if (warp == 1) {
+    if (producer && warp == 1) {
         __syncwarp();
         tmem_alloc_pair(sm.tmem_base, TMEM_COLS);
         tmem_relinquish_pair();
@@ -686,210 +757,259 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     if (tid == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmAh);
-        tma_prefetch_desc(&tmW1);
-        tma_prefetch_desc(&tmW3);
+        tma_prefetch_desc(&tmB0);
+        tma_prefetch_desc(&tmB1);
         tma_prefetch_desc(&tmOut);
+        if (MODE == 2 && producer) atomicMin(&p.trace[MOE_TRACE_GEMM2_START], globaltimer());
     }
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // both CTAs started, their barriers initialised and TMEM allocated
     tc_fence_after();
-    if (rank == 1 && tid == 0) st_cluster_u32(mapa_shared(smem_u32(sm.peer_base), 0u), *sm.tmem_base);
+    if (producer && rank == 1 && tid == 0) st_cluster_u32(mapa_shared(smem_u32(sm.peer_base), 0u), *sm.tmem_base);
     cluster_sync();  // rank 1's column base delivered to rank 0
-    const uint32_t tmem = *sm.tmem_base;
-    const int total = NI > 0 ? sm.tab[s.E] : 0;
-    const bool bad = rank == 0 && *sm.peer_base != tmem;  // the allocation was not one pair allocation
+    const uint32_t tmem = producer ? *sm.tmem_base : 0u;
+    const int total = (NI > 0 && sm.tab[s.E] > 0) ? sm.tab[s.E] : 0;
+    const bool bad = producer && rank == 0 && *sm.peer_base != tmem;  // not one pair allocation
+    const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
+    int* const tile_counter = &p.meta[(MODE == 1) ? META_TILES_UP : META_TILES_DOWN];
+    unsigned long long last_end = 0;
 
-    if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer (both CTAs): own A rows + own half of B ----------------
-        // Rank 0 arms its full barrier with the stage's bytes of both CTAs; rank 1's loads complete
-        // on that barrier (cta_group::2), so the UMMA issuer waits on one barrier per stage.
-        int st = 0;
-        uint32_t ph = 0, issued = 0, last_ph = 0;
-        bool ok = true;
-        int t = pair;  // rank 0: first tile static, the others from the hand-out counter
-        const int claim_kb = KB > 8 ? KB - 8 : 0;
-        for (int j = 0; ok && !bad; ++j) {
-            const int slot = j % PAIR_TILE_Q;
-            if (rank == 0) {
-                if (!mbar_wait(&sm.tq_empty[slot], ((uint32_t)(j / PAIR_TILE_Q) & 1u) ^ 1u, tmo, sm.abort)) {
-                    ok = false;
-                    break;
-                }
-                const int v = t < total ? t : -1;
-                sm.tq[slot] = v;
-                mbar_arrive(&sm.tq_full[slot]);
-                st_async_u32(mapa_shared(smem_u32(const_cast<int*>(sm.tq + slot)), 1u), (uint32_t)v,
-                             mapa_shared(smem_u32(&sm.tq_full[slot]), 1u));
-            } else {
-                t = pair_tile_wait(sm, j, tmo);
-                if (t == TILE_ABORT) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&sm.tq_full[slot], 4);  // armed for the slot's next use
-            }
-            if (t < 0 || t >= total) break;
-            const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, rank);
-            const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
-            int next = total;
-            for (int kb = 0; kb < KB; ++kb) {
-                if (rank == 0 && kb == claim_kb) next = npairs + atomicAdd(&p.meta[META_TILES_UP], 1);
-                if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* a = sm.stages + st * PAIR_STAGE_BYTES;
-                uint8_t* b = a + PAIR_A_BYTES;
-                if (rank == 0) {
-                    mbar_arrive_expect_tx(&sm.full[st], bytes);
-                    if (tr.mA >= 0) tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
-                    tma_load_3d(b, &tmW1, &sm.full[st], kb * BK, tr.n * BN1, tr.e);        // gate rows
-                } else {
-                    const uint32_t full0 = mapa_shared(smem_u32(&sm.full[st]), 0u);
-                    // an odd CTA without rows loads a box past the last row: zeros, so its idle
-                    // half of the UMMA multiplies zeros (less switching power than stale rows)
-                    tma_load_2d_pair(a, &tmA, full0, kb * BK, tr.mA >= 0 ? tr.lrowA : s.PC_max);
-                    tma_load_3d_pair(b, &tmW3, full0, kb * BK, tr.n * BN1, tr.e);           // up rows
-                }
-                issued |= 1u << st;
-                last_ph = (last_ph & ~(1u << st)) | (ph << st);
-                if (++st == PAIR_STAGES) {
-                    st = 0;
-                    ph ^= 1u;
-                }
-            }
-            if (rank == 0) t = next;
-        }
-        if (!ok) {
-            if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 10 + (int)rank);
-            pair_abort(sm, rank);
-            // let loads in flight land before the CTA leaves: rank 0 waits on its barriers; rank 1's
-            // complete on rank 0's, so it waits a fixed 50 us (a tile load takes a few us)
-            int never = 0;
-            if (rank == 0) {
-                for (int i = 0; i < PAIR_STAGES; ++i)
-                    if (issued & (1u << i)) mbar_wait(&sm.full[i], (last_ph >> i) & 1u, tmo, &never);
-            } else if (issued) {
-                const unsigned long long t0 = globaltimer();
-                while (globaltimer() - t0 < 50000ull) __nanosleep(1000);
-            }
-        }
-    } else if (warp == 1 && lane == 0) {
-        int st = 0;
-        uint32_t ph = 0;
-        bool ok = true;
-        if (rank == 0) {
-            // ---------------- UMMA issuer (rank 0) ----------------
-            if (bad) {
-                set_status(p.meta, ST_PAIR_TMEM, (int)*sm.peer_base);
-                pair_abort(sm, rank);
-            }
-            const uint32_t idesc = umma_idesc_bf16(2 * BM, 2 * BN1);
-            int b = 0;
-            uint32_t aph = 0;
+    if (producer) {
+        if (warp == 0 && lane == 0) {
+            // ---------------- TMA producer (both CTAs): own A rows + own half of B ----------------
+            // Rank 0 arms its full barrier with the stage's bytes of both CTAs; rank 1's loads
+            // complete on that barrier (cta_group::2), so the UMMA issuer waits on one barrier per
+            // stage.
+            int st = 0;
+            uint32_t ph = 0, issued = 0, last_ph = 0;
+            bool ok = true;
+            const int claim_kb = KB > 8 ? KB - 8 : 0;
+            int t = (rank == 0 && !bad) ? atomicAdd(tile_counter, 1) : 0;
             for (int j = 0; ok && !bad; ++j) {
-                const int t = pair_tile_wait(sm, j, tmo);
-                if (t == TILE_ABORT) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
-                if (t < 0) break;
-                if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1u, tmo, sm.abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t dt = tmem + (uint32_t)(b * 256);
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (!mbar_wait_cluster(&sm.full[st], ph, tmo, sm.abort)) {
+                const int slot = j % PAIR_TILE_Q;
+                if (rank == 0) {
+                    if (!mbar_wait(&sm.tq_empty[slot], ((uint32_t)(j / PAIR_TILE_Q) & 1u) ^ 1u, tmo, sm.abort)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sm.stages + st * PAIR_STAGE_BYTES);
-                    const uint64_t ad = sdesc_sw128(a_addr);
-                    const uint64_t bd = sdesc_sw128(a_addr + PAIR_A_BYTES);
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16_pair(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-                    umma_commit_pair(&sm.empty[st], 0x3);
+                    const int v = t < total ? t : -1;
+                    sm.tq[slot] = v;
+                    mbar_arrive(&sm.tq_full[slot]);
+                    st_async_u32(mapa_shared(smem_u32(const_cast<int*>(sm.tq + slot)), 1u), (uint32_t)v,
+                                 mapa_shared(smem_u32(&sm.tq_full[slot]), 1u));
+                } else {
+                    t = pair_tile_wait(sm, j, tmo);
+                    if (t == TILE_ABORT) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.tq_full[slot], 4);  // armed for the slot's next use
+                }
+                if (t < 0 || t >= total) break;
+                const TileRef tr = (MODE == 1)
+                                       ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
+                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank);
+                const bool halves = MODE == 2 && tr.mB >= 0 && tr.mB != tr.mA;  // two 64-row boxes
+                const int brow = (MODE == 1) ? tr.n * BN1 : tr.n * 2 * BN1 + (int)rank * BN1;
+                const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
+                int next = total;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (rank == 0 && kb == claim_kb) next = atomicAdd(tile_counter, 1);
+                    if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* a = sm.stages + st * PAIR_STAGE_BYTES;
+                    uint8_t* b = a + PAIR_A_BYTES;
+                    if (rank == 0) {
+                        mbar_arrive_expect_tx(&sm.full[st], bytes);
+                        if (halves) {
+                            tma_load_2d(a, &tmAh, &sm.full[st], kb * BK, tr.lrowA);
+                            tma_load_2d(a + PAIR_A_BYTES / 2, &tmAh, &sm.full[st], kb * BK, tr.lrowB);
+                        } else if (tr.mA >= 0) {
+                            tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
+                        }
+                        tma_load_3d(b, &tmB0, &sm.full[st], kb * BK, brow, tr.e);  // gate rows / W2 rows 0-127
+                    } else {
+                        const uint32_t full0 = mapa_shared(smem_u32(&sm.full[st]), 0u);
+                        // an odd CTA without rows loads a box past the last row: zeros, so its idle
+                        // half of the UMMA multiplies zeros (less switching power than stale rows)
+                        if (halves) {
+                            tma_load_2d_pair(a, &tmAh, full0, kb * BK, tr.lrowA);
+                            tma_load_2d_pair(a + PAIR_A_BYTES / 2, &tmAh, full0, kb * BK, tr.lrowB);
+                        } else {
+                            tma_load_2d_pair(a, &tmA, full0, kb * BK, tr.mA >= 0 ? tr.lrowA : s.PC_max);
+                        }
+                        tma_load_3d_pair(b, &tmB1, full0, kb * BK, brow, tr.e);  // up rows / W2 rows 128-255
+                    }
+                    issued |= 1u << st;
+                    last_ph = (last_ph & ~(1u << st)) | (ph << st);
                     if (++st == PAIR_STAGES) {
                         st = 0;
                         ph ^= 1u;
                     }
                 }
-                if (!ok) break;
-                umma_commit_pair(&sm.acc_full[b], 0x3);
+                if (rank == 0) t = next;
+            }
+            if (!ok) {
+                if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 10 + (int)rank);
+                pair_abort(sm, rank);
+                // let loads in flight land before the CTA leaves: rank 0 waits on its barriers;
+                // rank 1's complete on rank 0's, so it waits a fixed 50 us (a tile load takes a
+                // few us)
+                int never = 0;
+                if (rank == 0) {
+                    for (int i = 0; i < PAIR_STAGES; ++i)
+                        if (issued & (1u << i)) mbar_wait(&sm.full[i], (last_ph >> i) & 1u, tmo, &never);
+                } else if (issued) {
+                    const unsigned long long t0 = globaltimer();
+                    while (globaltimer() - t0 < 50000ull) __nanosleep(1000);
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            int st = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            if (rank == 0) {
+                // ---------------- UMMA issuer (rank 0) ----------------
+                if (bad) {
+                    set_status(p.meta, ST_PAIR_TMEM, (int)*sm.peer_base);
+                    pair_abort(sm, rank);
+                }
+                const uint32_t idesc = umma_idesc_bf16(2 * BM, 2 * BN1);
+                int b = 0;
+                uint32_t aph = 0;
+                for (int j = 0; ok && !bad; ++j) {
+                    const int t = pair_tile_wait(sm, j, tmo);
+                    if (t == TILE_ABORT) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
+                    if (t < 0) break;
+                    if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1u, tmo, sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t dt = tmem + (uint32_t)(b * 256);
+                    for (int kb = 0; kb < KB; ++kb) {
+                        if (!mbar_wait_cluster(&sm.full[st], ph, tmo, sm.abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(sm.stages + st * PAIR_STAGE_BYTES);
+                        const uint64_t ad = sdesc_sw128(a_addr);
+                        const uint64_t bd = sdesc_sw128(a_addr + PAIR_A_BYTES);
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_bf16_pair(dt, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                        umma_commit_pair(&sm.empty[st], 0x3);
+                        if (++st == PAIR_STAGES) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit_pair(&sm.acc_full[b], 0x3);
+                    b ^= 1;
+                    if (b == 0) aph ^= 1u;
+                }
+                // Final commit to both CTAs' drain barrier: every UMMA issued has completed when it
+                // fires.
+                umma_commit_pair(sm.drain, 0x3);
+            }
+            if (!ok) {
+                if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 12 + (int)rank);
+                pair_abort(sm, rank);
+            }
+            int never = 0;
+            if (!mbar_wait(sm.drain, 0, tmo, &never) && !*sm.abort)
+                set_status(p.meta, ST_PIPE_TIMEOUT, 14 + (int)rank);
+        } else if (warp >= 2) {
+            // ---------------- epilogue (both CTAs): this CTA's 128 rows ----------------
+            const int q = warp & 3;
+            const bool flags = (MODE == 2) && overlapped;
+            EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
+            const uint32_t acc_empty0 = mapa_shared(smem_u32(sm.acc_empty), 0u);
+            const uint32_t tq_empty0 = mapa_shared(smem_u32(sm.tq_empty), 0u);
+            int b = 0;
+            uint32_t aph = 0;
+            for (int j = 0; !bad; ++j) {
+                int t = 0;
+                if (lane == 0) {
+                    t = pair_tile_wait(sm, j, tmo);
+                    if (t != TILE_ABORT) {
+                        if (rank == 0) mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
+                        else mbar_arrive_cluster(tq_empty0 + 8u * (uint32_t)(j % PAIR_TILE_Q));
+                    }
+                }
+                t = __shfl_sync(0xffffffffu, t, 0);
+                if (t == TILE_ABORT) {
+                    if (lane == 0) {
+                        if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 18 + (int)rank);
+                        pair_abort(sm, rank);
+                    }
+                    break;
+                }
+                if (t < 0) break;
+                const TileRef tr = (MODE == 1)
+                                       ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
+                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank);
+                if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
+                    if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 16 + (int)rank);
+                    if (lane == 0) pair_abort(sm, rank);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
+                // rows 0-63 belong to band mA, rows 64-127 to band mB (or to mA for a 128-row band)
+                const int mq = (q < 2) ? tr.mA : tr.mB;
+                const bool active = mq >= 0;
+                const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
+                epilogue_rows<MODE>(es, &tmOut, tb, tr.n, 2 * BN1, y, active, lane);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty0 + b * 8u);
+                if (MODE == 2 && active) {
+                    if (flags && lane == 0) {
+                        // publish this warp's rows of the tile, as in gemm_kernel: stores complete,
+                        // async proxy fenced, then the release adds to the tile flag and band counter
+                        const uint32_t inc = (tr.mB == tr.mA) ? 1u : 2u;  // quarters per band: 4 in all
+                        bulk_wait_all();
+                        fence_proxy_async_global();
+                        __threadfence();
+                        red_release_gpu_add(p.flags + (size_t)mq * s.n_tiles_n2 + tr.n, inc);
+                        const uint32_t before = atom_release_gpu_add(p.bands + mq, inc);
+                        if (before + inc == FLAG_READY * (uint32_t)s.n_tiles_n2)
+                            atomicMax(&p.trace[MOE_TRACE_BAND_DONE], globaltimer());
+                    }
+                    __syncwarp();
+                    if (lane == 0) last_end = globaltimer();
+                }
                 b ^= 1;
                 if (b == 0) aph ^= 1u;
             }
-            // Final commit to both CTAs' drain barrier: every UMMA issued has completed when it fires.
-            umma_commit_pair(sm.drain, 0x3);
-        }
-        if (!ok) {
-            if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 12 + (int)rank);
-            pair_abort(sm, rank);
-        }
-        int never = 0;
-        if (!mbar_wait(sm.drain, 0, tmo, &never) && !*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 14 + (int)rank);
-    } else if (warp >= 2) {
-        // ---------------- epilogue (both CTAs): this CTA's 128 rows ----------------
-        const int q = warp & 3;
-        EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
-        const uint32_t acc_empty0 = mapa_shared(smem_u32(sm.acc_empty), 0u);
-        int b = 0;
-        uint32_t aph = 0;
-        const uint32_t tq_empty0 = mapa_shared(smem_u32(sm.tq_empty), 0u);
-        for (int j = 0; !bad; ++j) {
-            int t = 0;
-            if (lane == 0) {
-                t = pair_tile_wait(sm, j, tmo);
-                if (t != TILE_ABORT) {
-                    if (rank == 0) mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
-                    else mbar_arrive_cluster(tq_empty0 + 8u * (uint32_t)(j % PAIR_TILE_Q));
-                }
-            }
-            t = __shfl_sync(0xffffffffu, t, 0);
-            if (t == TILE_ABORT) {
-                if (lane == 0) {
-                    if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 18 + (int)rank);
-                    pair_abort(sm, rank);
-                }
-                break;
-            }
-            if (t < 0) break;
-            const TileRef tr = decode_pair_up(t, sm.tab, s.E, p.items_up, rank);
-            if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
-                if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 16 + (int)rank);
-                if (lane == 0) pair_abort(sm, rank);
-                break;
-            }
-            tc_fence_after();
-            const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
-            const int mq = (q < 2) ? tr.mA : tr.mB;
-            const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
-            epilogue_rows<1>(es, &tmOut, tb, tr.n, 2 * BN1, y, mq >= 0, lane);
-            tc_fence_before();
+            if (lane == 0) bulk_wait_all();  // staging buffers stay valid until every store is done
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty0 + b * 8u);
-            b ^= 1;
-            if (b == 0) aph ^= 1u;
         }
-        if (lane == 0) bulk_wait_all();  // staging buffers stay valid until every store is done
         __syncwarp();
-    }
-    __syncwarp();
-    tc_fence_before();
-    cluster_sync();  // both CTAs: all roles done, all UMMAs complete (drain), no remote access left
-    if (warp == 1) {
+        tc_fence_before();
+        cluster_sync();  // both CTAs: all roles done, all UMMAs complete (drain), no remote access left
+        if (warp == 1) {
+            __syncwarp();
+            tc_fence_after();
+            tmem_dealloc_pair(tmem, TMEM_COLS);
+        }
         __syncwarp();
-        tc_fence_after();
-        tmem_dealloc_pair(tmem, TMEM_COLS);
+        cluster_sync();  // neither CTA goes on (or leaves) while the pair's TMEM release is in progress
+        if (MODE == 2 && warp >= 2 && lane == 0 && last_end) atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
     }
-    __syncwarp();
-    cluster_sync();  // neither CTA leaves while the pair's TMEM release is in progress
+    // copy engines: consumer CTAs from the start, producers once their tiles are done (tail assist)
+    if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
+        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want);
 }
 
 static cudaError_t set_smem_attr(const void* fn) {
@@ -905,18 +1025,18 @@ cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensor
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA,
-                                    const CUtensorMap& tmAh, const CUtensorMap& tmW1, const CUtensorMap& tmW3,
-                                    const CUtensorMap& tmOut, cudaStream_t st) {
-    const void* fn = reinterpret_cast<const void*>(&gemm_pair_swiglu_kernel);
+// Co-resident clusters of two of a pair kernel on this device (cluster occupancy query, cached).
+template <int MODE>
+static cudaError_t pair_clusters(int* out) {
+    const void* fn = reinterpret_cast<const void*>(&gemm_pair_kernel<MODE>);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM);
     if (e != cudaSuccess) return e;
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static int pairs_cache[64] = {0};  // co-resident pairs per device (cluster occupancy query)
+    static int cache[64] = {0};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (pairs_cache[dev] == 0) {
+    if (cache[dev] == 0) {
         cudaLaunchConfig_t q = {};  // the cluster size (2) is the kernel's compile-time one
         q.gridDim = dim3(2, 1, 1);
         q.blockDim = dim3(GEMM_THREADS, 1, 1);
@@ -925,10 +1045,35 @@ cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUt
         e = cudaOccupancyMaxActiveClusters(&n, fn, &q);
         if (e != cudaSuccess) return e;
         if (n < 1) return cudaErrorInvalidConfiguration;
-        pairs_cache[dev] = n;
+        cache[dev] = n;
     }
-    gemm_pair_swiglu_kernel<<<2 * pairs_cache[dev], GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmAh, tmW1, tmW3,
-                                                                                  tmOut);
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA,
+                                    const CUtensorMap& tmAh, const CUtensorMap& tmW1, const CUtensorMap& tmW3,
+                                    const CUtensorMap& tmOut, cudaStream_t st) {
+    int pairs = 0;
+    cudaError_t e = pair_clusters<1>(&pairs);
+    if (e != cudaSuccess) return e;
+    gemm_pair_kernel<1><<<2 * pairs, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmAh, tmW1, tmW3, tmOut, 2 * pairs, 0);
+    return cudaGetLastError();
+}
+
+// Down-projection on CTA pairs: 2 x (co-resident clusters) CTAs, the last `consumers` (even) of them
+// consumer CTAs when overlapped. Every tile is handed out by the counter, so no CTA waits for a
+// particular one to become resident: no cooperative launch is needed.
+cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
+                                  const CUtensorMap& tmW2h, const CUtensorMap& tmOut, int consumers, bool overlapped,
+                                  cudaStream_t st) {
+    int pairs = 0;
+    cudaError_t e = pair_clusters<2>(&pairs);
+    if (e != cudaSuccess) return e;
+    const int grid = 2 * pairs, producers = overlapped ? grid - consumers : grid;
+    if ((consumers & 1) || producers < 2) return cudaErrorInvalidConfiguration;
+    gemm_pair_kernel<2><<<grid, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmAh, tmW2h, tmW2h, tmOut, producers,
+                                                               overlapped ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -299,7 +299,12 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     if (overlapped && (c.consumers < min_consumers || c.consumers > c.di.sms / 2))
         return fail(MOE_ERR_ARG, "consumer_ctas=%d must be in [%d, %d]", c.consumers, min_consumers, c.di.sms / 2);
 
-    CUtensorMap tXc, tXch, tHc, tHch, tW1, tW3, tW2, tHcOut, tYpOut;
+    // The down-projection runs on CTA pairs with MOE_PAIR_UMMA when its UMMA tile is 256 columns wide,
+    // the consumer partition is whole clusters and no copy warps are asked for; the sequential
+    // baseline of the same configuration uses the same kernel.
+    const bool pair_down = (S.flags & MOE_PAIR_UMMA) && !(S.flags & MOE_COPY_WARPS) && S.bn2 == 2 * BN1 &&
+                           (c.consumers % 2 == 0);
+    CUtensorMap tXc, tXch, tHc, tHch, tW1, tW3, tW2, tW2h, tHcOut, tYpOut;
     int rc = make_map(&tXc, c.p.Xc, 2, S.d, S.PC_max, 1, BM, "Xc");
     if (!rc) rc = make_map(&tXch, c.p.Xc, 2, S.d, S.PC_max, 1, BM / 2, "Xc (half)");
     if (!rc) rc = make_map(&tHc, c.p.Hc, 2, S.ffn, S.PC_max, 1, BM, "Hc");
@@ -309,6 +314,7 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     if (!rc) rc = make_map(&tW1, W1, 3, S.d, S.ffn, S.E, BN1, "W1");
     if (!rc) rc = make_map(&tW3, W3, 3, S.d, S.ffn, S.E, BN1, "W3");
     if (!rc) rc = make_map(&tW2, W2, 3, S.ffn, S.d, S.E, S.bn2, "W2");
+    if (!rc && pair_down) rc = make_map(&tW2h, W2, 3, S.ffn, S.d, S.E, BN1, "W2 (half)");
     if (rc) return rc;
     (void)L;
 
@@ -321,11 +327,13 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
     if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
     if (overlapped) {
-        e = launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, c.consumers, true, c.st);
+        e = pair_down ? launch_gemm_down_pair(S, c.p, tHc, tHch, tW2h, tYpOut, c.consumers, true, c.st)
+                      : launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, c.consumers, true, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "overlapped down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
     } else {
-        e = launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, 0, false, c.st);
+        e = pair_down ? launch_gemm_down_pair(S, c.p, tHc, tHch, tW2h, tYpOut, 0, false, c.st)
+                      : launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, 0, false, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
         e = launch_copy_seq(S, c.p, c.di.sms, c.st);

@@ -147,6 +147,11 @@ cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUt
 cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
                              const CUtensorMap& tmW2, const CUtensorMap& tmOut, int sms, int consumers, bool overlapped,
                              cudaStream_t st);
+// The down-projection on CTA pairs (tmW2h: 128-row boxes of W2; needs bn2 = 256, consumers even, no
+// copy warps); grid = 2 x co-resident pairs.
+cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
+                                  const CUtensorMap& tmW2h, const CUtensorMap& tmOut, int consumers, bool overlapped,
+                                  cudaStream_t st);
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
 
