@@ -59,10 +59,10 @@ def captured_traffic(workload: str, pair_umma: bool):
 
 
 # Copy configuration per workload (consumer CTAs, copy warps in the producer CTAs), the fastest
-# measured on one GB300: with the producers' copy warps the fine-grained layer needs no dedicated
-# partition and the Mixtral-shaped one only 4 CTAs; the skewed layer is fastest with 8 dedicated
-# CTAs alone.
-DEFAULT_COPY = {"tiny": (4, False), "mixtral": (4, True), "skew": (8, False), "fine": (0, True)}
+# measured on one GB300: the Mixtral-shaped layer with 4 dedicated CTAs and the skewed one with 8
+# (both then run the down-projection on CTA pairs); the fine-grained layer, whose copy is five
+# times longer, with the producers' copy warps and no dedicated partition.
+DEFAULT_COPY = {"tiny": (4, False), "mixtral": (4, False), "skew": (8, False), "fine": (0, True)}
 
 
 def parse_args():
@@ -336,12 +336,21 @@ def run_ours(args, rank: int, world: int):
     meta = ws.view("meta").cpu()
     P, items, items_up, PC = (int(meta[i].item()) for i in (0, 7, 8, 9))
     TK = w.T * w.topk
+    experts = ws.view("experts").cpu().numpy()
     if cfg.flags & tlc.MOE_PAIR_UMMA:
-        iu = ws.view("experts").cpu().numpy()[:, 4]
+        iu = experts[:, 4]
         exec_rows_up = 128 * int(np.sum(2 * ((iu + 1) // 2)))
     else:
         exec_rows_up = 128 * items_up
-    exec_rows = 128 * items
+    # the down-projection runs on CTA pairs under the same conditions as in the library
+    pair_down = bool(cfg.flags & tlc.MOE_PAIR_UMMA) and not (cfg.flags & tlc.MOE_COPY_WARPS) and \
+        w.d % 256 == 0 and args.consumers % 2 == 0
+    if pair_down:  # an expert's items in pairs: an odd one also occupies the idle half of its pair
+        first = np.sort(experts[:, 6])
+        cnt = np.diff(np.append(first, items))
+        exec_rows = 128 * int(np.sum(2 * ((cnt + 1) // 2)))
+    else:
+        exec_rows = 128 * items
     up_ms = float(np.median(st_ovl[:, tlc.EV_PLANNED]))
     down_ms = float(np.median(st_seq[:, tlc.EV_UP]))
     fl_up_alg, fl_down_alg = 4.0 * TK * w.d * w.ffn, 2.0 * TK * w.d * w.ffn
@@ -353,7 +362,7 @@ def run_ours(args, rank: int, world: int):
     roof_achieved = fl_up_alg / (up_ms * 1e-3) / 1e12
     # algorithmic DRAM bytes of the SwiGLU GEMM: W1 and W3 once, the compact rows in, the hidden out
     alg_bytes_up = 2 * w.E * w.ffn * w.d * 2 + PC * w.d * 2 + PC * w.ffn * 2
-    roofline = {"kernel": ("gemm_pair_swiglu_kernel (SwiGLU up-projection, CTA pairs)" if args.pair_umma
+    roofline = {"kernel": ("gemm_pair_kernel<1> (SwiGLU up-projection, CTA pairs)" if args.pair_umma
                            else "gemm_kernel<1> (SwiGLU up-projection)"), "bound": "tensor",
                 "achieved": round(roof_achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
                 "frac": round(roof_achieved / peak_tc, 4),
@@ -405,7 +414,8 @@ def run_ours(args, rank: int, world: int):
                  "algorithmic_frac_of_peak": round(gemm_alg_tflops / peak_tc, 4),
                  "executed_frac_of_burst_peak": round(gemm_exec_tflops / peaks["bf16_tflops"], 4),
                  "peak_tflops": peak_tc, "peak_source": peaks_src, "up_ms": round(up_ms, 4),
-                 "down_ms": round(down_ms, 4), "padded_rows": P, "compact_rows": PC,
+                 "down_ms": round(down_ms, 4), "down_kernel": "gemm_pair_kernel<2> (CTA pairs)" if pair_down
+                 else "gemm_kernel<2>", "padded_rows": P, "compact_rows": PC,
                  "executed_rows_up": exec_rows_up, "executed_rows_down": exec_rows, "work_items_up": items_up,
                  "work_items_down": items, "real_rows": TK},
         "overlap": {"hidden_pct": round(100 * statistics.median(hidden), 2),

@@ -84,3 +84,96 @@ def test_pair_full_size_sampled_tokens(name):
     _, _, want = moe_ref.moe_tokens(tokens, L.logits_np, x_rows, L.weights_f64, w.topk)
     err, rel = parity(got.double().cpu().numpy()[tokens], want)
     assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
+
+
+# ---- the down-projection on CTA pairs (d % 256 == 0, even consumer_ctas, no copy warps) ----------
+
+def check_ret_is_copy_of_yp(L: Layer, plan):
+    Yp = L.ws.view("Yp").view(torch.int16)
+    Ret = L.ws.view("Ret").view(torch.int16)
+    slot = torch.from_numpy(plan.slot.reshape(-1)).long().cuda()
+    rslot = torch.from_numpy(plan.ret_slot.reshape(-1)).long().cuda()
+    assert torch.equal(Ret[rslot], Yp[slot])
+
+
+def down_items_per_expert(L: Layer) -> np.ndarray:
+    """Down-projection work items of each expert (schedule order), from the device plan."""
+    experts = L.ws.view("experts").cpu().numpy().reshape(-1, 8)[:L.w.E]
+    items = int(L.ws.view("meta")[7].item())
+    first = np.sort(experts[:, 6])
+    return np.diff(np.append(first, items))
+
+
+@pytest.mark.parametrize("name,tile_M", [("mixtral", 128), ("skew", 128), ("skew", 64), ("fine", 128)])
+@pytest.mark.parametrize("consumers", [2, 8])
+def test_pair_down_projection_matches_single_cta(name, tile_M, consumers):
+    """The pair down-projection's owner-aligned output rows Yp, return buffer and layer output equal the
+    single-CTA kernel's bit for bit (same 16-wide K steps per element), overlapped and sequential;
+    every tile flag and band counter is complete. tile_M = 64 makes every band a half band, so the
+    pairs' items are two 64-row boxes each."""
+    w = small(name, tile_M=tile_M)
+    assert w.d % 256 == 0
+    L = Layer(w, seed=5, cfg_kw=dict(consumer_ctas=consumers, flags=tlc.MOE_TAIL_ASSIST, timeout_us=200000))
+    single = L.run(sequential=True)
+    yp_single = L.ws.view("Yp").clone()
+    P = int(L.ws.view("meta")[0].item())
+    ref = L.oracle_layer()
+    rows = torch.from_numpy(ref.plan.slot.reshape(-1)).long().cuda()
+    for seq in (False, True):
+        cfg = tlc.Config.from_workload(w, consumer_ctas=consumers, flags=PAIR | tlc.MOE_TAIL_ASSIST,
+                                       timeout_us=200000)
+        L.ws.view("Yp").zero_()
+        got = L.run(sequential=seq, cfg=cfg)
+        assert torch.equal(got, single)
+        assert torch.equal(L.ws.view("Yp")[rows], yp_single[rows])
+        check_ret_is_copy_of_yp(L, ref.plan)
+        if not seq:
+            MT = ref.plan.num_tiles
+            n2 = L.ws.layout["n_tiles_n2"]
+            assert torch.all(L.ws.view("flags")[:MT] == 4)
+            assert torch.all(L.ws.view("bands")[:MT] == 4 * n2)
+    assert P == ref.plan.P
+    err, rel = parity(got.double().cpu().numpy(), ref.out)
+    assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
+
+
+def test_pair_down_covers_odd_item_counts():
+    """Seeds until an expert has an odd number of down-projection items (its last pair has an idle
+    half), then checks the pair kernel bitwise against the single-CTA one."""
+    w = small("skew")
+    for seed in range(20):
+        L = Layer(w, seed=seed, cfg_kw=dict(consumer_ctas=4, flags=tlc.MOE_TAIL_ASSIST))
+        single = L.run(sequential=False)
+        if not np.any(down_items_per_expert(L) % 2 == 1):
+            continue
+        cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=PAIR | tlc.MOE_TAIL_ASSIST)
+        assert torch.equal(L.run(sequential=False, cfg=cfg), single)
+        return
+    pytest.fail("no seed gave an expert with an odd number of down-projection items")
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_pair_down_tile_checksum_falsifier(seed):
+    """The page's falsifier (every copied row equals the stored row) for the pair kernel's flags:
+    small consumer partitions (2-6 CTAs), tail assist on half the seeds, segments of 1-2 bands."""
+    w = inputs.WORKLOADS["skew"].replace(T=1024, d=256, ffn=256)
+    L = Layer(w, seed=seed, cfg_kw=dict(consumer_ctas=2 + 2 * (seed % 3), mgb=1 + seed % 2,
+                                        flags=PAIR | (tlc.MOE_TAIL_ASSIST if seed % 2 else 0)))
+    L.run(sequential=False)
+    idx, _ = moe_ref.route_topk(L.logits_np, w.topk)
+    plan = moe_ref.build_plan(idx, w.E, w.R, w.tile_M, L.cfg.mgb)
+    check_ret_is_copy_of_yp(L, plan)
+
+
+def test_pair_down_stalled_consumer_times_out_and_context_survives():
+    """Consumers of the pair kernel wait for a flag value that no producer writes: the bounded wait
+    runs out, the status says so, and the next call is correct."""
+    w = small("skew")
+    L = Layer(w, seed=0)
+    want = L.run(sequential=True)
+    cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=PAIR | tlc.MOE_TEST_STALL_CONSUMER, timeout_us=20000)
+    tlc.forward(cfg, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws)
+    rc, _ = tlc.status(cfg, L.ws)
+    assert rc == tlc.MOE_ERR_TIMEOUT
+    cfg_ok = tlc.Config.from_workload(w, consumer_ctas=4, flags=PAIR)
+    assert torch.equal(L.run(sequential=False, cfg=cfg_ok), want)
