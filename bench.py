@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu capture summarised in profiles/gemm_swiglu_mixtral_T4096.md, per (workload, CTA-pair kernel),
 # with the SHA-256 of the kernel sources it was taken on: the bench reports it only while those
 # sources are unchanged and the launch configuration is the captured one.
-SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 2303537920 + 248910080,
-                                      "sources_sha256": "f938731afcfcd5ed0bb2c3b7c737f35e6882f94a6bbd1568ecce08357b584834"}}
+SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 1953557248 + 245744896,
+                                      "sources_sha256": "447311b3e4450d0c731612860ae4575a09fb6d1c94f405442d9c6ea06019aada"}}
 KERNEL_SOURCES = ("tile_level_copy_gb300/csrc/gemm.cu", "tile_level_copy_gb300/csrc/moe_internal.cuh",
                   "tile_level_copy_gb300/csrc/copy_ring.cuh")
 

@@ -13,6 +13,11 @@ the same on one GB300, in three parts (one JSON object per point on stdout, "par
 
   python -m tile_level_copy_gb300.sweep [--parts layer mgb copy] [--tokens 1024 4096 ...]
       [--consumers 4 8 ...] [--owners 2 4 8] [--mgbs 1 2 4] [--copy-ctas 1 2 4 ...]
+      [--copy-warps] [--no-pair] [--no-tail-assist]
+
+Both expert GEMMs run on CTA pairs unless --no-pair (the down-projection on pairs needs an even
+consumer_ctas and no copy warps, else it runs on single CTAs); tail assist is on unless
+--no-tail-assist.
 """
 from __future__ import annotations
 
@@ -120,6 +125,7 @@ def part_layer(S: Setup, a, flags):
                 _, span_seq = trace_of(cfg, args_, ws, True)
                 print(json.dumps({"part": "layer", "T": T, "R": R, "consumer_ctas": c,
                                   "copy_warps": bool(flags & tlc.MOE_COPY_WARPS),
+                                  "pair_umma": bool(flags & tlc.MOE_PAIR_UMMA),
                                   "overlapped_ms": round(ovl_ms, 4), "sequential_ms": round(seq_ms, 4),
                                   "copy_alone_ms": round(copy_ms, 4), "tail_ms": round(tail, 4),
                                   "hidden_pct": round(100 * (1 - tail / copy_ms), 2),
@@ -188,9 +194,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--no-tail-assist", action="store_true")
     ap.add_argument("--copy-warps", action="store_true", help="also run copy warps in the producer CTAs")
+    ap.add_argument("--no-pair", action="store_true", help="single-CTA GEMMs instead of CTA pairs")
     a = ap.parse_args()
 
-    flags = (0 if a.no_tail_assist else tlc.MOE_TAIL_ASSIST) | (tlc.MOE_COPY_WARPS if a.copy_warps else 0)
+    flags = (0 if a.no_tail_assist else tlc.MOE_TAIL_ASSIST) | (tlc.MOE_COPY_WARPS if a.copy_warps else 0) | \
+        (0 if a.no_pair else tlc.MOE_PAIR_UMMA)
     S = Setup()
     if "copy" in a.parts:
         part_copy(S, a)
