@@ -6,8 +6,9 @@
 //   warps 2-5   epilogue: tcgen05.ld of the accumulator, conversion, staging in shared memory and
 //               TMA tensor stores of 32 x 32 chunks to global memory
 //   warps 6-7   (down-projection with MOE_COPY_WARPS) SIMT copy engines of the return copy
-// gemm_kernel<1|2> is the single-CTA kernel (UMMA 128 x N x 16, 4-stage ring); gemm_pair_swiglu_kernel
-// runs the SwiGLU GEMM on CTA pairs (UMMA 256 x 256 x 16, cta_group::2, 6-stage ring per CTA).
+// gemm_kernel<1|2> is the single-CTA kernel (UMMA 128 x N x 16, 4-stage ring); gemm_pair_kernel<1|2>
+// runs either GEMM on CTA pairs (UMMA 256 x 256 x 16, cta_group::2, 6-stage ring per CTA). Tiles are
+// handed out at run time from a counter per GEMM (see "Tile hand-out" below).
 //
 // Method: "Fine-grained Computation-Communication Overlap via Tile-level Signaling and Scheduling
 // for Mixture-of-Experts" (pith.science/paper/W2ZARMHG):
