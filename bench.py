@@ -82,8 +82,6 @@ def parse_args():
     ap.add_argument("--pair-umma", action=argparse.BooleanOptionalAction, default=True,
                     help="SwiGLU GEMM on CTA pairs (UMMA 256 x 256 over two SMs; the default, the fastest "
                          "measured on every workload)")
-    ap.add_argument("--fused", action=argparse.BooleanOptionalAction, default=False,
-                    help="both expert GEMMs in one CTA-pair launch (MOE_FUSED_GEMMS)")
     ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=True,
                     help="time the steps as replays of a CUDA graph of one step (default); the eager "
                          "launches are timed too and reported beside")
@@ -213,7 +211,7 @@ def run_ours(args, rank: int, world: int):
         args.copy_warps = dw
     seed = args.seed + rank
     flags = (0 if args.no_tail_assist else tlc.MOE_TAIL_ASSIST) | (tlc.MOE_COPY_WARPS if args.copy_warps else 0) | \
-        (tlc.MOE_PAIR_UMMA if args.pair_umma else 0) | (tlc.MOE_FUSED_GEMMS if args.fused else 0)
+        (tlc.MOE_PAIR_UMMA if args.pair_umma else 0)
     cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags)
     peaks, peaks_src = load_peaks()
 
@@ -331,33 +329,6 @@ def run_ours(args, rank: int, world: int):
         raise RuntimeError(f"device status {rc} ({detail}) in the dedicated-partition steps")
     page_ms = float(np.median([e[tlc.EV_BEGIN].elapsed_time(e[tlc.EV_END]) for e in page_ev]))
 
-    # both GEMMs in one launch (MOE_FUSED_GEMMS) beside the configuration timed above, where the
-    # down-projection runs on CTA pairs: eager steps of the two, alternating so that both see the
-    # same clocks
-    fused_side = None
-    pair_down_cfg = bool(cfg.flags & tlc.MOE_PAIR_UMMA) and not (cfg.flags & tlc.MOE_COPY_WARPS) and \
-        w.d % 256 == 0 and args.consumers % 2 == 0
-    if pair_down_cfg:
-        cfg_a = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb,
-                                         flags=cfg.flags & ~tlc.MOE_FUSED_GEMMS)
-        cfg_b = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb,
-                                         flags=cfg.flags | tlc.MOE_FUSED_GEMMS)
-        ab = {0: [], 1: []}
-        for i in range(12):
-            for which in ((0, 1) if i % 2 == 0 else (1, 0)):
-                ev = tlc.stage_events()
-                tlc.forward(cfg_b if which else cfg_a, logits, x, W["W1"], W["W3"], W["W2"], out, ws, events=ev)
-                torch.cuda.synchronize()
-                if i >= 2:
-                    ab[which].append(ev[tlc.EV_BEGIN].elapsed_time(ev[tlc.EV_END]))
-        for c_ in (cfg_a, cfg_b):
-            rc, detail = tlc.status(c_, ws)
-            if rc != tlc.MOE_OK:
-                raise RuntimeError(f"device status {rc} ({detail}) in the fused-GEMM comparison steps")
-        fused_side = {"eager_ms_per_step": round(float(np.median(ab[1])), 4),
-                      "separate_eager_ms_per_step": round(float(np.median(ab[0])), 4),
-                      "timing": "alternating eager steps, median of 10 each"}
-
     # GEMM numbers: real rows = T*k; executed rows = 128 per work item: SwiGLU items are 128 rows of
     # one expert in the compact layout (with CTA pairs, an expert's odd item also occupies the idle
     # half of its pair), down-projection items a band or two bands that need at most 64 rows each;
@@ -402,19 +373,6 @@ def run_ours(args, rank: int, world: int):
                 "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
                 "executed_tflops": round(fl_up_exe / (up_ms * 1e-3) / 1e12, 1),
                 "algorithmic_flops_per_launch": fl_up_alg, "launch_ms": round(up_ms, 4)}
-    if cfg.flags & tlc.MOE_FUSED_GEMMS and pair_down:
-        # one launch runs both GEMMs: its stage time covers both, and so does the roofline entry
-        fused_ms = up_ms
-        up_ms = down_ms = float("nan")
-        ach = (fl_up_alg + fl_down_alg) / (fused_ms * 1e-3) / 1e12
-        roofline = {"kernel": "gemm_pair_kernel<3> (SwiGLU and down-projection in one launch, CTA pairs)",
-                    "bound": "tensor", "achieved": round(ach, 1), "peak": peak_tc, "unit": "TFLOP/s",
-                    "frac": round(ach / peak_tc, 4), "traffic": None,
-                    "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
-                    "executed_tflops": round((fl_up_exe + fl_down_exe) / (fused_ms * 1e-3) / 1e12, 1),
-                    "algorithmic_flops_per_launch": fl_up_alg + fl_down_alg, "launch_ms": round(fused_ms, 4)}
-        gemm_exec_tflops = (fl_up_exe + fl_down_exe) / (fused_ms * 1e-3) / 1e12
-        gemm_alg_tflops = ach
 
     # HBM-bound stages against the measured copy bandwidth (algorithmic bytes / stage time)
     hbm = peaks["hbm_gbs"]
@@ -439,7 +397,7 @@ def run_ours(args, rank: int, world: int):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "ffn": w.ffn, "E": w.E, "topk": w.topk,
                    "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps),
-                   "pair_umma": bool(args.pair_umma), "fused_gemms": bool(args.fused), "mgb": args.mgb,
+                   "pair_umma": bool(args.pair_umma), "mgb": args.mgb,
                    "tail_assist": not args.no_tail_assist, "seed": args.seed,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "
@@ -455,12 +413,9 @@ def run_ours(args, rank: int, world: int):
                  "executed_frac_of_peak": round(gemm_exec_tflops / peak_tc, 4),
                  "algorithmic_frac_of_peak": round(gemm_alg_tflops / peak_tc, 4),
                  "executed_frac_of_burst_peak": round(gemm_exec_tflops / peaks["bf16_tflops"], 4),
-                 "peak_tflops": peak_tc, "peak_source": peaks_src,
-                 "up_ms": None if up_ms != up_ms else round(up_ms, 4),
-                 "down_ms": None if down_ms != down_ms else round(down_ms, 4),
-                 "down_kernel": ("gemm_pair_kernel<3> (both GEMMs, CTA pairs)" if cfg.flags & tlc.MOE_FUSED_GEMMS
-                                 else "gemm_pair_kernel<2> (CTA pairs)") if pair_down else "gemm_kernel<2>",
-                 "padded_rows": P, "compact_rows": PC,
+                 "peak_tflops": peak_tc, "peak_source": peaks_src, "up_ms": round(up_ms, 4),
+                 "down_ms": round(down_ms, 4), "down_kernel": "gemm_pair_kernel<2> (CTA pairs)" if pair_down
+                 else "gemm_kernel<2>", "padded_rows": P, "compact_rows": PC,
                  "executed_rows_up": exec_rows_up, "executed_rows_down": exec_rows, "work_items_up": items_up,
                  "work_items_down": items, "real_rows": TK},
         "overlap": {"hidden_pct": round(100 * statistics.median(hidden), 2),
@@ -481,8 +436,6 @@ def run_ours(args, rank: int, world: int):
         "clocks_sequential": clocks_seq,
         "hbm_stages": hbm_stages,
     }
-    if fused_side is not None:
-        res["fused_gemms"] = fused_side
 
     if not args.no_e2e:
         # End to end from pinned host memory: every step copies its logits and tokens in and its

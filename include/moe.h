@@ -65,10 +65,6 @@ extern "C" {
                                       /* (tcgen05 cta_group::2), half the B tile per SM; the   */
                                       /* down-projection too when d % 256 == 0, consumer_ctas  */
                                       /* is even and MOE_COPY_WARPS is not set                 */
-#define MOE_FUSED_GEMMS 0x10u         /* both expert GEMMs in one persistent CTA-pair launch  */
-                                      /* (SwiGLU tiles first, each down-projection tile after  */
-                                      /* its expert's SwiGLU tiles); needs the conditions of   */
-                                      /* the pair down-projection, else ignored                */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
 
@@ -144,8 +140,6 @@ typedef struct moe_layout {
     size_t in_logits;  /* f32  [2, T, E]    staging for moe_forward_host(_pipelined), 2 slots   */
     size_t in_x;       /* bf16 [2, T, d]    staging for moe_forward_host(_pipelined), 2 slots   */
     size_t out;        /* f32  [2, T, d]    staging for moe_forward_host(_pipelined), 2 slots   */
-    size_t xready;     /* uint32 [E]        MOE_FUSED_GEMMS: finished SwiGLU tile quarters per  */
-                       /*                   expert (a down-projection tile of e waits for all)  */
 } moe_layout;
 
 /* Trace slots (uint64 ns, %globaltimer) written by the last moe_forward / _sequential call. */
@@ -157,7 +151,6 @@ typedef struct moe_layout {
 #define MOE_TRACE_LAST_ACQUIRE 5 /* overlapped: latest time a copy engine acquired a band      */
 #define MOE_TRACE_LAST_LOAD 6    /* latest issue of a bulk load by a copy engine               */
 #define MOE_TRACE_LAST_DRAIN 7   /* latest start of a copy engine's final drain                */
-#define MOE_TRACE_UP_END 8       /* MOE_FUSED_GEMMS: latest end of a SwiGLU tile               */
 
 /* Size in bytes of the workspace for `cfg` (host-only arithmetic, no CUDA call).
  * Returns MOE_ERR_ARG for an invalid config. */

@@ -51,8 +51,7 @@ def test_layout_regions_are_aligned_and_disjoint(name):
     assert all(o % 1024 == 0 for o in offs)
     assert len(set(offs)) == len(offs) and offs[-1] < L["bytes"]
     ws_view_sizes = {"Xc": L["PC_max"] * w.d * 2, "Hc": L["PC_max"] * w.ffn * 2, "Yp": L["P_max"] * w.d * 2,
-                     "Ret": TK * w.d * 2, "items_up": L["IU_max"] * 8, "tile_crow": L["MT_max"] * 4,
-                     "xready": w.E * 4}
+                     "Ret": TK * w.d * 2, "items_up": L["IU_max"] * 8, "tile_crow": L["MT_max"] * 4}
     for r, n in ws_view_sizes.items():
         nxt = min(o for o in offs if o > L[r]) if L[r] != offs[-1] else L["bytes"]
         assert nxt - L[r] >= n

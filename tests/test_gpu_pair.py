@@ -177,77 +177,3 @@ def test_pair_down_stalled_consumer_times_out_and_context_survives():
     assert rc == tlc.MOE_ERR_TIMEOUT
     cfg_ok = tlc.Config.from_workload(w, consumer_ctas=4, flags=PAIR)
     assert torch.equal(L.run(sequential=False, cfg=cfg_ok), want)
-
-
-# ---- both GEMMs in one CTA-pair launch (MOE_FUSED_GEMMS) ------------------------------------------
-
-FUSED = PAIR | tlc.MOE_FUSED_GEMMS
-
-
-@pytest.mark.parametrize("name,tile_M", [("mixtral", 128), ("skew", 128), ("skew", 64), ("fine", 128)])
-@pytest.mark.parametrize("consumers", [2, 8])
-def test_fused_gemms_match_separate_launches(name, tile_M, consumers):
-    """One launch for both GEMMs gives the hidden rows, output rows, return buffer and layer output of
-    the separate launches bit for bit, overlapped and sequential; every expert's SwiGLU tile quarters
-    published (8 per pair tile), every tile flag and band counter complete."""
-    w = small(name, tile_M=tile_M)
-    L = Layer(w, seed=6, cfg_kw=dict(consumer_ctas=consumers, flags=tlc.MOE_TAIL_ASSIST, timeout_us=200000))
-    single = L.run(sequential=True)
-    hc_single, yp_single = L.ws.view("Hc").clone(), L.ws.view("Yp").clone()
-    ref = L.oracle_layer()
-    rows = torch.from_numpy(ref.plan.slot.reshape(-1)).long().cuda()
-    PC = int(L.ws.view("meta")[9].item())
-    for seq in (False, True):
-        cfg = tlc.Config.from_workload(w, consumer_ctas=consumers, flags=FUSED | tlc.MOE_TAIL_ASSIST,
-                                       timeout_us=200000)
-        L.ws.view("Hc").zero_()
-        L.ws.view("Yp").zero_()
-        got = L.run(sequential=seq, cfg=cfg)
-        assert torch.equal(got, single)
-        assert torch.equal(L.ws.view("Hc")[:PC], hc_single[:PC])
-        assert torch.equal(L.ws.view("Yp")[rows], yp_single[rows])
-        check_ret_is_copy_of_yp(L, ref.plan)
-        experts = L.ws.view("experts").cpu().numpy().reshape(-1, 8)[:w.E]
-        want_q = ((experts[:, 4] + 1) // 2) * (w.ffn // 128) * 8
-        assert np.array_equal(L.ws.view("xready").cpu().numpy(), want_q)
-        if not seq:
-            MT = ref.plan.num_tiles
-            n2 = L.ws.layout["n_tiles_n2"]
-            assert torch.all(L.ws.view("flags")[:MT] == 4)
-            assert torch.all(L.ws.view("bands")[:MT] == 4 * n2)
-
-
-@pytest.mark.parametrize("seed", range(12))
-def test_fused_tile_checksum_falsifier(seed):
-    """The page's falsifier for the fused launch: small consumer partitions that take SwiGLU tiles and
-    then copy, tail assist on half the seeds."""
-    w = inputs.WORKLOADS["skew"].replace(T=1024, d=256, ffn=256)
-    L = Layer(w, seed=seed, cfg_kw=dict(consumer_ctas=2 + 2 * (seed % 3), mgb=1 + seed % 2,
-                                        flags=FUSED | (tlc.MOE_TAIL_ASSIST if seed % 2 else 0)))
-    L.run(sequential=False)
-    idx, _ = moe_ref.route_topk(L.logits_np, w.topk)
-    plan = moe_ref.build_plan(idx, w.E, w.R, w.tile_M, L.cfg.mgb)
-    check_ret_is_copy_of_yp(L, plan)
-
-
-def test_fused_stalled_consumer_times_out_and_context_survives():
-    w = small("skew")
-    L = Layer(w, seed=0)
-    want = L.run(sequential=True)
-    cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=FUSED | tlc.MOE_TEST_STALL_CONSUMER, timeout_us=20000)
-    tlc.forward(cfg, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws)
-    rc, _ = tlc.status(cfg, L.ws)
-    assert rc == tlc.MOE_ERR_TIMEOUT
-    cfg_ok = tlc.Config.from_workload(w, consumer_ctas=4, flags=FUSED)
-    assert torch.equal(L.run(sequential=False, cfg=cfg_ok), want)
-
-
-@pytest.mark.slow
-@pytest.mark.parametrize("name", ["mixtral", "skew"])
-def test_fused_full_size(name):
-    w = inputs.WORKLOADS[name]
-    L = Layer(w, seed=0, cfg_kw=dict(consumer_ctas=4, flags=tlc.MOE_TAIL_ASSIST | PAIR))
-    separate = L.run(sequential=False)
-    cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=tlc.MOE_TAIL_ASSIST | FUSED)
-    assert torch.equal(L.run(sequential=False, cfg=cfg), separate)
-    assert torch.equal(L.run(sequential=True, cfg=cfg), separate)

@@ -28,12 +28,10 @@ MOE_PLAN_SKIP_PERMUTE = 0x1
 MOE_TAIL_ASSIST = 0x2
 MOE_COPY_WARPS = 0x4
 MOE_PAIR_UMMA = 0x8
-MOE_FUSED_GEMMS = 0x10
 MOE_TEST_STALL_CONSUMER = 0x100
 
 TRACE_GEMM2_START, TRACE_GEMM2_END, TRACE_COPY_START, TRACE_COPY_END = 0, 1, 2, 3
 TRACE_BAND_DONE, TRACE_LAST_ACQUIRE, TRACE_LAST_LOAD, TRACE_LAST_DRAIN = 4, 5, 6, 7
-TRACE_UP_END = 8
 
 # names of the C entry points (each declared in include/moe.h)
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_plan", "moe_forward", "moe_forward_sequential",
@@ -59,8 +57,7 @@ _LAYOUT_INTS = ("P_max", "MT_max", "n_chunks", "chunk_tokens", "n_tiles_n2", "bl
                 "units_per_band", "PC_max", "IU_max")
 LAYOUT_REGIONS = ("idx", "gate", "rank", "chunk_cnt", "chunk_base", "counts", "offsets", "ret_off", "tiles",
                   "tile_ret", "sched", "seg", "experts", "items_up", "items_down", "slot", "cslot", "ret_slot", "ccoff",
-                  "tile_crow", "meta", "flags", "bands", "trace", "Xc", "Hc", "Yp", "Ret", "in_logits", "in_x", "out",
-                  "xready")
+                  "tile_crow", "meta", "flags", "bands", "trace", "Xc", "Hc", "Yp", "Ret", "in_logits", "in_x", "out")
 
 
 class _Layout(ctypes.Structure):
@@ -176,7 +173,7 @@ class Workspace:
            "tile_ret": (torch.int32, "MT"), "sched": (torch.int32, "MT"), "seg": (torch.int32, "MT2"),
            "experts": (torch.int32, "E8"), "items_up": (torch.int32, "IU2"),
            "items_down": (torch.int32, "MT2"), "meta": (torch.int32, "META"), "flags": (torch.int32, "FL"),
-           "bands": (torch.int32, "MT"), "xready": (torch.int32, "E"),
+           "bands": (torch.int32, "MT"),
            "trace": (torch.int64, "TR"), "Xc": (torch.bfloat16, "PCd"), "Hc": (torch.bfloat16, "PCF"),
            "Yp": (torch.bfloat16, "Pd"), "Ret": (torch.bfloat16, "TKd")}
 
@@ -194,7 +191,7 @@ class Workspace:
                  "MT4": (L["MT_max"], 4), "MT": (L["MT_max"],), "MT2": (L["MT_max"], 2), "E8": (c.E, 8),
                  "META": (64,), "FL": (L["MT_max"], L["n_tiles_n2"]), "TR": (16,), "Pd": (L["P_max"], c.d),
                  "PCd": (L["PC_max"], c.d), "PCF": (L["PC_max"], c.ffn), "IU2": (L["IU_max"], 2),
-                 "TKd": (TK, c.d), "E": (c.E,)}[kind]
+                 "TKd": (TK, c.d)}[kind]
         n = 1
         for s in shape:
             n *= s

@@ -529,21 +529,15 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 // UMMA tile: each CTA stages the 128 rows of one work item of the expert and one half of the B
 // tile; one thread of rank 0 issues tcgen05.mma.cta_group::2, and each CTA's TMEM receives its own
 // 128 rows x 256 columns, so each CTA runs the single-CTA epilogue on its rows.
-//   SwiGLU tiles (up-projection -> Hc): rank 0 stages the gate half of B (W1 rows), rank 1 the up
-//       half (W3 rows); each CTA's accumulator holds 128 gate | 128 up columns. An expert's work
-//       items in pairs, N tiles outer, experts in schedule order.
-//   Down-projection tiles (-> Yp): rank 0 stages rows 0-127 of the 256-row W2 tile, rank 1 rows
+//   MODE 1 (SwiGLU up-projection): rank 0 stages the gate half of B (W1 rows), rank 1 the up half
+//       (W3 rows); each CTA's accumulator holds 128 gate | 128 up columns. Work items of an expert
+//       in pairs, N tiles outer.
+//   MODE 2 (down-projection): rank 0 stages rows 0-127 of the 256-row W2 tile, rank 1 rows
 //       128-255; each CTA's item is one band (or two half bands) of the page's padded layout, and
 //       its epilogue publishes the band flags as in gemm_kernel. Work items of an expert in pairs,
 //       in schedule order, all N tiles of a pair item together. Consumer CTAs (the last
 //       consumer_ctas blocks, whole clusters) and, with tail assist, finished producer CTAs run the
 //       bulk copy engines.
-// The template argument says which tiles a launch runs: 1 SwiGLU, 2 down-projection, 3 both
-// (MOE_FUSED_GEMMS): the SwiGLU tiles are handed out first; before the first tile of an expert's
-// down-projection, a TMA thread waits until all SwiGLU tile quarters of that expert have published
-// (xready[e], release-added by the SwiGLU epilogues after their stores completed), so the
-// down-projection starts on SMs that finish their SwiGLU tiles instead of after the whole GEMM. In
-// a fused launch the consumer clusters take SwiGLU tiles too and start copying when those run out.
 // An expert with an odd number of work items leaves rank 1 without rows in its last pair tile: it
 // still loads its B half (rank 0's columns need it), its A box lies past the last compact row
 // (zeros), and its accumulator rows are not stored.
@@ -554,17 +548,16 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 // on rank 0 (count 8: the four epilogue warps of each CTA). Every wait is bounded; a timeout
 // raises the abort word of both CTAs.
 //
-// Tile hand-out: rank 0's TMA thread takes every tile of the pair from the GEMMs' counters in the
+// Tile hand-out: rank 0's TMA thread takes every tile of the pair from the GEMM's counter in the
 // plan's meta words (the next one a few k-blocks before the current one's loads are all issued), so
 // tiles go to whichever pair is free first and no tile waits for a particular pair to be resident.
-// It publishes each index (SwiGLU tiles first, then down-projection tiles offset by their count) in
-// a ring of PAIR_TILE_Q slots of both CTAs: its own slot with a store and an arrive on tq_full, the
-// peer's with st.async, which completes 4 transaction bytes on the peer's tq_full (armed by the
-// peer's TMA thread, once at start and again each time it has read the slot). Rank 0's tq_empty
-// (count 9) collects rank 0's UMMA issuer and the epilogue warps of both CTAs. Rank 1's TMA thread
-// needs no arrive there: rank 0's TMA thread cannot run more than PAIR_STAGES k-blocks ahead of it
-// (every stage's barrier waits for rank 1's loads), so when rank 0 reuses a slot PAIR_TILE_Q tiles
-// later, rank 1 has long since read it.
+// It publishes each index in a ring of PAIR_TILE_Q slots of both CTAs: its own slot with a store and
+// an arrive on tq_full, the peer's with st.async, which completes 4 transaction bytes on the peer's
+// tq_full (armed by the peer's TMA thread, once at start and again each time it has read the slot).
+// Rank 0's tq_empty (count 9) collects rank 0's UMMA issuer and the epilogue warps of both CTAs.
+// Rank 1's TMA thread needs no arrive there: rank 0's TMA thread cannot run more than PAIR_STAGES
+// k-blocks ahead of it (every stage's barrier waits for rank 1's loads), so when rank 0 reuses a
+// slot PAIR_TILE_Q tiles later, rank 1 has long since read it.
 // =============================================================================================
 struct PairSmem {
     uint8_t* stages;
@@ -581,8 +574,7 @@ struct PairSmem {
     uint32_t* peer_base;
     volatile int* abort;
     volatile int* tq;
-    int* tab;  // SwiGLU table, down-projection table (each [cum (E+1) | first item (E) | items (E)],
-               // experts in schedule order), then the SwiGLU tile quarters per expert (E)
+    int* tab;  // [cum (E+1) | first item (E) | items (E)]
 };
 
 __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
@@ -608,7 +600,6 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
     return sm;
 }
 static_assert(COPY_NBUF * COPY_PIECE <= PAIR_STAGES * PAIR_STAGE_BYTES, "copy staging must fit the pair stage area");
-static_assert((45 * 8 + 4 * (3 + PAIR_TILE_Q) + 4 * (7 * MAX_E + 2)) <= PAIR_MISC_BYTES, "pair kernel misc area");
 
 // One thread: the j-th tile index of the pair from this CTA's hand-out ring (TILE_ABORT if the wait
 // ran out). Rank 1's slots are filled by st.async from rank 0, so the wait acquires at cluster
@@ -637,31 +628,31 @@ __device__ __forceinline__ int tab_segment(const int* cum, int E, int t) {
     return lo;
 }
 
-// SwiGLU pair tile t -> this CTA's rows: experts in the table's (schedule) order, N tiles outer,
-// pairs inner; rank r takes item 2 * pair + r of the expert (mA = -1: none, with the expert of rank
-// 0's item).
+// Pair tile t -> this CTA's rows (MODE 1). Order as in decode_up with two work items per pair:
+// experts in id order, N tiles outer, pairs inner; rank r takes item 2 * pair + r of the expert
+// (mA = -1: none).
 __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, const int32_t* items,
                                                   uint32_t rank) {
     const int* cum = tab;
     const int* first = tab + (E + 1);
     const int* count = first + E;
-    const int r = tab_segment(cum, E, t), local = t - cum[r], cnt = count[r], np = (cnt + 1) >> 1;
-    const int n = local / np, pi = local - n * np, it = 2 * pi + (int)rank;
+    const int e = tab_segment(cum, E, t), local = t - cum[e], cnt = count[e], np = (cnt + 1) >> 1;
+    const int n = local / np, it = 2 * (local - n * np) + (int)rank;
     if (it >= cnt) {
-        TileRef x;
-        x.mA = x.mB = -1;
-        x.n = n;
-        x.e = items[2 * (first[r] + 2 * pi) + 1];
-        x.rowA = x.rowB = x.lrowA = x.lrowB = 0;
-        return x;
+        TileRef r;
+        r.mA = r.mB = -1;
+        r.n = n;
+        r.e = e;
+        r.rowA = r.rowB = r.lrowA = r.lrowB = 0;
+        return r;
     }
-    const int item = first[r] + it;
-    return compact_ref(items[2 * item], n, items[2 * item + 1]);
+    const int item = first[e] + it;
+    return compact_ref(items[2 * item], n, e);
 }
 
-// Down-projection pair tile t -> this CTA's band(s). The expert's items in pairs, all nN tiles of a
-// pair item together; rank r takes item 2 * pair + r (mA = mB = -1: none, with the expert of rank
-// 0's item).
+// Pair tile t -> this CTA's band(s) (MODE 2). tab lists the experts in schedule order (first
+// down-projection item, items); the expert's items in pairs, all nN tiles of a pair item together;
+// rank r takes item 2 * pair + r (mA = mB = -1: none, with the expert of rank 0's item).
 __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E, int nN, const int32_t* items,
                                                     const int32_t* tiles, const int32_t* crow, uint32_t rank) {
     const int* cum = tab;
@@ -681,72 +672,25 @@ __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E
     return make_ref(items[2 * item], items[2 * item + 1], n, tiles, crow);
 }
 
-// Builds an expert table [cum (E+1) | first item (E) | items (E)] in shared memory, experts ordered
-// by (key, id) -- each thread places its experts by counting the smaller keys, so the order is a
-// permutation whatever the keys. Called by all threads; ends with the table complete.
-//   up:   key = schedule rank, first / items = the expert's SwiGLU items
-//   down: key = first down-projection item; items = the next expert's first item minus this one's
-//         (each expert's items are contiguous in the item list, experts in schedule order)
-// cum counts pair tiles: ceil(items / 2) * nN per expert.
-__device__ void build_pair_table(int* tab, const Shape& s, const PlanPtrs& p, bool up, int NI, int nN) {
-    const int E = s.E, tid = threadIdx.x;
-    int* first = tab + (E + 1);
-    int* count = first + E;
-    const int kf = up ? 3 : 6;
-    for (int e = tid; e < E; e += blockDim.x) {
-        const int key = p.experts[8 * e + kf];
-        int pos = 0;
-        for (int f = 0; f < E; ++f) {
-            const int kf2 = p.experts[8 * f + kf];
-            pos += (kf2 < key) || (kf2 == key && f < e);
-        }
-        first[pos] = up ? p.experts[8 * e + 5] : key;
-        if (up) count[pos] = p.experts[8 * e + 4];
-    }
-    __syncthreads();
-    if (!up)
-        for (int r = tid; r < E; r += blockDim.x) count[r] = ((r + 1 < E) ? first[r + 1] : NI) - first[r];
-    __syncthreads();
-    if (tid == 0) {
-        int acc = 0;
-        for (int r = 0; r < E; ++r) {
-            tab[r] = acc;
-            acc += ((count[r] + 1) >> 1) * nN;
-        }
-        tab[E] = acc;
-    }
-    __syncthreads();
-}
-
-template <int MODES>  // 1: SwiGLU tiles -> Hc; 2: down-projection tiles -> Yp (+ flags, consumers); 3: both
+template <int MODE>  // 1: SwiGLU up-projection -> Hc; 2: down-projection -> Yp (+ flags / consumers)
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
-    gemm_pair_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmXc,
-                     const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW3,
-                     const __grid_constant__ CUtensorMap tmHcOut, const __grid_constant__ CUtensorMap tmHc,
-                     const __grid_constant__ CUtensorMap tmHch, const __grid_constant__ CUtensorMap tmW2h,
-                     const __grid_constant__ CUtensorMap tmYpOut, int num_producers, int overlapped) {
-    constexpr bool HAS_UP = (MODES & 1) != 0, HAS_DN = (MODES & 2) != 0, FUSED = MODES == 3;
+    gemm_pair_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmB0,
+                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut,
+                     int num_producers, int overlapped) {
     extern __shared__ uint8_t smem_raw[];
     const PairSmem sm = carve_pair(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
-    // producers (both CTAs of a cluster share the role: num_producers is even) take down-projection
-    // tiles; the consumer clusters copy, after taking SwiGLU tiles in a fused launch
-    const bool producer = !HAS_DN || (int)blockIdx.x < num_producers;
-    const bool gemm_cta = producer || FUSED;
-    const int E = s.E;
-    int MT = HAS_DN ? p.meta[META_MTILES] : 0;
-    int NU = HAS_UP ? p.meta[META_ITEMS_UP] : 0;
-    int ND = HAS_DN ? p.meta[META_ITEMS] : 0;
-    if (MT < 0 || MT > s.MT_max || NU < 0 || NU > s.IU_max || ND < 0 || ND > MT) MT = NU = ND = 0;
-    const int nN_up = s.ffn / BN1, nN_dn = s.n_tiles_n2;
+    const bool producer = (int)blockIdx.x < num_producers;  // even: both CTAs of a cluster share the role
+    int MT = (MODE == 2) ? p.meta[META_MTILES] : 0;
+    int NI = p.meta[(MODE == 1) ? META_ITEMS_UP : META_ITEMS];
+    if (MT < 0 || MT > s.MT_max || NI < 0 || NI > ((MODE == 1) ? s.IU_max : MT)) MT = NI = 0;
+    const int nN = (MODE == 1) ? s.ffn / BN1 : s.n_tiles_n2;
+    const int KB = ((MODE == 1) ? s.d : s.ffn) / BK;
     const unsigned long long tmo = s.timeout_ns;
-    const int bad_item = __syncthreads_or((HAS_UP ? plan_items_bad(s, p, 1, NU, 0) : 0) |
-                                          (HAS_DN ? plan_items_bad(s, p, 2, ND, MT) : 0));  // same in every CTA
-    if (bad_item) NU = ND = 0;
-    int* const tab_up = sm.tab;
-    int* const tab_dn = sm.tab + (HAS_UP ? 3 * E + 1 : 0);
-    int* const xexp = sm.tab + 2 * (3 * E + 1);  // fused: SwiGLU tile quarters per expert (by id)
+    const int bad_item = __syncthreads_or(plan_items_bad(s, p, MODE, NI, MT));  // same answer in every CTA
+    if (bad_item) NI = 0;
 
     if (tid == 0) {
         for (int i = 0; i < PAIR_STAGES; ++i) {
@@ -764,51 +708,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         }
         for (int i = 0; i < COPY_NBUF; ++i) mbar_init(&sm.cbar[i], 1);
         *sm.abort = bad_item ? 1 : 0;  // a corrupt plan also stops the copy engines
-        if (bad_item && rank == 0) set_status(p.meta, ST_BAD_PLAN, -MODES);
+        if (bad_item && rank == 0) set_status(p.meta, ST_BAD_PLAN, -MODE);
         mbar_fence_init();
         if (rank == 1)  // arm every slot for rank 0's first st.async
             for (int i = 0; i < PAIR_TILE_Q; ++i) mbar_arrive_expect_tx(&sm.tq_full[i], 4);
     }
-    if (HAS_UP) build_pair_table(tab_up, s, p, true, NU, nN_up);
-    if (HAS_DN) build_pair_table(tab_dn, s, p, false, ND, nN_dn);
-    if (FUSED)
-        for (int e = tid; e < E; e += blockDim.x) xexp[e] = ((p.experts[8 * e + 4] + 1) >> 1) * nN_up * 8;
-    if (gemm_cta && warp == 1) {
+    if (MODE == 1) {
+        for (int e = tid; e < s.E; e += blockDim.x) {
+            sm.tab[(s.E + 1) + e] = p.experts[8 * e + 5];         // first work item
+            sm.tab[(s.E + 1) + s.E + e] = p.experts[8 * e + 4];   // work items
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int acc = 0;
+            for (int e = 0; e < s.E; ++e) {
+                sm.tab[e] = acc;
+                acc += ((sm.tab[(s.E + 1) + s.E + e] + 1) >> 1) * nN;
+            }
+            sm.tab[s.E] = acc;
+        }
+    } else if (tid == 0) {
+        // experts in schedule order: each expert's down-projection items are contiguous in the item
+        // list, experts in schedule order, so sorting the first items (0 <= first <= NI, checked by
+        // plan_items_bad) gives the order and the item counts
+        int* first = sm.tab + (s.E + 1);
+        int* count = first + s.E;
+        for (int e = 0; e < s.E; ++e) {
+            const int f = p.experts[8 * e + 6];
+            int i = e;
+            while (i > 0 && first[i - 1] > f) {
+                first[i] = first[i - 1];
+                --i;
+            }
+            first[i] = f;
+        }
+        int acc = 0;
+        for (int r = 0; r < s.E; ++r) {
+            count[r] = ((r + 1 < s.E) ? first[r + 1] : NI) - first[r];
+            sm.tab[r] = acc;
+            acc += ((count[r] + 1) >> 1) * nN;
+        }
+        sm.tab[s.E] = acc;
+    }
+    if (producer && warp == 1) {
         __syncwarp();
         tmem_alloc_pair(sm.tmem_base, TMEM_COLS);
         tmem_relinquish_pair();
     }
     if (tid == 0) {
-        tma_prefetch_desc(&tmXc);
-        tma_prefetch_desc(&tmW1);
-        tma_prefetch_desc(&tmW3);
-        tma_prefetch_desc(&tmHcOut);
-        tma_prefetch_desc(&tmHc);
-        tma_prefetch_desc(&tmHch);
-        tma_prefetch_desc(&tmW2h);
-        tma_prefetch_desc(&tmYpOut);
-        if (MODES == 2 && producer) atomicMin(&p.trace[MOE_TRACE_GEMM2_START], globaltimer());
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmAh);
+        tma_prefetch_desc(&tmB0);
+        tma_prefetch_desc(&tmB1);
+        tma_prefetch_desc(&tmOut);
+        if (MODE == 2 && producer) atomicMin(&p.trace[MOE_TRACE_GEMM2_START], globaltimer());
     }
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // both CTAs started, their barriers initialised and TMEM allocated
     tc_fence_after();
-    if (gemm_cta && rank == 1 && tid == 0) st_cluster_u32(mapa_shared(smem_u32(sm.peer_base), 0u), *sm.tmem_base);
+    if (producer && rank == 1 && tid == 0) st_cluster_u32(mapa_shared(smem_u32(sm.peer_base), 0u), *sm.tmem_base);
     cluster_sync();  // rank 1's column base delivered to rank 0
-    const uint32_t tmem = gemm_cta ? *sm.tmem_base : 0u;
-    const int N_up = (HAS_UP && NU > 0 && tab_up[E] > 0) ? tab_up[E] : 0;  // SwiGLU pair tiles
-    const int N_dn = (HAS_DN && ND > 0 && tab_dn[E] > 0) ? tab_dn[E] : 0;  // down-projection pair tiles
-    const bool bad = gemm_cta && rank == 0 && *sm.peer_base != tmem;       // not one pair allocation
+    const uint32_t tmem = producer ? *sm.tmem_base : 0u;
+    const int total = (NI > 0 && sm.tab[s.E] > 0) ? sm.tab[s.E] : 0;
+    const bool bad = producer && rank == 0 && *sm.peer_base != tmem;  // not one pair allocation
     const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
-    unsigned long long last_end = 0, up_end = 0;
-    // tile index t of the ring: [0, N_up) SwiGLU tiles, [N_up, N_up + N_dn) down-projection tiles
-    auto is_down = [&](int t) { return MODES == 2 || (MODES == 3 && t >= N_up); };
-    auto decode = [&](int t) {
-        return is_down(t) ? decode_pair_down(t - N_up, tab_dn, E, nN_dn, p.items_down, p.tiles, p.tile_crow, rank)
-                          : decode_pair_up(t, tab_up, E, p.items_up, rank);
-    };
+    int* const tile_counter = &p.meta[(MODE == 1) ? META_TILES_UP : META_TILES_DOWN];
+    unsigned long long last_end = 0;
 
-    if (gemm_cta) {
+    if (producer) {
         if (warp == 0 && lane == 0) {
             // ---------------- TMA producer (both CTAs): own A rows + own half of B ----------------
             // Rank 0 arms its full barrier with the stage's bytes of both CTAs; rank 1's loads
@@ -816,22 +784,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             // stage.
             int st = 0;
             uint32_t ph = 0, issued = 0, last_ph = 0;
-            bool ok = true, up_done = !HAS_UP, dn_started = false;
-            int ready_e = -1;  // fused: the expert whose SwiGLU tiles this thread saw complete
-            // rank 0: the next tile, SwiGLU tiles first; down-projection tiles only for producers
-            auto claim = [&]() -> int {
-                if (!up_done) {
-                    const int v = atomicAdd(&p.meta[META_TILES_UP], 1);
-                    if (v < N_up) return v;
-                    up_done = true;
-                }
-                if (HAS_DN && producer) {
-                    const int v = atomicAdd(&p.meta[META_TILES_DOWN], 1);
-                    if (v < N_dn) return N_up + v;
-                }
-                return -1;
-            };
-            int t = (rank == 0 && !bad) ? claim() : 0;
+            bool ok = true;
+            const int claim_kb = KB > 8 ? KB - 8 : 0;
+            int t = (rank == 0 && !bad) ? atomicAdd(tile_counter, 1) : 0;
             for (int j = 0; ok && !bad; ++j) {
                 const int slot = j % PAIR_TILE_Q;
                 if (rank == 0) {
@@ -839,9 +794,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    sm.tq[slot] = t;
+                    const int v = t < total ? t : -1;
+                    sm.tq[slot] = v;
                     mbar_arrive(&sm.tq_full[slot]);
-                    st_async_u32(mapa_shared(smem_u32(const_cast<int*>(sm.tq + slot)), 1u), (uint32_t)t,
+                    st_async_u32(mapa_shared(smem_u32(const_cast<int*>(sm.tq + slot)), 1u), (uint32_t)v,
                                  mapa_shared(smem_u32(&sm.tq_full[slot]), 1u));
                 } else {
                     t = pair_tile_wait(sm, j, tmo);
@@ -851,39 +807,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     }
                     mbar_arrive_expect_tx(&sm.tq_full[slot], 4);  // armed for the slot's next use
                 }
-                if (t < 0 || t >= N_up + N_dn) break;
-                const bool dn = is_down(t);
-                const TileRef tr = decode(t);
-                if (FUSED && dn && tr.e != ready_e) {
-                    // the expert's hidden rows are complete once every SwiGLU tile quarter of the
-                    // expert has published (stores completed, async proxy fenced, release add)
-                    const unsigned long long t0 = globaltimer();
-                    while (ld_acquire_gpu(p.xready + tr.e) < (uint32_t)xexp[tr.e]) {
-                        if (*sm.abort || globaltimer() - t0 > tmo) {
-                            if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 20 + (int)rank);
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(128);
-                    }
-                    if (!ok) break;
-                    fence_proxy_async_global();  // the TMA loads below read what the acquire ordered
-                    ready_e = tr.e;
-                }
-                if (FUSED && dn && rank == 0 && !dn_started) {
-                    dn_started = true;
-                    atomicMin(&p.trace[MOE_TRACE_GEMM2_START], globaltimer());
-                }
-                const bool halves = dn && tr.mB >= 0 && tr.mB != tr.mA;  // two 64-row boxes
-                const int brow = dn ? tr.n * 2 * BN1 + (int)rank * BN1 : tr.n * BN1;
-                const CUtensorMap* mA = dn ? &tmHc : &tmXc;
-                const CUtensorMap* mB = dn ? &tmW2h : (rank == 0 ? &tmW1 : &tmW3);
-                const int KB = (dn ? s.ffn : s.d) / BK;
-                const int claim_kb = KB > 8 ? KB - 8 : 0;
+                if (t < 0 || t >= total) break;
+                const TileRef tr = (MODE == 1)
+                                       ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
+                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank);
+                const bool halves = MODE == 2 && tr.mB >= 0 && tr.mB != tr.mA;  // two 64-row boxes
+                const int brow = (MODE == 1) ? tr.n * BN1 : tr.n * 2 * BN1 + (int)rank * BN1;
                 const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
-                int next = -1;
+                int next = total;
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (rank == 0 && kb == claim_kb) next = claim();
+                    if (rank == 0 && kb == claim_kb) next = atomicAdd(tile_counter, 1);
                     if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
                         ok = false;
                         break;
@@ -893,23 +826,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     if (rank == 0) {
                         mbar_arrive_expect_tx(&sm.full[st], bytes);
                         if (halves) {
-                            tma_load_2d(a, &tmHch, &sm.full[st], kb * BK, tr.lrowA);
-                            tma_load_2d(a + PAIR_A_BYTES / 2, &tmHch, &sm.full[st], kb * BK, tr.lrowB);
+                            tma_load_2d(a, &tmAh, &sm.full[st], kb * BK, tr.lrowA);
+                            tma_load_2d(a + PAIR_A_BYTES / 2, &tmAh, &sm.full[st], kb * BK, tr.lrowB);
                         } else if (tr.mA >= 0) {
-                            tma_load_2d(a, mA, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
+                            tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
                         }
-                        tma_load_3d(b, mB, &sm.full[st], kb * BK, brow, tr.e);  // gate rows / W2 rows 0-127
+                        tma_load_3d(b, &tmB0, &sm.full[st], kb * BK, brow, tr.e);  // gate rows / W2 rows 0-127
                     } else {
                         const uint32_t full0 = mapa_shared(smem_u32(&sm.full[st]), 0u);
                         // an odd CTA without rows loads a box past the last row: zeros, so its idle
                         // half of the UMMA multiplies zeros (less switching power than stale rows)
                         if (halves) {
-                            tma_load_2d_pair(a, &tmHch, full0, kb * BK, tr.lrowA);
-                            tma_load_2d_pair(a + PAIR_A_BYTES / 2, &tmHch, full0, kb * BK, tr.lrowB);
+                            tma_load_2d_pair(a, &tmAh, full0, kb * BK, tr.lrowA);
+                            tma_load_2d_pair(a + PAIR_A_BYTES / 2, &tmAh, full0, kb * BK, tr.lrowB);
                         } else {
-                            tma_load_2d_pair(a, mA, full0, kb * BK, tr.mA >= 0 ? tr.lrowA : s.PC_max);
+                            tma_load_2d_pair(a, &tmA, full0, kb * BK, tr.mA >= 0 ? tr.lrowA : s.PC_max);
                         }
-                        tma_load_3d_pair(b, mB, full0, kb * BK, brow, tr.e);  // up rows / W2 rows 128-255
+                        tma_load_3d_pair(b, &tmB1, full0, kb * BK, brow, tr.e);  // up rows / W2 rows 128-255
                     }
                     issued |= 1u << st;
                     last_ph = (last_ph & ~(1u << st)) | (ph << st);
@@ -955,8 +888,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         break;
                     }
                     mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
-                    if (t < 0 || t >= N_up + N_dn) break;
-                    const int KB = (is_down(t) ? s.ffn : s.d) / BK;
+                    if (t < 0) break;
                     if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1u, tmo, sm.abort)) {
                         ok = false;
                         break;
@@ -1000,6 +932,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         } else if (warp >= 2) {
             // ---------------- epilogue (both CTAs): this CTA's 128 rows ----------------
             const int q = warp & 3;
+            const bool flags = (MODE == 2) && overlapped;
             EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
             const uint32_t acc_empty0 = mapa_shared(smem_u32(sm.acc_empty), 0u);
             const uint32_t tq_empty0 = mapa_shared(smem_u32(sm.tq_empty), 0u);
@@ -1022,9 +955,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     }
                     break;
                 }
-                if (t < 0 || t >= N_up + N_dn) break;
-                const bool dn = is_down(t);
-                const TileRef tr = decode(t);
+                if (t < 0) break;
+                const TileRef tr = (MODE == 1)
+                                       ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
+                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank);
                 if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
                     if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 16 + (int)rank);
                     if (lane == 0) pair_abort(sm, rank);
@@ -1036,13 +970,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 const int mq = (q < 2) ? tr.mA : tr.mB;
                 const bool active = mq >= 0;
                 const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
-                if (dn) epilogue_rows<2>(es, &tmYpOut, tb, tr.n, 2 * BN1, y, active, lane);
-                else epilogue_rows<1>(es, &tmHcOut, tb, tr.n, 2 * BN1, y, active, lane);
+                epilogue_rows<MODE>(es, &tmOut, tb, tr.n, 2 * BN1, y, active, lane);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(acc_empty0 + b * 8u);
-                if (dn && active) {
-                    if (overlapped && lane == 0) {
+                if (MODE == 2 && active) {
+                    if (flags && lane == 0) {
                         // publish this warp's rows of the tile, as in gemm_kernel: stores complete,
                         // async proxy fenced, then the release adds to the tile flag and band counter
                         const uint32_t inc = (tr.mB == tr.mA) ? 1u : 2u;  // quarters per band: 4 in all
@@ -1056,17 +989,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     }
                     __syncwarp();
                     if (lane == 0) last_end = globaltimer();
-                }
-                if (FUSED && !dn && lane == 0) {
-                    // publish this warp's quarter of the SwiGLU tile to the expert's down-projection
-                    // (also for an idle half: every pair tile counts 8 quarters)
-                    if (active) {
-                        bulk_wait_all();
-                        fence_proxy_async_global();
-                        __threadfence();
-                    }
-                    red_release_gpu_add(p.xready + tr.e, 1u);
-                    up_end = globaltimer();
                 }
                 b ^= 1;
                 if (b == 0) aph ^= 1u;
@@ -1084,12 +1006,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         }
         __syncwarp();
         cluster_sync();  // neither CTA goes on (or leaves) while the pair's TMEM release is in progress
-        if (HAS_DN && warp >= 2 && lane == 0 && last_end) atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
-        if (FUSED && warp >= 2 && lane == 0 && up_end) atomicMax(&p.trace[MOE_TRACE_UP_END], up_end);
+        if (MODE == 2 && warp >= 2 && lane == 0 && last_end) atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
     }
-    // copy engines: consumer CTAs (after their SwiGLU tiles in a fused launch), producers once their
-    // tiles are done (tail assist)
-    if (HAS_DN && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
+    // copy engines: consumer CTAs from the start, producers once their tiles are done (tail assist)
+    if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
         copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want);
 }
 
@@ -1135,13 +1055,10 @@ static cudaError_t pair_clusters(int* out) {
 cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA,
                                     const CUtensorMap& tmAh, const CUtensorMap& tmW1, const CUtensorMap& tmW3,
                                     const CUtensorMap& tmOut, cudaStream_t st) {
-    (void)tmAh;
     int pairs = 0;
     cudaError_t e = pair_clusters<1>(&pairs);
     if (e != cudaSuccess) return e;
-    // the down-projection maps are not used by this launch: pass copies of the SwiGLU ones
-    gemm_pair_kernel<1><<<2 * pairs, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmW1, tmW3, tmOut, tmA, tmA, tmW1,
-                                                                    tmOut, 2 * pairs, 0);
+    gemm_pair_kernel<1><<<2 * pairs, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmAh, tmW1, tmW3, tmOut, 2 * pairs, 0);
     return cudaGetLastError();
 }
 
@@ -1156,26 +1073,8 @@ cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUten
     if (e != cudaSuccess) return e;
     const int grid = 2 * pairs, producers = overlapped ? grid - consumers : grid;
     if ((consumers & 1) || producers < 2) return cudaErrorInvalidConfiguration;
-    // the SwiGLU maps are not used by this launch: pass copies of the down-projection ones
-    gemm_pair_kernel<2><<<grid, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmW2h, tmW2h, tmOut, tmA, tmAh, tmW2h,
-                                                               tmOut, producers, overlapped ? 1 : 0);
-    return cudaGetLastError();
-}
-
-// Both GEMMs in one launch on CTA pairs (MOE_FUSED_GEMMS): SwiGLU tiles first, then down-projection
-// tiles, each waiting for its expert's SwiGLU tiles; the last `consumers` CTAs take SwiGLU tiles and
-// then copy.
-cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmXc,
-                                   const CUtensorMap& tmW1, const CUtensorMap& tmW3, const CUtensorMap& tmHcOut,
-                                   const CUtensorMap& tmHc, const CUtensorMap& tmHch, const CUtensorMap& tmW2h,
-                                   const CUtensorMap& tmYpOut, int consumers, bool overlapped, cudaStream_t st) {
-    int pairs = 0;
-    cudaError_t e = pair_clusters<3>(&pairs);
-    if (e != cudaSuccess) return e;
-    const int grid = 2 * pairs, producers = overlapped ? grid - consumers : grid;
-    if ((consumers & 1) || producers < 2) return cudaErrorInvalidConfiguration;
-    gemm_pair_kernel<3><<<grid, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmXc, tmW1, tmW3, tmHcOut, tmHc, tmHch, tmW2h,
-                                                               tmYpOut, producers, overlapped ? 1 : 0);
+    gemm_pair_kernel<2><<<grid, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmAh, tmW2h, tmW2h, tmOut, producers,
+                                                               overlapped ? 1 : 0);
     return cudaGetLastError();
 }
 

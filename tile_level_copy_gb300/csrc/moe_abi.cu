@@ -123,7 +123,6 @@ int make_layout(const moe_config* c, Layout* out) {
     L.in_logits = put(2 * (size_t)T * E * 4);
     L.in_x = put(2 * (size_t)T * d * 2);
     L.out = put(2 * (size_t)T * d * 4);
-    L.xready = put(E * 4);
     L.bytes = cur;
 
     Shape& S = o.S;
@@ -180,7 +179,6 @@ PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     p.meta = reinterpret_cast<int32_t*>(b + L.meta);
     p.flags = reinterpret_cast<uint32_t*>(b + L.flags);
     p.bands = reinterpret_cast<uint32_t*>(b + L.bands);
-    p.xready = reinterpret_cast<uint32_t*>(b + L.xready);
     p.trace = reinterpret_cast<unsigned long long*>(b + L.trace);
     p.Xc = reinterpret_cast<__nv_bfloat16*>(b + L.Xc);
     p.Hc = reinterpret_cast<__nv_bfloat16*>(b + L.Hc);
@@ -306,7 +304,6 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     // baseline of the same configuration uses the same kernel.
     const bool pair_down = (S.flags & MOE_PAIR_UMMA) && !(S.flags & MOE_COPY_WARPS) && S.bn2 == 2 * BN1 &&
                            (c.consumers % 2 == 0);
-    const bool fused = pair_down && (S.flags & MOE_FUSED_GEMMS);  // both GEMMs in one pair launch
     CUtensorMap tXc, tXch, tHc, tHch, tW1, tW3, tW2, tW2h, tHcOut, tYpOut;
     int rc = make_map(&tXc, c.p.Xc, 2, S.d, S.PC_max, 1, BM, "Xc");
     if (!rc) rc = make_map(&tXch, c.p.Xc, 2, S.d, S.PC_max, 1, BM / 2, "Xc (half)");
@@ -325,21 +322,6 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     rc = run_plan(c, logits, x, true);
     if (rc) return rc;
     if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
-    if (fused) {  // both GEMMs in one launch; the SwiGLU stage event marks nothing of its own
-        cudaError_t e = launch_gemm_fused_pair(S, c.p, tXc, tW1, tW3, tHcOut, tHc, tHch, tW2h, tYpOut,
-                                               overlapped ? c.consumers : 0, overlapped, c.st);
-        if (e != cudaSuccess) return cuda_fail(e, "fused GEMM launch");
-        if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
-        if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
-        if (!overlapped) {
-            e = launch_copy_seq(S, c.p, c.di.sms, c.st);
-            if (e != cudaSuccess) return cuda_fail(e, "return copy launch");
-        }
-        if ((rc = record(ev, MOE_EV_COPIED, c.st))) return rc;
-        e = launch_combine(S, c.p, out, c.di.sms, c.st);
-        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-        return record(ev, MOE_EV_END, c.st);
-    }
     cudaError_t e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.st)
                                               : launch_gemm_swiglu(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.di.sms, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
@@ -707,7 +689,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
                  o_tiles = put(MT * 16), o_tret = put(MT * 4), o_sched = put(MT * 4), o_seg = put(MT * 8),
                  o_exp = put(E * 32), o_iu = put((size_t)L.IU_max * 8), o_id = put(MT * 8), o_meta = put(META_COUNT * 4),
                  o_flags = put(MT * (size_t)L.n_tiles_n2 * 4), o_bands = put(MT * 4), o_trace = put(TR_COUNT * 8),
-                 o_cslot = put(TK * 4), o_ccoff = put(E * R * 4), o_tcrow = put(MT * 4), o_xready = put(E * 4);
+                 o_cslot = put(TK * 4), o_ccoff = put(E * R * 4), o_tcrow = put(MT * 4);
     if (cur > (size_t)MOE_STATIC_SCRATCH_BYTES)
         return fail(MOE_ERR_ARG, "this config needs %zu bytes of static scratch; the limit is %d", cur,
                     MOE_STATIC_SCRATCH_BYTES);
@@ -741,7 +723,6 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.meta = reinterpret_cast<int32_t*>(b + o_meta);
     p.flags = reinterpret_cast<uint32_t*>(b + o_flags);
     p.bands = reinterpret_cast<uint32_t*>(b + o_bands);
-    p.xready = reinterpret_cast<uint32_t*>(b + o_xready);
     p.trace = reinterpret_cast<unsigned long long*>(b + o_trace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_route(S, logits, p, st);

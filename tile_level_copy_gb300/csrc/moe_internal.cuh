@@ -70,10 +70,7 @@ constexpr int PAIR_STAGES = 6;
 constexpr int PAIR_A_BYTES = BM * BK * 2;              // 16 KB
 constexpr int PAIR_B_BYTES = 128 * BK * 2;             // 16 KB
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
-// the pair kernels' barriers, tile ring and expert tables (two tables of 3E+1 ints and E expected
-// counts with MOE_FUSED_GEMMS, E <= MAX_E)
-constexpr int PAIR_MISC_BYTES = 10240;
-constexpr int PAIR_SMEM = PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES + PAIR_MISC_BYTES + 1024;
+constexpr int PAIR_SMEM = PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES + MISC_BYTES + 1024;
 static_assert(PAIR_SMEM <= 227 * 1024, "pair GEMM shared memory");
 constexpr int BN1 = 128;                               // output columns of a SwiGLU tile
 constexpr uint32_t FLAG_READY = 4;                     // one release-add per epilogue warp
@@ -114,7 +111,6 @@ struct PlanPtrs {
     int32_t* meta;
     uint32_t* flags;
     uint32_t* bands;
-    uint32_t* xready;    // [E] finished SwiGLU tile quarters per expert (fused GEMMs)
     unsigned long long* trace;
     __nv_bfloat16* Xc;
     __nv_bfloat16* Hc;
@@ -156,11 +152,6 @@ cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMa
 cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
                                   const CUtensorMap& tmW2h, const CUtensorMap& tmOut, int consumers, bool overlapped,
                                   cudaStream_t st);
-// Both GEMMs in one CTA-pair launch (MOE_FUSED_GEMMS; the pair down-projection's conditions).
-cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmXc,
-                                   const CUtensorMap& tmW1, const CUtensorMap& tmW3, const CUtensorMap& tmHcOut,
-                                   const CUtensorMap& tmHc, const CUtensorMap& tmHch, const CUtensorMap& tmW2h,
-                                   const CUtensorMap& tmYpOut, int consumers, bool overlapped, cudaStream_t st);
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
 
