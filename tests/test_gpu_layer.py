@@ -67,6 +67,10 @@ EDGE_SHAPES = [
     dict(T=1000, d=128, ffn=256, E=256, topk=8, R=4, tile_M=128),  # max E, max k, mostly 1-row groups
     dict(T=64, d=128, ffn=128, E=16, topk=1, R=64, tile_M=128),  # one token per owner
     dict(T=512, d=384, ffn=384, E=6, topk=2, R=2, tile_M=128),   # d, ffn not multiples of 256
+    # d = 256: the down-projection runs on CTA pairs too (even consumer_ctas, no copy warps)
+    dict(T=8, d=256, ffn=128, E=1, topk=1, R=1, tile_M=64),      # one expert, one pair item, idle half
+    dict(T=1000, d=256, ffn=256, E=256, topk=8, R=4, tile_M=128),  # max E: many experts with 0 or 1 item
+    dict(T=64, d=256, ffn=128, E=16, topk=1, R=64, tile_M=128),  # one token per owner
 ]
 
 
@@ -98,7 +102,7 @@ def test_all_tokens_to_one_expert_layer():
     seq = L.run(sequential=True)
     err, rel = parity(seq.double().cpu().numpy(), ref.out)
     assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
-    for flags in (tlc.MOE_TAIL_ASSIST, tlc.MOE_PAIR_UMMA):
+    for flags in (tlc.MOE_TAIL_ASSIST, tlc.MOE_PAIR_UMMA, tlc.MOE_PAIR_UMMA | tlc.MOE_TAIL_ASSIST):
         cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=flags)
         assert torch.equal(L.run(sequential=False, cfg=cfg), seq)
 
