@@ -191,9 +191,10 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     int* s_tg = s_dyn + (mirror ? s.MT_max : 0);
 
     // 1. per group: chunk bases (exclusive prefix over the owner's chunks) and n_{e,r}; the counts
-    // are read eight at a time so that their loads are in flight together
-    for (int g = tid; g < G; g += PLAN_THREADS) {
-        const int e = g / R, r = g % R;
+    // are read eight at a time so that their loads are in flight together, and neighbouring threads
+    // take neighbouring experts of one owner, so that a warp's loads of one chunk are contiguous
+    for (int q = tid; q < G; q += PLAN_THREADS) {
+        const int r = q / E, e = q % E, g = e * R + r;
         const int32_t* __restrict__ cnt = p.chunk_cnt + e;
         int32_t* __restrict__ base = p.chunk_base + e;
         int acc = 0;
@@ -386,28 +387,40 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             }
     }
     __syncthreads();
-    for (int x = tid; x < E; x += PLAN_THREADS) {
-        const int cnt = s_mt[x];
+    // One warp per expert, its bands in schedule order 32 at a time: a band with more than 64 valid
+    // rows is an item of its own; bands with at most 64 pair up in order, each pair emitted at its
+    // second band, an unpaired last one at the end. An item's index is the number of items emitted
+    // before it: (full bands before it) + (half bands before it) / 2.
+    for (int x = tid >> 5; x < E; x += PLAN_THREADS / 32) {
+        const int lane = tid & 31, cnt = s_mt[x];
         int* out = p.items_down + 2 * s_ibase_down[x];
-        int n = 0, pending = -1;
-        for (int i = 0; i < cnt; ++i) {
-            const int m = sched_at(s_ebase[x] + i);
-            if (valid_of(m) > 64) {
-                out[2 * n] = m;
-                out[2 * n + 1] = m;
-                ++n;
-            } else if (pending < 0) {
-                pending = m;
-            } else {
-                out[2 * n] = pending;
-                out[2 * n + 1] = m;
-                ++n;
-                pending = -1;
+        int nfull = 0, nhalf = 0, pending = -1;  // before the current chunk; the unpaired half band
+        for (int b0 = 0; b0 < cnt; b0 += 32) {
+            const bool in = b0 + lane < cnt;
+            const int m = in ? sched_at(s_ebase[x] + b0 + lane) : -1;
+            const bool half = in && valid_of(m) <= 64;
+            const unsigned hm = __ballot_sync(0xffffffffu, half), fm = __ballot_sync(0xffffffffu, in && !half);
+            const unsigned lt = (1u << lane) - 1u;
+            const int hb = nhalf + __popc(hm & lt), fb = nfull + __popc(fm & lt);
+            const unsigned prev = hm & lt;  // half bands of this chunk before this lane
+            const int partner_lane = prev ? 31 - __clz(prev) : lane;
+            const int partner = __shfl_sync(0xffffffffu, m, partner_lane);
+            if (in && !half) {
+                out[2 * (fb + hb / 2)] = m;
+                out[2 * (fb + hb / 2) + 1] = m;
+            } else if (half && (hb & 1)) {  // second band of a pair
+                out[2 * (fb + hb / 2)] = prev ? partner : pending;
+                out[2 * (fb + hb / 2) + 1] = m;
             }
+            const int last_half_lane = hm ? 31 - __clz(hm) : 0;
+            const int last_half = __shfl_sync(0xffffffffu, m, last_half_lane);
+            nfull += __popc(fm);
+            nhalf += __popc(hm);
+            pending = (nhalf & 1) ? (hm ? last_half : pending) : -1;
         }
-        if (pending >= 0) {
-            out[2 * n] = pending;
-            out[2 * n + 1] = tbM == 64 ? -1 : pending;
+        if (lane == 0 && pending >= 0) {
+            out[2 * (nfull + nhalf / 2)] = pending;
+            out[2 * (nfull + nhalf / 2) + 1] = tbM == 64 ? -1 : pending;
         }
     }
 
