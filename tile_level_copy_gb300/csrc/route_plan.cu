@@ -10,59 +10,90 @@
 
 namespace moe {
 
-constexpr int ROUTE_THREADS = 128;   // one thread per token of a chunk of <= 128 tokens
+constexpr int ROUTE_THREADS = 256;   // threads per chunk of <= 128 tokens: 2 or more per token
 constexpr int KMAX = 8;
 
 // ---------------------------------------------------------------------------------------------
-// route_kernel<K>: one CTA per chunk of `chunk_tokens` consecutive tokens (a chunk never straddles
-// two owners), K = top-k. The chunk's logits are staged in shared memory with coalesced loads (rows
-// padded to E+1 words against bank conflicts); then thread t, for token t of the chunk, scans its E
-// logits once, keeping a sorted list of the K best (value descending, ties to the lower expert id:
-// a logit enters only if strictly greater than the list's last, and is inserted after every entry
-// not smaller than it), and forms the gates = softmax over the K chosen logits in fp32. Last, each
+// route_kernel<K>: one CTA per chunk of C = `chunk_tokens` consecutive tokens (a chunk never
+// straddles two owners), K = top-k. The chunk's logits are staged in shared memory (16-byte loads
+// when the rows allow, rows padded to E+1 words against bank conflicts). TPT = ROUTE_THREADS / C
+// threads share a token: each scans every TPT-th logit of the row, keeping a sorted list of its K
+// best (value descending, ties to the lower expert id: a logit enters only if strictly greater
+// than the list's last, and is inserted after every entry not smaller than it); the TPT lists are
+// merged with shuffles, K times taking the best head (value, then lower id) of the group, which is
+// the order a single scan of the row gives. The token's first thread forms the gates = softmax over
+// the K chosen logits in fp32. Last, thread t of the chunk's first C threads takes token t: each
 // warp ORs its lanes into a per-expert lane mask in shared memory, which gives each token's rank
 // among the chunk's tokens routed to that expert (ascending token order) and the chunk's count per
 // expert.
 // ---------------------------------------------------------------------------------------------
 template <int K>
 __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const float* __restrict__ logits, PlanPtrs p) {
-    extern __shared__ float s_logit[];  // [C][E + 1]
+    extern __shared__ float s_logit[];  // [C][E + 1], then the chosen experts [C][K] (ints)
     __shared__ uint32_t s_mask[ROUTE_THREADS / 32][MAX_E];
     __shared__ int32_t s_wpre[ROUTE_THREADS / 32][MAX_E];
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tl = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int C = s.chunk_tokens, E = s.E, ld = E + 1;
+    int* s_te = reinterpret_cast<int*>(s_logit + C * ld);
     const int t0 = blockIdx.x * C;
     const float* src = logits + (size_t)t0 * E;
     const int n = C * E;
-    for (int i0 = threadIdx.x; i0 < n; i0 += ROUTE_THREADS * 8) {  // eight loads in flight per thread
-        float v[8];
+    if ((E & 3) == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        // 16-byte loads, all in flight together (a row is a whole number of vectors)
+        const float4* src4 = reinterpret_cast<const float4*>(src);
+        const int n4 = n >> 2;
+        for (int i0 = tid; i0 < n4; i0 += ROUTE_THREADS * 8) {
+            float4 v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * ROUTE_THREADS;
-            v[u] = (i < n) ? __ldg(src + i) : 0.f;
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * ROUTE_THREADS;
+                if (i < n4) v[u] = __ldg(src4 + i);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * ROUTE_THREADS;
+                if (i < n4) {
+                    float* d = s_logit + ((4 * i) / E) * ld + (4 * i) % E;
+                    d[0] = v[u].x;
+                    d[1] = v[u].y;
+                    d[2] = v[u].z;
+                    d[3] = v[u].w;
+                }
+            }
         }
+    } else {
+        for (int i0 = tid; i0 < n; i0 += ROUTE_THREADS * 8) {  // eight loads in flight per thread
+            float v[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * ROUTE_THREADS;
-            if (i < n) s_logit[(i / E) * ld + (i % E)] = v[u];
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * ROUTE_THREADS;
+                v[u] = (i < n) ? __ldg(src + i) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * ROUTE_THREADS;
+                if (i < n) s_logit[(i / E) * ld + (i % E)] = v[u];
+            }
         }
     }
     __syncthreads();
     for (int e = lane; e < E; e += 32) s_mask[warp][e] = 0u;
-    __syncwarp();
 
-    const bool live = tl < C;
-    int te[K];
-    if (live) {
-        const float* row = s_logit + tl * ld;
+    // top-K of token tl by its TPT threads (TPT a power of two <= 32, so a token's threads share a
+    // warp); threads past the chunk's tokens keep empty lists
+    const int TPT = min(ROUTE_THREADS / C, 32), tl = tid / TPT, sub = tid % TPT;
+    const bool tok = tl < C;
+    {
+        const float* row = s_logit + (tok ? tl : 0) * ld;
         float tv[K];
+        int te[K];
 #pragma unroll
         for (int j = 0; j < K; ++j) {
             tv[j] = -INFINITY;
             te[j] = -1;
         }
-        for (int e = 0; e < E; ++e) {
+        for (int e = sub; tok && e < E; e += TPT) {
             const float v = row[e];
             if (te[K - 1] < 0 || v > tv[K - 1]) {
                 float cv = v;
@@ -82,22 +113,59 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
                 }
             }
         }
-        float z[K], sum = 0.f;
+        // merge: K times, the group's best head (greater value, then lower id; an empty list's head
+        // loses) is taken and its list advances
+        float mv[K];
+        int me[K];
 #pragma unroll
         for (int j = 0; j < K; ++j) {
-            z[j] = expf(tv[j] - tv[0]);
-            sum += z[j];
+            float bv = tv[0];
+            int be = te[0];
+            for (int o = 1; o < TPT; o <<= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                const bool take = oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be));
+                bv = take ? ov : bv;
+                be = take ? oe : be;
+            }
+            mv[j] = bv;
+            me[j] = be;
+            if (te[0] == be && be >= 0) {  // this thread's head was taken: pop it
+#pragma unroll
+                for (int q = 0; q + 1 < K; ++q) {
+                    tv[q] = tv[q + 1];
+                    te[q] = te[q + 1];
+                }
+                tv[K - 1] = -INFINITY;
+                te[K - 1] = -1;
+            }
         }
-        const int t = t0 + tl;
+        if (sub == 0 && tok) {
+            float z[K], sum = 0.f;
 #pragma unroll
-        for (int j = 0; j < K; ++j) {
-            p.idx[(size_t)t * K + j] = te[j];
-            p.gate[(size_t)t * K + j] = z[j] / sum;
-            atomicOr(&s_mask[warp][te[j]], 1u << lane);
+            for (int j = 0; j < K; ++j) {
+                z[j] = expf(mv[j] - mv[0]);
+                sum += z[j];
+            }
+            const int t = t0 + tl;
+#pragma unroll
+            for (int j = 0; j < K; ++j) {
+                p.idx[(size_t)t * K + j] = me[j];
+                p.gate[(size_t)t * K + j] = z[j] / sum;
+                s_te[tl * K + j] = me[j];
+            }
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += ROUTE_THREADS) {
+
+    // ranks and counts: thread tid < C takes token tid
+    const bool live = tid < C;
+    if (live) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) atomicOr(&s_mask[warp][s_te[tid * K + j]], 1u << lane);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += ROUTE_THREADS) {
         int acc = 0;
         for (int w = 0; w < ROUTE_THREADS / 32; ++w) {
             s_wpre[w][e] = acc;
@@ -108,29 +176,39 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
     __syncthreads();
     if (live) {
         const uint32_t lt = (1u << lane) - 1u;
-        const int t = t0 + tl;
+        const int t = t0 + tid;
 #pragma unroll
         for (int j = 0; j < K; ++j) {
-            const int e = te[j];
+            const int e = s_te[tid * K + j];
             p.rank[(size_t)t * K + j] = s_wpre[warp][e] + __popc(s_mask[warp][e] & lt);
         }
     }
 }
 
+template <int K>
+static cudaError_t launch_route_k(const Shape& s, const float* logits, const PlanPtrs& p, size_t smem, cudaStream_t st) {
+    // the staged logits and chosen experts can take the dynamic shared memory past 48 KB with the
+    // static per-warp masks: allow what this launch needs
+    const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&route_kernel<K>),
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    route_kernel<K><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p, cudaStream_t st) {
-    const size_t smem = (size_t)s.chunk_tokens * (s.E + 1) * sizeof(float);
+    const size_t smem = (size_t)s.chunk_tokens * ((s.E + 1) * sizeof(float) + s.k * sizeof(int));
     switch (s.k) {
-        case 1: route_kernel<1><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
-        case 2: route_kernel<2><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
-        case 3: route_kernel<3><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
-        case 4: route_kernel<4><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
-        case 5: route_kernel<5><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
-        case 6: route_kernel<6><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
-        case 7: route_kernel<7><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
-        case 8: route_kernel<8><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p); break;
+        case 1: return launch_route_k<1>(s, logits, p, smem, st);
+        case 2: return launch_route_k<2>(s, logits, p, smem, st);
+        case 3: return launch_route_k<3>(s, logits, p, smem, st);
+        case 4: return launch_route_k<4>(s, logits, p, smem, st);
+        case 5: return launch_route_k<5>(s, logits, p, smem, st);
+        case 6: return launch_route_k<6>(s, logits, p, smem, st);
+        case 7: return launch_route_k<7>(s, logits, p, smem, st);
+        case 8: return launch_route_k<8>(s, logits, p, smem, st);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------------------------
