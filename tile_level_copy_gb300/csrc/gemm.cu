@@ -20,8 +20,9 @@
 //       the band's counter with release semantics; copy engines read the band counter with
 //       ld.acquire.gpu (ready at 4 x tiles per band); bulk engines fence the async proxy first.
 //   "What carries the argument" - the consumer runs on a small dedicated SM partition; here the
-//       partition is the last consumer_ctas CTAs of the same cooperative launch, so producers and
-//       consumers are guaranteed to be co-resident.
+//       partition is the last consumer_ctas CTAs of the down-projection's own launch (a cooperative
+//       launch for the single-CTA kernel, so producers and consumers are co-resident; the pair
+//       kernel hands out every tile at run time, so no band waits for a particular CTA).
 #include "copy_ring.cuh"
 
 namespace moe {
