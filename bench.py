@@ -144,56 +144,153 @@ def aggregate(local_seconds: float, local_units: float, world: int):
 
 
 # ------------------------------------------------------------------------------------ clocks
+class Nvml:
+    """Read-only NVML queries (libnvidia-ml through ctypes) of one GPU: SM clock, maximum SM clock,
+    clock event (throttle) reason bits and power draw. Raises OSError where NVML is unavailable."""
+
+    CLOCK_SM = 1
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        self.ct = ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError as e:
+            raise OSError(f"libnvidia-ml: {e}")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.lib = lib
+        dev = ctypes.c_void_p()
+        ok = False
+        try:  # the CUDA device's UUID names the same GPU whatever CUDA_VISIBLE_DEVICES says
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(cuda_index).uuid)
+            ok = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(dev)) == 0
+        except Exception:
+            ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(dev)) != 0:
+            raise OSError("no NVML handle for the device")
+        self.dev = dev
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(dev, self.CLOCK_SM, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        try:
+            self._reasons = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def read(self):
+        """(SM MHz, max SM MHz, reason bits, power in W)."""
+        ct = self.ct
+        c, r, pw = ct.c_uint(0), ct.c_ulonglong(0), ct.c_uint(0)
+        self.lib.nvmlDeviceGetClockInfo(self.dev, self.CLOCK_SM, ct.byref(c))
+        self._reasons(self.dev, ct.byref(r))
+        self.lib.nvmlDeviceGetPowerUsage(self.dev, ct.byref(pw))
+        return float(c.value), self.max_mhz, int(r.value), pw.value / 1000.0
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+# NVML clock event reason bits (nvml.h) reported by name
+REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons during the timed region."""
+    """SM clock, power and clock event (throttle) reasons sampled during the timed region.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    A background thread reads NVML every 2 ms between __enter__ and __exit__, so even a timed region
+    of a few tens of milliseconds holds many samples taken under load. `reader` (for tests) replaces
+    NVML; where NVML cannot be opened, nvidia-smi is sampled every 200 ms instead (it needs a timed
+    region of a second or more to see the load)."""
 
-    def __init__(self, gpu_index: int):
+    SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_S = 0.002
+
+    def __init__(self, gpu_index: int, reader=None):
         self.gpu = gpu_index
+        self.reader = reader
+        self.nvml = None
         self.proc = None
+        self.thread = None
+        self.samples = []  # (sm MHz, max MHz, reason names, power W)
+        self.source = "unsampled"
+
+    def _poll(self, stop):
+        read = self.reader or self.nvml.read
+        while True:
+            try:
+                mhz, mx, bits, pw = read()
+                self.samples.append((mhz, mx, [n for b, n in REASON_BITS.items() if bits & b], pw))
+            except Exception:
+                return
+            if stop.wait(self.PERIOD_S):
+                return
 
     def __enter__(self):
+        import threading
+        if self.reader is None:
+            try:
+                self.nvml = Nvml(self.gpu)
+            except OSError:
+                self.nvml = None
+        if self.reader is not None or self.nvml is not None:
+            self.source = "nvml" if self.reader is None else "reader"
+            self._stop = threading.Event()
+            self.thread = threading.Thread(target=self._poll, args=(self._stop,), daemon=True)
+            self.thread.start()
+            return self
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.SMI_FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
         except OSError:
             self.proc = None
         time.sleep(0.3)
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        if self.thread is not None:
+            self._stop.set()
+            self.thread.join(timeout=5)
+            if self.nvml is not None:
+                self.nvml.close()
+            return
+        out = ""
         if self.proc is not None:
             time.sleep(0.25)
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                out, _ = self.proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
-
-    def summary(self):
-        sm, mx, reasons = [], 0.0, set()
+                out, _ = self.proc.communicate()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (self.out or "").splitlines():
+        for line in (out or "").splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = max(mx, float(parts[2]))
+                mhz, mx = float(parts[1]), float(parts[2])
+                pw = float(parts[3])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+            self.samples.append((mhz, mx, [n for n, v in zip(names, parts[5:9]) if v.lower().startswith("active")],
+                                 pw))
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "source": self.source}
+        reasons = sorted({n for s in self.samples for n in s[2]})
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples),
+                "sm_mhz_min": min(s[0] for s in self.samples),
+                "power_w_max": round(max(s[3] for s in self.samples), 1),
+                "reasons": reasons, "samples": len(self.samples), "source": self.source}
 
 
 # ---------------------------------------------------------------------------------- our arm
@@ -357,7 +454,16 @@ def run_ours(args, rank: int, world: int):
     fl_up_exe, fl_down_exe = 4.0 * exec_rows_up * w.d * w.ffn, 2.0 * exec_rows * w.d * w.ffn
     gemm_exec_tflops = (fl_up_exe + fl_down_exe) / ((up_ms + down_ms) * 1e-3) / 1e12
     gemm_alg_tflops = (fl_up_alg + fl_down_alg) / ((up_ms + down_ms) * 1e-3) / 1e12
-    peak_tc = peaks["bf16_tflops_sustained"]
+    # The SwiGLU launch time comes from the eager timed region. The measured sustained rate is a
+    # seconds-long GEMM loop under the power limit; a timed region shorter than a second runs
+    # before the power limiter pulls the clock down (the clock record shows it), so it is held to
+    # the burst rate instead.
+    eager_region_s = sec_ovl_eager
+    if eager_region_s >= 1.0:
+        peak_tc, peak_kind = peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
+    else:
+        peak_tc, peak_kind = peaks["bf16_tflops"], "bf16_tflops (burst)"
+    peak_note = f"{peaks_src} {peak_kind}: the kernel's launches were timed over a {eager_region_s:.3f} s region"
 
     roof_achieved = fl_up_alg / (up_ms * 1e-3) / 1e12
     # algorithmic DRAM bytes of the SwiGLU GEMM: W1 and W3 once, the compact rows in, the hidden out
@@ -370,7 +476,7 @@ def run_ours(args, rank: int, world: int):
                 "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch, "
                                   "profiles/gemm_swiglu_mixtral_T4096.md",
                 "algorithmic_bytes_per_launch": alg_bytes_up,
-                "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
+                "peak_source": peak_note,
                 "executed_tflops": round(fl_up_exe / (up_ms * 1e-3) / 1e12, 1),
                 "algorithmic_flops_per_launch": fl_up_alg, "launch_ms": round(up_ms, 4)}
 
@@ -412,8 +518,8 @@ def run_ours(args, rank: int, world: int):
         "gemm": {"executed_tflops": round(gemm_exec_tflops, 1), "algorithmic_tflops": round(gemm_alg_tflops, 1),
                  "executed_frac_of_peak": round(gemm_exec_tflops / peak_tc, 4),
                  "algorithmic_frac_of_peak": round(gemm_alg_tflops / peak_tc, 4),
-                 "executed_frac_of_burst_peak": round(gemm_exec_tflops / peaks["bf16_tflops"], 4),
-                 "peak_tflops": peak_tc, "peak_source": peaks_src, "up_ms": round(up_ms, 4),
+                 "executed_frac_of_sustained_peak": round(gemm_exec_tflops / peaks["bf16_tflops_sustained"], 4),
+                 "peak_tflops": peak_tc, "peak_source": peak_note, "up_ms": round(up_ms, 4),
                  "down_ms": round(down_ms, 4), "down_kernel": "gemm_pair_kernel<2> (CTA pairs)" if pair_down
                  else "gemm_kernel<2>", "padded_rows": P, "compact_rows": PC,
                  "executed_rows_up": exec_rows_up, "executed_rows_down": exec_rows, "work_items_up": items_up,
