@@ -652,15 +652,27 @@ __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, 
 }
 
 // Pair tile t -> this CTA's band(s) (MODE 2). tab lists the experts in schedule order (first
-// down-projection item, items); the expert's items in pairs, all nN tiles of a pair item together;
-// rank r takes item 2 * pair + r (mA = mB = -1: none, with the expert of rank 0's item).
+// down-projection item, items); the expert's items in pairs, all nN tiles of a pair item together
+// (band first), or with n_outer one N tile of all the expert's pair items after another, except
+// for the last expert, whose bands then still complete one after another while its tiles run; rank
+// r takes item 2 * pair + r (mA = mB = -1: none, with the expert of rank 0's item).
 __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E, int nN, const int32_t* items,
-                                                    const int32_t* tiles, const int32_t* crow, uint32_t rank) {
+                                                    const int32_t* tiles, const int32_t* crow, uint32_t rank,
+                                                    bool n_outer) {
     const int* cum = tab;
     const int* first = tab + (E + 1);
     const int* count = first + E;
     const int r = tab_segment(cum, E, t), local = t - cum[r];
-    const int pi = local / nN, n = local - pi * nN, it = 2 * pi + (int)rank;
+    int pi, n;
+    if (n_outer && cum[r + 1] != cum[E]) {  // the last expert's tiles stay band first
+        const int np = (count[r] + 1) >> 1;  // >= 1: an expert without items owns no tile
+        n = local / np;
+        pi = local - n * np;
+    } else {
+        pi = local / nN;
+        n = local - pi * nN;
+    }
+    const int it = 2 * pi + (int)rank;
     if (it >= count[r]) {
         TileRef x;
         x.mA = x.mB = -1;
@@ -811,7 +823,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 if (t < 0 || t >= total) break;
                 const TileRef tr = (MODE == 1)
                                        ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
-                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank);
+                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank,
+                                                          s.down_n_outer != 0);
                 const bool halves = MODE == 2 && tr.mB >= 0 && tr.mB != tr.mA;  // two 64-row boxes
                 const int brow = (MODE == 1) ? tr.n * BN1 : tr.n * 2 * BN1 + (int)rank * BN1;
                 const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
@@ -959,7 +972,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 if (t < 0) break;
                 const TileRef tr = (MODE == 1)
                                        ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
-                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank);
+                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank,
+                                                          s.down_n_outer != 0);
                 if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
                     if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 16 + (int)rank);
                     if (lane == 0) pair_abort(sm, rank);

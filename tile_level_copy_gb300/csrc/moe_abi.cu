@@ -147,6 +147,10 @@ int make_layout(const moe_config* c, Layout* out) {
     S.rows_per_unit_tail = (int)rpu_tail;
     S.units_per_band_tail = (int)((tbM + rpu_tail - 1) / rpu_tail);
     S.tail_bands = (TAIL_TILES + nN2 - 1) / nN2;
+    // An expert's W2 of at least half the L2 (128 MB) is streamed from DRAM again by each wave its
+    // band-first tiles span; N tile by N tile, each W2 tile is read by pair items that run together.
+    // Smaller W2 stay in L2 across waves, and there band-first order keeps each item's rows hot.
+    S.down_n_outer = (d * F * 2 >= (int64_t(64) << 20)) ? 1 : 0;
     S.timeout_ns = (unsigned long long)(c->timeout_us ? c->timeout_us : 2000000u) * 1000ull;
     S.flags = c->flags;
     *out = o;

@@ -128,6 +128,7 @@ struct Shape {
     int rows_per_unit, units_per_band;           // copy units of the leading bands
     int rows_per_unit_tail, units_per_band_tail;  // ... and of the last tail_bands bands
     int tail_bands;
+    int down_n_outer;               // pair down-projection: an expert's tiles N tile by N tile
     unsigned long long timeout_ns;
     uint32_t flags;
 };
