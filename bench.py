@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu capture summarised in profiles/gemm_swiglu_mixtral_T4096.md, per (workload, CTA-pair kernel),
 # with the SHA-256 of the kernel sources it was taken on: the bench reports it only while those
 # sources are unchanged and the launch configuration is the captured one.
-SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 1953557248 + 245744896,
-                                      "sources_sha256": "79d66df112f126aa648a24c0e9db837e5becb11dca31a40ea41569ec4cf9403d"}}
+SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 1953026304 + 247258624,
+                                      "sources_sha256": "7fb52c52e52cc32b497a4c9e6fceb7882867df2662ba32f7fe17b5b7c18b4a6b"}}
 KERNEL_SOURCES = ("tile_level_copy_gb300/csrc/gemm.cu", "tile_level_copy_gb300/csrc/moe_internal.cuh",
                   "tile_level_copy_gb300/csrc/copy_ring.cuh")
 
