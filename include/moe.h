@@ -187,8 +187,9 @@ MOE_API int moe_plan(const moe_config* cfg, const float* logits, const uint16_t*
  * Steps on `stream`: route, plan, permute, SwiGLU grouped GEMM over all experts (one persistent
  * launch), then one persistent launch in which all but consumer_ctas CTAs run the down-projection
  * GEMM, tiles handed out expert by expert in remote-first order (on CTA pairs, where one expert's W2
- * is at least 64 MB, an expert's tiles go N tile by N tile over its bands, the last expert's band by
- * band), and release a flag per finished tile while the last consumer_ctas CTAs acquire the flags
+ * is at least 64 MB and its rows of the hidden activations at most 64 MB, the expert's tiles go N
+ * tile by N tile over its bands, the last expert's band by band), and release a flag per finished
+ * tile while the last consumer_ctas CTAs acquire the flags
  * and copy each ready segment of row bands into its owner's slice of Ret, then the weighted top-k
  * combine. Flags: MOE_TAIL_ASSIST (producers that finished join the copy),
  * MOE_COPY_WARPS (copy engines also inside every producer CTA; consumer_ctas may be 0),

@@ -653,18 +653,19 @@ __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, 
 
 // Pair tile t -> this CTA's band(s) (MODE 2). tab lists the experts in schedule order (first
 // down-projection item, items); the expert's items in pairs, all nN tiles of a pair item together
-// (band first), or with n_outer one N tile of all the expert's pair items after another, except
-// for the last expert, whose bands then still complete one after another while its tiles run; rank
-// r takes item 2 * pair + r (mA = mB = -1: none, with the expert of rank 0's item).
+// (band first), or, for an expert of at most n_outer_items items, one N tile of all its pair items
+// after another, except for the last expert, whose bands then still complete one after another
+// while its tiles run; rank r takes item 2 * pair + r (mA = mB = -1: none, with the expert of rank
+// 0's item).
 __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E, int nN, const int32_t* items,
                                                     const int32_t* tiles, const int32_t* crow, uint32_t rank,
-                                                    bool n_outer) {
+                                                    int n_outer_items) {
     const int* cum = tab;
     const int* first = tab + (E + 1);
     const int* count = first + E;
     const int r = tab_segment(cum, E, t), local = t - cum[r];
     int pi, n;
-    if (n_outer && cum[r + 1] != cum[E]) {  // the last expert's tiles stay band first
+    if (count[r] <= n_outer_items && cum[r + 1] != cum[E]) {  // the last expert's tiles stay band first
         const int np = (count[r] + 1) >> 1;  // >= 1: an expert without items owns no tile
         n = local / np;
         pi = local - n * np;
@@ -824,7 +825,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 const TileRef tr = (MODE == 1)
                                        ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
                                        : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank,
-                                                          s.down_n_outer != 0);
+                                                          s.down_n_outer_items);
                 const bool halves = MODE == 2 && tr.mB >= 0 && tr.mB != tr.mA;  // two 64-row boxes
                 const int brow = (MODE == 1) ? tr.n * BN1 : tr.n * 2 * BN1 + (int)rank * BN1;
                 const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
@@ -973,7 +974,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 const TileRef tr = (MODE == 1)
                                        ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
                                        : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank,
-                                                          s.down_n_outer != 0);
+                                                          s.down_n_outer_items);
                 if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
                     if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 16 + (int)rank);
                     if (lane == 0) pair_abort(sm, rank);

@@ -148,9 +148,12 @@ int make_layout(const moe_config* c, Layout* out) {
     S.units_per_band_tail = (int)((tbM + rpu_tail - 1) / rpu_tail);
     S.tail_bands = (TAIL_TILES + nN2 - 1) / nN2;
     // An expert's W2 of at least half the L2 (128 MB) is streamed from DRAM again by each wave its
-    // band-first tiles span; N tile by N tile, each W2 tile is read by pair items that run together.
-    // Smaller W2 stay in L2 across waves, and there band-first order keeps each item's rows hot.
-    S.down_n_outer = (d * F * 2 >= (int64_t(64) << 20)) ? 1 : 0;
+    // band-first tiles span; N tile by N tile, each W2 tile is read by pair items that run together,
+    // but each item's rows are read once per N tile, so that order is taken only by experts whose
+    // rows (items x 128 x ffn x 2 bytes) fit in half the L2 as well. Smaller W2 stay in L2 across
+    // waves, and there band-first order keeps each item's rows hot.
+    const int64_t half_l2 = int64_t(64) << 20;
+    S.down_n_outer_items = (d * F * 2 >= half_l2) ? (int)(half_l2 / (int64_t(BM) * F * 2)) : 0;
     S.timeout_ns = (unsigned long long)(c->timeout_us ? c->timeout_us : 2000000u) * 1000ull;
     S.flags = c->flags;
     *out = o;

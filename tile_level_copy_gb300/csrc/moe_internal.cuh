@@ -128,7 +128,8 @@ struct Shape {
     int rows_per_unit, units_per_band;           // copy units of the leading bands
     int rows_per_unit_tail, units_per_band_tail;  // ... and of the last tail_bands bands
     int tail_bands;
-    int down_n_outer;               // pair down-projection: an expert's tiles N tile by N tile
+    int down_n_outer_items;         // pair down-projection: experts of at most this many items
+                                    // take their tiles N tile by N tile (0: none)
     unsigned long long timeout_ns;
     uint32_t flags;
 };
