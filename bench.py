@@ -191,9 +191,10 @@ class Nvml:
         self.lib.nvmlShutdown()
 
 
-# NVML clock event reason bits (nvml.h) reported by name
-REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
-               0x80: "hw_power_brake_slowdown"}
+# NVML clock event reason bits (nvml.h) reported by name (0x1, GPU idle, is not a limit)
+REASON_BITS = {0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x10: "sync_boost",
+               0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
 
 
 class ClockSampler:
@@ -289,6 +290,7 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(s[0] for s in self.samples),
                 "sm_max_mhz": max(s[1] for s in self.samples),
                 "sm_mhz_min": min(s[0] for s in self.samples),
+                "sm_mhz_distinct": len({s[0] for s in self.samples}),
                 "power_w_max": round(max(s[3] for s in self.samples), 1),
                 "reasons": reasons, "samples": len(self.samples), "source": self.source}
 

@@ -32,7 +32,13 @@ def test_reasons_are_named_by_their_nvml_bits():
         time.sleep(0.05)
     s = clk.summary()
     assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
-    assert s["sm_mhz_min"] == 1500.0
+    assert s["sm_mhz_min"] == 1500.0 and s["sm_mhz_distinct"] == 4
+
+
+def test_a_clock_lock_is_named():
+    with bench.ClockSampler(0, reader=fake_reader([(1200.0, 2070.0, 0x2, 500.0)])) as clk:
+        time.sleep(0.02)
+    assert clk.summary()["reasons"] == ["applications_clocks_setting"]
 
 
 def test_a_reader_that_fails_leaves_the_record_unsampled():
