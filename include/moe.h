@@ -67,6 +67,9 @@ extern "C" {
                                       /* is even and MOE_COPY_WARPS is not set                 */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
+#define MOE_TEST_PLAN_FAIL 0x200u     /* test hook: the plan kernel reports a failed bounds   */
+                                      /* check (MOE_ERR_PLAN, detail -3) although the plan is */
+                                      /* valid, to test that the status reaches the caller    */
 
 /*
  * Problem and knobs.
@@ -274,7 +277,8 @@ MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const f
  * moe_status: synchronises `stream`, then reads the device status word of the last call that used
  * `ws`. Returns MOE_OK, MOE_ERR_TIMEOUT (a flag or pipeline wait ran out; *detail = where) or
  * MOE_ERR_PLAN (a bounds check on plan indices failed). The word is cleared by the next call.
- * detail may be NULL.
+ * detail may be NULL. With ws == NULL it reads the status of the last moe_route_static call on the
+ * current device instead (cfg must be that call's config; it allocates nothing either).
  */
 MOE_API int moe_status(const moe_config* cfg, const void* ws, void* stream, int32_t* detail);
 
@@ -296,9 +300,13 @@ MOE_API int moe_device_info(int32_t* sm_count, int32_t* supported);
  * is a file-scope device array of MOE_STATIC_SCRATCH_BYTES that every GPU which loads the library
  * holds until the process exits. A config whose scratch would exceed that size returns MOE_ERR_ARG
  * with the needed size in moe_last_error(). The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress); make that first call before any stream capture. All calls share
- * the one array and each call overwrites what it reads: calls that can overlap on the GPU (two
- * streams, or two host threads) race and must be serialised by the caller.
+ * address (cudaGetSymbolAddress, once per CUDA context); make that first call before any stream
+ * capture. All calls share the one array and each call overwrites what it reads: calls that can
+ * overlap on the GPU (two streams, or two host threads) race and must be serialised by the caller.
+ * cfg->flags has no effect here (no token rows are moved, so MOE_PLAN_SKIP_PERMUTE changes nothing),
+ * except the test hook MOE_TEST_PLAN_FAIL. A plan entry that fails its device-side bounds check is
+ * reported by moe_status(cfg, NULL, stream, &detail), which reads this call's status words from the
+ * same array.
  */
 #define MOE_STATIC_SCRATCH_BYTES (4 << 20)
 MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t* topk_idx, float* topk_w,

@@ -93,3 +93,13 @@ def test_workspace_size_grows_with_tokens():
     cfg = cfg_of("mixtral")
     cfg.T = 8192
     assert tlc.workspace_size(cfg) > small
+
+
+def test_static_entry_point_rejects_null_pointers_without_a_gpu(built_library):
+    """moe_route_static checks its config and pointers before any CUDA call."""
+    c = cfg_of("tiny").to_c()
+    assert built_library.moe_route_static(ctypes.byref(c), None, None, None, None, None, None, None) == tlc.MOE_ERR_ARG
+    assert b"NULL" in built_library.moe_last_error()
+    c.R = 3  # T % R != 0
+    one = ctypes.c_void_p(16)
+    assert built_library.moe_route_static(ctypes.byref(c), one, one, one, one, one, one, None) == tlc.MOE_ERR_ARG

@@ -55,6 +55,43 @@ def test_static_scratch_plan_matches_workspace_plan_twice():
         for n in ("idx", "slot", "ret_slot", "offsets"):
             assert torch.equal(got[n], want[n]), n
         np.testing.assert_allclose(got["gate"].numpy(), want["gate"].numpy(), rtol=0, atol=0)
+        rc, detail = tlc.status(cfg, None)  # the static call's own status words
+        assert rc == tlc.MOE_OK, (rc, detail, tlc.lib().moe_last_error())
+
+
+def test_static_scratch_ignores_the_permute_flag():
+    """cfg.flags has no effect on the static entry point: with and without MOE_PLAN_SKIP_PERMUTE the
+    routing and row layout are the same, and equal to moe_plan's."""
+    w = inputs.WORKLOADS["skew"]
+    logits = torch.from_numpy(inputs.make_logits(w, 3)).cuda()
+    with_flag = via_static(tlc.Config.from_workload(w, flags=tlc.MOE_PLAN_SKIP_PERMUTE), logits)
+    cfg0 = tlc.Config.from_workload(w, flags=0)
+    without = via_static(cfg0, logits)
+    want = via_moe_plan(tlc.Config.from_workload(w, flags=tlc.MOE_PLAN_SKIP_PERMUTE), logits)
+    for n in ("idx", "gate", "slot", "ret_slot", "offsets"):
+        assert torch.equal(with_flag[n], without[n]), n
+        assert torch.equal(without[n], want[n]), n
+    assert tlc.status(cfg0, None)[0] == tlc.MOE_OK
+
+
+def test_static_scratch_reports_a_failed_plan_check():
+    """A plan that fails its device-side bounds check is reported to the caller of the static entry
+    point through moe_status(cfg, NULL): the test hook MOE_TEST_PLAN_FAIL makes the plan kernel report
+    one (detail -3); the next call without the hook clears it. The workspace path reports the same."""
+    w = inputs.WORKLOADS["fine"]
+    logits = torch.from_numpy(inputs.make_logits(w, 5)).cuda()
+    bad = tlc.Config.from_workload(w, flags=tlc.MOE_TEST_PLAN_FAIL)
+    via_static(bad, logits)
+    rc, detail = tlc.status(bad, None)
+    assert rc == tlc.MOE_ERR_PLAN and detail == -3
+    assert b"plan" in tlc.lib().moe_last_error()
+    good = tlc.Config.from_workload(w)
+    via_static(good, logits)
+    assert tlc.status(good, None) == (tlc.MOE_OK, 0)
+    bad_ws = tlc.Config.from_workload(w, flags=tlc.MOE_TEST_PLAN_FAIL | tlc.MOE_PLAN_SKIP_PERMUTE)
+    ws = tlc.Workspace(bad_ws)
+    tlc.plan(bad_ws, logits, None, ws)
+    assert tlc.status(bad_ws, ws) == (tlc.MOE_ERR_PLAN, -3)
 
 
 def test_static_scratch_rejects_configs_beyond_its_size():
@@ -65,3 +102,4 @@ def test_static_scratch_rejects_configs_beyond_its_size():
     rc = tlc.lib().moe_route_static(ctypes.byref(c), p, p, p, p, p, p, None)
     assert rc == tlc.MOE_ERR_ARG
     assert b"static scratch" in tlc.lib().moe_last_error()
+    assert tlc.status(cfg, None)[0] == tlc.MOE_ERR_ARG  # nor can its status be read

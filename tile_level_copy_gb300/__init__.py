@@ -29,6 +29,7 @@ MOE_TAIL_ASSIST = 0x2
 MOE_COPY_WARPS = 0x4
 MOE_PAIR_UMMA = 0x8
 MOE_TEST_STALL_CONSUMER = 0x100
+MOE_TEST_PLAN_FAIL = 0x200
 
 TRACE_GEMM2_START, TRACE_GEMM2_END, TRACE_COPY_START, TRACE_COPY_END = 0, 1, 2, 3
 TRACE_BAND_DONE, TRACE_LAST_ACQUIRE, TRACE_LAST_LOAD, TRACE_LAST_DRAIN = 4, 5, 6, 7
@@ -277,11 +278,12 @@ def copy_only(cfg: Config, ws: Workspace, ctas: int, stream=None) -> None:
     _check(lib().moe_copy_only(ctypes.byref(c), ws.ptr, ws.nbytes, int(ctas), _stream(stream)))
 
 
-def status(cfg: Config, ws: Workspace, stream=None):
-    """(return code, detail) of the last call on ws; synchronises the stream."""
+def status(cfg: Config, ws: Optional[Workspace], stream=None):
+    """(return code, detail) of the last call on ws (ws None: of the last moe_route_static call on this
+    device); synchronises the stream."""
     c = cfg.to_c()
     detail = ctypes.c_int32()
-    rc = lib().moe_status(ctypes.byref(c), ws.ptr, _stream(stream), ctypes.byref(detail))
+    rc = lib().moe_status(ctypes.byref(c), None if ws is None else ws.ptr, _stream(stream), ctypes.byref(detail))
     return rc, detail.value
 
 

@@ -358,30 +358,100 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
 // ---- static-scratch routing plan ------------------------------------------------------------------
 // Scratch of moe_route_static: one file-scope array per GPU that loads the library, kept until the
 // process exits. Host code must not pass `g_static_scratch` itself to a kernel (on the host the name
-// is only a stand-in); each device's address comes from cudaGetSymbolAddress below.
+// is only a stand-in); the device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES];
 
 namespace moe {
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mu;
-void* g_static_addr[kMaxDevices] = {};
+// Offsets of the plan's scratch regions inside the static array for one config (256-byte aligned).
+struct StaticLayout {
+    size_t rank, cnt, base, counts, ret, tiles, tret, sched, seg, exp, iu, id, meta, flags, bands, trace, cslot,
+        ccoff, tcrow, bytes;
+};
 
-// Device address of g_static_scratch on the current device (set up on the first call per device).
+StaticLayout static_layout(const Layout& lay) {
+    const moe_layout& L = lay.L;
+    const Shape& S = lay.S;
+    StaticLayout o{};
+    size_t cur = 0;
+    auto put = [&](size_t bytes) {
+        const size_t at = cur;
+        cur = align_up(cur + bytes, 256);
+        return at;
+    };
+    const size_t TK = (size_t)S.T * S.k, E = S.E, R = S.R, MT = L.MT_max;
+    o.rank = put(TK * 4);
+    o.cnt = put((size_t)L.n_chunks * E * 4);
+    o.base = put((size_t)L.n_chunks * E * 4);
+    o.counts = put(E * R * 4);
+    o.ret = put(R * (E + 1) * 4);
+    o.tiles = put(MT * 16);
+    o.tret = put(MT * 4);
+    o.sched = put(MT * 4);
+    o.seg = put(MT * 8);
+    o.exp = put(E * 32);
+    o.iu = put((size_t)L.IU_max * 8);
+    o.id = put(MT * 8);
+    o.meta = put(META_COUNT * 4);
+    o.flags = put(MT * (size_t)L.n_tiles_n2 * 4);
+    o.bands = put(MT * 4);
+    o.trace = put(TR_COUNT * 8);
+    o.cslot = put(TK * 4);
+    o.ccoff = put(E * R * 4);
+    o.tcrow = put(MT * 4);
+    o.bytes = cur;
+    return o;
+}
+
+// Device address of g_static_scratch in the current CUDA context. It is looked up once per context
+// (a context made after cudaDeviceReset loads the module again, at another address) and cached by
+// the context's process-unique id; without that id (an old driver) it is looked up on every call.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name, int version) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<Fn>(p);
+    return nullptr;
+}
+
+constexpr int kStaticCache = 64;
+std::mutex g_static_mu;
+unsigned long long g_static_ctx[kStaticCache] = {};
+void* g_static_addr[kStaticCache] = {};
+int g_static_used = 0;
+
 int static_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_DEVICE, "device index %d out of range", dev);
+    if (e == cudaSuccess) e = cudaSetDevice(dev);  // makes the device's primary context current
+    if (e != cudaSuccess) return cuda_fail(e, "selecting the current device");
+    static const CtxGetCurrentFn get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 12000);
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    const bool keyed = get_ctx && get_id && get_ctx(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS;
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
-        g_static_addr[dev] = p;
+    if (keyed)
+        for (int i = 0; i < g_static_used; ++i)
+            if (g_static_ctx[i] == id) {
+                *out = g_static_addr[i];
+                return MOE_OK;
+            }
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static scratch");
+    if (keyed && g_static_used < kStaticCache) {
+        g_static_ctx[g_static_used] = id;
+        g_static_addr[g_static_used] = p;
+        ++g_static_used;
     }
-    *out = g_static_addr[dev];
+    *out = p;
     return MOE_OK;
 }
 
@@ -643,13 +713,23 @@ MOE_API int moe_status(const moe_config* cfg, const void* ws, void* stream, int3
     Layout lay;
     int rc = make_layout(cfg, &lay);
     if (rc) return rc;
-    if (!ws) return fail(MOE_ERR_ARG, "workspace is NULL");
+    // ws == NULL: the status words of the last moe_route_static call, in the static scratch
+    const uint8_t* meta = nullptr;
+    if (ws) {
+        meta = static_cast<const uint8_t*>(ws) + lay.L.meta;
+    } else {
+        const StaticLayout o = static_layout(lay);
+        if (o.bytes > (size_t)MOE_STATIC_SCRATCH_BYTES)
+            return fail(MOE_ERR_ARG, "this config does not fit the static scratch (%zu bytes)", o.bytes);
+        void* base = nullptr;
+        if ((rc = static_scratch(&base))) return rc;
+        meta = static_cast<const uint8_t*>(base) + o.meta;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
     int32_t w[2] = {0, 0};
-    e = cudaMemcpy(w, static_cast<const uint8_t*>(ws) + lay.L.meta + META_STATUS * 4, sizeof(w),
-                   cudaMemcpyDeviceToHost);
+    e = cudaMemcpy(w, meta + META_STATUS * 4, sizeof(w), cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     if (detail) *detail = w[1];
     switch (w[0]) {
@@ -681,24 +761,9 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     if (rc) return rc;
     if (!logits || !topk_idx || !topk_w || !slot || !ret_slot || !offsets)
         return fail(MOE_ERR_ARG, "NULL input or output pointer");
-    const moe_layout& L = lay.L;
-    const Shape& S = lay.S;
-    // scratch regions, packed in the static array
-    size_t cur = 0;
-    auto put = [&](size_t bytes) {
-        const size_t at = cur;
-        cur = align_up(cur + bytes, 256);
-        return at;
-    };
-    const size_t TK = (size_t)S.T * S.k, E = S.E, R = S.R, MT = L.MT_max;
-    const size_t o_rank = put(TK * 4), o_cnt = put((size_t)L.n_chunks * E * 4),
-                 o_base = put((size_t)L.n_chunks * E * 4), o_counts = put(E * R * 4), o_ret = put(R * (E + 1) * 4),
-                 o_tiles = put(MT * 16), o_tret = put(MT * 4), o_sched = put(MT * 4), o_seg = put(MT * 8),
-                 o_exp = put(E * 32), o_iu = put((size_t)L.IU_max * 8), o_id = put(MT * 8), o_meta = put(META_COUNT * 4),
-                 o_flags = put(MT * (size_t)L.n_tiles_n2 * 4), o_bands = put(MT * 4), o_trace = put(TR_COUNT * 8),
-                 o_cslot = put(TK * 4), o_ccoff = put(E * R * 4), o_tcrow = put(MT * 4);
-    if (cur > (size_t)MOE_STATIC_SCRATCH_BYTES)
-        return fail(MOE_ERR_ARG, "this config needs %zu bytes of static scratch; the limit is %d", cur,
+    const StaticLayout o = static_layout(lay);
+    if (o.bytes > (size_t)MOE_STATIC_SCRATCH_BYTES)
+        return fail(MOE_ERR_ARG, "this config needs %zu bytes of static scratch; the limit is %d", o.bytes,
                     MOE_STATIC_SCRATCH_BYTES);
     DeviceInfo di;
     if ((rc = device_info(&di))) return rc;
@@ -709,32 +774,33 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     PlanPtrs p{};
     p.idx = topk_idx;
     p.gate = topk_w;
-    p.rank = reinterpret_cast<int32_t*>(b + o_rank);
-    p.chunk_cnt = reinterpret_cast<int32_t*>(b + o_cnt);
-    p.chunk_base = reinterpret_cast<int32_t*>(b + o_base);
-    p.counts = reinterpret_cast<int32_t*>(b + o_counts);
+    p.rank = reinterpret_cast<int32_t*>(b + o.rank);
+    p.chunk_cnt = reinterpret_cast<int32_t*>(b + o.cnt);
+    p.chunk_base = reinterpret_cast<int32_t*>(b + o.base);
+    p.counts = reinterpret_cast<int32_t*>(b + o.counts);
     p.offsets = offsets;
-    p.ret_off = reinterpret_cast<int32_t*>(b + o_ret);
-    p.tiles = reinterpret_cast<int32_t*>(b + o_tiles);
-    p.tile_ret = reinterpret_cast<int32_t*>(b + o_tret);
-    p.sched = reinterpret_cast<int32_t*>(b + o_sched);
-    p.seg = reinterpret_cast<int32_t*>(b + o_seg);
-    p.experts = reinterpret_cast<int32_t*>(b + o_exp);
-    p.items_up = reinterpret_cast<int32_t*>(b + o_iu);
-    p.items_down = reinterpret_cast<int32_t*>(b + o_id);
+    p.ret_off = reinterpret_cast<int32_t*>(b + o.ret);
+    p.tiles = reinterpret_cast<int32_t*>(b + o.tiles);
+    p.tile_ret = reinterpret_cast<int32_t*>(b + o.tret);
+    p.sched = reinterpret_cast<int32_t*>(b + o.sched);
+    p.seg = reinterpret_cast<int32_t*>(b + o.seg);
+    p.experts = reinterpret_cast<int32_t*>(b + o.exp);
+    p.items_up = reinterpret_cast<int32_t*>(b + o.iu);
+    p.items_down = reinterpret_cast<int32_t*>(b + o.id);
     p.slot = slot;
-    p.cslot = reinterpret_cast<int32_t*>(b + o_cslot);
+    p.cslot = reinterpret_cast<int32_t*>(b + o.cslot);
     p.ret_slot = ret_slot;
-    p.ccoff = reinterpret_cast<int32_t*>(b + o_ccoff);
-    p.tile_crow = reinterpret_cast<int32_t*>(b + o_tcrow);
-    p.meta = reinterpret_cast<int32_t*>(b + o_meta);
-    p.flags = reinterpret_cast<uint32_t*>(b + o_flags);
-    p.bands = reinterpret_cast<uint32_t*>(b + o_bands);
-    p.trace = reinterpret_cast<unsigned long long*>(b + o_trace);
+    p.ccoff = reinterpret_cast<int32_t*>(b + o.ccoff);
+    p.tile_crow = reinterpret_cast<int32_t*>(b + o.tcrow);
+    p.meta = reinterpret_cast<int32_t*>(b + o.meta);
+    p.flags = reinterpret_cast<uint32_t*>(b + o.flags);
+    p.bands = reinterpret_cast<uint32_t*>(b + o.bands);
+    p.trace = reinterpret_cast<unsigned long long*>(b + o.trace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_route(S, logits, p, st);
-    if (e == cudaSuccess) e = launch_plan(S, p, st);
-    if (e == cudaSuccess) e = launch_permute(S, nullptr, p, di.sms, st);
+    // the plan-only kernels: no token rows are moved (x = NULL), whatever cfg->flags says
+    cudaError_t e = launch_route(lay.S, logits, p, st);
+    if (e == cudaSuccess) e = launch_plan(lay.S, p, st);
+    if (e == cudaSuccess) e = launch_permute(lay.S, nullptr, p, di.sms, st);
     if (e != cudaSuccess) return cuda_fail(e, "static-scratch plan launch");
     return MOE_OK;
 }

@@ -516,9 +516,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         p.meta[META_QUEUE_SEQ] = 0;
         p.meta[META_TILES_UP] = 0;
         p.meta[META_TILES_DOWN] = 0;
-        const bool bad = P > s.P_max || PC > s.PC_max;
+        // MOE_TEST_PLAN_FAIL: report a failed check (detail -3) so that tests can see the status
+        // reach the caller; the plan itself is still complete and valid
+        const bool hook = (s.flags & MOE_TEST_PLAN_FAIL) != 0;
+        const bool bad = P > s.P_max || PC > s.PC_max || hook;
         p.meta[META_STATUS] = bad ? ST_BAD_PLAN : 0;
-        p.meta[META_STATUS_DETAIL] = bad ? (P > s.P_max ? P : PC) : 0;
+        p.meta[META_STATUS_DETAIL] = bad ? (hook ? -3 : P > s.P_max ? P : PC) : 0;
     }
     if (tid < TR_COUNT) p.trace[tid] = (tid == MOE_TRACE_GEMM2_START || tid == MOE_TRACE_COPY_START) ? ~0ull : 0ull;
     const int nflags = min(MT, s.MT_max) * s.n_tiles_n2;
