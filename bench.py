@@ -15,6 +15,7 @@ so N GPUs run N independent replicas (weak scaling), timed between barriers, max
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -35,10 +36,10 @@ from tile_level_copy_gb300 import inputs  # noqa: E402
 METRIC = "MoE-layer tokens/s; grouped-GEMM % of BF16 peak; return-copy overlap %"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes per launch of the SwiGLU GEMM (dram__bytes_read.sum + dram__bytes_write.sum) from the
-# ncu capture summarised in profiles/gemm_swiglu_mixtral_T4096.md, per (workload, CTA-pair kernel),
-# with the SHA-256 of the kernel sources it was taken on: the bench reports it only while those
-# sources are unchanged and the launch configuration is the captured one.
+# DRAM bytes per launch of the SwiGLU GEMM (dram__bytes_read.sum + dram__bytes_write.sum) from an
+# ncu capture of one launch on the Mixtral-shaped layer, per (workload, CTA-pair kernel), with the
+# SHA-256 of the kernel sources it was taken on: the bench reports it only while those sources are
+# unchanged and the launch configuration is the captured one.
 SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 1954745600 + 246188032,
                                       "sources_sha256": "cd7392f0a7f61bc7fafbf5b7207dcefca60707d72d31b2e4faef569980d75f0a"}}
 KERNEL_SOURCES = ("tile_level_copy_gb300/csrc/gemm.cu", "tile_level_copy_gb300/csrc/moe_internal.cuh",
@@ -82,6 +83,13 @@ def parse_args():
     ap.add_argument("--pair-umma", action=argparse.BooleanOptionalAction, default=True,
                     help="SwiGLU GEMM on CTA pairs (UMMA 256 x 256 over two SMs; the default, the fastest "
                          "measured on every workload)")
+    ap.add_argument("--direct-tail", action=argparse.BooleanOptionalAction, default=True,
+                    help="the down-projection's epilogue returns the last wave's bands itself (default); the "
+                         "layer without it is timed beside in the same alternation")
+    ap.add_argument("--tail-window", type=int, default=0,
+                    help="tile hand-out positions of the direct tail (0: one wave)")
+    ap.add_argument("--workloads", nargs="*", default=["skew", "fine"], choices=sorted(inputs.WORKLOADS),
+                    help="other workloads given a compact line in the default run (none: --workloads)")
     ap.add_argument("--graph", action=argparse.BooleanOptionalAction, default=True,
                     help="time the steps as replays of a CUDA graph of one step (default); the eager "
                          "launches are timed too and reported beside")
@@ -89,7 +97,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu DRAM bytes per launch of the SwiGLU GEMM (from profiles/), for the roofline")
+                    help="ncu DRAM bytes per launch of the SwiGLU GEMM, for the roofline")
     return ap.parse_args()
 
 
@@ -296,6 +304,121 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------- our arm
+def default_flags(copy_warps: bool, direct_tail: bool = True, tail_assist: bool = True, pair: bool = True) -> int:
+    """The bench's launch configuration: both expert GEMMs on CTA pairs, finished producers joining
+    the copy, the last wave's bands returned by the down-projection's epilogue, and (per workload)
+    the producers' copy warps."""
+    import tile_level_copy_gb300 as tlc
+    return ((tlc.MOE_TAIL_ASSIST if tail_assist else 0) | (tlc.MOE_COPY_WARPS if copy_warps else 0) |
+            (tlc.MOE_PAIR_UMMA if pair else 0) | (tlc.MOE_DIRECT_TAIL if direct_tail else 0))
+
+
+class LayerBench:
+    """One workload's inputs, weights, workspace and output on the device, and the ways to run it."""
+
+    def __init__(self, w, seed: int, dev):
+        import tile_level_copy_gb300 as tlc
+        self.tlc, self.w, self.dev = tlc, w, dev
+        self.logits_np = inputs.make_logits(w, seed)
+        self.x_cpu = inputs.make_x(w, seed)
+        self.logits, self.x = torch.from_numpy(self.logits_np).to(dev), self.x_cpu.to(dev)
+        self.W = {}
+        for n in ("W1", "W3", "W2"):
+            shape = (w.E, w.ffn, w.d) if n != "W2" else (w.E, w.d, w.ffn)
+            self.W[n] = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+            inputs.make_weight_into(w, seed, n, self.W[n])
+        self.ws = tlc.Workspace(tlc.Config.from_workload(w), dev)  # the layout depends on the shape only
+        self.out = torch.empty(w.T, w.d, dtype=torch.float32, device=dev)
+
+    def step(self, cfg, seq: bool, events=None):
+        self.tlc.forward(cfg, self.logits, self.x, self.W["W1"], self.W["W3"], self.W["W2"], self.out, self.ws,
+                         sequential=seq, events=events)
+
+    def check(self, cfg, where: str):
+        rc, detail = self.tlc.status(cfg, self.ws)
+        if rc != self.tlc.MOE_OK:
+            raise RuntimeError(f"device status {rc} ({detail}) {where}: {self.tlc.lib().moe_last_error().decode()}")
+
+    def graph(self, cfg, seq: bool):
+        """One step captured as a CUDA graph (after two eager steps on a side stream)."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                self.step(cfg, seq)
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(cfg, seq)
+        return g
+
+    def tails(self, cfg, reps: int):
+        """Copy tail after the last flag (ms) and the tail's trace marks (us) of `reps` overlapped steps."""
+        tails, marks = [], []
+        tlc = self.tlc
+        for _ in range(reps):
+            self.step(cfg, False)
+            torch.cuda.synchronize()
+            tr = self.ws.view("trace").cpu().numpy().astype(np.int64)
+            tails.append(max(0, int(tr[tlc.TRACE_COPY_END]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e6)
+            marks.append([(int(tr[i]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e3 for i in
+                          (tlc.TRACE_BAND_DONE, tlc.TRACE_LAST_ACQUIRE, tlc.TRACE_LAST_LOAD, tlc.TRACE_LAST_DRAIN,
+                           tlc.TRACE_COPY_END)])
+        self.check(cfg, "in the trace steps")
+        return tails, marks
+
+
+STAGES = ("route_plan_permute", "swiglu_gemm", "down_gemm", "copy", "combine")
+
+
+def alternate_eager(lb: LayerBench, arms, K: int, Wm: int):
+    """Eager steps of every arm, interleaved step by step (A B C A B C ...), each with stage events.
+    Returns {arm: array [K, 5] of stage ms}."""
+    tlc = lb.tlc
+    for _ in range(Wm):
+        for cfg, seq in arms.values():
+            lb.step(cfg, seq)
+    evs = {a: [tlc.stage_events() for _ in range(K)] for a in arms}
+    torch.cuda.synchronize()
+    for i in range(K):
+        for a, (cfg, seq) in arms.items():
+            lb.step(cfg, seq, evs[a][i])
+    torch.cuda.synchronize()
+    for a, (cfg, _) in arms.items():
+        lb.check(cfg, f"in the alternating eager steps ({a})")
+    return {a: np.array([[e[j].elapsed_time(e[j + 1]) for j in range(tlc.EV_COUNT - 1)] for e in evs[a]])
+            for a in arms}
+
+
+def alternate_graphs(lb: LayerBench, arms, K: int, Wm: int, dev_index: int):
+    """CUDA-graph replays of every arm interleaved replay by replay, each replay between two events on
+    the replaying stream. Returns ({arm: [K] ms}, clock summary of the whole interleaved region)."""
+    graphs = {a: lb.graph(cfg, seq) for a, (cfg, seq) in arms.items()}
+    for _ in range(Wm):
+        for g in graphs.values():
+            g.replay()
+    ev = {a: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+          for a in arms}
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        for i in range(K):
+            for a, g in graphs.items():
+                ev[a][i][0].record()
+                g.replay()
+                ev[a][i][1].record()
+        torch.cuda.synchronize()
+    for a, (cfg, _) in arms.items():
+        lb.check(cfg, f"in the alternating graph replays ({a})")
+    return {a: np.array([e0.elapsed_time(e1) for e0, e1 in ev[a]]) for a in arms}, clk.summary()
+
+
+def spread_ms(x) -> float:
+    """Step-to-step spread of a series of step times: 1.4826 x median absolute deviation (about one
+    standard deviation for normal noise, robust to outliers)."""
+    x = np.asarray(x, float)
+    return float(1.4826 * np.median(np.abs(x - np.median(x))))
+
+
 def run_ours(args, rank: int, world: int):
     import tile_level_copy_gb300 as tlc
     from tile_level_copy_gb300 import build as tlc_build
@@ -309,129 +432,98 @@ def run_ours(args, rank: int, world: int):
     if args.copy_warps is None:
         args.copy_warps = dw
     seed = args.seed + rank
-    flags = (0 if args.no_tail_assist else tlc.MOE_TAIL_ASSIST) | (tlc.MOE_COPY_WARPS if args.copy_warps else 0) | \
-        (tlc.MOE_PAIR_UMMA if args.pair_umma else 0)
-    cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags)
+    flags = default_flags(args.copy_warps, direct_tail=args.direct_tail, tail_assist=not args.no_tail_assist,
+                          pair=args.pair_umma)
+    cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags,
+                                   tail_window=args.tail_window)
     peaks, peaks_src = load_peaks()
-
-    logits_np = inputs.make_logits(w, seed)
-    x_cpu = inputs.make_x(w, seed)
-    logits, x = torch.from_numpy(logits_np).to(dev), x_cpu.to(dev)
-    W = {}
-    for n in ("W1", "W3", "W2"):
-        shape = (w.E, w.ffn, w.d) if n != "W2" else (w.E, w.d, w.ffn)
-        W[n] = torch.empty(shape, dtype=torch.bfloat16, device=dev)
-        inputs.make_weight_into(w, seed, n, W[n])
-    ws = tlc.Workspace(cfg, dev)
-    out = torch.empty(w.T, w.d, dtype=torch.float32, device=dev)
+    lb = LayerBench(w, seed, dev)
     K, Wm = args.steps, args.warmup
 
-    def step(seq, events=None):
-        tlc.forward(cfg, logits, x, W["W1"], W["W3"], W["W2"], out, ws, sequential=seq, events=events)
-
-    def timed(seq):
-        evs = [tlc.stage_events() for _ in range(K)]
-        for _ in range(Wm):
-            step(seq)
-        rc, detail = tlc.status(cfg, ws)
-        if rc != tlc.MOE_OK:
-            raise RuntimeError(f"device status {rc} ({detail}): {tlc.lib().moe_last_error().decode()}")
-        barrier(world)
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with ClockSampler(dev.index) as clk:
-            t0.record()
-            for i in range(K):
-                step(seq, evs[i])
-            t1.record()
-            torch.cuda.synchronize()
-        barrier(world)
-        rc, detail = tlc.status(cfg, ws)
-        if rc != tlc.MOE_OK:
-            raise RuntimeError(f"device status {rc} ({detail}) in the timed region")
-        stages = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(tlc.EV_COUNT - 1)] for e in evs])
-        return t0.elapsed_time(t1) / 1e3, stages, clk.summary()
-
-    def timed_graph(seq):
-        # one step captured as a CUDA graph (the launches and their dependencies recorded once) and
-        # replayed K times: the serving form of a fixed-shape layer
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            for _ in range(2):
-                step(seq)
-        torch.cuda.current_stream().wait_stream(side)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step(seq)
-        for _ in range(Wm):
-            graph.replay()
-        rc, detail = tlc.status(cfg, ws)
-        if rc != tlc.MOE_OK:
-            raise RuntimeError(f"device status {rc} ({detail}) in the graph warm-up")
-        barrier(world)
-        torch.cuda.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with ClockSampler(dev.index) as clk:
-            t0.record()
-            for _ in range(K):
-                graph.replay()
-            t1.record()
-            torch.cuda.synchronize()
-        barrier(world)
-        rc, detail = tlc.status(cfg, ws)
-        if rc != tlc.MOE_OK:
-            raise RuntimeError(f"device status {rc} ({detail}) in the timed graph replays")
-        return t0.elapsed_time(t1) / 1e3, clk.summary()
-
-    sec_ovl_eager, st_ovl, clocks_eager = timed(False)
-    sec_seq_eager, st_seq, clocks_seq_eager = timed(True)
+    # ---- headline: K contiguous steps of the overlapped layer (CUDA-graph replays, or eager launches)
     if args.graph:
-        sec_ovl, clocks = timed_graph(False)
-        sec_seq, clocks_seq = timed_graph(True)
+        g = lb.graph(cfg, False)
+        for _ in range(Wm):
+            g.replay()
+        lb.check(cfg, "in the graph warm-up")
+        run_k = lambda: [g.replay() for _ in range(K)]  # noqa: E731
     else:
-        sec_ovl, clocks, sec_seq, clocks_seq = sec_ovl_eager, clocks_eager, sec_seq_eager, clocks_seq_eager
-    value, sec_max = aggregate(sec_ovl, w.T * K, world)
-    seq_value, _ = aggregate(sec_seq, w.T * K, world)
-    eager_value, eager_sec_max = aggregate(sec_ovl_eager, w.T * K, world)
-
-    # overlap from %globaltimer stamps of a few extra overlapped steps
-    hidden, tails, marks = [], [], []
-    copy_alone_ms = float(np.median(st_seq[:, tlc.EV_DOWN]))
-    for _ in range(5):
-        step(False)
+        for _ in range(Wm):
+            lb.step(cfg, False)
+        lb.check(cfg, "in the warm-up")
+        run_k = lambda: [lb.step(cfg, False) for _ in range(K)]  # noqa: E731
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        t0.record()
+        run_k()
+        t1.record()
         torch.cuda.synchronize()
-        tr = ws.view("trace").cpu().numpy().astype(np.int64)
-        tail_ms = max(0, int(tr[tlc.TRACE_COPY_END]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e6
-        tails.append(tail_ms)
-        hidden.append(1.0 - tail_ms / copy_alone_ms)
-        marks.append([(int(tr[i]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e3 for i in
-                      (tlc.TRACE_BAND_DONE, tlc.TRACE_LAST_ACQUIRE, tlc.TRACE_LAST_LOAD, tlc.TRACE_LAST_DRAIN,
-                       tlc.TRACE_COPY_END)])
-    ms_ovl, ms_seq = sec_ovl * 1e3 / K, sec_seq * 1e3 / K
+    barrier(world)
+    lb.check(cfg, "in the timed region")
+    sec_ovl = t0.elapsed_time(t1) / 1e3
+    clocks = clk.summary()
+    value, sec_max = aggregate(sec_ovl, w.T * K, world)
 
-    # the page's own copy design beside it: a dedicated consumer partition of 8 CTAs (no copy warps),
-    # same GEMMs; its hidden fraction (trace stamps) and eager step time
-    cfg_page = tlc.Config.from_workload(w, consumer_ctas=8, mgb=args.mgb,
-                                        flags=(cfg.flags & ~tlc.MOE_COPY_WARPS) | tlc.MOE_TAIL_ASSIST)
-    page_tails = []
-    for _ in range(3):
-        tlc.forward(cfg_page, logits, x, W["W1"], W["W3"], W["W2"], out, ws)
+    # ---- the arms compared in alternation: overlapped, GEMM-then-copy, and (with the direct tail)
+    # the overlapped layer without it, i.e. every band through the consumer
+    arms = {"overlapped": (cfg, False), "sequential": (cfg, True)}
+    direct = bool(cfg.flags & tlc.MOE_DIRECT_TAIL)
+    if direct:
+        arms["overlapped_all_bands_copied"] = (dataclasses.replace(cfg, flags=cfg.flags & ~tlc.MOE_DIRECT_TAIL), False)
+    st = alternate_eager(lb, arms, K, Wm)
+    rep, clocks_alt = alternate_graphs(lb, arms, K, Wm, dev.index) if args.graph else (
+        {a: st[a].sum(1) for a in arms}, None)
+    med = {a: float(np.median(rep[a])) for a in arms}
+    eager_ms = {a: float(np.median(st[a].sum(1))) for a in arms}
+    stage_med = {a: {n: float(np.median(st[a][:, i])) for i, n in enumerate(STAGES)} for a in arms}
+    copy_alone_ms = stage_med["sequential"]["copy"]
+
+    # overlap from %globaltimer stamps of a few more overlapped steps of each overlapped arm
+    trace = {}
+    for _ in range(2):  # alternating, 3 steps per arm per round
+        for a in [x for x in arms if x != "sequential"]:
+            t_, m_ = lb.tails(arms[a][0], 3)
+            trace.setdefault(a, ([], []))
+            trace[a][0].extend(t_)
+            trace[a][1].extend(m_)
+
+    def hidden_of(a):
+        tails, marks = trace[a]
+        return {"hidden_pct": round(100 * (1 - statistics.median(tails) / copy_alone_ms), 2),
+                "tail_ms": round(statistics.median(tails), 4),
+                "tail_marks_us": dict(zip(["band_done", "last_acquire", "last_load", "last_drain", "copy_end"],
+                                          [round(float(v), 2) for v in np.median(np.array(marks), 0)]))}
+
+    ms_ovl, ms_seq = med["overlapped"], med["sequential"]
+    spread = max(spread_ms(rep["overlapped"]), spread_ms(rep["sequential"]))
+    wall = None
+    wall_note = (f"|T_seq - T_ovl| = {abs(ms_seq - ms_ovl) * 1e3:.1f} us is within the step-to-step spread "
+                 f"({spread * 1e3:.1f} us): no wall overlap is claimed")
+    if abs(ms_seq - ms_ovl) > spread:
+        wall = round(100 * (ms_seq - ms_ovl) / copy_alone_ms, 2)
+        wall_note = f"above the step-to-step spread ({spread * 1e3:.1f} us)"
+    swiglu_ratio = stage_med["sequential"]["swiglu_gemm"] / stage_med["overlapped"]["swiglu_gemm"]
+
+    # the page's own copy design beside it: a dedicated consumer partition of 8 CTAs (no copy warps,
+    # no direct tail), same GEMMs; its hidden fraction (trace stamps) and eager step time
+    cfg_page = dataclasses.replace(cfg, consumer_ctas=8,
+                                   flags=(cfg.flags & ~(tlc.MOE_COPY_WARPS | tlc.MOE_DIRECT_TAIL)) |
+                                   tlc.MOE_TAIL_ASSIST)
+    page_tails, _ = lb.tails(cfg_page, 5)
     page_ev = [tlc.stage_events() for _ in range(5)]
     for i in range(5):
-        tlc.forward(cfg_page, logits, x, W["W1"], W["W3"], W["W2"], out, ws, events=page_ev[i])
-        torch.cuda.synchronize()
-        tr = ws.view("trace").cpu().numpy().astype(np.int64)
-        page_tails.append(max(0, int(tr[tlc.TRACE_COPY_END]) - int(tr[tlc.TRACE_GEMM2_END])) / 1e6)
-    rc, detail = tlc.status(cfg_page, ws)
-    if rc != tlc.MOE_OK:
-        raise RuntimeError(f"device status {rc} ({detail}) in the dedicated-partition steps")
+        lb.step(cfg_page, False, page_ev[i])
+    torch.cuda.synchronize()
+    lb.check(cfg_page, "in the dedicated-partition steps")
     page_ms = float(np.median([e[tlc.EV_BEGIN].elapsed_time(e[tlc.EV_END]) for e in page_ev]))
 
     # GEMM numbers: real rows = T*k; executed rows = 128 per work item: SwiGLU items are 128 rows of
     # one expert in the compact layout (with CTA pairs, an expert's odd item also occupies the idle
     # half of its pair), down-projection items a band or two bands that need at most 64 rows each;
     # P = padded rows of the owner-aligned layout, PC = rows of the compact layout
+    ws = lb.ws
     meta = ws.view("meta").cpu()
     P, items, items_up, PC = (int(meta[i].item()) for i in (0, 7, 8, 9))
     TK = w.T * w.topk
@@ -450,17 +542,16 @@ def run_ours(args, rank: int, world: int):
         exec_rows = 128 * int(np.sum(2 * ((cnt + 1) // 2)))
     else:
         exec_rows = 128 * items
-    up_ms = float(np.median(st_ovl[:, tlc.EV_PLANNED]))
-    down_ms = float(np.median(st_seq[:, tlc.EV_UP]))
+    up_ms = stage_med["overlapped"]["swiglu_gemm"]
+    down_ms = stage_med["sequential"]["down_gemm"]
     fl_up_alg, fl_down_alg = 4.0 * TK * w.d * w.ffn, 2.0 * TK * w.d * w.ffn
     fl_up_exe, fl_down_exe = 4.0 * exec_rows_up * w.d * w.ffn, 2.0 * exec_rows * w.d * w.ffn
     gemm_exec_tflops = (fl_up_exe + fl_down_exe) / ((up_ms + down_ms) * 1e-3) / 1e12
     gemm_alg_tflops = (fl_up_alg + fl_down_alg) / ((up_ms + down_ms) * 1e-3) / 1e12
-    # The SwiGLU launch time comes from the eager timed region. The measured sustained rate is a
-    # seconds-long GEMM loop under the power limit; a timed region shorter than a second runs
-    # before the power limiter pulls the clock down (the clock record shows it), so it is held to
-    # the burst rate instead.
-    eager_region_s = sec_ovl_eager
+    # The SwiGLU launch time comes from the alternating eager steps. The measured sustained rate is a
+    # seconds-long GEMM loop under the power limit; a region shorter than a second runs before the
+    # power limiter pulls the clock down (the clock record shows it), so it is held to the burst rate.
+    eager_region_s = sum(float(st[a].sum()) for a in arms) / 1e3
     if eager_region_s >= 1.0:
         peak_tc, peak_kind = peaks["bf16_tflops_sustained"], "bf16_tflops_sustained"
     else:
@@ -470,13 +561,16 @@ def run_ours(args, rank: int, world: int):
     roof_achieved = fl_up_alg / (up_ms * 1e-3) / 1e12
     # algorithmic DRAM bytes of the SwiGLU GEMM: W1 and W3 once, the compact rows in, the hidden out
     alg_bytes_up = 2 * w.E * w.ffn * w.d * 2 + PC * w.d * 2 + PC * w.ffn * 2
+    traffic = args.traffic if args.traffic is not None else captured_traffic(args.workload, args.pair_umma)
     roofline = {"kernel": ("gemm_pair_kernel<1> (SwiGLU up-projection, CTA pairs)" if args.pair_umma
                            else "gemm_kernel<1> (SwiGLU up-projection)"), "bound": "tensor",
                 "achieved": round(roof_achieved, 1), "peak": peak_tc, "unit": "TFLOP/s",
                 "frac": round(roof_achieved / peak_tc, 4),
-                "traffic": args.traffic if args.traffic is not None else captured_traffic(args.workload, args.pair_umma),
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch, "
-                                  "profiles/gemm_swiglu_mixtral_T4096.md",
+                "traffic": traffic,
+                "traffic_source": ("--traffic argument" if args.traffic is not None else
+                                   "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of this kernel, "
+                                   "captured on another GB300 of the pool, not measured in this run (null when "
+                                   "the kernel sources differ from the captured ones)"),
                 "algorithmic_bytes_per_launch": alg_bytes_up,
                 "peak_source": peak_note,
                 "executed_tflops": round(fl_up_exe / (up_ms * 1e-3) / 1e12, 1),
@@ -492,8 +586,8 @@ def run_ours(args, rank: int, world: int):
         "copy": 2 * TK * d_ * 2,                                  # Yp rows in, Ret rows out
         "combine": TK * d_ * 2 + w.T * d_ * 4 + TK * 8,          # Ret rows + gates in, out written
     }
-    stage_ms = {"route_plan_permute": float(np.median(st_seq[:, tlc.EV_BEGIN])),
-                "copy": copy_alone_ms, "combine": float(np.median(st_seq[:, tlc.EV_COPIED]))}
+    stage_ms = {"route_plan_permute": stage_med["sequential"]["route_plan_permute"],
+                "copy": copy_alone_ms, "combine": stage_med["sequential"]["combine"]}
     hbm_stages = {n: {"bytes": int(b), "ms": round(stage_ms[n], 4),
                       "achieved_gbs": round(b / (stage_ms[n] * 1e-3) / 1e9, 1),
                       "frac_of_measured_hbm": round(b / (stage_ms[n] * 1e-3) / 1e9 / hbm, 3)}
@@ -518,13 +612,55 @@ def run_ours(args, rank: int, world: int):
                       "peaks": {"tflops": peak_tc, "hbm_gbs": hbm},
                       "note": "roofline step time / measured step time; the return copy counted as hidden"}
 
+    overlap = {**hidden_of("overlapped"), "copy_alone_ms": round(copy_alone_ms, 4),
+               "definition": "hidden = 1 - max(0, copy end - last down-projection flag) / the sequential copy's "
+                             "time (%globaltimer stamps of the same step)",
+               "wall_pct": wall, "wall_note": wall_note,
+               "sequential_ms_per_step": round(ms_seq, 4), "sequential_tokens_per_s": round(w.T / (ms_seq * 1e-3), 1),
+               "speedup_vs_sequential": round(ms_seq / ms_ovl, 4),
+               "alternating": {
+                   "method": (f"{K} CUDA-graph replays per arm, interleaved replay by replay "
+                              f"({' / '.join(arms)}), each between two events; medians per arm" if args.graph else
+                              f"{K} eager steps per arm, interleaved step by step; medians per arm"),
+                   "ms_per_step": {a: round(v, 4) for a, v in med.items()},
+                   "spread_ms": round(spread, 4),
+                   "eager_ms_per_step": {a: round(v, 4) for a, v in eager_ms.items()},
+                   "swiglu_stage_ratio_seq_over_ovl": round(swiglu_ratio, 4),
+                   "swiglu_stage_check": "ok" if abs(swiglu_ratio - 1) <= 0.01 else
+                   "the identical SwiGLU launch differs by more than 1% between the arms",
+                   "clocks": clocks_alt},
+               "dedicated_partition_c8": {
+                   "hidden_pct": round(100 * (1 - statistics.median(page_tails) / copy_alone_ms), 2),
+                   "tail_ms": round(statistics.median(page_tails), 4),
+                   "eager_ms_per_step": round(page_ms, 4)}}
+    if direct:
+        overlap["direct_tail"] = {
+            "tail_window": cfg.tail_window or "one wave (one tile per producer CTA pair)",
+            "bands_returned_by_epilogue": None,
+            "all_bands_copied": {**hidden_of("overlapped_all_bands_copied"),
+                                 "ms_per_step": round(med["overlapped_all_bands_copied"], 4),
+                                 "note": "the same layer without MOE_DIRECT_TAIL (every band through the "
+                                         "consumer), timed in the same alternation"}}
+        # which bands the epilogue returned: their Yp rows are left unwritten; count them from a step
+        # with Yp zeroed first
+        ws.view("Yp").zero_()
+        lb.step(cfg, False)
+        torch.cuda.synchronize()
+        tiles = ws.view("tiles").cpu().numpy()
+        MT = int(meta[1].item())
+        yp = ws.view("Yp").view(torch.int16)
+        n_direct = sum(1 for m in range(MT) if not bool(torch.any(
+            yp[int(tiles[m, 2]):int(tiles[m, 2]) + int(tiles[m, 3])] != 0)))
+        overlap["direct_tail"]["bands_returned_by_epilogue"] = f"{n_direct} of {MT}"
+
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": round(sec_max * 1e3 / K, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "ffn": w.ffn, "E": w.E, "topk": w.topk,
                    "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps),
-                   "pair_umma": bool(args.pair_umma), "mgb": args.mgb,
+                   "pair_umma": bool(args.pair_umma), "mgb": args.mgb, "direct_tail": direct,
+                   "tail_window": args.tail_window,
                    "tail_assist": not args.no_tail_assist, "seed": args.seed,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "
@@ -532,8 +668,9 @@ def run_ours(args, rank: int, world: int):
         "gpu_launches": 6 * K,
         "timing": ("CUDA-graph replays of one captured step (route, plan, permute, SwiGLU GEMM, "
                    "down-projection + copy, combine)" if args.graph else "eager launches"),
-        "eager": {"value": round(eager_value, 1), "ms_per_step": round(eager_sec_max * 1e3 / K, 4),
-                  "clocks": clocks_eager},
+        "eager": {"ms_per_step": round(eager_ms["overlapped"], 4),
+                  "value": round(w.T / (eager_ms["overlapped"] * 1e-3), 1),
+                  "note": "median of the alternating eager steps of the overlapped arm"},
         "clocks": clocks,
         "roofline": roofline,
         "gemm": {"executed_tflops": round(gemm_exec_tflops, 1), "algorithmic_tflops": round(gemm_alg_tflops, 1),
@@ -543,24 +680,11 @@ def run_ours(args, rank: int, world: int):
                  "peak_tflops": peak_tc, "peak_source": peak_note, "up_ms": round(up_ms, 4),
                  "down_ms": round(down_ms, 4), "down_kernel": "gemm_pair_kernel<2> (CTA pairs)" if pair_down
                  else "gemm_kernel<2>", "padded_rows": P, "compact_rows": PC,
+                 "down_algorithmic_frac_of_peak": round(fl_down_alg / (down_ms * 1e-3) / 1e12 / peak_tc, 4),
                  "executed_rows_up": exec_rows_up, "executed_rows_down": exec_rows, "work_items_up": items_up,
                  "work_items_down": items, "real_rows": TK},
-        "overlap": {"hidden_pct": round(100 * statistics.median(hidden), 2),
-                    "tail_ms": round(statistics.median(tails), 4), "copy_alone_ms": round(copy_alone_ms, 4),
-                    "tail_marks_us": dict(zip(["band_done", "last_acquire", "last_load", "last_drain", "copy_end"],
-                                              [round(float(v), 2) for v in np.median(np.array(marks), 0)])),
-                    "wall_pct": round(100 * (ms_seq - ms_ovl) / copy_alone_ms, 2),
-                    "sequential_ms_per_step": round(ms_seq, 4), "sequential_tokens_per_s": round(seq_value, 1),
-                    "speedup_vs_sequential": round(ms_seq / ms_ovl, 4),
-                    "dedicated_partition_c8": {
-                        "hidden_pct": round(100 * (1 - statistics.median(page_tails) / copy_alone_ms), 2),
-                        "tail_ms": round(statistics.median(page_tails), 4),
-                        "eager_ms_per_step": round(page_ms, 4)}},
-        "stages_ms": {"overlapped": {n: round(float(np.median(st_ovl[:, i])), 4) for i, n in enumerate(
-            ["route_plan_permute", "swiglu_gemm", "down_gemm_and_copy", "copy", "combine"])},
-            "sequential": {n: round(float(np.median(st_seq[:, i])), 4) for i, n in enumerate(
-                ["route_plan_permute", "swiglu_gemm", "down_gemm", "copy", "combine"])}},
-        "clocks_sequential": clocks_seq,
+        "overlap": overlap,
+        "stages_ms": {a: {n: round(v, 4) for n, v in stage_med[a].items()} for a in arms},
         "hbm_stages": hbm_stages,
         "layer_roofline": layer_roofline,
     }
@@ -569,8 +693,9 @@ def run_ours(args, rank: int, world: int):
         # End to end from pinned host memory: every step copies its logits and tokens in and its
         # output out. Headline: one moe_forward_host_pipelined call over the K steps (the transfers
         # of neighbouring steps overlap the layer); beside it, K separate moe_forward_host calls.
-        logits_h = torch.from_numpy(logits_np).pin_memory()
-        x_h = x_cpu.pin_memory()
+        W = lb.W
+        logits_h = torch.from_numpy(lb.logits_np).pin_memory()
+        x_h = lb.x_cpu.pin_memory()
         outs_h = [torch.empty(w.T, w.d, dtype=torch.float32).pin_memory() for _ in range(2)]
         h2d = logits_h.numel() * 4 + x_h.numel() * 2
         d2h = outs_h[0].numel() * 4
@@ -599,13 +724,61 @@ def run_ours(args, rank: int, world: int):
                 tlc.forward_host(cfg, logits_h, x_h, W["W1"], W["W3"], W["W2"], outs_h[0], ws)
 
         e2e_single, _ = aggregate(timed_e2e(per_call), w.T * K, world)
+        lb.check(cfg, "in the end-to-end steps")
         res["e2e"] = {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "call": f"moe_forward_host_pipelined ({K} batches in one call)",
                       "per_call_value": round(e2e_single, 1), "per_call": "moe_forward_host, one call per batch"}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, args.seed, tokens=256, W=W)
+        res["cpu_baseline"] = cpu_baseline(w, args.seed, tokens=256, W=lb.W)
+    if rank == 0 and world == 1 and args.workloads:
+        del lb
+        torch.cuda.empty_cache()
+        res["workloads"] = {n: other_workload(n, args, peaks) for n in args.workloads if n != args.workload}
     return res
+
+
+def other_workload(name: str, args, peaks) -> dict:
+    """A compact line for another workload in its default launch configuration: tokens/s over K
+    contiguous graph replays, hidden fraction of the return copy, SwiGLU GEMM roofline fraction."""
+    import tile_level_copy_gb300 as tlc
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = inputs.WORKLOADS[name]
+    c, warps = DEFAULT_COPY[name]
+    cfg = tlc.Config.from_workload(w, consumer_ctas=c, flags=default_flags(warps))
+    lb = LayerBench(w, args.seed, dev)
+    K, Wm = max(5, args.steps // 2), max(3, args.warmup)
+    g = lb.graph(cfg, False)
+    for _ in range(Wm):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        t0.record()
+        for _ in range(K):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+    lb.check(cfg, f"in the {name} replays")
+    ms = t0.elapsed_time(t1) / K
+    arms = {"overlapped": (cfg, False), "sequential": (cfg, True),
+            "overlapped_all_bands_copied": (dataclasses.replace(cfg, flags=cfg.flags & ~tlc.MOE_DIRECT_TAIL), False)}
+    st = alternate_eager(lb, arms, 5, 2)
+    copy_alone = float(np.median(st["sequential"][:, 3]))
+    up_ms = float(np.median(st["overlapped"][:, 1]))
+    tails, _ = lb.tails(cfg, 5)
+    tails_all, _ = lb.tails(arms["overlapped_all_bands_copied"][0], 5)
+    fl_up = 4.0 * w.T * w.topk * w.d * w.ffn
+    up_tflops = fl_up / (up_ms * 1e-3) / 1e12
+    return {"workload": workload_desc(w), "consumer_ctas": c, "copy_warps": warps, "steps": K,
+            "tokens_per_s": round(w.T / (ms * 1e-3), 1), "ms_per_step": round(ms, 4),
+            "hidden_pct": round(100 * (1 - statistics.median(tails) / copy_alone), 2),
+            "hidden_pct_all_bands_copied": round(100 * (1 - statistics.median(tails_all) / copy_alone), 2),
+            "copy_alone_ms": round(copy_alone, 4),
+            "swiglu_gemm": {"ms": round(up_ms, 4), "achieved_tflops": round(up_tflops, 1),
+                            "frac_of_measured_burst_peak": round(up_tflops / peaks["bf16_tflops"], 4)},
+            "eager_ms_per_step": {a: round(float(np.median(v.sum(1))), 4) for a, v in st.items()},
+            "clocks": clk.summary()}
 
 
 # ------------------------------------------------------------------------ CPU oracle timing

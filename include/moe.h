@@ -65,6 +65,11 @@ extern "C" {
                                       /* (tcgen05 cta_group::2), half the B tile per SM; the   */
                                       /* down-projection too when d % 256 == 0, consumer_ctas  */
                                       /* is even and MOE_COPY_WARPS is not set                 */
+#define MOE_DIRECT_TAIL 0x10u         /* the down-projection's epilogue writes the bands whose */
+                                      /* tiles are all handed out in the launch's last        */
+                                      /* tail_window tile positions (the last wave) straight  */
+                                      /* into their owner's slice of Ret; the consumer skips   */
+                                      /* them and their rows of Yp are not written             */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
 #define MOE_TEST_PLAN_FAIL 0x200u     /* test hook: the plan kernel reports a failed bounds   */
@@ -78,9 +83,12 @@ extern "C" {
  *   consumer_ctas = c_CTA, the SMs given to the consumer ([TLS "Axiom & Free-Parameter Ledger"],
  *   swept 2-24 on the page); mgb = bands per interior segment (same section, 1 or 2 there).
  *   timeout_us bounds every device-side wait (0 = 2,000,000 us).
+ *   tail_window (with MOE_DIRECT_TAIL): the number of the down-projection's last tile hand-out
+ *   positions whose bands are returned by the epilogue itself; 0 = one wave (one tile per
+ *   producer CTA, or per producer CTA pair on CTA pairs).
  * Limits: d % 128 == 0, ffn % 128 == 0, 1 <= topk <= min(E, 8), 1 <= E <= 256, T % R == 0,
  *   E*R <= 1024, tile_M in {64, 128}, 1 <= mgb <= 4, 1 <= consumer_ctas <= SMs/2 (0 allowed
- *   with MOE_COPY_WARPS; checked at launch), P_max < 2^30 (see moe_layout).
+ *   with MOE_COPY_WARPS; checked at launch), tail_window >= 0, P_max < 2^30 (see moe_layout).
  */
 typedef struct moe_config {
     int32_t T, d, ffn, E, topk, R, tile_M;
@@ -88,7 +96,8 @@ typedef struct moe_config {
     int32_t mgb;
     uint32_t flags;
     uint32_t timeout_us;
-    int32_t reserved[5]; /* must be zero */
+    int32_t tail_window;
+    int32_t reserved[4]; /* must be zero */
 } moe_config;
 
 /*
@@ -132,6 +141,7 @@ typedef struct moe_layout {
     size_t ret_slot;   /* int32 [T, topk]   row of pair (t, j) in Ret                          */
     size_t ccoff;      /* int32 [E*R]       first Xc row of group e*R+r                         */
     size_t tile_crow;  /* int32 [MT_max]    Xc / Hc row of the first row of each M-tile (band) */
+    size_t band_item;  /* int32 [MT_max]    down-projection work item holding each M-tile      */
     size_t meta;       /* int32 [64]        P, M-tiles, work counters, status (see csrc)       */
     size_t flags;      /* uint32 [MT_max, n_tiles_n2] per-tile readiness flags                 */
     size_t bands;      /* uint32 [MT_max]   per-band count of finished tile quarters           */

@@ -73,7 +73,7 @@ def test_invalid_configs_are_rejected(bad):
 
 def test_reserved_fields_must_be_zero(built_library):
     c = cfg_of("tiny").to_c()
-    c.reserved[2] = 1
+    c.reserved[1] = 1
     n = ctypes.c_size_t()
     assert built_library.moe_workspace_size(ctypes.byref(c), ctypes.byref(n)) == tlc.MOE_ERR_ARG
 
@@ -103,3 +103,10 @@ def test_static_entry_point_rejects_null_pointers_without_a_gpu(built_library):
     c.R = 3  # T % R != 0
     one = ctypes.c_void_p(16)
     assert built_library.moe_route_static(ctypes.byref(c), one, one, one, one, one, one, None) == tlc.MOE_ERR_ARG
+
+
+def test_negative_tail_window_is_rejected():
+    cfg = cfg_of("tiny", tail_window=-1)
+    with pytest.raises(tlc.MoEError) as ei:
+        tlc.workspace_size(cfg)
+    assert ei.value.code == tlc.MOE_ERR_ARG

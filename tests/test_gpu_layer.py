@@ -239,13 +239,13 @@ def test_argument_errors_on_gpu():
 @pytest.mark.parametrize("name", ["mixtral", "skew", "fine"])
 def test_full_size_sampled_tokens(name):
     """Full workload sizes in the bench's launch configuration (its per-workload copy configuration,
-    CTA-pair SwiGLU GEMM, tail assist); 48 sampled tokens against the oracle's per-token definition,
+    CTA-pair GEMMs, tail assist, direct tail); 48 sampled tokens against the oracle's per-token definition,
     plus bitwise overlapped == sequential over all tokens, also for the page's dedicated partition
     (8 consumer CTAs, single-CTA GEMMs) and for copy warps alone."""
     import bench
     w = inputs.WORKLOADS[name]
     c, warps = bench.DEFAULT_COPY[name]
-    flags = tlc.MOE_TAIL_ASSIST | tlc.MOE_PAIR_UMMA | (CW if warps else 0)
+    flags = bench.default_flags(warps)
     L = Layer(w, seed=0, cfg_kw=dict(consumer_ctas=c, flags=flags))
     got = L.run(sequential=False)
     seq = L.run(sequential=True)

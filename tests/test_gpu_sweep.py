@@ -55,7 +55,8 @@ def test_sweep_overlapped_equals_sequential(weights, T):
         assert tlc.status(base_cfg, ws)[0] == tlc.MOE_OK
         want = out.clone()
         for c in CONSUMERS:
-            for flags in (0, tlc.MOE_TAIL_ASSIST, tlc.MOE_TAIL_ASSIST | tlc.MOE_COPY_WARPS):
+            for flags in (0, tlc.MOE_TAIL_ASSIST, tlc.MOE_TAIL_ASSIST | tlc.MOE_COPY_WARPS,
+                          tlc.MOE_PAIR_UMMA | tlc.MOE_TAIL_ASSIST | tlc.MOE_DIRECT_TAIL):
                 cfg = tlc.Config.from_workload(w, consumer_ctas=c, flags=flags)
                 out.zero_()
                 tlc.forward(cfg, logits, x, weights["W1"], weights["W3"], weights["W2"], out, ws)

@@ -28,6 +28,7 @@ MOE_PLAN_SKIP_PERMUTE = 0x1
 MOE_TAIL_ASSIST = 0x2
 MOE_COPY_WARPS = 0x4
 MOE_PAIR_UMMA = 0x8
+MOE_DIRECT_TAIL = 0x10
 MOE_TEST_STALL_CONSUMER = 0x100
 MOE_TEST_PLAN_FAIL = 0x200
 
@@ -51,14 +52,15 @@ class MoEError(RuntimeError):
 
 class _Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "d", "ffn", "E", "topk", "R", "tile_M", "consumer_ctas", "mgb")] + [
-        ("flags", ctypes.c_uint32), ("timeout_us", ctypes.c_uint32), ("reserved", ctypes.c_int32 * 5)]
+        ("flags", ctypes.c_uint32), ("timeout_us", ctypes.c_uint32), ("tail_window", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 4)]
 
 
 _LAYOUT_INTS = ("P_max", "MT_max", "n_chunks", "chunk_tokens", "n_tiles_n2", "block_n2", "rows_per_unit",
                 "units_per_band", "PC_max", "IU_max")
 LAYOUT_REGIONS = ("idx", "gate", "rank", "chunk_cnt", "chunk_base", "counts", "offsets", "ret_off", "tiles",
                   "tile_ret", "sched", "seg", "experts", "items_up", "items_down", "slot", "cslot", "ret_slot", "ccoff",
-                  "tile_crow", "meta", "flags", "bands", "trace", "Xc", "Hc", "Yp", "Ret", "in_logits", "in_x", "out")
+                  "tile_crow", "band_item", "meta", "flags", "bands", "trace", "Xc", "Hc", "Yp", "Ret", "in_logits", "in_x", "out")
 
 
 class _Layout(ctypes.Structure):
@@ -81,6 +83,7 @@ class Config:
     mgb: int = 1
     flags: int = 0
     timeout_us: int = 0
+    tail_window: int = 0
 
     def to_c(self) -> _Config:
         c = _Config()
@@ -170,6 +173,7 @@ class Workspace:
     _DT = {"idx": (torch.int32, "TK"), "gate": (torch.float32, "TK"), "rank": (torch.int32, "TK"),
            "slot": (torch.int32, "TK"), "cslot": (torch.int32, "TK"), "ret_slot": (torch.int32, "TK"),
            "counts": (torch.int32, "ER"), "ccoff": (torch.int32, "ER"), "tile_crow": (torch.int32, "MT"),
+           "band_item": (torch.int32, "MT"),
            "offsets": (torch.int32, "G1"), "ret_off": (torch.int32, "RE1"), "tiles": (torch.int32, "MT4"),
            "tile_ret": (torch.int32, "MT"), "sched": (torch.int32, "MT"), "seg": (torch.int32, "MT2"),
            "experts": (torch.int32, "E8"), "items_up": (torch.int32, "IU2"),

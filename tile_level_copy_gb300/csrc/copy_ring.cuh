@@ -105,8 +105,10 @@ __device__ __forceinline__ bool copy_unit_ok(const Shape& s, const PlanPtrs& p, 
     return true;
 }
 
+// skip_item: bands of down-projection work items from this index on are returned by the GEMM's own
+// epilogue (MOE_DIRECT_TAIL): their units are passed over and their counters are not waited for.
 __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uint64_t* bars, volatile int* s_abort,
-                           int queue, bool wait_flags, uint32_t want) {
+                           int queue, bool wait_flags, uint32_t want, int skip_item) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int MT = p.meta[META_MTILES];
     if (MT < 0 || MT > s.MT_max) MT = 0;
@@ -134,7 +136,7 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
         }
         const int m = p.sched[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
-        if (rb >= valid) {
+        if (rb >= valid || p.band_item[m] >= skip_item) {
             if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
             continue;
         }
@@ -146,6 +148,7 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
             if (lane == 0) {
                 const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
                 for (int i = 0; i < nb && !failed; ++i) {
+                    if (p.band_item[p.sched[first + i]] >= skip_item) continue;  // returned by the epilogue
                     const uint32_t* bc = p.bands + p.sched[first + i];
                     if (ld_acquire_gpu(bc) == want) continue;
                     if (!engine_flush(ce, s.timeout_ns, s_abort)) {
@@ -225,7 +228,8 @@ __device__ __forceinline__ void st_cg_v4(uint4* p, const uint4& v) {
                  : "memory");
 }
 
-__device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int* s_abort, int queue, uint32_t want) {
+__device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int* s_abort, int queue, uint32_t want,
+                                int skip_item) {
     const int lane = threadIdx.x & 31;
     int MT = p.meta[META_MTILES];
     if (MT < 0 || MT > s.MT_max) MT = 0;
@@ -251,7 +255,7 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
         }
         const int m = p.sched[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
-        if (rb >= valid) {
+        if (rb >= valid || p.band_item[m] >= skip_item) {
             if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
             continue;
         }
@@ -260,6 +264,7 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
         if (lane == 0) {
             const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
             for (int i = 0; i < nb && !failed; ++i) {
+                if (p.band_item[p.sched[first + i]] >= skip_item) continue;  // returned by the epilogue
                 const uint32_t* bc = p.bands + p.sched[first + i];
                 if (ld_acquire_gpu(bc) == want) continue;
                 const unsigned long long t0 = globaltimer();

@@ -91,10 +91,13 @@ __device__ __forceinline__ int tile_take(const Smem& sm, int j, unsigned long lo
 // expert (mA = mB = 0), read and written in the compact layout.
 struct TileRef {
     int mA, mB, n, e, rowA, rowB, lrowA, lrowB;
+    int item;  // down-projection work item (index into the item list); -1 for SwiGLU tiles
 };
 
-__device__ __forceinline__ TileRef make_ref(int mA, int mB, int n, const int32_t* tiles, const int32_t* crow) {
+__device__ __forceinline__ TileRef make_ref(int mA, int mB, int n, const int32_t* tiles, const int32_t* crow,
+                                            int item) {
     TileRef r;
+    r.item = item;
     r.mA = mA;
     r.mB = mB;
     r.n = n;
@@ -109,6 +112,7 @@ __device__ __forceinline__ TileRef make_ref(int mA, int mB, int n, const int32_t
 
 __device__ __forceinline__ TileRef compact_ref(int row, int n, int e) {
     TileRef r;
+    r.item = -1;
     r.mA = r.mB = 0;
     r.n = n;
     r.e = e;
@@ -138,7 +142,7 @@ __device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, const
 __device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* items, const int32_t* tiles,
                                                const int32_t* crow) {
     const int it = t / nN;
-    return make_ref(items[2 * it], items[2 * it + 1], t - it * nN, tiles, crow);
+    return make_ref(items[2 * it], items[2 * it + 1], t - it * nN, tiles, crow, it);
 }
 
 // One epilogue warp's staging in shared memory: two 32-row x 32-column bf16 chunk buffers, used
@@ -167,6 +171,42 @@ struct EpiStage {
         }
         eb ^= 1;
     }
+    // Direct return of the chunk (MOE_DIRECT_TAIL): the same staging, then the warp stores the
+    // chunk's first `rows` rows with 16-byte stores, eight rows of 64 bytes per instruction, to
+    // dst (row 0 of the chunk) + row * pitch + col_bytes. Rows past `rows` are padding rows of the
+    // band: the owner's packed return rows have no room for them.
+    __device__ __forceinline__ void put_direct(const uint32_t (&pk)[16], uint8_t* dst, size_t pitch, int col_bytes,
+                                               int rows, int lane) {
+        if (lane == 0) bulk_wait_read_1();  // an earlier tensor store from this buffer has read it
+        __syncwarp();
+        uint8_t* chunk = buf + eb * EPI_CHUNK_BYTES;
+        uint4* row = reinterpret_cast<uint4*>(chunk + lane * (EPI_CHUNK * 2));
+        const uint4 u0 = make_uint4(pk[0], pk[1], pk[2], pk[3]), u1 = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        const uint4 u2 = make_uint4(pk[8], pk[9], pk[10], pk[11]);
+        const uint4 u3 = make_uint4(pk[12], pk[13], pk[14], pk[15]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int pi = (i + lane) & 3;
+            row[pi] = pi == 0 ? u0 : pi == 1 ? u1 : pi == 2 ? u2 : u3;
+        }
+        __syncwarp();
+        const uint4* src = reinterpret_cast<const uint4*>(chunk);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int piece = lane + 32 * i, r = piece >> 2;  // 4 pieces of 16 bytes per 64-byte row
+            if (r < rows)
+                *reinterpret_cast<uint4*>(dst + (size_t)r * pitch + col_bytes + (piece & 3) * 16) = src[piece];
+        }
+        __syncwarp();  // the buffer is read before it is written again
+        eb ^= 1;
+    }
+};
+
+// Destination of a warp's rows when its tile's band is returned by the epilogue itself
+// (MOE_DIRECT_TAIL): the Ret row of the warp's first tile row, and how many of its 32 rows are real.
+struct DirectDst {
+    uint8_t* row0;  // nullptr: the rows go to Yp through the output tensor map
+    int rows;
 };
 
 // Epilogue of one warp's 32 accumulator lanes (tile rows y..y+31) of a finished tile at TMEM
@@ -175,7 +215,8 @@ struct EpiStage {
 // rounded to bf16. Inactive warps (padding half of a 64-row band) read TMEM but store nothing.
 template <int MODE>
 __device__ __forceinline__ void epilogue_rows(EpiStage& es, const CUtensorMap* tmOut, uint32_t tb, int n, int BN,
-                                              int y, bool active, int lane) {
+                                              int y, bool active, int lane, DirectDst dd = DirectDst{nullptr, 0},
+                                              size_t pitch = 0) {
     if (MODE == 1) {
 #pragma unroll 1
         for (int c = 0; c < BN1 / 32; ++c) {
@@ -204,10 +245,25 @@ __device__ __forceinline__ void epilogue_rows(EpiStage& es, const CUtensorMap* t
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                es.put(tmOut, pk, n * BN + c * 32, y, lane);
+                if (dd.row0) {
+                    if (dd.rows > 0) es.put_direct(pk, dd.row0, pitch, (n * BN + c * 32) * 2, dd.rows, lane);
+                } else {
+                    es.put(tmOut, pk, n * BN + c * 32, y, lane);
+                }
             }
         }
     }
+}
+
+// Destination of epilogue warp q's rows (TMEM lane quarter q) when its band mq is returned directly:
+// its first row inside the band, the Ret row it goes to and how many of its 32 rows are real.
+__device__ __forceinline__ DirectDst direct_dst(const Shape& s, const PlanPtrs& p, const TileRef& tr, int q) {
+    const int mq = (q < 2) ? tr.mA : tr.mB;
+    const int rb = ((q >= 2 && tr.mB == tr.mA) ? 64 : 0) + (q & 1) * 32;
+    DirectDst dd;
+    dd.rows = max(0, min(32, p.tiles[4 * mq + 3] - rb));
+    dd.row0 = reinterpret_cast<uint8_t*>(p.Ret) + (size_t)(p.tile_ret[mq] + rb) * s.d * 2;
+    return dd;
 }
 
 // Bounds check of the plan entries a GEMM launch reads, by all threads of a CTA before any tile:
@@ -238,7 +294,9 @@ __device__ __forceinline__ int plan_items_bad(const Shape& s, const PlanPtrs& p,
                 const int m = ms[j];
                 if (m < 0) continue;
                 const int e = p.tiles[4 * m], row0 = p.tiles[4 * m + 2], crow = p.tile_crow[m];
-                if (e < 0 || e >= s.E || row0 < 0 || row0 + s.tbM > s.P_max || crow < 0 || crow >= s.PC_max)
+                const int valid = p.tiles[4 * m + 3], ret0 = p.tile_ret[m];
+                if (e < 0 || e >= s.E || row0 < 0 || row0 + s.tbM > s.P_max || crow < 0 || crow >= s.PC_max ||
+                    valid < 1 || valid > s.tbM || ret0 < 0 || ret0 + valid > s.T * s.k)
                     bad = it + 1;
             }
         }
@@ -270,6 +328,14 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     const int total = NI * nN;
     const uint32_t tx_bytes = A_STAGE_BYTES + BN * BK * 2;
     const unsigned long long tmo = s.timeout_ns;
+    // MOE_DIRECT_TAIL: items from `direct_from` on have every tile among the last `window` hand-out
+    // positions (item i's tiles are i*nN .. i*nN+nN-1); their epilogue writes the rows into Ret and
+    // the copy engines skip them
+    int direct_from = INT_MAX;
+    if (MODE == 2 && overlapped && (s.flags & MOE_DIRECT_TAIL)) {
+        const int window = s.tail_window > 0 ? s.tail_window : num_producers, thr = total - window;
+        direct_from = thr <= 0 ? 0 : min(NI, (thr + nN - 1) / nN);
+    }
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -326,7 +392,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 
     // Extra warps (launched with MOE_COPY_WARPS): SIMT copy engines beside the GEMM warps.
     if (warp >= GEMM_WARPS) {
-        if (MODE == 2 && overlapped) copy_units_simt(s, p, sm.abort, META_QUEUE, want);
+        if (MODE == 2 && overlapped) copy_units_simt(s, p, sm.abort, META_QUEUE, want, direct_from);
         return;
     }
 
@@ -480,7 +546,9 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                 const bool active = mq >= 0;
                 const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
                 const uint32_t inc = (tr.mB == tr.mA) ? 1u : 2u;  // quarters per band: 4 in all
-                epilogue_rows<MODE>(es, &tmOut, tb, tr.n, BN, y, active, lane);
+                const DirectDst dd = (MODE == 2 && active && tr.item >= direct_from) ? direct_dst(s, p, tr, q)
+                                                                                   : DirectDst{nullptr, 0};
+                epilogue_rows<MODE>(es, &tmOut, tb, tr.n, BN, y, active, lane, dd, (size_t)s.d * 2);
                 tc_fence_before();
                 mbar_arrive(&sm.acc_empty[b]);
                 if (MODE == 2 && active) {
@@ -522,7 +590,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
         atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
 
     if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
-        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want);
+        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want, direct_from);
 }
 
 // =============================================================================================
@@ -641,6 +709,7 @@ __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, 
     const int n = local / np, it = 2 * (local - n * np) + (int)rank;
     if (it >= cnt) {
         TileRef r;
+        r.item = -1;
         r.mA = r.mB = -1;
         r.n = n;
         r.e = e;
@@ -676,6 +745,7 @@ __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E
     const int it = 2 * pi + (int)rank;
     if (it >= count[r]) {
         TileRef x;
+        x.item = -1;
         x.mA = x.mB = -1;
         x.n = n;
         x.e = tiles[4 * items[2 * (first[r] + 2 * pi)]];
@@ -683,7 +753,7 @@ __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E
         return x;
     }
     const int item = first[r] + it;
-    return make_ref(items[2 * item], items[2 * item + 1], n, tiles, crow);
+    return make_ref(items[2 * item], items[2 * item + 1], n, tiles, crow, item);
 }
 
 template <int MODE>  // 1: SwiGLU up-projection -> Hc; 2: down-projection -> Yp (+ flags / consumers)
@@ -763,6 +833,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             acc += ((count[r] + 1) >> 1) * nN;
         }
         sm.tab[s.E] = acc;
+        // MOE_DIRECT_TAIL: the first item of the first pair item whose first tile is among the last
+        // `window` hand-out positions (the pair items' first tiles rise with the item index, so every
+        // later item is in the window too); its epilogue and every later one's write into Ret
+        int from = INT_MAX;
+        if (overlapped && (s.flags & MOE_DIRECT_TAIL) && NI > 0 && acc > 0) {
+            const int window = s.tail_window > 0 ? s.tail_window : num_producers / 2, thr = acc - window;
+            from = NI;
+            for (int r = 0; r < s.E; ++r) {
+                const int np = (count[r] + 1) >> 1;
+                if (np == 0 || sm.tab[r + 1] <= thr) continue;
+                const bool n_outer = count[r] <= s.down_n_outer_items && sm.tab[r + 1] != acc;
+                const int rel = thr - sm.tab[r];
+                const int pi = rel <= 0 ? 0 : (n_outer ? rel : (rel + nN - 1) / nN);
+                if (pi < np) {
+                    from = first[r] + 2 * pi;
+                    break;
+                }
+            }
+        }
+        sm.tab[3 * s.E + 1] = from;
     }
     if (producer && warp == 1) {
         __syncwarp();
@@ -789,6 +879,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
     int* const tile_counter = &p.meta[(MODE == 1) ? META_TILES_UP : META_TILES_DOWN];
     unsigned long long last_end = 0;
+    const int direct_from = (MODE == 2) ? sm.tab[3 * s.E + 1] : INT_MAX;
 
     if (producer) {
         if (warp == 0 && lane == 0) {
@@ -986,7 +1077,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 const int mq = (q < 2) ? tr.mA : tr.mB;
                 const bool active = mq >= 0;
                 const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
-                epilogue_rows<MODE>(es, &tmOut, tb, tr.n, 2 * BN1, y, active, lane);
+                const DirectDst dd = (MODE == 2 && active && tr.item >= direct_from) ? direct_dst(s, p, tr, q)
+                                                                                   : DirectDst{nullptr, 0};
+                epilogue_rows<MODE>(es, &tmOut, tb, tr.n, 2 * BN1, y, active, lane, dd, (size_t)s.d * 2);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(acc_empty0 + b * 8u);
@@ -1026,7 +1119,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     }
     // copy engines: consumer CTAs from the start, producers once their tiles are done (tail assist)
     if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
-        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want);
+        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want, direct_from);
 }
 
 static cudaError_t set_smem_attr(const void* fn) {
@@ -1126,7 +1219,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) copy_seq_kernel(Shape s, Plan
         mbar_fence_init();
     }
     __syncthreads();
-    copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE_SEQ, false, 0u);
+    copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE_SEQ, false, 0u, INT_MAX);
 }
 
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st) {

@@ -49,8 +49,9 @@ int make_layout(const moe_config* c, Layout* out) {
     if (E * R > 1024) return fail(MOE_ERR_ARG, "E*R=%lld exceeds 1024", (long long)(E * R));
     if (tbM != 64 && tbM != 128) return fail(MOE_ERR_ARG, "tile_M=%lld must be 64 or 128", (long long)tbM);
     if (c->mgb < 1 || c->mgb > 4) return fail(MOE_ERR_ARG, "mgb=%d must be in [1, 4]", c->mgb);
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < 4; ++i)
         if (c->reserved[i]) return fail(MOE_ERR_ARG, "reserved fields must be zero");
+    if (c->tail_window < 0) return fail(MOE_ERR_ARG, "tail_window=%d must be >= 0", c->tail_window);
 
     const int64_t TK = T * k, G = E * R;
     const int64_t P_max = (int64_t)align_up((size_t)(TK + (G < TK ? G : TK) * (tbM - 1)), (size_t)tbM);
@@ -112,6 +113,7 @@ int make_layout(const moe_config* c, Layout* out) {
     L.ret_slot = put(TK * 4);
     L.ccoff = put(G * 4);
     L.tile_crow = put(MT_max * 4);
+    L.band_item = put(MT_max * 4);
     L.meta = put(META_COUNT * 4);
     L.flags = put(MT_max * nN2 * 4);
     L.bands = put(MT_max * 4);
@@ -156,6 +158,7 @@ int make_layout(const moe_config* c, Layout* out) {
     S.down_n_outer_items = (d * F * 2 >= half_l2) ? (int)(half_l2 / (int64_t(BM) * F * 2)) : 0;
     S.timeout_ns = (unsigned long long)(c->timeout_us ? c->timeout_us : 2000000u) * 1000ull;
     S.flags = c->flags;
+    S.tail_window = c->tail_window;
     *out = o;
     return MOE_OK;
 }
@@ -183,6 +186,7 @@ PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     p.ret_slot = reinterpret_cast<int32_t*>(b + L.ret_slot);
     p.ccoff = reinterpret_cast<int32_t*>(b + L.ccoff);
     p.tile_crow = reinterpret_cast<int32_t*>(b + L.tile_crow);
+    p.band_item = reinterpret_cast<int32_t*>(b + L.band_item);
     p.meta = reinterpret_cast<int32_t*>(b + L.meta);
     p.flags = reinterpret_cast<uint32_t*>(b + L.flags);
     p.bands = reinterpret_cast<uint32_t*>(b + L.bands);
@@ -367,7 +371,7 @@ namespace {
 // Offsets of the plan's scratch regions inside the static array for one config (256-byte aligned).
 struct StaticLayout {
     size_t rank, cnt, base, counts, ret, tiles, tret, sched, seg, exp, iu, id, meta, flags, bands, trace, cslot,
-        ccoff, tcrow, bytes;
+        ccoff, tcrow, bitem, bytes;
 };
 
 StaticLayout static_layout(const Layout& lay) {
@@ -400,6 +404,7 @@ StaticLayout static_layout(const Layout& lay) {
     o.cslot = put(TK * 4);
     o.ccoff = put(E * R * 4);
     o.tcrow = put(MT * 4);
+    o.bitem = put(MT * 4);
     o.bytes = cur;
     return o;
 }
@@ -792,6 +797,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.ret_slot = ret_slot;
     p.ccoff = reinterpret_cast<int32_t*>(b + o.ccoff);
     p.tile_crow = reinterpret_cast<int32_t*>(b + o.tcrow);
+    p.band_item = reinterpret_cast<int32_t*>(b + o.bitem);
     p.meta = reinterpret_cast<int32_t*>(b + o.meta);
     p.flags = reinterpret_cast<uint32_t*>(b + o.flags);
     p.bands = reinterpret_cast<uint32_t*>(b + o.bands);

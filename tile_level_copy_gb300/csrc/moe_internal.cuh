@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -108,6 +110,7 @@ struct PlanPtrs {
     int32_t* ret_slot;
     int32_t* ccoff;      // [E*R] first compact row of each group
     int32_t* tile_crow;  // [MT_max] compact row of each band's first row
+    int32_t* band_item;  // [MT_max] down-projection work item holding each band
     int32_t* meta;
     uint32_t* flags;
     uint32_t* bands;
@@ -130,6 +133,7 @@ struct Shape {
     int tail_bands;
     int down_n_outer_items;         // pair down-projection: experts of at most this many items
                                     // take their tiles N tile by N tile (0: none)
+    int tail_window;                // MOE_DIRECT_TAIL: hand-out positions of the direct window (0: one wave)
     unsigned long long timeout_ns;
     uint32_t flags;
 };

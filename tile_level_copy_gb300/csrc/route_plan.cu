@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     // band with <= 64 valid rows when tbM = 128) shares a work item with another such band of the
     // same expert, each loaded as a 64-row box into one half of the A tile. Item (mA, mB): mB == mA
     // one 128-row band; mB == -1 one 64-row band alone; else two half bands; schedule order.
-    __shared__ int s_items[MAX_E], s_ibase_down[MAX_E];
+    __shared__ int s_items[MAX_E], s_ibase_down[MAX_E], s_nitems;
     for (int e = tid; e < E; e += PLAN_THREADS) {
         const int cnt = s_mt[e];
         int half = 0;  // bands with <= 64 valid rows: all of them when tbM = 64, else partial ones
@@ -453,6 +453,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         int down = 0;
         for (int f = 0; f < E; ++f) down += (s_erank[f] < s_erank[e]) ? s_items[f] : 0;
         s_ibase_down[e] = down;
+        if (s_erank[e] == E - 1) s_nitems = down + s_items[e];  // the last expert's items end the list
         const int iu = (s_load[e] + BM - 1) / BM;
         p.experts[8 * e + 4] = iu;
         p.experts[8 * e + 5] = s_cbase[e] / BM;
@@ -502,13 +503,21 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         }
     }
 
+    // 7b. the work item holding each band (the inverse of the item list), read by the copy engines
+    // to tell the bands that the down-projection's epilogue returns itself (MOE_DIRECT_TAIL)
+    __syncthreads();
+    const int items = s_nitems;
+    for (int i = tid; i < items; i += PLAN_THREADS) {
+        const int mA = p.items_down[2 * i], mB = p.items_down[2 * i + 1];
+        if (mA >= 0 && mA < MT) p.band_item[mA] = i;
+        if (mB >= 0 && mB < MT) p.band_item[mB] = i;
+    }
+
     // 8. per-call meta, flags and trace reset
     if (tid == 0) {
         p.meta[META_P] = P;
         p.meta[META_MTILES] = MT;
         p.meta[META_UNITS] = copy_unit_count(s, MT);
-        int items = 0;
-        for (int e = 0; e < E; ++e) items += s_items[e];
         p.meta[META_ITEMS] = items;
         p.meta[META_ITEMS_UP] = PC / BM;
         p.meta[META_PC] = PC;

@@ -5,9 +5,10 @@ latency against a GEMM-then-transfer baseline (its Figure 9), the overlap ratio 
 vary (Figure 4b), and the consumer's copy bandwidth and segment size (mgb). This module measures
 the same on one GB300, in three parts (one JSON object per point on stdout, "part" names it):
 
-  layer  for every (T, R, c): the overlapped layer, the GEMM-then-copy layer, the copy alone, the
-         exposed copy tail, the hidden fraction, and the GEMM slowdown of taking c SMs from the
-         down-projection (its producer span over the span of the same GEMM on all SMs)
+  layer  for every (T, R, c): the overlapped layer, the GEMM-then-copy layer (the two interleaved
+         step by step, so both see the same clocks; times also given in SM clock cycles), the copy
+         alone, the exposed copy tail, the hidden fraction, and the GEMM slowdown of taking c SMs
+         from the down-projection (its producer span over the span of the same GEMM on all SMs)
   mgb    at T=4096, R=4: hidden fraction and tail against the segment size mgb and c
   copy   the return copy alone on c SMs (moe_copy_only): copy bandwidth against c
 
@@ -56,19 +57,27 @@ class ClockWatch:
         return statistics.median(self.vals) if self.vals else None
 
 
-def time_steps(cfg, args_, ws, seq: bool, steps: int, warmup: int):
+def time_arms(arms, args_, ws, steps: int, warmup: int):
+    """Eager steps of every arm (name -> (cfg, sequential)) interleaved step by step, each step
+    between stage events; returns {name: (median step ms, median stage ms [5])}. Interleaving gives
+    every arm the same clock and power conditions."""
     for _ in range(warmup):
-        tlc.forward(cfg, *args_, ws, sequential=seq)
-    evs = [tlc.stage_events() for _ in range(steps)]
+        for cfg, seq in arms.values():
+            tlc.forward(cfg, *args_, ws, sequential=seq)
+    evs = {a: [tlc.stage_events() for _ in range(steps)] for a in arms}
     torch.cuda.synchronize()
     for i in range(steps):
-        tlc.forward(cfg, *args_, ws, sequential=seq, events=evs[i])
+        for a, (cfg, seq) in arms.items():
+            tlc.forward(cfg, *args_, ws, sequential=seq, events=evs[a][i])
     torch.cuda.synchronize()
-    rc, detail = tlc.status(cfg, ws)
-    if rc != tlc.MOE_OK:
-        raise RuntimeError(f"device status {rc} ({detail})")
-    st = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(tlc.EV_COUNT - 1)] for e in evs])
-    return float(np.median(st.sum(1))), np.median(st, 0)
+    out = {}
+    for a, (cfg, _) in arms.items():
+        rc, detail = tlc.status(cfg, ws)
+        if rc != tlc.MOE_OK:
+            raise RuntimeError(f"device status {rc} ({detail})")
+        st = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(tlc.EV_COUNT - 1)] for e in evs[a]])
+        out[a] = (float(np.median(st.sum(1))), np.median(st, 0))
+    return out
 
 
 def trace_of(cfg, args_, ws, seq: bool, reps: int = 5):
@@ -112,20 +121,17 @@ def part_layer(S: Setup, a, flags):
             ws = tlc.Workspace(tlc.Config.from_workload(w, consumer_ctas=8, flags=flags), S.dev)
             for c in a.consumers:
                 cfg = tlc.Config.from_workload(w, consumer_ctas=c, flags=flags)
-                seqs, ovls, copies = [], [], []
-                with ClockWatch() as clk:  # sequential and overlapped in alternation: same clocks
-                    for _ in range(2):
-                        seq_ms, seq_st = time_steps(cfg, args_, ws, True, a.steps, a.warmup)
-                        ovl_ms, _ = time_steps(cfg, args_, ws, False, a.steps, a.warmup)
-                        seqs.append(seq_ms)
-                        ovls.append(ovl_ms)
-                        copies.append(float(seq_st[tlc.EV_DOWN]))
-                seq_ms, ovl_ms, copy_ms = min(seqs), min(ovls), statistics.median(copies)
+                with ClockWatch() as clk:  # sequential and overlapped interleaved step by step
+                    r = time_arms({"seq": (cfg, True), "ovl": (cfg, False)}, args_, ws, a.steps, a.warmup)
+                (seq_ms, seq_st), (ovl_ms, _) = r["seq"], r["ovl"]
+                copy_ms = float(seq_st[tlc.EV_DOWN])
                 tail, span_ovl = trace_of(cfg, args_, ws, False)
                 _, span_seq = trace_of(cfg, args_, ws, True)
+                mhz = clk.median()
                 print(json.dumps({"part": "layer", "T": T, "R": R, "consumer_ctas": c,
                                   "copy_warps": bool(flags & tlc.MOE_COPY_WARPS),
                                   "pair_umma": bool(flags & tlc.MOE_PAIR_UMMA),
+                                  "direct_tail": bool(flags & tlc.MOE_DIRECT_TAIL),
                                   "overlapped_ms": round(ovl_ms, 4), "sequential_ms": round(seq_ms, 4),
                                   "copy_alone_ms": round(copy_ms, 4), "tail_ms": round(tail, 4),
                                   "hidden_pct": round(100 * (1 - tail / copy_ms), 2),
@@ -133,7 +139,10 @@ def part_layer(S: Setup, a, flags):
                                   "gemm_span_overlapped_ms": round(span_ovl, 4),
                                   "gemm_span_all_sms_ms": round(span_seq, 4),
                                   "gemm_slowdown": round(span_ovl / span_seq, 4),
-                                  "tokens_per_s": round(T / ovl_ms * 1e3, 1), "sm_mhz": clk.median()}), flush=True)
+                                  "tokens_per_s": round(T / ovl_ms * 1e3, 1), "sm_mhz": mhz,
+                                  "overlapped_mcycles": round(ovl_ms * mhz / 1e3, 3) if mhz else None,
+                                  "sequential_mcycles": round(seq_ms * mhz / 1e3, 3) if mhz else None}),
+                      flush=True)
             del ws
 
 
@@ -143,8 +152,8 @@ def part_mgb(S: Setup, a, flags):
     for mgb in a.mgbs:
         for c in a.consumers:
             cfg = tlc.Config.from_workload(w, consumer_ctas=c, flags=flags, mgb=mgb)
-            ovl_ms, _ = time_steps(cfg, args_, ws, False, a.steps, a.warmup)
-            _, seq_st = time_steps(cfg, args_, ws, True, a.steps, a.warmup)
+            r = time_arms({"seq": (cfg, True), "ovl": (cfg, False)}, args_, ws, a.steps, a.warmup)
+            (_, seq_st), (ovl_ms, _) = r["seq"], r["ovl"]
             tail, _ = trace_of(cfg, args_, ws, False)
             copy_ms = float(seq_st[tlc.EV_DOWN])
             print(json.dumps({"part": "mgb", "T": 4096, "R": 4, "mgb": mgb, "consumer_ctas": c,
@@ -195,10 +204,12 @@ def main():
     ap.add_argument("--no-tail-assist", action="store_true")
     ap.add_argument("--copy-warps", action="store_true", help="also run copy warps in the producer CTAs")
     ap.add_argument("--no-pair", action="store_true", help="single-CTA GEMMs instead of CTA pairs")
+    ap.add_argument("--direct-tail", action="store_true",
+                    help="the down-projection's epilogue returns the last wave's bands itself")
     a = ap.parse_args()
 
     flags = (0 if a.no_tail_assist else tlc.MOE_TAIL_ASSIST) | (tlc.MOE_COPY_WARPS if a.copy_warps else 0) | \
-        (0 if a.no_pair else tlc.MOE_PAIR_UMMA)
+        (0 if a.no_pair else tlc.MOE_PAIR_UMMA) | (tlc.MOE_DIRECT_TAIL if a.direct_tail else 0)
     S = Setup()
     if "copy" in a.parts:
         part_copy(S, a)
