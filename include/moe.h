@@ -75,6 +75,11 @@ extern "C" {
 #define MOE_TEST_PLAN_FAIL 0x200u     /* test hook: the plan kernel reports a failed bounds   */
                                       /* check (MOE_ERR_PLAN, detail -3) although the plan is */
                                       /* valid, to test that the status reaches the caller    */
+#define MOE_TEST_STALL_PIPE0 0x400u   /* test hooks: in the CTA-pair GEMMs the TMA thread of   */
+#define MOE_TEST_STALL_PIPE1 0x800u   /* rank 0 (PIPE0) or rank 1 (PIPE1) of every pair stops  */
+                                      /* issuing loads halfway through its first tile, so the */
+                                      /* pair's bounded waits run out (MOE_ERR_TIMEOUT) and   */
+                                      /* its abort path settles the loads still in flight     */
 
 /*
  * Problem and knobs.
@@ -128,14 +133,22 @@ typedef struct moe_layout {
     size_t ret_off;    /* int32 [R, E + 1]  exclusive prefix over e of n_{e,r}                 */
     size_t tiles;      /* int32 [MT_max, 4] (e, r, row0, valid) per M-tile, layout order       */
     size_t tile_ret;   /* int32 [MT_max]    row of Ret receiving the tile's first row          */
-    size_t sched;      /* int32 [MT_max]    M-tile at each schedule position                   */
-    size_t seg;        /* int32 [MT_max, 2] (first position, bands) of each position's segment */
-    size_t experts;    /* int32 [E, 8]      first M-tile, M-tiles, first schedule position,    */
-                       /*                   schedule rank, SwiGLU work items, first SwiGLU    */
+    size_t sched;      /* int32 [MT_max]    M-tile at each position of the remote-first        */
+                       /*                   schedule: valid rows descending, ties in layout   */
+                       /*                   order ([TLS "What carries the argument"])         */
+    size_t order;      /* int32 [MT_max]    M-tile at each position of the down-projection's   */
+                       /*                   hand-out order: the schedule re-sorted stably by  */
+                       /*                   expert, most loaded (most rows) first, ties to    */
+                       /*                   the lower id; the consumer copies in this order   */
+    size_t seg;        /* int32 [MT_max, 2] (first position, bands) of each hand-out position's */
+                       /*                   segment                                           */
+    size_t experts;    /* int32 [E, 8]      first M-tile, M-tiles, first hand-out position,    */
+                       /*                   hand-out rank, SwiGLU work items, first SwiGLU    */
                        /*                   item, first down-projection item, first Xc row    */
     size_t items_up;   /* int32 [IU_max, 2] SwiGLU work items: (first Xc row, expert), 128 rows */
-    size_t items_down; /* int32 [MT_max, 2] down-projection work items: one band, or two bands */
-                       /*                   of one expert with <= 64 valid rows each          */
+    size_t items_down; /* int32 [MT_max, 2] down-projection work items in hand-out order: one  */
+                       /*                   band, or two bands of one expert with <= 64 valid */
+                       /*                   rows each                                         */
     size_t slot;       /* int32 [T, topk]   row of pair (t, j) in Yp (padded layout)            */
     size_t cslot;      /* int32 [T, topk]   row of pair (t, j) in Xc / Hc (compact layout)      */
     size_t ret_slot;   /* int32 [T, topk]   row of pair (t, j) in Ret                          */
@@ -199,16 +212,16 @@ MOE_API int moe_plan(const moe_config* cfg, const float* logits, const uint16_t*
  *   ws     workspace as in moe_plan. Weights and x are only read; 16-byte aligned pointers.
  * Steps on `stream`: route, plan, permute, SwiGLU grouped GEMM over all experts (one persistent
  * launch), then one persistent launch in which all but consumer_ctas CTAs run the down-projection
- * GEMM, tiles handed out expert by expert in remote-first order (on CTA pairs, where one expert's W2
- * is at least 64 MB and its rows of the hidden activations at most 64 MB, the expert's tiles go N
- * tile by N tile over its bands, the last expert's band by band), and release a flag per finished
- * tile while the last consumer_ctas CTAs acquire the flags
- * and copy each ready segment of row bands into its owner's slice of Ret, then the weighted top-k
- * combine. Flags: MOE_TAIL_ASSIST (producers that finished join the copy),
+ * GEMM, tiles handed out in the hand-out order (the remote-first schedule re-sorted by expert: see
+ * moe_layout.order; on CTA pairs, where one expert's W2 is at least 64 MB and its rows of the hidden
+ * activations at most 64 MB, the expert's tiles go N tile by N tile over its bands, the last
+ * expert's band by band), and release a flag per finished tile while the last consumer_ctas CTAs
+ * acquire the flags and copy each ready segment of row bands into its owner's slice of Ret, then
+ * the weighted top-k combine. Flags: MOE_TAIL_ASSIST (producers that finished join the copy),
  * MOE_COPY_WARPS (copy engines also inside every producer CTA; consumer_ctas may be 0),
- * MOE_PAIR_UMMA (the expert GEMMs on CTA pairs); none changes the result, bit for bit. A bounded
- * wait that runs out, or a plan entry that fails its bounds check, is reported by moe_status(),
- * not here.
+ * MOE_PAIR_UMMA (the expert GEMMs on CTA pairs), MOE_DIRECT_TAIL (the last wave's bands written into
+ * Ret by the epilogue); none changes out or Ret, bit for bit. A bounded wait that runs out, or a plan
+ * entry that fails its bounds check, is reported by moe_status(), not here.
  */
 MOE_API int moe_forward(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
                         const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes,
@@ -243,6 +256,8 @@ MOE_API int moe_copy_only(const moe_config* cfg, void* ws, size_t ws_bytes, int 
  *                                                                 (overlapped: GEMM + return copy)
  *   [MOE_EV_COPIED]    after the return copy (overlapped: same point as MOE_EV_DOWN)
  *   [MOE_EV_END]       after the combine
+ * While `stream` is being captured into a CUDA graph, each record becomes an event-record node of
+ * the graph (cudaEventRecordExternal), recorded again by every replay.
  */
 #define MOE_EV_BEGIN 0
 #define MOE_EV_PLANNED 1

@@ -35,8 +35,14 @@ Readings where the page is silent (each listed in the design notes):
     silu(a) = a / (1 + exp(-a));
   * rows inside a group: ascending token id; padding rows of Xp are zero;
   * owner return buffer: packed rows, experts ascending, then group order;
-  * schedule: bands sorted by (-expert load, expert, -valid rows, owner, row);
-  * segment: up to mgb consecutive schedule positions holding adjacent bands of one
+  * schedule ("the largest remote-bound transfers earliest"): a band's transfer is its
+    valid rows (the consumer writes one row-band segment at a time); bands sorted by
+    valid rows, descending, ties kept in layout order (expert, owner, row);
+  * hand-out order: the order in which the down-projection takes the bands, derived
+    from the schedule by a stated rule (experts one after another, most loaded first,
+    each expert's bands in schedule order); not a step of the page, pinned so that the
+    order the kernels execute is checked;
+  * segment: up to mgb consecutive hand-out positions holding adjacent bands of one
     group, counted from the start of each such run.
 
 Parity pins live in tests/test_oracle_*.py: brute-force pure-Python versions on tiny
@@ -97,8 +103,9 @@ class Plan:
     ret_off[r, e] first row of (e, r) inside owner r's return slice (exclusive prefix)
     ret_row0[m]   destination row in Ret of tile m's first row
     ret_slot[t,j] row of pair (t, j) in Ret
-    sched[p]      M-tile index at schedule position p
-    seg[p]        (first position, number of bands) of the segment holding position p
+    sched[p]      M-tile at position p of the page's remote-first schedule
+    order[p]      M-tile at position p of the hand-out order derived from the schedule
+    seg[p]        (first position, number of bands) of the segment holding hand-out position p
     """
 
     T: int
@@ -115,6 +122,7 @@ class Plan:
     ret_row0: np.ndarray
     ret_slot: np.ndarray
     sched: np.ndarray
+    order: np.ndarray
     seg: np.ndarray
 
     @property
@@ -181,44 +189,64 @@ def build_plan(idx: np.ndarray, E: int, R: int, tbM: int, mgb: int = 1) -> Plan:
     tiles = np.array(tiles, dtype=np.int64).reshape(-1, 4)
     ret_row0 = np.array(ret_row0, dtype=np.int64)
 
-    sched = remote_first_schedule(tiles, n)
-    seg = segments(tiles, sched, tbM, mgb)
-    return Plan(T, E, R, k, tbM, mgb, n, off, tiles, slot, ret_off, ret_row0, ret_slot, sched, seg)
+    sched = remote_first_schedule(tiles)
+    order = handout_order(tiles, sched, n)
+    seg = segments(tiles, order, tbM, mgb)
+    return Plan(T, E, R, k, tbM, mgb, n, off, tiles, slot, ret_off, ret_row0, ret_slot, sched, order, seg)
 
 
-def remote_first_schedule(tiles: np.ndarray, n: np.ndarray) -> np.ndarray:
-    """Order of M-tiles for the producer: largest owner-bound transfers first.
+def remote_first_schedule(tiles: np.ndarray) -> np.ndarray:
+    """Order of the M-tiles (row bands): the largest owner-bound transfers first.
 
-    [TLS "What carries the argument"] and [TLS "Core claim"]: one producer covers all
-    experts, schedules remote-bound tiles first and emits the largest transfers
-    earliest. Reading: every group is owner-bound on one GPU; the producer takes the
-    experts one after another, the most loaded first (ties to the lower id), and inside
-    an expert the bands with the most valid rows first (ties to the lower owner, then
-    the lower row). Key: (-expert load, expert, -valid, owner, row).
+    [TLS "What carries the argument"]: a remote-first tile schedule emits the largest
+    remote-bound transfers earliest; [TLS "Core claim"]: the consumer issues one
+    contiguous write per row-band segment, so the transfer a band makes is its valid
+    rows over the full width. Reading: every band is owner-bound on one GPU (there is
+    no local rank); bands are sorted by valid rows, descending, and bands of equal
+    size keep their layout order (expert, owner, row).
     """
     if tiles.shape[0] == 0:
         return np.zeros(0, dtype=np.int64)
-    e, r, row0, valid = tiles[:, 0], tiles[:, 1], tiles[:, 2], tiles[:, 3]
-    load = n.sum(axis=1)[e]
-    return np.lexsort((row0, r, -valid, e, -load)).astype(np.int64)
+    valid = tiles[:, 3]
+    return np.lexsort((np.arange(tiles.shape[0]), -valid)).astype(np.int64)
 
 
-def segments(tiles: np.ndarray, sched: np.ndarray, tbM: int, mgb: int) -> np.ndarray:
+def handout_order(tiles: np.ndarray, sched: np.ndarray, n: np.ndarray) -> np.ndarray:
+    """Order in which the down-projection takes the bands, derived from the schedule.
+
+    Not a step of the page: the rule by which the producer turns the schedule into its
+    hand-out order, kept here so that the order the kernels execute is pinned too. The
+    schedule is re-sorted stably by expert, the experts taken one after another, the
+    most loaded (most real rows) first, ties to the lower expert id; inside an expert
+    the bands keep their schedule order.
+    """
+    if sched.shape[0] == 0:
+        return np.zeros(0, dtype=np.int64)
+    E = n.shape[0]
+    load = n.sum(axis=1)
+    rank = np.empty(E, dtype=np.int64)
+    rank[np.lexsort((np.arange(E), -load))] = np.arange(E)
+    e = tiles[sched, 0]
+    return sched[np.lexsort((np.arange(sched.shape[0]), rank[e]))].astype(np.int64)
+
+
+def segments(tiles: np.ndarray, order: np.ndarray, tbM: int, mgb: int) -> np.ndarray:
     """Row-band segments: up to mgb adjacent bands of one group, copied as one piece.
 
     [TLS "What carries the argument"]: a row band is a strip of output rows over the
     full width; [TLS "Axiom & Free-Parameter Ledger"]: mgb consecutive bands are
-    merged into an interior segment. Runs are maximal stretches of schedule positions
-    whose bands are in the same group with rows directly following each other; each
-    run is cut into pieces of mgb bands from its start.
+    merged into an interior segment. Runs are maximal stretches of hand-out positions
+    (the order in which bands are produced and copied) whose bands are in the same
+    group with rows directly following each other; each run is cut into pieces of mgb
+    bands from its start.
     """
-    m = len(sched)
+    m = len(order)
     seg = np.zeros((m, 2), dtype=np.int64)
     p = 0
     while p < m:
         q = p + 1
         while q < m:
-            a, b = tiles[sched[q - 1]], tiles[sched[q]]
+            a, b = tiles[order[q - 1]], tiles[order[q]]
             if a[0] != b[0] or a[1] != b[1] or b[2] != a[2] + tbM:
                 break
             q += 1

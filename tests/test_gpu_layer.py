@@ -206,13 +206,13 @@ def test_copy_only_reproduces_the_return_copy():
 
 
 def test_corrupt_plan_entry_is_reported_not_used():
-    """A schedule entry pointing past the last band makes the copy report MOE_ERR_PLAN (its bounds
-    check runs before the entry is used); the next forward re-plans and is correct again."""
+    """A hand-out order entry pointing past the last band makes the copy report MOE_ERR_PLAN (its
+    bounds check runs before the entry is used); the next forward re-plans and is correct again."""
     w = small("skew")
     L = Layer(w, seed=3)
     want = L.run(sequential=True)
     MT = int(L.ws.view("meta")[1].item())
-    L.ws.view("sched")[0] = MT + 7
+    L.ws.view("order")[0] = MT + 7
     tlc.copy_only(L.cfg, L.ws, 4)
     rc, detail = tlc.status(L.cfg, L.ws)
     assert rc == tlc.MOE_ERR_PLAN and detail == 0
@@ -259,3 +259,23 @@ def test_full_size_sampled_tokens(name):
     _, _, want = moe_ref.moe_tokens(tokens, L.logits_np, x_rows, L.weights_f64, w.topk)
     err, rel = parity(got.double().cpu().numpy()[tokens], want)
     assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,seed", [("mixtral", 0), ("skew", 3)])
+def test_full_size_every_token_against_the_oracle(name, seed):
+    """Every token of the full-size layer, in the bench's launch configuration (its copy configuration,
+    CTA-pair GEMMs, tail assist, direct tail), against the oracle's per-token definition in fp64,
+    element by element: covers every band of the down-projection's hand-out order, the N-tile-outer
+    order of the Mixtral shape and the bands the epilogue returns itself."""
+    import bench
+    w = inputs.WORKLOADS[name]
+    c, warps = bench.DEFAULT_COPY[name]
+    L = Layer(w, seed=seed, cfg_kw=dict(consumer_ctas=c, flags=bench.default_flags(warps)))
+    got = L.run(sequential=False).double().cpu().numpy()
+    idx, _, want = moe_ref.moe_tokens(np.arange(w.T), L.logits_np, inputs.bf16_to_f64(L.x_cpu), L.weights_f64,
+                                      w.topk)
+    np.testing.assert_array_equal(L.ws.view("idx").cpu().numpy(), idx)
+    err, rel = parity(got, want)
+    assert err <= MAX_ABS and rel <= REL_L2, (err, rel)
+    assert per_token_rel_distance(got, want).max() < 5e-2

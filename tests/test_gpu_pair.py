@@ -177,3 +177,22 @@ def test_pair_down_stalled_consumer_times_out_and_context_survives():
     assert rc == tlc.MOE_ERR_TIMEOUT
     cfg_ok = tlc.Config.from_workload(w, consumer_ctas=4, flags=PAIR)
     assert torch.equal(L.run(sequential=False, cfg=cfg_ok), want)
+
+
+@pytest.mark.parametrize("hook", [tlc.MOE_TEST_STALL_PIPE0, tlc.MOE_TEST_STALL_PIPE1], ids=["rank0", "rank1"])
+@pytest.mark.parametrize("sequential", [False, True])
+def test_pair_pipeline_abort_settles_loads_and_context_survives(hook, sequential):
+    """One CTA of every pair stops issuing its TMA loads halfway through its first tile (rank 0: its
+    peer runs up to a ring of stages ahead; rank 1: rank 0 arms stages whose peer bytes never come).
+    The pair's bounded waits run out, the status says so, the abort path settles every load still in
+    flight before either CTA leaves, and the next call on the same context is correct."""
+    w = small("mixtral")  # d % 256 == 0: both GEMMs run on CTA pairs
+    L = Layer(w, seed=0)
+    want = L.run(sequential=True)
+    cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=PAIR | hook, timeout_us=20000)
+    tlc.forward(cfg, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws, sequential=sequential)
+    rc, _ = tlc.status(cfg, L.ws)
+    assert rc == tlc.MOE_ERR_TIMEOUT
+    assert "timed out" in tlc.lib().moe_last_error().decode()
+    cfg_ok = tlc.Config.from_workload(w, consumer_ctas=4, flags=PAIR | tlc.MOE_TAIL_ASSIST)
+    assert torch.equal(L.run(sequential=sequential, cfg=cfg_ok), want)

@@ -1,7 +1,8 @@
 """Routing, plan and permute on the GPU, bit-exact against the oracle.
 
-Indices, counts, offsets, tile-owner map, schedule, segments, slots, return slots and the permuted
-rows (with zero padding) have exactly one correct value each, so they are compared for equality.
+Indices, counts, offsets, tile-owner map, schedule, hand-out order, segments, slots, return slots and
+the permuted rows (with zero padding) have exactly one correct value each, so they are compared for
+equality.
 The permuted rows are checked in the expert-compact layout of the GEMM inputs, whose rows follow
 from the oracle's plan (tests.gpu_util.compact_layout).
 """
@@ -46,6 +47,7 @@ def check_plan(w, logits_np, x_cpu, mgb=1):
     np.testing.assert_array_equal(v("tiles")[:MT], plan.tiles)
     np.testing.assert_array_equal(v("tile_ret")[:MT], plan.ret_row0)
     np.testing.assert_array_equal(v("sched")[:MT], plan.sched)
+    np.testing.assert_array_equal(v("order")[:MT], plan.order)
     np.testing.assert_array_equal(v("seg")[:MT], plan.seg)
     np.testing.assert_array_equal(v("slot"), plan.slot)
     np.testing.assert_array_equal(v("ret_slot"), plan.ret_slot)
@@ -129,7 +131,8 @@ def test_plan_skip_permute_leaves_xp_untouched():
 @pytest.mark.parametrize("name", ["tiny", "mixtral", "skew", "fine"])
 def test_work_items_cover_every_band_once(name):
     """Down-projection work items: every band in exactly one item; a shared item holds two bands of
-    the same expert that each need at most 64 rows; the list follows the schedule. SwiGLU work items
+    the same expert that each need at most 64 rows; the list follows the hand-out order, and the
+    band -> item map is its inverse. SwiGLU work items
     cover every real row of the compact layout once, 128 rows of one expert each, and are never more
     than the down-projection's."""
     w = inputs.WORKLOADS[name]
@@ -137,10 +140,12 @@ def test_work_items_cover_every_band_once(name):
     meta = ws.view("meta").cpu().numpy()
     MT, NI, NU, PC = int(meta[1]), int(meta[7]), int(meta[8]), int(meta[9])
     tiles = ws.view("tiles").cpu().numpy()[:MT]
-    sched = ws.view("sched").cpu().numpy()[:MT]
+    order = ws.view("order").cpu().numpy()[:MT]
+    band_item = ws.view("band_item").cpu().numpy()[:MT]
     items = ws.view("items_down").cpu().numpy()[:NI]
     seen = []
-    for a, b in items.tolist():
+    for i, (a, b) in enumerate(items.tolist()):
+        assert band_item[a] == i and (b < 0 or band_item[b] == i)
         seen.append(a)
         if b == a:
             assert w.tile_M == 128
@@ -149,7 +154,7 @@ def test_work_items_cover_every_band_once(name):
         else:
             seen.append(b)
             assert tiles[a, 0] == tiles[b, 0] and tiles[a, 3] <= 64 and tiles[b, 3] <= 64
-    assert seen == sched.tolist() and sorted(seen) == list(range(MT))
+    assert seen == order.tolist() and sorted(seen) == list(range(MT))
     # two half bands cut the GEMM work wherever partial bands are small
     assert NI <= MT and (w.tile_M == 128 or NI == (MT + 1) // 2 or NI < MT)
     up = ws.view("items_up").cpu().numpy()[:NU]

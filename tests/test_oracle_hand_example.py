@@ -11,8 +11,9 @@ Routing (descending logit, ties to the lower id):
 Groups (pairs (t, j), ascending t): e0r0 (0,0)(2,0); e0r1 (4,0)(6,0)(7,1); e1r0 (1,0)(2,1)(3,1);
   e1r1 (4,1)(5,0)(6,1); e2r0 (0,1)(1,1)(3,0); e2r1 (5,1)(7,0).
 Padded sizes 2,4,4,4,4,2 -> offsets 0,2,6,10,14,18,20.
-Expert loads 5, 6, 5 -> expert order e1, e0, e2; inside each expert full bands first (in layout
-order), then partial bands by valid rows (ties to the lower owner).
+Schedule (largest transfers first): the six full bands m0 m1 m3 m5 m7 m9 (2 rows each, layout
+order), then the four 1-row bands m2 m4 m6 m8.
+Hand-out order: expert loads 5, 6, 5 -> experts e1, e0, e2, each expert's bands in schedule order.
 """
 import math
 
@@ -43,9 +44,11 @@ def test_hand_example_layout():
     assert p.ret_off.tolist() == [[0, 2, 5, 8], [0, 3, 6, 8]]
     assert p.ret_slot.tolist() == [[0, 5], [2, 6], [1, 3], [7, 4], [8, 11], [12, 14], [9, 13], [15, 10]]
     assert p.ret_row0.tolist() == [0, 8, 10, 2, 4, 11, 13, 5, 7, 14]
-    # e1: full m3, m5, partial m4, m6; e0: full m0, m1, partial m2; e2: full m7, m9, partial m8
-    assert p.sched.tolist() == [3, 5, 4, 6, 0, 1, 2, 7, 9, 8]
-    # m1 (rows 2-3) and m2 (row 4) are adjacent bands of group e0r1 -> one segment of 2 bands
+    assert p.sched.tolist() == [0, 1, 3, 5, 7, 9, 2, 4, 6, 8]
+    # e1: m3, m5 (full), m4, m6; e0: m0, m1, m2; e2: m7, m9, m8
+    assert p.order.tolist() == [3, 5, 4, 6, 0, 1, 2, 7, 9, 8]
+    # in hand-out order m1 (rows 2-3) and m2 (row 4) are adjacent bands of group e0r1 -> one
+    # segment of 2 bands
     assert p.seg.tolist() == [[0, 1], [1, 1], [2, 1], [3, 1], [4, 1], [5, 2], [5, 2], [7, 1], [8, 1], [9, 1]]
 
 
@@ -55,5 +58,5 @@ def test_hand_example_segments():
     idx, _ = ref.route_topk(logits, 1)
     p = ref.build_plan(idx, 2, 1, 1, mgb=2)
     assert p.slot.tolist() == [[0], [3], [1], [2]]
-    assert p.sched.tolist() == [0, 1, 2, 3]
+    assert p.sched.tolist() == [0, 1, 2, 3] and p.order.tolist() == [0, 1, 2, 3]
     assert p.seg.tolist() == [[0, 2], [0, 2], [2, 1], [3, 1]]

@@ -107,8 +107,9 @@ def check_invariants(plan, idx):
     assert np.array_equal(np.sort(rs), np.arange(T * k))
     slice_rows = (T // R) * k
     assert np.all(rs // slice_rows == own[np.repeat(np.arange(T), k)])
-    # schedule: a permutation of the tiles
+    # schedule and hand-out order: permutations of the tiles
     assert np.array_equal(np.sort(plan.sched), np.arange(plan.num_tiles))
+    assert np.array_equal(np.sort(plan.order), np.arange(plan.num_tiles))
 
 
 @pytest.mark.parametrize("name", ["tiny", "mixtral", "skew", "fine"])
@@ -131,13 +132,25 @@ def test_skew_has_empty_groups_and_invariants_hold():
 
 
 def brute_schedule(plan):
-    load = plan.n.sum(1)
-    keys = [(-load[t[0]], t[0], -t[3], t[1], t[2]) for t in plan.tiles.tolist()]
+    """Largest transfer (valid rows) first, ties in layout order: a pure-Python sort on the key."""
+    keys = [(-t[3], t[0], t[1], t[2]) for t in plan.tiles.tolist()]
     return sorted(range(len(keys)), key=lambda m: keys[m])
 
 
+def brute_order(plan):
+    """Hand-out order: experts by (load descending, id), each expert's bands in schedule order;
+    written as nested loops over experts, not as a sort of the schedule."""
+    load = [sum(row) for row in plan.n.tolist()]
+    experts = sorted(range(plan.E), key=lambda e: (-load[e], e))
+    sched = brute_schedule(plan)
+    out = []
+    for e in experts:
+        out += [m for m in sched if plan.tiles[m][0] == e]
+    return out
+
+
 def brute_segments(plan, mgb):
-    s = plan.sched
+    s = plan.order
     T = plan.tiles
 
     def adjacent(p, q):
@@ -166,18 +179,21 @@ def test_schedule_and_segments_bruteforce(mgb, seed):
     idx = np.stack([rng.choice(E, size=k, replace=False, p=[.5, .2, .15, .1, .05]) for _ in range(T)])
     plan = ref.build_plan(idx.astype(np.int32), E, R, tbM, mgb)
     assert plan.sched.tolist() == brute_schedule(plan)
+    assert plan.order.tolist() == brute_order(plan)
     assert [tuple(v) for v in plan.seg.tolist()] == brute_segments(plan, mgb)
-    # experts one after another, most loaded first; inside an expert full bands before
-    # partial ones; segments never span groups
-    e = plan.tiles[plan.sched, 0]
+    # the schedule: transfer sizes never grow along it
+    assert np.all(np.diff(plan.tiles[plan.sched, 3]) <= 0)
+    # the hand-out order: experts one after another, most loaded first; inside an expert full
+    # bands before partial ones; segments never span groups
+    e = plan.tiles[plan.order, 0]
     assert all(len(set(e[i:].tolist()) & set(e[:i].tolist())) == 0 for i in range(1, len(e)) if e[i] != e[i - 1])
     load = plan.n.sum(1)[e]
     assert np.all(np.diff(load) <= 0)
     for x in np.unique(e):
-        assert np.all(np.diff(plan.tiles[plan.sched[e == x], 3]) <= 0)
+        assert np.all(np.diff(plan.tiles[plan.order[e == x], 3]) <= 0)
     for p, (first, ln) in enumerate(plan.seg.tolist()):
-        assert first <= p < first + ln <= len(plan.sched) and 1 <= ln <= mgb
-        grp = {tuple(plan.tiles[plan.sched[q], :2]) for q in range(first, first + ln)}
+        assert first <= p < first + ln <= len(plan.order) and 1 <= ln <= mgb
+        grp = {tuple(plan.tiles[plan.order[q], :2]) for q in range(first, first + ln)}
         assert len(grp) == 1
 
 
@@ -207,3 +223,23 @@ def test_empty_routing_degenerate_cases():
     plan = ref.build_plan(idx, 3, 2, 2)
     assert plan.n[1:].sum() == 0 and set(plan.tiles[:, 0].tolist()) == {0}
     assert plan.off.tolist() == [0, 4, 8, 8, 8, 8, 8]
+
+
+@pytest.mark.parametrize("mutation", ["smallest_first", "ties_reversed", "least_loaded_first"])
+def test_schedule_pins_catch_planted_mistakes(monkeypatch, mutation):
+    """A planted schedule or hand-out order mistake must fail the brute-force pins."""
+    rng = np.random.default_rng(31)
+    T, E, k, R, tbM = 96, 5, 2, 3, 8
+    idx = np.stack([rng.choice(E, size=k, replace=False, p=[.5, .2, .15, .1, .05]) for _ in range(T)])
+    orig_order = ref.handout_order
+    if mutation == "smallest_first":
+        monkeypatch.setattr(ref, "remote_first_schedule",
+                            lambda tiles: np.lexsort((np.arange(len(tiles)), tiles[:, 3])))
+    elif mutation == "ties_reversed":
+        monkeypatch.setattr(ref, "remote_first_schedule",
+                            lambda tiles: np.lexsort((-np.arange(len(tiles)), -tiles[:, 3])))
+    else:
+        monkeypatch.setattr(ref, "handout_order",
+                            lambda tiles, sched, n: orig_order(tiles, sched, -n))
+    plan = ref.build_plan(idx.astype(np.int32), E, R, tbM, 1)
+    assert not (plan.sched.tolist() == brute_schedule(plan) and plan.order.tolist() == brute_order(plan))

@@ -31,6 +31,8 @@ MOE_PAIR_UMMA = 0x8
 MOE_DIRECT_TAIL = 0x10
 MOE_TEST_STALL_CONSUMER = 0x100
 MOE_TEST_PLAN_FAIL = 0x200
+MOE_TEST_STALL_PIPE0 = 0x400
+MOE_TEST_STALL_PIPE1 = 0x800
 
 TRACE_GEMM2_START, TRACE_GEMM2_END, TRACE_COPY_START, TRACE_COPY_END = 0, 1, 2, 3
 TRACE_BAND_DONE, TRACE_LAST_ACQUIRE, TRACE_LAST_LOAD, TRACE_LAST_DRAIN = 4, 5, 6, 7
@@ -59,7 +61,7 @@ class _Config(ctypes.Structure):
 _LAYOUT_INTS = ("P_max", "MT_max", "n_chunks", "chunk_tokens", "n_tiles_n2", "block_n2", "rows_per_unit",
                 "units_per_band", "PC_max", "IU_max")
 LAYOUT_REGIONS = ("idx", "gate", "rank", "chunk_cnt", "chunk_base", "counts", "offsets", "ret_off", "tiles",
-                  "tile_ret", "sched", "seg", "experts", "items_up", "items_down", "slot", "cslot", "ret_slot", "ccoff",
+                  "tile_ret", "sched", "order", "seg", "experts", "items_up", "items_down", "slot", "cslot", "ret_slot", "ccoff",
                   "tile_crow", "band_item", "meta", "flags", "bands", "trace", "Xc", "Hc", "Yp", "Ret", "in_logits", "in_x", "out")
 
 
@@ -175,7 +177,8 @@ class Workspace:
            "counts": (torch.int32, "ER"), "ccoff": (torch.int32, "ER"), "tile_crow": (torch.int32, "MT"),
            "band_item": (torch.int32, "MT"),
            "offsets": (torch.int32, "G1"), "ret_off": (torch.int32, "RE1"), "tiles": (torch.int32, "MT4"),
-           "tile_ret": (torch.int32, "MT"), "sched": (torch.int32, "MT"), "seg": (torch.int32, "MT2"),
+           "tile_ret": (torch.int32, "MT"), "sched": (torch.int32, "MT"), "order": (torch.int32, "MT"),
+           "seg": (torch.int32, "MT2"),
            "experts": (torch.int32, "E8"), "items_up": (torch.int32, "IU2"),
            "items_down": (torch.int32, "MT2"), "meta": (torch.int32, "META"), "flags": (torch.int32, "FL"),
            "bands": (torch.int32, "MT"),

@@ -12,8 +12,9 @@
 // flight, also across unit boundaries. SIMT engine (copy_units_simt): one warp moving rows through
 // registers with 16-byte loads and stores, no shared memory, for the extra warps of producer CTAs.
 //
-// Work units: band (schedule position) x row chunk of rows_per_unit rows, handed out in schedule
-// order by an atomic counter, so idle engines always take the oldest outstanding band.
+// Work units: band (hand-out position) x row chunk of rows_per_unit rows, handed out in the
+// down-projection's hand-out order by an atomic counter, so idle engines always take the oldest
+// outstanding band.
 #pragma once
 
 #include "moe_internal.cuh"
@@ -85,11 +86,11 @@ __device__ __forceinline__ void engine_drain(CopyEngine& ce, unsigned long long 
 // band of the unit's segment (== want: all tiles of the band published) before copying. An engine
 // claims its next unit only once the current one is acquired (never while it waits on a band), and
 // the next unit's counters are polled while the previous unit's pieces are still in flight.
-// Bounds check of the plan entries one copy unit reads (schedule position pos -> band m, its rows
+// Bounds check of the plan entries one copy unit reads (hand-out position pos -> band m, its rows
 // in Yp and Ret, and the bands of its segment). A failure is reported as ST_BAD_PLAN and the copy
 // stops, so a corrupt plan never turns into an out-of-range access.
 __device__ __forceinline__ bool copy_unit_ok(const Shape& s, const PlanPtrs& p, int MT, int pos, bool wait_flags) {
-    const int m = p.sched[pos];
+    const int m = p.order[pos];
     if (m < 0 || m >= MT) return false;
     const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3], ret0 = p.tile_ret[m];
     if (valid < 1 || valid > s.tbM || row0 < 0 || row0 + valid > s.P_max || ret0 < 0 || ret0 + valid > s.T * s.k)
@@ -98,7 +99,7 @@ __device__ __forceinline__ bool copy_unit_ok(const Shape& s, const PlanPtrs& p, 
         const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
         if (first < 0 || nb < 1 || nb > s.mgb || first + nb > MT) return false;
         for (int i = 0; i < nb; ++i) {
-            const int b = p.sched[first + i];
+            const int b = p.order[first + i];
             if (b < 0 || b >= MT) return false;
         }
     }
@@ -134,7 +135,7 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
             }
             break;
         }
-        const int m = p.sched[pos];
+        const int m = p.order[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
         if (rb >= valid || p.band_item[m] >= skip_item) {
             if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
@@ -148,8 +149,8 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
             if (lane == 0) {
                 const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
                 for (int i = 0; i < nb && !failed; ++i) {
-                    if (p.band_item[p.sched[first + i]] >= skip_item) continue;  // returned by the epilogue
-                    const uint32_t* bc = p.bands + p.sched[first + i];
+                    if (p.band_item[p.order[first + i]] >= skip_item) continue;  // returned by the epilogue
+                    const uint32_t* bc = p.bands + p.order[first + i];
                     if (ld_acquire_gpu(bc) == want) continue;
                     if (!engine_flush(ce, s.timeout_ns, s_abort)) {
                         *s_abort = 1;
@@ -167,7 +168,7 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
                         }
                         if (globaltimer() - t0 > s.timeout_ns) {
                             *s_abort = 1;
-                            set_status(p.meta, ST_FLAG_TIMEOUT, p.sched[first + i]);
+                            set_status(p.meta, ST_FLAG_TIMEOUT, p.order[first + i]);
                             failed = true;
                             break;
                         }
@@ -253,7 +254,7 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
             }
             break;
         }
-        const int m = p.sched[pos];
+        const int m = p.order[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
         if (rb >= valid || p.band_item[m] >= skip_item) {
             if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
@@ -264,8 +265,8 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
         if (lane == 0) {
             const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
             for (int i = 0; i < nb && !failed; ++i) {
-                if (p.band_item[p.sched[first + i]] >= skip_item) continue;  // returned by the epilogue
-                const uint32_t* bc = p.bands + p.sched[first + i];
+                if (p.band_item[p.order[first + i]] >= skip_item) continue;  // returned by the epilogue
+                const uint32_t* bc = p.bands + p.order[first + i];
                 if (ld_acquire_gpu(bc) == want) continue;
                 const unsigned long long t0 = globaltimer();
                 for (unsigned ns = 64;; ns = ns < 512 ? 2 * ns : ns) {
@@ -277,7 +278,7 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
                     }
                     if (globaltimer() - t0 > s.timeout_ns) {
                         *s_abort = 1;
-                        set_status(p.meta, ST_FLAG_TIMEOUT, p.sched[first + i]);
+                        set_status(p.meta, ST_FLAG_TIMEOUT, p.order[first + i]);
                         failed = true;
                         break;
                     }

@@ -138,7 +138,8 @@ __device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, const
     return compact_ref(items[2 * it], n, e);
 }
 
-// Down-projection order: work items in schedule (remote-first) order, all N tiles of an item together.
+// Down-projection order: work items in hand-out order (the remote-first schedule re-sorted by expert),
+// all N tiles of an item together.
 __device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* items, const int32_t* tiles,
                                                const int32_t* crow) {
     const int it = t / nN;
@@ -604,7 +605,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 //   MODE 2 (down-projection): rank 0 stages rows 0-127 of the 256-row W2 tile, rank 1 rows
 //       128-255; each CTA's item is one band (or two half bands) of the page's padded layout, and
 //       its epilogue publishes the band flags as in gemm_kernel. Work items of an expert in pairs,
-//       in schedule order, all N tiles of a pair item together. Consumer CTAs (the last
+//       in hand-out order, all N tiles of a pair item together. Consumer CTAs (the last
 //       consumer_ctas blocks, whole clusters) and, with tail assist, finished producer CTAs run the
 //       bulk copy engines.
 // An expert with an odd number of work items leaves rank 1 without rows in its last pair tile: it
@@ -641,9 +642,10 @@ struct PairSmem {
     uint64_t* cbar;      // copy engines (down-projection consumers and tail assist)
     uint32_t* tmem_base;
     uint32_t* peer_base;
+    volatile uint32_t* peer_k;  // rank 0: k-blocks rank 1's TMA thread issued (abort path)
     volatile int* abort;
     volatile int* tq;
-    int* tab;  // [cum (E+1) | first item (E) | items (E)]
+    int* tab;  // [cum (E+1) | first item (E) | items (E) | first direct item]
 };
 
 __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
@@ -663,7 +665,8 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
     sm.cbar = sm.tq_empty + PAIR_TILE_Q;
     sm.tmem_base = reinterpret_cast<uint32_t*>(sm.cbar + COPY_NBUF);
     sm.peer_base = sm.tmem_base + 1;
-    sm.abort = reinterpret_cast<volatile int*>(sm.peer_base + 1);
+    sm.peer_k = sm.peer_base + 1;
+    sm.abort = reinterpret_cast<volatile int*>(const_cast<uint32_t*>(sm.peer_k) + 1);
     sm.tq = sm.abort + 1;
     sm.tab = const_cast<int*>(sm.tq + PAIR_TILE_Q);
     return sm;
@@ -685,6 +688,28 @@ __device__ __forceinline__ int pair_tile_wait(const PairSmem& sm, int j, unsigne
 __device__ __forceinline__ void pair_abort(const PairSmem& sm, uint32_t rank) {
     *sm.abort = 1;
     st_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(sm.abort)), rank ^ 1u), 1u);
+}
+
+// Abort path of a pair (rank 0's TMA thread, after both CTAs have stopped issuing): no TMA load of the
+// pair may still be in flight when either CTA leaves. Both TMA threads walk the same sequence of
+// k-blocks (stage i % PAIR_STAGES, phase (i / PAIR_STAGES) & 1): rank 0 arms k-block i's full
+// barrier with both CTAs' bytes and issues its own loads, rank 1's loads complete on that barrier.
+// `a` k-blocks were armed and loaded by rank 0, `b` loaded by rank 1; the two differ by at most
+// PAIR_STAGES, and every k-block below min(a, b) got both. For i in [b, a) rank 1's bytes never come:
+// they are completed without a copy; for i in [a, b) rank 0 never armed the phase: it arrives now,
+// expecting rank 1's bytes. Then every barrier's last phase is waited for (bounded): a phase completes
+// only when all of its loads have landed, and earlier phases completed before it.
+__device__ __forceinline__ void pair_settle(const PairSmem& sm, uint32_t a, uint32_t b, unsigned long long tmo) {
+    const uint32_t peer_bytes = PAIR_A_BYTES + PAIR_B_BYTES;  // rank 1's loads of one k-block
+    const uint32_t lo = a < b ? a : b, hi = a < b ? b : a;
+    for (uint32_t i = lo; i < hi; ++i) {
+        uint64_t* bar = &sm.full[i % PAIR_STAGES];
+        if (i < a) mbar_complete_tx(bar, peer_bytes);
+        else mbar_arrive_expect_tx(bar, peer_bytes);
+    }
+    int never = 0;
+    for (uint32_t i = hi > (uint32_t)PAIR_STAGES ? hi - PAIR_STAGES : 0u; i < hi; ++i)
+        mbar_wait(&sm.full[i % PAIR_STAGES], (i / PAIR_STAGES) & 1u, tmo, &never);
 }
 
 // Largest e with cum[e] <= t (cum non-decreasing, cum[0] = 0 <= t).
@@ -720,7 +745,7 @@ __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, 
     return compact_ref(items[2 * item], n, e);
 }
 
-// Pair tile t -> this CTA's band(s) (MODE 2). tab lists the experts in schedule order (first
+// Pair tile t -> this CTA's band(s) (MODE 2). tab lists the experts in hand-out order (first
 // down-projection item, items); the expert's items in pairs, all nN tiles of a pair item together
 // (band first), or, for an expert of at most n_outer_items items, one N tile of all its pair items
 // after another, except for the last expert, whose bands then still complete one after another
@@ -812,8 +837,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             sm.tab[s.E] = acc;
         }
     } else if (tid == 0) {
-        // experts in schedule order: each expert's down-projection items are contiguous in the item
-        // list, experts in schedule order, so sorting the first items (0 <= first <= NI, checked by
+        // experts in hand-out order: each expert's down-projection items are contiguous in the item
+        // list, experts in hand-out order, so sorting the first items (0 <= first <= NI, checked by
         // plan_items_bad) gives the order and the item counts
         int* first = sm.tab + (s.E + 1);
         int* count = first + s.E;
@@ -880,6 +905,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     int* const tile_counter = &p.meta[(MODE == 1) ? META_TILES_UP : META_TILES_DOWN];
     unsigned long long last_end = 0;
     const int direct_from = (MODE == 2) ? sm.tab[3 * s.E + 1] : INT_MAX;
+    uint32_t nk = 0;  // TMA thread: k-blocks whose loads this CTA issued (rank 0: armed and issued)
 
     if (producer) {
         if (warp == 0 && lane == 0) {
@@ -888,8 +914,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             // complete on that barrier (cta_group::2), so the UMMA issuer waits on one barrier per
             // stage.
             int st = 0;
-            uint32_t ph = 0, issued = 0, last_ph = 0;
+            uint32_t ph = 0;
             bool ok = true;
+            const bool stall = (s.flags & (rank == 0 ? MOE_TEST_STALL_PIPE0 : MOE_TEST_STALL_PIPE1)) != 0;
             const int claim_kb = KB > 8 ? KB - 8 : 0;
             int t = (rank == 0 && !bad) ? atomicAdd(tile_counter, 1) : 0;
             for (int j = 0; ok && !bad; ++j) {
@@ -922,6 +949,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
                 int next = total;
                 for (int kb = 0; kb < KB; ++kb) {
+                    if (stall && j == 0 && kb == KB / 2) {
+                        // test hook: this CTA stops issuing, as a stuck load stream would; the
+                        // pair's bounded waits run out and the abort path settles what is in flight
+                        const unsigned long long t0 = globaltimer();
+                        while (!*sm.abort && globaltimer() - t0 < tmo) __nanosleep(1000);
+                        ok = false;
+                        break;
+                    }
                     if (rank == 0 && kb == claim_kb) next = atomicAdd(tile_counter, 1);
                     if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
                         ok = false;
@@ -950,8 +985,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         }
                         tma_load_3d_pair(b, &tmB1, full0, kb * BK, brow, tr.e);  // up rows / W2 rows 128-255
                     }
-                    issued |= 1u << st;
-                    last_ph = (last_ph & ~(1u << st)) | (ph << st);
+                    ++nk;
                     if (++st == PAIR_STAGES) {
                         st = 0;
                         ph ^= 1u;
@@ -959,20 +993,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 }
                 if (rank == 0) t = next;
             }
-            if (!ok) {
+            if (!ok) {  // the loads still in flight are settled below, once both CTAs have stopped
                 if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 10 + (int)rank);
                 pair_abort(sm, rank);
-                // let loads in flight land before the CTA leaves: rank 0 waits on its barriers;
-                // rank 1's complete on rank 0's, so it waits a fixed 50 us (a tile load takes a
-                // few us)
-                int never = 0;
-                if (rank == 0) {
-                    for (int i = 0; i < PAIR_STAGES; ++i)
-                        if (issued & (1u << i)) mbar_wait(&sm.full[i], (last_ph >> i) & 1u, tmo, &never);
-                } else if (issued) {
-                    const unsigned long long t0 = globaltimer();
-                    while (globaltimer() - t0 < 50000ull) __nanosleep(1000);
-                }
             }
         } else if (warp == 1 && lane == 0) {
             int st = 0;
@@ -1108,6 +1131,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         __syncwarp();
         tc_fence_before();
         cluster_sync();  // both CTAs: all roles done, all UMMAs complete (drain), no remote access left
+        // Every abort word write (pair_abort sets both CTAs') came before that barrier, so both CTAs
+        // take this branch or neither. Rank 1 hands its count of issued k-blocks to rank 0, which
+        // settles every load still in flight before either CTA goes on.
+        if (*sm.abort) {
+            if (warp == 0 && lane == 0 && rank == 1)
+                st_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(sm.peer_k)), 0u), nk);
+            cluster_sync();
+            if (warp == 0 && lane == 0 && rank == 0) pair_settle(sm, nk, *sm.peer_k, tmo);
+            cluster_sync();
+        }
         if (warp == 1) {
             __syncwarp();
             tc_fence_after();

@@ -104,6 +104,7 @@ int make_layout(const moe_config* c, Layout* out) {
     L.tiles = put(MT_max * 16);
     L.tile_ret = put(MT_max * 4);
     L.sched = put(MT_max * 4);
+    L.order = put(MT_max * 4);
     L.seg = put(MT_max * 8);
     L.experts = put(E * 32);
     L.items_up = put(IU_max * 8);
@@ -177,6 +178,7 @@ PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     p.tiles = reinterpret_cast<int32_t*>(b + L.tiles);
     p.tile_ret = reinterpret_cast<int32_t*>(b + L.tile_ret);
     p.sched = reinterpret_cast<int32_t*>(b + L.sched);
+    p.order = reinterpret_cast<int32_t*>(b + L.order);
     p.seg = reinterpret_cast<int32_t*>(b + L.seg);
     p.experts = reinterpret_cast<int32_t*>(b + L.experts);
     p.items_up = reinterpret_cast<int32_t*>(b + L.items_up);
@@ -292,9 +294,17 @@ int run_plan(Call& c, const float* logits, const uint16_t* x, bool permute) {
     return MOE_OK;
 }
 
+// Records a caller's stage event. While `st` is being captured into a CUDA graph the record becomes
+// an event-record node of the graph (cudaEventRecordExternal), so every replay records it: timing a
+// graph of several steps then gives each kernel's duration inside the replayed region.
 int record(void* const* ev, int i, cudaStream_t st) {
     if (!ev || !ev[i]) return MOE_OK;
-    const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e == cudaSuccess)
+        e = (cs == cudaStreamCaptureStatusActive)
+                ? cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), st, cudaEventRecordExternal)
+                : cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
     return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaEventRecord of a stage event");
 }
 
@@ -370,8 +380,8 @@ namespace {
 
 // Offsets of the plan's scratch regions inside the static array for one config (256-byte aligned).
 struct StaticLayout {
-    size_t rank, cnt, base, counts, ret, tiles, tret, sched, seg, exp, iu, id, meta, flags, bands, trace, cslot,
-        ccoff, tcrow, bitem, bytes;
+    size_t rank, cnt, base, counts, ret, tiles, tret, sched, order, seg, exp, iu, id, meta, flags, bands, trace,
+        cslot, ccoff, tcrow, bitem, bytes;
 };
 
 StaticLayout static_layout(const Layout& lay) {
@@ -393,6 +403,7 @@ StaticLayout static_layout(const Layout& lay) {
     o.tiles = put(MT * 16);
     o.tret = put(MT * 4);
     o.sched = put(MT * 4);
+    o.order = put(MT * 4);
     o.seg = put(MT * 8);
     o.exp = put(E * 32);
     o.iu = put((size_t)L.IU_max * 8);
@@ -788,6 +799,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.tiles = reinterpret_cast<int32_t*>(b + o.tiles);
     p.tile_ret = reinterpret_cast<int32_t*>(b + o.tret);
     p.sched = reinterpret_cast<int32_t*>(b + o.sched);
+    p.order = reinterpret_cast<int32_t*>(b + o.order);
     p.seg = reinterpret_cast<int32_t*>(b + o.seg);
     p.experts = reinterpret_cast<int32_t*>(b + o.exp);
     p.items_up = reinterpret_cast<int32_t*>(b + o.iu);

@@ -99,12 +99,13 @@ struct PlanPtrs {
     int32_t* ret_off;
     int32_t* tiles;      // [MT_max][4]
     int32_t* tile_ret;
-    int32_t* sched;
-    int32_t* seg;        // [MT_max][2]
-    int32_t* experts;    // [E][8]: first M-tile, M-tiles, first schedule position, schedule rank,
+    int32_t* sched;      // remote-first schedule (bands by valid rows, descending)
+    int32_t* order;      // hand-out order of the down-projection and the copy (band at each position)
+    int32_t* seg;        // [MT_max][2] segment of each hand-out position
+    int32_t* experts;    // [E][8]: first M-tile, M-tiles, first hand-out position, hand-out rank,
                          //         SwiGLU items, first SwiGLU item, first down item, first Xc row
     int32_t* items_up;   // [IU_max][2] SwiGLU work items (first Xc row, expert), experts in id order
-    int32_t* items_down; // [MT_max][2] work items of the down-projection, in schedule order
+    int32_t* items_down; // [MT_max][2] work items of the down-projection, in hand-out order
     int32_t* slot;       // padded-layout row (Yp) of each (token, choice)
     int32_t* cslot;      // compact-layout row (Xc, Hc) of each (token, choice)
     int32_t* ret_slot;
@@ -161,13 +162,13 @@ cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUten
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
 
-// Copy units of a call with MT bands: the last min(tail_bands, MT) bands in schedule order are cut
+// Copy units of a call with MT bands: the last min(tail_bands, MT) bands in hand-out order are cut
 // into smaller units than the others, so the copy after the last tile spreads over more engines.
 __host__ __device__ inline int copy_unit_count(const Shape& s, int MT) {
     const int tb = MT < s.tail_bands ? MT : s.tail_bands;
     return (MT - tb) * s.units_per_band + tb * s.units_per_band_tail;
 }
-// Unit u -> (schedule position, first row within the band, rows per unit of that band).
+// Unit u -> (hand-out position, first row within the band, rows per unit of that band).
 __host__ __device__ inline void copy_unit_decode(const Shape& s, int MT, int u, int* pos, int* rb, int* rpu) {
     const int tb = MT < s.tail_bands ? MT : s.tail_bands;
     const int lead = (MT - tb) * s.units_per_band;
@@ -214,6 +215,11 @@ __device__ __forceinline__ void mbar_fence_init() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+// Complete `bytes` transaction bytes on `bar` without a copy: settles a phase that expects bytes of
+// loads that were never issued.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");

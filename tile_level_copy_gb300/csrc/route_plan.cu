@@ -215,7 +215,7 @@ cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p,
 // plan_kernel: one CTA of 1024 threads builds the whole plan from the per-chunk counts.
 // ---------------------------------------------------------------------------------------------
 constexpr int PLAN_THREADS = 1024;
-constexpr int PLAN_SMEM_TILES = 16384;  // tiles whose schedule and group fit in shared memory (128 KB)
+constexpr int PLAN_SMEM_TILES = 16384;  // tiles whose hand-out order and group fit in shared memory (128 KB)
 
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* s_total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -251,9 +251,11 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     __shared__ int s_erank[MAX_E];   // position of the expert in (load desc, id asc) order
     __shared__ int s_fb[MAX_E];      // full bands per expert
     __shared__ int s_mt[MAX_E];      // M-tiles per expert
-    __shared__ int s_ebase[MAX_E];   // first schedule position of the expert's bands
+    __shared__ int s_ebase[MAX_E];   // first hand-out position of the expert's bands
     __shared__ int s_cbase[MAX_E];   // first row of the expert in the compact layout
     __shared__ int s_cc[1024];       // first compact row of group g
+    __shared__ int s_fbp[1024];      // full bands of the groups before g (layout order)
+    __shared__ int s_pkey[1024];     // sort key of group g's partial band in the schedule
     __shared__ int s_warp[32];
     __shared__ int s_total;
 
@@ -261,11 +263,11 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     const int cpo = (s.T / R) / s.chunk_tokens;  // chunks per owner
     const int slice = (s.T / R) * s.k;           // rows per owner slice of Ret
 
-    // Shared-memory copies of the schedule and of each tile's group, read by steps 6 and 7 (global
-    // memory when the tile count exceeds PLAN_SMEM_TILES).
+    // Shared-memory copies of the hand-out order and of each tile's group, read by steps 6 and 7
+    // (global memory when the tile count exceeds PLAN_SMEM_TILES).
     extern __shared__ int s_dyn[];
     const bool mirror = s.MT_max <= PLAN_SMEM_TILES;
-    int* s_sched = s_dyn;
+    int* s_order = s_dyn;
     int* s_tg = s_dyn + (mirror ? s.MT_max : 0);
 
     // 1. per group: chunk bases (exclusive prefix over the owner's chunks) and n_{e,r}; the counts
@@ -310,6 +312,24 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     const int P = s_off[G];
     const int MT = P / tbM;
     for (int g = tid; g <= G; g += PLAN_THREADS) p.offsets[g] = s_off[g];
+
+    // 2b. remote-first schedule, the largest transfers first: bands by valid rows, descending, ties
+    // in layout order. The full bands come first, in layout order (position = full bands of the
+    // groups before + index); each group's partial band (valid = n mod tbM) follows, ranked by the
+    // key (tbM - valid, group) among the partial bands.
+    int n_full;
+    {
+        const int g = tid;
+        const int fb = (g < G) ? s_n[g] / tbM : 0;
+        const int o = block_exclusive_scan(fb, s_warp, &s_total);
+        if (g < G) {
+            s_fbp[g] = o;
+            const int v = s_n[g] % tbM;
+            s_pkey[g] = v ? (tbM - v) * 1024 + g : INT_MAX;
+        }
+        n_full = s_total;
+    }
+    __syncthreads();
 
     // 3. owner return offsets: ret_off[r][e] = sum_{e' < e} n_{e',r}
     for (int r = tid; r < R; r += PLAN_THREADS) {
@@ -365,15 +385,16 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         for (int f = 0; f < E; ++f)
             if (s_erank[f] < s_erank[e]) base += s_mt[f];
         s_ebase[e] = base;
-        p.experts[8 * e + 2] = base;        // first schedule position of the expert's bands
-        p.experts[8 * e + 3] = s_erank[e];  // the expert's rank in schedule order
+        p.experts[8 * e + 2] = base;        // first hand-out position of the expert's bands
+        p.experts[8 * e + 3] = s_erank[e];  // the expert's rank in the hand-out order
     }
     __syncthreads();
 
-    // 5. tiles, destination rows, and schedule positions.
-    // Schedule key (expert rank, -valid, owner, row): experts one after another in rank order
-    // (most loaded first); inside an expert its full bands in layout order, then its partial
-    // bands by valid rows descending (ties to the lower owner).
+    // 5. tiles, destination rows, schedule positions and hand-out positions.
+    // Hand-out order (the schedule re-sorted stably by expert): experts one after another in rank
+    // order (most loaded first); inside an expert its full bands in layout order, then its partial
+    // bands by valid rows descending (ties to the lower owner), i.e. key (expert rank, -valid,
+    // owner, row).
     for (int g = tid; g < G; g += PLAN_THREADS) {
         const int e = g / R, r = g % R, n = s_n[g];
         const int m0 = s_off[g] / tbM;
@@ -392,8 +413,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             p.tile_crow[m] = s_cc[g] + i * tbM;
             if (mirror) s_tg[m] = g;
             if (i < nfull) {
-                p.sched[s_ebase[e] + fpre + i] = m;
-                if (mirror) s_sched[s_ebase[e] + fpre + i] = m;
+                p.sched[s_fbp[g] + i] = m;
+                p.order[s_ebase[e] + fpre + i] = m;
+                if (mirror) s_order[s_ebase[e] + fpre + i] = m;
             }
         }
         if (nt > nfull) {  // one partial band
@@ -404,23 +426,28 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
                 if (vh == 0 || rh == r) continue;
                 pos += (vh > valid) || (vh == valid && rh < r);
             }
-            p.sched[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
-            if (mirror) s_sched[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
+            p.order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
+            if (mirror) s_order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
+            const int key = s_pkey[g];
+            int before = 0;  // partial bands earlier in the schedule
+            for (int h = 0; h < G; ++h) before += s_pkey[h] < key;
+            p.sched[n_full + before] = m0 + nfull;
         }
     }
     __syncthreads();
     __threadfence_block();
-    auto sched_at = [&](int pos) { return mirror ? s_sched[pos] : p.sched[pos]; };
+    auto order_at = [&](int pos) { return mirror ? s_order[pos] : p.order[pos]; };
     auto group_of = [&](int m) { return mirror ? s_tg[m] : p.tiles[4 * m] * R + p.tiles[4 * m + 1]; };
     auto valid_of = [&](int m) {  // valid rows of tile m, from its group's row count
         const int g = group_of(m), i = m - s_off[g] / tbM;
         return min(tbM, s_n[g] - i * tbM);
     };
 
-    // 6. segments: runs of adjacent bands of one group, cut into pieces of mgb bands
+    // 6. segments: runs of hand-out positions holding adjacent bands of one group, cut into pieces
+    // of mgb bands
     for (int q = tid; q < MT; q += PLAN_THREADS) {
         auto adjacent = [&](int a, int b) {  // same group, consecutive bands (rows tbM apart)
-            const int ma = sched_at(a), mb = sched_at(b);
+            const int ma = order_at(a), mb = order_at(b);
             return mb == ma + 1 && group_of(ma) == group_of(mb);
         };
         int start = q;
@@ -437,7 +464,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     // owner): a band that needs only 64 of the UMMA tile's 128 rows (every band when tbM = 64, a
     // band with <= 64 valid rows when tbM = 128) shares a work item with another such band of the
     // same expert, each loaded as a 64-row box into one half of the A tile. Item (mA, mB): mB == mA
-    // one 128-row band; mB == -1 one 64-row band alone; else two half bands; schedule order.
+    // one 128-row band; mB == -1 one 64-row band alone; else two half bands; hand-out order.
     __shared__ int s_items[MAX_E], s_ibase_down[MAX_E], s_nitems;
     for (int e = tid; e < E; e += PLAN_THREADS) {
         const int cnt = s_mt[e];
@@ -466,7 +493,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             }
     }
     __syncthreads();
-    // One warp per expert, its bands in schedule order 32 at a time: a band with more than 64 valid
+    // One warp per expert, its bands in hand-out order 32 at a time: a band with more than 64 valid
     // rows is an item of its own; bands with at most 64 pair up in order, each pair emitted at its
     // second band, an unpaired last one at the end. An item's index is the number of items emitted
     // before it: (full bands before it) + (half bands before it) / 2.
@@ -476,7 +503,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         int nfull = 0, nhalf = 0, pending = -1;  // before the current chunk; the unpaired half band
         for (int b0 = 0; b0 < cnt; b0 += 32) {
             const bool in = b0 + lane < cnt;
-            const int m = in ? sched_at(s_ebase[x] + b0 + lane) : -1;
+            const int m = in ? order_at(s_ebase[x] + b0 + lane) : -1;
             const bool half = in && valid_of(m) <= 64;
             const unsigned hm = __ballot_sync(0xffffffffu, half), fm = __ballot_sync(0xffffffffu, in && !half);
             const unsigned lt = (1u << lane) - 1u;
