@@ -26,7 +26,8 @@
  *     CUDA device; "host" pointers to host memory (pinned for asynchronous copies).
  *   - bf16 arrays are passed as uint16_t bit patterns (IEEE bfloat16).
  *   - The caller owns every buffer and the stream. The library never allocates device memory,
- *     never frees anything and never synchronises the stream except in moe_status().
+ *     never frees anything and never synchronises the stream except in moe_status() (and
+ *     moe_forward_dma, which waits on the host for the GPU's progress).
  *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default stream.
  *   - Return value: MOE_OK or a negative MOE_ERR_* code; no exception crosses the ABI, and the
  *     device never traps. moe_last_error() gives a message for the calling thread.
@@ -297,6 +298,33 @@ MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const f
                                        const uint16_t* const* x_h, const uint16_t* W1, const uint16_t* W3,
                                        const uint16_t* W2, float* const* out_h, void* ws, size_t ws_bytes,
                                        int sequential, void* stream);
+
+/*
+ * moe_forward_dma: moe_forward with the return copy on the GPU's copy engines (DMA) instead of SMs,
+ * the DMA-offload idea of the FiCCO page ("Design Space Exploration of DMA based Finer-Grain Compute
+ * Communication Overlap", "Core claim": offloading communication to the GPU's DMA engines reduces
+ * its contention with compute). Same arguments, result (out, Ret, bit for bit) and workspace as
+ * moe_forward, plus:
+ *   host_rec     pinned host memory mapped into the device (e.g. cudaHostAlloc, or any page-locked
+ *                memory on a system with unified addressing), 16-byte aligned, host_bytes >=
+ *                moe_dma_host_bytes(cfg). Owned by the caller; not to be used by two calls at once.
+ *   stage_events as in moe_forward_ex (may be NULL); [MOE_EV_COPIED] is recorded on the library's
+ *                copy stream after the last band's copy.
+ * The down-projection runs on every SM (consumer_ctas, MOE_TAIL_ASSIST, MOE_COPY_WARPS and
+ * MOE_DIRECT_TAIL are ignored); the epilogue warp that completes a band writes a record (its Yp row,
+ * Ret row and valid rows, tagged with the call) into host_rec with a system-scope release. The calling
+ * thread polls the records and issues one cudaMemcpyAsync per ready band, device to device, on a copy
+ * stream of the library's own, which starts after the work enqueued on `stream` before this call;
+ * `stream` waits for that copy stream before the combine. So this call returns only after the
+ * down-projection has finished on the GPU (it blocks for the layer's GEMMs) and cannot be captured
+ * into a CUDA graph (MOE_ERR_ARG while `stream` is capturing). If the down-projection stops early (a
+ * bounded wait ran out), the call sees the stream finish with records missing and returns
+ * MOE_ERR_TIMEOUT; moe_status then gives the device status.
+ */
+MOE_API int moe_dma_host_bytes(const moe_config* cfg, size_t* bytes);
+MOE_API int moe_forward_dma(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
+                            const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes,
+                            void* host_rec, size_t host_bytes, void* const* stage_events, void* stream);
 
 /*
  * moe_status: synchronises `stream`, then reads the device status word of the last call that used

@@ -39,8 +39,8 @@ TRACE_BAND_DONE, TRACE_LAST_ACQUIRE, TRACE_LAST_LOAD, TRACE_LAST_DRAIN = 4, 5, 6
 
 # names of the C entry points (each declared in include/moe.h)
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_plan", "moe_forward", "moe_forward_sequential",
-           "moe_forward_ex", "moe_forward_host", "moe_forward_host_pipelined", "moe_copy_only", "moe_status", "moe_device_info", "moe_route_static",
-           "moe_last_error")
+           "moe_forward_ex", "moe_forward_host", "moe_forward_host_pipelined", "moe_copy_only", "moe_dma_host_bytes",
+           "moe_forward_dma", "moe_status", "moe_device_info", "moe_route_static", "moe_last_error")
 
 # stage events of moe_forward_ex
 EV_BEGIN, EV_PLANNED, EV_UP, EV_DOWN, EV_COPIED, EV_END, EV_COUNT = range(7)
@@ -120,6 +120,8 @@ def lib() -> ctypes.CDLL:
         L.moe_forward_host_pipelined.argtypes = [cfgp, ctypes.c_int, ctypes.POINTER(vp), ctypes.POINTER(vp), vp, vp,
                                                  vp, ctypes.POINTER(vp), vp, sz, ctypes.c_int, vp]
         L.moe_copy_only.argtypes = [cfgp, vp, sz, ctypes.c_int, vp]
+        L.moe_dma_host_bytes.argtypes = [cfgp, ctypes.POINTER(sz)]
+        L.moe_forward_dma.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, ctypes.POINTER(vp), vp]
         L.moe_status.argtypes = [cfgp, vp, vp, i32p]
         L.moe_device_info.argtypes = [i32p, i32p]
         L.moe_route_static.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp]
@@ -277,6 +279,31 @@ def forward_host_pipelined(cfg: Config, logits_h, x_h, W1: torch.Tensor, W3: tor
     _check(lib().moe_forward_host_pipelined(ctypes.byref(c), n, pl, px, _ptr(W1, bf, "cuda", "W1"),
                                             _ptr(W3, bf, "cuda", "W3"), _ptr(W2, bf, "cuda", "W2"), po, ws.ptr,
                                             ws.nbytes, 1 if sequential else 0, _stream(stream)))
+
+
+def dma_host_bytes(cfg: Config) -> int:
+    n = ctypes.c_size_t()
+    c = cfg.to_c()
+    _check(lib().moe_dma_host_bytes(ctypes.byref(c), ctypes.byref(n)))
+    return n.value
+
+
+def forward_dma(cfg: Config, logits: torch.Tensor, x: torch.Tensor, W1: torch.Tensor, W3: torch.Tensor,
+                W2: torch.Tensor, out: torch.Tensor, ws: Workspace, host_rec: torch.Tensor, stream=None,
+                events=None) -> None:
+    """moe_forward_dma: the return copy on the copy engines. host_rec: a pinned host tensor of at least
+    dma_host_bytes(cfg) bytes. Blocks until the down-projection has finished on the GPU."""
+    c = cfg.to_c()
+    bf = torch.bfloat16
+    if not host_rec.is_pinned():
+        raise ValueError("host_rec must be pinned host memory")
+    arr = None if events is None else (ctypes.c_void_p * EV_COUNT)(
+        *[None if e is None else ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(lib().moe_forward_dma(ctypes.byref(c), _ptr(logits, torch.float32, "cuda", "logits"), _ptr(x, bf, "cuda", "x"),
+                                 _ptr(W1, bf, "cuda", "W1"), _ptr(W3, bf, "cuda", "W3"), _ptr(W2, bf, "cuda", "W2"),
+                                 _ptr(out, torch.float32, "cuda", "out"), ws.ptr, ws.nbytes,
+                                 _ptr(host_rec, None, "cpu", "host_rec"), host_rec.numel() * host_rec.element_size(),
+                                 arr, _stream(stream)))
 
 
 def copy_only(cfg: Config, ws: Workspace, ctas: int, stream=None) -> None:

@@ -566,8 +566,10 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                             __threadfence();
                             red_release_gpu_add(p.flags + (size_t)mq * s.n_tiles_n2 + tr.n, inc);
                             const uint32_t before = atom_release_gpu_add(p.bands + mq, inc);
-                            if (before + inc == FLAG_READY * (uint32_t)s.n_tiles_n2)
+                            if (before + inc == FLAG_READY * (uint32_t)s.n_tiles_n2) {
                                 atomicMax(&p.trace[MOE_TRACE_BAND_DONE], globaltimer());
+                                if (p.host_rec) host_band_record(s, p, mq);  // the band's last quarter
+                            }
                         }
                         __syncwarp();
                     }
@@ -1116,8 +1118,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         __threadfence();
                         red_release_gpu_add(p.flags + (size_t)mq * s.n_tiles_n2 + tr.n, inc);
                         const uint32_t before = atom_release_gpu_add(p.bands + mq, inc);
-                        if (before + inc == FLAG_READY * (uint32_t)s.n_tiles_n2)
+                        if (before + inc == FLAG_READY * (uint32_t)s.n_tiles_n2) {
                             atomicMax(&p.trace[MOE_TRACE_BAND_DONE], globaltimer());
+                            if (p.host_rec) host_band_record(s, p, mq);  // the band's last quarter
+                        }
                     }
                     __syncwarp();
                     if (lane == 0) last_end = globaltimer();

@@ -1,10 +1,12 @@
 // Host side of libmoe: argument checks, workspace layout, TMA descriptors and the launch
 // sequences behind the C ABI declared in include/moe.h.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "moe_internal.cuh"
 
@@ -166,7 +168,7 @@ int make_layout(const moe_config* c, Layout* out) {
 
 PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     uint8_t* b = static_cast<uint8_t*>(ws);
-    PlanPtrs p;
+    PlanPtrs p{};  // host_rec stays null except in moe_forward_dma
     p.idx = reinterpret_cast<int32_t*>(b + L.idx);
     p.gate = reinterpret_cast<float*>(b + L.gate);
     p.rank = reinterpret_cast<int32_t*>(b + L.rank);
@@ -722,6 +724,173 @@ MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const f
     for (int sl = 0; sl < 2 && e == cudaSuccess && steps > sl; ++sl) e = cudaStreamWaitEvent(c.st, h->out_free[sl], 0);
     if (e != cudaSuccess) return cuda_fail(e, "pipelined host copies");
     return MOE_OK;
+}
+
+// ---- copy-engine return copy (moe_forward_dma) ------------------------------------------------
+// The return copy on the GPU's copy engines: the down-projection runs on every SM without consumers,
+// and the epilogue warp that completes a band writes a record into pinned host memory (Yp row, Ret
+// row, valid rows, then the call's tag, released at system scope). The calling thread polls the
+// records and issues one cudaMemcpyAsync per ready band on a copy stream of its own; the combine
+// waits for that stream. Records: 4 words of header (tag, band count, padded rows, 0), then 4 words
+// per band (tag, Ret row, valid rows, Yp row).
+struct DmaPipe {
+    cudaStream_t cs = nullptr;
+    cudaEvent_t start = nullptr, copied = nullptr;
+    bool ok = false;
+};
+
+static int dma_pipe(DmaPipe** out) {
+    static DmaPipe pipes[64];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(MOE_ERR_DEVICE, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    DmaPipe& d = pipes[dev];
+    if (!d.ok) {
+        e = cudaStreamCreateWithFlags(&d.cs, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.start, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.copied, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "creating the copy-engine stream and events");
+        d.ok = true;
+    }
+    *out = &d;
+    return MOE_OK;
+}
+
+static size_t dma_host_bytes(const Layout& lay) { return (size_t)(lay.L.MT_max + 1) * 16; }
+
+static int run_forward_dma(Call& c, const float* logits, const uint16_t* x, const uint16_t* W1, const uint16_t* W3,
+                           const uint16_t* W2, float* out, void* host_rec, size_t host_bytes, void* const* ev) {
+    if (!logits || !x || !W1 || !W3 || !W2 || !out) return fail(MOE_ERR_ARG, "NULL input or output pointer");
+    if (!aligned(x, 16) || !aligned(W1, 16) || !aligned(W3, 16) || !aligned(W2, 16) || !aligned(out, 16) ||
+        !aligned(logits, 4))
+        return fail(MOE_ERR_ARG, "x, W1, W3, W2, out must be 16-byte aligned, logits 4-byte aligned");
+    if (!host_rec || !aligned(host_rec, 16)) return fail(MOE_ERR_ARG, "host_rec must be non-NULL and 16-byte aligned");
+    if (host_bytes < dma_host_bytes(c.lay))
+        return fail(MOE_ERR_ARG, "host_rec has %zu bytes, needs %zu", host_bytes, dma_host_bytes(c.lay));
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(c.st, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(MOE_ERR_ARG, "moe_forward_dma waits on the host for the GPU: it cannot be captured in a graph");
+    void* dev_rec = nullptr;
+    e = cudaHostGetDevicePointer(&dev_rec, host_rec, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "host_rec is not pinned memory mapped into the device");
+    DmaPipe* dp = nullptr;
+    int rc = dma_pipe(&dp);
+    if (rc) return rc;
+
+    // no consumer SMs: the down-projection on every SM, flags published, nothing copied by SMs
+    static std::atomic<uint32_t> g_epoch{0};
+    uint32_t epoch = ++g_epoch;
+    if (epoch == 0) epoch = ++g_epoch;
+    Shape& S = c.lay.S;
+    S.flags &= ~(uint32_t)(MOE_TAIL_ASSIST | MOE_COPY_WARPS | MOE_DIRECT_TAIL | MOE_TEST_STALL_CONSUMER);
+    S.host_epoch = epoch;
+    c.p.host_rec = static_cast<uint32_t*>(dev_rec);
+    const bool pair_down = (S.flags & MOE_PAIR_UMMA) && S.bn2 == 2 * BN1;
+    CUtensorMap tXc, tXch, tHc, tHch, tW1, tW3, tW2, tW2h, tHcOut, tYpOut;
+    rc = make_map(&tXc, c.p.Xc, 2, S.d, S.PC_max, 1, BM, "Xc");
+    if (!rc) rc = make_map(&tXch, c.p.Xc, 2, S.d, S.PC_max, 1, BM / 2, "Xc (half)");
+    if (!rc) rc = make_map(&tHc, c.p.Hc, 2, S.ffn, S.PC_max, 1, BM, "Hc");
+    if (!rc) rc = make_map(&tHch, c.p.Hc, 2, S.ffn, S.PC_max, 1, BM / 2, "Hc (half)");
+    if (!rc) rc = make_map(&tHcOut, c.p.Hc, 2, S.ffn, S.PC_max, 1, 32, "Hc (store)", EPI_CHUNK, false);
+    if (!rc) rc = make_map(&tYpOut, c.p.Yp, 2, S.d, S.P_max, 1, 32, "Yp (store)", EPI_CHUNK, false);
+    if (!rc) rc = make_map(&tW1, W1, 3, S.d, S.ffn, S.E, BN1, "W1");
+    if (!rc) rc = make_map(&tW3, W3, 3, S.d, S.ffn, S.E, BN1, "W3");
+    if (!rc) rc = make_map(&tW2, W2, 3, S.ffn, S.d, S.E, S.bn2, "W2");
+    if (!rc && pair_down) rc = make_map(&tW2h, W2, 3, S.ffn, S.d, S.E, BN1, "W2 (half)");
+    if (rc) return rc;
+
+    // the copy stream starts after everything the caller enqueued before (the last combine read Ret)
+    e = cudaEventRecord(dp->start, c.st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(dp->cs, dp->start, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "ordering the copy stream");
+    if ((rc = record(ev, MOE_EV_BEGIN, c.st))) return rc;
+    if ((rc = run_plan(c, logits, x, true))) return rc;
+    if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
+    e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.st)
+                                  : launch_gemm_swiglu(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.di.sms, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
+    if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
+    e = pair_down ? launch_gemm_down_pair(S, c.p, tHc, tHch, tW2h, tYpOut, 0, true, c.st)
+                  : launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, 0, true, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "down-projection launch");
+    if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
+
+    // Poll the records; a band's copy is issued as soon as its record carries this call's tag. The
+    // wait needs no time limit: once the main stream has run everything enqueued (its last kernel is
+    // the down-projection), every record of the call has been written, so a scan after that which
+    // still misses one is an error (a kernel stopped early), not a reason to wait longer.
+    volatile uint32_t* h = static_cast<volatile uint32_t*>(host_rec);
+    const size_t rowb = (size_t)S.d * 2;
+    uint8_t* Yp = reinterpret_cast<uint8_t*>(c.p.Yp);
+    uint8_t* Ret = reinterpret_cast<uint8_t*>(c.p.Ret);
+    int MT = -1, issued = 0;
+    std::vector<char> done;
+    bool drained = false;  // the main stream had finished before the current scan began
+    for (uint64_t it = 0;; ++it) {
+        const bool last_scan = drained;
+        if (MT < 0 && h[0] == epoch) {
+            std::atomic_thread_fence(std::memory_order_acquire);
+            MT = (int)h[1];
+            if (MT < 0 || MT > S.MT_max) return fail(MOE_ERR_PLAN, "band count %d out of range", MT);
+            done.assign((size_t)MT, 0);
+        }
+        for (int m = 0; MT > 0 && m < MT; ++m) {
+            if (done[m] || h[4 + 4 * (size_t)m] != epoch) continue;
+            std::atomic_thread_fence(std::memory_order_acquire);
+            const uint32_t ret0 = h[4 + 4 * (size_t)m + 1], valid = h[4 + 4 * (size_t)m + 2],
+                           row0 = h[4 + 4 * (size_t)m + 3];
+            if (valid < 1 || valid > (uint32_t)S.tbM || (size_t)ret0 + valid > (size_t)S.T * S.k ||
+                (size_t)row0 + valid > (size_t)S.P_max)
+                return fail(MOE_ERR_PLAN, "band %d record out of range", m);
+            e = cudaMemcpyAsync(Ret + (size_t)ret0 * rowb, Yp + (size_t)row0 * rowb, valid * rowb,
+                                cudaMemcpyDeviceToDevice, dp->cs);
+            if (e != cudaSuccess) return cuda_fail(e, "copy-engine band copy");
+            done[m] = 1;
+            ++issued;
+        }
+        if (MT >= 0 && issued == MT) break;
+        if (last_scan) {
+            if (MT < 0) return fail(MOE_ERR_PLAN, "the plan kernel finished without its host record");
+            return fail(MOE_ERR_TIMEOUT, "the down-projection finished with %d of %d band records (see moe_status)",
+                        issued, MT);
+        }
+        if ((it & 15) == 15) {
+            e = cudaStreamQuery(c.st);
+            if (e == cudaSuccess) drained = true;  // one more scan, then every record must be there
+            else if (e != cudaErrorNotReady) return cuda_fail(e, "main stream");
+        }
+    }
+    if ((rc = record(ev, MOE_EV_COPIED, dp->cs))) return rc;
+    e = cudaEventRecord(dp->copied, dp->cs);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(c.st, dp->copied, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "joining the copy stream");
+    e = launch_combine(S, c.p, out, c.di.sms, c.st);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return record(ev, MOE_EV_END, c.st);
+}
+
+MOE_API int moe_dma_host_bytes(const moe_config* cfg, size_t* bytes) {
+    g_err.clear();
+    if (!bytes) return fail(MOE_ERR_ARG, "bytes is NULL");
+    Layout lay;
+    const int rc = make_layout(cfg, &lay);
+    if (rc) return rc;
+    *bytes = dma_host_bytes(lay);
+    return MOE_OK;
+}
+
+MOE_API int moe_forward_dma(const moe_config* cfg, const float* logits, const uint16_t* x, const uint16_t* W1,
+                            const uint16_t* W3, const uint16_t* W2, float* out, void* ws, size_t ws_bytes,
+                            void* host_rec, size_t host_bytes, void* const* stage_events, void* stream) {
+    Call c;
+    const int rc = begin_call(cfg, ws, ws_bytes, stream, &c);
+    if (rc) return rc;
+    return run_forward_dma(c, logits, x, W1, W3, W2, out, host_rec, host_bytes, stage_events);
 }
 
 MOE_API int moe_status(const moe_config* cfg, const void* ws, void* stream, int32_t* detail) {

@@ -116,6 +116,7 @@ struct PlanPtrs {
     uint32_t* flags;
     uint32_t* bands;
     unsigned long long* trace;
+    uint32_t* host_rec;  // moe_forward_dma: band records in mapped pinned host memory (else null)
     __nv_bfloat16* Xc;
     __nv_bfloat16* Hc;
     __nv_bfloat16* Yp;
@@ -135,6 +136,7 @@ struct Shape {
     int down_n_outer_items;         // pair down-projection: experts of at most this many items
                                     // take their tiles N tile by N tile (0: none)
     int tail_window;                // MOE_DIRECT_TAIL: hand-out positions of the direct window (0: one wave)
+    uint32_t host_epoch;            // moe_forward_dma: the call's tag of its host records
     unsigned long long timeout_ns;
     uint32_t flags;
 };
@@ -306,6 +308,22 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 // ---- GPU-scope release / acquire -----------------------------------------------------------------
+// System-scope release store (host-visible word of mapped pinned memory).
+__device__ __forceinline__ void st_release_sys(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// moe_forward_dma: tell the host that band m is complete: its Yp row, Ret row and valid rows, then
+// the call's tag, released at system scope after a system-scope fence (the band's rows were made
+// visible at GPU scope by every warp that stored them, and this warp's counter update came last).
+__device__ __forceinline__ void host_band_record(const Shape& s, const PlanPtrs& p, int m) {
+    uint32_t* rec = p.host_rec + 4 + 4 * (size_t)m;
+    __threadfence_system();
+    rec[1] = (uint32_t)p.tile_ret[m];
+    rec[2] = (uint32_t)p.tiles[4 * m + 3];
+    rec[3] = (uint32_t)p.tiles[4 * m + 2];
+    __threadfence_system();
+    st_release_sys(rec, s.host_epoch);
+}
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

@@ -560,6 +560,12 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         p.meta[META_STATUS_DETAIL] = bad ? (hook ? -3 : P > s.P_max ? P : PC) : 0;
     }
     if (tid < TR_COUNT) p.trace[tid] = (tid == MOE_TRACE_GEMM2_START || tid == MOE_TRACE_COPY_START) ? ~0ull : 0ull;
+    if (tid == 0 && p.host_rec) {  // moe_forward_dma: the band count for the host, then the call's tag
+        p.host_rec[1] = (uint32_t)MT;
+        p.host_rec[2] = (uint32_t)P;
+        __threadfence_system();
+        st_release_sys(p.host_rec, s.host_epoch);
+    }
     const int nflags = min(MT, s.MT_max) * s.n_tiles_n2;
     for (int i = tid; i < nflags; i += PLAN_THREADS) p.flags[i] = 0u;
     for (int i = tid; i < min(MT, s.MT_max); i += PLAN_THREADS) p.bands[i] = 0u;
