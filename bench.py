@@ -86,6 +86,9 @@ def parse_args():
     ap.add_argument("--direct-tail", action=argparse.BooleanOptionalAction, default=True,
                     help="the down-projection's epilogue returns the last wave's bands itself (default); the "
                          "layer without it is timed beside in the same alternation")
+    ap.add_argument("--fused-dispatch", action=argparse.BooleanOptionalAction, default=False,
+                    help="copy the token rows inside the SwiGLU GEMM instead of a permute launch (the other "
+                         "choice is timed beside in the same alternation)")
     ap.add_argument("--tail-window", type=int, default=0,
                     help="tile hand-out positions of the direct tail (0: one wave)")
     ap.add_argument("--dma", action=argparse.BooleanOptionalAction, default=True,
@@ -306,13 +309,15 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------- our arm
-def default_flags(copy_warps: bool, direct_tail: bool = True, tail_assist: bool = True, pair: bool = True) -> int:
+def default_flags(copy_warps: bool, direct_tail: bool = True, tail_assist: bool = True, pair: bool = True,
+                  fused_dispatch: bool = False) -> int:
     """The bench's launch configuration: both expert GEMMs on CTA pairs, finished producers joining
     the copy, the last wave's bands returned by the down-projection's epilogue, and (per workload)
     the producers' copy warps."""
     import tile_level_copy_gb300 as tlc
     return ((tlc.MOE_TAIL_ASSIST if tail_assist else 0) | (tlc.MOE_COPY_WARPS if copy_warps else 0) |
-            (tlc.MOE_PAIR_UMMA if pair else 0) | (tlc.MOE_DIRECT_TAIL if direct_tail else 0))
+            (tlc.MOE_PAIR_UMMA if pair else 0) | (tlc.MOE_DIRECT_TAIL if direct_tail else 0) |
+            (tlc.MOE_FUSED_DISPATCH if fused_dispatch else 0))
 
 
 class LayerBench:
@@ -460,7 +465,7 @@ def run_ours(args, rank: int, world: int):
         args.copy_warps = dw
     seed = args.seed + rank
     flags = default_flags(args.copy_warps, direct_tail=args.direct_tail, tail_assist=not args.no_tail_assist,
-                          pair=args.pair_umma)
+                          pair=args.pair_umma, fused_dispatch=args.fused_dispatch)
     cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags,
                                    tail_window=args.tail_window)
     peaks, peaks_src = load_peaks()
@@ -521,6 +526,11 @@ def run_ours(args, rank: int, world: int):
     direct = bool(cfg.flags & tlc.MOE_DIRECT_TAIL)
     if direct:
         arms["overlapped_all_bands_copied"] = (dataclasses.replace(cfg, flags=cfg.flags & ~tlc.MOE_DIRECT_TAIL), False)
+    # the permute as its own launch against the row copies fused into the SwiGLU GEMM, whichever is
+    # not the default
+    fused = bool(cfg.flags & tlc.MOE_FUSED_DISPATCH)
+    other_dispatch = "overlapped_separate_permute" if fused else "overlapped_fused_dispatch"
+    arms[other_dispatch] = (dataclasses.replace(cfg, flags=cfg.flags ^ tlc.MOE_FUSED_DISPATCH), False)
     eager_arms = dict(arms)
     if args.dma:  # the copy-engine variant: eager only (its host thread issues the copies)
         eager_arms["copy_engines"] = (cfg, "dma")
@@ -692,6 +702,13 @@ def run_ours(args, rank: int, world: int):
                    "hidden_pct": round(100 * (1 - statistics.median(page_tails) / copy_alone_ms), 2),
                    "tail_ms": round(statistics.median(page_tails), 4),
                    "eager_ms_per_step": round(page_ms, 4)}}
+    overlap["dispatch"] = {
+        "default": "fused into the SwiGLU GEMM" if fused else "separate permute launch",
+        "other": other_dispatch, "ms_per_step": round(med[other_dispatch], 4),
+        "paired_diff_other_minus_default_ms": round(float(np.median(rep[other_dispatch] - rep["overlapped"])), 4),
+        "paired_spread_ms": round(spread_ms(rep[other_dispatch] - rep["overlapped"]), 4),
+        "swiglu_and_permute_ms": {a: round(stage_med[a]["route_plan_permute"] + stage_med[a]["swiglu_gemm"], 4)
+                                  for a in ("overlapped", other_dispatch)}}
     if args.dma:
         # copy engines: the "copy" stage runs from the down-projection's end to the last band copy's end
         # (the copy stream's event), so its median is the exposed tail
@@ -730,7 +747,7 @@ def run_ours(args, rank: int, world: int):
         "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "ffn": w.ffn, "E": w.E, "topk": w.topk,
                    "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps),
                    "pair_umma": bool(args.pair_umma), "mgb": args.mgb, "direct_tail": direct,
-                   "tail_window": args.tail_window,
+                   "tail_window": args.tail_window, "fused_dispatch": bool(args.fused_dispatch),
                    "tail_assist": not args.no_tail_assist, "seed": args.seed,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "

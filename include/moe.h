@@ -71,6 +71,12 @@ extern "C" {
                                       /* tail_window tile positions (the last wave) straight  */
                                       /* into their owner's slice of Ret; the consumer skips   */
                                       /* them and their rows of Yp are not written             */
+#define MOE_FUSED_DISPATCH 0x20u      /* the permute's row copies move into the SwiGLU GEMM:  */
+                                      /* its epilogue warps copy the token rows into Xc,      */
+                                      /* expert by expert, before their first tile and        */
+                                      /* release a per-expert row count that the TMA threads  */
+                                      /* acquire before loading an expert's rows; the permute */
+                                      /* launch only computes the slots                       */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
 #define MOE_TEST_PLAN_FAIL 0x200u     /* test hook: the plan kernel reports a failed bounds   */
@@ -156,6 +162,8 @@ typedef struct moe_layout {
     size_t ccoff;      /* int32 [E*R]       first Xc row of group e*R+r                         */
     size_t tile_crow;  /* int32 [MT_max]    Xc / Hc row of the first row of each M-tile (band) */
     size_t band_item;  /* int32 [MT_max]    down-projection work item holding each M-tile      */
+    size_t tok_of;     /* int32 [PC_max]    token of each Xc / Hc row, -1 for a padding row     */
+    size_t xrows;      /* uint32 [E]        rows of each expert copied into Xc (fused dispatch) */
     size_t meta;       /* int32 [64]        P, M-tiles, work counters, status (see csrc)       */
     size_t flags;      /* uint32 [MT_max, n_tiles_n2] per-tile readiness flags                 */
     size_t bands;      /* uint32 [MT_max]   per-band count of finished tile quarters           */

@@ -65,6 +65,10 @@ def check_plan(w, logits_np, x_cpu, mgb=1):
     np.testing.assert_array_equal(experts[:, 7], cbase)
     want_items = [(cbase[e] + 128 * i, e) for e in range(w.E) for i in range(runs[e])]
     np.testing.assert_array_equal(v("items_up")[:PC // 128], np.array(want_items).reshape(-1, 2))
+    # the token of every compact row (-1 for the zero rows that pad each expert's run)
+    tok = np.full(PC, -1, np.int64)
+    tok[cslot.reshape(-1)] = np.repeat(np.arange(w.T), w.topk)
+    np.testing.assert_array_equal(v("tok_of")[:PC], tok)
     if x_cpu is not None:
         xb = x_cpu.view(torch.int16).numpy()
         want = np.zeros((PC, w.d), np.int16)  # padding rows are zero

@@ -267,6 +267,84 @@ __device__ __forceinline__ DirectDst direct_dst(const Shape& s, const PlanPtrs& 
     return dd;
 }
 
+// Fused dispatch (MOE_FUSED_DISPATCH), the permute's row copies inside the SwiGLU GEMM: before its
+// first tile, every epilogue warp of every CTA (idle until the first accumulator is ready) takes
+// blocks of DISPATCH_ROWS compact rows from a queue in row order, i.e. expert by expert, copies each
+// row's token (or zeros for a padding row) into Xc with 16-byte loads and stores, and then adds the
+// block's rows to its expert's count with release semantics. A TMA thread loads an expert's rows
+// only once that count covers every row of the expert (acquire, then an async-proxy fence). The
+// copying warps wait on nothing, so every count completes whatever CTAs are resident.
+constexpr int DISPATCH_ROWS = 4;
+
+__device__ void dispatch_rows(const Shape& s, const PlanPtrs& p) {
+    const int lane = threadIdx.x & 31;
+    int PC = p.meta[META_PC];
+    if (PC < 0 || PC > s.PC_max) PC = 0;
+    const int nb = PC / DISPATCH_ROWS;  // PC is a multiple of 128
+    const int vec = s.d / 8;            // 16-byte vectors per row
+    const uint4* xs = reinterpret_cast<const uint4*>(p.x);
+    uint4* xc = reinterpret_cast<uint4*>(p.Xc);
+    constexpr int V = 16;               // vectors per lane in flight
+    for (;;) {
+        int b = 0;
+        if (lane == 0) b = atomicAdd(&p.meta[META_DISPATCH], 1);
+        b = __shfl_sync(0xffffffffu, b, 0);
+        if (b >= nb) break;
+        const int r0 = b * DISPATCH_ROWS;
+        const int e = p.items_up[2 * (r0 / BM) + 1];  // a block lies in one 128-row item of one expert
+        int tk = (lane < DISPATCH_ROWS) ? p.tok_of[r0 + lane] : -1;
+        const bool bad = __any_sync(0xffffffffu, tk < -1 || tk >= s.T) || e < 0 || e >= s.E;
+        if (bad) {
+            if (lane == 0) set_status(p.meta, ST_BAD_PLAN, -4);
+            break;
+        }
+        for (int r = 0; r < DISPATCH_ROWS; ++r) {
+            const int t = __shfl_sync(0xffffffffu, tk, r);
+            uint4* dst = xc + (size_t)(r0 + r) * vec;
+            for (int base = 0; base < vec; base += 32 * V) {
+                uint4 v[V];
+#pragma unroll
+                for (int i = 0; i < V; ++i) {
+                    const int vi = base + i * 32 + lane;
+                    v[i] = make_uint4(0, 0, 0, 0);
+                    if (t >= 0 && vi < vec) v[i] = __ldg(xs + (size_t)t * vec + vi);
+                }
+#pragma unroll
+                for (int i = 0; i < V; ++i) {
+                    const int vi = base + i * 32 + lane;
+                    if (vi < vec) dst[vi] = v[i];
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence();
+            red_release_gpu_add(p.xrows + e, DISPATCH_ROWS);
+        }
+    }
+    __syncwarp();
+}
+
+// TMA thread of a SwiGLU GEMM with fused dispatch: wait (bounded) until every compact row of expert e
+// has been copied, then order the async-proxy loads after the acquire. Returns false on timeout.
+__device__ __forceinline__ bool wait_expert_rows(const Shape& s, const PlanPtrs& p, int e, volatile int* abort,
+                                                 int where) {
+    const uint32_t need = (uint32_t)p.experts[8 * e + 4] * BM;
+    if (ld_acquire_gpu(p.xrows + e) < need) {
+        const unsigned long long t0 = globaltimer();
+        while (ld_acquire_gpu(p.xrows + e) < need) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > s.timeout_ns) {
+                set_status(p.meta, ST_PIPE_TIMEOUT, where);
+                return false;
+            }
+            __nanosleep(64);
+        }
+    }
+    fence_proxy_async_global();
+    return true;
+}
+
 // Bounds check of the plan entries a GEMM launch reads, by all threads of a CTA before any tile:
 // SwiGLU items (first compact row, expert) and the expert table of the item lists; down-projection
 // items (bands mA, mB) and each band's expert, output rows and compact rows. Returns nonzero if this
@@ -329,6 +407,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     const int total = NI * nN;
     const uint32_t tx_bytes = A_STAGE_BYTES + BN * BK * 2;
     const unsigned long long tmo = s.timeout_ns;
+    const bool dispatch = MODE == 1 && (s.flags & MOE_FUSED_DISPATCH);
     // MOE_DIRECT_TAIL: items from `direct_from` on have every tile among the last `window` hand-out
     // positions (item i's tiles are i*nN .. i*nN+nN-1); their epilogue writes the rows into Ret and
     // the copy engines skip them
@@ -404,6 +483,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
             uint32_t ph = 0, issued = 0, last_ph = 0;
             bool ok = true;
             int t = blockIdx.x;  // first tile static, the others from the hand-out counter
+            int ready_e = -1;    // fused dispatch: the expert whose rows are known to be copied
             int* tile_counter = &p.meta[(MODE == 1) ? META_TILES_UP : META_TILES_DOWN];
             const int claim_kb = KB > 8 ? KB - 8 : 0;
             for (int j = 0; ok; ++j) {
@@ -417,6 +497,13 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                 if (t >= total) break;
                 const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up)
                                                : decode_down(t, nN, p.items_down, p.tiles, p.tile_crow);
+                if (MODE == 1 && dispatch && tr.e != ready_e) {
+                    if (!wait_expert_rows(s, p, tr.e, sm.abort, 30)) {
+                        ok = false;
+                        break;
+                    }
+                    ready_e = tr.e;
+                }
                 int next = total;
                 for (int kb = 0; kb < KB; ++kb) {
                     // the next tile is taken a few k-blocks before this one's loads are all issued,
@@ -518,6 +605,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
             // TMA tensor store of the chunk. Two staging buffers per warp alternate.
             const int q = warp & 3;  // TMEM lane quarter this warp may access
             const bool flags = (MODE == 2) && overlapped;
+            if (MODE == 1 && dispatch) dispatch_rows(s, p);
             EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
             int b = 0;
             uint32_t aph = 0;
@@ -800,6 +888,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const int nN = (MODE == 1) ? s.ffn / BN1 : s.n_tiles_n2;
     const int KB = ((MODE == 1) ? s.d : s.ffn) / BK;
     const unsigned long long tmo = s.timeout_ns;
+    const bool dispatch = MODE == 1 && (s.flags & MOE_FUSED_DISPATCH);
     const int bad_item = __syncthreads_or(plan_items_bad(s, p, MODE, NI, MT));  // same answer in every CTA
     if (bad_item) NI = 0;
 
@@ -918,6 +1007,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             int st = 0;
             uint32_t ph = 0;
             bool ok = true;
+            int ready_e = -1;  // fused dispatch: the expert whose rows are known to be copied
             const bool stall = (s.flags & (rank == 0 ? MOE_TEST_STALL_PIPE0 : MOE_TEST_STALL_PIPE1)) != 0;
             const int claim_kb = KB > 8 ? KB - 8 : 0;
             int t = (rank == 0 && !bad) ? atomicAdd(tile_counter, 1) : 0;
@@ -946,6 +1036,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                                        ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
                                        : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank,
                                                           s.down_n_outer_items);
+                if (MODE == 1 && dispatch && tr.e != ready_e) {
+                    if (!wait_expert_rows(s, p, tr.e, sm.abort, 30 + (int)rank)) {
+                        ok = false;
+                        break;
+                    }
+                    ready_e = tr.e;
+                }
                 const bool halves = MODE == 2 && tr.mB >= 0 && tr.mB != tr.mA;  // two 64-row boxes
                 const int brow = (MODE == 1) ? tr.n * BN1 : tr.n * 2 * BN1 + (int)rank * BN1;
                 const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
@@ -1064,6 +1161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             // ---------------- epilogue (both CTAs): this CTA's 128 rows ----------------
             const int q = warp & 3;
             const bool flags = (MODE == 2) && overlapped;
+            if (MODE == 1 && dispatch) dispatch_rows(s, p);
             EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
             const uint32_t acc_empty0 = mapa_shared(smem_u32(sm.acc_empty), 0u);
             const uint32_t tq_empty0 = mapa_shared(smem_u32(sm.tq_empty), 0u);

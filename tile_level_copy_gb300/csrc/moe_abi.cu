@@ -117,6 +117,8 @@ int make_layout(const moe_config* c, Layout* out) {
     L.ccoff = put(G * 4);
     L.tile_crow = put(MT_max * 4);
     L.band_item = put(MT_max * 4);
+    L.tok_of = put(PC_max * 4);
+    L.xrows = put(E * 4);
     L.meta = put(META_COUNT * 4);
     L.flags = put(MT_max * nN2 * 4);
     L.bands = put(MT_max * 4);
@@ -191,6 +193,8 @@ PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     p.ccoff = reinterpret_cast<int32_t*>(b + L.ccoff);
     p.tile_crow = reinterpret_cast<int32_t*>(b + L.tile_crow);
     p.band_item = reinterpret_cast<int32_t*>(b + L.band_item);
+    p.tok_of = reinterpret_cast<int32_t*>(b + L.tok_of);
+    p.xrows = reinterpret_cast<uint32_t*>(b + L.xrows);
     p.meta = reinterpret_cast<int32_t*>(b + L.meta);
     p.flags = reinterpret_cast<uint32_t*>(b + L.flags);
     p.bands = reinterpret_cast<uint32_t*>(b + L.bands);
@@ -342,7 +346,10 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     (void)L;
 
     if ((rc = record(ev, MOE_EV_BEGIN, c.st))) return rc;
-    rc = run_plan(c, logits, x, true);
+    // with MOE_FUSED_DISPATCH the permute only computes the slots; the SwiGLU GEMM copies the rows
+    const bool fused_dispatch = (S.flags & MOE_FUSED_DISPATCH) != 0;
+    c.p.x = reinterpret_cast<const __nv_bfloat16*>(x);
+    rc = run_plan(c, logits, x, !fused_dispatch);
     if (rc) return rc;
     if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
     cudaError_t e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.st)
@@ -383,7 +390,7 @@ namespace {
 // Offsets of the plan's scratch regions inside the static array for one config (256-byte aligned).
 struct StaticLayout {
     size_t rank, cnt, base, counts, ret, tiles, tret, sched, order, seg, exp, iu, id, meta, flags, bands, trace,
-        cslot, ccoff, tcrow, bitem, bytes;
+        cslot, ccoff, tcrow, bitem, tokof, xrows, bytes;
 };
 
 StaticLayout static_layout(const Layout& lay) {
@@ -418,6 +425,8 @@ StaticLayout static_layout(const Layout& lay) {
     o.ccoff = put(E * R * 4);
     o.tcrow = put(MT * 4);
     o.bitem = put(MT * 4);
+    o.tokof = put((size_t)L.PC_max * 4);
+    o.xrows = put(E * 4);
     o.bytes = cur;
     return o;
 }
@@ -809,7 +818,8 @@ static int run_forward_dma(Call& c, const float* logits, const uint16_t* x, cons
     if (e == cudaSuccess) e = cudaStreamWaitEvent(dp->cs, dp->start, 0);
     if (e != cudaSuccess) return cuda_fail(e, "ordering the copy stream");
     if ((rc = record(ev, MOE_EV_BEGIN, c.st))) return rc;
-    if ((rc = run_plan(c, logits, x, true))) return rc;
+    c.p.x = reinterpret_cast<const __nv_bfloat16*>(x);
+    if ((rc = run_plan(c, logits, x, !(S.flags & MOE_FUSED_DISPATCH)))) return rc;
     if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
     e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.st)
                                   : launch_gemm_swiglu(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.di.sms, c.st);
@@ -979,6 +989,8 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.ccoff = reinterpret_cast<int32_t*>(b + o.ccoff);
     p.tile_crow = reinterpret_cast<int32_t*>(b + o.tcrow);
     p.band_item = reinterpret_cast<int32_t*>(b + o.bitem);
+    p.tok_of = reinterpret_cast<int32_t*>(b + o.tokof);
+    p.xrows = reinterpret_cast<uint32_t*>(b + o.xrows);
     p.meta = reinterpret_cast<int32_t*>(b + o.meta);
     p.flags = reinterpret_cast<uint32_t*>(b + o.flags);
     p.bands = reinterpret_cast<uint32_t*>(b + o.bands);

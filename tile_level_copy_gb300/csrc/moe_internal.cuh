@@ -26,6 +26,7 @@ enum Meta : int {
     META_ITEMS = 7,        // down-projection work items (one band, or two bands of <= 64 rows)
     META_ITEMS_UP = 8,     // SwiGLU work items (128 rows of one expert in the compact layout)
     META_PC = 9,           // rows of the compact layout used by this call
+    META_DISPATCH = 24,    // next block of compact rows to copy (MOE_FUSED_DISPATCH)
     META_TILES_UP = 32,    // next SwiGLU GEMM tile to hand out (single-CTA kernel), minus the grid
     META_TILES_DOWN = 48,  // next down-projection tile to hand out, minus the producer count
                            // (both on a 128-byte line away from the copy queues' line)
@@ -117,6 +118,9 @@ struct PlanPtrs {
     uint32_t* bands;
     unsigned long long* trace;
     uint32_t* host_rec;  // moe_forward_dma: band records in mapped pinned host memory (else null)
+    const __nv_bfloat16* x;  // tokens [T, d] (MOE_FUSED_DISPATCH: read by the SwiGLU GEMM)
+    int32_t* tok_of;     // [PC_max] token of each compact row, -1 for a padding row
+    uint32_t* xrows;     // [E] compact rows of each expert copied so far (MOE_FUSED_DISPATCH)
     __nv_bfloat16* Xc;
     __nv_bfloat16* Hc;
     __nv_bfloat16* Yp;

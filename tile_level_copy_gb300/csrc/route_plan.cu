@@ -552,6 +552,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         p.meta[META_QUEUE_SEQ] = 0;
         p.meta[META_TILES_UP] = 0;
         p.meta[META_TILES_DOWN] = 0;
+        p.meta[META_DISPATCH] = 0;
         // MOE_TEST_PLAN_FAIL: report a failed check (detail -3) so that tests can see the status
         // reach the caller; the plan itself is still complete and valid
         const bool hook = (s.flags & MOE_TEST_PLAN_FAIL) != 0;
@@ -569,6 +570,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     const int nflags = min(MT, s.MT_max) * s.n_tiles_n2;
     for (int i = tid; i < nflags; i += PLAN_THREADS) p.flags[i] = 0u;
     for (int i = tid; i < min(MT, s.MT_max); i += PLAN_THREADS) p.bands[i] = 0u;
+    for (int e = tid; e < E; e += PLAN_THREADS) p.xrows[e] = 0u;
 }
 
 cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
@@ -585,10 +587,11 @@ cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
 
 // ---------------------------------------------------------------------------------------------
 // permute_kernel: one warp per work item. Items [0, T): token t computes its k slots (padded
-// layout), compact slots and return slots, and copies x[t] into its k rows of Xc: each lane first
-// loads up to 16 vectors of 16 bytes (all loads in flight together), then stores them to the k
-// rows. Items [T, T + E * BM/8): one group of 8 rows of an expert's last BM-row tile in the compact
-// layout, zeroing those rows past the expert's rows. With x == nullptr only the slots are written.
+// layout), compact slots and return slots, records t as the token of its k compact rows, and copies
+// x[t] into those rows of Xc: each lane first loads up to 16 vectors of 16 bytes (all loads in
+// flight together), then stores them to the k rows. Items [T, T + E * BM/8): one group of 8 rows of
+// an expert's last BM-row tile in the compact layout, marking those rows past the expert's rows as
+// padding (token -1) and zeroing them. With x == nullptr only the slots and tokens are written.
 // ---------------------------------------------------------------------------------------------
 constexpr int PERM_VEC = 16;  // 16-byte vectors per lane per pass
 
@@ -602,7 +605,7 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
     uint4* xc = reinterpret_cast<uint4*>(p.Xc);
     const bool ok_pc = PC >= 0 && PC <= s.PC_max;
     const int groups = BM / 8;
-    const int pad_items = (ok_pc && xs != nullptr) ? E * groups : 0;
+    const int pad_items = ok_pc ? E * groups : 0;
 
     for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < s.T + pad_items; item += nwarps) {
         if (item < s.T) {
@@ -627,6 +630,7 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
                 if (lane == 0) set_status(p.meta, ST_BAD_PLAN, t);
                 continue;
             }
+            if (lane < k) p.tok_of[my_cs] = t;  // the compact row's token (read by a fused dispatch)
             if (xs == nullptr) continue;  // plan only: slots without the row copy
             for (int base = 0; base < vec; base += 32 * PERM_VEC) {
                 uint4 v[PERM_VEC];
@@ -655,6 +659,8 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
             for (int rr = max(rows, (iu - 1) * BM + g * 8); rr < (iu - 1) * BM + (g + 1) * 8; ++rr) {
                 const size_t row = (size_t)cb + rr;
                 if (row >= (size_t)PC) break;
+                if (lane == 0) p.tok_of[row] = -1;  // a padding row: zeros
+                if (xs == nullptr) continue;
                 for (int v = lane; v < vec; v += 32) xc[row * vec + v] = z;
             }
         }
