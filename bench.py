@@ -40,8 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu capture of one launch on the Mixtral-shaped layer, per (workload, CTA-pair kernel), with the
 # SHA-256 of the kernel sources it was taken on: the bench reports it only while those sources are
 # unchanged and the launch configuration is the captured one.
-SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 1954745600 + 246188032,
-                                      "sources_sha256": "cd7392f0a7f61bc7fafbf5b7207dcefca60707d72d31b2e4faef569980d75f0a"}}
+SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 1953190656 + 246202112,
+                                      "sources_sha256": "c13face15085d54397e597202df7689f118e07a369461eaa7a55225ef9f85f01"}}
 KERNEL_SOURCES = ("tile_level_copy_gb300/csrc/gemm.cu", "tile_level_copy_gb300/csrc/moe_internal.cuh",
                   "tile_level_copy_gb300/csrc/copy_ring.cuh")
 
@@ -89,6 +89,8 @@ def parse_args():
     ap.add_argument("--fused-dispatch", action=argparse.BooleanOptionalAction, default=False,
                     help="copy the token rows inside the SwiGLU GEMM instead of a permute launch (the other "
                          "choice is timed beside in the same alternation)")
+    ap.add_argument("--fused-gemms", action=argparse.BooleanOptionalAction, default=False,
+                    help="both expert GEMMs in one launch (the other choice is timed beside in the same alternation)")
     ap.add_argument("--tail-window", type=int, default=0,
                     help="tile hand-out positions of the direct tail (0: one wave)")
     ap.add_argument("--dma", action=argparse.BooleanOptionalAction, default=True,
@@ -310,14 +312,14 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------------- our arm
 def default_flags(copy_warps: bool, direct_tail: bool = True, tail_assist: bool = True, pair: bool = True,
-                  fused_dispatch: bool = False) -> int:
+                  fused_dispatch: bool = False, fused_gemms: bool = False) -> int:
     """The bench's launch configuration: both expert GEMMs on CTA pairs, finished producers joining
     the copy, the last wave's bands returned by the down-projection's epilogue, and (per workload)
     the producers' copy warps."""
     import tile_level_copy_gb300 as tlc
     return ((tlc.MOE_TAIL_ASSIST if tail_assist else 0) | (tlc.MOE_COPY_WARPS if copy_warps else 0) |
             (tlc.MOE_PAIR_UMMA if pair else 0) | (tlc.MOE_DIRECT_TAIL if direct_tail else 0) |
-            (tlc.MOE_FUSED_DISPATCH if fused_dispatch else 0))
+            (tlc.MOE_FUSED_DISPATCH if fused_dispatch else 0) | (tlc.MOE_FUSED_GEMMS if fused_gemms else 0))
 
 
 class LayerBench:
@@ -465,7 +467,7 @@ def run_ours(args, rank: int, world: int):
         args.copy_warps = dw
     seed = args.seed + rank
     flags = default_flags(args.copy_warps, direct_tail=args.direct_tail, tail_assist=not args.no_tail_assist,
-                          pair=args.pair_umma, fused_dispatch=args.fused_dispatch)
+                          pair=args.pair_umma, fused_dispatch=args.fused_dispatch, fused_gemms=args.fused_gemms)
     cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags,
                                    tail_window=args.tail_window)
     peaks, peaks_src = load_peaks()
@@ -531,6 +533,11 @@ def run_ours(args, rank: int, world: int):
     fused = bool(cfg.flags & tlc.MOE_FUSED_DISPATCH)
     other_dispatch = "overlapped_separate_permute" if fused else "overlapped_fused_dispatch"
     arms[other_dispatch] = (dataclasses.replace(cfg, flags=cfg.flags ^ tlc.MOE_FUSED_DISPATCH), False)
+    # both GEMMs in one launch against two launches, whichever is not the default (needs the
+    # down-projection on CTA pairs)
+    fused_gemms = bool(cfg.flags & tlc.MOE_FUSED_GEMMS)
+    other_gemms = "overlapped_separate_gemms" if fused_gemms else "overlapped_fused_gemms"
+    arms[other_gemms] = (dataclasses.replace(cfg, flags=cfg.flags ^ tlc.MOE_FUSED_GEMMS), False)
     eager_arms = dict(arms)
     if args.dma:  # the copy-engine variant: eager only (its host thread issues the copies)
         eager_arms["copy_engines"] = (cfg, "dma")
@@ -709,6 +716,11 @@ def run_ours(args, rank: int, world: int):
         "paired_spread_ms": round(spread_ms(rep[other_dispatch] - rep["overlapped"]), 4),
         "swiglu_and_permute_ms": {a: round(stage_med[a]["route_plan_permute"] + stage_med[a]["swiglu_gemm"], 4)
                                   for a in ("overlapped", other_dispatch)}}
+    overlap["gemm_launches"] = {
+        "default": "one launch for both GEMMs" if fused_gemms else "a launch per GEMM",
+        "other": other_gemms, "ms_per_step": round(med[other_gemms], 4),
+        "paired_diff_other_minus_default_ms": round(float(np.median(rep[other_gemms] - rep["overlapped"])), 4),
+        "paired_spread_ms": round(spread_ms(rep[other_gemms] - rep["overlapped"]), 4)}
     if args.dma:
         # copy engines: the "copy" stage runs from the down-projection's end to the last band copy's end
         # (the copy stream's event), so its median is the exposed tail
@@ -748,6 +760,7 @@ def run_ours(args, rank: int, world: int):
                    "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps),
                    "pair_umma": bool(args.pair_umma), "mgb": args.mgb, "direct_tail": direct,
                    "tail_window": args.tail_window, "fused_dispatch": bool(args.fused_dispatch),
+                   "fused_gemms": bool(args.fused_gemms),
                    "tail_assist": not args.no_tail_assist, "seed": args.seed,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "

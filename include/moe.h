@@ -77,6 +77,11 @@ extern "C" {
                                       /* release a per-expert row count that the TMA threads  */
                                       /* acquire before loading an expert's rows; the permute */
                                       /* launch only computes the slots                       */
+#define MOE_FUSED_GEMMS 0x40u         /* both expert GEMMs in one persistent launch on CTA     */
+                                      /* pairs (needs the down-projection on pairs): SwiGLU   */
+                                      /* tiles first; an expert's down-projection tiles start */
+                                      /* once all its SwiGLU tiles have published; the        */
+                                      /* consumer clusters take SwiGLU tiles, then copy       */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
 #define MOE_TEST_PLAN_FAIL 0x200u     /* test hook: the plan kernel reports a failed bounds   */
@@ -164,6 +169,7 @@ typedef struct moe_layout {
     size_t band_item;  /* int32 [MT_max]    down-projection work item holding each M-tile      */
     size_t tok_of;     /* int32 [PC_max]    token of each Xc / Hc row, -1 for a padding row     */
     size_t xrows;      /* uint32 [E]        rows of each expert copied into Xc (fused dispatch) */
+    size_t xready;     /* uint32 [E]        SwiGLU tile quarters published per expert (fused)   */
     size_t meta;       /* int32 [64]        P, M-tiles, work counters, status (see csrc)       */
     size_t flags;      /* uint32 [MT_max, n_tiles_n2] per-tile readiness flags                 */
     size_t bands;      /* uint32 [MT_max]   per-band count of finished tile quarters           */
@@ -265,6 +271,8 @@ MOE_API int moe_copy_only(const moe_config* cfg, void* ws, size_t ws_bytes, int 
  *                                                                 (overlapped: GEMM + return copy)
  *   [MOE_EV_COPIED]    after the return copy (overlapped: same point as MOE_EV_DOWN)
  *   [MOE_EV_END]       after the combine
+ * With MOE_FUSED_GEMMS (one launch for both GEMMs) MOE_EV_UP, MOE_EV_DOWN and MOE_EV_COPIED all
+ * follow that launch.
  * While `stream` is being captured into a CUDA graph, each record becomes an event-record node of
  * the graph (cudaEventRecordExternal), recorded again by every replay.
  */

@@ -30,6 +30,7 @@ MOE_COPY_WARPS = 0x4
 MOE_PAIR_UMMA = 0x8
 MOE_DIRECT_TAIL = 0x10
 MOE_FUSED_DISPATCH = 0x20
+MOE_FUSED_GEMMS = 0x40
 MOE_TEST_STALL_CONSUMER = 0x100
 MOE_TEST_PLAN_FAIL = 0x200
 MOE_TEST_STALL_PIPE0 = 0x400
@@ -63,7 +64,7 @@ _LAYOUT_INTS = ("P_max", "MT_max", "n_chunks", "chunk_tokens", "n_tiles_n2", "bl
                 "units_per_band", "PC_max", "IU_max")
 LAYOUT_REGIONS = ("idx", "gate", "rank", "chunk_cnt", "chunk_base", "counts", "offsets", "ret_off", "tiles",
                   "tile_ret", "sched", "order", "seg", "experts", "items_up", "items_down", "slot", "cslot", "ret_slot", "ccoff",
-                  "tile_crow", "band_item", "tok_of", "xrows", "meta", "flags", "bands", "trace", "Xc", "Hc", "Yp", "Ret", "in_logits", "in_x", "out")
+                  "tile_crow", "band_item", "tok_of", "xrows", "xready", "meta", "flags", "bands", "trace", "Xc", "Hc", "Yp", "Ret", "in_logits", "in_x", "out")
 
 
 class _Layout(ctypes.Structure):
@@ -179,6 +180,7 @@ class Workspace:
            "slot": (torch.int32, "TK"), "cslot": (torch.int32, "TK"), "ret_slot": (torch.int32, "TK"),
            "counts": (torch.int32, "ER"), "ccoff": (torch.int32, "ER"), "tile_crow": (torch.int32, "MT"),
            "band_item": (torch.int32, "MT"), "tok_of": (torch.int32, "PC"), "xrows": (torch.int32, "E"),
+           "xready": (torch.int32, "E"),
            "offsets": (torch.int32, "G1"), "ret_off": (torch.int32, "RE1"), "tiles": (torch.int32, "MT4"),
            "tile_ret": (torch.int32, "MT"), "sched": (torch.int32, "MT"), "order": (torch.int32, "MT"),
            "seg": (torch.int32, "MT2"),

@@ -812,26 +812,27 @@ __device__ __forceinline__ int tab_segment(const int* cum, int E, int t) {
     return lo;
 }
 
-// Pair tile t -> this CTA's rows (MODE 1). Order as in decode_up with two work items per pair:
-// experts in id order, N tiles outer, pairs inner; rank r takes item 2 * pair + r of the expert
-// (mA = -1: none).
+// Pair tile t -> this CTA's rows (SwiGLU tiles). Order as in decode_up with two work items per pair:
+// the table's experts in order (ids in `eid`, or the table's order is the id order when eid is
+// null), N tiles outer, pairs inner; rank r takes item 2 * pair + r of the expert (mA = -1: none).
 __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, const int32_t* items,
-                                                  uint32_t rank) {
+                                                  uint32_t rank, const int* eid = nullptr) {
     const int* cum = tab;
     const int* first = tab + (E + 1);
     const int* count = first + E;
-    const int e = tab_segment(cum, E, t), local = t - cum[e], cnt = count[e], np = (cnt + 1) >> 1;
+    const int r = tab_segment(cum, E, t), local = t - cum[r], cnt = count[r], np = (cnt + 1) >> 1;
+    const int e = eid ? eid[r] : r;
     const int n = local / np, it = 2 * (local - n * np) + (int)rank;
     if (it >= cnt) {
-        TileRef r;
-        r.item = -1;
-        r.mA = r.mB = -1;
-        r.n = n;
-        r.e = e;
-        r.rowA = r.rowB = r.lrowA = r.lrowB = 0;
-        return r;
+        TileRef x;
+        x.item = -1;
+        x.mA = x.mB = -1;
+        x.n = n;
+        x.e = e;
+        x.rowA = x.rowB = x.lrowA = x.lrowB = 0;
+        return x;
     }
-    const int item = first[e] + it;
+    const int item = first[r] + it;
     return compact_ref(items[2 * item], n, e);
 }
 
@@ -871,26 +872,49 @@ __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E
     return make_ref(items[2 * item], items[2 * item + 1], n, tiles, crow, item);
 }
 
-template <int MODE>  // 1: SwiGLU up-projection -> Hc; 2: down-projection -> Yp (+ flags / consumers)
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
-    gemm_pair_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut,
-                     int num_producers, int overlapped) {
+// The CTA-pair GEMM. MODE 1: SwiGLU tiles -> Hc; 2: down-projection tiles -> Yp (+ flags, consumer
+// CTAs); 3: both in one launch (MOE_FUSED_GEMMS). In MODE 3 the SwiGLU tiles are handed out first,
+// experts in hand-out order (the most loaded first); each SwiGLU epilogue warp, once its TMA stores
+// have completed, fences the async proxy and release-adds 1 to its expert's count (xready), and a
+// TMA thread starts an expert's down-projection tiles only when that count covers every SwiGLU tile
+// quarter of the expert (acquire, then an async-proxy fence before the loads of Hc). So the
+// down-projection starts on the SMs that finish their SwiGLU tiles instead of after the whole GEMM;
+// the consumer clusters take SwiGLU tiles too and start copying when those run out. Every count is
+// completed by epilogue warps that wait on nothing of the down-projection, so no wait can stall for
+// good. Operands: mA / mAh / mB0 / mB1 / mOut are the launch's (MODE 1: Xc, -, W1, W3, Hc store;
+// MODE 2: Hc, Hc halves, W2 halves twice, Yp store); MODE 3 passes the SwiGLU ones there and the
+// down-projection's as mA2 / mA2h / mB2 / mOut2.
+template <int MODE>
+__device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, const CUtensorMap* mA,
+                                          const CUtensorMap* mAh, const CUtensorMap* mB0, const CUtensorMap* mB1,
+                                          const CUtensorMap* mOut, const CUtensorMap* mA2, const CUtensorMap* mA2h,
+                                          const CUtensorMap* mB2, const CUtensorMap* mOut2, int num_producers,
+                                          int overlapped) {
+    constexpr bool HAS_UP = MODE != 2, HAS_DN = MODE != 1, FUSED = MODE == 3;
     extern __shared__ uint8_t smem_raw[];
     const PairSmem sm = carve_pair(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     const bool producer = (int)blockIdx.x < num_producers;  // even: both CTAs of a cluster share the role
-    int MT = (MODE == 2) ? p.meta[META_MTILES] : 0;
-    int NI = p.meta[(MODE == 1) ? META_ITEMS_UP : META_ITEMS];
-    if (MT < 0 || MT > s.MT_max || NI < 0 || NI > ((MODE == 1) ? s.IU_max : MT)) MT = NI = 0;
-    const int nN = (MODE == 1) ? s.ffn / BN1 : s.n_tiles_n2;
-    const int KB = ((MODE == 1) ? s.d : s.ffn) / BK;
+    const bool gemm_cta = producer || FUSED;                 // fused: consumer clusters take SwiGLU tiles
+    const int E = s.E;
+    int MT = HAS_DN ? p.meta[META_MTILES] : 0;
+    int NU = HAS_UP ? p.meta[META_ITEMS_UP] : 0;
+    int ND = HAS_DN ? p.meta[META_ITEMS] : 0;
+    if (MT < 0 || MT > s.MT_max || NU < 0 || NU > s.IU_max || ND < 0 || ND > MT) MT = NU = ND = 0;
+    const int nN_up = s.ffn / BN1, nN_dn = s.n_tiles_n2;
+    const int KB_up = s.d / BK, KB_dn = s.ffn / BK;
     const unsigned long long tmo = s.timeout_ns;
-    const bool dispatch = MODE == 1 && (s.flags & MOE_FUSED_DISPATCH);
-    const int bad_item = __syncthreads_or(plan_items_bad(s, p, MODE, NI, MT));  // same answer in every CTA
-    if (bad_item) NI = 0;
+    const bool dispatch = HAS_UP && (s.flags & MOE_FUSED_DISPATCH);
+    const int bad_item = __syncthreads_or((HAS_UP ? plan_items_bad(s, p, 1, NU, MT) : 0) |
+                                          (HAS_DN ? plan_items_bad(s, p, 2, ND, MT) : 0));  // same in every CTA
+    if (bad_item) NU = ND = 0;
+    // expert tables: the down-projection's at tab ([cum (E+1) | first item (E) | items (E) | first
+    // direct item]); the SwiGLU one at tab in MODE 1, after the down-projection's in MODE 3 (with the
+    // experts' ids, as its experts are in hand-out order), then the SwiGLU tile quarters per expert
+    int* const tab_up = sm.tab + (FUSED ? 3 * E + 2 : 0);
+    int* const eid_up = tab_up + 3 * E + 1;
+    int* const xexp = eid_up + E;
 
     if (tid == 0) {
         for (int i = 0; i < PAIR_STAGES; ++i) {
@@ -914,26 +938,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             for (int i = 0; i < PAIR_TILE_Q; ++i) mbar_arrive_expect_tx(&sm.tq_full[i], 4);
     }
     if (MODE == 1) {
-        for (int e = tid; e < s.E; e += blockDim.x) {
-            sm.tab[(s.E + 1) + e] = p.experts[8 * e + 5];         // first work item
-            sm.tab[(s.E + 1) + s.E + e] = p.experts[8 * e + 4];   // work items
+        for (int e = tid; e < E; e += blockDim.x) {
+            sm.tab[(E + 1) + e] = p.experts[8 * e + 5];         // first work item
+            sm.tab[(E + 1) + E + e] = p.experts[8 * e + 4];     // work items
         }
         __syncthreads();
         if (tid == 0) {
             int acc = 0;
-            for (int e = 0; e < s.E; ++e) {
+            for (int e = 0; e < E; ++e) {
                 sm.tab[e] = acc;
-                acc += ((sm.tab[(s.E + 1) + s.E + e] + 1) >> 1) * nN;
+                acc += ((sm.tab[(E + 1) + E + e] + 1) >> 1) * nN_up;
             }
-            sm.tab[s.E] = acc;
+            sm.tab[E] = acc;
         }
     } else if (tid == 0) {
         // experts in hand-out order: each expert's down-projection items are contiguous in the item
-        // list, experts in hand-out order, so sorting the first items (0 <= first <= NI, checked by
+        // list, experts in hand-out order, so sorting the first items (0 <= first <= ND, checked by
         // plan_items_bad) gives the order and the item counts
-        int* first = sm.tab + (s.E + 1);
-        int* count = first + s.E;
-        for (int e = 0; e < s.E; ++e) {
+        int* first = sm.tab + (E + 1);
+        int* count = first + E;
+        for (int e = 0; e < E; ++e) {
             const int f = p.experts[8 * e + 6];
             int i = e;
             while (i > 0 && first[i - 1] > f) {
@@ -943,62 +967,93 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             first[i] = f;
         }
         int acc = 0;
-        for (int r = 0; r < s.E; ++r) {
-            count[r] = ((r + 1 < s.E) ? first[r + 1] : NI) - first[r];
+        for (int r = 0; r < E; ++r) {
+            count[r] = ((r + 1 < E) ? first[r + 1] : ND) - first[r];
             sm.tab[r] = acc;
-            acc += ((count[r] + 1) >> 1) * nN;
+            acc += ((count[r] + 1) >> 1) * nN_dn;
         }
-        sm.tab[s.E] = acc;
+        sm.tab[E] = acc;
         // MOE_DIRECT_TAIL: the first item of the first pair item whose first tile is among the last
         // `window` hand-out positions (the pair items' first tiles rise with the item index, so every
         // later item is in the window too); its epilogue and every later one's write into Ret
         int from = INT_MAX;
-        if (overlapped && (s.flags & MOE_DIRECT_TAIL) && NI > 0 && acc > 0) {
+        if (overlapped && (s.flags & MOE_DIRECT_TAIL) && ND > 0 && acc > 0) {
             const int window = s.tail_window > 0 ? s.tail_window : num_producers / 2, thr = acc - window;
-            from = NI;
-            for (int r = 0; r < s.E; ++r) {
+            from = ND;
+            for (int r = 0; r < E; ++r) {
                 const int np = (count[r] + 1) >> 1;
                 if (np == 0 || sm.tab[r + 1] <= thr) continue;
                 const bool n_outer = count[r] <= s.down_n_outer_items && sm.tab[r + 1] != acc;
                 const int rel = thr - sm.tab[r];
-                const int pi = rel <= 0 ? 0 : (n_outer ? rel : (rel + nN - 1) / nN);
+                const int pi = rel <= 0 ? 0 : (n_outer ? rel : (rel + nN_dn - 1) / nN_dn);
                 if (pi < np) {
                     from = first[r] + 2 * pi;
                     break;
                 }
             }
         }
-        sm.tab[3 * s.E + 1] = from;
+        sm.tab[3 * E + 1] = from;
+        if (FUSED) {
+            // SwiGLU table, experts in hand-out rank order (a permutation: the plan's ranks)
+            int* ufirst = tab_up + (E + 1);
+            int* ucount = ufirst + E;
+            for (int e = 0; e < E; ++e) {
+                const int r = min(max(p.experts[8 * e + 3], 0), E - 1);
+                ufirst[r] = p.experts[8 * e + 5];
+                ucount[r] = p.experts[8 * e + 4];
+                eid_up[r] = e;
+                xexp[e] = ((p.experts[8 * e + 4] + 1) >> 1) * nN_up * 8;  // epilogue warps of both CTAs
+            }
+            int uacc = 0;
+            for (int r = 0; r < E; ++r) {
+                tab_up[r] = uacc;
+                uacc += ((ucount[r] + 1) >> 1) * nN_up;
+            }
+            tab_up[E] = uacc;
+        }
     }
-    if (producer && warp == 1) {
+    if (gemm_cta && warp == 1) {
         __syncwarp();
         tmem_alloc_pair(sm.tmem_base, TMEM_COLS);
         tmem_relinquish_pair();
     }
     if (tid == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmAh);
-        tma_prefetch_desc(&tmB0);
-        tma_prefetch_desc(&tmB1);
-        tma_prefetch_desc(&tmOut);
+        tma_prefetch_desc(mA);
+        if (MODE == 2) tma_prefetch_desc(mAh);
+        tma_prefetch_desc(mB0);
+        tma_prefetch_desc(mB1);
+        tma_prefetch_desc(mOut);
+        if (FUSED) {
+            tma_prefetch_desc(mA2);
+            tma_prefetch_desc(mA2h);
+            tma_prefetch_desc(mB2);
+            tma_prefetch_desc(mOut2);
+        }
         if (MODE == 2 && producer) atomicMin(&p.trace[MOE_TRACE_GEMM2_START], globaltimer());
     }
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // both CTAs started, their barriers initialised and TMEM allocated
     tc_fence_after();
-    if (producer && rank == 1 && tid == 0) st_cluster_u32(mapa_shared(smem_u32(sm.peer_base), 0u), *sm.tmem_base);
+    if (gemm_cta && rank == 1 && tid == 0) st_cluster_u32(mapa_shared(smem_u32(sm.peer_base), 0u), *sm.tmem_base);
     cluster_sync();  // rank 1's column base delivered to rank 0
-    const uint32_t tmem = producer ? *sm.tmem_base : 0u;
-    const int total = (NI > 0 && sm.tab[s.E] > 0) ? sm.tab[s.E] : 0;
-    const bool bad = producer && rank == 0 && *sm.peer_base != tmem;  // not one pair allocation
+    const uint32_t tmem = gemm_cta ? *sm.tmem_base : 0u;
+    const int N_up = HAS_UP ? ((NU > 0 && tab_up[E] > 0) ? tab_up[E] : 0) : 0;  // SwiGLU pair tiles
+    const int N_dn = HAS_DN ? ((ND > 0 && sm.tab[E] > 0) ? sm.tab[E] : 0) : 0;  // down-projection pair tiles
+    const int total = N_up + N_dn;  // tile t: [0, N_up) SwiGLU, [N_up, total) down-projection
+    const bool bad = gemm_cta && rank == 0 && *sm.peer_base != tmem;  // not one pair allocation
     const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
-    int* const tile_counter = &p.meta[(MODE == 1) ? META_TILES_UP : META_TILES_DOWN];
     unsigned long long last_end = 0;
-    const int direct_from = (MODE == 2) ? sm.tab[3 * s.E + 1] : INT_MAX;
+    const int direct_from = HAS_DN ? sm.tab[3 * E + 1] : INT_MAX;
     uint32_t nk = 0;  // TMA thread: k-blocks whose loads this CTA issued (rank 0: armed and issued)
+    auto is_dn = [&](int t) { return MODE == 2 || (MODE == 3 && t >= N_up); };
+    auto decode = [&](int t) {
+        return is_dn(t) ? decode_pair_down(t - N_up, sm.tab, E, nN_dn, p.items_down, p.tiles, p.tile_crow, rank,
+                                           s.down_n_outer_items)
+                        : decode_pair_up(t, tab_up, E, p.items_up, rank, FUSED ? eid_up : nullptr);
+    };
 
-    if (producer) {
+    if (gemm_cta) {
         if (warp == 0 && lane == 0) {
             // ---------------- TMA producer (both CTAs): own A rows + own half of B ----------------
             // Rank 0 arms its full barrier with the stage's bytes of both CTAs; rank 1's loads
@@ -1007,10 +1062,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             int st = 0;
             uint32_t ph = 0;
             bool ok = true;
-            int ready_e = -1;  // fused dispatch: the expert whose rows are known to be copied
+            int ready_x = -1;  // fused dispatch: the expert whose rows are known to be copied
+            int ready_h = -1;  // fused GEMMs: the expert whose hidden rows are known to be complete
+            bool up_done = !HAS_UP, dn_started = false;
             const bool stall = (s.flags & (rank == 0 ? MOE_TEST_STALL_PIPE0 : MOE_TEST_STALL_PIPE1)) != 0;
-            const int claim_kb = KB > 8 ? KB - 8 : 0;
-            int t = (rank == 0 && !bad) ? atomicAdd(tile_counter, 1) : 0;
+            // rank 0: the next tile (fused: SwiGLU tiles first, down-projection tiles for producers)
+            auto claim = [&]() -> int {
+                if (!FUSED) return atomicAdd(&p.meta[(MODE == 1) ? META_TILES_UP : META_TILES_DOWN], 1);
+                if (!up_done) {
+                    const int v = atomicAdd(&p.meta[META_TILES_UP], 1);
+                    if (v < N_up) return v;
+                    up_done = true;
+                }
+                if (producer) {
+                    const int v = atomicAdd(&p.meta[META_TILES_DOWN], 1);
+                    if (v < N_dn) return N_up + v;
+                }
+                return total;
+            };
+            int t = (rank == 0 && !bad) ? claim() : 0;
             for (int j = 0; ok && !bad; ++j) {
                 const int slot = j % PAIR_TILE_Q;
                 if (rank == 0) {
@@ -1032,19 +1102,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     mbar_arrive_expect_tx(&sm.tq_full[slot], 4);  // armed for the slot's next use
                 }
                 if (t < 0 || t >= total) break;
-                const TileRef tr = (MODE == 1)
-                                       ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
-                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank,
-                                                          s.down_n_outer_items);
-                if (MODE == 1 && dispatch && tr.e != ready_e) {
+                const bool dn = is_dn(t);
+                const TileRef tr = decode(t);
+                if (HAS_UP && dispatch && !dn && tr.e != ready_x) {
                     if (!wait_expert_rows(s, p, tr.e, sm.abort, 30 + (int)rank)) {
                         ok = false;
                         break;
                     }
-                    ready_e = tr.e;
+                    ready_x = tr.e;
                 }
-                const bool halves = MODE == 2 && tr.mB >= 0 && tr.mB != tr.mA;  // two 64-row boxes
-                const int brow = (MODE == 1) ? tr.n * BN1 : tr.n * 2 * BN1 + (int)rank * BN1;
+                if (FUSED && dn && tr.e != ready_h) {
+                    // the expert's hidden rows are complete once every SwiGLU tile quarter of the
+                    // expert has published (stores completed, async proxy fenced, release add)
+                    const uint32_t need = (uint32_t)xexp[tr.e];
+                    const unsigned long long t0 = globaltimer();
+                    while (ld_acquire_gpu(p.xready + tr.e) < need) {
+                        if (*sm.abort || globaltimer() - t0 > tmo) {
+                            if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 20 + (int)rank);
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(128);
+                    }
+                    if (!ok) break;
+                    fence_proxy_async_global();  // the TMA loads below read what the acquire ordered
+                    ready_h = tr.e;
+                    if (rank == 0 && !dn_started) {
+                        dn_started = true;
+                        atomicMin(&p.trace[MOE_TRACE_GEMM2_START], globaltimer());
+                    }
+                }
+                const bool halves = dn && tr.mB >= 0 && tr.mB != tr.mA;  // two 64-row boxes
+                const int brow = dn ? tr.n * 2 * BN1 + (int)rank * BN1 : tr.n * BN1;
+                const CUtensorMap* ta = (FUSED && dn) ? mA2 : mA;
+                const CUtensorMap* tah = FUSED ? mA2h : mAh;
+                const CUtensorMap* tb = (FUSED && dn) ? mB2 : (rank == 0 ? mB0 : mB1);
+                const int KB = dn ? KB_dn : KB_up;
+                const int claim_kb = KB > 8 ? KB - 8 : 0;
                 const uint32_t bytes = 2 * (PAIR_A_BYTES + PAIR_B_BYTES);
                 int next = total;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -1056,7 +1150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    if (rank == 0 && kb == claim_kb) next = atomicAdd(tile_counter, 1);
+                    if (rank == 0 && kb == claim_kb) next = claim();
                     if (!mbar_wait(&sm.empty[st], ph ^ 1u, tmo, sm.abort)) {
                         ok = false;
                         break;
@@ -1066,23 +1160,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     if (rank == 0) {
                         mbar_arrive_expect_tx(&sm.full[st], bytes);
                         if (halves) {
-                            tma_load_2d(a, &tmAh, &sm.full[st], kb * BK, tr.lrowA);
-                            tma_load_2d(a + PAIR_A_BYTES / 2, &tmAh, &sm.full[st], kb * BK, tr.lrowB);
+                            tma_load_2d(a, tah, &sm.full[st], kb * BK, tr.lrowA);
+                            tma_load_2d(a + PAIR_A_BYTES / 2, tah, &sm.full[st], kb * BK, tr.lrowB);
                         } else if (tr.mA >= 0) {
-                            tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
+                            tma_load_2d(a, ta, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
                         }
-                        tma_load_3d(b, &tmB0, &sm.full[st], kb * BK, brow, tr.e);  // gate rows / W2 rows 0-127
+                        tma_load_3d(b, tb, &sm.full[st], kb * BK, brow, tr.e);  // gate rows / W2 rows 0-127
                     } else {
                         const uint32_t full0 = mapa_shared(smem_u32(&sm.full[st]), 0u);
                         // an odd CTA without rows loads a box past the last row: zeros, so its idle
                         // half of the UMMA multiplies zeros (less switching power than stale rows)
                         if (halves) {
-                            tma_load_2d_pair(a, &tmAh, full0, kb * BK, tr.lrowA);
-                            tma_load_2d_pair(a + PAIR_A_BYTES / 2, &tmAh, full0, kb * BK, tr.lrowB);
+                            tma_load_2d_pair(a, tah, full0, kb * BK, tr.lrowA);
+                            tma_load_2d_pair(a + PAIR_A_BYTES / 2, tah, full0, kb * BK, tr.lrowB);
                         } else {
-                            tma_load_2d_pair(a, &tmA, full0, kb * BK, tr.mA >= 0 ? tr.lrowA : s.PC_max);
+                            tma_load_2d_pair(a, ta, full0, kb * BK, tr.mA >= 0 ? tr.lrowA : s.PC_max);
                         }
-                        tma_load_3d_pair(b, &tmB1, full0, kb * BK, brow, tr.e);  // up rows / W2 rows 128-255
+                        tma_load_3d_pair(b, tb, full0, kb * BK, brow, tr.e);  // up rows / W2 rows 128-255
                     }
                     ++nk;
                     if (++st == PAIR_STAGES) {
@@ -1117,6 +1211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     }
                     mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
                     if (t < 0) break;
+                    const int KB = is_dn(t) ? KB_dn : KB_up;
                     if (!mbar_wait_cluster(&sm.acc_empty[b], aph ^ 1u, tmo, sm.abort)) {
                         ok = false;
                         break;
@@ -1160,8 +1255,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         } else if (warp >= 2) {
             // ---------------- epilogue (both CTAs): this CTA's 128 rows ----------------
             const int q = warp & 3;
-            const bool flags = (MODE == 2) && overlapped;
-            if (MODE == 1 && dispatch) dispatch_rows(s, p);
+            const bool flags = HAS_DN && overlapped;
+            if (HAS_UP && dispatch) dispatch_rows(s, p);
             EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
             const uint32_t acc_empty0 = mapa_shared(smem_u32(sm.acc_empty), 0u);
             const uint32_t tq_empty0 = mapa_shared(smem_u32(sm.tq_empty), 0u);
@@ -1185,10 +1280,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     break;
                 }
                 if (t < 0) break;
-                const TileRef tr = (MODE == 1)
-                                       ? decode_pair_up(t, sm.tab, s.E, p.items_up, rank)
-                                       : decode_pair_down(t, sm.tab, s.E, nN, p.items_down, p.tiles, p.tile_crow, rank,
-                                                          s.down_n_outer_items);
+                const bool dn = is_dn(t);
+                const TileRef tr = decode(t);
                 if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
                     if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 16 + (int)rank);
                     if (lane == 0) pair_abort(sm, rank);
@@ -1200,13 +1293,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                 const int mq = (q < 2) ? tr.mA : tr.mB;
                 const bool active = mq >= 0;
                 const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
-                const DirectDst dd = (MODE == 2 && active && tr.item >= direct_from) ? direct_dst(s, p, tr, q)
-                                                                                   : DirectDst{nullptr, 0};
-                epilogue_rows<MODE>(es, &tmOut, tb, tr.n, 2 * BN1, y, active, lane, dd, (size_t)s.d * 2);
+                if (dn) {
+                    const DirectDst dd = (active && tr.item >= direct_from) ? direct_dst(s, p, tr, q)
+                                                                            : DirectDst{nullptr, 0};
+                    epilogue_rows<2>(es, FUSED ? mOut2 : mOut, tb, tr.n, 2 * BN1, y, active, lane, dd,
+                                     (size_t)s.d * 2);
+                } else {
+                    epilogue_rows<1>(es, mOut, tb, tr.n, 2 * BN1, y, active, lane);
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(acc_empty0 + b * 8u);
-                if (MODE == 2 && active) {
+                if (dn && active) {
                     if (flags && lane == 0) {
                         // publish this warp's rows of the tile, as in gemm_kernel: stores complete,
                         // async proxy fenced, then the release adds to the tile flag and band counter
@@ -1223,6 +1321,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     }
                     __syncwarp();
                     if (lane == 0) last_end = globaltimer();
+                }
+                if (FUSED && !dn && lane == 0) {
+                    // this warp's quarter of the SwiGLU tile (stored or idle) counts towards its
+                    // expert's hidden rows being complete: stores complete, async proxy fenced, release
+                    bulk_wait_all();
+                    fence_proxy_async_global();
+                    __threadfence();
+                    red_release_gpu_add(p.xready + tr.e, 1u);
                 }
                 b ^= 1;
                 if (b == 0) aph ^= 1u;
@@ -1250,11 +1356,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         }
         __syncwarp();
         cluster_sync();  // neither CTA goes on (or leaves) while the pair's TMEM release is in progress
-        if (MODE == 2 && warp >= 2 && lane == 0 && last_end) atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
+        if (HAS_DN && warp >= 2 && lane == 0 && last_end) atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
     }
-    // copy engines: consumer CTAs from the start, producers once their tiles are done (tail assist)
-    if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
+    // copy engines: consumer CTAs from the start (fused: after their SwiGLU tiles), producers once
+    // their tiles are done (tail assist)
+    if (HAS_DN && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
         copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want, direct_from);
+}
+
+template <int MODE>  // 1: SwiGLU up-projection -> Hc; 2: down-projection -> Yp (+ flags / consumers)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+    gemm_pair_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmB0,
+                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut,
+                     int num_producers, int overlapped) {
+    pair_body<MODE>(s, p, &tmA, &tmAh, &tmB0, &tmB1, &tmOut, nullptr, nullptr, nullptr, nullptr, num_producers,
+                    overlapped);
+}
+
+// Both expert GEMMs in one launch (MOE_FUSED_GEMMS): the MODE 3 body.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+    gemm_fused_pair_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmXc,
+                           const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW3,
+                           const __grid_constant__ CUtensorMap tmHcOut, const __grid_constant__ CUtensorMap tmHc,
+                           const __grid_constant__ CUtensorMap tmHch, const __grid_constant__ CUtensorMap tmW2h,
+                           const __grid_constant__ CUtensorMap tmYpOut, int num_producers) {
+    pair_body<3>(s, p, &tmXc, nullptr, &tmW1, &tmW3, &tmHcOut, &tmHc, &tmHch, &tmW2h, &tmYpOut, num_producers, 1);
 }
 
 static cudaError_t set_smem_attr(const void* fn) {
@@ -1319,6 +1446,36 @@ cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUten
     if ((consumers & 1) || producers < 2) return cudaErrorInvalidConfiguration;
     gemm_pair_kernel<2><<<grid, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmAh, tmW2h, tmW2h, tmOut, producers,
                                                                overlapped ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmXc, const CUtensorMap& tmW1,
+                                   const CUtensorMap& tmW3, const CUtensorMap& tmHcOut, const CUtensorMap& tmHc,
+                                   const CUtensorMap& tmHch, const CUtensorMap& tmW2h, const CUtensorMap& tmYpOut,
+                                   int consumers, cudaStream_t st) {
+    const void* fn = reinterpret_cast<const void*>(&gemm_fused_pair_kernel);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_FUSED);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static int cache[64] = {0};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (cache[dev] == 0) {
+        cudaLaunchConfig_t q = {};  // the cluster size (2) is the kernel's compile-time one
+        q.gridDim = dim3(2, 1, 1);
+        q.blockDim = dim3(GEMM_THREADS, 1, 1);
+        q.dynamicSmemBytes = PAIR_SMEM_FUSED;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, fn, &q);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        cache[dev] = n;
+    }
+    const int grid = 2 * cache[dev], producers = grid - consumers;
+    if ((consumers & 1) || producers < 2) return cudaErrorInvalidConfiguration;
+    gemm_fused_pair_kernel<<<grid, GEMM_THREADS, PAIR_SMEM_FUSED, st>>>(s, p, tmXc, tmW1, tmW3, tmHcOut, tmHc, tmHch,
+                                                                        tmW2h, tmYpOut, producers);
     return cudaGetLastError();
 }
 

@@ -119,6 +119,7 @@ int make_layout(const moe_config* c, Layout* out) {
     L.band_item = put(MT_max * 4);
     L.tok_of = put(PC_max * 4);
     L.xrows = put(E * 4);
+    L.xready = put(E * 4);
     L.meta = put(META_COUNT * 4);
     L.flags = put(MT_max * nN2 * 4);
     L.bands = put(MT_max * 4);
@@ -195,6 +196,7 @@ PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     p.band_item = reinterpret_cast<int32_t*>(b + L.band_item);
     p.tok_of = reinterpret_cast<int32_t*>(b + L.tok_of);
     p.xrows = reinterpret_cast<uint32_t*>(b + L.xrows);
+    p.xready = reinterpret_cast<uint32_t*>(b + L.xready);
     p.meta = reinterpret_cast<int32_t*>(b + L.meta);
     p.flags = reinterpret_cast<uint32_t*>(b + L.flags);
     p.bands = reinterpret_cast<uint32_t*>(b + L.bands);
@@ -352,8 +354,20 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     rc = run_plan(c, logits, x, !fused_dispatch);
     if (rc) return rc;
     if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
-    cudaError_t e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.st)
-                                              : launch_gemm_swiglu(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.di.sms, c.st);
+    cudaError_t e;
+    if (overlapped && pair_down && (S.flags & MOE_FUSED_GEMMS)) {
+        // both GEMMs in one launch: the stage events after it mark the end of both
+        e = launch_gemm_fused_pair(S, c.p, tXc, tW1, tW3, tHcOut, tHc, tHch, tW2h, tYpOut, c.consumers, c.st);
+        if (e != cudaSuccess) return cuda_fail(e, "fused GEMM launch");
+        if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
+        if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
+        if ((rc = record(ev, MOE_EV_COPIED, c.st))) return rc;
+        e = launch_combine(S, c.p, out, c.di.sms, c.st);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+        return record(ev, MOE_EV_END, c.st);
+    }
+    e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.st)
+                                  : launch_gemm_swiglu(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.di.sms, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
     if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
     if (overlapped) {
@@ -390,7 +404,7 @@ namespace {
 // Offsets of the plan's scratch regions inside the static array for one config (256-byte aligned).
 struct StaticLayout {
     size_t rank, cnt, base, counts, ret, tiles, tret, sched, order, seg, exp, iu, id, meta, flags, bands, trace,
-        cslot, ccoff, tcrow, bitem, tokof, xrows, bytes;
+        cslot, ccoff, tcrow, bitem, tokof, xrows, xready, bytes;
 };
 
 StaticLayout static_layout(const Layout& lay) {
@@ -427,6 +441,7 @@ StaticLayout static_layout(const Layout& lay) {
     o.bitem = put(MT * 4);
     o.tokof = put((size_t)L.PC_max * 4);
     o.xrows = put(E * 4);
+    o.xready = put(E * 4);
     o.bytes = cur;
     return o;
 }
@@ -991,6 +1006,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.band_item = reinterpret_cast<int32_t*>(b + o.bitem);
     p.tok_of = reinterpret_cast<int32_t*>(b + o.tokof);
     p.xrows = reinterpret_cast<uint32_t*>(b + o.xrows);
+    p.xready = reinterpret_cast<uint32_t*>(b + o.xready);
     p.meta = reinterpret_cast<int32_t*>(b + o.meta);
     p.flags = reinterpret_cast<uint32_t*>(b + o.flags);
     p.bands = reinterpret_cast<uint32_t*>(b + o.bands);

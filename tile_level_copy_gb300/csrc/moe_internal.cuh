@@ -75,6 +75,9 @@ constexpr int PAIR_B_BYTES = 128 * BK * 2;             // 16 KB
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_SMEM = PAIR_STAGES * PAIR_STAGE_BYTES + EPI_BYTES + MISC_BYTES + 1024;
 static_assert(PAIR_SMEM <= 227 * 1024, "pair GEMM shared memory");
+// the fused launch of both GEMMs (MOE_FUSED_GEMMS) keeps two expert tables and the SwiGLU tile counts
+constexpr int PAIR_SMEM_FUSED = PAIR_SMEM + 4096;
+static_assert(PAIR_SMEM_FUSED <= 227 * 1024, "fused pair GEMM shared memory");
 constexpr int BN1 = 128;                               // output columns of a SwiGLU tile
 constexpr uint32_t FLAG_READY = 4;                     // one release-add per epilogue warp
 constexpr int MAX_E = 256;
@@ -121,6 +124,7 @@ struct PlanPtrs {
     const __nv_bfloat16* x;  // tokens [T, d] (MOE_FUSED_DISPATCH: read by the SwiGLU GEMM)
     int32_t* tok_of;     // [PC_max] token of each compact row, -1 for a padding row
     uint32_t* xrows;     // [E] compact rows of each expert copied so far (MOE_FUSED_DISPATCH)
+    uint32_t* xready;    // [E] SwiGLU tile quarters of each expert published (MOE_FUSED_GEMMS)
     __nv_bfloat16* Xc;
     __nv_bfloat16* Hc;
     __nv_bfloat16* Yp;
@@ -165,6 +169,13 @@ cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMa
 cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
                                   const CUtensorMap& tmW2h, const CUtensorMap& tmOut, int consumers, bool overlapped,
                                   cudaStream_t st);
+// Both expert GEMMs in one launch on CTA pairs (MOE_FUSED_GEMMS): SwiGLU operands (Xc, W1, W3, Hc
+// store) and down-projection operands (Hc, Hc halves, W2 halves, Yp store); the last `consumers`
+// (even) CTAs copy once the SwiGLU tiles are gone.
+cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmXc, const CUtensorMap& tmW1,
+                                   const CUtensorMap& tmW3, const CUtensorMap& tmHcOut, const CUtensorMap& tmHc,
+                                   const CUtensorMap& tmHch, const CUtensorMap& tmW2h, const CUtensorMap& tmYpOut,
+                                   int consumers, cudaStream_t st);
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
 

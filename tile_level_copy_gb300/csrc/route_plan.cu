@@ -570,7 +570,10 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     const int nflags = min(MT, s.MT_max) * s.n_tiles_n2;
     for (int i = tid; i < nflags; i += PLAN_THREADS) p.flags[i] = 0u;
     for (int i = tid; i < min(MT, s.MT_max); i += PLAN_THREADS) p.bands[i] = 0u;
-    for (int e = tid; e < E; e += PLAN_THREADS) p.xrows[e] = 0u;
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        p.xrows[e] = 0u;
+        p.xready[e] = 0u;
+    }
 }
 
 cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
