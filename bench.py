@@ -91,6 +91,9 @@ def parse_args():
                          "choice is timed beside in the same alternation)")
     ap.add_argument("--fused-gemms", action=argparse.BooleanOptionalAction, default=False,
                     help="both expert GEMMs in one launch (the other choice is timed beside in the same alternation)")
+    ap.add_argument("--pdl", action=argparse.BooleanOptionalAction, default=True,
+                    help="programmatic dependent launch between the layer's kernels (the other choice is timed "
+                         "beside in the same alternation)")
     ap.add_argument("--tail-window", type=int, default=0,
                     help="tile hand-out positions of the direct tail (0: one wave)")
     ap.add_argument("--dma", action=argparse.BooleanOptionalAction, default=True,
@@ -312,14 +315,15 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------------- our arm
 def default_flags(copy_warps: bool, direct_tail: bool = True, tail_assist: bool = True, pair: bool = True,
-                  fused_dispatch: bool = False, fused_gemms: bool = False) -> int:
+                  fused_dispatch: bool = False, fused_gemms: bool = False, pdl: bool = True) -> int:
     """The bench's launch configuration: both expert GEMMs on CTA pairs, finished producers joining
-    the copy, the last wave's bands returned by the down-projection's epilogue, and (per workload)
-    the producers' copy warps."""
+    the copy, the last wave's bands returned by the down-projection's epilogue, programmatic
+    dependent launch between the kernels, and (per workload) the producers' copy warps."""
     import tile_level_copy_gb300 as tlc
     return ((tlc.MOE_TAIL_ASSIST if tail_assist else 0) | (tlc.MOE_COPY_WARPS if copy_warps else 0) |
             (tlc.MOE_PAIR_UMMA if pair else 0) | (tlc.MOE_DIRECT_TAIL if direct_tail else 0) |
-            (tlc.MOE_FUSED_DISPATCH if fused_dispatch else 0) | (tlc.MOE_FUSED_GEMMS if fused_gemms else 0))
+            (tlc.MOE_FUSED_DISPATCH if fused_dispatch else 0) | (tlc.MOE_FUSED_GEMMS if fused_gemms else 0) |
+            (tlc.MOE_PDL if pdl else 0))
 
 
 class LayerBench:
@@ -467,7 +471,8 @@ def run_ours(args, rank: int, world: int):
         args.copy_warps = dw
     seed = args.seed + rank
     flags = default_flags(args.copy_warps, direct_tail=args.direct_tail, tail_assist=not args.no_tail_assist,
-                          pair=args.pair_umma, fused_dispatch=args.fused_dispatch, fused_gemms=args.fused_gemms)
+                          pair=args.pair_umma, fused_dispatch=args.fused_dispatch, fused_gemms=args.fused_gemms,
+                          pdl=args.pdl)
     cfg = tlc.Config.from_workload(w, consumer_ctas=args.consumers, mgb=args.mgb, flags=flags,
                                    tail_window=args.tail_window)
     peaks, peaks_src = load_peaks()
@@ -538,6 +543,10 @@ def run_ours(args, rank: int, world: int):
     fused_gemms = bool(cfg.flags & tlc.MOE_FUSED_GEMMS)
     other_gemms = "overlapped_separate_gemms" if fused_gemms else "overlapped_fused_gemms"
     arms[other_gemms] = (dataclasses.replace(cfg, flags=cfg.flags ^ tlc.MOE_FUSED_GEMMS), False)
+    # programmatic dependent launch between the kernels against serial launches
+    pdl = bool(cfg.flags & tlc.MOE_PDL)
+    other_pdl = "overlapped_serial_launches" if pdl else "overlapped_pdl"
+    arms[other_pdl] = (dataclasses.replace(cfg, flags=cfg.flags ^ tlc.MOE_PDL), False)
     eager_arms = dict(arms)
     if args.dma:  # the copy-engine variant: eager only (its host thread issues the copies)
         eager_arms["copy_engines"] = (cfg, "dma")
@@ -716,6 +725,11 @@ def run_ours(args, rank: int, world: int):
         "paired_spread_ms": round(spread_ms(rep[other_dispatch] - rep["overlapped"]), 4),
         "swiglu_and_permute_ms": {a: round(stage_med[a]["route_plan_permute"] + stage_med[a]["swiglu_gemm"], 4)
                                   for a in ("overlapped", other_dispatch)}}
+    overlap["launch_dependencies"] = {
+        "default": "programmatic dependent launch" if pdl else "serial launches",
+        "other": other_pdl, "ms_per_step": round(med[other_pdl], 4),
+        "paired_diff_other_minus_default_ms": round(float(np.median(rep[other_pdl] - rep["overlapped"])), 4),
+        "paired_spread_ms": round(spread_ms(rep[other_pdl] - rep["overlapped"]), 4)}
     overlap["gemm_launches"] = {
         "default": "one launch for both GEMMs" if fused_gemms else "a launch per GEMM",
         "other": other_gemms, "ms_per_step": round(med[other_gemms], 4),
@@ -760,7 +774,7 @@ def run_ours(args, rank: int, world: int):
                    "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps),
                    "pair_umma": bool(args.pair_umma), "mgb": args.mgb, "direct_tail": direct,
                    "tail_window": args.tail_window, "fused_dispatch": bool(args.fused_dispatch),
-                   "fused_gemms": bool(args.fused_gemms),
+                   "fused_gemms": bool(args.fused_gemms), "pdl": bool(args.pdl),
                    "tail_assist": not args.no_tail_assist, "seed": args.seed,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "

@@ -82,6 +82,12 @@ extern "C" {
                                       /* tiles first; an expert's down-projection tiles start */
                                       /* once all its SwiGLU tiles have published; the        */
                                       /* consumer clusters take SwiGLU tiles, then copy       */
+#define MOE_PDL 0x80u                 /* programmatic dependent launch between the layer's    */
+                                      /* kernels: each starts its prologue (barriers, TMEM,   */
+                                      /* descriptor prefetch, plan tables) while the previous */
+                                      /* one finishes and waits on the GPU before reading its */
+                                      /* outputs (not for the cooperative single-CTA down-    */
+                                      /* projection, nor for the first kernel of the layer)   */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
 #define MOE_TEST_PLAN_FAIL 0x200u     /* test hook: the plan kernel reports a failed bounds   */

@@ -31,6 +31,7 @@ MOE_PAIR_UMMA = 0x8
 MOE_DIRECT_TAIL = 0x10
 MOE_FUSED_DISPATCH = 0x20
 MOE_FUSED_GEMMS = 0x40
+MOE_PDL = 0x80
 MOE_TEST_STALL_CONSUMER = 0x100
 MOE_TEST_PLAN_FAIL = 0x200
 MOE_TEST_STALL_PIPE0 = 0x400

@@ -12,6 +12,7 @@ namespace moe {
 // k loads in flight instead of one.
 template <int K>  // K = top-k, so that the per-lane arrays have exactly K entries
 __global__ void __launch_bounds__(256, 4) combine_kernel(Shape s, PlanPtrs p, float* __restrict__ out) {
+    griddep_wait();  // the return copy (and every row of Ret) is complete
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int vec = s.d / 8;
@@ -71,18 +72,19 @@ __global__ void __launch_bounds__(256, 4) combine_kernel(Shape s, PlanPtrs p, fl
 
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st) {
     const int blocks = min((s.T + 7) / 8, sms * 8);
+    const bool pdl = (s.flags & MOE_PDL) != 0;
+    const dim3 g(blocks), b(256);
     switch (s.k) {
-        case 1: combine_kernel<1><<<blocks, 256, 0, st>>>(s, p, out); break;
-        case 2: combine_kernel<2><<<blocks, 256, 0, st>>>(s, p, out); break;
-        case 3: combine_kernel<3><<<blocks, 256, 0, st>>>(s, p, out); break;
-        case 4: combine_kernel<4><<<blocks, 256, 0, st>>>(s, p, out); break;
-        case 5: combine_kernel<5><<<blocks, 256, 0, st>>>(s, p, out); break;
-        case 6: combine_kernel<6><<<blocks, 256, 0, st>>>(s, p, out); break;
-        case 7: combine_kernel<7><<<blocks, 256, 0, st>>>(s, p, out); break;
-        case 8: combine_kernel<8><<<blocks, 256, 0, st>>>(s, p, out); break;
+        case 1: return launch_k(combine_kernel<1>, g, b, 0, st, pdl, s, p, out);
+        case 2: return launch_k(combine_kernel<2>, g, b, 0, st, pdl, s, p, out);
+        case 3: return launch_k(combine_kernel<3>, g, b, 0, st, pdl, s, p, out);
+        case 4: return launch_k(combine_kernel<4>, g, b, 0, st, pdl, s, p, out);
+        case 5: return launch_k(combine_kernel<5>, g, b, 0, st, pdl, s, p, out);
+        case 6: return launch_k(combine_kernel<6>, g, b, 0, st, pdl, s, p, out);
+        case 7: return launch_k(combine_kernel<7>, g, b, 0, st, pdl, s, p, out);
+        case 8: return launch_k(combine_kernel<8>, g, b, 0, st, pdl, s, p, out);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -466,6 +466,8 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_wait();  // MOE_PDL: the previous kernel's outputs (the plan tables above were complete before)
+    griddep_launch();
     const uint32_t tmem = producer ? *sm.tmem_base : 0u;
     unsigned long long last_end = 0;
     const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
@@ -1037,6 +1039,10 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
     tc_fence_after();
     if (gemm_cta && rank == 1 && tid == 0) st_cluster_u32(mapa_shared(smem_u32(sm.peer_base), 0u), *sm.tmem_base);
     cluster_sync();  // rank 1's column base delivered to rank 0
+    // MOE_PDL: this launch may have started while the previous kernel was finishing; wait for its
+    // outputs here. The plan tables read above were complete before that kernel started.
+    griddep_wait();
+    griddep_launch();
     const uint32_t tmem = gemm_cta ? *sm.tmem_base : 0u;
     const int N_up = HAS_UP ? ((NU > 0 && tab_up[E] > 0) ? tab_up[E] : 0) : 0;  // SwiGLU pair tiles
     const int N_dn = HAS_DN ? ((ND > 0 && sm.tab[E] > 0) ? sm.tab[E] : 0) : 0;  // down-projection pair tiles
@@ -1393,8 +1399,8 @@ cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensor
                                cudaStream_t st) {
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<1>));
     if (e != cudaSuccess) return e;
-    gemm_kernel<1><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(s, p, tmA, tmAh, tmW1, tmW3, tmOut, sms, 0);
-    return cudaGetLastError();
+    return launch_k(gemm_kernel<1>, dim3(sms), dim3(GEMM_THREADS), GEMM_SMEM, st, (s.flags & MOE_PDL) != 0, s, p, tmA,
+                    tmAh, tmW1, tmW3, tmOut, sms, 0);
 }
 
 // Co-resident clusters of two of a pair kernel on this device (cluster occupancy query, cached).
@@ -1429,8 +1435,8 @@ cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUt
     int pairs = 0;
     cudaError_t e = pair_clusters<1>(&pairs);
     if (e != cudaSuccess) return e;
-    gemm_pair_kernel<1><<<2 * pairs, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmAh, tmW1, tmW3, tmOut, 2 * pairs, 0);
-    return cudaGetLastError();
+    return launch_k(gemm_pair_kernel<1>, dim3(2 * pairs), dim3(GEMM_THREADS), PAIR_SMEM, st, (s.flags & MOE_PDL) != 0,
+                    s, p, tmA, tmAh, tmW1, tmW3, tmOut, 2 * pairs, 0);
 }
 
 // Down-projection on CTA pairs: 2 x (co-resident clusters) CTAs, the last `consumers` (even) of them
@@ -1444,9 +1450,8 @@ cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUten
     if (e != cudaSuccess) return e;
     const int grid = 2 * pairs, producers = overlapped ? grid - consumers : grid;
     if ((consumers & 1) || producers < 2) return cudaErrorInvalidConfiguration;
-    gemm_pair_kernel<2><<<grid, GEMM_THREADS, PAIR_SMEM, st>>>(s, p, tmA, tmAh, tmW2h, tmW2h, tmOut, producers,
-                                                               overlapped ? 1 : 0);
-    return cudaGetLastError();
+    return launch_k(gemm_pair_kernel<2>, dim3(grid), dim3(GEMM_THREADS), PAIR_SMEM, st, (s.flags & MOE_PDL) != 0, s, p,
+                    tmA, tmAh, tmW2h, tmW2h, tmOut, producers, overlapped ? 1 : 0);
 }
 
 cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmXc, const CUtensorMap& tmW1,
@@ -1474,9 +1479,8 @@ cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUte
     }
     const int grid = 2 * cache[dev], producers = grid - consumers;
     if ((consumers & 1) || producers < 2) return cudaErrorInvalidConfiguration;
-    gemm_fused_pair_kernel<<<grid, GEMM_THREADS, PAIR_SMEM_FUSED, st>>>(s, p, tmXc, tmW1, tmW3, tmHcOut, tmHc, tmHch,
-                                                                        tmW2h, tmYpOut, producers);
-    return cudaGetLastError();
+    return launch_k(gemm_fused_pair_kernel, dim3(grid), dim3(GEMM_THREADS), PAIR_SMEM_FUSED, st,
+                    (s.flags & MOE_PDL) != 0, s, p, tmXc, tmW1, tmW3, tmHcOut, tmHc, tmHch, tmW2h, tmYpOut, producers);
 }
 
 cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,

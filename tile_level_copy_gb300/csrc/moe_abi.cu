@@ -1013,6 +1013,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.trace = reinterpret_cast<unsigned long long*>(b + o.trace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the plan-only kernels: no token rows are moved (x = NULL), whatever cfg->flags says
+    lay.S.flags &= MOE_TEST_PLAN_FAIL;
     cudaError_t e = launch_route(lay.S, logits, p, st);
     if (e == cudaSuccess) e = launch_plan(lay.S, p, st);
     if (e == cudaSuccess) e = launch_permute(lay.S, nullptr, p, di.sms, st);

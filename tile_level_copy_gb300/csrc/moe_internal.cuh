@@ -179,6 +179,25 @@ cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUte
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
 
+// Launch with or without programmatic dependent launch (PDL, MOE_PDL): with it the kernel may start
+// before the previous kernel on the stream has finished; it must call griddep_wait() before it
+// touches that kernel's outputs (every kernel launched this way does, after its prologue).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                           Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Copy units of a call with MT bands: the last min(tail_bands, MT) bands in hand-out order are cut
 // into smaller units than the others, so the copy after the last tile spreads over more engines.
 __host__ __device__ inline int copy_unit_count(const Shape& s, int MT) {
@@ -215,6 +234,12 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+
+// Programmatic dependent launch: wait until the grids this launch depends on have completed and
+// their writes are visible (a no-op for a launch without a programmatic dependency), and let the
+// next launch on the stream start its prologue (it waits the same way before reading ours).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Record the first error of a call in the status word.
 __device__ __forceinline__ void set_status(int32_t* meta, int code, int detail) {

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
     __shared__ uint32_t s_mask[ROUTE_THREADS / 32][MAX_E];
     __shared__ int32_t s_wpre[ROUTE_THREADS / 32][MAX_E];
 
+    griddep_launch();  // the plan kernel may start (it waits for this grid before reading)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int C = s.chunk_tokens, E = s.E, ld = E + 1;
     int* s_te = reinterpret_cast<int*>(s_logit + C * ld);
@@ -245,6 +246,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* s_t
 }
 
 __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p) {
+    griddep_wait();  // the routing kernel's counts
+    griddep_launch();
     __shared__ int s_n[1024];        // n_{e,r}, group g = e*R + r
     __shared__ int s_off[1025];
     __shared__ int s_load[MAX_E];    // rows per expert
@@ -584,8 +587,7 @@ cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
                                  (int)smem);
         if (e != cudaSuccess) return e;
     }
-    plan_kernel<<<1, PLAN_THREADS, smem, st>>>(s, p);
-    return cudaGetLastError();
+    return launch_k(plan_kernel, dim3(1), dim3(PLAN_THREADS), smem, st, (s.flags & MOE_PDL) != 0, s, p);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -599,6 +601,8 @@ cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
 constexpr int PERM_VEC = 16;  // 16-byte vectors per lane per pass
 
 __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat16* __restrict__ x, PlanPtrs p) {
+    griddep_wait();  // the plan
+    griddep_launch();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int PC = p.meta[META_PC];
@@ -673,8 +677,7 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
 cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtrs& p, int sms, cudaStream_t st) {
     const int items = s.T + s.E * (BM / 8);
     const int blocks = min((items + 7) / 8, sms * 16);
-    permute_kernel<<<blocks, 256, 0, st>>>(s, x, p);
-    return cudaGetLastError();
+    return launch_k(permute_kernel, dim3(blocks), dim3(256), 0, st, (s.flags & MOE_PDL) != 0, s, x, p);
 }
 
 }  // namespace moe
