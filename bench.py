@@ -91,9 +91,11 @@ def parse_args():
                          "choice is timed beside in the same alternation)")
     ap.add_argument("--fused-gemms", action=argparse.BooleanOptionalAction, default=False,
                     help="both expert GEMMs in one launch (the other choice is timed beside in the same alternation)")
-    ap.add_argument("--pdl", action=argparse.BooleanOptionalAction, default=True,
-                    help="programmatic dependent launch between the layer's kernels (the other choice is timed "
-                         "beside in the same alternation)")
+    ap.add_argument("--pdl", action=argparse.BooleanOptionalAction, default=None,
+                    help="programmatic dependent launch between the layer's kernels (default: on unless the copy "
+                         "warps run; the other choice is timed beside in the same alternation)")
+    ap.add_argument("--alt-consumers", type=int, nargs="*", default=[],
+                    help="also time these consumer partitions in the alternation")
     ap.add_argument("--tail-window", type=int, default=0,
                     help="tile hand-out positions of the direct tail (0: one wave)")
     ap.add_argument("--dma", action=argparse.BooleanOptionalAction, default=True,
@@ -315,11 +317,15 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------------- our arm
 def default_flags(copy_warps: bool, direct_tail: bool = True, tail_assist: bool = True, pair: bool = True,
-                  fused_dispatch: bool = False, fused_gemms: bool = False, pdl: bool = True) -> int:
+                  fused_dispatch: bool = False, fused_gemms: bool = False, pdl=None) -> int:
     """The bench's launch configuration: both expert GEMMs on CTA pairs, finished producers joining
-    the copy, the last wave's bands returned by the down-projection's epilogue, programmatic
-    dependent launch between the kernels, and (per workload) the producers' copy warps."""
+    the copy, the last wave's bands returned by the down-projection's epilogue, and (per workload)
+    the producers' copy warps; programmatic dependent launch between the kernels unless the copy
+    warps run (their down-projection is the cooperative single-CTA kernel, with which it measured
+    slower)."""
     import tile_level_copy_gb300 as tlc
+    if pdl is None:
+        pdl = not copy_warps
     return ((tlc.MOE_TAIL_ASSIST if tail_assist else 0) | (tlc.MOE_COPY_WARPS if copy_warps else 0) |
             (tlc.MOE_PAIR_UMMA if pair else 0) | (tlc.MOE_DIRECT_TAIL if direct_tail else 0) |
             (tlc.MOE_FUSED_DISPATCH if fused_dispatch else 0) | (tlc.MOE_FUSED_GEMMS if fused_gemms else 0) |
@@ -543,6 +549,9 @@ def run_ours(args, rank: int, world: int):
     fused_gemms = bool(cfg.flags & tlc.MOE_FUSED_GEMMS)
     other_gemms = "overlapped_separate_gemms" if fused_gemms else "overlapped_fused_gemms"
     arms[other_gemms] = (dataclasses.replace(cfg, flags=cfg.flags ^ tlc.MOE_FUSED_GEMMS), False)
+    # another consumer partition, when asked for (same flags otherwise)
+    for c_alt in args.alt_consumers:
+        arms[f"overlapped_c{c_alt}"] = (dataclasses.replace(cfg, consumer_ctas=c_alt), False)
     # programmatic dependent launch between the kernels against serial launches
     pdl = bool(cfg.flags & tlc.MOE_PDL)
     other_pdl = "overlapped_serial_launches" if pdl else "overlapped_pdl"
@@ -725,6 +734,14 @@ def run_ours(args, rank: int, world: int):
         "paired_spread_ms": round(spread_ms(rep[other_dispatch] - rep["overlapped"]), 4),
         "swiglu_and_permute_ms": {a: round(stage_med[a]["route_plan_permute"] + stage_med[a]["swiglu_gemm"], 4)
                                   for a in ("overlapped", other_dispatch)}}
+    if args.alt_consumers:
+        overlap["consumer_partitions"] = {
+            f"c{c_alt}": {"ms_per_step": round(med[f"overlapped_c{c_alt}"], 4),
+                          "paired_diff_minus_default_ms": round(float(np.median(rep[f"overlapped_c{c_alt}"] -
+                                                                                 rep["overlapped"])), 4),
+                          "paired_spread_ms": round(spread_ms(rep[f"overlapped_c{c_alt}"] - rep["overlapped"]), 4),
+                          "hidden_pct": hidden_of(f"overlapped_c{c_alt}")["hidden_pct"]}
+            for c_alt in args.alt_consumers}
     overlap["launch_dependencies"] = {
         "default": "programmatic dependent launch" if pdl else "serial launches",
         "other": other_pdl, "ms_per_step": round(med[other_pdl], 4),
@@ -774,7 +791,7 @@ def run_ours(args, rank: int, world: int):
                    "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps),
                    "pair_umma": bool(args.pair_umma), "mgb": args.mgb, "direct_tail": direct,
                    "tail_window": args.tail_window, "fused_dispatch": bool(args.fused_dispatch),
-                   "fused_gemms": bool(args.fused_gemms), "pdl": bool(args.pdl),
+                   "fused_gemms": bool(args.fused_gemms), "pdl": bool(flags & tlc.MOE_PDL),
                    "tail_assist": not args.no_tail_assist, "seed": args.seed,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": f"no flush: each step streams {3 * w.E * w.d * w.ffn * 2 / 1e9:.2f} GB of expert weights "
