@@ -610,10 +610,10 @@ def run_ours(args, rank: int, world: int):
     lb.check(cfg_page, "in the dedicated-partition steps")
     page_ms = float(np.median([e[tlc.EV_BEGIN].elapsed_time(e[tlc.EV_END]) for e in page_ev]))
 
-    # GEMM numbers: real rows = T*k; executed rows = 128 per work item: SwiGLU items are 128 rows of
-    # one expert in the compact layout (with CTA pairs, an expert's odd item also occupies the idle
-    # half of its pair), down-projection items a band or two bands that need at most 64 rows each;
-    # P = padded rows of the owner-aligned layout, PC = rows of the compact layout
+    # GEMM numbers: real rows = T*k; executed rows = 128 per work item: both GEMMs take the same
+    # items, 128 rows of one expert in the compact layout (with CTA pairs, an expert's odd item also
+    # occupies the idle half of its pair); P = padded rows of the owner-aligned layout (the
+    # down-projection's output rows), PC = rows of the compact layout
     ws = lb.ws
     meta = ws.view("meta").cpu()
     P, items, items_up, PC = (int(meta[i].item()) for i in (0, 7, 8, 9))
@@ -757,8 +757,8 @@ def run_ours(args, rank: int, world: int):
         # (the copy stream's event), so its median is the exposed tail
         dma_tail = max(0.0, stage_med["copy_engines"]["copy"])
         overlap["copy_engines"] = {
-            "call": "moe_forward_dma: no consumer SMs; one cudaMemcpyAsync per band issued by the calling thread as "
-                    "the band's record arrives in pinned host memory",
+            "call": "moe_forward_dma: no consumer SMs; one cudaMemcpyAsync per ready band (per run of ready bands "
+                    "adjacent in Yp and Ret) issued by the calling thread as the records arrive in pinned host memory",
             "eager_ms_per_step": round(eager_ms["copy_engines"], 4),
             "eager_ms_per_step_sm_consumers": round(eager_ms["overlapped"], 4),
             "down_gemm_ms": round(stage_med["copy_engines"]["down_gemm"], 4),

@@ -66,11 +66,12 @@ extern "C" {
                                       /* (tcgen05 cta_group::2), half the B tile per SM; the   */
                                       /* down-projection too when d % 256 == 0, consumer_ctas  */
                                       /* is even and MOE_COPY_WARPS is not set                 */
-#define MOE_DIRECT_TAIL 0x10u         /* the down-projection's epilogue writes the bands whose */
-                                      /* tiles are all handed out in the launch's last        */
-                                      /* tail_window tile positions (the last wave) straight  */
-                                      /* into their owner's slice of Ret; the consumer skips   */
-                                      /* them and their rows of Yp are not written             */
+#define MOE_DIRECT_TAIL 0x10u         /* the down-projection's epilogue writes the bands that  */
+                                      /* its work items with a tile among the launch's last    */
+                                      /* tail_window tile positions (the last wave) complete   */
+                                      /* straight into their owner's slice of Ret; the         */
+                                      /* consumer skips them and their rows of Yp are not      */
+                                      /* written                                               */
 #define MOE_FUSED_DISPATCH 0x20u      /* the permute's row copies move into the SwiGLU GEMM:  */
                                       /* its epilogue warps copy the token rows into Xc,      */
                                       /* expert by expert, before their first tile and        */
@@ -107,8 +108,9 @@ extern "C" {
  *   swept 2-24 on the page); mgb = bands per interior segment (same section, 1 or 2 there).
  *   timeout_us bounds every device-side wait (0 = 2,000,000 us).
  *   tail_window (with MOE_DIRECT_TAIL): the number of the down-projection's last tile hand-out
- *   positions whose bands are returned by the epilogue itself; 0 = one wave (one tile per
- *   producer CTA, or per producer CTA pair on CTA pairs).
+ *   positions; the bands completed by work items with a tile among them are returned by the
+ *   epilogue itself; 0 = one wave (one tile per producer CTA, or per producer CTA pair on CTA
+ *   pairs).
  * Limits: d % 128 == 0, ffn % 128 == 0, 1 <= topk <= min(E, 8), 1 <= E <= 256, T % R == 0,
  *   E*R <= 1024, tile_M in {64, 128}, 1 <= mgb <= 4, 1 <= consumer_ctas <= SMs/2 (0 allowed
  *   with MOE_COPY_WARPS; checked at launch), tail_window >= 0, P_max < 2^30 (see moe_layout).
@@ -164,21 +166,22 @@ typedef struct moe_layout {
                        /*                   hand-out rank, SwiGLU work items, first SwiGLU    */
                        /*                   item, first down-projection item, first Xc row    */
     size_t items_up;   /* int32 [IU_max, 2] SwiGLU work items: (first Xc row, expert), 128 rows */
-    size_t items_down; /* int32 [MT_max, 2] down-projection work items in hand-out order: one  */
-                       /*                   band, or two bands of one expert with <= 64 valid */
-                       /*                   rows each                                         */
+    size_t items_down; /* int32 [MT_max, 2] down-projection work items: the SwiGLU items with   */
+                       /*                   the experts in hand-out rank order                */
     size_t slot;       /* int32 [T, topk]   row of pair (t, j) in Yp (padded layout)            */
     size_t cslot;      /* int32 [T, topk]   row of pair (t, j) in Xc / Hc (compact layout)      */
     size_t ret_slot;   /* int32 [T, topk]   row of pair (t, j) in Ret                          */
-    size_t ccoff;      /* int32 [E*R]       first Xc row of group e*R+r                         */
+    size_t yrow;       /* int32 [PC_max]    Yp row of each Xc / Hc row, -1 for a padding row    */
     size_t tile_crow;  /* int32 [MT_max]    Xc / Hc row of the first row of each M-tile (band) */
-    size_t band_item;  /* int32 [MT_max]    down-projection work item holding each M-tile      */
+    size_t band_item;  /* int32 [MT_max]    down-projection work item holding each M-tile's last row */
     size_t tok_of;     /* int32 [PC_max]    token of each Xc / Hc row, -1 for a padding row     */
     size_t xrows;      /* uint32 [E]        rows of each expert copied into Xc (fused dispatch) */
     size_t xready;     /* uint32 [E]        SwiGLU tile quarters published per expert (fused)   */
     size_t meta;       /* int32 [64]        P, M-tiles, work counters, status (see csrc)       */
-    size_t flags;      /* uint32 [MT_max, n_tiles_n2] per-tile readiness flags                 */
-    size_t bands;      /* uint32 [MT_max]   per-band count of finished tile quarters           */
+    size_t flags;      /* uint32 [MT_max, n_tiles_n2] rows of each tile stored (ready at its   */
+                       /*                   valid rows)                                       */
+    size_t bands;      /* uint32 [MT_max]   rows of each band stored over all its N tiles      */
+                       /*                   (ready at valid rows x n_tiles_n2)                */
     size_t trace;      /* uint64 [16]       %globaltimer stamps of the last call (ns)          */
     size_t Xc;         /* bf16 [PC_max, d]  permuted tokens, expert-compact, zero padding rows */
     size_t Hc;         /* bf16 [PC_max, ffn] SwiGLU hidden, same rows                          */
@@ -335,9 +338,10 @@ MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const f
  * The down-projection runs on every SM (consumer_ctas, MOE_TAIL_ASSIST, MOE_COPY_WARPS and
  * MOE_DIRECT_TAIL are ignored); the epilogue warp that completes a band writes a record (its Yp row,
  * Ret row and valid rows, tagged with the call) into host_rec with a system-scope release. The calling
- * thread polls the records and issues one cudaMemcpyAsync per ready band, device to device, on a copy
- * stream of the library's own, which starts after the work enqueued on `stream` before this call;
- * `stream` waits for that copy stream before the combine. So this call returns only after the
+ * thread polls the records and issues one cudaMemcpyAsync per ready band (one per run of ready bands
+ * that are adjacent in both Yp and Ret), device to device, on a copy stream of the library's own,
+ * which starts after the work enqueued on `stream` before this call; `stream` waits for that copy
+ * stream before the combine. So this call returns only after the
  * down-projection has finished on the GPU (it blocks for the layer's GEMMs) and cannot be captured
  * into a CUDA graph (MOE_ERR_ARG while `stream` is capturing). If the down-projection stops early (a
  * bounded wait ran out), the call sees the stream finish with records missing and returns

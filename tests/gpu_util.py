@@ -67,18 +67,26 @@ class Layer:
 def compact_layout(plan: moe_ref.Plan, idx: np.ndarray):
     """Expected expert-compact layout of the GEMM inputs for an oracle plan.
 
-    Each expert's rows contiguous (its groups in owner order, each group's rows in plan order), each
-    expert's run padded to a multiple of the 128-row UMMA tile. Returns (cbase [E], ccoff [E*R],
-    cslot [T, k], PC)."""
-    E, R, T = plan.E, plan.R, plan.T
-    n = plan.n.astype(np.int64)
-    runs = -(-n.sum(1) // 128) * 128
+    Each expert's rows contiguous, its run padded to a multiple of the 128-row UMMA tile; inside the
+    run the expert's bands follow one another in hand-out order (plan.order), each band's valid rows
+    in row order. Returns (cbase [E], tile_crow [MT], cslot [T, k], yrow [PC], PC): the run starts,
+    the compact row of each band's first row, the compact row of every pair and the padded (Yp) row
+    of every compact row (-1 for the rows that pad a run)."""
+    E, tbM = plan.E, plan.tbM
+    runs = -(-plan.n.sum(1).astype(np.int64) // 128) * 128
     cbase = np.concatenate([[0], np.cumsum(runs)])[:E]
-    before = np.concatenate([np.zeros((E, 1), np.int64), np.cumsum(n, 1)[:, :-1]], 1)
-    ccoff = (cbase[:, None] + before).reshape(-1)
-    g = np.asarray(idx, np.int64) * R + moe_ref.owners(T, R)[:, None]
-    cslot = ccoff[g] + (plan.slot - plan.off[g])
-    return cbase, ccoff, cslot, int(runs.sum())
+    tile_crow = np.zeros(plan.num_tiles, np.int64)
+    fill = cbase.copy()
+    for m in plan.order.tolist():
+        e, valid = int(plan.tiles[m, 0]), int(plan.tiles[m, 3])
+        tile_crow[m] = fill[e]
+        fill[e] += valid
+    slot = plan.slot.astype(np.int64)
+    cslot = tile_crow[slot // tbM] + slot % tbM  # band m holds padded rows m*tbM .. m*tbM + valid - 1
+    PC = int(runs.sum())
+    yrow = np.full(PC, -1, np.int64)
+    yrow[cslot.reshape(-1)] = slot.reshape(-1)
+    return cbase, tile_crow, cslot, yrow, PC
 
 
 def parity(got: np.ndarray, want: np.ndarray):
@@ -98,3 +106,14 @@ def plan_oracle(name: str, seed: int, mgb: int):
     logits = inputs.make_logits(w, seed)
     idx, gate = moe_ref.route_topk(logits, w.topk)
     return idx, gate, moe_ref.build_plan(idx, w.E, w.R, w.tile_M, mgb)
+
+
+def check_flag_counts(L: "Layer", plan: moe_ref.Plan):
+    """After an overlapped run: every tile flag holds its band's valid rows (each stored row counted
+    once per N tile) and every band counter valid rows x N tiles."""
+    MT, n2 = plan.num_tiles, L.ws.layout["n_tiles_n2"]
+    valid = torch.from_numpy(plan.tiles[:, 3].astype(np.int32)).to(L.ws.view("flags").device)
+    flags = L.ws.view("flags").reshape(-1)[:MT * n2].reshape(MT, n2)
+    assert torch.all(flags == valid[:, None]), "tile flags"
+    assert torch.all(L.ws.view("bands")[:MT] == valid * n2), "band counters"
+

@@ -1,8 +1,8 @@
 """Direct return of the last wave's bands (MOE_DIRECT_TAIL).
 
-With the flag, the down-projection's epilogue writes the bands whose tiles are all among the launch's
-last `tail_window` tile hand-out positions straight into their owner's slice of Ret (0 = one wave),
-and the consumer skips them: after the last tile there is nothing left to copy.
+With the flag, the down-projection's epilogue writes the bands completed by work items with a tile
+among the launch's last `tail_window` tile hand-out positions straight into their owner's slice of
+Ret (0 = one wave), and the consumer skips them: after the last tile there is nothing left to copy.
 
 Bar: the layer output and Ret bitwise equal to the GEMM-then-copy path on the same inputs; every tile
 flag and band counter complete; the bands whose Yp rows were left unwritten are exactly the bands of a
@@ -17,7 +17,7 @@ import torch
 import tile_level_copy_gb300 as tlc
 from oracle import moe_ref
 from tile_level_copy_gb300 import inputs
-from tests.gpu_util import MAX_ABS, REL_L2, Layer, parity, small
+from tests.gpu_util import MAX_ABS, REL_L2, Layer, check_flag_counts, parity, small
 
 pytestmark = pytest.mark.gpu
 
@@ -37,9 +37,7 @@ def run_direct(L: Layer, cfg):
     assert torch.equal(got, want)
     assert torch.equal(L.ws.view("Ret"), ret_seq)
     MT = plan.num_tiles
-    n2 = L.ws.layout["n_tiles_n2"]
-    assert torch.all(L.ws.view("flags")[:MT] == 4)
-    assert torch.all(L.ws.view("bands")[:MT] == 4 * n2)
+    check_flag_counts(L, plan)
     Yp = L.ws.view("Yp").view(torch.int16).cpu().numpy()
     Ret = L.ws.view("Ret").view(torch.int16).cpu().numpy()
     band_item = L.ws.view("band_item").cpu().numpy()[:MT]
@@ -54,6 +52,9 @@ def run_direct(L: Layer, cfg):
     if direct:  # a suffix of the work items: every band of an item from the first direct one on
         first = min(band_item[m] for m in direct)
         assert direct == {m for m in range(MT) if band_item[m] >= first}
+        # and the last positions of the hand-out order
+        pos = sorted(plan.order.tolist().index(m) for m in direct)
+        assert pos == list(range(MT - len(direct), MT))
     return direct, plan
 
 

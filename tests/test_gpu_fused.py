@@ -14,7 +14,7 @@ import torch
 import tile_level_copy_gb300 as tlc
 from oracle import moe_ref
 from tile_level_copy_gb300 import inputs
-from tests.gpu_util import MAX_ABS, REL_L2, Layer, parity, small
+from tests.gpu_util import MAX_ABS, REL_L2, Layer, check_flag_counts, parity, small
 
 pytestmark = pytest.mark.gpu
 
@@ -38,8 +38,8 @@ def compare(L: Layer, flags, consumers):
         experts = L.ws.view("experts").cpu().numpy()
         want_x = (experts[:, 4] + 1) // 2 * (L.w.ffn // 128) * 8
         np.testing.assert_array_equal(L.ws.view("xready").cpu().numpy(), want_x)
-        MT = int(L.ws.view("meta")[1].item())
-        assert torch.all(L.ws.view("bands")[:MT] == 4 * L.ws.layout["n_tiles_n2"])
+        idx, _ = moe_ref.route_topk(L.logits_np, L.w.topk)
+        check_flag_counts(L, moe_ref.build_plan(idx, L.w.E, L.w.R, L.w.tile_M, L.cfg.mgb))
     return P
 
 

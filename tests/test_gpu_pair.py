@@ -12,7 +12,7 @@ import torch
 import tile_level_copy_gb300 as tlc
 from oracle import moe_ref
 from tile_level_copy_gb300 import inputs
-from tests.gpu_util import MAX_ABS, REL_L2, Layer, parity, small
+from tests.gpu_util import MAX_ABS, REL_L2, Layer, check_flag_counts, parity, small
 
 pytestmark = pytest.mark.gpu
 
@@ -128,10 +128,7 @@ def test_pair_down_projection_matches_single_cta(name, tile_M, consumers):
         assert torch.equal(L.ws.view("Yp")[rows], yp_single[rows])
         check_ret_is_copy_of_yp(L, ref.plan)
         if not seq:
-            MT = ref.plan.num_tiles
-            n2 = L.ws.layout["n_tiles_n2"]
-            assert torch.all(L.ws.view("flags")[:MT] == 4)
-            assert torch.all(L.ws.view("bands")[:MT] == 4 * n2)
+            check_flag_counts(L, ref.plan)
     assert P == ref.plan.P
     err, rel = parity(got.double().cpu().numpy(), ref.out)
     assert err <= MAX_ABS and rel <= REL_L2, (err, rel)

@@ -52,12 +52,11 @@ def check_plan(w, logits_np, x_cpu, mgb=1):
     np.testing.assert_array_equal(v("slot"), plan.slot)
     np.testing.assert_array_equal(v("ret_slot"), plan.ret_slot)
     # expert-compact layout of the GEMM inputs
-    cbase, ccoff, cslot, PC = compact_layout(plan, ridx)
+    cbase, tile_crow, cslot, yrow, PC = compact_layout(plan, ridx)
     assert meta[9] == PC and meta[8] == PC // 128
-    np.testing.assert_array_equal(v("ccoff").reshape(-1), ccoff)
+    np.testing.assert_array_equal(v("tile_crow")[:MT], tile_crow)
     np.testing.assert_array_equal(v("cslot"), cslot)
-    g_t = plan.tiles[:, 0] * w.R + plan.tiles[:, 1]
-    np.testing.assert_array_equal(v("tile_crow")[:MT], ccoff[g_t] + plan.tiles[:, 2] - plan.off[g_t])
+    np.testing.assert_array_equal(v("yrow")[:PC], yrow)
     runs = -(-plan.n.sum(1) // 128)
     experts = v("experts").reshape(-1, 8)
     np.testing.assert_array_equal(experts[:, 4], runs)
@@ -65,6 +64,16 @@ def check_plan(w, logits_np, x_cpu, mgb=1):
     np.testing.assert_array_equal(experts[:, 7], cbase)
     want_items = [(cbase[e] + 128 * i, e) for e in range(w.E) for i in range(runs[e])]
     np.testing.assert_array_equal(v("items_up")[:PC // 128], np.array(want_items).reshape(-1, 2))
+    # the down-projection takes the same items, experts in hand-out rank order (most rows first,
+    # ties to the lower id), and the item holding each band's last row
+    rank_order = sorted(range(w.E), key=lambda e: (-int(plan.n[e].sum()), e))
+    down = [(cbase[e] + 128 * i, e) for e in rank_order for i in range(runs[e])]
+    np.testing.assert_array_equal(v("items_down")[:PC // 128], np.array(down).reshape(-1, 2))
+    first_down = {e: sum(runs[f] for f in rank_order[:rank_order.index(e)]) for e in range(w.E)}
+    np.testing.assert_array_equal(experts[:, 6], [first_down[e] for e in range(w.E)])
+    want_bi = [first_down[int(plan.tiles[m, 0])] + (tile_crow[m] + plan.tiles[m, 3] - 1 - cbase[plan.tiles[m, 0]]) // 128
+               for m in range(MT)]
+    np.testing.assert_array_equal(v("band_item")[:MT], want_bi)
     # the token of every compact row (-1 for the zero rows that pad each expert's run)
     tok = np.full(PC, -1, np.int64)
     tok[cslot.reshape(-1)] = np.repeat(np.arange(w.T), w.topk)
@@ -133,38 +142,41 @@ def test_plan_skip_permute_leaves_xp_untouched():
 
 
 @pytest.mark.parametrize("name", ["tiny", "mixtral", "skew", "fine"])
-def test_work_items_cover_every_band_once(name):
-    """Down-projection work items: every band in exactly one item; a shared item holds two bands of
-    the same expert that each need at most 64 rows; the list follows the hand-out order, and the
-    band -> item map is its inverse. SwiGLU work items
-    cover every real row of the compact layout once, 128 rows of one expert each, and are never more
-    than the down-projection's."""
+def test_work_items_cover_every_row_once(name):
+    """Work items of both GEMMs: 128 compact rows of one expert each, disjoint, covering every real
+    row once; the down-projection's list holds the same items with the experts in hand-out order, so
+    each band's rows lie in the item band_item names and, when they start before it, in the item
+    before it of the same expert; a full band of tile height 128 fills exactly one item."""
     w = inputs.WORKLOADS[name]
-    cfg, ws, _, _ = run_plan(w, inputs.make_logits(w, 0), None, skip_permute=True)
+    cfg, ws, _, _ = run_plan(w, inputs.make_logits(w, 0), None, skip_permute=True)  # slots, no row copy
     meta = ws.view("meta").cpu().numpy()
     MT, NI, NU, PC = int(meta[1]), int(meta[7]), int(meta[8]), int(meta[9])
     tiles = ws.view("tiles").cpu().numpy()[:MT]
-    order = ws.view("order").cpu().numpy()[:MT]
+    tile_crow = ws.view("tile_crow").cpu().numpy()[:MT]
     band_item = ws.view("band_item").cpu().numpy()[:MT]
     items = ws.view("items_down").cpu().numpy()[:NI]
-    seen = []
-    for i, (a, b) in enumerate(items.tolist()):
-        assert band_item[a] == i and (b < 0 or band_item[b] == i)
-        seen.append(a)
-        if b == a:
-            assert w.tile_M == 128
-        elif b == -1:
-            assert w.tile_M == 64 and tiles[a, 3] <= 64
-        else:
-            seen.append(b)
-            assert tiles[a, 0] == tiles[b, 0] and tiles[a, 3] <= 64 and tiles[b, 3] <= 64
-    assert seen == order.tolist() and sorted(seen) == list(range(MT))
-    # two half bands cut the GEMM work wherever partial bands are small
-    assert NI <= MT and (w.tile_M == 128 or NI == (MT + 1) // 2 or NI < MT)
     up = ws.view("items_up").cpu().numpy()[:NU]
+    assert NI == NU and NU * 128 == PC and NI <= MT
+    assert sorted(map(tuple, items.tolist())) == sorted(map(tuple, up.tolist()))
+    for m in range(MT):
+        e, valid, c0 = int(tiles[m, 0]), int(tiles[m, 3]), int(tile_crow[m])
+        i = int(band_item[m])
+        r0, ie = items[i]
+        assert ie == e and r0 <= c0 + valid - 1 < r0 + 128
+        if c0 < r0:  # the band starts in the item before, of the same expert
+            assert i > 0 and items[i - 1][1] == e and items[i - 1][0] == r0 - 128 <= c0
+        if valid == 128 and w.tile_M == 128:
+            assert c0 == r0
+    # along the hand-out order the completing item never decreases (the copy engines stop at the
+    # first band the epilogue returns, so those bands must be the last positions)
+    order = ws.view("order").cpu().numpy()[:MT]
+    assert np.all(np.diff(band_item[order]) >= 0)
     cslot = ws.view("cslot").cpu().numpy().reshape(-1)
     idx = ws.view("idx").cpu().numpy().reshape(-1)
-    assert NU * 128 == PC and NU <= NI
+    yrow = ws.view("yrow").cpu().numpy()[:PC]
+    slot = ws.view("slot").cpu().numpy().reshape(-1)
     rows_of = {(r0 + i): e for r0, e in up.tolist() for i in range(128)}
     assert len(rows_of) == PC  # disjoint 128-row items
     assert all(rows_of[c] == e for c, e in zip(cslot.tolist(), idx.tolist()))
+    np.testing.assert_array_equal(yrow[cslot], slot)  # each pair's compact row names its Yp row
+    assert (yrow >= 0).sum() == len(slot)              # and every other compact row is padding

@@ -64,7 +64,7 @@ class _Config(ctypes.Structure):
 _LAYOUT_INTS = ("P_max", "MT_max", "n_chunks", "chunk_tokens", "n_tiles_n2", "block_n2", "rows_per_unit",
                 "units_per_band", "PC_max", "IU_max")
 LAYOUT_REGIONS = ("idx", "gate", "rank", "chunk_cnt", "chunk_base", "counts", "offsets", "ret_off", "tiles",
-                  "tile_ret", "sched", "order", "seg", "experts", "items_up", "items_down", "slot", "cslot", "ret_slot", "ccoff",
+                  "tile_ret", "sched", "order", "seg", "experts", "items_up", "items_down", "slot", "cslot", "ret_slot", "yrow",
                   "tile_crow", "band_item", "tok_of", "xrows", "xready", "meta", "flags", "bands", "trace", "Xc", "Hc", "Yp", "Ret", "in_logits", "in_x", "out")
 
 
@@ -179,7 +179,7 @@ class Workspace:
 
     _DT = {"idx": (torch.int32, "TK"), "gate": (torch.float32, "TK"), "rank": (torch.int32, "TK"),
            "slot": (torch.int32, "TK"), "cslot": (torch.int32, "TK"), "ret_slot": (torch.int32, "TK"),
-           "counts": (torch.int32, "ER"), "ccoff": (torch.int32, "ER"), "tile_crow": (torch.int32, "MT"),
+           "counts": (torch.int32, "ER"), "yrow": (torch.int32, "PC"), "tile_crow": (torch.int32, "MT"),
            "band_item": (torch.int32, "MT"), "tok_of": (torch.int32, "PC"), "xrows": (torch.int32, "E"),
            "xready": (torch.int32, "E"),
            "offsets": (torch.int32, "G1"), "ret_off": (torch.int32, "RE1"), "tiles": (torch.int32, "MT4"),

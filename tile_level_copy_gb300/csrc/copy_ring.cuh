@@ -3,8 +3,9 @@
 // "Fine-grained Computation-Communication Overlap via Tile-level Signaling and Scheduling for
 // Mixture-of-Experts" (pith.science/paper/W2ZARMHG), "Core claim": the consumer polls the tile
 // flags and issues one contiguous write per row-band segment. On one GPU the write is an
-// HBM-to-HBM copy, and the poll reads one counter per band, which every finished tile quarter of
-// the band release-adds to beside its tile flag (ready at 4 x tiles per band).
+// HBM-to-HBM copy, and the poll reads one counter per band, to which every epilogue warp that stored
+// rows of the band release-adds their number beside its tile flag (ready at valid rows x tiles per
+// band).
 //
 // Bulk engine (copy_units): every warp of a copying CTA takes a work unit, waits for the unit's
 // bands, and moves the rows through two shared-memory buffers with TMA bulk copies (global ->
@@ -80,15 +81,9 @@ __device__ __forceinline__ void engine_drain(CopyEngine& ce, unsigned long long 
     bulk_wait_all();
 }
 
-// Called by every thread of the CTA. Each warp is an independent copy engine with its own slice of
-// the staging area (`ring`, COPY_WARPS * 2 * COPY_PIECE bytes) and two of the mbarriers in `bars`;
-// it takes units from meta[queue] until none is left. wait_flags: acquire the band counter of every
-// band of the unit's segment (== want: all tiles of the band published) before copying. An engine
-// claims its next unit only once the current one is acquired (never while it waits on a band), and
-// the next unit's counters are polled while the previous unit's pieces are still in flight.
 // Bounds check of the plan entries one copy unit reads (hand-out position pos -> band m, its rows
-// in Yp and Ret, and the bands of its segment). A failure is reported as ST_BAD_PLAN and the copy
-// stops, so a corrupt plan never turns into an out-of-range access.
+// in Yp and Ret, and the bands of its segment with their valid rows). A failure is reported as
+// ST_BAD_PLAN and the copy stops, so a corrupt plan never turns into an out-of-range access.
 __device__ __forceinline__ bool copy_unit_ok(const Shape& s, const PlanPtrs& p, int MT, int pos, bool wait_flags) {
     const int m = p.order[pos];
     if (m < 0 || m >= MT) return false;
@@ -100,16 +95,30 @@ __device__ __forceinline__ bool copy_unit_ok(const Shape& s, const PlanPtrs& p, 
         if (first < 0 || nb < 1 || nb > s.mgb || first + nb > MT) return false;
         for (int i = 0; i < nb; ++i) {
             const int b = p.order[first + i];
-            if (b < 0 || b >= MT) return false;
+            if (b < 0 || b >= MT || p.tiles[4 * b + 3] < 1 || p.tiles[4 * b + 3] > s.tbM) return false;
         }
     }
     return true;
 }
 
-// skip_item: bands of down-projection work items from this index on are returned by the GEMM's own
-// epilogue (MOE_DIRECT_TAIL): their units are passed over and their counters are not waited for.
+// Count at which band b's counter says that every row of every N tile of the band is stored
+// (stall = 1: a count it never reaches, the stalled-consumer test hook).
+__device__ __forceinline__ uint32_t band_ready(const Shape& s, const PlanPtrs& p, int b, uint32_t stall) {
+    return (uint32_t)p.tiles[4 * b + 3] * (uint32_t)s.n_tiles_n2 + stall;
+}
+
+// Called by every thread of the CTA. Each warp is an independent copy engine with its own slice of
+// the staging area (`ring`, COPY_WARPS * 2 * COPY_PIECE bytes) and two of the mbarriers in `bars`;
+// it takes units from meta[queue] until none is left. wait_flags: acquire the band counter of every
+// band of the unit's segment (== band_ready: all rows of all tiles of the band published) before
+// copying. An engine claims its next unit only once the current one is acquired (never while it
+// waits on a band), and the next unit's counters are polled while the previous unit's pieces are
+// still in flight.
+// skip_item: bands whose last row's down-projection work item is at or past this index are returned
+// by the GEMM's own epilogue (MOE_DIRECT_TAIL): their counters are not waited for, and an engine that
+// reaches one of their units stops (they are the last hand-out positions).
 __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uint64_t* bars, volatile int* s_abort,
-                           int queue, bool wait_flags, uint32_t want, int skip_item) {
+                           int queue, bool wait_flags, uint32_t stall, int skip_item) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int MT = p.meta[META_MTILES];
     if (MT < 0 || MT > s.MT_max) MT = 0;
@@ -137,7 +146,10 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
         }
         const int m = p.order[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
-        if (rb >= valid || p.band_item[m] >= skip_item) {
+        // the bands the epilogue returns are a suffix of the hand-out positions (band_item does not
+        // decrease along them), so every unit from here on is theirs: stop instead of claiming them
+        if (p.band_item[m] >= skip_item) break;
+        if (rb >= valid) {
             if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
             continue;
         }
@@ -149,8 +161,10 @@ __device__ void copy_units(const Shape& s, const PlanPtrs& p, uint8_t* ring, uin
             if (lane == 0) {
                 const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
                 for (int i = 0; i < nb && !failed; ++i) {
-                    if (p.band_item[p.order[first + i]] >= skip_item) continue;  // returned by the epilogue
-                    const uint32_t* bc = p.bands + p.order[first + i];
+                    const int b = p.order[first + i];
+                    if (p.band_item[b] >= skip_item) continue;  // returned by the epilogue
+                    const uint32_t* bc = p.bands + b;
+                    const uint32_t want = band_ready(s, p, b, stall);
                     if (ld_acquire_gpu(bc) == want) continue;
                     if (!engine_flush(ce, s.timeout_ns, s_abort)) {
                         *s_abort = 1;
@@ -229,7 +243,7 @@ __device__ __forceinline__ void st_cg_v4(uint4* p, const uint4& v) {
                  : "memory");
 }
 
-__device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int* s_abort, int queue, uint32_t want,
+__device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int* s_abort, int queue, uint32_t stall,
                                 int skip_item) {
     const int lane = threadIdx.x & 31;
     int MT = p.meta[META_MTILES];
@@ -256,7 +270,10 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
         }
         const int m = p.order[pos];
         const int row0 = p.tiles[4 * m + 2], valid = p.tiles[4 * m + 3];
-        if (rb >= valid || p.band_item[m] >= skip_item) {
+        // the bands the epilogue returns are a suffix of the hand-out positions (band_item does not
+        // decrease along them), so every unit from here on is theirs: stop instead of claiming them
+        if (p.band_item[m] >= skip_item) break;
+        if (rb >= valid) {
             if (lane == 0) u_next = atomicAdd(&p.meta[queue], 1);
             continue;
         }
@@ -265,8 +282,10 @@ __device__ void copy_units_simt(const Shape& s, const PlanPtrs& p, volatile int*
         if (lane == 0) {
             const int first = p.seg[2 * pos], nb = p.seg[2 * pos + 1];
             for (int i = 0; i < nb && !failed; ++i) {
-                if (p.band_item[p.order[first + i]] >= skip_item) continue;  // returned by the epilogue
-                const uint32_t* bc = p.bands + p.order[first + i];
+                const int b = p.order[first + i];
+                if (p.band_item[b] >= skip_item) continue;  // returned by the epilogue
+                const uint32_t* bc = p.bands + b;
+                const uint32_t want = band_ready(s, p, b, stall);
                 if (ld_acquire_gpu(bc) == want) continue;
                 const unsigned long long t0 = globaltimer();
                 for (unsigned ns = 64;; ns = ns < 512 ? 2 * ns : ns) {

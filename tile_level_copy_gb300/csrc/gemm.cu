@@ -15,10 +15,11 @@
 //   "Core claim" - one rank-wide persistent GEMM covers all experts in one launch and publishes a
 //       readiness flag after each tile's epilogue store;
 //   "Load-bearing premise" and "Referee Report" major comment 2 (§3.3.1) - the tile must be
-//       visible before the flag: each of the four epilogue warps waits until its TMA stores of the
-//       tile have completed, fences the async proxy, then adds its share to the tile flag and to
+//       visible before the flag: each of the four epilogue warps waits until its stores of the
+//       tile have completed, fences the async proxy, then adds its rows to the tile flag and to
 //       the band's counter with release semantics; copy engines read the band counter with
-//       ld.acquire.gpu (ready at 4 x tiles per band); bulk engines fence the async proxy first.
+//       ld.acquire.gpu (ready at valid rows x tiles per band); bulk engines fence the async proxy
+//       first.
 //   "What carries the argument" - the consumer runs on a small dedicated SM partition; here the
 //       partition is the last consumer_ctas CTAs of the down-projection's own launch (a cooperative
 //       launch for the single-CTA kernel, so producers and consumers are co-resident; the pair
@@ -83,41 +84,20 @@ __device__ __forceinline__ int tile_take(const Smem& sm, int j, unsigned long lo
     return t;
 }
 
-// One GEMM tile: work item (mA, mB) x N tile n of expert e. Rows 0-63 of the UMMA tile are loaded
-// from input row lrowA on and stored to output row rowA on, rows 64-127 from lrowB / to rowB
-// (lrowA + 64 / rowA + 64 when the item is a single 128-row run). Down-projection items are bands
-// (mB == mA: one band of 128 rows; mB == -1: one 64-row band alone; otherwise two half bands), read
-// from the compact layout and written to the padded one; SwiGLU items are 128 compact rows of one
-// expert (mA = mB = 0), read and written in the compact layout.
+// One GEMM tile as one CTA sees it: 128 rows of the expert-compact layout from `row` on (-1: this
+// CTA of a pair has no rows in the tile), N tile n, expert e, and the work item's index in its list.
+// Both GEMMs take the same items, 128 compact rows of one expert; the SwiGLU GEMM stores its rows
+// in the compact layout, the down-projection's epilogue sends each row to its owner-aligned row.
 struct TileRef {
-    int mA, mB, n, e, rowA, rowB, lrowA, lrowB;
-    int item;  // down-projection work item (index into the item list); -1 for SwiGLU tiles
+    int row, n, e, item;
 };
 
-__device__ __forceinline__ TileRef make_ref(int mA, int mB, int n, const int32_t* tiles, const int32_t* crow,
-                                            int item) {
+__device__ __forceinline__ TileRef tile_ref(int row, int n, int e, int item) {
     TileRef r;
-    r.item = item;
-    r.mA = mA;
-    r.mB = mB;
-    r.n = n;
-    r.e = tiles[4 * mA + 0];
-    r.rowA = tiles[4 * mA + 2];
-    r.lrowA = crow[mA];
-    const bool two = mB >= 0 && mB != mA;
-    r.rowB = two ? tiles[4 * mB + 2] : r.rowA + 64;
-    r.lrowB = two ? crow[mB] : r.lrowA + 64;
-    return r;
-}
-
-__device__ __forceinline__ TileRef compact_ref(int row, int n, int e) {
-    TileRef r;
-    r.item = -1;
-    r.mA = r.mB = 0;
+    r.row = row;
     r.n = n;
     r.e = e;
-    r.rowA = r.lrowA = row;
-    r.rowB = r.lrowB = row + 64;
+    r.item = item;
     return r;
 }
 
@@ -135,15 +115,14 @@ __device__ __forceinline__ TileRef decode_up(int t, const int* tab, int E, const
     }
     const int e = lo, local = t - cum[e], cnt = count[e];
     const int n = local / cnt, it = first[e] + local % cnt;
-    return compact_ref(items[2 * it], n, e);
+    return tile_ref(items[2 * it], n, e, it);
 }
 
-// Down-projection order: work items in hand-out order (the remote-first schedule re-sorted by expert),
-// all N tiles of an item together.
-__device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* items, const int32_t* tiles,
-                                               const int32_t* crow) {
+// Down-projection order: work items in hand-out order (experts by rank, each expert's items in
+// compact-row order, which follows its bands in hand-out order), all N tiles of an item together.
+__device__ __forceinline__ TileRef decode_down(int t, int nN, const int32_t* items) {
     const int it = t / nN;
-    return make_ref(items[2 * it], items[2 * it + 1], t - it * nN, tiles, crow, it);
+    return tile_ref(items[2 * it], t - it * nN, items[2 * it + 1], it);
 }
 
 // One epilogue warp's staging in shared memory: two 32-row x 32-column bf16 chunk buffers, used
@@ -172,13 +151,14 @@ struct EpiStage {
         }
         eb ^= 1;
     }
-    // Direct return of the chunk (MOE_DIRECT_TAIL): the same staging, then the warp stores the
-    // chunk's first `rows` rows with 16-byte stores, eight rows of 64 bytes per instruction, to
-    // dst (row 0 of the chunk) + row * pitch + col_bytes. Rows past `rows` are padding rows of the
-    // band: the owner's packed return rows have no room for them.
-    __device__ __forceinline__ void put_direct(const uint32_t (&pk)[16], uint8_t* dst, size_t pitch, int col_bytes,
-                                               int rows, int lane) {
-        if (lane == 0) bulk_wait_read_1();  // an earlier tensor store from this buffer has read it
+    // The same staging, then the warp stores the chunk row by row with 16-byte stores, eight rows
+    // of 64 bytes per instruction: row r of the chunk to rp[i] + col_bytes, where rp[i] (i = r / 8)
+    // is that row's destination as lane (lane / 4 + 8 i) holds it (nullptr: the row goes nowhere).
+    __device__ __forceinline__ void put_rows(const uint32_t (&pk)[16], uint8_t* const (&rp)[4], int col_bytes,
+                                             int lane) {
+        // every tensor store has read its buffer: this path commits no bulk group of its own, so the
+        // last group may be the one that read this buffer (put() followed by put_rows() twice)
+        if (lane == 0) bulk_wait_read_all();
         __syncwarp();
         uint8_t* chunk = buf + eb * EPI_CHUNK_BYTES;
         uint4* row = reinterpret_cast<uint4*>(chunk + lane * (EPI_CHUNK * 2));
@@ -194,77 +174,134 @@ struct EpiStage {
         const uint4* src = reinterpret_cast<const uint4*>(chunk);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int piece = lane + 32 * i, r = piece >> 2;  // 4 pieces of 16 bytes per 64-byte row
-            if (r < rows)
-                *reinterpret_cast<uint4*>(dst + (size_t)r * pitch + col_bytes + (piece & 3) * 16) = src[piece];
+            const int piece = lane + 32 * i;  // row piece >> 2, 16-byte piece piece & 3 of its 64 bytes
+            if (rp[i]) *reinterpret_cast<uint4*>(rp[i] + col_bytes + (piece & 3) * 16) = src[piece];
         }
         __syncwarp();  // the buffer is read before it is written again
         eb ^= 1;
     }
 };
 
-// Destination of a warp's rows when its tile's band is returned by the epilogue itself
-// (MOE_DIRECT_TAIL): the Ret row of the warp's first tile row, and how many of its 32 rows are real.
-struct DirectDst {
-    uint8_t* row0;  // nullptr: the rows go to Yp through the output tensor map
-    int rows;
-};
-
-// Epilogue of one warp's 32 accumulator lanes (tile rows y..y+31) of a finished tile at TMEM
-// address tb. MODE 1: columns 0-127 hold the gate and 128-255 the up projection of output columns
-// n*128..; h = silu(gate) * up, rounded to bf16. MODE 2: the BN columns of output columns n*BN..,
-// rounded to bf16. Inactive warps (padding half of a 64-row band) read TMEM but store nothing.
-template <int MODE>
-__device__ __forceinline__ void epilogue_rows(EpiStage& es, const CUtensorMap* tmOut, uint32_t tb, int n, int BN,
-                                              int y, bool active, int lane, DirectDst dd = DirectDst{nullptr, 0},
-                                              size_t pitch = 0) {
-    if (MODE == 1) {
+// Epilogue of one warp's 32 accumulator lanes of a finished SwiGLU tile at TMEM address tb (tile
+// rows y..y+31 of the compact layout): columns 0-127 hold the gate and 128-255 the up projection of
+// output columns n*128..; h = silu(gate) * up, rounded to bf16. An inactive warp (a pair CTA
+// without rows) stores nothing.
+__device__ __forceinline__ void epilogue_swiglu(EpiStage& es, const CUtensorMap* tmOut, uint32_t tb, int n, int y,
+                                                bool active, int lane) {
 #pragma unroll 1
-        for (int c = 0; c < BN1 / 32; ++c) {
-            uint32_t g[32], u[32];
-            tmem_ld32(tb + c * 32, g);
-            tmem_ld32(tb + BN1 + c * 32, u);
-            if (active) {
-                uint32_t pk[16];
+    for (int c = 0; c < BN1 / 32; ++c) {
+        uint32_t g[32], u[32];
+        tmem_ld32(tb + c * 32, g);
+        tmem_ld32(tb + BN1 + c * 32, u);
+        if (active) {
+            uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-                    const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * __uint_as_float(u[2 * i]);
-                    const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
-                    pk[i] = pack_bf16x2(h0, h1);
-                }
-                es.put(tmOut, pk, n * BN1 + c * 32, y, lane);
+            for (int i = 0; i < 16; ++i) {
+                const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * __uint_as_float(u[2 * i]);
+                const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
+                pk[i] = pack_bf16x2(h0, h1);
             }
-        }
-    } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tb + c * 32, v);
-            if (active) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                if (dd.row0) {
-                    if (dd.rows > 0) es.put_direct(pk, dd.row0, pitch, (n * BN + c * 32) * 2, dd.rows, lane);
-                } else {
-                    es.put(tmOut, pk, n * BN + c * 32, y, lane);
-                }
-            }
+            es.put(tmOut, pk, n * BN1 + c * 32, y, lane);
         }
     }
 }
 
-// Destination of epilogue warp q's rows (TMEM lane quarter q) when its band mq is returned directly:
-// its first row inside the band, the Ret row it goes to and how many of its 32 rows are real.
-__device__ __forceinline__ DirectDst direct_dst(const Shape& s, const PlanPtrs& p, const TileRef& tr, int q) {
-    const int mq = (q < 2) ? tr.mA : tr.mB;
-    const int rb = ((q >= 2 && tr.mB == tr.mA) ? 64 : 0) + (q & 1) * 32;
-    DirectDst dd;
-    dd.rows = max(0, min(32, p.tiles[4 * mq + 3] - rb));
-    dd.row0 = reinterpret_cast<uint8_t*>(p.Ret) + (size_t)(p.tile_ret[mq] + rb) * s.d * 2;
-    return dd;
+// Where one row of a down-projection tile goes: the compact row's output row in Yp (the plan's yrow
+// table, written by the permute), or, when its band is returned by the epilogue itself
+// (MOE_DIRECT_TAIL: the item holding the band's last row is at or past direct_from), its row in the
+// owner's slice of Ret. A padding row goes nowhere (band -1). A row whose table entries are out of
+// range is reported (ST_BAD_PLAN, detail -2) and not stored.
+struct DownRow {
+    uint8_t* dst;  // row start, or nullptr
+    int y;         // Yp row (-1: none)
+    int band;      // -1: none
+    bool direct;
+};
+
+__device__ __forceinline__ DownRow down_row(const Shape& s, const PlanPtrs& p, int c, int MT, int direct_from) {
+    DownRow r{nullptr, -1, -1, false};
+    const int y = (c >= 0 && c < s.PC_max) ? p.yrow[c] : -1;
+    if (y < 0) return r;
+    const int m = y / s.tbM, rb = y - m * s.tbM;
+    const size_t pitch = (size_t)s.d * 2;
+    if (y >= s.P_max || m >= MT || rb >= p.tiles[4 * m + 3]) {
+        set_status(p.meta, ST_BAD_PLAN, -2);
+        return r;
+    }
+    if (p.band_item[m] >= direct_from) {
+        const int ret = p.tile_ret[m] + rb;
+        if (ret < 0 || ret >= s.T * s.k) {
+            set_status(p.meta, ST_BAD_PLAN, -2);
+            return r;
+        }
+        r.dst = reinterpret_cast<uint8_t*>(p.Ret) + (size_t)ret * pitch;
+        r.direct = true;
+    } else {
+        r.dst = reinterpret_cast<uint8_t*>(p.Yp) + (size_t)y * pitch;
+    }
+    r.y = y;
+    r.band = m;
+    return r;
+}
+
+// Epilogue of one warp's 32 accumulator lanes of a finished down-projection tile (BN columns of
+// output columns n*BN..), rounded to bf16; lane i's row goes to dr.dst. When the warp's 32 rows are
+// 32 consecutive Yp rows from y0 (a quarter of a full band: the common case), each 32-column chunk
+// leaves with one TMA tensor store, else with row-by-row 16-byte stores (put_rows).
+__device__ __forceinline__ void epilogue_down(EpiStage& es, const CUtensorMap* tmOut, uint32_t tb, int n, int BN,
+                                              const DownRow& dr, int lane) {
+    if (!__any_sync(0xffffffffu, dr.dst != nullptr)) return;  // padding rows only
+    const int y0 = __shfl_sync(0xffffffffu, dr.y, 0);
+    const bool tma = __all_sync(0xffffffffu, dr.dst != nullptr && !dr.direct && dr.y == y0 + lane);
+    uint8_t* rp[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        rp[i] = reinterpret_cast<uint8_t*>(
+            __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(dr.dst), (lane >> 2) + 8 * i));
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tb + c * 32, v);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        if (tma) es.put(tmOut, pk, n * BN + c * 32, y0, lane);
+        else es.put_rows(pk, rp, (n * BN + c * 32) * 2, lane);
+    }
+}
+
+// Publish one warp's rows of a finished down-projection tile (overlapped runs): the tensor stores
+// lane 0 issued have completed, the row stores of every lane are ordered before lane 0 by the warp
+// barrier, the async proxy is fenced against the generic one; then lane 0 adds, for each band among
+// the warp's rows, that band's row count to the tile flag (ready at the band's valid rows) and to the
+// band counter (ready at valid rows x N tiles), each with release semantics. The add that completes
+// a band (acquire-release: it reads every other warp's released add, so their rows are ordered
+// before it) stamps the trace and, for moe_forward_dma, writes the band's host record.
+__device__ __forceinline__ void publish_rows(const Shape& s, const PlanPtrs& p, const DownRow& dr, int n, int lane) {
+    const unsigned same = __match_any_sync(0xffffffffu, dr.band);
+    unsigned leaders = __ballot_sync(0xffffffffu, dr.band >= 0 && (same & ((1u << lane) - 1u)) == 0u);
+    if (!leaders) return;
+    if (lane == 0) {
+        bulk_wait_all();
+        fence_proxy_async_global();
+        __threadfence();
+    }
+    const uint32_t nN = (uint32_t)s.n_tiles_n2;
+    for (; leaders; leaders &= leaders - 1u) {
+        const int l = __ffs(leaders) - 1;
+        const int m = __shfl_sync(0xffffffffu, dr.band, l);
+        const uint32_t cnt = (uint32_t)__popc(__shfl_sync(0xffffffffu, same, l));
+        if (lane == 0) {
+            red_release_gpu_add(p.flags + (size_t)m * nN + n, cnt);
+            const uint32_t before = atom_acq_rel_gpu_add(p.bands + m, cnt);
+            if (before + cnt == (uint32_t)p.tiles[4 * m + 3] * nN) {
+                atomicMax(&p.trace[MOE_TRACE_BAND_DONE], globaltimer());
+                if (p.host_rec) host_band_record(s, p, m);  // the band's last rows
+            }
+        }
+    }
+    __syncwarp();
 }
 
 // Fused dispatch (MOE_FUSED_DISPATCH), the permute's row copies inside the SwiGLU GEMM: before its
@@ -346,50 +383,27 @@ __device__ __forceinline__ bool wait_expert_rows(const Shape& s, const PlanPtrs&
 }
 
 // Bounds check of the plan entries a GEMM launch reads, by all threads of a CTA before any tile:
-// SwiGLU items (first compact row, expert) and the expert table of the item lists; down-projection
-// items (bands mA, mB) and each band's expert, output rows and compact rows. Returns nonzero if this
-// thread found a bad entry. Every CTA reaches the same answer, so a corrupt plan stops the whole
-// launch; the status detail is -1 (SwiGLU items) or -2 (down-projection items).
-__device__ __forceinline__ int plan_items_bad(const Shape& s, const PlanPtrs& p, int mode, int NI, int MT) {
+// work items (first compact row, expert) and the expert table of the item list. Returns nonzero if
+// this thread found a bad entry. Every CTA reaches the same answer, so a corrupt plan stops the whole
+// launch; the status detail is -1 (SwiGLU items) or -2 (down-projection items). The entries a
+// down-projection row is sent by (yrow, the band tables) are checked row by row (down_row).
+__device__ __forceinline__ int plan_items_bad(const Shape& s, const PlanPtrs& p, int mode, int NI) {
     int bad = 0;
-    if (mode == 1) {
-        for (int it = threadIdx.x; it < NI && !bad; it += blockDim.x) {
-            const int crow = p.items_up[2 * it], e = p.items_up[2 * it + 1];
-            if (e < 0 || e >= s.E || crow < 0 || crow % BM != 0 || crow + BM > s.PC_max) bad = it + 1;
-        }
-        for (int e = threadIdx.x; e < s.E && !bad; e += blockDim.x) {
-            const int cnt = p.experts[8 * e + 4], first = p.experts[8 * e + 5];
-            if (cnt < 0 || first < 0 || first + cnt > NI) bad = e + 1;
-        }
-    } else {
-        for (int it = threadIdx.x; it < NI && !bad; it += blockDim.x) {
-            const int mA = p.items_down[2 * it], mB = p.items_down[2 * it + 1];
-            const int ms[2] = {mA, mB};
-            if (mA < 0 || mA >= MT || mB < -1 || mB >= MT) {
-                bad = it + 1;
-                break;
-            }
-            for (int j = 0; j < 2; ++j) {
-                const int m = ms[j];
-                if (m < 0) continue;
-                const int e = p.tiles[4 * m], row0 = p.tiles[4 * m + 2], crow = p.tile_crow[m];
-                const int valid = p.tiles[4 * m + 3], ret0 = p.tile_ret[m];
-                if (e < 0 || e >= s.E || row0 < 0 || row0 + s.tbM > s.P_max || crow < 0 || crow >= s.PC_max ||
-                    valid < 1 || valid > s.tbM || ret0 < 0 || ret0 + valid > s.T * s.k)
-                    bad = it + 1;
-            }
-        }
-        for (int e = threadIdx.x; e < s.E && !bad; e += blockDim.x) {  // first item of each expert
-            const int first = p.experts[8 * e + 6];
-            if (first < 0 || first > NI) bad = NI + e + 1;
-        }
+    const int32_t* items = (mode == 1) ? p.items_up : p.items_down;
+    for (int it = threadIdx.x; it < NI && !bad; it += blockDim.x) {
+        const int crow = items[2 * it], e = items[2 * it + 1];
+        if (e < 0 || e >= s.E || crow < 0 || crow % BM != 0 || crow + BM > s.PC_max) bad = it + 1;
+    }
+    for (int e = threadIdx.x; e < s.E && !bad; e += blockDim.x) {
+        const int cnt = p.experts[8 * e + 4], first = p.experts[8 * e + ((mode == 1) ? 5 : 6)];
+        if (cnt < 0 || first < 0 || first + cnt > NI) bad = NI + e + 1;
     }
     return bad;
 }
 
 template <int MODE>  // 1: SwiGLU up-projection -> Hc; 2: down-projection -> Yp (+ flags / consumer)
 __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
-    gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAh,
+    gemm_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                 const __grid_constant__ CUtensorMap tmOut, int num_producers, int overlapped) {
     extern __shared__ uint8_t smem_raw[];
@@ -402,19 +416,19 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     const int nN = (MODE == 1) ? s.ffn / BN1 : s.n_tiles_n2;
     const int BN = (MODE == 1) ? 2 * BN1 : s.bn2;  // UMMA N
     const int KB = ((MODE == 1) ? s.d : s.ffn) / BK;
-    const int bad_item = __syncthreads_or(plan_items_bad(s, p, MODE, NI, MT));
+    const int bad_item = __syncthreads_or(plan_items_bad(s, p, MODE, NI));
     if (bad_item) NI = 0;  // no tile runs; the copy engines stop at the abort word set below
     const int total = NI * nN;
     const uint32_t tx_bytes = A_STAGE_BYTES + BN * BK * 2;
     const unsigned long long tmo = s.timeout_ns;
     const bool dispatch = MODE == 1 && (s.flags & MOE_FUSED_DISPATCH);
-    // MOE_DIRECT_TAIL: items from `direct_from` on have every tile among the last `window` hand-out
-    // positions (item i's tiles are i*nN .. i*nN+nN-1); their epilogue writes the rows into Ret and
-    // the copy engines skip them
+    // MOE_DIRECT_TAIL: items from `direct_from` on have a tile among the last `window` hand-out
+    // positions (item i's tiles are i*nN .. i*nN+nN-1), so they may complete bands in the last wave;
+    // their epilogue writes those bands' rows into Ret and the copy engines skip them
     int direct_from = INT_MAX;
     if (MODE == 2 && overlapped && (s.flags & MOE_DIRECT_TAIL)) {
         const int window = s.tail_window > 0 ? s.tail_window : num_producers, thr = total - window;
-        direct_from = thr <= 0 ? 0 : min(NI, (thr + nN - 1) / nN);
+        direct_from = thr <= 0 ? 0 : min(NI, thr / nN);
     }
 
     if (tid == 0) {
@@ -457,7 +471,6 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     }
     if (producer && tid == 0) {
         tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmAh);
         tma_prefetch_desc(&tmB0);
         tma_prefetch_desc(&tmOut);
         if (MODE == 1) tma_prefetch_desc(&tmB1);
@@ -470,11 +483,11 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     griddep_launch();
     const uint32_t tmem = producer ? *sm.tmem_base : 0u;
     unsigned long long last_end = 0;
-    const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
+    const uint32_t stall = (s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u;  // a count no band reaches
 
     // Extra warps (launched with MOE_COPY_WARPS): SIMT copy engines beside the GEMM warps.
     if (warp >= GEMM_WARPS) {
-        if (MODE == 2 && overlapped) copy_units_simt(s, p, sm.abort, META_QUEUE, want, direct_from);
+        if (MODE == 2 && overlapped) copy_units_simt(s, p, sm.abort, META_QUEUE, stall, direct_from);
         return;
     }
 
@@ -497,8 +510,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                 sm.tq[slot] = t < total ? t : -1;
                 mbar_arrive(&sm.tq_full[slot]);
                 if (t >= total) break;
-                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up)
-                                               : decode_down(t, nN, p.items_down, p.tiles, p.tile_crow);
+                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up) : decode_down(t, nN, p.items_down);
                 if (MODE == 1 && dispatch && tr.e != ready_e) {
                     if (!wait_expert_rows(s, p, tr.e, sm.abort, 30)) {
                         ok = false;
@@ -519,12 +531,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                     mbar_arrive_expect_tx(&sm.full[st], tx_bytes);
                     uint8_t* a = sm.stages + st * STAGE_BYTES;
                     uint8_t* b = a + A_STAGE_BYTES;
-                    if (tr.mB >= 0 && tr.mB != tr.mA) {  // two half bands: two 64-row boxes
-                        tma_load_2d(a, &tmAh, &sm.full[st], kb * BK, tr.lrowA);
-                        tma_load_2d(a + A_STAGE_BYTES / 2, &tmAh, &sm.full[st], kb * BK, tr.lrowB);
-                    } else {
-                        tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.lrowA);
-                    }
+                    tma_load_2d(a, &tmA, &sm.full[st], kb * BK, tr.row);  // 128 compact rows
                     if (MODE == 1) {
                         tma_load_3d(b, &tmB0, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
                         tma_load_3d(b + BN1 * BK * 2, &tmB1, &sm.full[st], kb * BK, tr.n * BN1, tr.e);
@@ -623,8 +630,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                     break;
                 }
                 if (t < 0) break;
-                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up)
-                                               : decode_down(t, nN, p.items_down, p.tiles, p.tile_crow);
+                const TileRef tr = (MODE == 1) ? decode_up(t, sm.tab, s.E, p.items_up) : decode_down(t, nN, p.items_down);
                 if (!mbar_wait(&sm.acc_full[b], aph, tmo, sm.abort)) {
                     if (!*sm.abort) set_status(p.meta, ST_PIPE_TIMEOUT, 2);
                     *sm.abort = 1;
@@ -632,38 +638,19 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
                 }
                 tc_fence_after();
                 const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
-                // rows 0-63 belong to band mA, rows 64-127 to band mB (or to mA for a 128-row band)
-                const int mq = (q < 2) ? tr.mA : tr.mB;
-                const bool active = mq >= 0;
-                const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
-                const uint32_t inc = (tr.mB == tr.mA) ? 1u : 2u;  // quarters per band: 4 in all
-                const DirectDst dd = (MODE == 2 && active && tr.item >= direct_from) ? direct_dst(s, p, tr, q)
-                                                                                   : DirectDst{nullptr, 0};
-                epilogue_rows<MODE>(es, &tmOut, tb, tr.n, BN, y, active, lane, dd, (size_t)s.d * 2);
-                tc_fence_before();
-                mbar_arrive(&sm.acc_empty[b]);
-                if (MODE == 2 && active) {
-                    if (flags) {
-                        // Publish this warp's rows of the tile: its TMA stores must be complete (not
-                        // only read out of shared memory), the async proxy fenced against the generic
-                        // one, then lane 0 adds its share (1 for a quarter of a 128-row band, 2 for
-                        // half of a 64-row one) to the tile's flag with release semantics (the tile
-                        // is ready at 4) and to its band's counter (the band is ready at 4 x tiles
-                        // per band), which is what consumers poll.
-                        if (lane == 0) {
-                            bulk_wait_all();
-                            fence_proxy_async_global();
-                            __threadfence();
-                            red_release_gpu_add(p.flags + (size_t)mq * s.n_tiles_n2 + tr.n, inc);
-                            const uint32_t before = atom_release_gpu_add(p.bands + mq, inc);
-                            if (before + inc == FLAG_READY * (uint32_t)s.n_tiles_n2) {
-                                atomicMax(&p.trace[MOE_TRACE_BAND_DONE], globaltimer());
-                                if (p.host_rec) host_band_record(s, p, mq);  // the band's last quarter
-                            }
-                        }
-                        __syncwarp();
-                    }
-                    if (lane == 0) last_end = globaltimer();
+                const int c0 = tr.row + q * 32;  // this warp's first compact row
+                if (MODE == 1) {
+                    epilogue_swiglu(es, &tmOut, tb, tr.n, c0, true, lane);
+                    tc_fence_before();
+                    mbar_arrive(&sm.acc_empty[b]);
+                } else {
+                    const DownRow dr = down_row(s, p, c0 + lane, MT, direct_from);
+                    epilogue_down(es, &tmOut, tb, tr.n, BN, dr, lane);
+                    tc_fence_before();
+                    mbar_arrive(&sm.acc_empty[b]);
+                    if (flags) publish_rows(s, p, dr, tr.n, lane);
+                    const bool stored = __any_sync(0xffffffffu, dr.band >= 0);
+                    if (lane == 0 && stored) last_end = globaltimer();
                 }
                 b ^= 1;
                 if (b == 0) aph ^= 1u;
@@ -683,7 +670,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
         atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
 
     if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
-        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want, direct_from);
+        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, stall, direct_from);
 }
 
 // =============================================================================================
@@ -695,9 +682,9 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 //       (W3 rows); each CTA's accumulator holds 128 gate | 128 up columns. Work items of an expert
 //       in pairs, N tiles outer.
 //   MODE 2 (down-projection): rank 0 stages rows 0-127 of the 256-row W2 tile, rank 1 rows
-//       128-255; each CTA's item is one band (or two half bands) of the page's padded layout, and
-//       its epilogue publishes the band flags as in gemm_kernel. Work items of an expert in pairs,
-//       in hand-out order, all N tiles of a pair item together. Consumer CTAs (the last
+//       128-255; each CTA's item is 128 compact rows of one expert, whose epilogue sends every row
+//       to its owner-aligned band and publishes the band flags as in gemm_kernel. Work items of an
+//       expert in pairs, in hand-out order, all N tiles of a pair item together. Consumer CTAs (the last
 //       consumer_ctas blocks, whole clusters) and, with tail assist, finished producer CTAs run the
 //       bulk copy engines.
 // An expert with an odd number of work items leaves rank 1 without rows in its last pair tile: it
@@ -816,7 +803,7 @@ __device__ __forceinline__ int tab_segment(const int* cum, int E, int t) {
 
 // Pair tile t -> this CTA's rows (SwiGLU tiles). Order as in decode_up with two work items per pair:
 // the table's experts in order (ids in `eid`, or the table's order is the id order when eid is
-// null), N tiles outer, pairs inner; rank r takes item 2 * pair + r of the expert (mA = -1: none).
+// null), N tiles outer, pairs inner; rank r takes item 2 * pair + r of the expert (row -1: none).
 __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, const int32_t* items,
                                                   uint32_t rank, const int* eid = nullptr) {
     const int* cum = tab;
@@ -825,34 +812,25 @@ __device__ __forceinline__ TileRef decode_pair_up(int t, const int* tab, int E, 
     const int r = tab_segment(cum, E, t), local = t - cum[r], cnt = count[r], np = (cnt + 1) >> 1;
     const int e = eid ? eid[r] : r;
     const int n = local / np, it = 2 * (local - n * np) + (int)rank;
-    if (it >= cnt) {
-        TileRef x;
-        x.item = -1;
-        x.mA = x.mB = -1;
-        x.n = n;
-        x.e = e;
-        x.rowA = x.rowB = x.lrowA = x.lrowB = 0;
-        return x;
-    }
+    if (it >= cnt) return tile_ref(-1, n, e, -1);
     const int item = first[r] + it;
-    return compact_ref(items[2 * item], n, e);
+    return tile_ref(items[2 * item], n, e, item);
 }
 
-// Pair tile t -> this CTA's band(s) (MODE 2). tab lists the experts in hand-out order (first
-// down-projection item, items); the expert's items in pairs, all nN tiles of a pair item together
-// (band first), or, for an expert of at most n_outer_items items, one N tile of all its pair items
-// after another, except for the last expert, whose bands then still complete one after another
-// while its tiles run; rank r takes item 2 * pair + r (mA = mB = -1: none, with the expert of rank
-// 0's item).
+// Pair tile t -> this CTA's rows (down-projection tiles). tab lists the experts in hand-out order
+// (first down-projection item, items); the expert's items in pairs, all nN tiles of a pair item
+// together (item first), or, for an expert of at most n_outer_items items, one N tile of all its
+// pair items after another, except for the last expert, whose bands then still complete one after
+// another while its tiles run; rank r takes item 2 * pair + r (row -1: none, with the expert of
+// rank 0's item).
 __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E, int nN, const int32_t* items,
-                                                    const int32_t* tiles, const int32_t* crow, uint32_t rank,
-                                                    int n_outer_items) {
+                                                    uint32_t rank, int n_outer_items) {
     const int* cum = tab;
     const int* first = tab + (E + 1);
     const int* count = first + E;
     const int r = tab_segment(cum, E, t), local = t - cum[r];
     int pi, n;
-    if (count[r] <= n_outer_items && cum[r + 1] != cum[E]) {  // the last expert's tiles stay band first
+    if (count[r] <= n_outer_items && cum[r + 1] != cum[E]) {  // the last expert's tiles stay item first
         const int np = (count[r] + 1) >> 1;  // >= 1: an expert without items owns no tile
         n = local / np;
         pi = local - n * np;
@@ -861,17 +839,9 @@ __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E
         n = local - pi * nN;
     }
     const int it = 2 * pi + (int)rank;
-    if (it >= count[r]) {
-        TileRef x;
-        x.item = -1;
-        x.mA = x.mB = -1;
-        x.n = n;
-        x.e = tiles[4 * items[2 * (first[r] + 2 * pi)]];
-        x.rowA = x.rowB = x.lrowA = x.lrowB = 0;
-        return x;
-    }
+    if (it >= count[r]) return tile_ref(-1, n, items[2 * (first[r] + 2 * pi) + 1], -1);
     const int item = first[r] + it;
-    return make_ref(items[2 * item], items[2 * item + 1], n, tiles, crow, item);
+    return tile_ref(items[2 * item], n, items[2 * item + 1], item);
 }
 
 // The CTA-pair GEMM. MODE 1: SwiGLU tiles -> Hc; 2: down-projection tiles -> Yp (+ flags, consumer
@@ -883,15 +853,14 @@ __device__ __forceinline__ TileRef decode_pair_down(int t, const int* tab, int E
 // down-projection starts on the SMs that finish their SwiGLU tiles instead of after the whole GEMM;
 // the consumer clusters take SwiGLU tiles too and start copying when those run out. Every count is
 // completed by epilogue warps that wait on nothing of the down-projection, so no wait can stall for
-// good. Operands: mA / mAh / mB0 / mB1 / mOut are the launch's (MODE 1: Xc, -, W1, W3, Hc store;
-// MODE 2: Hc, Hc halves, W2 halves twice, Yp store); MODE 3 passes the SwiGLU ones there and the
-// down-projection's as mA2 / mA2h / mB2 / mOut2.
+// good. Operands: mA / mB0 / mB1 / mOut are the launch's (MODE 1: Xc, W1, W3, Hc store; MODE 2: Hc,
+// W2 halves twice, Yp store); MODE 3 passes the SwiGLU ones there and the down-projection's as
+// mA2 / mB2 / mOut2.
 template <int MODE>
 __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, const CUtensorMap* mA,
-                                          const CUtensorMap* mAh, const CUtensorMap* mB0, const CUtensorMap* mB1,
-                                          const CUtensorMap* mOut, const CUtensorMap* mA2, const CUtensorMap* mA2h,
-                                          const CUtensorMap* mB2, const CUtensorMap* mOut2, int num_producers,
-                                          int overlapped) {
+                                          const CUtensorMap* mB0, const CUtensorMap* mB1, const CUtensorMap* mOut,
+                                          const CUtensorMap* mA2, const CUtensorMap* mB2, const CUtensorMap* mOut2,
+                                          int num_producers, int overlapped) {
     constexpr bool HAS_UP = MODE != 2, HAS_DN = MODE != 1, FUSED = MODE == 3;
     extern __shared__ uint8_t smem_raw[];
     const PairSmem sm = carve_pair(smem_raw);
@@ -908,8 +877,8 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
     const int KB_up = s.d / BK, KB_dn = s.ffn / BK;
     const unsigned long long tmo = s.timeout_ns;
     const bool dispatch = HAS_UP && (s.flags & MOE_FUSED_DISPATCH);
-    const int bad_item = __syncthreads_or((HAS_UP ? plan_items_bad(s, p, 1, NU, MT) : 0) |
-                                          (HAS_DN ? plan_items_bad(s, p, 2, ND, MT) : 0));  // same in every CTA
+    const int bad_item = __syncthreads_or((HAS_UP ? plan_items_bad(s, p, 1, NU) : 0) |
+                                          (HAS_DN ? plan_items_bad(s, p, 2, ND) : 0));  // same in every CTA
     if (bad_item) NU = ND = 0;
     // expert tables: the down-projection's at tab ([cum (E+1) | first item (E) | items (E) | first
     // direct item]); the SwiGLU one at tab in MODE 1, after the down-projection's in MODE 3 (with the
@@ -975,9 +944,13 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
             acc += ((count[r] + 1) >> 1) * nN_dn;
         }
         sm.tab[E] = acc;
-        // MOE_DIRECT_TAIL: the first item of the first pair item whose first tile is among the last
-        // `window` hand-out positions (the pair items' first tiles rise with the item index, so every
-        // later item is in the window too); its epilogue and every later one's write into Ret
+        // MOE_DIRECT_TAIL: the first item of the first pair item with a tile among the last `window`
+        // hand-out positions, i.e. whose last tile is (the pair items' last tiles rise with the item
+        // index, so every later item has one there too): those items may complete bands in the last
+        // wave, so their epilogue and every later one's write those bands into Ret. In the first
+        // expert that reaches the window (rel = the window's start inside its tiles) that is pair
+        // item rel / nN (item first: pair item p's tiles end at (p + 1) nN - 1) or
+        // rel - (nN - 1) np (N tile by N tile: pair item p's last tile is at (nN - 1) np + p)
         int from = INT_MAX;
         if (overlapped && (s.flags & MOE_DIRECT_TAIL) && ND > 0 && acc > 0) {
             const int window = s.tail_window > 0 ? s.tail_window : num_producers / 2, thr = acc - window;
@@ -987,7 +960,7 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
                 if (np == 0 || sm.tab[r + 1] <= thr) continue;
                 const bool n_outer = count[r] <= s.down_n_outer_items && sm.tab[r + 1] != acc;
                 const int rel = thr - sm.tab[r];
-                const int pi = rel <= 0 ? 0 : (n_outer ? rel : (rel + nN_dn - 1) / nN_dn);
+                const int pi = rel <= 0 ? 0 : (n_outer ? max(0, rel - (nN_dn - 1) * np) : rel / nN_dn);
                 if (pi < np) {
                     from = first[r] + 2 * pi;
                     break;
@@ -1021,13 +994,11 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
     }
     if (tid == 0) {
         tma_prefetch_desc(mA);
-        if (MODE == 2) tma_prefetch_desc(mAh);
         tma_prefetch_desc(mB0);
         tma_prefetch_desc(mB1);
         tma_prefetch_desc(mOut);
         if (FUSED) {
             tma_prefetch_desc(mA2);
-            tma_prefetch_desc(mA2h);
             tma_prefetch_desc(mB2);
             tma_prefetch_desc(mOut2);
         }
@@ -1048,14 +1019,13 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
     const int N_dn = HAS_DN ? ((ND > 0 && sm.tab[E] > 0) ? sm.tab[E] : 0) : 0;  // down-projection pair tiles
     const int total = N_up + N_dn;  // tile t: [0, N_up) SwiGLU, [N_up, total) down-projection
     const bool bad = gemm_cta && rank == 0 && *sm.peer_base != tmem;  // not one pair allocation
-    const uint32_t want = FLAG_READY * s.n_tiles_n2 + ((s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u);
+    const uint32_t stall = (s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u;  // a count no band reaches
     unsigned long long last_end = 0;
     const int direct_from = HAS_DN ? sm.tab[3 * E + 1] : INT_MAX;
     uint32_t nk = 0;  // TMA thread: k-blocks whose loads this CTA issued (rank 0: armed and issued)
     auto is_dn = [&](int t) { return MODE == 2 || (MODE == 3 && t >= N_up); };
     auto decode = [&](int t) {
-        return is_dn(t) ? decode_pair_down(t - N_up, sm.tab, E, nN_dn, p.items_down, p.tiles, p.tile_crow, rank,
-                                           s.down_n_outer_items)
+        return is_dn(t) ? decode_pair_down(t - N_up, sm.tab, E, nN_dn, p.items_down, rank, s.down_n_outer_items)
                         : decode_pair_up(t, tab_up, E, p.items_up, rank, FUSED ? eid_up : nullptr);
     };
 
@@ -1138,10 +1108,8 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
                         atomicMin(&p.trace[MOE_TRACE_GEMM2_START], globaltimer());
                     }
                 }
-                const bool halves = dn && tr.mB >= 0 && tr.mB != tr.mA;  // two 64-row boxes
                 const int brow = dn ? tr.n * 2 * BN1 + (int)rank * BN1 : tr.n * BN1;
                 const CUtensorMap* ta = (FUSED && dn) ? mA2 : mA;
-                const CUtensorMap* tah = FUSED ? mA2h : mAh;
                 const CUtensorMap* tb = (FUSED && dn) ? mB2 : (rank == 0 ? mB0 : mB1);
                 const int KB = dn ? KB_dn : KB_up;
                 const int claim_kb = KB > 8 ? KB - 8 : 0;
@@ -1165,23 +1133,13 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
                     uint8_t* b = a + PAIR_A_BYTES;
                     if (rank == 0) {
                         mbar_arrive_expect_tx(&sm.full[st], bytes);
-                        if (halves) {
-                            tma_load_2d(a, tah, &sm.full[st], kb * BK, tr.lrowA);
-                            tma_load_2d(a + PAIR_A_BYTES / 2, tah, &sm.full[st], kb * BK, tr.lrowB);
-                        } else if (tr.mA >= 0) {
-                            tma_load_2d(a, ta, &sm.full[st], kb * BK, tr.lrowA);  // 128 compact rows
-                        }
+                        tma_load_2d(a, ta, &sm.full[st], kb * BK, tr.row >= 0 ? tr.row : s.PC_max);  // 128 compact rows
                         tma_load_3d(b, tb, &sm.full[st], kb * BK, brow, tr.e);  // gate rows / W2 rows 0-127
                     } else {
                         const uint32_t full0 = mapa_shared(smem_u32(&sm.full[st]), 0u);
                         // an odd CTA without rows loads a box past the last row: zeros, so its idle
                         // half of the UMMA multiplies zeros (less switching power than stale rows)
-                        if (halves) {
-                            tma_load_2d_pair(a, tah, full0, kb * BK, tr.lrowA);
-                            tma_load_2d_pair(a + PAIR_A_BYTES / 2, tah, full0, kb * BK, tr.lrowB);
-                        } else {
-                            tma_load_2d_pair(a, ta, full0, kb * BK, tr.mA >= 0 ? tr.lrowA : s.PC_max);
-                        }
+                        tma_load_2d_pair(a, ta, full0, kb * BK, tr.row >= 0 ? tr.row : s.PC_max);
                         tma_load_3d_pair(b, tb, full0, kb * BK, brow, tr.e);  // up rows / W2 rows 128-255
                     }
                     ++nk;
@@ -1295,38 +1253,21 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
                 }
                 tc_fence_after();
                 const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 256);
-                // rows 0-63 belong to band mA, rows 64-127 to band mB (or to mA for a 128-row band)
-                const int mq = (q < 2) ? tr.mA : tr.mB;
-                const bool active = mq >= 0;
-                const int y = (q < 2 ? tr.rowA : tr.rowB) + (q & 1) * 32;
+                const int c0 = tr.row + q * 32;  // this warp's first compact row (tr.row < 0: no rows)
+                DownRow dr{nullptr, -1, -1, false};
                 if (dn) {
-                    const DirectDst dd = (active && tr.item >= direct_from) ? direct_dst(s, p, tr, q)
-                                                                            : DirectDst{nullptr, 0};
-                    epilogue_rows<2>(es, FUSED ? mOut2 : mOut, tb, tr.n, 2 * BN1, y, active, lane, dd,
-                                     (size_t)s.d * 2);
+                    if (tr.row >= 0) dr = down_row(s, p, c0 + lane, MT, direct_from);
+                    epilogue_down(es, FUSED ? mOut2 : mOut, tb, tr.n, 2 * BN1, dr, lane);
                 } else {
-                    epilogue_rows<1>(es, mOut, tb, tr.n, 2 * BN1, y, active, lane);
+                    epilogue_swiglu(es, mOut, tb, tr.n, c0, tr.row >= 0, lane);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(acc_empty0 + b * 8u);
-                if (dn && active) {
-                    if (flags && lane == 0) {
-                        // publish this warp's rows of the tile, as in gemm_kernel: stores complete,
-                        // async proxy fenced, then the release adds to the tile flag and band counter
-                        const uint32_t inc = (tr.mB == tr.mA) ? 1u : 2u;  // quarters per band: 4 in all
-                        bulk_wait_all();
-                        fence_proxy_async_global();
-                        __threadfence();
-                        red_release_gpu_add(p.flags + (size_t)mq * s.n_tiles_n2 + tr.n, inc);
-                        const uint32_t before = atom_release_gpu_add(p.bands + mq, inc);
-                        if (before + inc == FLAG_READY * (uint32_t)s.n_tiles_n2) {
-                            atomicMax(&p.trace[MOE_TRACE_BAND_DONE], globaltimer());
-                            if (p.host_rec) host_band_record(s, p, mq);  // the band's last quarter
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) last_end = globaltimer();
+                if (dn) {
+                    if (flags) publish_rows(s, p, dr, tr.n, lane);
+                    const bool stored = __any_sync(0xffffffffu, dr.band >= 0);
+                    if (lane == 0 && stored) last_end = globaltimer();
                 }
                 if (FUSED && !dn && lane == 0) {
                     // this warp's quarter of the SwiGLU tile (stored or idle) counts towards its
@@ -1367,17 +1308,15 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
     // copy engines: consumer CTAs from the start (fused: after their SwiGLU tiles), producers once
     // their tiles are done (tail assist)
     if (HAS_DN && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
-        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, want, direct_from);
+        copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, stall, direct_from);
 }
 
 template <int MODE>  // 1: SwiGLU up-projection -> Hc; 2: down-projection -> Yp (+ flags / consumers)
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_pair_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmAh, const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut,
-                     int num_producers, int overlapped) {
-    pair_body<MODE>(s, p, &tmA, &tmAh, &tmB0, &tmB1, &tmOut, nullptr, nullptr, nullptr, nullptr, num_producers,
-                    overlapped);
+                     const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                     const __grid_constant__ CUtensorMap tmOut, int num_producers, int overlapped) {
+    pair_body<MODE>(s, p, &tmA, &tmB0, &tmB1, &tmOut, nullptr, nullptr, nullptr, num_producers, overlapped);
 }
 
 // Both expert GEMMs in one launch (MOE_FUSED_GEMMS): the MODE 3 body.
@@ -1385,22 +1324,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_fused_pair_kernel(Shape s, PlanPtrs p, const __grid_constant__ CUtensorMap tmXc,
                            const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmW3,
                            const __grid_constant__ CUtensorMap tmHcOut, const __grid_constant__ CUtensorMap tmHc,
-                           const __grid_constant__ CUtensorMap tmHch, const __grid_constant__ CUtensorMap tmW2h,
-                           const __grid_constant__ CUtensorMap tmYpOut, int num_producers) {
-    pair_body<3>(s, p, &tmXc, nullptr, &tmW1, &tmW3, &tmHcOut, &tmHc, &tmHch, &tmW2h, &tmYpOut, num_producers, 1);
+                           const __grid_constant__ CUtensorMap tmW2h, const __grid_constant__ CUtensorMap tmYpOut,
+                           int num_producers) {
+    pair_body<3>(s, p, &tmXc, &tmW1, &tmW3, &tmHcOut, &tmHc, &tmW2h, &tmYpOut, num_producers, 1);
 }
 
 static cudaError_t set_smem_attr(const void* fn) {
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
 }
 
-cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
-                               const CUtensorMap& tmW1, const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms,
-                               cudaStream_t st) {
+cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW1,
+                               const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms, cudaStream_t st) {
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<1>));
     if (e != cudaSuccess) return e;
     return launch_k(gemm_kernel<1>, dim3(sms), dim3(GEMM_THREADS), GEMM_SMEM, st, (s.flags & MOE_PDL) != 0, s, p, tmA,
-                    tmAh, tmW1, tmW3, tmOut, sms, 0);
+                    tmW1, tmW3, tmOut, sms, 0);
 }
 
 // Co-resident clusters of two of a pair kernel on this device (cluster occupancy query, cached).
@@ -1430,34 +1368,33 @@ static cudaError_t pair_clusters(int* out) {
 }
 
 cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA,
-                                    const CUtensorMap& tmAh, const CUtensorMap& tmW1, const CUtensorMap& tmW3,
-                                    const CUtensorMap& tmOut, cudaStream_t st) {
+                                    const CUtensorMap& tmW1, const CUtensorMap& tmW3, const CUtensorMap& tmOut,
+                                    cudaStream_t st) {
     int pairs = 0;
     cudaError_t e = pair_clusters<1>(&pairs);
     if (e != cudaSuccess) return e;
     return launch_k(gemm_pair_kernel<1>, dim3(2 * pairs), dim3(GEMM_THREADS), PAIR_SMEM, st, (s.flags & MOE_PDL) != 0,
-                    s, p, tmA, tmAh, tmW1, tmW3, tmOut, 2 * pairs, 0);
+                    s, p, tmA, tmW1, tmW3, tmOut, 2 * pairs, 0);
 }
 
 // Down-projection on CTA pairs: 2 x (co-resident clusters) CTAs, the last `consumers` (even) of them
 // consumer CTAs when overlapped. Every tile is handed out by the counter, so no CTA waits for a
 // particular one to become resident: no cooperative launch is needed.
-cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
-                                  const CUtensorMap& tmW2h, const CUtensorMap& tmOut, int consumers, bool overlapped,
-                                  cudaStream_t st) {
+cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2h,
+                                  const CUtensorMap& tmOut, int consumers, bool overlapped, cudaStream_t st) {
     int pairs = 0;
     cudaError_t e = pair_clusters<2>(&pairs);
     if (e != cudaSuccess) return e;
     const int grid = 2 * pairs, producers = overlapped ? grid - consumers : grid;
     if ((consumers & 1) || producers < 2) return cudaErrorInvalidConfiguration;
     return launch_k(gemm_pair_kernel<2>, dim3(grid), dim3(GEMM_THREADS), PAIR_SMEM, st, (s.flags & MOE_PDL) != 0, s, p,
-                    tmA, tmAh, tmW2h, tmW2h, tmOut, producers, overlapped ? 1 : 0);
+                    tmA, tmW2h, tmW2h, tmOut, producers, overlapped ? 1 : 0);
 }
 
 cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmXc, const CUtensorMap& tmW1,
                                    const CUtensorMap& tmW3, const CUtensorMap& tmHcOut, const CUtensorMap& tmHc,
-                                   const CUtensorMap& tmHch, const CUtensorMap& tmW2h, const CUtensorMap& tmYpOut,
-                                   int consumers, cudaStream_t st) {
+                                   const CUtensorMap& tmW2h, const CUtensorMap& tmYpOut, int consumers,
+                                   cudaStream_t st) {
     const void* fn = reinterpret_cast<const void*>(&gemm_fused_pair_kernel);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, PAIR_SMEM_FUSED);
     if (e != cudaSuccess) return e;
@@ -1480,12 +1417,11 @@ cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUte
     const int grid = 2 * cache[dev], producers = grid - consumers;
     if ((consumers & 1) || producers < 2) return cudaErrorInvalidConfiguration;
     return launch_k(gemm_fused_pair_kernel, dim3(grid), dim3(GEMM_THREADS), PAIR_SMEM_FUSED, st,
-                    (s.flags & MOE_PDL) != 0, s, p, tmXc, tmW1, tmW3, tmHcOut, tmHc, tmHch, tmW2h, tmYpOut, producers);
+                    (s.flags & MOE_PDL) != 0, s, p, tmXc, tmW1, tmW3, tmHcOut, tmHc, tmW2h, tmYpOut, producers);
 }
 
-cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
-                             const CUtensorMap& tmW2, const CUtensorMap& tmOut, int sms, int consumers, bool overlapped,
-                             cudaStream_t st) {
+cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2,
+                             const CUtensorMap& tmOut, int sms, int consumers, bool overlapped, cudaStream_t st) {
     cudaError_t e = set_smem_attr(reinterpret_cast<const void*>(&gemm_kernel<2>));
     if (e != cudaSuccess) return e;
     const int producers = overlapped ? sms - consumers : sms;
@@ -1493,14 +1429,14 @@ cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMa
     const int threads = (overlapped && (s.flags & MOE_COPY_WARPS)) ? GEMM_THREADS_MAX : GEMM_THREADS;
     Shape sa = s;
     PlanPtrs pa = p;
-    CUtensorMap a = tmA, ah = tmAh, b0 = tmW2, b1 = tmW2, o = tmOut;
+    CUtensorMap a = tmA, b0 = tmW2, b1 = tmW2, o = tmOut;
     if (!overlapped) {
-        gemm_kernel<2><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(sa, pa, a, ah, b0, b1, o, producers, ov);
+        gemm_kernel<2><<<sms, GEMM_THREADS, GEMM_SMEM, st>>>(sa, pa, a, b0, b1, o, producers, ov);
         return cudaGetLastError();
     }
     // Cooperative launch: every CTA (producers and consumers) is resident at once, or the launch
     // fails; the consumers' waits on producer flags can therefore always be satisfied.
-    void* args[] = {&sa, &pa, &a, &ah, &b0, &b1, &o, (void*)&producers, &ov};
+    void* args[] = {&sa, &pa, &a, &b0, &b1, &o, (void*)&producers, &ov};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(&gemm_kernel<2>), dim3(sms), dim3(threads),
                                        args, GEMM_SMEM, st);
 }

@@ -114,7 +114,7 @@ int make_layout(const moe_config* c, Layout* out) {
     L.slot = put(TK * 4);
     L.cslot = put(TK * 4);
     L.ret_slot = put(TK * 4);
-    L.ccoff = put(G * 4);
+    L.yrow = put(PC_max * 4);
     L.tile_crow = put(MT_max * 4);
     L.band_item = put(MT_max * 4);
     L.tok_of = put(PC_max * 4);
@@ -191,7 +191,7 @@ PlanPtrs plan_ptrs(const moe_layout& L, void* ws) {
     p.slot = reinterpret_cast<int32_t*>(b + L.slot);
     p.cslot = reinterpret_cast<int32_t*>(b + L.cslot);
     p.ret_slot = reinterpret_cast<int32_t*>(b + L.ret_slot);
-    p.ccoff = reinterpret_cast<int32_t*>(b + L.ccoff);
+    p.yrow = reinterpret_cast<int32_t*>(b + L.yrow);
     p.tile_crow = reinterpret_cast<int32_t*>(b + L.tile_crow);
     p.band_item = reinterpret_cast<int32_t*>(b + L.band_item);
     p.tok_of = reinterpret_cast<int32_t*>(b + L.tok_of);
@@ -333,11 +333,9 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     // baseline of the same configuration uses the same kernel.
     const bool pair_down = (S.flags & MOE_PAIR_UMMA) && !(S.flags & MOE_COPY_WARPS) && S.bn2 == 2 * BN1 &&
                            (c.consumers % 2 == 0);
-    CUtensorMap tXc, tXch, tHc, tHch, tW1, tW3, tW2, tW2h, tHcOut, tYpOut;
+    CUtensorMap tXc, tHc, tW1, tW3, tW2, tW2h, tHcOut, tYpOut;
     int rc = make_map(&tXc, c.p.Xc, 2, S.d, S.PC_max, 1, BM, "Xc");
-    if (!rc) rc = make_map(&tXch, c.p.Xc, 2, S.d, S.PC_max, 1, BM / 2, "Xc (half)");
     if (!rc) rc = make_map(&tHc, c.p.Hc, 2, S.ffn, S.PC_max, 1, BM, "Hc");
-    if (!rc) rc = make_map(&tHch, c.p.Hc, 2, S.ffn, S.PC_max, 1, BM / 2, "Hc (half)");
     if (!rc) rc = make_map(&tHcOut, c.p.Hc, 2, S.ffn, S.PC_max, 1, 32, "Hc (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tYpOut, c.p.Yp, 2, S.d, S.P_max, 1, 32, "Yp (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tW1, W1, 3, S.d, S.ffn, S.E, BN1, "W1");
@@ -357,7 +355,7 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
     cudaError_t e;
     if (overlapped && pair_down && (S.flags & MOE_FUSED_GEMMS)) {
         // both GEMMs in one launch: the stage events after it mark the end of both
-        e = launch_gemm_fused_pair(S, c.p, tXc, tW1, tW3, tHcOut, tHc, tHch, tW2h, tYpOut, c.consumers, c.st);
+        e = launch_gemm_fused_pair(S, c.p, tXc, tW1, tW3, tHcOut, tHc, tW2h, tYpOut, c.consumers, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "fused GEMM launch");
         if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
@@ -366,18 +364,18 @@ int run_forward(Call& c, const float* logits, const uint16_t* x, const uint16_t*
         if (e != cudaSuccess) return cuda_fail(e, "combine launch");
         return record(ev, MOE_EV_END, c.st);
     }
-    e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.st)
-                                  : launch_gemm_swiglu(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.di.sms, c.st);
+    e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tW1, tW3, tHcOut, c.st)
+                                  : launch_gemm_swiglu(S, c.p, tXc, tW1, tW3, tHcOut, c.di.sms, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
     if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
     if (overlapped) {
-        e = pair_down ? launch_gemm_down_pair(S, c.p, tHc, tHch, tW2h, tYpOut, c.consumers, true, c.st)
-                      : launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, c.consumers, true, c.st);
+        e = pair_down ? launch_gemm_down_pair(S, c.p, tHc, tW2h, tYpOut, c.consumers, true, c.st)
+                      : launch_gemm_down(S, c.p, tHc, tW2, tYpOut, c.di.sms, c.consumers, true, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "overlapped down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
     } else {
-        e = pair_down ? launch_gemm_down_pair(S, c.p, tHc, tHch, tW2h, tYpOut, 0, false, c.st)
-                      : launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, 0, false, c.st);
+        e = pair_down ? launch_gemm_down_pair(S, c.p, tHc, tW2h, tYpOut, 0, false, c.st)
+                      : launch_gemm_down(S, c.p, tHc, tW2, tYpOut, c.di.sms, 0, false, c.st);
         if (e != cudaSuccess) return cuda_fail(e, "down-projection launch");
         if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
         e = launch_copy_seq(S, c.p, c.di.sms, c.st);
@@ -404,7 +402,7 @@ namespace {
 // Offsets of the plan's scratch regions inside the static array for one config (256-byte aligned).
 struct StaticLayout {
     size_t rank, cnt, base, counts, ret, tiles, tret, sched, order, seg, exp, iu, id, meta, flags, bands, trace,
-        cslot, ccoff, tcrow, bitem, tokof, xrows, xready, bytes;
+        cslot, yrow, tcrow, bitem, tokof, xrows, xready, bytes;
 };
 
 StaticLayout static_layout(const Layout& lay) {
@@ -436,7 +434,7 @@ StaticLayout static_layout(const Layout& lay) {
     o.bands = put(MT * 4);
     o.trace = put(TR_COUNT * 8);
     o.cslot = put(TK * 4);
-    o.ccoff = put(E * R * 4);
+    o.yrow = put((size_t)L.PC_max * 4);
     o.tcrow = put(MT * 4);
     o.bitem = put(MT * 4);
     o.tokof = put((size_t)L.PC_max * 4);
@@ -754,7 +752,8 @@ MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const f
 // The return copy on the GPU's copy engines: the down-projection runs on every SM without consumers,
 // and the epilogue warp that completes a band writes a record into pinned host memory (Yp row, Ret
 // row, valid rows, then the call's tag, released at system scope). The calling thread polls the
-// records and issues one cudaMemcpyAsync per ready band on a copy stream of its own; the combine
+// records and issues one cudaMemcpyAsync per run of ready bands that are adjacent in both Yp and Ret
+// (else per band) on a copy stream of its own; the combine
 // waits for that stream. Records: 4 words of header (tag, band count, padded rows, 0), then 4 words
 // per band (tag, Ret row, valid rows, Yp row).
 struct DmaPipe {
@@ -815,11 +814,9 @@ static int run_forward_dma(Call& c, const float* logits, const uint16_t* x, cons
     S.host_epoch = epoch;
     c.p.host_rec = static_cast<uint32_t*>(dev_rec);
     const bool pair_down = (S.flags & MOE_PAIR_UMMA) && S.bn2 == 2 * BN1;
-    CUtensorMap tXc, tXch, tHc, tHch, tW1, tW3, tW2, tW2h, tHcOut, tYpOut;
+    CUtensorMap tXc, tHc, tW1, tW3, tW2, tW2h, tHcOut, tYpOut;
     rc = make_map(&tXc, c.p.Xc, 2, S.d, S.PC_max, 1, BM, "Xc");
-    if (!rc) rc = make_map(&tXch, c.p.Xc, 2, S.d, S.PC_max, 1, BM / 2, "Xc (half)");
     if (!rc) rc = make_map(&tHc, c.p.Hc, 2, S.ffn, S.PC_max, 1, BM, "Hc");
-    if (!rc) rc = make_map(&tHch, c.p.Hc, 2, S.ffn, S.PC_max, 1, BM / 2, "Hc (half)");
     if (!rc) rc = make_map(&tHcOut, c.p.Hc, 2, S.ffn, S.PC_max, 1, 32, "Hc (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tYpOut, c.p.Yp, 2, S.d, S.P_max, 1, 32, "Yp (store)", EPI_CHUNK, false);
     if (!rc) rc = make_map(&tW1, W1, 3, S.d, S.ffn, S.E, BN1, "W1");
@@ -836,12 +833,12 @@ static int run_forward_dma(Call& c, const float* logits, const uint16_t* x, cons
     c.p.x = reinterpret_cast<const __nv_bfloat16*>(x);
     if ((rc = run_plan(c, logits, x, !(S.flags & MOE_FUSED_DISPATCH)))) return rc;
     if ((rc = record(ev, MOE_EV_PLANNED, c.st))) return rc;
-    e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.st)
-                                  : launch_gemm_swiglu(S, c.p, tXc, tXch, tW1, tW3, tHcOut, c.di.sms, c.st);
+    e = (S.flags & MOE_PAIR_UMMA) ? launch_gemm_swiglu_pair(S, c.p, tXc, tW1, tW3, tHcOut, c.st)
+                                  : launch_gemm_swiglu(S, c.p, tXc, tW1, tW3, tHcOut, c.di.sms, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "SwiGLU GEMM launch");
     if ((rc = record(ev, MOE_EV_UP, c.st))) return rc;
-    e = pair_down ? launch_gemm_down_pair(S, c.p, tHc, tHch, tW2h, tYpOut, 0, true, c.st)
-                  : launch_gemm_down(S, c.p, tHc, tHch, tW2, tYpOut, c.di.sms, 0, true, c.st);
+    e = pair_down ? launch_gemm_down_pair(S, c.p, tHc, tW2h, tYpOut, 0, true, c.st)
+                  : launch_gemm_down(S, c.p, tHc, tW2, tYpOut, c.di.sms, 0, true, c.st);
     if (e != cudaSuccess) return cuda_fail(e, "down-projection launch");
     if ((rc = record(ev, MOE_EV_DOWN, c.st))) return rc;
 
@@ -864,20 +861,37 @@ static int run_forward_dma(Call& c, const float* logits, const uint16_t* x, cons
             if (MT < 0 || MT > S.MT_max) return fail(MOE_ERR_PLAN, "band count %d out of range", MT);
             done.assign((size_t)MT, 0);
         }
+        // Ready bands that are adjacent in both Yp and Ret (a group's bands in layout order) go out as
+        // one copy: one host call per run instead of per band.
+        uint32_t run_ret = 0, run_row = 0, run_rows = 0;
+        auto flush = [&]() -> int {
+            if (run_rows == 0) return MOE_OK;
+            const cudaError_t ce = cudaMemcpyAsync(Ret + (size_t)run_ret * rowb, Yp + (size_t)run_row * rowb,
+                                                   run_rows * rowb, cudaMemcpyDeviceToDevice, dp->cs);
+            run_rows = 0;
+            return ce == cudaSuccess ? MOE_OK : cuda_fail(ce, "copy-engine band copy");
+        };
         for (int m = 0; MT > 0 && m < MT; ++m) {
-            if (done[m] || h[4 + 4 * (size_t)m] != epoch) continue;
+            if (done[m] || h[4 + 4 * (size_t)m] != epoch) {
+                if ((rc = flush())) return rc;
+                continue;
+            }
             std::atomic_thread_fence(std::memory_order_acquire);
             const uint32_t ret0 = h[4 + 4 * (size_t)m + 1], valid = h[4 + 4 * (size_t)m + 2],
                            row0 = h[4 + 4 * (size_t)m + 3];
             if (valid < 1 || valid > (uint32_t)S.tbM || (size_t)ret0 + valid > (size_t)S.T * S.k ||
                 (size_t)row0 + valid > (size_t)S.P_max)
                 return fail(MOE_ERR_PLAN, "band %d record out of range", m);
-            e = cudaMemcpyAsync(Ret + (size_t)ret0 * rowb, Yp + (size_t)row0 * rowb, valid * rowb,
-                                cudaMemcpyDeviceToDevice, dp->cs);
-            if (e != cudaSuccess) return cuda_fail(e, "copy-engine band copy");
+            if (run_rows && (ret0 != run_ret + run_rows || row0 != run_row + run_rows) && (rc = flush())) return rc;
+            if (run_rows == 0) {
+                run_ret = ret0;
+                run_row = row0;
+            }
+            run_rows += valid;
             done[m] = 1;
             ++issued;
         }
+        if ((rc = flush())) return rc;
         if (MT >= 0 && issued == MT) break;
         if (last_scan) {
             if (MT < 0) return fail(MOE_ERR_PLAN, "the plan kernel finished without its host record");
@@ -1001,7 +1015,7 @@ MOE_API int moe_route_static(const moe_config* cfg, const float* logits, int32_t
     p.slot = slot;
     p.cslot = reinterpret_cast<int32_t*>(b + o.cslot);
     p.ret_slot = ret_slot;
-    p.ccoff = reinterpret_cast<int32_t*>(b + o.ccoff);
+    p.yrow = reinterpret_cast<int32_t*>(b + o.yrow);
     p.tile_crow = reinterpret_cast<int32_t*>(b + o.tcrow);
     p.band_item = reinterpret_cast<int32_t*>(b + o.bitem);
     p.tok_of = reinterpret_cast<int32_t*>(b + o.tokof);

@@ -23,7 +23,7 @@ enum Meta : int {
     META_QUEUE_SEQ = 4,    // next copy unit to hand out (sequential copy)
     META_STATUS = 5,       // 0 or a Status code (first error wins)
     META_STATUS_DETAIL = 6,
-    META_ITEMS = 7,        // down-projection work items (one band, or two bands of <= 64 rows)
+    META_ITEMS = 7,        // down-projection work items (128 compact rows of one expert)
     META_ITEMS_UP = 8,     // SwiGLU work items (128 rows of one expert in the compact layout)
     META_PC = 9,           // rows of the compact layout used by this call
     META_DISPATCH = 24,    // next block of compact rows to copy (MOE_FUSED_DISPATCH)
@@ -79,7 +79,6 @@ static_assert(PAIR_SMEM <= 227 * 1024, "pair GEMM shared memory");
 constexpr int PAIR_SMEM_FUSED = PAIR_SMEM + 4096;
 static_assert(PAIR_SMEM_FUSED <= 227 * 1024, "fused pair GEMM shared memory");
 constexpr int BN1 = 128;                               // output columns of a SwiGLU tile
-constexpr uint32_t FLAG_READY = 4;                     // one release-add per epilogue warp
 constexpr int MAX_E = 256;
 
 // copy engines of the consumer (one per warp, two staging buffers each, in the stage area)
@@ -109,13 +108,13 @@ struct PlanPtrs {
     int32_t* experts;    // [E][8]: first M-tile, M-tiles, first hand-out position, hand-out rank,
                          //         SwiGLU items, first SwiGLU item, first down item, first Xc row
     int32_t* items_up;   // [IU_max][2] SwiGLU work items (first Xc row, expert), experts in id order
-    int32_t* items_down; // [MT_max][2] work items of the down-projection, in hand-out order
+    int32_t* items_down; // [MT_max][2] the SwiGLU items, experts in hand-out rank order
     int32_t* slot;       // padded-layout row (Yp) of each (token, choice)
     int32_t* cslot;      // compact-layout row (Xc, Hc) of each (token, choice)
     int32_t* ret_slot;
-    int32_t* ccoff;      // [E*R] first compact row of each group
+    int32_t* yrow;       // [PC_max] Yp row of each compact row, -1 for a padding row
     int32_t* tile_crow;  // [MT_max] compact row of each band's first row
-    int32_t* band_item;  // [MT_max] down-projection work item holding each band
+    int32_t* band_item;  // [MT_max] down-projection work item holding each band's last row
     int32_t* meta;
     uint32_t* flags;
     uint32_t* bands;
@@ -153,29 +152,27 @@ struct Shape {
 cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p, cudaStream_t st);
 cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st);
 cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtrs& p, int sms, cudaStream_t st);
-// tmA: 128-row boxes of the token rows; tmAh: 64-row boxes of the same tensor (shared work items)
-cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
-                               const CUtensorMap& tmW1, const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms,
-                               cudaStream_t st);
+// tmA: 128-row boxes of the compact token rows
+cudaError_t launch_gemm_swiglu(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW1,
+                               const CUtensorMap& tmW3, const CUtensorMap& tmOut, int sms, cudaStream_t st);
 // The same SwiGLU GEMM on CTA pairs (cluster of 2, UMMA M = 256); grid = 2 x co-resident pairs.
 cudaError_t launch_gemm_swiglu_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA,
-                                    const CUtensorMap& tmAh, const CUtensorMap& tmW1, const CUtensorMap& tmW3,
-                                    const CUtensorMap& tmOut, cudaStream_t st);
-cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
-                             const CUtensorMap& tmW2, const CUtensorMap& tmOut, int sms, int consumers, bool overlapped,
-                             cudaStream_t st);
+                                    const CUtensorMap& tmW1, const CUtensorMap& tmW3, const CUtensorMap& tmOut,
+                                    cudaStream_t st);
+// tmA: 128-row boxes of the compact hidden rows; tmOut: 32 x 32 boxes of Yp
+cudaError_t launch_gemm_down(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2,
+                             const CUtensorMap& tmOut, int sms, int consumers, bool overlapped, cudaStream_t st);
 // The down-projection on CTA pairs (tmW2h: 128-row boxes of W2; needs bn2 = 256, consumers even, no
 // copy warps); grid = 2 x co-resident pairs.
-cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmAh,
-                                  const CUtensorMap& tmW2h, const CUtensorMap& tmOut, int consumers, bool overlapped,
-                                  cudaStream_t st);
+cudaError_t launch_gemm_down_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmA, const CUtensorMap& tmW2h,
+                                  const CUtensorMap& tmOut, int consumers, bool overlapped, cudaStream_t st);
 // Both expert GEMMs in one launch on CTA pairs (MOE_FUSED_GEMMS): SwiGLU operands (Xc, W1, W3, Hc
-// store) and down-projection operands (Hc, Hc halves, W2 halves, Yp store); the last `consumers`
-// (even) CTAs copy once the SwiGLU tiles are gone.
+// store) and down-projection operands (Hc, W2 halves, Yp store); the last `consumers` (even) CTAs
+// copy once the SwiGLU tiles are gone.
 cudaError_t launch_gemm_fused_pair(const Shape& s, const PlanPtrs& p, const CUtensorMap& tmXc, const CUtensorMap& tmW1,
                                    const CUtensorMap& tmW3, const CUtensorMap& tmHcOut, const CUtensorMap& tmHc,
-                                   const CUtensorMap& tmHch, const CUtensorMap& tmW2h, const CUtensorMap& tmYpOut,
-                                   int consumers, cudaStream_t st);
+                                   const CUtensorMap& tmW2h, const CUtensorMap& tmYpOut, int consumers,
+                                   cudaStream_t st);
 cudaError_t launch_copy_seq(const Shape& s, const PlanPtrs& p, int sms, cudaStream_t st);
 cudaError_t launch_combine(const Shape& s, const PlanPtrs& p, float* out, int sms, cudaStream_t st);
 
@@ -370,9 +367,9 @@ __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
 __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t atom_release_gpu_add(uint32_t* p, uint32_t v) {
+__device__ __forceinline__ uint32_t atom_acq_rel_gpu_add(uint32_t* p, uint32_t v) {
     uint32_t old;
-    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {

@@ -256,7 +256,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     __shared__ int s_mt[MAX_E];      // M-tiles per expert
     __shared__ int s_ebase[MAX_E];   // first hand-out position of the expert's bands
     __shared__ int s_cbase[MAX_E];   // first row of the expert in the compact layout
-    __shared__ int s_cc[1024];       // first compact row of group g
     __shared__ int s_fbp[1024];      // full bands of the groups before g (layout order)
     __shared__ int s_pkey[1024];     // sort key of group g's partial band in the schedule
     __shared__ int s_warp[32];
@@ -359,8 +358,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     }
     __syncthreads();
 
-    // 4b. expert-compact layout of the GEMM inputs: each expert's rows contiguous (its groups in
-    // owner order, rows in plan order), the run padded to a multiple of the UMMA tile height BM.
+    // 4b. expert-compact layout of the GEMM inputs: each expert's rows contiguous, the run padded to
+    // a multiple of the UMMA tile height BM; inside the run the expert's bands follow one another in
+    // hand-out order, each band's valid rows in row order (step 5 places them).
     {
         const int e = tid;
         const int rows = (e < E) ? ((s_load[e] + BM - 1) / BM) * BM : 0;
@@ -369,13 +369,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     }
     __syncthreads();
     const int PC = s_total;
-    for (int g = tid; g < G; g += PLAN_THREADS) {
-        const int e = g / R, r = g % R;
-        int acc = s_cbase[e];
-        for (int q = 0; q < r; ++q) acc += s_n[e * R + q];
-        s_cc[g] = acc;
-        p.ccoff[g] = acc;
-    }
     for (int e = tid; e < E; e += PLAN_THREADS) {
         int rk = 0;
         for (int f = 0; f < E; ++f)
@@ -397,7 +390,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     // Hand-out order (the schedule re-sorted stably by expert): experts one after another in rank
     // order (most loaded first); inside an expert its full bands in layout order, then its partial
     // bands by valid rows descending (ties to the lower owner), i.e. key (expert rank, -valid,
-    // owner, row).
+    // owner, row). A band's compact rows start after the valid rows of the expert's bands before it
+    // in hand-out order: full bands fill whole tiles from the run's start, partial bands follow.
     for (int g = tid; g < G; g += PLAN_THREADS) {
         const int e = g / R, r = g % R, n = s_n[g];
         const int m0 = s_off[g] / tbM;
@@ -413,7 +407,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             p.tiles[4 * m + 2] = s_off[g] + i * tbM;
             p.tiles[4 * m + 3] = valid;
             p.tile_ret[m] = rbase + i * tbM;
-            p.tile_crow[m] = s_cc[g] + i * tbM;
+            if (i < nfull) p.tile_crow[m] = s_cbase[e] + (fpre + i) * tbM;
             if (mirror) s_tg[m] = g;
             if (i < nfull) {
                 p.sched[s_fbp[g] + i] = m;
@@ -423,12 +417,15 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         }
         if (nt > nfull) {  // one partial band
             const int valid = n - nfull * tbM;
-            int pos = 0;
+            int pos = 0, rows_before = 0;  // partial bands of the expert before this one, their rows
             for (int rh = 0; rh < R; ++rh) {
                 const int vh = s_n[e * R + rh] % tbM;
                 if (vh == 0 || rh == r) continue;
-                pos += (vh > valid) || (vh == valid && rh < r);
+                const bool before = (vh > valid) || (vh == valid && rh < r);
+                pos += before;
+                rows_before += before ? vh : 0;
             }
+            p.tile_crow[m0 + nfull] = s_cbase[e] + s_fb[e] * tbM + rows_before;
             p.order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
             if (mirror) s_order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
             const int key = s_pkey[g];
@@ -441,10 +438,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     __threadfence_block();
     auto order_at = [&](int pos) { return mirror ? s_order[pos] : p.order[pos]; };
     auto group_of = [&](int m) { return mirror ? s_tg[m] : p.tiles[4 * m] * R + p.tiles[4 * m + 1]; };
-    auto valid_of = [&](int m) {  // valid rows of tile m, from its group's row count
-        const int g = group_of(m), i = m - s_off[g] / tbM;
-        return min(tbM, s_n[g] - i * tbM);
-    };
 
     // 6. segments: runs of hand-out positions holding adjacent bands of one group, cut into pieces
     // of mgb bands
@@ -462,85 +455,43 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         p.seg[2 * q + 1] = min(s.mgb, end - first);
     }
 
-    // 7. GEMM work items. SwiGLU GEMM: the expert's compact run cut into BM-row tiles, item
-    // (first compact row, expert), experts in id order. Down-projection (output tiles must have one
-    // owner): a band that needs only 64 of the UMMA tile's 128 rows (every band when tbM = 64, a
-    // band with <= 64 valid rows when tbM = 128) shares a work item with another such band of the
-    // same expert, each loaded as a 64-row box into one half of the A tile. Item (mA, mB): mB == mA
-    // one 128-row band; mB == -1 one 64-row band alone; else two half bands; hand-out order.
+    // 7. GEMM work items: each expert's compact run cut into BM-row items (first compact row,
+    // expert). The SwiGLU GEMM takes them with the experts in id order; the down-projection takes
+    // the same items with the experts in hand-out order (rank order), so its item list is the SwiGLU
+    // list re-ordered by expert. The down-projection's output rows go to the owner-aligned bands of
+    // Yp, each band counted complete when all its rows of every N tile have been stored.
     __shared__ int s_items[MAX_E], s_ibase_down[MAX_E], s_nitems;
-    for (int e = tid; e < E; e += PLAN_THREADS) {
-        const int cnt = s_mt[e];
-        int half = 0;  // bands with <= 64 valid rows: all of them when tbM = 64, else partial ones
-        for (int r = 0; r < R; ++r) {
-            const int n = s_n[e * R + r];
-            half += (tbM == 64) ? (n + 63) / 64 : (n % 128 != 0 && n % 128 <= 64);
-        }
-        s_items[e] = (cnt - half) + (half + 1) / 2;
-    }
+    for (int e = tid; e < E; e += PLAN_THREADS) s_items[e] = (s_load[e] + BM - 1) / BM;
     __syncthreads();
     for (int e = tid; e < E; e += PLAN_THREADS) {
         int down = 0;
         for (int f = 0; f < E; ++f) down += (s_erank[f] < s_erank[e]) ? s_items[f] : 0;
         s_ibase_down[e] = down;
         if (s_erank[e] == E - 1) s_nitems = down + s_items[e];  // the last expert's items end the list
-        const int iu = (s_load[e] + BM - 1) / BM;
+        const int iu = s_items[e];
         p.experts[8 * e + 4] = iu;
         p.experts[8 * e + 5] = s_cbase[e] / BM;
         p.experts[8 * e + 6] = down;
         p.experts[8 * e + 7] = s_cbase[e];
-        if (s_cbase[e] / BM + iu <= s.IU_max)
+        if (s_cbase[e] / BM + iu <= s.IU_max && down + iu <= s.MT_max)
             for (int i = 0; i < iu; ++i) {
                 p.items_up[2 * (s_cbase[e] / BM + i)] = s_cbase[e] + i * BM;
                 p.items_up[2 * (s_cbase[e] / BM + i) + 1] = e;
+                p.items_down[2 * (down + i)] = s_cbase[e] + i * BM;
+                p.items_down[2 * (down + i) + 1] = e;
             }
     }
     __syncthreads();
-    // One warp per expert, its bands in hand-out order 32 at a time: a band with more than 64 valid
-    // rows is an item of its own; bands with at most 64 pair up in order, each pair emitted at its
-    // second band, an unpaired last one at the end. An item's index is the number of items emitted
-    // before it: (full bands before it) + (half bands before it) / 2.
-    for (int x = tid >> 5; x < E; x += PLAN_THREADS / 32) {
-        const int lane = tid & 31, cnt = s_mt[x];
-        int* out = p.items_down + 2 * s_ibase_down[x];
-        int nfull = 0, nhalf = 0, pending = -1;  // before the current chunk; the unpaired half band
-        for (int b0 = 0; b0 < cnt; b0 += 32) {
-            const bool in = b0 + lane < cnt;
-            const int m = in ? order_at(s_ebase[x] + b0 + lane) : -1;
-            const bool half = in && valid_of(m) <= 64;
-            const unsigned hm = __ballot_sync(0xffffffffu, half), fm = __ballot_sync(0xffffffffu, in && !half);
-            const unsigned lt = (1u << lane) - 1u;
-            const int hb = nhalf + __popc(hm & lt), fb = nfull + __popc(fm & lt);
-            const unsigned prev = hm & lt;  // half bands of this chunk before this lane
-            const int partner_lane = prev ? 31 - __clz(prev) : lane;
-            const int partner = __shfl_sync(0xffffffffu, m, partner_lane);
-            if (in && !half) {
-                out[2 * (fb + hb / 2)] = m;
-                out[2 * (fb + hb / 2) + 1] = m;
-            } else if (half && (hb & 1)) {  // second band of a pair
-                out[2 * (fb + hb / 2)] = prev ? partner : pending;
-                out[2 * (fb + hb / 2) + 1] = m;
-            }
-            const int last_half_lane = hm ? 31 - __clz(hm) : 0;
-            const int last_half = __shfl_sync(0xffffffffu, m, last_half_lane);
-            nfull += __popc(fm);
-            nhalf += __popc(hm);
-            pending = (nhalf & 1) ? (hm ? last_half : pending) : -1;
-        }
-        if (lane == 0 && pending >= 0) {
-            out[2 * (nfull + nhalf / 2)] = pending;
-            out[2 * (nfull + nhalf / 2) + 1] = tbM == 64 ? -1 : pending;
-        }
-    }
 
-    // 7b. the work item holding each band (the inverse of the item list), read by the copy engines
-    // to tell the bands that the down-projection's epilogue returns itself (MOE_DIRECT_TAIL)
-    __syncthreads();
+    // 7b. the down-projection item holding each band's last row, i.e. the item whose tiles complete
+    // the band (a band's rows lie in this item and possibly the one before it of its expert), read by
+    // the epilogue and the copy engines to tell the bands that the epilogue returns itself
+    // (MOE_DIRECT_TAIL): a band is returned that way when this item is in the direct window, so no
+    // band completed by the last wave is left to the copy engines
     const int items = s_nitems;
-    for (int i = tid; i < items; i += PLAN_THREADS) {
-        const int mA = p.items_down[2 * i], mB = p.items_down[2 * i + 1];
-        if (mA >= 0 && mA < MT) p.band_item[mA] = i;
-        if (mB >= 0 && mB < MT) p.band_item[mB] = i;
+    for (int m = tid; m < MT; m += PLAN_THREADS) {
+        const int e = p.tiles[4 * m], valid = p.tiles[4 * m + 3];
+        p.band_item[m] = s_ibase_down[e] + (p.tile_crow[m] + valid - 1 - s_cbase[e]) / BM;
     }
 
     // 8. per-call meta, flags and trace reset
@@ -592,11 +543,13 @@ cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
 
 // ---------------------------------------------------------------------------------------------
 // permute_kernel: one warp per work item. Items [0, T): token t computes its k slots (padded
-// layout), compact slots and return slots, records t as the token of its k compact rows, and copies
-// x[t] into those rows of Xc: each lane first loads up to 16 vectors of 16 bytes (all loads in
-// flight together), then stores them to the k rows. Items [T, T + E * BM/8): one group of 8 rows of
-// an expert's last BM-row tile in the compact layout, marking those rows past the expert's rows as
-// padding (token -1) and zeroing them. With x == nullptr only the slots and tokens are written.
+// layout), compact slots (the compact row of its band's first row plus its row inside the band) and
+// return slots, records t as the token and the padded row as the Yp row of its k compact rows, and
+// copies x[t] into those rows of Xc: each lane first loads up to 16 vectors of 16 bytes (all loads
+// in flight together), then stores them to the k rows. Items [T, T + E * BM/8): one group of 8 rows
+// of an expert's last BM-row tile in the compact layout, marking those rows past the expert's rows
+// as padding (token -1, no Yp row) and zeroing them. With x == nullptr only the slots, tokens and
+// Yp rows are written.
 // ---------------------------------------------------------------------------------------------
 constexpr int PERM_VEC = 16;  // 16-byte vectors per lane per pass
 
@@ -617,12 +570,14 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
     for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < s.T + pad_items; item += nwarps) {
         if (item < s.T) {
             const int t = item, r = t / per, c = t / s.chunk_tokens;
-            int my_cs = 0;
+            int my_cs = 0, my_y = 0;
             if (lane < k) {
                 const int e = p.idx[(size_t)t * k + lane];
                 const int rk = p.chunk_base[(size_t)c * E + e] + p.rank[(size_t)t * k + lane];
-                my_cs = p.ccoff[e * R + r] + rk;
-                p.slot[(size_t)t * k + lane] = p.offsets[e * R + r] + rk;
+                my_y = p.offsets[e * R + r] + rk;
+                const int m = my_y / s.tbM;  // bands start at multiples of the tile height
+                my_cs = (m >= 0 && m < s.MT_max) ? p.tile_crow[m] + (my_y - m * s.tbM) : -1;
+                p.slot[(size_t)t * k + lane] = my_y;
                 p.cslot[(size_t)t * k + lane] = my_cs;
                 p.ret_slot[(size_t)t * k + lane] = r * slice + p.ret_off[r * (E + 1) + e] + rk;
             }
@@ -637,7 +592,10 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
                 if (lane == 0) set_status(p.meta, ST_BAD_PLAN, t);
                 continue;
             }
-            if (lane < k) p.tok_of[my_cs] = t;  // the compact row's token (read by a fused dispatch)
+            if (lane < k) {
+                p.tok_of[my_cs] = t;    // the compact row's token (read by a fused dispatch)
+                p.yrow[my_cs] = my_y;   // and its output row (read by the down-projection's epilogue)
+            }
             if (xs == nullptr) continue;  // plan only: slots without the row copy
             for (int base = 0; base < vec; base += 32 * PERM_VEC) {
                 uint4 v[PERM_VEC];
@@ -660,13 +618,17 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
             // the expert's run is [cb, cb + iu * BM) and holds `rows` real rows
             const int q = item - s.T, e = q / groups, g = q % groups;
             const int iu = p.experts[8 * e + 4], cb = p.experts[8 * e + 7];
-            const int rows = p.ccoff[e * R + R - 1] + p.counts[e * R + R - 1] - cb;
+            int rows = 0;
+            for (int r = 0; r < R; ++r) rows += p.counts[e * R + r];
             if (iu <= 0) continue;
             const uint4 z = make_uint4(0, 0, 0, 0);
             for (int rr = max(rows, (iu - 1) * BM + g * 8); rr < (iu - 1) * BM + (g + 1) * 8; ++rr) {
                 const size_t row = (size_t)cb + rr;
                 if (row >= (size_t)PC) break;
-                if (lane == 0) p.tok_of[row] = -1;  // a padding row: zeros
+                if (lane == 0) {  // a padding row: zeros
+                    p.tok_of[row] = -1;
+                    p.yrow[row] = -1;
+                }
                 if (xs == nullptr) continue;
                 for (int v = lane; v < vec; v += 32) xc[row * vec + v] = z;
             }
