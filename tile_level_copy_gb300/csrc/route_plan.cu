@@ -376,11 +376,18 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         s_erank[e] = rk;
     }
     __syncthreads();
+    // hand-out positions and down-projection items of the experts before each one in rank order
+    __shared__ int s_ibase_down[MAX_E], s_nitems;
     for (int e = tid; e < E; e += PLAN_THREADS) {
-        int base = 0;
+        int base = 0, down = 0;
         for (int f = 0; f < E; ++f)
-            if (s_erank[f] < s_erank[e]) base += s_mt[f];
+            if (s_erank[f] < s_erank[e]) {
+                base += s_mt[f];
+                down += (s_load[f] + BM - 1) / BM;
+            }
         s_ebase[e] = base;
+        s_ibase_down[e] = down;
+        if (s_erank[e] == E - 1) s_nitems = down + (s_load[e] + BM - 1) / BM;  // the last expert's end the list
         p.experts[8 * e + 2] = base;        // first hand-out position of the expert's bands
         p.experts[8 * e + 3] = s_erank[e];  // the expert's rank in the hand-out order
     }
@@ -392,13 +399,20 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     // bands by valid rows descending (ties to the lower owner), i.e. key (expert rank, -valid,
     // owner, row). A band's compact rows start after the valid rows of the expert's bands before it
     // in hand-out order: full bands fill whole tiles from the run's start, partial bands follow.
+    // band_item: the down-projection item holding the band's last row, i.e. the item whose tiles
+    // complete the band (its rows lie in this item and possibly the one before it of its expert),
+    // read by the epilogue and the copy engines to tell the bands that the epilogue returns itself
+    // (MOE_DIRECT_TAIL): a band is returned that way when this item is in the direct window, so no
+    // band completed by the last wave is left to the copy engines.
+    auto band_item_of = [&](int e, int crow, int valid) { return s_ibase_down[e] + (crow + valid - 1 - s_cbase[e]) / BM; };
     for (int g = tid; g < G; g += PLAN_THREADS) {
         const int e = g / R, r = g % R, n = s_n[g];
         const int m0 = s_off[g] / tbM;
         const int nt = (n + tbM - 1) / tbM, nfull = n / tbM;
         int fpre = 0;
         for (int q = 0; q < r; ++q) fpre += s_n[e * R + q] / tbM;
-        const int rbase = r * slice + p.ret_off[r * (E + 1) + e];
+        int rbase = r * slice;  // owner r's rows of the experts before e (ret_off, from shared memory)
+        for (int f = 0; f < e; ++f) rbase += s_n[f * R + r];
         for (int i = 0; i < nt; ++i) {
             const int m = m0 + i;
             const int valid = min(tbM, n - i * tbM);
@@ -407,9 +421,11 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             p.tiles[4 * m + 2] = s_off[g] + i * tbM;
             p.tiles[4 * m + 3] = valid;
             p.tile_ret[m] = rbase + i * tbM;
-            if (i < nfull) p.tile_crow[m] = s_cbase[e] + (fpre + i) * tbM;
             if (mirror) s_tg[m] = g;
             if (i < nfull) {
+                const int crow = s_cbase[e] + (fpre + i) * tbM;
+                p.tile_crow[m] = crow;
+                p.band_item[m] = band_item_of(e, crow, valid);
                 p.sched[s_fbp[g] + i] = m;
                 p.order[s_ebase[e] + fpre + i] = m;
                 if (mirror) s_order[s_ebase[e] + fpre + i] = m;
@@ -425,7 +441,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
                 pos += before;
                 rows_before += before ? vh : 0;
             }
-            p.tile_crow[m0 + nfull] = s_cbase[e] + s_fb[e] * tbM + rows_before;
+            const int crow = s_cbase[e] + s_fb[e] * tbM + rows_before;
+            p.tile_crow[m0 + nfull] = crow;
+            p.band_item[m0 + nfull] = band_item_of(e, crow, valid);
             p.order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
             if (mirror) s_order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
             const int key = s_pkey[g];
@@ -460,15 +478,8 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     // the same items with the experts in hand-out order (rank order), so its item list is the SwiGLU
     // list re-ordered by expert. The down-projection's output rows go to the owner-aligned bands of
     // Yp, each band counted complete when all its rows of every N tile have been stored.
-    __shared__ int s_items[MAX_E], s_ibase_down[MAX_E], s_nitems;
-    for (int e = tid; e < E; e += PLAN_THREADS) s_items[e] = (s_load[e] + BM - 1) / BM;
-    __syncthreads();
     for (int e = tid; e < E; e += PLAN_THREADS) {
-        int down = 0;
-        for (int f = 0; f < E; ++f) down += (s_erank[f] < s_erank[e]) ? s_items[f] : 0;
-        s_ibase_down[e] = down;
-        if (s_erank[e] == E - 1) s_nitems = down + s_items[e];  // the last expert's items end the list
-        const int iu = s_items[e];
+        const int down = s_ibase_down[e], iu = (s_load[e] + BM - 1) / BM;
         p.experts[8 * e + 4] = iu;
         p.experts[8 * e + 5] = s_cbase[e] / BM;
         p.experts[8 * e + 6] = down;
@@ -481,18 +492,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
                 p.items_down[2 * (down + i) + 1] = e;
             }
     }
-    __syncthreads();
-
-    // 7b. the down-projection item holding each band's last row, i.e. the item whose tiles complete
-    // the band (a band's rows lie in this item and possibly the one before it of its expert), read by
-    // the epilogue and the copy engines to tell the bands that the epilogue returns itself
-    // (MOE_DIRECT_TAIL): a band is returned that way when this item is in the direct window, so no
-    // band completed by the last wave is left to the copy engines
     const int items = s_nitems;
-    for (int m = tid; m < MT; m += PLAN_THREADS) {
-        const int e = p.tiles[4 * m], valid = p.tiles[4 * m + 3];
-        p.band_item[m] = s_ibase_down[e] + (p.tile_crow[m] + valid - 1 - s_cbase[e]) / BM;
-    }
 
     // 8. per-call meta, flags and trace reset
     if (tid == 0) {
