@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     __shared__ int s_ebase[MAX_E];   // first hand-out position of the expert's bands
     __shared__ int s_cbase[MAX_E];   // first row of the expert in the compact layout
     __shared__ int s_fbp[1024];      // full bands of the groups before g (layout order)
-    __shared__ int s_pkey[1024];     // sort key of group g's partial band in the schedule
+    __shared__ int s_prank[1024];    // rank of group g's partial band among the partial bands
     __shared__ int s_warp[32];
     __shared__ int s_total;
 
@@ -317,19 +317,41 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
 
     // 2b. remote-first schedule, the largest transfers first: bands by valid rows, descending, ties
     // in layout order. The full bands come first, in layout order (position = full bands of the
-    // groups before + index); each group's partial band (valid = n mod tbM) follows, ranked by the
-    // key (tbM - valid, group) among the partial bands.
+    // groups before + index); each group's partial band (valid = n mod tbM) follows, ranked by
+    // (tbM - valid, group) among the partial bands: a counting sort over the buckets tbM - valid,
+    // the groups of one bucket in group order (inside a warp of 32 consecutive groups by a match
+    // mask, across warps by per-warp bucket counts). G <= PLAN_THREADS: thread g holds group g.
+    __shared__ int s_bcnt[PLAN_THREADS / 32][128];  // partial bands per (warp of groups, bucket)
+    __shared__ int s_bbase[128];                    // first rank of each bucket
     int n_full;
     {
         const int g = tid;
         const int fb = (g < G) ? s_n[g] / tbM : 0;
         const int o = block_exclusive_scan(fb, s_warp, &s_total);
-        if (g < G) {
-            s_fbp[g] = o;
-            const int v = s_n[g] % tbM;
-            s_pkey[g] = v ? (tbM - v) * 1024 + g : INT_MAX;
-        }
+        if (g < G) s_fbp[g] = o;
         n_full = s_total;
+    }
+    for (int i = tid; i < (PLAN_THREADS / 32) * 128; i += PLAN_THREADS) s_bcnt[i >> 7][i & 127] = 0;
+    __syncthreads();
+    {
+        const int w = tid >> 5, lane = tid & 31;
+        const int pv = (tid < G) ? s_n[tid] % tbM : 0;
+        const int pb = pv ? tbM - pv : -1;  // bucket 1 .. tbM-1: the largest partial bands first
+        const unsigned same = __match_any_sync(0xffffffffu, pb);
+        const int in_warp = __popc(same & ((1u << lane) - 1u));
+        if (pb >= 0 && in_warp == 0) s_bcnt[w][pb] = __popc(same);
+        __syncthreads();
+        int tot = 0;
+        if (tid < tbM)
+            for (int x = 0; x < PLAN_THREADS / 32; ++x) tot += s_bcnt[x][tid];
+        const int o = block_exclusive_scan(tid < tbM ? tot : 0, s_warp, &s_total);
+        if (tid < tbM) s_bbase[tid] = o;
+        __syncthreads();
+        if (pb >= 0) {
+            int rk = s_bbase[pb] + in_warp;
+            for (int x = 0; x < w; ++x) rk += s_bcnt[x][pb];
+            s_prank[tid] = rk;
+        }
     }
     __syncthreads();
 
@@ -446,10 +468,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             p.band_item[m0 + nfull] = band_item_of(e, crow, valid);
             p.order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
             if (mirror) s_order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
-            const int key = s_pkey[g];
-            int before = 0;  // partial bands earlier in the schedule
-            for (int h = 0; h < G; ++h) before += s_pkey[h] < key;
-            p.sched[n_full + before] = m0 + nfull;
+            p.sched[n_full + s_prank[g]] = m0 + nfull;
         }
     }
     __syncthreads();
@@ -554,10 +573,24 @@ cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
 constexpr int PERM_VEC = 16;  // 16-byte vectors per lane per pass
 
 __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat16* __restrict__ x, PlanPtrs p) {
-    griddep_wait();  // the plan
-    griddep_launch();
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    // The first token's row does not depend on the plan: its loads are issued before the wait for
+    // the plan kernel (MOE_PDL: while it runs), the rest of the work after.
+    const int item0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int vec0 = s.d / 8;
+    uint4 v[PERM_VEC];  // one pass of a row: the first token's first pass is loaded here
+    const bool prefetched = x != nullptr && item0 < s.T;
+    if (prefetched) {
+        const uint4* xs0 = reinterpret_cast<const uint4*>(x) + (size_t)item0 * vec0;
+#pragma unroll
+        for (int i = 0; i < PERM_VEC; ++i) {
+            const int vi = i * 32 + lane;
+            if (vi < vec0) v[i] = __ldg(xs0 + vi);
+        }
+    }
+    griddep_wait();  // the plan
+    griddep_launch();
     const int PC = p.meta[META_PC];
     const int per = s.T / s.R, slice = per * s.k, E = s.E, R = s.R, k = s.k;
     const int vec = s.d / 8;  // 16-byte vectors per row
@@ -567,7 +600,7 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
     const int groups = BM / 8;
     const int pad_items = ok_pc ? E * groups : 0;
 
-    for (int item = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < s.T + pad_items; item += nwarps) {
+    for (int item = item0; item < s.T + pad_items; item += nwarps) {
         if (item < s.T) {
             const int t = item, r = t / per, c = t / s.chunk_tokens;
             int my_cs = 0, my_y = 0;
@@ -598,11 +631,12 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
             }
             if (xs == nullptr) continue;  // plan only: slots without the row copy
             for (int base = 0; base < vec; base += 32 * PERM_VEC) {
-                uint4 v[PERM_VEC];
+                if (!(prefetched && item == item0 && base == 0)) {
 #pragma unroll
-                for (int i = 0; i < PERM_VEC; ++i) {
-                    const int vi = base + i * 32 + lane;
-                    if (vi < vec) v[i] = __ldg(xs + (size_t)t * vec + vi);
+                    for (int i = 0; i < PERM_VEC; ++i) {
+                        const int vi = base + i * 32 + lane;
+                        if (vi < vec) v[i] = __ldg(xs + (size_t)t * vec + vi);
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < KMAX; ++j) {
