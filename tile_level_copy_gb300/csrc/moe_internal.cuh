@@ -361,9 +361,6 @@ __device__ __forceinline__ void host_band_record(const Shape& s, const PlanPtrs&
     __threadfence_system();
     st_release_sys(rec, s.host_epoch);
 }
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
