@@ -758,7 +758,8 @@ def run_ours(args, rank: int, world: int):
         dma_tail = max(0.0, stage_med["copy_engines"]["copy"])
         overlap["copy_engines"] = {
             "call": "moe_forward_dma: no consumer SMs; one cudaMemcpyAsync per ready band (per run of ready bands "
-                    "adjacent in Yp and Ret) issued by the calling thread as the records arrive in pinned host memory",
+                    "adjacent in Yp and Ret) issued by the calling thread as the records arrive in pinned host memory; "
+                    "with the default flags the bands the last wave completes are written by the epilogue (direct tail)",
             "eager_ms_per_step": round(eager_ms["copy_engines"], 4),
             "eager_ms_per_step_sm_consumers": round(eager_ms["overlapped"], 4),
             "down_gemm_ms": round(stage_med["copy_engines"]["down_gemm"], 4),

@@ -335,9 +335,11 @@ MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const f
  *                moe_dma_host_bytes(cfg). Owned by the caller; not to be used by two calls at once.
  *   stage_events as in moe_forward_ex (may be NULL); [MOE_EV_COPIED] is recorded on the library's
  *                copy stream after the last band's copy.
- * The down-projection runs on every SM (consumer_ctas, MOE_TAIL_ASSIST, MOE_COPY_WARPS and
- * MOE_DIRECT_TAIL are ignored); the epilogue warp that completes a band writes a record (its Yp row,
- * Ret row and valid rows, tagged with the call) into host_rec with a system-scope release. The calling
+ * The down-projection runs on every SM (consumer_ctas, MOE_TAIL_ASSIST and MOE_COPY_WARPS are
+ * ignored); the epilogue warp that completes a band writes a record (its Yp row, Ret row and valid
+ * rows, tagged with the call) into host_rec with a system-scope release. With MOE_DIRECT_TAIL the
+ * bands the last wave completes are written into Ret by the epilogue and their records carry 0 rows
+ * (nothing to copy). The calling
  * thread polls the records and issues one cudaMemcpyAsync per ready band (one per run of ready bands
  * that are adjacent in both Yp and Ret), device to device, on a copy stream of the library's own,
  * which starts after the work enqueued on `stream` before this call; `stream` waits for that copy

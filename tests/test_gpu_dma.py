@@ -42,6 +42,39 @@ def test_dma_copy_equals_sequential(name, flags):
         assert torch.equal(L.ws.view("Ret"), ret_seq)
 
 
+@pytest.mark.parametrize("window", [0, 20, 1 << 20])
+@pytest.mark.parametrize("flags", [PAIR, 0], ids=["pairs", "single"])
+def test_dma_copy_with_direct_tail(flags, window):
+    """MOE_DIRECT_TAIL on the copy-engine path: the bands the window's items complete are written into
+    Ret by the epilogue and their records carry 0 rows (no copy issued); out and Ret stay equal to the
+    GEMM-then-copy path, and those bands' Yp rows (zeroed first) stay untouched."""
+    w = small("skew")
+    L = Layer(w, seed=5, cfg_kw=dict(consumer_ctas=4, flags=flags))
+    want = L.run(sequential=True)
+    ret_seq = L.ws.view("Ret").clone()
+    cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=flags | tlc.MOE_DIRECT_TAIL, tail_window=window)
+    rec = host_rec_for(cfg)
+    L.ws.view("Ret").zero_()
+    L.ws.view("Yp").zero_()
+    tlc.forward_dma(cfg, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws, rec)
+    assert tlc.status(cfg, L.ws)[0] == tlc.MOE_OK
+    assert torch.equal(L.out, want)
+    assert torch.equal(L.ws.view("Ret"), ret_seq)
+    MT = int(L.ws.view("meta")[1].item())
+    valid = rec[4:4 + 4 * MT].view(MT, 4)[:, 2].tolist()
+    tiles = L.ws.view("tiles").cpu().numpy()[:MT]
+    Yp = L.ws.view("Yp").view(torch.int16).cpu().numpy()
+    zero_rows = [m for m in range(MT) if valid[m] == 0]
+    for m in range(MT):  # a record says 0 rows exactly for the bands left out of Yp
+        row0, v = int(tiles[m, 2]), int(tiles[m, 3])
+        assert (valid[m] == 0) == (not Yp[row0:row0 + v].any()), m
+        assert valid[m] in (0, v)
+    if window == 20:
+        assert 0 < len(zero_rows) < MT
+    else:  # a huge window, or one wave: the small layer has fewer tiles than that
+        assert len(zero_rows) == MT
+
+
 def test_dma_copy_calls_in_a_row_with_new_inputs_and_events():
     """Three calls with different routing on one workspace and one record buffer; each output equals
     the sequential path's of its own inputs; the copy-done event follows the down-projection's."""

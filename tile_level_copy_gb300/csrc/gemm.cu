@@ -292,12 +292,13 @@ __device__ __forceinline__ void publish_rows(const Shape& s, const PlanPtrs& p, 
         const int l = __ffs(leaders) - 1;
         const int m = __shfl_sync(0xffffffffu, dr.band, l);
         const uint32_t cnt = (uint32_t)__popc(__shfl_sync(0xffffffffu, same, l));
+        const bool direct = __shfl_sync(0xffffffffu, dr.direct ? 1 : 0, l) != 0;  // a property of the band
         if (lane == 0) {
             red_release_gpu_add(p.flags + (size_t)m * nN + n, cnt);
             const uint32_t before = atom_acq_rel_gpu_add(p.bands + m, cnt);
             if (before + cnt == (uint32_t)p.tiles[4 * m + 3] * nN) {
                 atomicMax(&p.trace[MOE_TRACE_BAND_DONE], globaltimer());
-                if (p.host_rec) host_band_record(s, p, m);  // the band's last rows
+                if (p.host_rec) host_band_record(s, p, m, direct);  // the band's last rows
             }
         }
     }

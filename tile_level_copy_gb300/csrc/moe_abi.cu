@@ -810,7 +810,7 @@ static int run_forward_dma(Call& c, const float* logits, const uint16_t* x, cons
     uint32_t epoch = ++g_epoch;
     if (epoch == 0) epoch = ++g_epoch;
     Shape& S = c.lay.S;
-    S.flags &= ~(uint32_t)(MOE_TAIL_ASSIST | MOE_COPY_WARPS | MOE_DIRECT_TAIL | MOE_TEST_STALL_CONSUMER);
+    S.flags &= ~(uint32_t)(MOE_TAIL_ASSIST | MOE_COPY_WARPS | MOE_TEST_STALL_CONSUMER);
     S.host_epoch = epoch;
     c.p.host_rec = static_cast<uint32_t*>(dev_rec);
     const bool pair_down = (S.flags & MOE_PAIR_UMMA) && S.bn2 == 2 * BN1;
@@ -879,9 +879,15 @@ static int run_forward_dma(Call& c, const float* logits, const uint16_t* x, cons
             std::atomic_thread_fence(std::memory_order_acquire);
             const uint32_t ret0 = h[4 + 4 * (size_t)m + 1], valid = h[4 + 4 * (size_t)m + 2],
                            row0 = h[4 + 4 * (size_t)m + 3];
-            if (valid < 1 || valid > (uint32_t)S.tbM || (size_t)ret0 + valid > (size_t)S.T * S.k ||
+            if (valid > (uint32_t)S.tbM || (size_t)ret0 + valid > (size_t)S.T * S.k ||
                 (size_t)row0 + valid > (size_t)S.P_max)
                 return fail(MOE_ERR_PLAN, "band %d record out of range", m);
+            if (valid == 0) {  // returned by the down-projection's epilogue (MOE_DIRECT_TAIL)
+                if ((rc = flush())) return rc;
+                done[m] = 1;
+                ++issued;
+                continue;
+            }
             if (run_rows && (ret0 != run_ret + run_rows || row0 != run_row + run_rows) && (rc = flush())) return rc;
             if (run_rows == 0) {
                 run_ret = ret0;

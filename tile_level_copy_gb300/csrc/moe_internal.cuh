@@ -349,14 +349,15 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ void st_release_sys(uint32_t* p, uint32_t v) {
     asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-// moe_forward_dma: tell the host that band m is complete: its Yp row, Ret row and valid rows, then
-// the call's tag, released at system scope after a system-scope fence (the band's rows were made
-// visible at GPU scope by every warp that stored them, and this warp's counter update came last).
-__device__ __forceinline__ void host_band_record(const Shape& s, const PlanPtrs& p, int m) {
+// moe_forward_dma: tell the host that band m is complete: its Yp row, Ret row and valid rows (0 for a
+// band the epilogue wrote into Ret itself, MOE_DIRECT_TAIL: nothing to copy), then the call's tag,
+// released at system scope after a system-scope fence (the band's rows were made visible at GPU
+// scope by every warp that stored them, and this warp's counter update came last).
+__device__ __forceinline__ void host_band_record(const Shape& s, const PlanPtrs& p, int m, bool direct) {
     uint32_t* rec = p.host_rec + 4 + 4 * (size_t)m;
     __threadfence_system();
     rec[1] = (uint32_t)p.tile_ret[m];
-    rec[2] = (uint32_t)p.tiles[4 * m + 3];
+    rec[2] = direct ? 0u : (uint32_t)p.tiles[4 * m + 3];
     rec[3] = (uint32_t)p.tiles[4 * m + 2];
     __threadfence_system();
     st_release_sys(rec, s.host_epoch);
