@@ -318,16 +318,18 @@ class ClockSampler:
 # ---------------------------------------------------------------------------------- our arm
 def default_flags(copy_warps: bool, direct_tail: bool = True, tail_assist: bool = True, pair: bool = True,
                   fused_dispatch: bool = False, fused_gemms: bool = False, pdl=None) -> int:
-    """The bench's launch configuration: both expert GEMMs on CTA pairs, finished producers joining
-    the copy, the last wave's bands returned by the down-projection's epilogue, and (per workload)
-    the producers' copy warps; programmatic dependent launch between the kernels unless the copy
+    """The bench's launch configuration: both expert GEMMs on CTA pairs (the down-projection's consumer
+    partition picked at run time from its tile count), finished producers joining the copy, the last
+    wave's bands returned by the down-projection's epilogue, and (per workload) the producers' copy
+    warps; programmatic dependent launch between the kernels unless the copy
     warps run (their down-projection is the cooperative single-CTA kernel, with which it measured
     slower)."""
     import tile_level_copy_gb300 as tlc
     if pdl is None:
         pdl = not copy_warps
     return ((tlc.MOE_TAIL_ASSIST if tail_assist else 0) | (tlc.MOE_COPY_WARPS if copy_warps else 0) |
-            (tlc.MOE_PAIR_UMMA if pair else 0) | (tlc.MOE_DIRECT_TAIL if direct_tail else 0) |
+            (tlc.MOE_PAIR_UMMA | tlc.MOE_ADAPTIVE_CONSUMERS if pair else 0) |
+            (tlc.MOE_DIRECT_TAIL if direct_tail else 0) |
             (tlc.MOE_FUSED_DISPATCH if fused_dispatch else 0) | (tlc.MOE_FUSED_GEMMS if fused_gemms else 0) |
             (tlc.MOE_PDL if pdl else 0))
 
@@ -518,6 +520,9 @@ def run_ours(args, rank: int, world: int):
     value, sec_max = aggregate(sec_ovl, w.T * K, world)
     hl_st = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(tlc.EV_COUNT - 1)] for e in hl_ev if e])
     hl_med = {n: float(np.median(hl_st[:, i])) for i, n in enumerate(STAGES)}
+    # the CTA-pair down-projection's producer CTAs in the timed steps (MOE_ADAPTIVE_CONSUMERS picks
+    # them from the tile count; 0 when no overlapped pair launch ran)
+    producer_ctas = int(lb.ws.view("meta")[10].item())
 
     # eager launches of the same K steps, contiguous, beside the headline
     for _ in range(Wm):
@@ -549,9 +554,10 @@ def run_ours(args, rank: int, world: int):
     fused_gemms = bool(cfg.flags & tlc.MOE_FUSED_GEMMS)
     other_gemms = "overlapped_separate_gemms" if fused_gemms else "overlapped_fused_gemms"
     arms[other_gemms] = (dataclasses.replace(cfg, flags=cfg.flags ^ tlc.MOE_FUSED_GEMMS), False)
-    # another consumer partition, when asked for (same flags otherwise)
+    # another (fixed) consumer partition, when asked for (same flags otherwise)
     for c_alt in args.alt_consumers:
-        arms[f"overlapped_c{c_alt}"] = (dataclasses.replace(cfg, consumer_ctas=c_alt), False)
+        arms[f"overlapped_c{c_alt}"] = (dataclasses.replace(cfg, consumer_ctas=c_alt,
+                                                            flags=cfg.flags & ~tlc.MOE_ADAPTIVE_CONSUMERS), False)
     # programmatic dependent launch between the kernels against serial launches
     pdl = bool(cfg.flags & tlc.MOE_PDL)
     other_pdl = "overlapped_serial_launches" if pdl else "overlapped_pdl"
@@ -600,8 +606,8 @@ def run_ours(args, rank: int, world: int):
     # the page's own copy design beside it: a dedicated consumer partition of 8 CTAs (no copy warps,
     # no direct tail), same GEMMs; its hidden fraction (trace stamps) and eager step time
     cfg_page = dataclasses.replace(cfg, consumer_ctas=8,
-                                   flags=(cfg.flags & ~(tlc.MOE_COPY_WARPS | tlc.MOE_DIRECT_TAIL)) |
-                                   tlc.MOE_TAIL_ASSIST)
+                                   flags=(cfg.flags & ~(tlc.MOE_COPY_WARPS | tlc.MOE_DIRECT_TAIL |
+                                                        tlc.MOE_ADAPTIVE_CONSUMERS)) | tlc.MOE_TAIL_ASSIST)
     page_tails, _ = lb.tails(cfg_page, 5)
     page_ev = [tlc.stage_events() for _ in range(5)]
     for i in range(5):
@@ -789,7 +795,9 @@ def run_ours(args, rank: int, world: int):
         "ms_per_step": round(sec_max * 1e3 / K, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(w), "T": w.T, "d": w.d, "ffn": w.ffn, "E": w.E, "topk": w.topk,
-                   "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers, "copy_warps": bool(args.copy_warps),
+                   "R": w.R, "tile_M": w.tile_M, "consumer_ctas": args.consumers,
+                   "adaptive_consumers": bool(flags & tlc.MOE_ADAPTIVE_CONSUMERS),
+                   "down_producer_ctas": producer_ctas or None, "copy_warps": bool(args.copy_warps),
                    "pair_umma": bool(args.pair_umma), "mgb": args.mgb, "direct_tail": direct,
                    "tail_window": args.tail_window, "fused_dispatch": bool(args.fused_dispatch),
                    "fused_gemms": bool(args.fused_gemms), "pdl": bool(flags & tlc.MOE_PDL),

@@ -94,6 +94,12 @@ extern "C" {
 #define MOE_TEST_PLAN_FAIL 0x200u     /* test hook: the plan kernel reports a failed bounds   */
                                       /* check (MOE_ERR_PLAN, detail -3) although the plan is */
                                       /* valid, to test that the status reaches the caller    */
+#define MOE_ADAPTIVE_CONSUMERS 0x1000u /* the CTA-pair down-projection picks its consumer      */
+                                      /* partition at run time from its tile count: the       */
+                                      /* fewest producer pairs that finish the tiles in the    */
+                                      /* fewest waves any partition with one or more consumer */
+                                      /* pairs allows; every other pair copies (consumer_ctas */
+                                      /* then only sizes the launch's default)                */
 #define MOE_TEST_STALL_PIPE0 0x400u   /* test hooks: in the CTA-pair GEMMs the TMA thread of   */
 #define MOE_TEST_STALL_PIPE1 0x800u   /* rank 0 (PIPE0) or rank 1 (PIPE1) of every pair stops  */
                                       /* issuing loads halfway through its first tile, so the */
@@ -335,8 +341,8 @@ MOE_API int moe_forward_host_pipelined(const moe_config* cfg, int steps, const f
  *                moe_dma_host_bytes(cfg). Owned by the caller; not to be used by two calls at once.
  *   stage_events as in moe_forward_ex (may be NULL); [MOE_EV_COPIED] is recorded on the library's
  *                copy stream after the last band's copy.
- * The down-projection runs on every SM (consumer_ctas, MOE_TAIL_ASSIST and MOE_COPY_WARPS are
- * ignored); the epilogue warp that completes a band writes a record (its Yp row, Ret row and valid
+ * The down-projection runs on every SM (consumer_ctas, MOE_TAIL_ASSIST, MOE_COPY_WARPS and
+ * MOE_ADAPTIVE_CONSUMERS are ignored); the epilogue warp that completes a band writes a record (its Yp row, Ret row and valid
  * rows, tagged with the call) into host_rec with a system-scope release. With MOE_DIRECT_TAIL the
  * bands the last wave completes are written into Ret by the epilogue and their records carry 0 rows
  * (nothing to copy). The calling

@@ -69,6 +69,33 @@ def test_pair_with_overlapped_down_projection(flags):
     assert torch.equal(L.run(sequential=False, cfg=cfg), want)
 
 
+@pytest.mark.parametrize("name,consumers", [("mixtral", 4), ("mixtral", 24), ("skew", 8), ("mixtral", 2)])
+@pytest.mark.parametrize("direct", [False, True])
+def test_adaptive_consumer_partition(name, consumers, direct):
+    """MOE_ADAPTIVE_CONSUMERS: the pair down-projection sets its producer pairs from its tile count
+    (the fewest that finish in the fewest waves a partition with a consumer pair allows), whatever
+    consumer_ctas says; the result stays bitwise equal to the GEMM-then-copy path and every band
+    completes."""
+    w = small(name)
+    L = Layer(w, seed=3)
+    want = L.run(sequential=True)
+    ret_seq = L.ws.view("Ret").clone()
+    flags = PAIR | tlc.MOE_TAIL_ASSIST | tlc.MOE_ADAPTIVE_CONSUMERS | (tlc.MOE_DIRECT_TAIL if direct else 0)
+    cfg = tlc.Config.from_workload(w, consumer_ctas=consumers, flags=flags)
+    L.ws.view("Ret").zero_()
+    assert torch.equal(L.run(sequential=False, cfg=cfg), want)
+    assert torch.equal(L.ws.view("Ret"), ret_seq)
+    idx, _ = moe_ref.route_topk(L.logits_np, w.topk)
+    check_flag_counts(L, moe_ref.build_plan(idx, w.E, w.R, w.tile_M, cfg.mgb))
+    # the producer count the kernel chose, against the rule on the plan's item counts (the pair
+    # grid is one cluster of two per two SMs)
+    items = L.ws.view("experts").cpu().numpy()[:, 4]
+    tiles = int(np.sum((items + 1) // 2)) * L.ws.layout["n_tiles_n2"]
+    pairs = tlc.device_info()[0] // 2
+    w_min = -(-tiles // (pairs - 1))
+    assert int(L.ws.view("meta")[10].item()) == 2 * (-(-tiles // w_min))
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mixtral", "skew", "fine"])
 def test_pair_full_size_sampled_tokens(name):

@@ -725,6 +725,7 @@ struct PairSmem {
     volatile uint32_t* peer_k;  // rank 0: k-blocks rank 1's TMA thread issued (abort path)
     volatile int* abort;
     volatile int* tq;
+    volatile int* nprod;  // producer CTAs of this launch (the launch's, or MOE_ADAPTIVE_CONSUMERS')
     int* tab;  // [cum (E+1) | first item (E) | items (E) | first direct item]
 };
 
@@ -748,7 +749,8 @@ __device__ __forceinline__ PairSmem carve_pair(uint8_t* raw) {
     sm.peer_k = sm.peer_base + 1;
     sm.abort = reinterpret_cast<volatile int*>(const_cast<uint32_t*>(sm.peer_k) + 1);
     sm.tq = sm.abort + 1;
-    sm.tab = const_cast<int*>(sm.tq + PAIR_TILE_Q);
+    sm.nprod = sm.tq + PAIR_TILE_Q;
+    sm.tab = const_cast<int*>(sm.nprod + 1);
     return sm;
 }
 static_assert(COPY_NBUF * COPY_PIECE <= PAIR_STAGES * PAIR_STAGE_BYTES, "copy staging must fit the pair stage area");
@@ -867,8 +869,6 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
     const PairSmem sm = carve_pair(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
-    const bool producer = (int)blockIdx.x < num_producers;  // even: both CTAs of a cluster share the role
-    const bool gemm_cta = producer || FUSED;                 // fused: consumer clusters take SwiGLU tiles
     const int E = s.E;
     int MT = HAS_DN ? p.meta[META_MTILES] : 0;
     int NU = HAS_UP ? p.meta[META_ITEMS_UP] : 0;
@@ -945,6 +945,20 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
             acc += ((count[r] + 1) >> 1) * nN_dn;
         }
         sm.tab[E] = acc;
+        // MOE_ADAPTIVE_CONSUMERS: the tiles are of one size and handed out as pairs become free, so
+        // the down-projection takes ceil(tiles / producer pairs) waves. The fewest waves any
+        // partition with at least one consumer pair allows is w = ceil(tiles / (pairs - 1)); the
+        // fewest producer pairs that still finish in w waves is ceil(tiles / w), and every other
+        // pair copies. (With the launch's fixed partition one pair too few costs a whole extra
+        // wave of tiles when the tile count lies just above a multiple of the producer pairs.)
+        int prod = num_producers;
+        const int pairs = (int)gridDim.x / 2;
+        if (overlapped && (s.flags & MOE_ADAPTIVE_CONSUMERS) && acc > 0 && pairs >= 2) {
+            const int w = (acc + pairs - 2) / (pairs - 1);
+            prod = 2 * ((acc + w - 1) / w);
+        }
+        *sm.nprod = prod;
+        if (blockIdx.x == 0 && overlapped) p.meta[META_PRODUCERS] = prod;
         // MOE_DIRECT_TAIL: the first item of the first pair item with a tile among the last `window`
         // hand-out positions, i.e. whose last tile is (the pair items' last tiles rise with the item
         // index, so every later item has one there too): those items may complete bands in the last
@@ -954,7 +968,7 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
         // rel - (nN - 1) np (N tile by N tile: pair item p's last tile is at (nN - 1) np + p)
         int from = INT_MAX;
         if (overlapped && (s.flags & MOE_DIRECT_TAIL) && ND > 0 && acc > 0) {
-            const int window = s.tail_window > 0 ? s.tail_window : num_producers / 2, thr = acc - window;
+            const int window = s.tail_window > 0 ? s.tail_window : prod / 2, thr = acc - window;
             from = ND;
             for (int r = 0; r < E; ++r) {
                 const int np = (count[r] + 1) >> 1;
@@ -988,6 +1002,11 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
             tab_up[E] = uacc;
         }
     }
+    if (MODE == 1 && tid == 0) *sm.nprod = num_producers;
+    __syncthreads();
+    const int num_prod = *sm.nprod;
+    const bool producer = (int)blockIdx.x < num_prod;  // even: both CTAs of a cluster share the role
+    const bool gemm_cta = producer || FUSED;            // fused: consumer clusters take SwiGLU tiles
     if (gemm_cta && warp == 1) {
         __syncwarp();
         tmem_alloc_pair(sm.tmem_base, TMEM_COLS);

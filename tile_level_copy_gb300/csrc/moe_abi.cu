@@ -810,7 +810,7 @@ static int run_forward_dma(Call& c, const float* logits, const uint16_t* x, cons
     uint32_t epoch = ++g_epoch;
     if (epoch == 0) epoch = ++g_epoch;
     Shape& S = c.lay.S;
-    S.flags &= ~(uint32_t)(MOE_TAIL_ASSIST | MOE_COPY_WARPS | MOE_TEST_STALL_CONSUMER);
+    S.flags &= ~(uint32_t)(MOE_TAIL_ASSIST | MOE_COPY_WARPS | MOE_ADAPTIVE_CONSUMERS | MOE_TEST_STALL_CONSUMER);
     S.host_epoch = epoch;
     c.p.host_rec = static_cast<uint32_t*>(dev_rec);
     const bool pair_down = (S.flags & MOE_PAIR_UMMA) && S.bn2 == 2 * BN1;

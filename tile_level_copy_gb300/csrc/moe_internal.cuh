@@ -26,6 +26,7 @@ enum Meta : int {
     META_ITEMS = 7,        // down-projection work items (128 compact rows of one expert)
     META_ITEMS_UP = 8,     // SwiGLU work items (128 rows of one expert in the compact layout)
     META_PC = 9,           // rows of the compact layout used by this call
+    META_PRODUCERS = 10,   // producer CTAs of the last overlapped CTA-pair down-projection
     META_DISPATCH = 24,    // next block of compact rows to copy (MOE_FUSED_DISPATCH)
     META_TILES_UP = 32,    // next SwiGLU GEMM tile to hand out (single-CTA kernel), minus the grid
     META_TILES_DOWN = 48,  // next down-projection tile to hand out, minus the producer count
