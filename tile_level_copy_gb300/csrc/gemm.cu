@@ -704,10 +704,16 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
 // It publishes each index in a ring of PAIR_TILE_Q slots of both CTAs: its own slot with a store and
 // an arrive on tq_full, the peer's with st.async, which completes 4 transaction bytes on the peer's
 // tq_full (armed by the peer's TMA thread, once at start and again each time it has read the slot).
-// Rank 0's tq_empty (count 9) collects rank 0's UMMA issuer and the epilogue warps of both CTAs.
-// Rank 1's TMA thread needs no arrive there: rank 0's TMA thread cannot run more than PAIR_STAGES
-// k-blocks ahead of it (every stage's barrier waits for rank 1's loads), so when rank 0 reuses a
-// slot PAIR_TILE_Q tiles later, rank 1 has long since read it.
+// Rank 0's tq_empty (count 5) collects rank 0's UMMA issuer and epilogue warps. Rank 1's readers
+// need no arrive there. Its TMA thread: rank 0's TMA thread cannot run more than PAIR_STAGES k-blocks
+// ahead of it (every stage's barrier waits for rank 1's loads), so when rank 0 reuses a slot
+// PAIR_TILE_Q tiles later, rank 1 has long since read it. Its epilogue warps: rank 0's TMA thread
+// writes the slot of its tile j + 8 only after issuing every k-block of tile j + 7, which needs the
+// stages freed by the UMMAs of a k-block of tile j + 8 - ceil(7 / KB) or later, whose tile began only
+// after both CTAs' epilogues released the accumulator of tile j + 6 - ceil(7 / KB) >= j + 2 (KB >= 2
+// k-blocks per tile: d, ffn >= 128); the epilogue takes its tiles in order, so it read slot j before.
+// (A cluster-scope arrive waits for the SM's outstanding memory operations: four of them per tile
+// held rank 1's epilogue up on short tiles.)
 // =============================================================================================
 struct PairSmem {
     uint8_t* stages;
@@ -900,7 +906,7 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
         mbar_init(sm.drain, 1);
         for (int i = 0; i < PAIR_TILE_Q; ++i) {
             mbar_init(&sm.tq_full[i], 1);
-            mbar_init(&sm.tq_empty[i], 1 + 4 + 4);
+            mbar_init(&sm.tq_empty[i], 1 + 4);
         }
         for (int i = 0; i < COPY_NBUF; ++i) mbar_init(&sm.cbar[i], 1);
         *sm.abort = bad_item ? 1 : 0;  // a corrupt plan also stops the copy engines
@@ -1243,17 +1249,13 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
             if (HAS_UP && dispatch) dispatch_rows(s, p);
             EpiStage es{sm.epi + (warp - 2) * 2 * EPI_CHUNK_BYTES, 0};
             const uint32_t acc_empty0 = mapa_shared(smem_u32(sm.acc_empty), 0u);
-            const uint32_t tq_empty0 = mapa_shared(smem_u32(sm.tq_empty), 0u);
             int b = 0;
             uint32_t aph = 0;
             for (int j = 0; !bad; ++j) {
                 int t = 0;
                 if (lane == 0) {
                     t = pair_tile_wait(sm, j, tmo);
-                    if (t != TILE_ABORT) {
-                        if (rank == 0) mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
-                        else mbar_arrive_cluster(tq_empty0 + 8u * (uint32_t)(j % PAIR_TILE_Q));
-                    }
+                    if (t != TILE_ABORT && rank == 0) mbar_arrive(&sm.tq_empty[j % PAIR_TILE_Q]);
                 }
                 t = __shfl_sync(0xffffffffu, t, 0);
                 if (t == TILE_ABORT) {
