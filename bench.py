@@ -40,8 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu capture of one launch on the Mixtral-shaped layer, per (workload, CTA-pair kernel), with the
 # SHA-256 of the kernel sources it was taken on: the bench reports it only while those sources are
 # unchanged and the launch configuration is the captured one.
-SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 1954899968 + 246500608,
-                                      "sources_sha256": "f5c0dc3abb91a82ffb3e7cc541629e2fbd229edd17369017759cffe1799ade2c"}}
+SWIGLU_TRAFFIC = {("mixtral", True): {"bytes": 1953533696 + 246302720,
+                                      "sources_sha256": "b67541f713897f157dfab8ff0900d4f534c1e668613b838c4b48ff8e0a14ffac"}}
 KERNEL_SOURCES = ("tile_level_copy_gb300/csrc/gemm.cu", "tile_level_copy_gb300/csrc/moe_internal.cuh",
                   "tile_level_copy_gb300/csrc/copy_ring.cuh")
 
@@ -315,6 +315,20 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.samples), "source": self.source}
 
 
+def zero_kernel_clocks(ws):
+    """Zero the workspace's SM clock counters (the GEMM launches add to them)."""
+    ws.view("trace")[8:12].zero_()
+
+
+def kernel_clocks(ws) -> dict:
+    """Mean SM clock (MHz) of the expert-GEMM launches since the counters were zeroed: CTA 0 of each
+    launch adds its SM's cycle count and the global-timer nanoseconds of the same span."""
+    v = ws.view("trace")[8:12].cpu().numpy().astype(np.int64)
+    mhz = lambda c, n: round(1000.0 * float(c) / float(n), 1) if n > 0 else None  # noqa: E731
+    return {"swiglu_gemm": mhz(v[0], v[1]), "down_projection": mhz(v[2], v[3]),
+            "source": "SM cycle counter over the global timer, CTA 0 of each GEMM launch in the region"}
+
+
 # ---------------------------------------------------------------------------------- our arm
 def default_flags(copy_warps: bool, direct_tail: bool = True, tail_assist: bool = True, pair: bool = True,
                   fused_dispatch: bool = False, fused_gemms: bool = False, pdl=None) -> int:
@@ -445,6 +459,7 @@ def alternate_graphs(lb: LayerBench, arms, K: int, Wm: int, dev_index: int):
             g.replay()
     ev = {a: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
           for a in arms}
+    zero_kernel_clocks(lb.ws)
     torch.cuda.synchronize()
     with ClockSampler(dev_index) as clk:
         for i in range(K):
@@ -455,7 +470,9 @@ def alternate_graphs(lb: LayerBench, arms, K: int, Wm: int, dev_index: int):
         torch.cuda.synchronize()
     for a, (cfg, _) in arms.items():
         lb.check(cfg, f"in the alternating graph replays ({a})")
-    return {a: np.array([e0.elapsed_time(e1) for e0, e1 in ev[a]]) for a in arms}, clk.summary()
+    summary = clk.summary()
+    summary["kernel_sm_mhz"] = kernel_clocks(lb.ws)
+    return {a: np.array([e0.elapsed_time(e1) for e0, e1 in ev[a]]) for a in arms}, summary
 
 
 def spread_ms(x) -> float:
@@ -505,6 +522,7 @@ def run_ours(args, rank: int, world: int):
             lb.step(cfg, False)
         lb.check(cfg, "in the warm-up")
         run_k = lambda: [lb.step(cfg, False, hl_ev[i]) for i in range(K)]  # noqa: E731
+    zero_kernel_clocks(lb.ws)
     barrier(world)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -517,6 +535,8 @@ def run_ours(args, rank: int, world: int):
     lb.check(cfg, "in the timed region")
     sec_ovl = t0.elapsed_time(t1) / 1e3
     clocks = clk.summary()
+    # NVML averages over a longer window than this region: the kernels' own clock beside it
+    clocks["kernel_sm_mhz"] = kernel_clocks(lb.ws)
     value, sec_max = aggregate(sec_ovl, w.T * K, world)
     hl_st = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(tlc.EV_COUNT - 1)] for e in hl_ev if e])
     hl_med = {n: float(np.median(hl_st[:, i])) for i, n in enumerate(STAGES)}
@@ -674,6 +694,14 @@ def run_ours(args, rank: int, world: int):
                 "algorithmic_flops_per_launch": fl_up_alg, "launch_ms": round(up_ms, 4),
                 "launch_ms_source": f"median of {len(sampled)} of the {K} launches inside the timed region (steps "
                                     f"{', '.join(str(i) for i in sampled)} record stage events)"}
+    # the same launches against the tensor pipe's own peak at the clock they ran at (8192 dense bf16
+    # FLOP per SM per clock)
+    up_mhz = clocks["kernel_sm_mhz"]["swiglu_gemm"]
+    if up_mhz:
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        roofline["kernel_sm_mhz"] = up_mhz
+        roofline["executed_frac_of_tensor_peak_at_kernel_clock"] = round(
+            fl_up_exe / (up_ms * 1e-3) / (n_sm * 8192 * up_mhz * 1e6), 4)
 
     # HBM-bound stages against the measured copy bandwidth (algorithmic bytes / stage time)
     hbm = peaks["hbm_gbs"]
@@ -896,6 +924,7 @@ def other_workload(name: str, args, peaks) -> dict:
     g1, gk = lb.graph(cfg, False), lb.graph_steps(cfg, ev)
     for _ in range(Wm):
         g1.replay()
+    zero_kernel_clocks(lb.ws)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
@@ -904,6 +933,7 @@ def other_workload(name: str, args, peaks) -> dict:
         t1.record()
         torch.cuda.synchronize()
     lb.check(cfg, f"in the {name} replays")
+    kclk = kernel_clocks(lb.ws)
     ms = t0.elapsed_time(t1) / K
     up_ms = float(np.median([e[tlc.EV_PLANNED].elapsed_time(e[tlc.EV_UP]) for e in ev if e]))
     arms = {"overlapped": (cfg, False), "sequential": (cfg, True),
@@ -922,7 +952,7 @@ def other_workload(name: str, args, peaks) -> dict:
             "swiglu_gemm": {"ms": round(up_ms, 4), "achieved_tflops": round(up_tflops, 1),
                             "frac_of_measured_burst_peak": round(up_tflops / peaks["bf16_tflops"], 4)},
             "eager_ms_per_step": {a: round(float(np.median(v.sum(1))), 4) for a, v in st.items()},
-            "clocks": clk.summary()}
+            "clocks": dict(clk.summary(), kernel_sm_mhz=kclk)}
 
 
 # ------------------------------------------------------------------------ CPU oracle timing

@@ -188,7 +188,8 @@ typedef struct moe_layout {
                        /*                   valid rows)                                       */
     size_t bands;      /* uint32 [MT_max]   rows of each band stored over all its N tiles      */
                        /*                   (ready at valid rows x n_tiles_n2)                */
-    size_t trace;      /* uint64 [16]       %globaltimer stamps of the last call (ns)          */
+    size_t trace;      /* uint64 [16]       %globaltimer stamps of the last call (ns), [0, 8);  */
+                       /*                   SM clock counters, [8, 12), zeroed by the caller  */
     size_t Xc;         /* bf16 [PC_max, d]  permuted tokens, expert-compact, zero padding rows */
     size_t Hc;         /* bf16 [PC_max, ffn] SwiGLU hidden, same rows                          */
     size_t Yp;         /* bf16 [P_max, d]   expert outputs                                     */
@@ -207,6 +208,15 @@ typedef struct moe_layout {
 #define MOE_TRACE_LAST_ACQUIRE 5 /* overlapped: latest time a copy engine acquired a band      */
 #define MOE_TRACE_LAST_LOAD 6    /* latest issue of a bulk load by a copy engine               */
 #define MOE_TRACE_LAST_DRAIN 7   /* latest start of a copy engine's final drain                */
+
+/* Clock counters (uint64), summed over calls until the caller zeroes them (moe_plan leaves them):
+ * CTA 0 of each expert-GEMM launch adds the cycles of its SM's clock (%clock64) and the %globaltimer
+ * nanoseconds of one span, from the end of its wait for the previous kernel to the end of its tiles.
+ * 1000 * cycles / ns is the mean SM clock in MHz over those launches. */
+#define MOE_TRACE_UP_CYCLES 8    /* SwiGLU GEMM (both GEMMs in MOE_FUSED_GEMMS)                */
+#define MOE_TRACE_UP_NS 9
+#define MOE_TRACE_DOWN_CYCLES 10 /* down-projection                                          */
+#define MOE_TRACE_DOWN_NS 11
 
 /* Size in bytes of the workspace for `cfg` (host-only arithmetic, no CUDA call).
  * Returns MOE_ERR_ARG for an invalid config. */

@@ -40,6 +40,7 @@ MOE_TEST_STALL_PIPE1 = 0x800
 
 TRACE_GEMM2_START, TRACE_GEMM2_END, TRACE_COPY_START, TRACE_COPY_END = 0, 1, 2, 3
 TRACE_BAND_DONE, TRACE_LAST_ACQUIRE, TRACE_LAST_LOAD, TRACE_LAST_DRAIN = 4, 5, 6, 7
+TRACE_UP_CYCLES, TRACE_UP_NS, TRACE_DOWN_CYCLES, TRACE_DOWN_NS = 8, 9, 10, 11
 
 # names of the C entry points (each declared in include/moe.h)
 EXPORTS = ("moe_workspace_size", "moe_workspace_layout", "moe_plan", "moe_forward", "moe_forward_sequential",

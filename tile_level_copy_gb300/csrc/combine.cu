@@ -13,6 +13,7 @@ namespace moe {
 template <int K>  // K = top-k, so that the per-lane arrays have exactly K entries
 __global__ void __launch_bounds__(256, 4) combine_kernel(Shape s, PlanPtrs p, float* __restrict__ out) {
     griddep_wait();  // the return copy (and every row of Ret) is complete
+    griddep_launch();  // MOE_PDL: the next layer's routing kernel may start; it waits for this grid
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int vec = s.d / 8;

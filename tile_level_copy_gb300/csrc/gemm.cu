@@ -482,6 +482,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     tc_fence_after();
     griddep_wait();  // MOE_PDL: the previous kernel's outputs (the plan tables above were complete before)
     griddep_launch();
+    const ClockSpan clk = clock_span_start(blockIdx.x == 0 && tid == 0);
     const uint32_t tmem = producer ? *sm.tmem_base : 0u;
     unsigned long long last_end = 0;
     const uint32_t stall = (s.flags & MOE_TEST_STALL_CONSUMER) ? 1u : 0u;  // a count no band reaches
@@ -669,6 +670,7 @@ __global__ void __launch_bounds__(GEMM_THREADS_MAX, 1)
     }
     if (MODE == 2 && producer && warp >= 2 && lane == 0 && last_end)
         atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
+    clock_span_add(p, clk, MODE == 2 ? MOE_TRACE_DOWN_CYCLES : MOE_TRACE_UP_CYCLES);
 
     if (MODE == 2 && overlapped && (!producer || (s.flags & MOE_TAIL_ASSIST)))
         copy_units(s, p, sm.stages, sm.cbar, sm.abort, META_QUEUE, true, stall, direct_from);
@@ -1040,6 +1042,7 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
     // outputs here. The plan tables read above were complete before that kernel started.
     griddep_wait();
     griddep_launch();
+    const ClockSpan clk = clock_span_start(blockIdx.x == 0 && tid == 0);
     const uint32_t tmem = gemm_cta ? *sm.tmem_base : 0u;
     const int N_up = HAS_UP ? ((NU > 0 && tab_up[E] > 0) ? tab_up[E] : 0) : 0;  // SwiGLU pair tiles
     const int N_dn = HAS_DN ? ((ND > 0 && sm.tab[E] > 0) ? sm.tab[E] : 0) : 0;  // down-projection pair tiles
@@ -1326,6 +1329,7 @@ __device__ __forceinline__ void pair_body(const Shape& s, const PlanPtrs& p, con
         __syncwarp();
         cluster_sync();  // neither CTA goes on (or leaves) while the pair's TMEM release is in progress
         if (HAS_DN && warp >= 2 && lane == 0 && last_end) atomicMax(&p.trace[MOE_TRACE_GEMM2_END], last_end);
+        clock_span_add(p, clk, MODE == 2 ? MOE_TRACE_DOWN_CYCLES : MOE_TRACE_UP_CYCLES);
     }
     // copy engines: consumer CTAs from the start (fused: after their SwiGLU tiles), producers once
     // their tiles are done (tail assist)

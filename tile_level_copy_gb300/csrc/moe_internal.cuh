@@ -43,8 +43,9 @@ enum Status : int {
     ST_PAIR_TMEM = 5,      // the two CTAs of a pair got different TMEM column bases
 };
 
-// Trace slots (uint64) beyond the public ones.
-enum Trace : int { TR_COUNT = 16 };
+// Trace slots (uint64): [0, TR_STEP) are the public per-call stamps, reset by the plan kernel;
+// [TR_STEP, TR_COUNT) the clock counters, which the caller zeroes.
+enum Trace : int { TR_STEP = 8, TR_COUNT = 16 };
 
 // ---- GEMM geometry --------------------------------------------------------------------------
 constexpr int BM = 128;            // UMMA M (rows of one MMA tile)
@@ -231,6 +232,28 @@ __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// SM clock of a launch: one thread notes its SM's cycle counter and the global timer at the start
+// of the span and adds both differences to a pair of trace counters at its end; summed cycles over
+// summed nanoseconds is the mean SM clock over the launches (all SMs share one clock).
+struct ClockSpan {
+    long long cycles;
+    unsigned long long ns;
+    bool on;
+};
+__device__ __forceinline__ ClockSpan clock_span_start(bool on) {
+    ClockSpan c{0, 0, on};
+    if (on) {
+        c.cycles = clock64();
+        c.ns = globaltimer();
+    }
+    return c;
+}
+__device__ __forceinline__ void clock_span_add(const PlanPtrs& p, const ClockSpan& c, int slot) {
+    if (!c.on) return;
+    atomicAdd(&p.trace[slot], (unsigned long long)(clock64() - c.cycles));
+    atomicAdd(&p.trace[slot + 1], globaltimer() - c.ns);
 }
 
 // Programmatic dependent launch: wait until the grids this launch depends on have completed and

@@ -34,6 +34,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
     __shared__ int32_t s_wpre[ROUTE_THREADS / 32][MAX_E];
 
     griddep_launch();  // the plan kernel may start (it waits for this grid before reading)
+    // MOE_PDL: the kernel before this one on the stream (the caller's, which may have written the
+    // logits, or the previous layer's combine, which reads what this grid writes) is complete
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int C = s.chunk_tokens, E = s.E, ld = E + 1;
     int* s_te = reinterpret_cast<int*>(s_logit + C * ld);
@@ -193,8 +196,8 @@ static cudaError_t launch_route_k(const Shape& s, const float* logits, const Pla
     const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&route_kernel<K>),
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    route_kernel<K><<<s.n_chunks, ROUTE_THREADS, smem, st>>>(s, logits, p);
-    return cudaGetLastError();
+    return launch_k(route_kernel<K>, dim3(s.n_chunks), dim3(ROUTE_THREADS), smem, st, (s.flags & MOE_PDL) != 0, s,
+                    logits, p);
 }
 
 cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p, cudaStream_t st) {
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         p.meta[META_STATUS] = bad ? ST_BAD_PLAN : 0;
         p.meta[META_STATUS_DETAIL] = bad ? (hook ? -3 : P > s.P_max ? P : PC) : 0;
     }
-    if (tid < TR_COUNT) p.trace[tid] = (tid == MOE_TRACE_GEMM2_START || tid == MOE_TRACE_COPY_START) ? ~0ull : 0ull;
+    if (tid < TR_STEP) p.trace[tid] = (tid == MOE_TRACE_GEMM2_START || tid == MOE_TRACE_COPY_START) ? ~0ull : 0ull;
     if (tid == 0 && p.host_rec) {  // moe_forward_dma: the band count for the host, then the call's tag
         p.host_rec[1] = (uint32_t)MT;
         p.host_rec[2] = (uint32_t)P;
