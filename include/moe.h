@@ -84,16 +84,22 @@ extern "C" {
                                       /* once all its SwiGLU tiles have published; the        */
                                       /* consumer clusters take SwiGLU tiles, then copy       */
 #define MOE_PDL 0x80u                 /* programmatic dependent launch between the layer's    */
-                                      /* kernels: each starts its prologue (barriers, TMEM,   */
+                                      /* GEMMs and combine too (the routing, plan and permute */
+                                      /* kernels always use it; the permute starts once the   */
+                                      /* plan has published the row layout, beside the rest  */
+                                      /* of it): each starts its prologue (barriers, TMEM,    */
                                       /* descriptor prefetch, plan tables) while the previous */
                                       /* one finishes and waits on the GPU before reading its */
                                       /* outputs (not for the cooperative single-CTA down-    */
-                                      /* projection, nor for the first kernel of the layer)   */
+                                      /* projection)                                          */
 #define MOE_TEST_STALL_CONSUMER 0x100u /* test hook: consumers wait for a flag value that no  */
                                       /* producer writes, so their bounded wait runs out      */
 #define MOE_TEST_PLAN_FAIL 0x200u     /* test hook: the plan kernel reports a failed bounds   */
                                       /* check (MOE_ERR_PLAN, detail -3) although the plan is */
                                       /* valid, to test that the status reaches the caller    */
+#define MOE_TEST_STALL_LAYOUT 0x2000u /* test hook: the plan never publishes the row layout, */
+                                      /* so the permute's bounded wait for it runs out        */
+                                      /* (MOE_ERR_TIMEOUT) and it copies no row               */
 #define MOE_ADAPTIVE_CONSUMERS 0x1000u /* the CTA-pair down-projection picks its consumer      */
                                       /* partition at run time from its tile count: the       */
                                       /* fewest producer pairs that finish the tiles in the    */

@@ -21,6 +21,18 @@ def test_header_declares_the_binding_exports():
     assert declared_symbols() == set(tlc.EXPORTS)
 
 
+def test_header_constants_match_the_binding():
+    """Every MOE_ flag, error code, trace slot and stage event the header defines has the same value
+    in the binding (trace slots and events drop the MOE_ prefix there)."""
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    defs = re.findall(r"#define\s+(MOE_\w+)\s+\(?(-?(?:0x[0-9a-fA-F]+|\d+))u?\)?\s*(?:/\*|$)", text, re.M)
+    assert len(defs) > 30
+    for name, val in defs:
+        attr = name[4:] if name.startswith(("MOE_TRACE_", "MOE_EV_")) else name
+        assert hasattr(tlc, attr), name
+        assert getattr(tlc, attr) == int(val, 0), name
+
+
 def test_library_exports_every_declared_symbol(built_library):
     for name in declared_symbols():
         assert hasattr(built_library, name), name

@@ -150,6 +150,22 @@ def test_stalled_consumer_times_out_and_context_survives(consumers, flags):
     assert torch.equal(L.run(sequential=False), want)
 
 
+@pytest.mark.parametrize("pdl", [False, True], ids=["serial", "pdl"])
+def test_stalled_layout_wait_times_out_and_context_survives(pdl):
+    """MOE_TEST_STALL_LAYOUT: the plan never publishes the row layout, so the permute's bounded wait
+    for it runs out; the call reports MOE_ERR_TIMEOUT, and the next call is correct."""
+    w = small("tiny")
+    L = Layer(w, seed=0)
+    want = L.run(sequential=True)
+    flags = tlc.MOE_TEST_STALL_LAYOUT | (tlc.MOE_PDL if pdl else 0)
+    cfg = tlc.Config.from_workload(w, consumer_ctas=4, flags=flags, timeout_us=20000)
+    tlc.forward(cfg, L.logits, L.x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws)
+    rc, detail = tlc.status(cfg, L.ws)
+    assert rc == tlc.MOE_ERR_TIMEOUT
+    assert "row layout" in tlc.lib().moe_last_error().decode()
+    assert torch.equal(L.run(sequential=False), want)
+
+
 def test_forward_host_equals_device_forward():
     w = small("mixtral")
     L = Layer(w, seed=2, cfg_kw=dict(consumer_ctas=8))

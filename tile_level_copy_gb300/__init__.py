@@ -35,6 +35,7 @@ MOE_PDL = 0x80
 MOE_TEST_STALL_CONSUMER = 0x100
 MOE_TEST_PLAN_FAIL = 0x200
 MOE_ADAPTIVE_CONSUMERS = 0x1000
+MOE_TEST_STALL_LAYOUT = 0x2000
 MOE_TEST_STALL_PIPE0 = 0x400
 MOE_TEST_STALL_PIPE1 = 0x800
 

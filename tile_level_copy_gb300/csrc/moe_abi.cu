@@ -969,6 +969,7 @@ MOE_API int moe_status(const moe_config* cfg, const void* ws, void* stream, int3
         case ST_COPY_TIMEOUT: return fail(MOE_ERR_TIMEOUT, "row-band copy timed out (M-tile %d)", w[1]);
         case ST_BAD_PLAN: return fail(MOE_ERR_PLAN, "plan index out of bounds (%d)", w[1]);
         case ST_PAIR_TMEM: return fail(MOE_ERR_DEVICE, "CTA pair got different TMEM bases (peer %d)", w[1]);
+        case ST_LAYOUT_TIMEOUT: return fail(MOE_ERR_TIMEOUT, "permute's wait for the row layout timed out");
         default: return fail(MOE_ERR_PLAN, "unknown device status %d", w[0]);
     }
 }

@@ -27,6 +27,7 @@ enum Meta : int {
     META_ITEMS_UP = 8,     // SwiGLU work items (128 rows of one expert in the compact layout)
     META_PC = 9,           // rows of the compact layout used by this call
     META_PRODUCERS = 10,   // producer CTAs of the last overlapped CTA-pair down-projection
+    META_LAYOUT = 16,      // 1 once the plan has published the row layout the permute reads
     META_DISPATCH = 24,    // next block of compact rows to copy (MOE_FUSED_DISPATCH)
     META_TILES_UP = 32,    // next SwiGLU GEMM tile to hand out (single-CTA kernel), minus the grid
     META_TILES_DOWN = 48,  // next down-projection tile to hand out, minus the producer count
@@ -41,6 +42,7 @@ enum Status : int {
     ST_COPY_TIMEOUT = 3,   // a bulk copy did not complete in time
     ST_BAD_PLAN = 4,       // a plan index failed its bounds check
     ST_PAIR_TMEM = 5,      // the two CTAs of a pair got different TMEM column bases
+    ST_LAYOUT_TIMEOUT = 6, // the permute gave up waiting for the plan's row layout
 };
 
 // Trace slots (uint64): [0, TR_STEP) are the public per-call stamps, reset by the plan kernel;
@@ -398,6 +400,16 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+// Bounded wait until the GPU-scope word *w is non-zero (acquire); false after timeout_ns.
+__device__ __forceinline__ bool wait_word(const uint32_t* w, unsigned long long timeout_ns) {
+    if (ld_acquire_gpu(w)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(w)) return true;
+        if (globaltimer() - t0 > timeout_ns) return false;
+    }
 }
 
 // ---- tcgen05 ---------------------------------------------------------------------------------------

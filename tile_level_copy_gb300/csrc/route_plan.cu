@@ -34,8 +34,10 @@ __global__ void __launch_bounds__(ROUTE_THREADS) route_kernel(Shape s, const flo
     __shared__ int32_t s_wpre[ROUTE_THREADS / 32][MAX_E];
 
     griddep_launch();  // the plan kernel may start (it waits for this grid before reading)
-    // MOE_PDL: the kernel before this one on the stream (the caller's, which may have written the
-    // logits, or the previous layer's combine, which reads what this grid writes) is complete
+    // The routing, plan and permute kernels are always launched with programmatic dependent launch
+    // (MOE_PDL extends it to the GEMMs and the combine): the kernel before this one on the stream
+    // (the caller's, which may have written the logits, or the previous layer's combine, which reads
+    // what this grid writes) is complete past this wait
     griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int C = s.chunk_tokens, E = s.E, ld = E + 1;
@@ -196,8 +198,7 @@ static cudaError_t launch_route_k(const Shape& s, const float* logits, const Pla
     const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(&route_kernel<K>),
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_k(route_kernel<K>, dim3(s.n_chunks), dim3(ROUTE_THREADS), smem, st, (s.flags & MOE_PDL) != 0, s,
-                    logits, p);
+    return launch_k(route_kernel<K>, dim3(s.n_chunks), dim3(ROUTE_THREADS), smem, st, true, s, logits, p);
 }
 
 cudaError_t launch_route(const Shape& s, const float* logits, const PlanPtrs& p, cudaStream_t st) {
@@ -250,6 +251,15 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* s_t
 
 __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p) {
     griddep_wait();  // the routing kernel's counts
+    // The call's status word and layout word are cleared before the permute may start (it runs
+    // beside the rest of this kernel once the layout is published, step 5a).
+    if (threadIdx.x == 0) {
+        p.meta[META_STATUS] = 0;
+        p.meta[META_STATUS_DETAIL] = 0;
+        p.meta[META_LAYOUT] = 0;
+        __threadfence();
+    }
+    __syncthreads();
     griddep_launch();
     __shared__ int s_n[1024];        // n_{e,r}, group g = e*R + r
     __shared__ int s_off[1025];
@@ -318,7 +328,80 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     const int MT = P / tbM;
     for (int g = tid; g <= G; g += PLAN_THREADS) p.offsets[g] = s_off[g];
 
-    // 2b. remote-first schedule, the largest transfers first: bands by valid rows, descending, ties
+    // 3. owner return offsets: ret_off[r][e] = sum_{e' < e} n_{e',r}
+    for (int r = tid; r < R; r += PLAN_THREADS) {
+        int acc = 0;
+        for (int e = 0; e < E; ++e) {
+            p.ret_off[r * (E + 1) + e] = acc;
+            acc += s_n[e * R + r];
+        }
+        p.ret_off[r * (E + 1) + E] = acc;
+    }
+
+    // 4. expert loads, full bands, expert table
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        int load = 0, fb = 0;
+        for (int r = 0; r < R; ++r) {
+            load += s_n[e * R + r];
+            fb += s_n[e * R + r] / tbM;
+        }
+        s_load[e] = load;
+        s_fb[e] = fb;
+        s_mt[e] = (s_off[(e + 1) * R] - s_off[e * R]) / tbM;
+        p.experts[8 * e + 0] = s_off[e * R] / tbM;
+        p.experts[8 * e + 1] = s_mt[e];
+    }
+    __syncthreads();
+
+    // 4b. expert-compact layout of the GEMM inputs: each expert's rows contiguous, the run padded to
+    // a multiple of the UMMA tile height BM; inside the run the expert's bands follow one another in
+    // hand-out order, each band's valid rows in row order (step 5a places them).
+    {
+        const int e = tid;
+        const int rows = (e < E) ? ((s_load[e] + BM - 1) / BM) * BM : 0;
+        const int o = block_exclusive_scan(rows, s_warp, &s_total);
+        if (e < E) s_cbase[e] = o;
+    }
+    __syncthreads();
+    const int PC = s_total;
+
+    // 5a. the compact row of each band's first row (the expert's run start, then the valid rows of
+    // the expert's bands before it in hand-out order: full bands in layout order, then partial bands
+    // by valid rows descending, ties to the lower owner); with the offsets, return offsets, chunk
+    // bases and each expert's run this is all the permute needs, so it is published here and the
+    // permute copies rows while the rest of the plan is built. (Step 5 computes the same rows again
+    // for band_item rather than reading them back.)
+    auto full_crow = [&](int e, int fpre, int i) { return s_cbase[e] + (fpre + i) * tbM; };
+    auto partial_crow = [&](int e, int rows_before) { return s_cbase[e] + s_fb[e] * tbM + rows_before; };
+    for (int g = tid; g < G; g += PLAN_THREADS) {
+        const int e = g / R, r = g % R, n = s_n[g];
+        const int m0 = s_off[g] / tbM, nfull = n / tbM;
+        int fpre = 0;
+        for (int q = 0; q < r; ++q) fpre += s_n[e * R + q] / tbM;
+        for (int i = 0; i < nfull; ++i) p.tile_crow[m0 + i] = full_crow(e, fpre, i);
+        if (n > nfull * tbM) {  // one partial band
+            const int valid = n - nfull * tbM;
+            int rows_before = 0;  // rows of the expert's partial bands before this one
+            for (int rh = 0; rh < R; ++rh) {
+                const int vh = s_n[e * R + rh] % tbM;
+                if (vh == 0 || rh == r) continue;
+                rows_before += ((vh > valid) || (vh == valid && rh < r)) ? vh : 0;
+            }
+            p.tile_crow[m0 + nfull] = partial_crow(e, rows_before);
+        }
+    }
+    for (int e = tid; e < E; e += PLAN_THREADS) {
+        p.experts[8 * e + 4] = (s_load[e] + BM - 1) / BM;
+        p.experts[8 * e + 7] = s_cbase[e];
+    }
+    if (tid == 0) p.meta[META_PC] = PC;
+    __threadfence();
+    __syncthreads();
+    // (MOE_TEST_STALL_LAYOUT: never published, so that the permute's bounded wait runs out)
+    if (tid == 0 && !(s.flags & MOE_TEST_STALL_LAYOUT))
+        red_release_gpu_add(reinterpret_cast<uint32_t*>(p.meta + META_LAYOUT), 1u);
+
+    // 5b. remote-first schedule, the largest transfers first: bands by valid rows, descending, ties
     // in layout order. The full bands come first, in layout order (position = full bands of the
     // groups before + index); each group's partial band (valid = n mod tbM) follows, ranked by
     // (tbM - valid, group) among the partial bands: a counting sort over the buckets tbM - valid,
@@ -358,42 +441,6 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
     }
     __syncthreads();
 
-    // 3. owner return offsets: ret_off[r][e] = sum_{e' < e} n_{e',r}
-    for (int r = tid; r < R; r += PLAN_THREADS) {
-        int acc = 0;
-        for (int e = 0; e < E; ++e) {
-            p.ret_off[r * (E + 1) + e] = acc;
-            acc += s_n[e * R + r];
-        }
-        p.ret_off[r * (E + 1) + E] = acc;
-    }
-
-    // 4. expert loads, full bands, expert table
-    for (int e = tid; e < E; e += PLAN_THREADS) {
-        int load = 0, fb = 0;
-        for (int r = 0; r < R; ++r) {
-            load += s_n[e * R + r];
-            fb += s_n[e * R + r] / tbM;
-        }
-        s_load[e] = load;
-        s_fb[e] = fb;
-        s_mt[e] = (s_off[(e + 1) * R] - s_off[e * R]) / tbM;
-        p.experts[8 * e + 0] = s_off[e * R] / tbM;
-        p.experts[8 * e + 1] = s_mt[e];
-    }
-    __syncthreads();
-
-    // 4b. expert-compact layout of the GEMM inputs: each expert's rows contiguous, the run padded to
-    // a multiple of the UMMA tile height BM; inside the run the expert's bands follow one another in
-    // hand-out order, each band's valid rows in row order (step 5 places them).
-    {
-        const int e = tid;
-        const int rows = (e < E) ? ((s_load[e] + BM - 1) / BM) * BM : 0;
-        const int o = block_exclusive_scan(rows, s_warp, &s_total);
-        if (e < E) s_cbase[e] = o;
-    }
-    __syncthreads();
-    const int PC = s_total;
     for (int e = tid; e < E; e += PLAN_THREADS) {
         int rk = 0;
         for (int f = 0; f < E; ++f)
@@ -448,9 +495,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
             p.tile_ret[m] = rbase + i * tbM;
             if (mirror) s_tg[m] = g;
             if (i < nfull) {
-                const int crow = s_cbase[e] + (fpre + i) * tbM;
-                p.tile_crow[m] = crow;
-                p.band_item[m] = band_item_of(e, crow, valid);
+                p.band_item[m] = band_item_of(e, full_crow(e, fpre, i), valid);
                 p.sched[s_fbp[g] + i] = m;
                 p.order[s_ebase[e] + fpre + i] = m;
                 if (mirror) s_order[s_ebase[e] + fpre + i] = m;
@@ -466,9 +511,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
                 pos += before;
                 rows_before += before ? vh : 0;
             }
-            const int crow = s_cbase[e] + s_fb[e] * tbM + rows_before;
-            p.tile_crow[m0 + nfull] = crow;
-            p.band_item[m0 + nfull] = band_item_of(e, crow, valid);
+            p.band_item[m0 + nfull] = band_item_of(e, partial_crow(e, rows_before), valid);
             p.order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
             if (mirror) s_order[s_ebase[e] + s_fb[e] + pos] = m0 + nfull;
             p.sched[n_full + s_prank[g]] = m0 + nfull;
@@ -533,8 +576,7 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(Shape s, PlanPtrs p)
         // reach the caller; the plan itself is still complete and valid
         const bool hook = (s.flags & MOE_TEST_PLAN_FAIL) != 0;
         const bool bad = P > s.P_max || PC > s.PC_max || hook;
-        p.meta[META_STATUS] = bad ? ST_BAD_PLAN : 0;
-        p.meta[META_STATUS_DETAIL] = bad ? (hook ? -3 : P > s.P_max ? P : PC) : 0;
+        if (bad) set_status(p.meta, ST_BAD_PLAN, hook ? -3 : P > s.P_max ? P : PC);
     }
     if (tid < TR_STEP) p.trace[tid] = (tid == MOE_TRACE_GEMM2_START || tid == MOE_TRACE_COPY_START) ? ~0ull : 0ull;
     if (tid == 0 && p.host_rec) {  // moe_forward_dma: the band count for the host, then the call's tag
@@ -560,7 +602,7 @@ cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
                                  (int)smem);
         if (e != cudaSuccess) return e;
     }
-    return launch_k(plan_kernel, dim3(1), dim3(PLAN_THREADS), smem, st, (s.flags & MOE_PDL) != 0, s, p);
+    return launch_k(plan_kernel, dim3(1), dim3(PLAN_THREADS), smem, st, true, s, p);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -579,8 +621,15 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     // The first token's row does not depend on the plan: its loads are issued before the wait for
-    // the plan kernel (MOE_PDL: while it runs), the rest of the work after.
+    // the plan kernel (while it runs), the rest of the work after.
     const int item0 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    // nor do the first token's experts and ranks (the routing kernel completed before this grid
+    // started): their loads overlap the wait too
+    int e0 = 0, rk0 = 0;
+    if (item0 < s.T && lane < s.k) {
+        e0 = p.idx[(size_t)item0 * s.k + lane];
+        rk0 = p.rank[(size_t)item0 * s.k + lane];
+    }
     const int vec0 = s.d / 8;
     uint4 v[PERM_VEC];  // one pass of a row: the first token's first pass is loaded here
     const bool prefetched = x != nullptr && item0 < s.T;
@@ -592,8 +641,25 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
             if (vi < vec0) v[i] = __ldg(xs0 + vi);
         }
     }
-    griddep_wait();  // the plan
-    griddep_launch();
+    // This grid starts once the plan kernel has passed its own wait for the routing kernel,
+    // so the routing outputs are complete. The plan's layout (offsets, return offsets, chunk bases,
+    // the bands' compact rows, each expert's run) is published part-way through the plan with a
+    // release; thread 0's acquire and the barrier order every thread's later loads after it, and no
+    // thread of this grid reads those tables before. The next launch reads the rest of the plan from
+    // its prologue on, so it may start only after the plan kernel has completed: every block but the
+    // last lets it start at once, the last block (which starts last) only after waiting for the plan
+    // kernel; it can start only once every block has done so, and this grid completes after the plan.
+    __shared__ int s_layout;
+    const bool last = blockIdx.x == gridDim.x - 1;
+    if (threadIdx.x == 0) {
+        const bool ok = wait_word(reinterpret_cast<const uint32_t*>(p.meta + META_LAYOUT), s.timeout_ns);
+        if (!ok) set_status(p.meta, ST_LAYOUT_TIMEOUT, 0);
+        if (last) griddep_wait();
+        s_layout = ok;
+    }
+    __syncthreads();
+    if (!last || threadIdx.x == 0) griddep_launch();
+    if (!s_layout) return;
     const int PC = p.meta[META_PC];
     const int per = s.T / s.R, slice = per * s.k, E = s.E, R = s.R, k = s.k;
     const int vec = s.d / 8;  // 16-byte vectors per row
@@ -608,8 +674,9 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
             const int t = item, r = t / per, c = t / s.chunk_tokens;
             int my_cs = 0, my_y = 0;
             if (lane < k) {
-                const int e = p.idx[(size_t)t * k + lane];
-                const int rk = p.chunk_base[(size_t)c * E + e] + p.rank[(size_t)t * k + lane];
+                const bool first = item == item0;
+                const int e = first ? e0 : p.idx[(size_t)t * k + lane];
+                const int rk = p.chunk_base[(size_t)c * E + e] + (first ? rk0 : p.rank[(size_t)t * k + lane]);
                 my_y = p.offsets[e * R + r] + rk;
                 const int m = my_y / s.tbM;  // bands start at multiples of the tile height
                 my_cs = (m >= 0 && m < s.MT_max) ? p.tile_crow[m] + (my_y - m * s.tbM) : -1;
@@ -676,7 +743,7 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
 cudaError_t launch_permute(const Shape& s, const __nv_bfloat16* x, const PlanPtrs& p, int sms, cudaStream_t st) {
     const int items = s.T + s.E * (BM / 8);
     const int blocks = min((items + 7) / 8, sms * 16);
-    return launch_k(permute_kernel, dim3(blocks), dim3(256), 0, st, (s.flags & MOE_PDL) != 0, s, x, p);
+    return launch_k(permute_kernel, dim3(blocks), dim3(256), 0, st, true, s, x, p);
 }
 
 }  // namespace moe
