@@ -61,6 +61,32 @@ def test_pdl_in_a_replayed_graph():
         assert torch.equal(L.out, want)
 
 
+@pytest.mark.parametrize("consumers,flags", CONFIGS, ids=IDS)
+def test_back_to_back_layers_with_different_routings(consumers, flags):
+    """Sixteen calls on two alternating inputs (different routings, so different layouts, work items
+    and bands), enqueued back to back on one stream with no other work between them, each into its
+    own output: every output equals its input's result from a call run alone. A call that read a
+    layout, a plan table, a flag or a return row of the call before it would differ."""
+    w = small("mixtral")
+    L = Layer(w, seed=4)
+    ins = [(L.logits, L.x), (torch.from_numpy(inputs.make_logits(w, 21)).cuda(), inputs.make_x(w, 21).cuda())]
+    cfg = tlc.Config.from_workload(w, consumer_ctas=consumers, flags=flags | PDL)
+    want = []
+    for lg, x in ins:
+        tlc.forward(cfg, lg, x, L.W["W1"], L.W["W3"], L.W["W2"], L.out, L.ws)
+        assert tlc.status(cfg, L.ws)[0] == tlc.MOE_OK
+        want.append(L.out.clone())
+    assert not torch.equal(want[0], want[1])
+    outs = [torch.full_like(L.out, float("nan")) for _ in range(16)]
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        lg, x = ins[i % 2]
+        tlc.forward(cfg, lg, x, L.W["W1"], L.W["W3"], L.W["W2"], o, L.ws)
+    assert tlc.status(cfg, L.ws)[0] == tlc.MOE_OK
+    for i, o in enumerate(outs):
+        assert torch.equal(o, want[i % 2]), i
+
+
 @pytest.mark.parametrize("name", ["mixtral", "fine"])
 def test_pdl_full_size_in_the_bench_configuration(name):
     import bench
