@@ -613,7 +613,8 @@ cudaError_t launch_plan(const Shape& s, const PlanPtrs& p, cudaStream_t st) {
 // in flight together), then stores them to the k rows. Items [T, T + E * BM/8): one group of 8 rows
 // of an expert's last BM-row tile in the compact layout, marking those rows past the expert's rows
 // as padding (token -1, no Yp row) and zeroing them. With x == nullptr only the slots, tokens and
-// Yp rows are written.
+// Yp rows are written. The kernel runs beside the second half of the plan kernel: each block waits
+// for the row layout the plan publishes part-way through (see below), not for the plan's end.
 // ---------------------------------------------------------------------------------------------
 constexpr int PERM_VEC = 16;  // 16-byte vectors per lane per pass
 
