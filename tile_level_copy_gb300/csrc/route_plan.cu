@@ -648,8 +648,9 @@ __global__ void __launch_bounds__(256) permute_kernel(Shape s, const __nv_bfloat
     // release; thread 0's acquire and the barrier order every thread's later loads after it, and no
     // thread of this grid reads those tables before. The next launch reads the rest of the plan from
     // its prologue on, so it may start only after the plan kernel has completed: every block but the
-    // last lets it start at once, the last block (which starts last) only after waiting for the plan
-    // kernel; it can start only once every block has done so, and this grid completes after the plan.
+    // last lets it start at once, the last block only after waiting for the plan kernel; it can start
+    // only once every block has done so, and this grid completes after the plan. (The last block is
+    // normally the last to start, so it rarely waits; the start order matters for speed only.)
     __shared__ int s_layout;
     const bool last = blockIdx.x == gridDim.x - 1;
     if (threadIdx.x == 0) {
