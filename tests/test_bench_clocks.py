@@ -1,4 +1,5 @@
-"""The bench's clock record: samples taken during the timed region, throttle reasons by name.
+"""The bench's clock record: samples taken during the timed region, throttle reasons by name, and
+the GEMMs' own clock counters read from the trace region.
 
 NVML is replaced by a fake reader (no GPU here); the sampler must keep polling it for as long as
 the timed region lasts and name every clock event reason any sample carried.
@@ -47,3 +48,26 @@ def test_a_reader_that_fails_leaves_the_record_unsampled():
     with bench.ClockSampler(0, reader=broken) as clk:
         time.sleep(0.01)
     assert clk.summary()["reasons"] == ["unsampled"]
+
+
+class _FakeWorkspace:
+    """A workspace whose trace region is a host tensor (the bench's clock-counter helpers only view
+    it)."""
+
+    def __init__(self, values):
+        import torch
+        self.trace = torch.tensor(values, dtype=torch.int64)
+
+    def view(self, name):
+        assert name == "trace"
+        return self.trace
+
+
+def test_kernel_clocks_from_the_trace_counters():
+    """Slots 8-11 hold (SwiGLU cycles, ns, down-projection cycles, ns): the mean clock is cycles per
+    microsecond; a GEMM with no recorded span reads None, and zeroing touches those four slots only."""
+    ws = _FakeWorkspace([7] * 8 + [1_700_000, 1_000_000, 0, 0] + [9] * 4)
+    got = bench.kernel_clocks(ws)
+    assert got["swiglu_gemm"] == 1700.0 and got["down_projection"] is None
+    bench.zero_kernel_clocks(ws)
+    assert ws.trace.tolist() == [7] * 8 + [0, 0, 0, 0] + [9] * 4
